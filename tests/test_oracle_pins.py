@@ -1,0 +1,428 @@
+"""Pins of the CPU oracle against what the method and the mathematics fix.
+
+None of these re-derives a value with the oracle's own code: each compares
+the oracle with a library routine (scipy's Hadamard matrix, numpy fp64
+matmul), a closed form of the method, exact rational arithmetic, brute force
+on tiny inputs, or an error bound of the quantizer.
+"""
+import math
+
+import numpy as np
+import pytest
+import scipy.linalg
+
+import oracle
+from tests.exact_ref import exact_signed_sum, round_fraction_to_f32
+
+H_SCIPY = scipy.linalg.hadamard(16).astype(np.int64)
+
+
+def gray_bitrev_sequency(k):
+    """Walsh (sequency) order of Sylvester rows: row = bitrev4(gray(k))."""
+    g = k ^ (k >> 1)
+    return int(f"{g:04b}"[::-1], 2)
+
+
+def sign_changes(row):
+    return int(np.sum(row[1:] != row[:-1]))
+
+
+# ------------------------------------------------------------------ Hadamard
+
+def test_hadamard_matches_scipy_sylvester():
+    H = oracle.hadamard16().astype(np.int64)
+    assert np.array_equal(H, H_SCIPY)
+
+
+def test_hadamard_orthogonal_up_to_16():
+    H = oracle.hadamard16().astype(np.int64)
+    assert np.array_equal(H @ H.T, 16 * np.eye(16, dtype=np.int64))
+
+
+def test_sequency_order_gray_code_and_golden():
+    sigma = oracle.sequency_order()
+    assert [int(s) for s in sigma] == [gray_bitrev_sequency(k) for k in range(16)]
+    golden = [int(t) for t in open(
+        __file__.replace("test_oracle_pins.py", "golden/sequency16.txt")
+    ).read().split("#")[0].split()]
+    assert [int(s) for s in sigma] == golden
+    for k in range(16):
+        assert sign_changes(H_SCIPY[sigma[k]]) == k
+    # rank 8 keeps exactly the even Sylvester rows
+    assert sorted(int(s) for s in sigma[:8]) == [0, 2, 4, 6, 8, 10, 12, 14]
+
+
+# ------------------------------------------------------------ exact sums
+
+def _adversarial_vectors(rng):
+    out = []
+    for spread in (0, 5, 12, 13, 20, 25, 26, 41, 42, 60, 100, 200):
+        mant = rng.standard_normal(16)
+        exps = rng.integers(-spread // 2 - 1, spread // 2 + 1, 16)
+        exps[0], exps[1] = -spread // 2, spread - spread // 2
+        out.append((mant * np.exp2(exps.astype(np.float64))).astype(np.float32))
+    # cancellation: big values that cancel, leaving tiny ones
+    v = np.zeros(16, np.float32)
+    v[0], v[1], v[2] = 2.0 ** 40, 2.0 ** 40, np.float32(1e-30)
+    out.append(v)
+    # subnormals
+    out.append((rng.standard_normal(16) * 1e-40).astype(np.float32))
+    v = np.zeros(16, np.float32)
+    v[3] = np.float32(1.4e-45)
+    v[5] = np.float32(-2.8e-45)
+    out.append(v)
+    # exact ties at fp32 rounding: 1 + 2^-24 (+ tiny) patterns
+    v = np.zeros(16, np.float32)
+    v[0], v[1] = 1.0, 2.0 ** -24
+    out.append(v)
+    v = v.copy()
+    v[2] = 2.0 ** -60
+    out.append(v)
+    v = np.zeros(16, np.float32)
+    v[0], v[1] = 1.0 + 2.0 ** -23, 2.0 ** -24
+    out.append(v)
+    # all zero, signed zeros
+    out.append(np.zeros(16, np.float32))
+    out.append(-np.zeros(16, np.float32))
+    # large magnitudes
+    out.append((rng.standard_normal(16) * 1e37).astype(np.float32))
+    return out
+
+
+def test_exact_sum_brute_force_fractions():
+    rng = np.random.default_rng(7)
+    H = oracle.hadamard16()
+    vecs = _adversarial_vectors(rng) + [
+        rng.standard_normal(16).astype(np.float32) for _ in range(20)]
+    for v in vecs:
+        for i in range(16):
+            for hrow in (H[i], -H[i]):
+                got = oracle.exact_sum_f32(hrow, v)
+                want = exact_signed_sum(hrow, v)
+                assert got == want or (got == 0 and want == 0), (v, i, got, want)
+
+
+def test_round_to_f32_ties_to_even():
+    # 1 + 2^-24 is a tie between 1 and 1+2^-23: even mantissa is 1
+    H1 = np.ones(2, np.int32)
+    assert oracle.exact_sum_f32(H1, np.array([1.0, 2.0 ** -24], np.float32)) == 1.0
+    # 1+2^-23 + 2^-24 ties between 1+2^-23 (odd) and 1+2^-22 (even)
+    got = oracle.exact_sum_f32(H1, np.array([1.0 + 2.0 ** -23, 2.0 ** -24], np.float32))
+    assert got == np.float32(1.0 + 2.0 ** -22)
+    # just above a tie rounds up
+    H3 = np.ones(3, np.int32)
+    got = oracle.exact_sum_f32(H3, np.array([1.0, 2.0 ** -24, 2.0 ** -70], np.float32))
+    assert got == np.float32(1.0 + 2.0 ** -23)
+
+
+# ------------------------------------------------------------ transforms
+
+def _blockdiag_H(n):
+    return np.kron(np.eye(n // 16, dtype=np.int64), H_SCIPY)
+
+
+def test_hq_transform_equals_fp64_matmul_when_exact():
+    # bf16-like values with a small exponent spread: fp64 sums are exact,
+    # so RN_f32(fp64 matmul) is the exactly rounded sum.
+    rng = np.random.default_rng(1)
+    g = (rng.standard_normal((8, 64)) * 0.01).astype(np.float32)
+    g = np.round(g * 2 ** 12) / 2 ** 12
+    g = g.astype(np.float32)
+    D = _blockdiag_H(64)
+    want = (g.astype(np.float64) @ D.T).astype(np.float32)
+    assert np.array_equal(oracle.hq_transform(g, 0), want)
+    w = g.T.copy()                              # [64, 8], blocks along rows
+    want_w = (D @ w.astype(np.float64)).astype(np.float32)
+    assert np.array_equal(oracle.hq_transform(w, 1), want_w)
+
+
+def test_hq_transform_brute_force_adversarial():
+    rng = np.random.default_rng(3)
+    vecs = _adversarial_vectors(rng)
+    g = np.stack(vecs[:4]).astype(np.float32)        # [4, 16]
+    Y = oracle.hq_transform(np.concatenate([g, g[::-1]], 1), 0)
+    for r in range(4):
+        for i in range(16):
+            assert Y[r, i] == exact_signed_sum(H_SCIPY[i], g[r])
+            assert Y[r, 16 + i] == exact_signed_sum(H_SCIPY[i], g[3 - r])
+    Yw = oracle.hq_transform(np.ascontiguousarray(g.T), 1)   # [16, 4]
+    for c in range(4):
+        for i in range(16):
+            assert Yw[i, c] == exact_signed_sum(H_SCIPY[i], g[c])
+
+
+def test_hla_transform_matches_selection_matrix():
+    rng = np.random.default_rng(2)
+    T, C = 64, 24
+    x = np.round(rng.standard_normal((T, C)) * 2 ** 10) / 2 ** 10
+    x = x.astype(np.float32)
+    for rank in (1, 2, 4, 8, 16):
+        rows = [gray_bitrev_sequency(k) for k in range(rank)]
+        P = np.zeros((T // 16 * rank, T), dtype=np.int64)
+        for b in range(T // 16):
+            for k in range(rank):
+                P[b * rank + k, 16 * b:16 * b + 16] = H_SCIPY[rows[k]]
+        want = (P @ x.astype(np.float64)).T.astype(np.float32)   # [C, T']
+        assert np.array_equal(oracle.hla_transform(x, rank), want), rank
+
+
+def test_hla_transform_brute_force_adversarial():
+    rng = np.random.default_rng(4)
+    vecs = _adversarial_vectors(rng)[:6]
+    x = np.stack(vecs, axis=1).astype(np.float32)     # [16, 6]
+    out = oracle.hla_transform(x, 8)                   # [6, 8]
+    for c in range(6):
+        for k in range(8):
+            want = exact_signed_sum(H_SCIPY[gray_bitrev_sequency(k)], x[:, c])
+            assert out[c, k] == want
+
+
+# ------------------------------------------- closed forms, quantization off
+
+def test_hq_quant_off_reproduces_gy_w():
+    """H orthogonal up to 16: (1/16) (g_y D^T)(D w) = g_y w."""
+    rng = np.random.default_rng(5)
+    T, Cin, Cout = 48, 32, 64
+    gy = rng.standard_normal((T, Cout))
+    w = rng.standard_normal((Cout, Cin))
+    Y = oracle.hq_transform_f64(gy, 0)
+    Wt = oracle.hq_transform_f64(w, 1)
+    got = Y @ Wt / 16.0
+    want = gy @ w
+    assert np.max(np.abs(got - want)) <= 1e-12 * np.max(np.abs(want)) * Cout
+
+
+def test_hla_full_rank_quant_off_reproduces_gyT_x():
+    rng = np.random.default_rng(6)
+    T, Cin, Cout = 64, 24, 40
+    gy = rng.standard_normal((T, Cout))
+    x = rng.standard_normal((T, Cin))
+    G = oracle.hla_transform_f64(gy, 16)
+    X = oracle.hla_transform_f64(x, 16)
+    got = G @ X.T / 16.0
+    want = gy.T @ x
+    assert np.max(np.abs(got - want)) <= 1e-12 * np.max(np.abs(want)) * T
+
+
+@pytest.mark.parametrize("rank", [1, 2, 4, 8])
+def test_hla_low_rank_quant_off_group_sum_closed_form(rank):
+    """Lowest-sequency rows span the vectors constant on runs of 16/rank
+    tokens, so (1/16) Gbar^T Xbar = (rank/16) sum_runs S_g S_x^T."""
+    rng = np.random.default_rng(10 + rank)
+    T, Cin, Cout = 96, 20, 28
+    gy = rng.standard_normal((T, Cout))
+    x = rng.standard_normal((T, Cin))
+    G = oracle.hla_transform_f64(gy, rank)
+    X = oracle.hla_transform_f64(x, rank)
+    got = G @ X.T / 16.0
+    L = 16 // rank
+    Sg = gy.reshape(T // L, L, Cout).sum(1)
+    Sx = x.reshape(T // L, L, Cin).sum(1)
+    want = (rank / 16.0) * (Sg.T @ Sx)
+    assert np.max(np.abs(got - want)) <= 1e-12 * np.max(np.abs(want)) * T
+
+
+def test_hla_rank8_exact_on_equal_token_pairs():
+    rng = np.random.default_rng(9)
+    T, Cin, Cout = 64, 12, 20
+    gy = np.repeat(rng.standard_normal((T // 2, Cout)), 2, axis=0)
+    x = np.repeat(rng.standard_normal((T // 2, Cin)), 2, axis=0)
+    G = oracle.hla_transform_f64(gy, 8)
+    X = oracle.hla_transform_f64(x, 8)
+    assert np.allclose(G @ X.T / 16.0, gy.T @ x, rtol=1e-12, atol=1e-12)
+
+
+# ------------------------------------------------------------ quantizers
+
+def test_scale_rule_and_zero_tensor():
+    Y = np.array([[0.0, -3.5, 1.0, 2.0]], np.float32)
+    q, s = oracle.hq_quantize(Y, oracle.PER_TENSOR, oracle.RNE, 0, 0)
+    assert s[0] == np.float32(3.5) / np.float32(7.0)
+    assert list(q[0]) == [0, -7, 2, 4]
+    q, s = oracle.hq_quantize(np.zeros((3, 16), np.float32), oracle.PER_TOKEN,
+                              oracle.SR, 0, 0)
+    assert np.all(q == 0) and np.all(s == 0)
+
+
+def test_rne_error_bound_and_ties():
+    rng = np.random.default_rng(11)
+    Y = rng.standard_normal((64, 128)).astype(np.float32)
+    for gran in (oracle.PER_TENSOR, oracle.PER_TOKEN):
+        q, s = oracle.hq_quantize(Y, gran, oracle.RNE, 0, 0)
+        sc = s[:, None] if gran == oracle.PER_TOKEN else s[0]
+        x = Y / sc                                   # fp32 division, as defined
+        assert np.all(np.abs(q) <= 7)
+        inside = np.abs(x) <= 7
+        assert np.all(np.abs(q[inside] - x[inside]) <= 0.5)
+        assert np.all(q[~inside] == np.sign(x[~inside]) * 7)
+    # exact ties: amax 7 -> s = 1, values k + 0.5 go to the even neighbour
+    Y = np.array([[7.0, 0.5, 1.5, 2.5, -0.5, -1.5, -2.5, 3.5]], np.float32)
+    q, _ = oracle.hq_quantize(Y, oracle.PER_TENSOR, oracle.RNE, 0, 0)
+    assert list(q[0]) == [7, 0, 2, 2, 0, -2, -2, 4]
+    v = np.array([127.0, 0.5, 1.5, -2.5, 126.5, -126.5], np.float32)
+    q8, s8 = oracle.int8_quantize(v)
+    assert s8 == 1.0 and list(q8) == [127, 0, 2, -2, 126, -126]
+
+
+def test_int8_rne_bound():
+    rng = np.random.default_rng(12)
+    v = (rng.standard_t(3, 5000) * 1e-3).astype(np.float32)
+    q, s = oracle.int8_quantize(v)
+    assert s == np.float32(np.max(np.abs(v))) / np.float32(127.0)
+    x = v / s
+    assert np.all(np.abs(q) <= 127)
+    ok = np.abs(x) <= 127
+    assert np.all(np.abs(q[ok] - x[ok]) <= 0.5)
+
+
+def test_clamp_when_scale_rounds_down():
+    # amax/7 rounded to fp32 can be below the true quotient, so amax/s > 7
+    for amax in np.float32([1.0, 3.0, 5.0, 0.1, 1e-3, 123.456]):
+        s = amax / np.float32(7)
+        Y = np.array([[amax, -amax]], np.float32)
+        q, _ = oracle.hq_quantize(Y, oracle.PER_TENSOR, oracle.SR, 1, 0)
+        assert list(q[0]) == [7, -7]
+
+
+def test_sr_error_bound_and_determinism():
+    rng = np.random.default_rng(13)
+    Y = rng.standard_normal((32, 64)).astype(np.float32)
+    q1, s = oracle.hq_quantize(Y, oracle.PER_TOKEN, oracle.SR, 123, 0)
+    q2, _ = oracle.hq_quantize(Y, oracle.PER_TOKEN, oracle.SR, 123, 0)
+    q3, _ = oracle.hq_quantize(Y, oracle.PER_TOKEN, oracle.SR, 124, 0)
+    assert np.array_equal(q1, q2) and not np.array_equal(q1, q3)
+    x = Y / s[:, None]
+    assert np.all(np.abs(q1 - x) < 1.0 + 1e-6)
+    assert np.all((q1 == np.floor(x)) | (q1 == np.floor(x) + 1) | (np.abs(x) > 7))
+
+
+def test_sr_unbiased_over_seeds():
+    rng = np.random.default_rng(14)
+    Y = rng.uniform(-7, 7, size=(1, 32)).astype(np.float32)
+    Y[0, 0] = 7.0                                     # amax 7 -> s = 1
+    n = 2048
+    acc = np.zeros(32)
+    for seed in range(n):
+        q, s = oracle.hq_quantize(Y, oracle.PER_TENSOR, oracle.SR, seed, 0)
+        assert s[0] == 1.0
+        acc += q[0]
+    mean = acc / n
+    frac = Y[0] - np.floor(Y[0])
+    sigma = np.sqrt(frac * (1 - frac) / n) + 1e-9
+    assert np.all(np.abs(mean - Y[0]) <= 4.5 * sigma + 1e-9)
+
+
+def test_sr_uses_element_index_and_stream():
+    """Values at k + 1/2 round up exactly when the element's Philox word has
+    its top bit clear: ties the code of element (r, c) to word r*cols + c."""
+    rows, cols = 4, 32
+    Y = np.full((rows, cols), 0.5, np.float32)
+    Y[0, 0] = 7.0
+    for stream in (0, 1):
+        q, s = oracle.hq_quantize(Y, oracle.PER_TENSOR, oracle.SR, 99, stream)
+        for r in range(rows):
+            for c in range(cols):
+                if (r, c) == (0, 0):
+                    continue
+                word = oracle.philox_word(99, stream, r * cols + c)
+                assert q[r, c] == (1 if (word >> 8) < (1 << 23) else 0)
+
+
+# ------------------------------------------------------------ Philox
+
+def test_philox_uniformity_and_counter_sensitivity():
+    words = np.array([oracle.philox_word(5, 0, e) for e in range(40000)],
+                     dtype=np.uint64)
+    u = (words >> 8).astype(np.float64) / 2 ** 24
+    assert abs(u.mean() - 0.5) < 4 * math.sqrt(1 / 12 / len(u))
+    hist = np.bincount((words >> 28).astype(np.int64), minlength=16)
+    expected = len(words) / 16
+    chi2 = np.sum((hist - expected) ** 2 / expected)
+    assert chi2 < 45.0                         # 15 dof, p ~ 1e-4
+    assert oracle.philox_word(5, 0, 0) != oracle.philox_word(5, 1, 0)
+    assert oracle.philox_word(5, 0, 0) != oracle.philox_word(6, 0, 0)
+    assert oracle.philox_word(5, 0, 1 << 34) != oracle.philox_word(5, 0, 0)
+    # word e%4 of one block
+    blk = oracle.philox4x32_10([3, 0, 0, 0], [5, 0])
+    assert [oracle.philox_word(5, 0, 12 + i) for i in range(4)] == list(blk)
+
+
+# ------------------------------------------------------------ GEMM, packing
+
+def test_gemm_brute_force():
+    rng = np.random.default_rng(15)
+    A = rng.integers(-127, 128, (5, 37)).astype(np.int8)
+    B = rng.integers(-127, 128, (7, 37)).astype(np.int8)
+    C = oracle.gemm_i64(A, B)
+    for m in range(5):
+        for n in range(7):
+            assert C[m, n] == sum(int(A[m, k]) * int(B[n, k]) for k in range(37))
+
+
+def test_gemm_exhaustive_int4_range():
+    vals = np.arange(-7, 8, dtype=np.int8)
+    A = np.array([[a] * 16 for a in vals], dtype=np.int8)          # [15, 16]
+    B = np.array([[b] * 16 for b in vals], dtype=np.int8)
+    C = oracle.gemm_i64(A, B)
+    assert np.array_equal(C, 16 * np.outer(vals.astype(np.int64),
+                                           vals.astype(np.int64)))
+
+
+def test_pack_int4_layout():
+    codes = np.array([[1, -1, 7, -7, 0, 3]], np.int8)
+    p = oracle.pack_int4(codes)
+    assert list(p[0]) == [0xF1, 0x97, 0x30]
+
+
+def test_dequant_matches_fp64():
+    rng = np.random.default_rng(16)
+    acc = rng.integers(-10 ** 6, 10 ** 6, (6, 5))
+    s_gy = rng.uniform(0.1, 2, 6).astype(np.float32)
+    got = oracle.dequant_gx(acc, s_gy, oracle.PER_TOKEN, np.float32(0.25))
+    want = acc * s_gy.astype(np.float64)[:, None] * 0.25 / 16
+    assert np.allclose(got, want, rtol=1e-15, atol=0)
+    got = oracle.dequant_gw(acc, np.float32(0.5), np.float32(3.0))
+    assert np.allclose(got, acc * 1.5 / 16, rtol=1e-15, atol=0)
+
+
+# --------------------------------------------------- whole paths, lossless
+
+def _lossless_hq_operand(rng, rows, n16, s0):
+    """Data whose Hadamard transform is exactly integer codes times s0."""
+    codes = rng.integers(-7, 8, (rows, 16 * n16))
+    codes[:, 0] = 7                                   # amax = 7*s0 per row
+    D = np.kron(np.eye(n16, dtype=np.int64), H_SCIPY)
+    v = codes @ D / 16.0 * s0                         # D^{-1} = D/16 (symmetric)
+    return v.astype(np.float32), codes
+
+
+def test_gx_path_lossless_equals_gy_w():
+    rng = np.random.default_rng(17)
+    T, Cin, Cout = 32, 48, 64
+    gy, _ = _lossless_hq_operand(rng, T, Cout // 16, 2.0 ** -6)
+    wT, _ = _lossless_hq_operand(rng, Cin, Cout // 16, 2.0 ** -3)
+    w = np.ascontiguousarray(wT.T)                    # [Cout, Cin]
+    for gran in (oracle.PER_TOKEN, oracle.PER_TENSOR):
+        for rnd in (oracle.RNE, oracle.SR):
+            r = oracle.gx_path(gy, w, gran_gy=gran, rnd=rnd, seed=3)
+            want = gy.astype(np.float64) @ w.astype(np.float64)
+            assert np.allclose(r["g_x"], want, rtol=1e-12, atol=1e-15)
+
+
+def test_gw_path_lossless_equals_gyT_x():
+    rng = np.random.default_rng(18)
+    T, Cin, Cout = 64, 20, 24
+    # token pairs equal -> only the kept (even) Hadamard rows are non-zero;
+    # values on a power-of-two grid with |Xbar| hitting 127*s exactly.
+    gy = np.repeat(rng.integers(-3, 4, (T // 2, Cout)), 2, 0).astype(np.float64)
+    x = np.repeat(rng.integers(-3, 4, (T // 2, Cin)), 2, 0).astype(np.float64)
+    gy[:16, 0] = 127 / 16.0 * 2
+    x[:16, 0] = 127 / 16.0 * 2
+    gy = (gy * 2.0 ** -7).astype(np.float32)
+    x = (x * 2.0 ** -2).astype(np.float32)
+    q, s = oracle.compress_activation(x, 8)
+    r = oracle.gw_path(gy, q, s, 8)
+    # lossless only if every coefficient is an integer multiple of its scale
+    assert np.array_equal(r["qG"].astype(np.float64) * r["s_g"], r["Gb"])
+    want = gy.astype(np.float64).T @ x.astype(np.float64)
+    assert np.allclose(r["g_w"], want, rtol=1e-12, atol=1e-15)
