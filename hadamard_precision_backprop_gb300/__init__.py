@@ -1,0 +1,291 @@
+"""hadamard_precision_backprop_gb300: GB300 kernels of the HLQ/HOT backward pass.
+
+The compute lives in ``libhlq.so`` (hand-written sm_103a CUDA behind the C
+ABI of ``include/hlq.h``); this module is the thin Python binding: it
+marshals torch tensors to pointers, allocates outputs and workspaces with
+torch, and passes torch's current CUDA stream.  Every step of the path runs
+in libhlq's kernels; there is no CPU or PyTorch fallback, and loading fails
+loudly when the library has not been built.
+
+Entry points (same names as the C ABI):
+  hlq_compress_activation(x, rank)            -> (xbar int8 [Cin, T'], s_x)
+  hlq_linear_backward_gx(g_y, w, ...)         -> g_x fp32 [T, Cin]
+  hlq_linear_backward_gw(g_y, xbar, s_x, ...) -> g_w fp32 [Cout, Cin]
+  hlq_debug_gx_parts / hlq_debug_gw_parts     -> intermediates for checks
+  hlq_workspace_bytes, hlq_read_device_status, hlq_status_string
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+PER_TENSOR, PER_TOKEN = 0, 1
+RNE, SR = 0, 1
+F32, BF16 = 0, 1
+OP_COMPRESS_ACTIVATION, OP_BACKWARD_GX, OP_BACKWARD_GW = 0, 1, 2
+DEV_NONFINITE, DEV_TIMEOUT, DEV_BADCODE = 0x1, 0x2, 0x4
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "libhlq.so")
+
+EXPORTS = [
+    "hlq_workspace_bytes", "hlq_compress_activation", "hlq_linear_backward_gx",
+    "hlq_linear_backward_gw", "hlq_debug_gx_parts", "hlq_debug_gw_parts",
+    "hlq_read_device_status", "hlq_status_string", "hlq_version",
+    "hlq_debug_hq_transform", "hlq_debug_hla_transform",
+]
+
+_lock = threading.Lock()
+_lib = None
+
+
+class HLQError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+
+
+def build_library(force: bool = False) -> str:
+    """Compile libhlq.so in-tree (nvcc, sm_103a)."""
+    from .build import build as _build
+    return _build(force=force)
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libhlq (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"libhlq is not built ({LIB_PATH} missing); run "
+                "`python -m hadamard_precision_backprop_gb300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        P, i64, i32, u64, sz = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
+                                ctypes.c_uint64, ctypes.c_size_t)
+        sig = {
+            "hlq_workspace_bytes": (sz, [i32, i64, i64, i64, i32, i32]),
+            "hlq_compress_activation": (i32, [P, i32, i64, i64, i32, i32, P, P,
+                                              P, sz, P]),
+            "hlq_linear_backward_gx": (i32, [P, P, i32, i64, i64, i64, i32, i32,
+                                             i32, i32, u64, P, P, sz, P]),
+            "hlq_linear_backward_gw": (i32, [P, i32, P, P, i64, i64, i64, i32,
+                                             i32, P, P, sz, P]),
+            "hlq_debug_gx_parts": (i32, [P, P, i32, i64, i64, i64, i32, i32,
+                                         i32, i32, u64, P, P, sz, P, P, P, P,
+                                         P, P]),
+            "hlq_debug_gw_parts": (i32, [P, i32, P, P, i64, i64, i64, i32, i32,
+                                         P, P, sz, P, P, P, P]),
+            "hlq_read_device_status": (i32, [P, i32, P]),
+            "hlq_debug_hq_transform": (i32, [P, i32, i64, i64, i32, P, P]),
+            "hlq_debug_hla_transform": (i32, [P, i32, i64, i64, i32, P, P]),
+            "hlq_status_string": (ctypes.c_char_p, [i32]),
+            "hlq_version": (i32, []),
+        }
+        for name, (res, args) in sig.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+        return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().hlq_status_string(int(status)).decode()
+
+
+hlq_status_string = status_string
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise HLQError(rc, what)
+
+
+# ----------------------------------------------------------------------------
+# torch marshalling
+# ----------------------------------------------------------------------------
+
+def _torch():
+    import torch
+    return torch
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    torch = _torch()
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return F32
+    raise TypeError(f"unsupported dtype {t.dtype}: use bfloat16 or float32")
+
+
+def _need_cuda_contig(*ts):
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("tensors must be contiguous CUDA tensors")
+
+
+def hlq_workspace_bytes(op: int, T: int, Cin: int, Cout: int, block: int = 16,
+                        rank: int = 8) -> int:
+    return int(lib().hlq_workspace_bytes(op, T, Cin, Cout, block, rank))
+
+
+def workspace(op, T, Cin, Cout, block=16, rank=8, device=None):
+    torch = _torch()
+    n = hlq_workspace_bytes(op, T, Cin, Cout, block, rank)
+    return torch.empty(max(n, 256), dtype=torch.uint8,
+                       device=device or torch.cuda.current_device())
+
+
+def hlq_compress_activation(x, rank: int = 8, block: int = 16, out=None,
+                            scale=None, ws=None, stream=None):
+    """ACBP: x [T, Cin] -> (int8 codes [Cin, T*rank/16], fp32 scale [1])."""
+    torch = _torch()
+    _need_cuda_contig(x)
+    T, Cin = x.shape
+    Tp = T // 16 * rank
+    if out is None:
+        out = torch.empty((Cin, Tp), dtype=torch.int8, device=x.device)
+    if scale is None:
+        scale = torch.empty(1, dtype=torch.float32, device=x.device)
+    if ws is None:
+        ws = workspace(OP_COMPRESS_ACTIVATION, T, Cin, 16, block, rank, x.device)
+    _check(lib().hlq_compress_activation(
+        _ptr(x), _dtype_code(x), T, Cin, block, rank, _ptr(out), _ptr(scale),
+        _ptr(ws), ws.numel(), _stream(stream)), "hlq_compress_activation")
+    return out, scale
+
+
+def hlq_linear_backward_gx(g_y, w, gran_gy: int = PER_TOKEN,
+                           gran_w: int = PER_TENSOR, rnd: int = SR,
+                           seed: int = 0, block: int = 16, out=None, ws=None,
+                           stream=None):
+    """g_x [T, Cin] (fp32) of y = x w^T from g_y [T, Cout] and w [Cout, Cin]."""
+    torch = _torch()
+    _need_cuda_contig(g_y, w)
+    T, Cout = g_y.shape
+    Cout2, Cin = w.shape
+    if Cout2 != Cout or g_y.dtype != w.dtype:
+        raise ValueError("shape/dtype mismatch between g_y and w")
+    if out is None:
+        out = torch.empty((T, Cin), dtype=torch.float32, device=g_y.device)
+    if ws is None:
+        ws = workspace(OP_BACKWARD_GX, T, Cin, Cout, block, 16, g_y.device)
+    _check(lib().hlq_linear_backward_gx(
+        _ptr(g_y), _ptr(w), _dtype_code(g_y), T, Cin, Cout, block, gran_gy,
+        gran_w, rnd, seed, _ptr(out), _ptr(ws), ws.numel(), _stream(stream)),
+        "hlq_linear_backward_gx")
+    return out
+
+
+def hlq_linear_backward_gw(g_y, xbar, xbar_scale, rank: int = 8,
+                           block: int = 16, out=None, ws=None, stream=None):
+    """g_w [Cout, Cin] (fp32) from g_y [T, Cout] and the ACBP buffer."""
+    torch = _torch()
+    _need_cuda_contig(g_y, xbar, xbar_scale)
+    T, Cout = g_y.shape
+    Cin = xbar.shape[0]
+    if out is None:
+        out = torch.empty((Cout, Cin), dtype=torch.float32, device=g_y.device)
+    if ws is None:
+        ws = workspace(OP_BACKWARD_GW, T, Cin, Cout, block, rank, g_y.device)
+    _check(lib().hlq_linear_backward_gw(
+        _ptr(g_y), _dtype_code(g_y), _ptr(xbar), _ptr(xbar_scale), T, Cin,
+        Cout, block, rank, _ptr(out), _ptr(ws), ws.numel(), _stream(stream)),
+        "hlq_linear_backward_gw")
+    return out
+
+
+def hlq_debug_gx_parts(g_y, w, gran_gy=PER_TOKEN, gran_w=PER_TENSOR, rnd=SR,
+                       seed=0, block=16, stream=None):
+    """g_x plus its intermediates: dict(g_x, qgy, sgy, qw, sw, acc)."""
+    torch = _torch()
+    _need_cuda_contig(g_y, w)
+    T, Cout = g_y.shape
+    Cin = w.shape[1]
+    dev = g_y.device
+    r = dict(
+        g_x=torch.empty((T, Cin), dtype=torch.float32, device=dev),
+        qgy=torch.empty((T, Cout), dtype=torch.int8, device=dev),
+        sgy=torch.empty(T if gran_gy == PER_TOKEN else 1, dtype=torch.float32,
+                        device=dev),
+        qw=torch.empty((Cin, Cout), dtype=torch.int8, device=dev),
+        sw=torch.empty(1, dtype=torch.float32, device=dev),
+        acc=torch.empty((T, Cin), dtype=torch.int32, device=dev),
+    )
+    ws = workspace(OP_BACKWARD_GX, T, Cin, Cout, block, 16, dev)
+    _check(lib().hlq_debug_gx_parts(
+        _ptr(g_y), _ptr(w), _dtype_code(g_y), T, Cin, Cout, block, gran_gy,
+        gran_w, rnd, seed, _ptr(r["g_x"]), _ptr(ws), ws.numel(),
+        _ptr(r["qgy"]), _ptr(r["sgy"]), _ptr(r["qw"]), _ptr(r["sw"]),
+        _ptr(r["acc"]), _stream(stream)), "hlq_debug_gx_parts")
+    return r
+
+
+def hlq_debug_gw_parts(g_y, xbar, xbar_scale, rank=8, block=16, stream=None):
+    """g_w plus its intermediates: dict(g_w, qg, sg, acc)."""
+    torch = _torch()
+    _need_cuda_contig(g_y, xbar, xbar_scale)
+    T, Cout = g_y.shape
+    Cin = xbar.shape[0]
+    Tp = T // 16 * rank
+    dev = g_y.device
+    r = dict(
+        g_w=torch.empty((Cout, Cin), dtype=torch.float32, device=dev),
+        qg=torch.empty((Cout, Tp), dtype=torch.int8, device=dev),
+        sg=torch.empty(1, dtype=torch.float32, device=dev),
+        acc=torch.empty((Cout, Cin), dtype=torch.int32, device=dev),
+    )
+    ws = workspace(OP_BACKWARD_GW, T, Cin, Cout, block, rank, dev)
+    _check(lib().hlq_debug_gw_parts(
+        _ptr(g_y), _dtype_code(g_y), _ptr(xbar), _ptr(xbar_scale), T, Cin,
+        Cout, block, rank, _ptr(r["g_w"]), _ptr(ws), ws.numel(), _ptr(r["qg"]),
+        _ptr(r["sg"]), _ptr(r["acc"]), _stream(stream)), "hlq_debug_gw_parts")
+    return r
+
+
+def hlq_debug_hq_transform(src, axis: int, stream=None):
+    """fp32 Hadamard coefficients of src [rows, cols] along cols (axis 0) or
+    rows (axis 1), each the exact sum rounded once to fp32."""
+    torch = _torch()
+    _need_cuda_contig(src)
+    rows, cols = src.shape
+    y = torch.empty((rows, cols), dtype=torch.float32, device=src.device)
+    _check(lib().hlq_debug_hq_transform(_ptr(src), _dtype_code(src), rows,
+                                        cols, axis, _ptr(y), _stream(stream)),
+           "hlq_debug_hq_transform")
+    return y
+
+
+def hlq_debug_hla_transform(src, rank: int = 8, stream=None):
+    """fp32 HLA coefficients [C, T*rank/16] of src [T, C]."""
+    torch = _torch()
+    _need_cuda_contig(src)
+    T, C = src.shape
+    out = torch.empty((C, T // 16 * rank), dtype=torch.float32,
+                      device=src.device)
+    _check(lib().hlq_debug_hla_transform(_ptr(src), _dtype_code(src), T, C,
+                                         rank, _ptr(out), _stream(stream)),
+           "hlq_debug_hla_transform")
+    return out
+
+
+def hlq_read_device_status(clear: bool = False, stream=None) -> int:
+    flags = ctypes.c_uint32(0)
+    _check(lib().hlq_read_device_status(ctypes.byref(flags), 1 if clear else 0,
+                                        _stream(stream)),
+           "hlq_read_device_status")
+    return int(flags.value)

@@ -1,0 +1,367 @@
+// hlq_api.cu -- the C ABI of libhlq (declared in include/hlq.h): argument
+// validation, workspace layout and the launch sequence of each step.
+#include <cstdint>
+#include <cstring>
+#include <cuda_runtime.h>
+
+#include "hlq.h"
+#include "hlq_kernels.h"
+
+namespace hlq {
+
+// Device status word of this library (HLQ_DEV_* flags).  Host code reaches
+// it only through its device address (device_status_ptr).
+__device__ unsigned int g_status_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+unsigned int* g_status_ptr[kMaxDevices] = {};
+
+// Address of the status word on the current device (looked up once).
+unsigned int* device_status_ptr() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    return nullptr;
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+    g_status_ptr[dev] = static_cast<unsigned int*>(p);
+  }
+  return g_status_ptr[dev];
+}
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned256(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
+
+// Workspace layouts (offsets in bytes from ws).
+struct GxLayout {
+  size_t amax, sgy, sw, qy, qw, total;
+};
+struct GwLayout {
+  size_t amax, sg, qg, xw, total;
+};
+
+GxLayout gx_layout(int64_t T, int64_t Cin, int64_t Cout) {
+  GxLayout L{};
+  size_t o = 0;
+  L.amax = o; o += kAlign;                                   // 2 amax slots
+  L.sw = o;   o += kAlign;                                   // s_w
+  L.sgy = o;  o += align_up((size_t)(T > 0 ? T : 1) * 4);    // s_gy
+  L.qy = o;   o += align_up((size_t)T * (size_t)Cout);       // E4M3 [T, Cout]
+  L.qw = o;   o += align_up((size_t)Cin * (size_t)Cout);     // E4M3 [Cin, Cout]
+  L.total = o;
+  return L;
+}
+
+GwLayout gw_layout(int64_t T, int64_t Cin, int64_t Cout, int rank) {
+  GwLayout L{};
+  const int64_t Tp = T / 16 * rank;
+  size_t o = 0;
+  L.amax = o; o += kAlign;
+  L.sg = o;   o += kAlign;
+  L.qg = o;   o += align_up((size_t)Cout * (size_t)Tp * 2);  // bf16 [Cout, T']
+  L.xw = o;   o += align_up((size_t)Cin * (size_t)Tp * 2);   // bf16 [Cin, T']
+  L.total = o;
+  return L;
+}
+
+size_t compress_ws(int64_t, int64_t) { return kAlign; }
+
+bool rank_ok(int rank) {
+  return rank == 1 || rank == 2 || rank == 4 || rank == 8 || rank == 16;
+}
+
+hlq_status check_common(int dt, int64_t T, int64_t Cin, int64_t Cout,
+                        int block) {
+  if (dt != HLQ_F32 && dt != HLQ_BF16) return HLQ_ERR_INVALID_ARG;
+  if (block != 16) return HLQ_ERR_INVALID_ARG;
+  if (T < 0 || Cin < 0 || Cout < 0) return HLQ_ERR_SHAPE;
+  if (T % 16 || Cin % 16 || Cout % 16) return HLQ_ERR_SHAPE;
+  // grid limits of the transform kernels: T/256 and Cout/16 index grid.y
+  if (T > (int64_t)256 * 65535 || Cout > (int64_t)16 * 65535 ||
+      Cin > ((int64_t)1 << 24))
+    return HLQ_ERR_UNSUPPORTED;
+  return HLQ_OK;
+}
+
+hlq_status cuda_status(cudaError_t e) { return e == cudaSuccess ? HLQ_OK : HLQ_ERR_CUDA; }
+
+#define HLQ_TRY(expr)                                  \
+  do {                                                 \
+    cudaError_t _e = (expr);                           \
+    if (_e != cudaSuccess) return HLQ_ERR_CUDA;        \
+  } while (0)
+
+hlq_status gx_impl(const void* gy, const void* w, int dt, int64_t T,
+                   int64_t Cin, int64_t Cout, int block, int gran_gy,
+                   int gran_w, int rnd, uint64_t seed, float* gx, void* ws,
+                   size_t ws_bytes, int8_t* dbg_qgy, float* dbg_sgy,
+                   int8_t* dbg_qw, float* dbg_sw, int32_t* dbg_acc,
+                   void* stream) {
+  hlq_status st = check_common(dt, T, Cin, Cout, block);
+  if (st != HLQ_OK) return st;
+  if (gran_gy != HLQ_PER_TENSOR && gran_gy != HLQ_PER_TOKEN) return HLQ_ERR_INVALID_ARG;
+  if (gran_w != HLQ_PER_TENSOR && gran_w != HLQ_PER_TOKEN) return HLQ_ERR_INVALID_ARG;
+  if (gran_w != HLQ_PER_TENSOR) return HLQ_ERR_UNSUPPORTED;
+  if (rnd != HLQ_RNE && rnd != HLQ_SR) return HLQ_ERR_INVALID_ARG;
+  const int64_t n_gx = T * Cin;
+  if (n_gx > 0 && !gx) return HLQ_ERR_INVALID_ARG;
+  if (T * Cout > 0 && !gy) return HLQ_ERR_INVALID_ARG;
+  if (Cout * Cin > 0 && !w) return HLQ_ERR_INVALID_ARG;
+  if (!aligned16(gy) || !aligned16(w) || !aligned16(gx)) return HLQ_ERR_ALIGN;
+  // |acc| <= 49 * Cout must stay exact through an fp32 accumulator
+  if (49 * Cout >= ((int64_t)1 << 24)) return HLQ_ERR_OVERFLOW;
+  const GxLayout L = gx_layout(T, Cin, Cout);
+  if (!ws || ws_bytes < L.total) return HLQ_ERR_WORKSPACE;
+  if (!aligned256(ws)) return HLQ_ERR_ALIGN;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (n_gx == 0) return HLQ_OK;
+  if (Cout == 0) {  // empty contraction: g_x = 0
+    HLQ_TRY(cudaMemsetAsync(gx, 0, (size_t)n_gx * 4, s));
+    if (dbg_acc) HLQ_TRY(cudaMemsetAsync(dbg_acc, 0, (size_t)n_gx * 4, s));
+    return HLQ_OK;
+  }
+  unsigned int* status = device_status_ptr();
+  if (!status) return HLQ_ERR_CUDA;
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  unsigned int* amax = reinterpret_cast<unsigned int*>(base + L.amax);
+  float* sgy = reinterpret_cast<float*>(base + L.sgy);
+  float* sw = reinterpret_cast<float*>(base + L.sw);
+  uint8_t* qy = base + L.qy;
+  uint8_t* qw = base + L.qw;
+  const bool bf16 = dt == HLQ_BF16;
+  const bool per_token = gran_gy == HLQ_PER_TOKEN;
+
+  HLQ_TRY(cudaMemsetAsync(amax, 0, 8, s));
+  if (!per_token)
+    HLQ_TRY(launch_hq_rows(gy, bf16, T, Cout, false, true, amax, nullptr,
+                           nullptr, rnd, seed, 0, status, s));
+  HLQ_TRY(launch_hq_rows(gy, bf16, T, Cout, per_token, false, amax, qy, sgy,
+                         rnd, seed, 0, status, s));
+  HLQ_TRY(launch_hq_cols(w, bf16, Cout, Cin, true, amax + 1, nullptr, nullptr,
+                         rnd, seed, 1, status, s));
+  HLQ_TRY(launch_hq_cols(w, bf16, Cout, Cin, false, amax + 1, qw, sw, rnd,
+                         seed, 1, status, s));
+  HLQ_TRY(launch_gemm_simple(qy, kFmtE4M3, qw, kFmtE4M3, T, Cin, Cout, sgy,
+                             per_token, sw, gx, dbg_acc, s));
+  if (dbg_qgy) HLQ_TRY(launch_decode_e4m3(qy, dbg_qgy, T * Cout, s));
+  if (dbg_qw) HLQ_TRY(launch_decode_e4m3(qw, dbg_qw, Cin * Cout, s));
+  if (dbg_sgy)
+    HLQ_TRY(cudaMemcpyAsync(dbg_sgy, sgy, (size_t)(per_token ? T : 1) * 4,
+                            cudaMemcpyDeviceToDevice, s));
+  if (dbg_sw) HLQ_TRY(cudaMemcpyAsync(dbg_sw, sw, 4, cudaMemcpyDeviceToDevice, s));
+  return HLQ_OK;
+}
+
+hlq_status gw_impl(const void* gy, int dt, const int8_t* xbar,
+                   const float* xscale, int64_t T, int64_t Cin, int64_t Cout,
+                   int block, int rank, float* gw, void* ws, size_t ws_bytes,
+                   int8_t* dbg_qg, float* dbg_sg, int32_t* dbg_acc,
+                   void* stream) {
+  hlq_status st = check_common(dt, T, Cin, Cout, block);
+  if (st != HLQ_OK) return st;
+  if (!rank_ok(rank)) return HLQ_ERR_INVALID_ARG;
+  const int64_t Tp = T / 16 * rank;
+  const int64_t n_gw = Cout * Cin;
+  if (n_gw > 0 && !gw) return HLQ_ERR_INVALID_ARG;
+  if (T * Cout > 0 && !gy) return HLQ_ERR_INVALID_ARG;
+  if (Cin * Tp > 0 && !xbar) return HLQ_ERR_INVALID_ARG;
+  if (!xscale) return HLQ_ERR_INVALID_ARG;
+  if (!aligned16(gy) || !aligned16(xbar) || !aligned16(gw)) return HLQ_ERR_ALIGN;
+  if (Tp * 127 * 127 >= ((int64_t)1 << 31)) return HLQ_ERR_OVERFLOW;
+  const GwLayout L = gw_layout(T, Cin, Cout, rank);
+  if (!ws || ws_bytes < L.total) return HLQ_ERR_WORKSPACE;
+  if (!aligned256(ws)) return HLQ_ERR_ALIGN;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (n_gw == 0) return HLQ_OK;
+  if (Tp == 0) {  // no tokens: g_w = 0
+    HLQ_TRY(cudaMemsetAsync(gw, 0, (size_t)n_gw * 4, s));
+    if (dbg_acc) HLQ_TRY(cudaMemsetAsync(dbg_acc, 0, (size_t)n_gw * 4, s));
+    return HLQ_OK;
+  }
+  unsigned int* status = device_status_ptr();
+  if (!status) return HLQ_ERR_CUDA;
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  unsigned int* amax = reinterpret_cast<unsigned int*>(base + L.amax);
+  float* sg = reinterpret_cast<float*>(base + L.sg);
+  void* qg = base + L.qg;
+  const bool bf16 = dt == HLQ_BF16;
+
+  HLQ_TRY(cudaMemsetAsync(amax, 0, 4, s));
+  HLQ_TRY(launch_hla(gy, bf16, T, Cout, rank, true, true, amax, nullptr,
+                     nullptr, status, s));
+  HLQ_TRY(launch_hla(gy, bf16, T, Cout, rank, false, true, amax, qg, sg,
+                     status, s));
+  HLQ_TRY(launch_gemm_simple(qg, kFmtBF16, xbar, kFmtI8, Cout, Cin, Tp, sg,
+                             false, xscale, gw, dbg_acc, s));
+  if (dbg_qg) HLQ_TRY(launch_decode_bf16(qg, dbg_qg, Cout * Tp, s));
+  if (dbg_sg) HLQ_TRY(cudaMemcpyAsync(dbg_sg, sg, 4, cudaMemcpyDeviceToDevice, s));
+  return HLQ_OK;
+}
+
+}  // namespace
+}  // namespace hlq
+
+using namespace hlq;
+
+extern "C" {
+
+size_t hlq_workspace_bytes(int op, int64_t T, int64_t Cin, int64_t Cout,
+                           int block, int rank) {
+  (void)block;
+  if (T < 0 || Cin < 0 || Cout < 0) return 0;
+  switch (op) {
+    case HLQ_OP_COMPRESS_ACTIVATION:
+      return compress_ws(T, Cin);
+    case HLQ_OP_BACKWARD_GX:
+      return gx_layout(T, Cin, Cout).total;
+    case HLQ_OP_BACKWARD_GW:
+      return gw_layout(T, Cin, Cout, rank_ok(rank) ? rank : 16).total;
+    default:
+      return 0;
+  }
+}
+
+hlq_status hlq_compress_activation(const void* d_x, int dt, int64_t T,
+                                   int64_t Cin, int block, int rank,
+                                   int8_t* d_xbar, float* d_xbar_scale,
+                                   void* d_ws, size_t ws_bytes, void* stream) {
+  hlq_status st = check_common(dt, T, Cin, 16, block);
+  if (st != HLQ_OK) return st;
+  if (!rank_ok(rank)) return HLQ_ERR_INVALID_ARG;
+  const int64_t Tp = T / 16 * rank;
+  if (!d_xbar_scale) return HLQ_ERR_INVALID_ARG;
+  if (Cin * Tp > 0 && (!d_x || !d_xbar)) return HLQ_ERR_INVALID_ARG;
+  if (!aligned16(d_x) || !aligned16(d_xbar)) return HLQ_ERR_ALIGN;
+  if (!d_ws || ws_bytes < compress_ws(T, Cin)) return HLQ_ERR_WORKSPACE;
+  if (!aligned256(d_ws)) return HLQ_ERR_ALIGN;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (Cin * Tp == 0) {
+    HLQ_TRY(cudaMemsetAsync(d_xbar_scale, 0, 4, s));
+    return HLQ_OK;
+  }
+  unsigned int* status = device_status_ptr();
+  if (!status) return HLQ_ERR_CUDA;
+  unsigned int* amax = static_cast<unsigned int*>(d_ws);
+  const bool bf16 = dt == HLQ_BF16;
+  HLQ_TRY(cudaMemsetAsync(amax, 0, 4, s));
+  HLQ_TRY(launch_hla(d_x, bf16, T, Cin, rank, true, false, amax, nullptr,
+                     nullptr, status, s));
+  HLQ_TRY(launch_hla(d_x, bf16, T, Cin, rank, false, false, amax, d_xbar,
+                     d_xbar_scale, status, s));
+  return HLQ_OK;
+}
+
+hlq_status hlq_linear_backward_gx(const void* d_gy, const void* d_w, int dt,
+                                  int64_t T, int64_t Cin, int64_t Cout,
+                                  int block, int gran_gy, int gran_w, int rnd,
+                                  uint64_t seed, float* d_gx, void* d_ws,
+                                  size_t ws_bytes, void* stream) {
+  return gx_impl(d_gy, d_w, dt, T, Cin, Cout, block, gran_gy, gran_w, rnd,
+                 seed, d_gx, d_ws, ws_bytes, nullptr, nullptr, nullptr,
+                 nullptr, nullptr, stream);
+}
+
+hlq_status hlq_linear_backward_gw(const void* d_gy, int dt,
+                                  const int8_t* d_xbar,
+                                  const float* d_xbar_scale, int64_t T,
+                                  int64_t Cin, int64_t Cout, int block,
+                                  int rank, float* d_gw, void* d_ws,
+                                  size_t ws_bytes, void* stream) {
+  return gw_impl(d_gy, dt, d_xbar, d_xbar_scale, T, Cin, Cout, block, rank,
+                 d_gw, d_ws, ws_bytes, nullptr, nullptr, nullptr, stream);
+}
+
+hlq_status hlq_debug_gx_parts(const void* d_gy, const void* d_w, int dt,
+                              int64_t T, int64_t Cin, int64_t Cout, int block,
+                              int gran_gy, int gran_w, int rnd, uint64_t seed,
+                              float* d_gx, void* d_ws, size_t ws_bytes,
+                              int8_t* d_qgy, float* d_sgy, int8_t* d_qw,
+                              float* d_sw, int32_t* d_acc, void* stream) {
+  return gx_impl(d_gy, d_w, dt, T, Cin, Cout, block, gran_gy, gran_w, rnd,
+                 seed, d_gx, d_ws, ws_bytes, d_qgy, d_sgy, d_qw, d_sw, d_acc,
+                 stream);
+}
+
+hlq_status hlq_debug_gw_parts(const void* d_gy, int dt, const int8_t* d_xbar,
+                              const float* d_xbar_scale, int64_t T,
+                              int64_t Cin, int64_t Cout, int block, int rank,
+                              float* d_gw, void* d_ws, size_t ws_bytes,
+                              int8_t* d_qg, float* d_sg, int32_t* d_acc,
+                              void* stream) {
+  return gw_impl(d_gy, dt, d_xbar, d_xbar_scale, T, Cin, Cout, block, rank,
+                 d_gw, d_ws, ws_bytes, d_qg, d_sg, d_acc, stream);
+}
+
+hlq_status hlq_debug_hq_transform(const void* d_src, int dt, int64_t rows,
+                                  int64_t cols, int axis, float* d_y,
+                                  void* stream) {
+  if (dt != HLQ_F32 && dt != HLQ_BF16) return HLQ_ERR_INVALID_ARG;
+  if (axis != 0 && axis != 1) return HLQ_ERR_INVALID_ARG;
+  if (rows < 0 || cols < 0 || rows % 16 || cols % 16) return HLQ_ERR_SHAPE;
+  if (rows / 16 > 65535 && axis == 1) return HLQ_ERR_UNSUPPORTED;
+  if (rows * cols > 0 && (!d_src || !d_y)) return HLQ_ERR_INVALID_ARG;
+  if (!aligned16(d_src) || !aligned16(d_y)) return HLQ_ERR_ALIGN;
+  if (rows * cols == 0) return HLQ_OK;
+  unsigned int* status = device_status_ptr();
+  if (!status) return HLQ_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool bf16 = dt == HLQ_BF16;
+  if (axis == 0)
+    HLQ_TRY(launch_hq_rows_transform(d_src, bf16, rows, cols, d_y, status, s));
+  else
+    HLQ_TRY(launch_hq_cols_transform(d_src, bf16, rows, cols, d_y, status, s));
+  return HLQ_OK;
+}
+
+hlq_status hlq_debug_hla_transform(const void* d_src, int dt, int64_t T,
+                                   int64_t C, int rank, float* d_out,
+                                   void* stream) {
+  if (dt != HLQ_F32 && dt != HLQ_BF16) return HLQ_ERR_INVALID_ARG;
+  if (!rank_ok(rank)) return HLQ_ERR_INVALID_ARG;
+  if (T < 0 || C < 0 || T % 16 || C % 16) return HLQ_ERR_SHAPE;
+  if (T / 16 > 65535) return HLQ_ERR_UNSUPPORTED;
+  if (T * C > 0 && (!d_src || !d_out)) return HLQ_ERR_INVALID_ARG;
+  if (!aligned16(d_src) || !aligned16(d_out)) return HLQ_ERR_ALIGN;
+  if (T * C == 0) return HLQ_OK;
+  unsigned int* status = device_status_ptr();
+  if (!status) return HLQ_ERR_CUDA;
+  HLQ_TRY(launch_hla_transform(d_src, dt == HLQ_BF16, T, C, rank, d_out, status,
+                               static_cast<cudaStream_t>(stream)));
+  return HLQ_OK;
+}
+
+hlq_status hlq_read_device_status(uint32_t* flags, int clear, void* stream) {
+  if (!flags) return HLQ_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned int* status = device_status_ptr();
+  if (!status) return HLQ_ERR_CUDA;
+  unsigned int v = 0;
+  HLQ_TRY(cudaMemcpyAsync(&v, status, 4, cudaMemcpyDeviceToHost, s));
+  if (clear) HLQ_TRY(cudaMemsetAsync(status, 0, 4, s));
+  HLQ_TRY(cudaStreamSynchronize(s));
+  *flags = v;
+  return HLQ_OK;
+}
+
+const char* hlq_status_string(int status) {
+  switch (status) {
+    case HLQ_OK: return "HLQ_OK";
+    case HLQ_ERR_INVALID_ARG: return "HLQ_ERR_INVALID_ARG";
+    case HLQ_ERR_SHAPE: return "HLQ_ERR_SHAPE";
+    case HLQ_ERR_ALIGN: return "HLQ_ERR_ALIGN";
+    case HLQ_ERR_UNSUPPORTED: return "HLQ_ERR_UNSUPPORTED";
+    case HLQ_ERR_WORKSPACE: return "HLQ_ERR_WORKSPACE";
+    case HLQ_ERR_OVERFLOW: return "HLQ_ERR_OVERFLOW";
+    case HLQ_ERR_CUDA: return "HLQ_ERR_CUDA";
+    default: return "HLQ_UNKNOWN_STATUS";
+  }
+}
+
+int hlq_version(void) { return 0x000100; }
+
+}  // extern "C"

@@ -1,0 +1,284 @@
+// hlq_device.cuh -- device building blocks shared by the HLQ kernels:
+// input decoding, the exact 16-point Hadamard sums, Philox4x32-10, the
+// int4/int8 quantizers and the device status word.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "hlq.h"
+
+namespace hlq {
+
+// Device status word (HLQ_DEV_* flags): every kernel that can detect a
+// device-side condition takes its address; hlq_read_device_status reads it.
+__device__ __forceinline__ void raise_flag(unsigned int* status, unsigned int f) {
+  atomicOr(status, f);
+}
+
+// ---------------------------------------------------------------------------
+// Input decoding.  bf16 is the top half of an fp32, so widening is exact.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float bf16_lo(uint32_t pair) {
+  return __uint_as_float(pair << 16);
+}
+__device__ __forceinline__ float bf16_hi(uint32_t pair) {
+  return __uint_as_float(pair & 0xffff0000u);
+}
+
+// ---------------------------------------------------------------------------
+// Exactness test for the fp32 butterfly.
+//
+// A 16-point Hadamard sum of values whose largest exponent field is emax and
+// whose smallest (non-zero, subnormals counted as field 1) is emin needs
+// emax - emin + 24 + 4 bits for fp32 inputs (24-bit significands) and
+// emax - emin + 8 + 4 bits for bf16 inputs (8-bit significands).  When that fits in fp32's 24-bit
+// significand, every partial sum of the butterfly is exact, so the result is
+// the exact sum whatever the order, i.e. the once-rounded value.
+// We track, per value, (field, field_for_min) with zeros mapped to
+// (0, 255) so that they drop out of both extremes.
+// ---------------------------------------------------------------------------
+struct ExpRange {
+  uint32_t emax;  // max exponent field
+  uint32_t emin;  // min exponent field over non-zero values (>= 1)
+};
+
+__device__ __forceinline__ void exp_range_add(ExpRange& r, float v) {
+  uint32_t b = __float_as_uint(v) & 0x7fffffffu;
+  uint32_t e = b >> 23;
+  uint32_t emn = (b == 0u) ? 255u : max(e, 1u);
+  r.emax = max(r.emax, e);
+  r.emin = min(r.emin, emn);
+}
+
+__device__ __forceinline__ ExpRange exp_range_init() { return {0u, 255u}; }
+
+// bf16 inputs: exact when emax - emin <= 12; fp32 inputs never qualify.
+template <bool kBf16>
+__device__ __forceinline__ bool butterfly_exact(const ExpRange& r) {
+  if (r.emin == 255u) return true;  // all zero
+  if (!kBf16) return false;
+  return r.emax - r.emin <= 12u;
+}
+
+__device__ __forceinline__ bool any_nonfinite(const ExpRange& r) {
+  return r.emax == 255u;
+}
+
+// ---------------------------------------------------------------------------
+// Exact signed sum of 16 fp32 values, rounded once to fp32 (nearest, ties to
+// even).  Fallback for blocks whose exponent spread defeats the fp32
+// butterfly.  Each finite fp32 is m * 2^(p - 149) with m < 2^24, p >= 0;
+// the sum is held as a signed 320-bit two's-complement integer in units of
+// 2^-149 spread over ten 32-bit digits carried in int64 (signed digits, one
+// carry pass at the end), then rounded by direct construction of the fp32
+// bit pattern.  `neg_mask` bit j negates term j.
+// ---------------------------------------------------------------------------
+static __device__ __noinline__ float exact_sum16(const float* v, uint32_t neg_mask) {
+  long long d[10];
+#pragma unroll
+  for (int i = 0; i < 10; ++i) d[i] = 0;
+  for (int j = 0; j < 16; ++j) {
+    uint32_t b = __float_as_uint(v[j]);
+    uint32_t e = (b >> 23) & 0xffu;
+    uint32_t m = b & 0x7fffffu;
+    if (e == 255u) continue;  // non-finite: flagged elsewhere
+    if (e != 0u) m |= 0x800000u;
+    if (m == 0u) continue;
+    int p = (e != 0u) ? int(e) - 1 : 0;
+    unsigned long long w = (unsigned long long)m << (p & 31);
+    long long lo = (long long)(w & 0xffffffffull), hi = (long long)(w >> 32);
+    int li = p >> 5;
+    bool neg = ((b >> 31) ^ ((neg_mask >> j) & 1u)) != 0u;
+    if (neg) {
+      d[li] -= lo;
+      d[li + 1] -= hi;
+    } else {
+      d[li] += lo;
+      d[li + 1] += hi;
+    }
+  }
+  // carry pass: digits 0..8 end in [0, 2^32); digit 9 keeps the sign
+  for (int i = 0; i < 9; ++i) {
+    long long c = d[i] >> 32;  // arithmetic shift: floor division
+    d[i] -= c * 4294967296ll;
+    d[i + 1] += c;
+  }
+  bool negative = d[9] < 0;
+  uint32_t u[10];
+  if (negative) {  // magnitude = two's complement of the 320-bit value
+    unsigned long long carry = 1;
+    for (int i = 0; i < 10; ++i) {
+      unsigned long long t =
+          (unsigned long long)(~(uint32_t)(d[i] & 0xffffffffll)) + carry;
+      u[i] = (uint32_t)t;
+      carry = t >> 32;
+    }
+  } else {
+    for (int i = 0; i < 10; ++i) u[i] = (uint32_t)d[i];
+  }
+  int top = -1;
+  for (int i = 9; i >= 0; --i)
+    if (u[i] != 0u) {
+      top = i * 32 + 31 - __clz(u[i]);
+      break;
+    }
+  if (top < 0) return 0.0f;
+  uint32_t bits;
+  if (top <= 23) {
+    bits = u[0];  // m * 2^-149 with m < 2^24 is its own fp32 bit pattern
+  } else {
+    int shift = top - 23;
+    int k = shift >> 5, r = shift & 31;
+    unsigned long long win =
+        (unsigned long long)u[k] | ((unsigned long long)u[k + 1] << 32);
+    uint32_t keep = (uint32_t)(win >> r) & 0xffffffu;  // r + 24 <= 56 bits
+    // round bit (shift-1) and sticky bits (below shift-1)
+    int rb = shift - 1;
+    uint32_t round_bit = (u[rb >> 5] >> (rb & 31)) & 1u;
+    bool sticky = (u[rb >> 5] & ((1u << (rb & 31)) - 1u)) != 0u;
+    for (int i = 0; i < (rb >> 5); ++i) sticky |= (u[i] != 0u);
+    if (round_bit && (sticky || (keep & 1u))) ++keep;
+    if (keep == (1u << 24)) {
+      keep >>= 1;
+      ++shift;
+    }
+    bits = ((uint32_t)shift << 23) + keep;  // exponent field shift+1
+  }
+  return __uint_as_float(bits | (negative ? 0x80000000u : 0u));
+}
+
+// Sylvester H16 row i as a negate mask: bit j set when popcount(i & j) odd.
+__device__ __forceinline__ uint32_t hrow_negmask(int i) {
+  uint32_t m = 0;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) m |= (uint32_t)(__popc(i & j) & 1) << j;
+  return m;
+}
+
+// In-place 16-point fast Walsh-Hadamard transform in Sylvester (natural)
+// order: y_i = sum_j (-1)^popcount(i&j) x_j.
+__device__ __forceinline__ void fwht16(float* x) {
+#pragma unroll
+  for (int h = 1; h < 16; h <<= 1)
+#pragma unroll
+    for (int a = 0; a < 16; ++a)
+      if ((a & h) == 0) {
+        float p = x[a], q = x[a + h];
+        x[a] = p + q;
+        x[a + h] = p - q;
+      }
+}
+
+// 8-point butterfly (the three within-octet stages of a 16-point one).
+__device__ __forceinline__ void fwht8(float* x) {
+#pragma unroll
+  for (int h = 1; h < 8; h <<= 1)
+#pragma unroll
+    for (int a = 0; a < 8; ++a)
+      if ((a & h) == 0) {
+        float p = x[a], q = x[a + h];
+        x[a] = p + q;
+        x[a + h] = p - q;
+      }
+}
+
+// Sylvester row of sequency k: bit-reversed (4 bits) Gray code of k.
+__device__ __forceinline__ int sequency_row(int k) {
+  int g = k ^ (k >> 1);
+  return ((g & 1) << 3) | ((g & 2) << 1) | ((g & 4) >> 1) | ((g & 8) >> 3);
+}
+
+// ---------------------------------------------------------------------------
+// Philox4x32-10 (Salmon et al., "Parallel Random Numbers: As Easy as 1, 2,
+// 3", SC'11).  Counter (c0..c3), key (k0, k1).
+// ---------------------------------------------------------------------------
+struct U4 {
+  uint32_t x, y, z, w;
+};
+
+__device__ __forceinline__ U4 philox4x32_10(uint32_t c0, uint32_t c1,
+                                            uint32_t c2, uint32_t c3,
+                                            uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    unsigned long long p0 = (unsigned long long)0xD2511F53u * c0;
+    unsigned long long p1 = (unsigned long long)0xCD9E8D57u * c2;
+    uint32_t n0 = (uint32_t)(p1 >> 32) ^ c1 ^ k0;
+    uint32_t n2 = (uint32_t)(p0 >> 32) ^ c3 ^ k1;
+    c1 = (uint32_t)p1;
+    c3 = (uint32_t)p0;
+    c0 = n0;
+    c2 = n2;
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  return {c0, c1, c2, c3};
+}
+
+// The four words for elements 4q .. 4q+3 of `stream`.
+__device__ __forceinline__ U4 philox_block(uint64_t seed, uint32_t stream,
+                                           uint64_t q) {
+  return philox4x32_10((uint32_t)q, (uint32_t)(q >> 32), stream, 0u,
+                       (uint32_t)seed, (uint32_t)(seed >> 32));
+}
+
+// ---------------------------------------------------------------------------
+// Quantizers.  s == 0 gives code 0.  Division is IEEE round-to-nearest.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int quant_sr(float y, float s, uint32_t word,
+                                        int qmax) {
+  if (s == 0.0f) return 0;
+  float x = __fdiv_rn(y, s);
+  float f = floorf(x);
+  float frac = x - f;
+  float u = __uint2float_rn(word >> 8) * 5.9604644775390625e-08f;  // 2^-24
+  float r = f + ((u < frac) ? 1.0f : 0.0f);
+  r = fminf(fmaxf(r, -(float)qmax), (float)qmax);
+  return (int)r;
+}
+
+__device__ __forceinline__ int quant_rne(float y, float s, int qmax) {
+  if (s == 0.0f) return 0;
+  float x = __fdiv_rn(y, s);
+  float r = rintf(x);
+  r = fminf(fmaxf(r, -(float)qmax), (float)qmax);
+  return (int)r;
+}
+
+// E4M3 byte of an integer in [-7, 7] (exact): |q| = 1.m * 2^e, bias 7.
+__device__ __forceinline__ uint32_t e4m3_of_int(int q) {
+  // table for |q| = 0..7: 0x00 0x38 0x40 0x44 0x48 0x4A 0x4C 0x4E
+  const uint32_t lo = 0x44403800u, hi = 0x4E4C4A48u;
+  int a = q < 0 ? -q : q;
+  uint32_t mag = ((a < 4 ? lo : hi) >> (8 * (a & 3))) & 0xffu;
+  return mag | (q < 0 ? 0x80u : 0u);
+}
+
+// Integer value of an E4M3 byte that encodes an integer in [-7, 7].
+__device__ __forceinline__ int int_of_e4m3(uint32_t b) {
+  uint32_t mag = b & 0x7fu;
+  int v;
+  if (mag == 0u) {
+    v = 0;
+  } else {
+    int e = int(mag >> 3) - 7;          // unbiased exponent (0..2 here)
+    int m = int(mag & 7u) | 8;          // 1.mmm as 4 bits
+    v = (e >= 3) ? (m << (e - 3)) : (m >> (3 - e));
+  }
+  return (b & 0x80u) ? -v : v;
+}
+
+// Max of non-negative floats by their bit patterns (monotone for >= 0).
+__device__ __forceinline__ void atomic_max_nonneg(unsigned int* slot, float v) {
+  atomicMax(slot, __float_as_uint(v));
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+}  // namespace hlq

@@ -1,0 +1,68 @@
+// hlq_kernels.h -- host-side launchers of the libhlq kernels (internal).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace hlq {
+
+// HQ of a [rows, cols] tensor along cols (g_y).  amax_only: per-tensor
+// pre-pass into *amax_slot.  Otherwise writes E4M3 codes [rows, cols] and
+// scales ([rows] if per_token else [1], from *amax_slot).
+cudaError_t launch_hq_rows(const void* src, bool bf16, int64_t rows,
+                           int64_t cols, bool per_token, bool amax_only,
+                           unsigned int* amax_slot, uint8_t* codes,
+                           float* scales, int rnd, uint64_t seed,
+                           uint32_t stream_id, unsigned int* status,
+                           cudaStream_t st);
+
+// HQ of a [rows, cols] tensor along rows (w), codes written transposed
+// [cols, rows] (E4M3), per-tensor scale from *amax_slot.
+cudaError_t launch_hq_cols(const void* src, bool bf16, int64_t rows,
+                           int64_t cols, bool amax_only,
+                           unsigned int* amax_slot, uint8_t* codes_t,
+                           float* scale, int rnd, uint64_t seed,
+                           uint32_t stream_id, unsigned int* status,
+                           cudaStream_t st);
+
+// HLA of src [T, C] along tokens -> codes [C, T*rank/16] (int8, or bf16
+// values when out_bf16), per-tensor scale from *amax_slot.
+cudaError_t launch_hla(const void* src, bool bf16, int64_t T, int64_t C,
+                       int rank, bool amax_only, bool out_bf16,
+                       unsigned int* amax_slot, void* out, float* scale,
+                       unsigned int* status, cudaStream_t st);
+size_t hla_smem_bytes(int rank, bool out_bf16);
+
+// Transform only (fp32 coefficients), for bit-exact checks.
+cudaError_t launch_hq_rows_transform(const void* src, bool bf16, int64_t rows,
+                                     int64_t cols, float* Y,
+                                     unsigned int* status, cudaStream_t st);
+cudaError_t launch_hq_cols_transform(const void* src, bool bf16, int64_t rows,
+                                     int64_t cols, float* Y,
+                                     unsigned int* status, cudaStream_t st);
+cudaError_t launch_hla_transform(const void* src, bool bf16, int64_t T,
+                                 int64_t C, int rank, float* out,
+                                 unsigned int* status, cudaStream_t st);
+
+cudaError_t launch_widen_i8_bf16(const int8_t* in, void* out, int64_t n,
+                                 cudaStream_t st);
+cudaError_t launch_decode_e4m3(const uint8_t* in, int8_t* out, int64_t n,
+                               cudaStream_t st);
+cudaError_t launch_decode_bf16(const void* in, int8_t* out, int64_t n,
+                               cudaStream_t st);
+
+// Operand code formats of the GEMMs.
+enum CodeFmt { kFmtE4M3 = 0, kFmtI8 = 1, kFmtBF16 = 2 };
+
+// Exact integer GEMM on CUDA cores (dp4a): acc[m, n] = sum_k A[m,k] B[n,k],
+// A [M, K], B [N, K] (contraction dim contiguous).  Epilogue:
+// out[m, n] = float(acc) * (sa[per_row_a ? m : 0] * sb[0]) * 0.0625f.
+// acc_out (nullable) receives the int32 sums.
+cudaError_t launch_gemm_simple(const void* A, int fmtA, const void* B,
+                               int fmtB, int64_t M, int64_t N, int64_t K,
+                               const float* sa, bool per_row_a,
+                               const float* sb, float* out, int32_t* acc_out,
+                               cudaStream_t st);
+
+}  // namespace hlq

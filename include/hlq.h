@@ -1,0 +1,201 @@
+/*
+ * hlq.h -- C ABI of libhlq, the GB300 (sm_103a) kernels of the HLQ/HOT
+ * backward pass of one linear layer y = x . w^T (or an im2col'd conv).
+ *
+ * Method: "HLQ: Fast and Efficient Backpropagation via Hadamard Low-rank
+ * Quantization" (Kim & Park), TL;DR: g_x = g_y . w through 4-bit Hadamard
+ * quantization (HQ) and g_w = (1/B) gbar_y^T . xbar through the Hadamard
+ * low-rank approximation (HLA) with int8 arithmetic, the stored activation
+ * compressed at forward time (ACBP); "HOT: Hadamard-based Optimized
+ * Training", Approach: the same assignment of HQ / HLA+int8 to the two
+ * gradient paths, activation buffer compression, and per-token vs
+ * per-tensor quantizer chosen per layer.
+ *
+ * Shapes: x [T, Cin], w [Cout, Cin], g_y [T, Cout], g_x [T, Cin],
+ * g_w [Cout, Cin]; every matrix row-major (last index contiguous).
+ * Block B = 16 (Hadamard block, also the 1/B of the g_w formula).
+ * T' = T * rank / 16 is the reduced token count of the HLA.
+ *
+ * Conventions for every entry point:
+ *  - Pointers named d_* are device pointers owned by the caller; the library
+ *    never allocates or frees device memory.  Scratch goes in a caller
+ *    workspace `ws` of at least hlq_workspace_bytes(...) bytes (256-byte
+ *    aligned).  Device pointers must be 16-byte aligned.
+ *  - All work is enqueued on `stream` (a cudaStream_t passed as void*;
+ *    NULL = legacy default stream) and is asynchronous.  The only call that
+ *    waits is hlq_read_device_status.
+ *  - Arguments are validated on the host before anything is enqueued; a
+ *    non-OK status means nothing was launched and no memory was written.
+ *    Launch errors return HLQ_ERR_CUDA.  Nothing aborts, throws or traps:
+ *    device-side conditions (non-finite input) set a flag that
+ *    hlq_read_device_status returns.
+ *  - Preconditions: block == 16; rank in {1, 2, 4, 8, 16}; T, Cin, Cout
+ *    multiples of 16 (zero allowed: the outputs are then zero-filled);
+ *    finite inputs with |v| <= FLT_MAX/16.
+ */
+#ifndef HLQ_H
+#define HLQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    HLQ_OK = 0,
+    HLQ_ERR_INVALID_ARG = 1, /* null pointer, bad enum, bad block/rank */
+    HLQ_ERR_SHAPE = 2,       /* size not a multiple of 16, negative */
+    HLQ_ERR_ALIGN = 3,       /* pointer not 16-byte (ws: 256-byte) aligned */
+    HLQ_ERR_UNSUPPORTED = 4, /* valid but not implemented (e.g. per-token w) */
+    HLQ_ERR_WORKSPACE = 5,   /* ws_bytes below hlq_workspace_bytes() */
+    HLQ_ERR_OVERFLOW = 6,    /* an integer accumulator could overflow */
+    HLQ_ERR_CUDA = 7         /* a CUDA launch or copy failed */
+} hlq_status;
+
+typedef enum { HLQ_F32 = 0, HLQ_BF16 = 1 } hlq_dtype;
+
+/* Layer-wise quantizer selection (HOT, Approach): one scale per tensor, or
+ * one scale per token (row of g_y). */
+typedef enum { HLQ_PER_TENSOR = 0, HLQ_PER_TOKEN = 1 } hlq_gran;
+
+/* Rounding of the int4 HQ codes: stochastic (Philox4x32-10 keyed on seed and
+ * element index) or round-to-nearest-even (for tests). */
+typedef enum { HLQ_RNE = 0, HLQ_SR = 1 } hlq_round;
+
+typedef enum {
+    HLQ_OP_COMPRESS_ACTIVATION = 0,
+    HLQ_OP_BACKWARD_GX = 1,
+    HLQ_OP_BACKWARD_GW = 2
+} hlq_op;
+
+/* Device status flags (hlq_read_device_status). */
+#define HLQ_DEV_NONFINITE 0x1u /* a transform input was inf or NaN */
+#define HLQ_DEV_TIMEOUT 0x2u   /* a bounded device wait gave up */
+#define HLQ_DEV_BADCODE 0x4u   /* an operand code was outside its range */
+
+/*
+ * Workspace bytes needed by one call of `op` with these sizes (rank is used
+ * by the g_w op only).  The result is a multiple of 256.
+ */
+size_t hlq_workspace_bytes(int op, int64_t T, int64_t Cin, int64_t Cout,
+                           int block, int rank);
+
+/*
+ * ACBP at forward time (HOT, Approach: stored activations compressed when
+ * the forward pass runs; HLQ TL;DR: "activation-compression").
+ * x [T, Cin] (dtype dt) -> d_xbar [Cin, T'] int8 codes (token dim
+ * contiguous) and d_xbar_scale [1] fp32:
+ *   Xbar[c, rank*b + k] = RN_f32( sum_j H16[sigma(k)][j] x[16b + j, c] )
+ *   s = RN_f32(max|Xbar| / 127),  code = clamp(rne(RN_f32(Xbar / s)), +-127)
+ * where sigma(k) is the Sylvester row of sequency k (the rank lowest-
+ * sequency Walsh rows are kept).  s == 0 gives all-zero codes.
+ */
+hlq_status hlq_compress_activation(const void *d_x, int dt, int64_t T,
+                                   int64_t Cin, int block, int rank,
+                                   int8_t *d_xbar, float *d_xbar_scale,
+                                   void *d_ws, size_t ws_bytes, void *stream);
+
+/*
+ * Activation gradient g_x = g_y . w with int4 HQ (HLQ TL;DR; HLQ sections
+ * "Alternative Optimization Technique: Hadamard Quantization" and "HLQ:
+ * Hadamard Low-rank Quantization"):
+ *   Y  = g_y transformed by H16 along Cout in blocks of 16 (Sylvester order),
+ *   Wt = w   transformed by H16 along Cout,
+ *   each rounded once to fp32 from the exact sum;
+ *   s_gy = RN(amax/7) per token (gran_gy) or per tensor; s_w per tensor;
+ *   codes: x = RN(Y/s), stochastic rounding q = floor(x) + [u < x-floor(x)],
+ *   u = (word >> 8) * 2^-24 of Philox4x32-10 with key (seed lo, seed hi) and
+ *   counter (e/4 lo, e/4 hi, stream, 0), word e%4, e = row*cols + col of the
+ *   transformed tensor, stream 0 for g_y and 1 for w; clamp to [-7, 7];
+ *   acc[t, i] = sum_c qY[t, c] qW[i, c]  (exact integer);
+ *   g_x[t, i] = acc * s_gy[t] * s_w / 16   (fp32).
+ * gran_w must be HLQ_PER_TENSOR.
+ */
+hlq_status hlq_linear_backward_gx(const void *d_gy, const void *d_w, int dt,
+                                  int64_t T, int64_t Cin, int64_t Cout,
+                                  int block, int gran_gy, int gran_w, int rnd,
+                                  uint64_t seed, float *d_gx, void *d_ws,
+                                  size_t ws_bytes, void *stream);
+
+/*
+ * Weight gradient g_w = (1/16) gbar_y^T . xbar with HLA + int8 (HLQ TL;DR,
+ * with B read as the Hadamard block size; HOT, Approach):
+ *   gbar_y = HLA of g_y along tokens as in hlq_compress_activation,
+ *   s_g = RN(amax/127) per tensor, int8 codes by round-to-nearest-even,
+ *   acc[o, i] = sum_t' qG[o, t'] qX[i, t']  (exact integer),
+ *   g_w[o, i] = acc * s_g * s_x / 16   (fp32).
+ * d_xbar / d_xbar_scale come from hlq_compress_activation with the same T,
+ * Cin and rank.  Needs T' * 127^2 < 2^31.
+ */
+hlq_status hlq_linear_backward_gw(const void *d_gy, int dt, const int8_t *d_xbar,
+                                  const float *d_xbar_scale, int64_t T,
+                                  int64_t Cin, int64_t Cout, int block,
+                                  int rank, float *d_gw, void *d_ws,
+                                  size_t ws_bytes, void *stream);
+
+/*
+ * hlq_linear_backward_gx with its intermediates copied out, for bit-exact
+ * checks (same formulas):
+ *   d_qgy [T, Cout]  int8 codes of Y,   d_sgy [T] or [1] fp32,
+ *   d_qw  [Cin, Cout] int8 codes of Wt (transposed: contraction dim
+ *   contiguous),  d_sw [1],  d_acc [T, Cin] int32 accumulators.
+ * Any of the five may be NULL.  Workspace as for HLQ_OP_BACKWARD_GX.
+ */
+hlq_status hlq_debug_gx_parts(const void *d_gy, const void *d_w, int dt,
+                              int64_t T, int64_t Cin, int64_t Cout, int block,
+                              int gran_gy, int gran_w, int rnd, uint64_t seed,
+                              float *d_gx, void *d_ws, size_t ws_bytes,
+                              int8_t *d_qgy, float *d_sgy, int8_t *d_qw,
+                              float *d_sw, int32_t *d_acc, void *stream);
+
+/*
+ * hlq_linear_backward_gw with its intermediates copied out:
+ *   d_qg [Cout, T'] int8 codes of gbar_y, d_sg [1], d_acc [Cout, Cin] int32.
+ * Any of the three may be NULL.  Workspace as for HLQ_OP_BACKWARD_GW.
+ */
+hlq_status hlq_debug_gw_parts(const void *d_gy, int dt, const int8_t *d_xbar,
+                              const float *d_xbar_scale, int64_t T, int64_t Cin,
+                              int64_t Cout, int block, int rank, float *d_gw,
+                              void *d_ws, size_t ws_bytes, int8_t *d_qg,
+                              float *d_sg, int32_t *d_acc, void *stream);
+
+/*
+ * The exactly rounded Hadamard coefficients alone, for bit-exact checks of
+ * the transform ("HLQ ...", section "Hadamard Transform"):
+ *   axis 0: src [rows, cols], Y[r, 16b+i] = RN_f32(sum_j H16[i][j] src[r, 16b+j])
+ *   axis 1: src [rows, cols], Y[16b+i, c] = RN_f32(sum_j H16[i][j] src[16b+j, c])
+ * d_y [rows, cols] fp32.  rows, cols multiples of 16; axis 1 needs
+ * rows <= 16 * 65535.
+ */
+hlq_status hlq_debug_hq_transform(const void *d_src, int dt, int64_t rows,
+                                  int64_t cols, int axis, float *d_y,
+                                  void *stream);
+
+/*
+ * The HLA coefficients alone: src [T, C] -> d_out [C, T'] fp32,
+ *   out[c, rank*b + k] = RN_f32(sum_j H16[sigma(k)][j] src[16b + j, c]).
+ * T <= 16 * 65535.
+ */
+hlq_status hlq_debug_hla_transform(const void *d_src, int dt, int64_t T,
+                                   int64_t C, int rank, float *d_out,
+                                   void *stream);
+
+/*
+ * Read (and, if `clear` is non-zero, reset) the device status flags of the
+ * current device.  Synchronises `stream` first.  *flags is a host pointer.
+ */
+hlq_status hlq_read_device_status(uint32_t *flags, int clear, void *stream);
+
+/* Static text for a status code. */
+const char *hlq_status_string(int status);
+
+/* Library version, e.g. 0x000100 for 0.1.0. */
+int hlq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HLQ_H */

@@ -67,6 +67,10 @@ def _load():
                 "orc_philox4x32_10": (None, [P, P, P]),
                 "orc_philox_word": (u32, [u64, u32, u64]),
                 "orc_hq_quantize": (i32, [P, i64, i64, i32, i32, u64, u32, P, P]),
+                "orc_hq_quantize_rows": (i32, [P, i64, i64, P, i32,
+                                               ctypes.c_float, i32, u64, u32,
+                                               P, P]),
+                "orc_amax": (ctypes.c_float, [P, i64]),
                 "orc_int8_quantize": (i32, [P, i64, P, P]),
                 "orc_pack_int4": (i32, [P, i64, P]),
                 "orc_gemm_i64": (None, [P, P, i64, i64, i64, P]),
@@ -177,6 +181,29 @@ def hq_quantize(Y, gran: int, rnd: int, seed: int, stream: int):
     _check(_load().orc_hq_quantize(_p(Y), rows, cols, gran, rnd, seed, stream,
                                    _p(codes), _p(scales)), "hq_quantize")
     return codes, scales
+
+
+def hq_quantize_rows(Yrows, row_ids, gran: int, rnd: int, seed: int,
+                     stream: int, tensor_amax=0.0):
+    """Quantize some rows of a larger transformed tensor (row numbers
+    ``row_ids`` in the full tensor; ``tensor_amax`` = its max |Y| for the
+    per-tensor scale)."""
+    Yrows = _f32(Yrows)
+    ids = np.ascontiguousarray(row_ids, dtype=np.int64)
+    n, cols = Yrows.shape
+    assert ids.shape == (n,)
+    codes = np.empty((n, cols), dtype=np.int8)
+    scales = np.empty(n if gran == PER_TOKEN else 1, dtype=np.float32)
+    _check(_load().orc_hq_quantize_rows(_p(Yrows), n, cols, _p(ids), gran,
+                                        float(tensor_amax), rnd, seed, stream,
+                                        _p(codes), _p(scales)),
+           "hq_quantize_rows")
+    return codes, scales
+
+
+def amax(v) -> np.float32:
+    v = _f32(v)
+    return np.float32(_load().orc_amax(_p(v), v.size))
 
 
 def int8_quantize(v):

@@ -432,7 +432,7 @@ static int quant_one(float y, float s, int qmax, int rnd, uint32_t word)
         r = rintf(x); /* default rounding mode: nearest, ties to even */
     } else {
         float f = floorf(x);
-        float frac = x - f; /* exact */
+        float frac = x - f; /* fp32 difference (exact unless -2^-24 < x < 0) */
         float u = (float)(word >> 8) * 0x1p-24f;
         r = f + ((u < frac) ? 1.0f : 0.0f);
     }
@@ -449,20 +449,21 @@ static int quant_one(float y, float s, int qmax, int rnd, uint32_t word)
  * gran 0 = one scale for the tensor).  s = RN_f32(amax / 7).  Element
  * (r, c) draws Philox word e = r*cols + c of `stream`.
  * codes [rows, cols] int8 in [-7, 7]; scales [rows] or [1].
+ *
+ * orc_hq_quantize_rows quantizes a subset of the rows of a larger tensor:
+ * Y holds `nrows` rows whose row numbers in the full tensor are row_ids[],
+ * and, for gran 0, tensor_amax is the max |Y| over the full tensor.
  */
-int orc_hq_quantize(const float *Y, int64_t rows, int64_t cols, int gran,
-                    int rnd, uint64_t seed, uint32_t stream, int8_t *codes,
-                    float *scales)
+int orc_hq_quantize_rows(const float *Y, int64_t nrows, int64_t cols,
+                         const int64_t *row_ids, int gran, float tensor_amax,
+                         int rnd, uint64_t seed, uint32_t stream,
+                         int8_t *codes, float *scales)
 {
     const int qmax = 7;
-    float tensor_amax = 0.0f;
-    for (int64_t i = 0; i < rows * cols; ++i) {
+    for (int64_t i = 0; i < nrows * cols; ++i)
         if (!is_finite_f32(Y[i]))
             return ORC_ERR_NONFINITE;
-        if (fabsf(Y[i]) > tensor_amax)
-            tensor_amax = fabsf(Y[i]);
-    }
-    for (int64_t r = 0; r < rows; ++r) {
+    for (int64_t r = 0; r < nrows; ++r) {
         float amax = tensor_amax;
         if (gran == 1) {
             amax = 0.0f;
@@ -475,14 +476,40 @@ int orc_hq_quantize(const float *Y, int64_t rows, int64_t cols, int gran,
             scales[r] = s;
         else if (r == 0)
             scales[0] = s;
+        int64_t row = row_ids ? row_ids[r] : r;
         for (int64_t c = 0; c < cols; ++c) {
-            uint64_t e = (uint64_t)(r * cols + c);
+            uint64_t e = (uint64_t)(row * cols + c);
             uint32_t word = (rnd == ORC_SR) ? orc_philox_word(seed, stream, e) : 0;
             codes[r * cols + c] =
                 (int8_t)quant_one(Y[r * cols + c], s, qmax, rnd, word);
         }
     }
     return ORC_OK;
+}
+
+int orc_hq_quantize(const float *Y, int64_t rows, int64_t cols, int gran,
+                    int rnd, uint64_t seed, uint32_t stream, int8_t *codes,
+                    float *scales)
+{
+    float tensor_amax = 0.0f;
+    for (int64_t i = 0; i < rows * cols; ++i) {
+        if (!is_finite_f32(Y[i]))
+            return ORC_ERR_NONFINITE;
+        if (fabsf(Y[i]) > tensor_amax)
+            tensor_amax = fabsf(Y[i]);
+    }
+    return orc_hq_quantize_rows(Y, rows, cols, NULL, gran, tensor_amax, rnd,
+                                seed, stream, codes, scales);
+}
+
+/* Largest |v| of an fp32 array. */
+float orc_amax(const float *v, int64_t n)
+{
+    float amax = 0.0f;
+    for (int64_t i = 0; i < n; ++i)
+        if (fabsf(v[i]) > amax)
+            amax = fabsf(v[i]);
+    return amax;
 }
 
 /* int8 quantizer with one scale per tensor, s = RN_f32(amax / 127),

@@ -1,0 +1,128 @@
+"""The C ABI library loads, exports every declared symbol, and rejects bad
+arguments on the host before touching the GPU (no device needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import hadamard_precision_backprop_gb300 as hlq
+from hadamard_precision_backprop_gb300 import build as hbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    hbuild.build()
+    return hlq.lib()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "hlq.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(hlq_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = declared_functions()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(names) == set(hlq.EXPORTS)
+
+
+def test_status_strings_and_version(L):
+    assert hlq.status_string(0) == "HLQ_OK"
+    assert hlq.status_string(5) == "HLQ_ERR_WORKSPACE"
+    assert hlq.status_string(99) == "HLQ_UNKNOWN_STATUS"
+    assert L.hlq_version() == 0x000100
+
+
+def test_workspace_sizes(L):
+    for op in (0, 1, 2):
+        n = hlq.hlq_workspace_bytes(op, 12608, 768, 2304, 16, 8)
+        assert n > 0 and n % 256 == 0
+    # g_x workspace holds one byte per int4 code of g_y and of w
+    n = hlq.hlq_workspace_bytes(1, 256, 64, 128)
+    assert n >= 256 * 128 + 64 * 128
+    assert hlq.hlq_workspace_bytes(7, 16, 16, 16) == 0
+    assert hlq.hlq_workspace_bytes(1, -16, 16, 16) == 0
+
+
+# A 16-byte aligned non-null address.  Every call below has one invalid
+# argument, so validation rejects it before any CUDA call: nothing is ever
+# launched on these fake pointers.
+FAKE = 1 << 20
+FAKE_WS = 1 << 24
+
+
+def gx(L, **kw):
+    a = dict(gy=FAKE, w=FAKE, dt=1, T=256, Cin=64, Cout=128, block=16,
+             gran_gy=1, gran_w=0, rnd=1, seed=0, gx=FAKE, ws=FAKE_WS,
+             ws_bytes=1 << 30, stream=None)
+    a.update(kw)
+    return L.hlq_linear_backward_gx(
+        a["gy"], a["w"], a["dt"], a["T"], a["Cin"], a["Cout"], a["block"],
+        a["gran_gy"], a["gran_w"], a["rnd"], a["seed"], a["gx"], a["ws"],
+        a["ws_bytes"], a["stream"])
+
+
+def gw(L, **kw):
+    a = dict(gy=FAKE, dt=1, xbar=FAKE, xs=FAKE, T=256, Cin=64, Cout=128,
+             block=16, rank=8, gw=FAKE, ws=FAKE_WS, ws_bytes=1 << 30,
+             stream=None)
+    a.update(kw)
+    return L.hlq_linear_backward_gw(
+        a["gy"], a["dt"], a["xbar"], a["xs"], a["T"], a["Cin"], a["Cout"],
+        a["block"], a["rank"], a["gw"], a["ws"], a["ws_bytes"], a["stream"])
+
+
+def test_gx_argument_validation(L):
+    assert gx(L, block=8) == 1
+    assert gx(L, dt=5) == 1
+    assert gx(L, gran_gy=3) == 1
+    assert gx(L, rnd=2) == 1
+    assert gx(L, T=17) == 2
+    assert gx(L, Cin=-16) == 2
+    assert gx(L, Cout=100) == 2
+    assert gx(L, gy=FAKE + 4) == 3
+    assert gx(L, gx=FAKE + 8) == 3
+    assert gx(L, ws=FAKE_WS + 16) == 3
+    assert gx(L, gran_w=1) == 4
+    assert gx(L, ws_bytes=1024) == 5
+    assert gx(L, ws=None) == 5
+    assert gx(L, gy=None) == 1
+    assert gx(L, Cout=342400) == 6            # 49 * Cout >= 2^24
+
+
+def test_gw_argument_validation(L):
+    assert gw(L, rank=3) == 1
+    assert gw(L, rank=32) == 1
+    assert gw(L, block=32) == 1
+    assert gw(L, xs=None) == 1
+    assert gw(L, T=8) == 2
+    assert gw(L, xbar=FAKE + 1) == 3
+    assert gw(L, ws_bytes=0) == 5
+    assert gw(L, T=266304) == 6               # T' * 127^2 >= 2^31
+
+
+def test_compress_argument_validation(L):
+    f = L.hlq_compress_activation
+    assert f(FAKE, 1, 256, 64, 15, 8, FAKE, FAKE, FAKE_WS, 1 << 20, None) == 1
+    assert f(FAKE, 1, 256, 64, 16, 5, FAKE, FAKE, FAKE_WS, 1 << 20, None) == 1
+    assert f(FAKE, 1, 250, 64, 16, 8, FAKE, FAKE, FAKE_WS, 1 << 20, None) == 2
+    assert f(FAKE, 1, 256, 64, 16, 8, FAKE, None, FAKE_WS, 1 << 20, None) == 1
+    assert f(FAKE + 2, 1, 256, 64, 16, 8, FAKE, FAKE, FAKE_WS, 1 << 20, None) == 3
+    assert f(FAKE, 1, 256, 64, 16, 8, FAKE, FAKE, FAKE_WS, 0, None) == 5
+
+
+def test_read_status_rejects_null(L):
+    assert L.hlq_read_device_status(None, 0, None) == 1
+
+
+def test_product_path_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(hlq, "_lib", None)
+    monkeypatch.setattr(hlq, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        hlq.lib()
