@@ -1,0 +1,456 @@
+#!/usr/bin/env python
+"""Benchmark of the HLQ/HOT backward pass of one linear layer on GB300.
+
+One step = the whole hot path on one batch of synthetic input:
+  ACBP compression of x at forward time (hlq_compress_activation), then the
+  backward pass: g_x through int4 Hadamard quantization
+  (hlq_linear_backward_gx) and g_w through the Hadamard low-rank
+  approximation with int8 (hlq_linear_backward_gw).
+Default workload: the ViT-B qkv layer, T = 64 x 197 = 12608 tokens,
+Cin = 768, Cout = 2304, bf16 inputs, per-token g_y quantizer.
+
+Prints one JSON line (rank 0).  `value` is microseconds per layer step
+(lower is better), device-timed with CUDA events on the launching stream,
+inputs resident in HBM, L2 flushed (256 MiB write) before every timed step.
+`e2e` is the same through host buffers (pinned host -> device copies of
+x, g_y, w and device -> host copies of g_x, g_w inside the timed region).
+`roofline` is for the kernel with the largest device time, from per-launch
+CUDA events recorded by libhlq's tracing hooks; `cpu_baseline` times the CPU
+oracle on a bounded token sample on this host.
+
+--impl reference times the CPU oracle itself (the only reference there is)
+per step on a bounded token sample and prints the same metric.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = ("HLQ linear-backward µs/layer & effective TOPS; % of "
+          "int8-tensor / HBM roofline")
+UNIT = "us/layer"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0,
+                  "bf16_tflops_sustained": 1700.0}
+NOMINAL_FP8_OVER_BF16 = 4.5 / 2.25
+
+
+def parse_args():
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default=workloads.WORKLOADS[1].name,
+                   help="workload name or index into workloads.WORKLOADS")
+    p.add_argument("--cpu-sample-tokens", type=int, default=4096)
+    p.add_argument("--ref-sample-tokens", type=int, default=512)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def pick_workload(spec):
+    if spec.isdigit():
+        return workloads.WORKLOADS[int(spec)]
+    return workloads.BY_NAME[spec]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        d["source"] = "measured"
+        return d
+    d = dict(FALLBACK_PEAKS)
+    d["source"] = "fallback"
+    return d
+
+
+# ----------------------------------------------------------------------------
+# algorithmic work per kernel launch
+# ----------------------------------------------------------------------------
+
+def algorithmic(name, wl, e):
+    """(bound, amount) of one launch: bytes for HBM-bound kernels, ops for
+    the GEMMs.  Reads count the input once, writes count the codes/scales.
+    The per-tensor amax pre-passes re-read the input; they are credited with
+    that read."""
+    T, Cin, Cout, Tp = wl.T, wl.Cin, wl.Cout, wl.Tp
+    per_tok = wl.gran_gy == workloads.PER_TOKEN
+    table = {
+        "hla_x_amax": ("hbm", T * Cin * e),
+        "hla_x_quant": ("hbm", T * Cin * e + Cin * Tp),
+        "hq_rows_amax": ("hbm", T * Cout * e),
+        "hq_rows_quant": ("hbm", T * Cout * e + T * Cout + (4 * T if per_tok else 4)),
+        "hq_cols_amax": ("hbm", Cout * Cin * e),
+        "hq_cols_quant": ("hbm", Cout * Cin * e + Cin * Cout),
+        "hla_gy_amax": ("hbm", T * Cout * e),
+        "hla_gy_quant": ("hbm", T * Cout * e + Cout * Tp * 2),
+        "widen_xbar": ("hbm", Cin * Tp * 3),
+        "gemm_gx": ("ops", 2 * T * Cin * Cout),
+        "gemm_gw": ("ops", 2 * Cout * Cin * Tp),
+    }
+    return table.get(name.replace("_simple", "").replace("_tc", ""), ("hbm", 0))
+
+
+def kernel_peak(name, peaks, sustained):
+    """(bound label, peak, unit) for a kernel; GEMM peaks per operand type."""
+    bf16 = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
+    if name.endswith("_simple"):
+        # CUDA-core dp4a GEMM: 152 SMs x 64 dp4a/clk (assumed half rate)
+        # x 8 int ops x 2.07 GHz
+        return "alu", 152 * 64 * 8 * 2.07e9 / 1e12, "TOPS"
+    if name.startswith("gemm_gx"):       # E4M3 operands on the FP8 tensor pipe
+        return "tensor", bf16 * NOMINAL_FP8_OVER_BF16, "TFLOP/s"
+    if name.startswith("gemm_gw"):       # bf16 operands
+        return "tensor", bf16, "TFLOP/s"
+    return "hbm", peaks["hbm_gbs"], "GB/s"
+
+
+# ----------------------------------------------------------------------------
+# clocks
+# ----------------------------------------------------------------------------
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,"
+             "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="hlq_clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.dev}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle timing (test infrastructure: only this leg runs it)
+# ----------------------------------------------------------------------------
+
+def oracle_layer_seconds(wl, inp, tokens):
+    """Oracle time of one layer step on the first `tokens` tokens, plus the
+    token-independent part (the HQ of w), in seconds."""
+    import oracle
+    oracle.build()
+    Ts = tokens
+    gy = inp["g_y"][:Ts]
+    x = inp["x"][:Ts]
+    t0 = time.perf_counter()
+    Wt = oracle.hq_transform(inp["w"], 1)
+    qWt, s_w = oracle.hq_quantize(Wt, oracle.PER_TENSOR, oracle.SR, wl.seed,
+                                  oracle.STREAM_W)
+    qW = np.ascontiguousarray(qWt.T)
+    t_w = time.perf_counter() - t0
+    t1 = time.perf_counter()
+    qx, s_x = oracle.compress_activation(x, wl.rank)
+    Y = oracle.hq_transform(gy, 0)
+    qY, s_gy = oracle.hq_quantize(Y, wl.gran_gy, oracle.SR, wl.seed,
+                                  oracle.STREAM_GY)
+    acc = oracle.gemm_i64(qY, qW)
+    oracle.dequant_gx(acc, s_gy, wl.gran_gy, s_w[0])
+    oracle.gw_path(gy, qx, s_x, wl.rank)
+    t_tok = time.perf_counter() - t1
+    return t_w, t_tok
+
+
+def cpu_baseline(wl, inp, tokens):
+    t_w, t_tok = oracle_layer_seconds(wl, inp, tokens)
+    est = t_w + t_tok * (wl.T / tokens)
+    return {"value": est * 1e6, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": (f"oracle on the first {tokens} of {wl.T} tokens "
+                       f"({t_tok:.2f} s) scaled by T/{tokens}, plus the full "
+                       f"HQ of w ({t_w:.2f} s); single thread"),
+            "measured_s": t_w + t_tok}
+
+
+# ----------------------------------------------------------------------------
+# arms
+# ----------------------------------------------------------------------------
+
+def run_reference(args, wl, rank, world):
+    if rank != 0:
+        return 0
+    inp = workloads.make_inputs(wl, T=max(args.ref_sample_tokens, 16))
+    per_step = []
+    for i in range(args.warmup + args.steps):
+        t_w, t_tok = oracle_layer_seconds(wl, inp, args.ref_sample_tokens)
+        if i >= args.warmup:
+            per_step.append(t_w + t_tok * (wl.T / args.ref_sample_tokens))
+    us = statistics.mean(per_step) * 1e6
+    sample = (f"oracle on the first {args.ref_sample_tokens} of {wl.T} tokens "
+              f"per step, token part scaled by T/{args.ref_sample_tokens}, "
+              "plus the full HQ of w; single thread")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": us, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": us / 1e3, "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int64", "data": "synthetic",
+        "config": config_of(wl),
+        "cpu_baseline": {"value": us, "unit": UNIT, "cores": 1,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": us, "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_of(wl):
+    return {"workload": wl.name, "T": wl.T, "Cin": wl.Cin, "Cout": wl.Cout,
+            "input_dtype": wl.dtype, "block": wl.block, "rank": wl.rank,
+            "gran_gy": "per-token" if wl.gran_gy else "per-tensor",
+            "l2": "flushed before every timed step (256 MiB write)"}
+
+
+def run_ours(args, wl, rank, world, local_rank):
+    import torch
+    import hadamard_precision_backprop_gb300 as hlq
+    from hadamard_precision_backprop_gb300 import build as hbuild
+
+    hbuild.build()
+    hlq.lib()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    inp = workloads.make_inputs(wl)
+    e = 2 if wl.dtype == "bf16" else 4
+
+    def host_tensor(name):
+        if wl.dtype == "bf16":
+            t = torch.from_numpy(inp[name + "_bits"].view(np.int16)).view(torch.bfloat16)
+        else:
+            t = torch.from_numpy(inp[name])
+        return t.pin_memory()
+
+    h_x, h_gy, h_w = host_tensor("x"), host_tensor("g_y"), host_tensor("w")
+    x, gy, w = (t.to(dev) for t in (h_x, h_gy, h_w))
+    T, Cin, Cout, Tp = wl.T, wl.Cin, wl.Cout, wl.Tp
+    ws0 = hlq.workspace(hlq.OP_COMPRESS_ACTIVATION, T, Cin, Cout, 16, wl.rank, dev)
+    ws1 = hlq.workspace(hlq.OP_BACKWARD_GX, T, Cin, Cout, 16, wl.rank, dev)
+    ws2 = hlq.workspace(hlq.OP_BACKWARD_GW, T, Cin, Cout, 16, wl.rank, dev)
+    xbar = torch.empty((Cin, Tp), dtype=torch.int8, device=dev)
+    sx = torch.empty(1, dtype=torch.float32, device=dev)
+    gx = torch.empty((T, Cin), dtype=torch.float32, device=dev)
+    gw = torch.empty((Cout, Cin), dtype=torch.float32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(xx, gg, ww):
+        hlq.hlq_compress_activation(xx, rank=wl.rank, out=xbar, scale=sx, ws=ws0)
+        hlq.hlq_linear_backward_gx(gg, ww, gran_gy=wl.gran_gy, gran_w=wl.gran_w,
+                                   rnd=hlq.SR, seed=wl.seed, out=gx, ws=ws1)
+        hlq.hlq_linear_backward_gw(gg, xbar, sx, rank=wl.rank, out=gw, ws=ws2)
+
+    # ---- device-resident timing ------------------------------------------
+    for _ in range(args.warmup):
+        step(x, gy, w)
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    hlq.hlq_trace_begin(64 * args.steps + 64)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    for a, b in evs:
+        flush.fill_(1)
+        a.record(stream)
+        step(x, gy, w)
+        b.record(stream)
+    torch.cuda.synchronize()
+    launches = hlq.hlq_trace_end()
+    barrier()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    step_ms = [a.elapsed_time(b) for a, b in evs]
+    ms = statistics.mean(step_ms)
+    if dist is not None:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # ---- end to end through host buffers ---------------------------------
+    h_gx = torch.empty((T, Cin), dtype=torch.float32).pin_memory()
+    h_gw = torch.empty((Cout, Cin), dtype=torch.float32).pin_memory()
+    d_x, d_gy, d_w = torch.empty_like(x), torch.empty_like(gy), torch.empty_like(w)
+
+    def e2e_step():
+        d_x.copy_(h_x, non_blocking=True)
+        d_gy.copy_(h_gy, non_blocking=True)
+        d_w.copy_(h_w, non_blocking=True)
+        step(d_x, d_gy, d_w)
+        h_gx.copy_(gx, non_blocking=True)
+        h_gw.copy_(gw, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    e2e_ms = []
+    for _ in range(args.steps):
+        flush.fill_(1)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        e2e_step()
+        b.record(stream)
+        b.synchronize()
+        e2e_ms.append(a.elapsed_time(b))
+    e2e = statistics.mean(e2e_ms)
+    if dist is not None:
+        t = torch.tensor([e2e], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e = float(t.item())
+    barrier()
+
+    if rank != 0:
+        return 0
+
+    # ---- per-kernel attribution and roofline -----------------------------
+    peaks = load_peaks()
+    per_kernel = {}
+    for name, kms in launches:
+        d = per_kernel.setdefault(name, [0, 0.0])
+        d[0] += 1
+        d[1] += kms
+    kernels = {}
+    for name, (n, tot) in sorted(per_kernel.items(), key=lambda kv: -kv[1][1]):
+        bound, amount = algorithmic(name, wl, e)
+        avg_s = tot / n / 1e3
+        kind, peak, unit = kernel_peak(name, peaks, sustained=False)
+        achieved = amount / avg_s / (1e9 if unit == "GB/s" else 1e12)
+        kernels[name] = {"launches": n, "avg_us": avg_s * 1e6,
+                         "share": tot / sum(v[1] for v in per_kernel.values()),
+                         "achieved": achieved, "unit": unit,
+                         "frac": achieved / peak}
+    top = next(iter(kernels))
+    kind, peak, unit = kernel_peak(top, peaks, sustained=False)
+    traffic = load_traffic(top, wl)
+    roofline = {"bound": kind, "kernel": top,
+                "achieved": kernels[top]["achieved"], "peak": peak,
+                "unit": unit, "frac": kernels[top]["achieved"] / peak,
+                "traffic": traffic, "peak_source": peaks["source"]}
+
+    us = ms * 1e3 / world                 # job-wide us per layer step
+    bwd_ms = sum(v[1] for k, v in per_kernel.items()
+                 if not k.startswith("hla_x")) / args.steps
+    line = {
+        "metric": METRIC, "value": us, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+        "dtype": "int4/int8", "data": "synthetic",
+        "config": config_of(wl),
+        "backward_us": bwd_ms * 1e3,
+        "forward_acbp_us": sum(v[1] for k, v in per_kernel.items()
+                               if k.startswith("hla_x")) / args.steps * 1e3,
+        "effective_tops": 4 * T * Cin * Cout / (bwd_ms / 1e3) / 1e12,
+        "roofline": roofline,
+        "kernels": kernels,
+        "gpu_launches": len(launches),
+        "clocks": clk,
+        "e2e": {"value": e2e * 1e3 / world, "unit": UNIT,
+                "h2d_bytes_per_step": (x.numel() + gy.numel() + w.numel()) * e,
+                "d2h_bytes_per_step": (gx.numel() + gw.numel()) * 4},
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, inp, min(args.cpu_sample_tokens, wl.T))
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def load_traffic(kernel, wl):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary of the
+    current kernels, or None when no capture of this kernel exists."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    v = d.get(wl.name, {}).get(kernel)
+    return None if v is None else v.get("dram_bytes_per_launch")
+
+
+def main():
+    args = parse_args()
+    wl = pick_workload(args.workload)
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, wl, rank, world)
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        return run_ours(args, wl, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -34,6 +34,8 @@ EXPORTS = [
     "hlq_linear_backward_gw", "hlq_debug_gx_parts", "hlq_debug_gw_parts",
     "hlq_read_device_status", "hlq_status_string", "hlq_version",
     "hlq_debug_hq_transform", "hlq_debug_hla_transform",
+    "hlq_trace_begin", "hlq_trace_end", "hlq_trace_get", "hlq_trace_free",
+    "hlq_debug_reference_gemm",
 ]
 
 _lock = threading.Lock()
@@ -81,6 +83,11 @@ def lib() -> ctypes.CDLL:
             "hlq_read_device_status": (i32, [P, i32, P]),
             "hlq_debug_hq_transform": (i32, [P, i32, i64, i64, i32, P, P]),
             "hlq_debug_hla_transform": (i32, [P, i32, i64, i64, i32, P, P]),
+            "hlq_trace_begin": (i32, [i32]),
+            "hlq_debug_reference_gemm": (i32, [i32, P, P, i64, i64, i64, P, P]),
+            "hlq_trace_end": (i32, [P]),
+            "hlq_trace_get": (i32, [i32, P, P]),
+            "hlq_trace_free": (i32, []),
             "hlq_status_string": (ctypes.c_char_p, [i32]),
             "hlq_version": (i32, []),
         }
@@ -280,6 +287,40 @@ def hlq_debug_hla_transform(src, rank: int = 8, stream=None):
     _check(lib().hlq_debug_hla_transform(_ptr(src), _dtype_code(src), T, C,
                                          rank, _ptr(out), _stream(stream)),
            "hlq_debug_hla_transform")
+    return out
+
+
+def hlq_debug_reference_gemm(a, b, stream=None):
+    """int32 a @ b^T of int8 code matrices a [M, K], b [N, K] on CUDA cores."""
+    torch = _torch()
+    _need_cuda_contig(a, b)
+    M, K = a.shape
+    N = b.shape[0]
+    acc = torch.empty((M, N), dtype=torch.int32, device=a.device)
+    _check(lib().hlq_debug_reference_gemm(0, _ptr(a), _ptr(b), M, N, K,
+                                          _ptr(acc), _stream(stream)),
+           "hlq_debug_reference_gemm")
+    return acc
+
+
+def hlq_trace_begin(capacity: int = 4096):
+    """Start recording per-launch device times of libhlq's kernels."""
+    _check(lib().hlq_trace_begin(capacity), "hlq_trace_begin")
+
+
+def hlq_trace_end():
+    """Stop tracing; return [(kernel name, ms), ...] in launch order."""
+    L = lib()
+    n = ctypes.c_int(0)
+    _check(L.hlq_trace_end(ctypes.byref(n)), "hlq_trace_end")
+    out = []
+    for i in range(n.value):
+        name = ctypes.c_char_p()
+        ms = ctypes.c_float()
+        _check(L.hlq_trace_get(i, ctypes.byref(name), ctypes.byref(ms)),
+               "hlq_trace_get")
+        out.append((name.value.decode(), float(ms.value)))
+    L.hlq_trace_free()
     return out
 
 

@@ -31,6 +31,40 @@ unsigned int* device_status_ptr() {
   return g_status_ptr[dev];
 }
 
+// ---------------------------------------------------------------------------
+// Launch tracing (hlq_trace_*): while enabled, every kernel launch of this
+// library is bracketed by two events recorded on its stream, so per-kernel
+// device time can be read back without a profiler.
+// ---------------------------------------------------------------------------
+struct Trace {
+  bool on = false;
+  int cap = 0, n = 0;
+  cudaEvent_t* ev = nullptr;  // 2 * cap events
+  const char** name = nullptr;
+};
+Trace g_trace;
+
+void trace_free() {
+  if (g_trace.ev) {
+    for (int i = 0; i < 2 * g_trace.cap; ++i) cudaEventDestroy(g_trace.ev[i]);
+    delete[] g_trace.ev;
+    delete[] g_trace.name;
+  }
+  g_trace = Trace{};
+}
+
+inline void trace_before(cudaStream_t s) {
+  if (g_trace.on && g_trace.n < g_trace.cap)
+    cudaEventRecord(g_trace.ev[2 * g_trace.n], s);
+}
+inline void trace_after(const char* what, cudaStream_t s) {
+  if (g_trace.on && g_trace.n < g_trace.cap) {
+    cudaEventRecord(g_trace.ev[2 * g_trace.n + 1], s);
+    g_trace.name[g_trace.n] = what;
+    ++g_trace.n;
+  }
+}
+
 constexpr size_t kAlign = 256;
 inline size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
@@ -42,7 +76,8 @@ struct GxLayout {
   size_t amax, sgy, sw, qy, qw, total;
 };
 struct GwLayout {
-  size_t amax, sg, qg, xw, total;
+  size_t amax, sg, qg, xw, split, total;
+  int64_t ld;  // row stride (codes) of the bf16 operand buffers
 };
 
 GxLayout gx_layout(int64_t T, int64_t Cin, int64_t Cout) {
@@ -60,13 +95,28 @@ GxLayout gx_layout(int64_t T, int64_t Cin, int64_t Cout) {
 GwLayout gw_layout(int64_t T, int64_t Cin, int64_t Cout, int rank) {
   GwLayout L{};
   const int64_t Tp = T / 16 * rank;
+  L.ld = (Tp + 7) / 8 * 8;  // 16-byte rows for the TMA
   size_t o = 0;
-  L.amax = o; o += kAlign;
-  L.sg = o;   o += kAlign;
-  L.qg = o;   o += align_up((size_t)Cout * (size_t)Tp * 2);  // bf16 [Cout, T']
-  L.xw = o;   o += align_up((size_t)Cin * (size_t)Tp * 2);   // bf16 [Cin, T']
+  L.amax = o;  o += kAlign;
+  L.sg = o;    o += kAlign;
+  L.qg = o;    o += align_up((size_t)Cout * (size_t)L.ld * 2);  // bf16 [Cout, ld]
+  L.xw = o;    o += align_up((size_t)Cin * (size_t)L.ld * 2);   // bf16 [Cin, ld]
+  L.split = o; o += align_up(gemm_tc_split_ws_bytes(Cout, Cin)); // int32 split-K
   L.total = o;
   return L;
+}
+
+int device_sm_count() {
+  static int count[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  if (!count[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return 0;
+    count[dev] = n;
+  }
+  return count[dev];
 }
 
 size_t compress_ws(int64_t, int64_t) { return kAlign; }
@@ -94,6 +144,15 @@ hlq_status cuda_status(cudaError_t e) { return e == cudaSuccess ? HLQ_OK : HLQ_E
   do {                                                 \
     cudaError_t _e = (expr);                           \
     if (_e != cudaSuccess) return HLQ_ERR_CUDA;        \
+  } while (0)
+
+// A kernel launch: traced when tracing is on.
+#define HLQ_LAUNCH(name, s, expr)                      \
+  do {                                                 \
+    trace_before(s);                                   \
+    cudaError_t _e = (expr);                           \
+    if (_e != cudaSuccess) return HLQ_ERR_CUDA;        \
+    trace_after(name, s);                              \
   } while (0)
 
 hlq_status gx_impl(const void* gy, const void* w, int dt, int64_t T,
@@ -138,16 +197,24 @@ hlq_status gx_impl(const void* gy, const void* w, int dt, int64_t T,
 
   HLQ_TRY(cudaMemsetAsync(amax, 0, 8, s));
   if (!per_token)
-    HLQ_TRY(launch_hq_rows(gy, bf16, T, Cout, false, true, amax, nullptr,
-                           nullptr, rnd, seed, 0, status, s));
-  HLQ_TRY(launch_hq_rows(gy, bf16, T, Cout, per_token, false, amax, qy, sgy,
-                         rnd, seed, 0, status, s));
-  HLQ_TRY(launch_hq_cols(w, bf16, Cout, Cin, true, amax + 1, nullptr, nullptr,
-                         rnd, seed, 1, status, s));
-  HLQ_TRY(launch_hq_cols(w, bf16, Cout, Cin, false, amax + 1, qw, sw, rnd,
-                         seed, 1, status, s));
-  HLQ_TRY(launch_gemm_simple(qy, kFmtE4M3, qw, kFmtE4M3, T, Cin, Cout, sgy,
-                             per_token, sw, gx, dbg_acc, s));
+    HLQ_LAUNCH("hq_rows_amax", s,
+               launch_hq_rows(gy, bf16, T, Cout, false, true, amax, nullptr,
+                              nullptr, rnd, seed, 0, status, s));
+  HLQ_LAUNCH("hq_rows_quant", s,
+             launch_hq_rows(gy, bf16, T, Cout, per_token, false, amax, qy, sgy,
+                            rnd, seed, 0, status, s));
+  HLQ_LAUNCH("hq_cols_amax", s,
+             launch_hq_cols(w, bf16, Cout, Cin, true, amax + 1, nullptr, nullptr,
+                            rnd, seed, 1, status, s));
+  HLQ_LAUNCH("hq_cols_quant", s,
+             launch_hq_cols(w, bf16, Cout, Cin, false, amax + 1, qw, sw, rnd,
+                            seed, 1, status, s));
+  const int sms = device_sm_count();
+  if (sms <= 0) return HLQ_ERR_CUDA;
+  const GemmPlan plan = plan_gemm_tc(0, T, Cin, Cout, sms, 1);
+  HLQ_LAUNCH("gemm_gx_tc", s,
+             launch_gemm_tc(0, qy, Cout, qw, Cout, T, Cin, Cout, plan, sgy,
+                            per_token, sw, gx, dbg_acc, nullptr, status, s));
   if (dbg_qgy) HLQ_TRY(launch_decode_e4m3(qy, dbg_qgy, T * Cout, s));
   if (dbg_qw) HLQ_TRY(launch_decode_e4m3(qw, dbg_qw, Cin * Cout, s));
   if (dbg_sgy)
@@ -192,13 +259,21 @@ hlq_status gw_impl(const void* gy, int dt, const int8_t* xbar,
   const bool bf16 = dt == HLQ_BF16;
 
   HLQ_TRY(cudaMemsetAsync(amax, 0, 4, s));
-  HLQ_TRY(launch_hla(gy, bf16, T, Cout, rank, true, true, amax, nullptr,
-                     nullptr, status, s));
-  HLQ_TRY(launch_hla(gy, bf16, T, Cout, rank, false, true, amax, qg, sg,
-                     status, s));
-  HLQ_TRY(launch_gemm_simple(qg, kFmtBF16, xbar, kFmtI8, Cout, Cin, Tp, sg,
-                             false, xscale, gw, dbg_acc, s));
-  if (dbg_qg) HLQ_TRY(launch_decode_bf16(qg, dbg_qg, Cout * Tp, s));
+  void* xw = base + L.xw;
+  HLQ_LAUNCH("hla_gy_amax", s,
+             launch_hla(gy, bf16, T, Cout, rank, true, true, amax, nullptr, 0,
+                        nullptr, status, s));
+  HLQ_LAUNCH("hla_gy_quant", s,
+             launch_hla(gy, bf16, T, Cout, rank, false, true, amax, qg, L.ld,
+                        sg, status, s));
+  HLQ_LAUNCH("widen_xbar", s, launch_widen_i8_bf16(xbar, xw, Cin, Tp, L.ld, s));
+  const int sms = device_sm_count();
+  if (sms <= 0) return HLQ_ERR_CUDA;
+  const GemmPlan plan = plan_gemm_tc(1, Cout, Cin, Tp, sms, 16);
+  HLQ_LAUNCH("gemm_gw_tc", s,
+             launch_gemm_tc(1, qg, L.ld, xw, L.ld, Cout, Cin, Tp, plan, sg, false,
+                            xscale, gw, dbg_acc, base + L.split, status, s));
+  if (dbg_qg) HLQ_TRY(launch_decode_bf16(qg, dbg_qg, Cout, Tp, L.ld, s));
   if (dbg_sg) HLQ_TRY(cudaMemcpyAsync(dbg_sg, sg, 4, cudaMemcpyDeviceToDevice, s));
   return HLQ_OK;
 }
@@ -249,10 +324,12 @@ hlq_status hlq_compress_activation(const void* d_x, int dt, int64_t T,
   unsigned int* amax = static_cast<unsigned int*>(d_ws);
   const bool bf16 = dt == HLQ_BF16;
   HLQ_TRY(cudaMemsetAsync(amax, 0, 4, s));
-  HLQ_TRY(launch_hla(d_x, bf16, T, Cin, rank, true, false, amax, nullptr,
-                     nullptr, status, s));
-  HLQ_TRY(launch_hla(d_x, bf16, T, Cin, rank, false, false, amax, d_xbar,
-                     d_xbar_scale, status, s));
+  HLQ_LAUNCH("hla_x_amax", s,
+             launch_hla(d_x, bf16, T, Cin, rank, true, false, amax, nullptr, 0,
+                        nullptr, status, s));
+  HLQ_LAUNCH("hla_x_quant", s,
+             launch_hla(d_x, bf16, T, Cin, rank, false, false, amax, d_xbar, Tp,
+                        d_xbar_scale, status, s));
   return HLQ_OK;
 }
 
@@ -332,6 +409,64 @@ hlq_status hlq_debug_hla_transform(const void* d_src, int dt, int64_t T,
   if (!status) return HLQ_ERR_CUDA;
   HLQ_TRY(launch_hla_transform(d_src, dt == HLQ_BF16, T, C, rank, d_out, status,
                                static_cast<cudaStream_t>(stream)));
+  return HLQ_OK;
+}
+
+hlq_status hlq_debug_reference_gemm(int kind, const void* d_a, const void* d_b,
+                                    int64_t M, int64_t N, int64_t K,
+                                    int32_t* d_acc, void* stream) {
+  if (kind != 0 && kind != 1) return HLQ_ERR_INVALID_ARG;
+  if (M < 0 || N < 0 || K < 0) return HLQ_ERR_SHAPE;
+  if (M * N > 0 && (!d_a || !d_b || !d_acc)) return HLQ_ERR_INVALID_ARG;
+  if (!aligned16(d_a) || !aligned16(d_b) || !aligned16(d_acc)) return HLQ_ERR_ALIGN;
+  if (M * N == 0) return HLQ_OK;
+  HLQ_TRY(launch_gemm_simple(d_a, kFmtI8, d_b, kFmtI8, M, N, K, nullptr, false,
+                             nullptr, nullptr, d_acc, static_cast<cudaStream_t>(stream)));
+  return HLQ_OK;
+}
+
+hlq_status hlq_trace_begin(int capacity) {
+  if (capacity <= 0 || capacity > (1 << 20)) return HLQ_ERR_INVALID_ARG;
+  trace_free();
+  g_trace.ev = new cudaEvent_t[2 * (size_t)capacity]();
+  g_trace.name = new const char*[capacity]();
+  for (int i = 0; i < 2 * capacity; ++i) {
+    if (cudaEventCreate(&g_trace.ev[i]) != cudaSuccess) {
+      g_trace.cap = i / 2;  // destroy what was created
+      for (int j = 0; j < i; ++j) cudaEventDestroy(g_trace.ev[j]);
+      delete[] g_trace.ev;
+      delete[] g_trace.name;
+      g_trace = Trace{};
+      return HLQ_ERR_CUDA;
+    }
+  }
+  g_trace.cap = capacity;
+  g_trace.n = 0;
+  g_trace.on = true;
+  return HLQ_OK;
+}
+
+hlq_status hlq_trace_end(int* n_launches) {
+  if (!n_launches) return HLQ_ERR_INVALID_ARG;
+  g_trace.on = false;
+  *n_launches = g_trace.n;
+  for (int i = 0; i < g_trace.n; ++i)
+    if (cudaEventSynchronize(g_trace.ev[2 * i + 1]) != cudaSuccess)
+      return HLQ_ERR_CUDA;
+  return HLQ_OK;
+}
+
+hlq_status hlq_trace_get(int i, const char** name, float* ms) {
+  if (!name || !ms || i < 0 || i >= g_trace.n) return HLQ_ERR_INVALID_ARG;
+  *name = g_trace.name[i];
+  if (cudaEventElapsedTime(ms, g_trace.ev[2 * i], g_trace.ev[2 * i + 1]) !=
+      cudaSuccess)
+    return HLQ_ERR_CUDA;
+  return HLQ_OK;
+}
+
+hlq_status hlq_trace_free(void) {
+  trace_free();
   return HLQ_OK;
 }
 

@@ -74,12 +74,12 @@ __global__ void __launch_bounds__(256) gemm_simple_kernel(
   for (int i = 0; i < 4; ++i) {
     const int64_t m = m0 + ty + 16 * i;
     if (m >= M) continue;
-    const float scale = (per_row_a ? sa[m] : sa[0]) * sb[0];
+    const float scale = out ? (per_row_a ? sa[m] : sa[0]) * sb[0] : 0.0f;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int64_t n = n0 + tx + 16 * j;
       if (n >= N) continue;
-      out[m * N + n] = (float)acc[i][j] * scale * 0.0625f;
+      if (out) out[m * N + n] = (float)acc[i][j] * scale * 0.0625f;
       if (acc_out) acc_out[m * N + n] = acc[i][j];
     }
   }

@@ -1,0 +1,521 @@
+// hlq_gemm_tc.cu -- exact integer GEMMs of the HLQ backward pass on the
+// sm_103a tensor cores (tcgen05 + TMA + TMEM).
+//
+//   acc[m, n] = sum_k A[m, k] * B[n, k]     (A [M, K], B [N, K], K contiguous)
+//   out[m, n] = float(acc) * (sa[m or 0] * sb[0] / 16)
+//
+// sm_103a has no integer MMA kind, so the integer codes ride on float
+// operand types that hold them exactly:
+//   - g_x path: int4 codes in [-7, 7] as E4M3 bytes, tcgen05.mma kind::f8f6f4;
+//   - g_w path: int8 codes in [-127, 127] as bf16, tcgen05.mma kind::f16.
+// Products are integers and the fp32 TMEM accumulator holds every partial
+// sum exactly while it stays below 2^24; the K loop is therefore cut into
+// chunks of at most `chunk_kb` k-blocks whose accumulators are drained into
+// int32 registers (49 * K < 2^24 lets the E4M3 path use one chunk; the bf16
+// path uses chunks of 16 k-blocks = 1024 codes, 1024 * 127^2 < 2^24).
+//
+// CTA layout (one 128 x BN output tile; optional split of the K range over
+// gridDim.z, reduced exactly in int32 through a workspace):
+//   warp 0      TMA producer (one lane): A and B k-blocks of 128 bytes per
+//               row into a kStages ring of 128B-swizzled smem tiles;
+//   warp 1      TMEM allocator and MMA issuer (one lane), 4 MMAs per k-block
+//               into one of two TMEM accumulators (double buffer per chunk);
+//   warps 2..   epilogue: drain TMEM (tcgen05.ld) into int32 registers per
+//               chunk, then dequantize and store fp32 rows.
+// Every mbarrier wait is bounded (HLQ_DEV_TIMEOUT, then the CTA winds down).
+#include <cstdint>
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "hlq_device.cuh"
+#include "hlq_kernels.h"
+
+namespace hlq {
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kRowBytes = 128;  // bytes of one k-block per row (swizzle span)
+constexpr int kStages = 4;
+constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s per wait
+
+__device__ __forceinline__ uint32_t saddr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long now_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(saddr(b)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(saddr(b)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(saddr(b)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_test(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(saddr(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for the phase of parity `parity` to complete; gives up after kWaitNs
+// (or as soon as another role gave up), raising HLQ_DEV_TIMEOUT once.
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity,
+                                          volatile int* abort_flag,
+                                          unsigned int* status) {
+  if (mbar_test(b, parity)) return true;
+  const unsigned long long t0 = now_ns();
+  while (true) {
+    if (mbar_test(b, parity)) return true;
+    if (*abort_flag) return false;
+    if (now_ns() - t0 > kWaitNs) {
+      if (atomicExch((int*)abort_flag, 1) == 0) atomicOr(status, HLQ_DEV_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map,
+                                            uint64_t* bar, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(saddr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(saddr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major tile stored with the 128-byte
+// swizzle (rows of 128 bytes, 8-row groups 1024 bytes apart).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t addr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr & 0x3FFFFu) >> 4);  // start address
+  d |= (uint64_t)1 << 16;                  // leading byte offset (unused here)
+  d |= (uint64_t)(1024 >> 4) << 32;        // stride byte offset: 8 rows
+  d |= (uint64_t)1 << 46;                  // descriptor version
+  d |= (uint64_t)2 << 61;                  // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor: fp32 accumulator, A/B K-major, shape M x N.
+// kKind 0: kind::f8f6f4 with E4M3 operands; kKind 1: kind::f16 with bf16.
+__host__ __device__ constexpr uint32_t make_idesc(int kKind, int M, int N) {
+  return (1u << 4) | ((kKind == 1 ? 1u : 0u) << 7) | ((kKind == 1 ? 1u : 0u) << 10) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+template <int kKind>
+__device__ __forceinline__ void mma_issue(uint32_t d_tmem, uint64_t a, uint64_t b,
+                                          uint32_t idesc, uint32_t accumulate) {
+  if (kKind == 0) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+  }
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          saddr(bar))
+      : "memory");
+}
+
+// 32 TMEM lanes x 32 consecutive 32-bit columns; thread i gets lane i.
+__device__ __forceinline__ void tmem_ld_x32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, "
+      "[%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+        "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
+        "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]),
+        "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+        "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+template <int BN>
+struct TcCfg {
+  static constexpr int kEpiWarps = BN / 32;               // 4 or 8
+  static constexpr int kColsPerThread = BN / (kEpiWarps / 4);  // 128
+  static constexpr int kThreads = 64 + 32 * kEpiWarps;
+  static constexpr uint32_t kABytes = kBM * kRowBytes;
+  static constexpr uint32_t kBBytes = BN * kRowBytes;
+  static constexpr uint32_t kStageBytes = kABytes + kBBytes;
+  static constexpr uint32_t kTmemCols = 2 * BN;           // two accumulators
+  static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + 256;
+};
+
+template <int kKind, int BN>
+__global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(
+    const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+    int M, int N, int num_kb, int chunk_kb, int kb_per_split,
+    const float* __restrict__ sa, int per_row_a, const float* __restrict__ sb,
+    float* __restrict__ out, int32_t* __restrict__ acc_out,
+    int32_t* __restrict__ split_acc, unsigned int* __restrict__ tile_count,
+    unsigned int* __restrict__ status) {
+  using C = TcCfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * C::kStageBytes);
+  uint64_t* empty = full + kStages;
+  uint64_t* tfull = empty + kStages;  // [2]
+  uint64_t* tempty = tfull + 2;       // [2]
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(tempty + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  int* last_flag = const_cast<int*>(abort_flag) + 1;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m0 = blockIdx.y * kBM, n0 = blockIdx.x * BN;
+  const int kb_begin = blockIdx.z * kb_per_split;
+  const int kb_end = min(num_kb, kb_begin + kb_per_split);
+  const int my_kb = max(0, kb_end - kb_begin);
+  const int num_chunks = (my_kb + chunk_kb - 1) / chunk_kb;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], C::kEpiWarps);
+    }
+    *abort_flag = 0;
+    *last_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     saddr(tmem_holder)),
+                 "r"(C::kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA))
+                   : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB))
+                   : "memory");
+      const int elems = kRowBytes / (kKind == 1 ? 2 : 1);
+      int issued = 0;
+      for (int i = 0; i < my_kb; ++i) {
+        const int s = i % kStages;
+        const uint32_t ph = (uint32_t)(i / kStages) & 1u;
+        if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, status)) break;
+        mbar_expect_tx(&full[s], C::kStageBytes);
+        uint8_t* a = smem + s * C::kStageBytes;
+        const int kx = (kb_begin + i) * elems;
+        tma_load_2d(a, &tmA, &full[s], kx, m0);
+        tma_load_2d(a + C::kABytes, &tmB, &full[s], kx, n0);
+        ++issued;
+      }
+      if (*abort_flag) {  // let the copies already issued land before exit
+        for (int i = max(0, issued - kStages); i < issued; ++i) {
+          const unsigned long long t0 = now_ns();
+          while (!mbar_test(&full[i % kStages], (uint32_t)(i / kStages) & 1u) &&
+                 now_ns() - t0 < kWaitNs) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = make_idesc(kKind, kBM, BN);
+      int i = 0;
+      bool ok = true;
+      for (int c = 0; c < num_chunks && ok; ++c) {
+        const int buf = c & 1;
+        const uint32_t use = (uint32_t)(c >> 1);
+        if (!mbar_wait(&tempty[buf], (use & 1u) ^ 1u, abort_flag, status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem_base + (uint32_t)(buf * BN);
+        const int i_end = min(my_kb, i + chunk_kb);
+        for (int j = 0; i < i_end; ++i, ++j) {
+          const int s = i % kStages;
+          const uint32_t ph = (uint32_t)(i / kStages) & 1u;
+          if (!mbar_wait(&full[s], ph, abort_flag, status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a = saddr(smem + s * C::kStageBytes);
+          const uint32_t b = a + C::kABytes;
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_issue<kKind>(d, sw128_desc(a + 32 * k), sw128_desc(b + 32 * k), idesc,
+                             (j > 0 || k > 0) ? 1u : 0u);
+          mma_commit(&empty[s]);
+        }
+        if (ok) mma_commit(&tfull[buf]);
+      }
+    }
+  } else {
+    // ---------------- epilogue ----------------
+    const int ew = warp - 2;
+    const int quarter = warp & 3;  // TMEM lanes this warp may access
+    const int colgrp = ew >> 2;
+    const int row = quarter * 32 + lane;
+    int32_t acc[C::kColsPerThread];
+#pragma unroll
+    for (int i = 0; i < C::kColsPerThread; ++i) acc[i] = 0;
+    bool ok = true;
+    for (int c = 0; c < num_chunks; ++c) {
+      const int buf = c & 1;
+      const uint32_t use = (uint32_t)(c >> 1);
+      ok = mbar_wait(&tfull[buf], use & 1u, abort_flag, status);
+      ok = __all_sync(0xffffffffu, ok);  // also reconverges the warp
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) +
+                             (uint32_t)(buf * BN + colgrp * C::kColsPerThread);
+#pragma unroll
+      for (int j = 0; j < C::kColsPerThread / 32; ++j) {
+        uint32_t r[32];
+        tmem_ld_x32(taddr + 32 * j, r);
+#pragma unroll
+        for (int q = 0; q < 32; ++q) acc[32 * j + q] += __float2int_rn(__uint_as_float(r[q]));
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[buf]);
+    }
+    const int m = m0 + row;
+    const int nb = n0 + colgrp * C::kColsPerThread;
+    if (ok && gridDim.z > 1) {
+      // split K: add this CTA's exact partial into the int32 workspace tile
+      if (m < M) {
+#pragma unroll
+        for (int q = 0; q < C::kColsPerThread; ++q)
+          if (nb + q < N) atomicAdd(&split_acc[(size_t)m * N + nb + q], acc[q]);
+      }
+    }
+    if (ok && gridDim.z == 1 && m < M) {
+      const float scale = (per_row_a ? sa[m] : sa[0]) * sb[0] * 0.0625f;
+      float* orow = out + (size_t)m * N;
+#pragma unroll
+      for (int q = 0; q < C::kColsPerThread; q += 4) {
+        const int n = nb + q;
+        if (n + 4 <= N) {
+          *reinterpret_cast<float4*>(orow + n) =
+              make_float4((float)acc[q] * scale, (float)acc[q + 1] * scale,
+                          (float)acc[q + 2] * scale, (float)acc[q + 3] * scale);
+          if (acc_out)
+            *reinterpret_cast<int4*>(acc_out + (size_t)m * N + n) =
+                make_int4(acc[q], acc[q + 1], acc[q + 2], acc[q + 3]);
+        }
+      }
+    }
+  }
+
+  // ---- split K: the last CTA of a tile dequantizes the summed tile ----
+  if (gridDim.z > 1) {
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0 && !*abort_flag) {
+      const unsigned int t = blockIdx.y * gridDim.x + blockIdx.x;
+      const unsigned int prev = atomicAdd(&tile_count[t], 1u);
+      *last_flag = (prev == gridDim.z - 1) ? 1 : 0;
+    }
+    __syncthreads();
+    if (*last_flag) {
+      __threadfence();
+      const int rows = min(kBM, M - m0), cols = min(BN, N - n0);
+      const float scale_t = sb[0] * 0.0625f;
+      for (int idx = threadIdx.x; idx < rows * cols; idx += blockDim.x) {
+        const int r = idx / cols, cc = idx % cols;
+        const int m = m0 + r, n = n0 + cc;
+        const int32_t v = __ldcg(&split_acc[(size_t)m * N + n]);
+        const float scale = (per_row_a ? sa[m] : sa[0]) * scale_t;
+        out[(size_t)m * N + n] = (float)v * scale;
+        if (acc_out) acc_out[(size_t)m * N + n] = v;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag) {  // let in-flight tensor-core work finish before freeing TMEM
+    const unsigned long long t0 = now_ns();
+    while (now_ns() - t0 < 1000000ull) {
+    }
+  }
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(C::kTmemCols)
+                 : "memory");
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+bool get_encode() {
+  if (g_encode) return true;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                       cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !fn)
+    return false;
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  return true;
+}
+
+// 2-D K-major operand [rows, K] with row stride ld (elements), boxes of
+// 128 bytes x box_rows, 128-byte swizzle, zero fill outside the tensor.
+bool make_map(CUtensorMap* map, const void* ptr, bool bf16, int64_t rows, int64_t K,
+              int64_t ld, int box_rows) {
+  const int esz = bf16 ? 2 : 1;
+  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(ld * esz)};
+  cuuint32_t box[2] = {(cuuint32_t)(kRowBytes / esz), (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                        2, const_cast<void*>(ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int kKind, int BN>
+cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, int64_t M, int64_t N,
+                      int num_kb, int chunk_kb, int splits, const float* sa,
+                      bool per_row_a, const float* sb, float* out, int32_t* acc_out,
+                      int32_t* split_acc, unsigned int* tile_count,
+                      unsigned int* status, cudaStream_t st) {
+  using C = TcCfg<BN>;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_set[dev]) {
+    e = cudaFuncSetAttribute(gemm_tc_kernel<kKind, BN>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  const int kb_per_split = (num_kb + splits - 1) / splits;
+  dim3 grid((unsigned)((N + BN - 1) / BN), (unsigned)((M + kBM - 1) / kBM),
+            (unsigned)splits);
+  gemm_tc_kernel<kKind, BN><<<grid, C::kThreads, C::kSmem, st>>>(
+      a, b, (int)M, (int)N, num_kb, chunk_kb, kb_per_split, sa, per_row_a ? 1 : 0, sb,
+      out, acc_out, split_acc, tile_count, status);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t gemm_tc_split_ws_bytes(int64_t M, int64_t N) {
+  const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + 127) / 128);
+  return (size_t)M * (size_t)N * 4 + (size_t)tiles * 4 + 256;
+}
+
+GemmPlan plan_gemm_tc(int kind, int64_t M, int64_t N, int64_t K, int num_sms,
+                      int max_splits) {
+  GemmPlan p{};
+  const int elems = kRowBytes / (kind == 1 ? 2 : 1);
+  p.num_kb = (int)((K + elems - 1) / elems);
+  p.chunk_kb = (kind == 1) ? 16 : p.num_kb;  // bf16: 1024 codes per exact chunk
+  if (p.chunk_kb < 1) p.chunk_kb = 1;
+  // choose the tile width and split count that fill the GPU best
+  double best = 1e30;
+  for (int bn : {128, 256}) {
+    const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + bn - 1) / bn);
+    for (int s = 1; s <= max_splits; ++s) {
+      if (s > 1 && (p.num_kb + s - 1) / s < 4) break;
+      const int64_t ctas = tiles * s;
+      const int64_t waves = (ctas + num_sms - 1) / num_sms;
+      const int kb_split = (p.num_kb + s - 1) / s;
+      // per CTA: k-blocks of MMA work (proportional to bn), plus the
+      // epilogue / reduction overhead of a split
+      const double cost = (double)waves * ((double)kb_split * bn / 128.0 + 2.0 + (s > 1 ? 2.0 : 0.0));
+      if (cost < best - 1e-9) {
+        best = cost;
+        p.bn = bn;
+        p.splits = s;
+      }
+    }
+  }
+  return p;
+}
+
+cudaError_t launch_gemm_tc(int kind, const void* A, int64_t lda, const void* B,
+                           int64_t ldb, int64_t M, int64_t N, int64_t K,
+                           const GemmPlan& plan, const float* sa, bool per_row_a,
+                           const float* sb, float* out, int32_t* acc_out,
+                           void* split_ws, unsigned int* status, cudaStream_t st) {
+  if (M == 0 || N == 0) return cudaSuccess;
+  if (!get_encode()) return cudaErrorNotSupported;
+  const bool bf16 = kind == 1;
+  CUtensorMap ma, mb;
+  if (!make_map(&ma, A, bf16, M, K, lda, kBM)) return cudaErrorInvalidValue;
+  if (!make_map(&mb, B, bf16, N, K, ldb, plan.bn)) return cudaErrorInvalidValue;
+  int32_t* split_acc = nullptr;
+  unsigned int* tile_count = nullptr;
+  if (plan.splits > 1) {
+    split_acc = static_cast<int32_t*>(split_ws);
+    tile_count = reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(split_ws) +
+                                                 (size_t)M * (size_t)N * 4);
+    const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + plan.bn - 1) / plan.bn);
+    cudaError_t e = cudaMemsetAsync(split_ws, 0, (size_t)M * (size_t)N * 4 + (size_t)tiles * 4, st);
+    if (e != cudaSuccess) return e;
+  }
+#define TC(KIND, BN)                                                                  \
+  launch_tc<KIND, BN>(ma, mb, M, N, plan.num_kb, plan.chunk_kb, plan.splits, sa,      \
+                      per_row_a, sb, out, acc_out, split_acc, tile_count, status, st)
+  if (kind == 0) return plan.bn == 256 ? TC(0, 256) : TC(0, 128);
+  return plan.bn == 256 ? TC(1, 256) : TC(1, 128);
+#undef TC
+}
+
+}  // namespace hlq

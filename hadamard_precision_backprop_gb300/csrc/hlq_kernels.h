@@ -28,10 +28,11 @@ cudaError_t launch_hq_cols(const void* src, bool bf16, int64_t rows,
 
 // HLA of src [T, C] along tokens -> codes [C, T*rank/16] (int8, or bf16
 // values when out_bf16), per-tensor scale from *amax_slot.
+// out_ld: row stride of `out` in codes (>= T*rank/16).
 cudaError_t launch_hla(const void* src, bool bf16, int64_t T, int64_t C,
                        int rank, bool amax_only, bool out_bf16,
-                       unsigned int* amax_slot, void* out, float* scale,
-                       unsigned int* status, cudaStream_t st);
+                       unsigned int* amax_slot, void* out, int64_t out_ld,
+                       float* scale, unsigned int* status, cudaStream_t st);
 size_t hla_smem_bytes(int rank, bool out_bf16);
 
 // Transform only (fp32 coefficients), for bit-exact checks.
@@ -45,12 +46,13 @@ cudaError_t launch_hla_transform(const void* src, bool bf16, int64_t T,
                                  int64_t C, int rank, float* out,
                                  unsigned int* status, cudaStream_t st);
 
-cudaError_t launch_widen_i8_bf16(const int8_t* in, void* out, int64_t n,
-                                 cudaStream_t st);
+// in [rows, cols] int8 (row stride cols) -> out [rows, out_ld] bf16.
+cudaError_t launch_widen_i8_bf16(const int8_t* in, void* out, int64_t rows,
+                                 int64_t cols, int64_t out_ld, cudaStream_t st);
 cudaError_t launch_decode_e4m3(const uint8_t* in, int8_t* out, int64_t n,
                                cudaStream_t st);
-cudaError_t launch_decode_bf16(const void* in, int8_t* out, int64_t n,
-                               cudaStream_t st);
+cudaError_t launch_decode_bf16(const void* in, int8_t* out, int64_t rows,
+                               int64_t cols, int64_t ld, cudaStream_t st);
 
 // Operand code formats of the GEMMs.
 enum CodeFmt { kFmtE4M3 = 0, kFmtI8 = 1, kFmtBF16 = 2 };
@@ -64,5 +66,23 @@ cudaError_t launch_gemm_simple(const void* A, int fmtA, const void* B,
                                const float* sa, bool per_row_a,
                                const float* sb, float* out, int32_t* acc_out,
                                cudaStream_t st);
+
+// Tensor-core GEMM (hlq_gemm_tc.cu).  kind 0: E4M3 operands (int4 codes),
+// kind 1: bf16 operands (int8 codes).  A [M, K] (row stride lda elements),
+// B [N, K] (ldb); out [M, N] fp32 = acc * sa[m or 0] * sb[0] / 16.
+struct GemmPlan {
+  int bn = 128;      // tile width (128 or 256)
+  int splits = 1;    // K split over gridDim.z (int32 workspace reduction)
+  int num_kb = 0;    // k-blocks of 128 bytes
+  int chunk_kb = 0;  // k-blocks per exact fp32 accumulation chunk
+};
+GemmPlan plan_gemm_tc(int kind, int64_t M, int64_t N, int64_t K, int num_sms,
+                      int max_splits);
+size_t gemm_tc_split_ws_bytes(int64_t M, int64_t N);
+cudaError_t launch_gemm_tc(int kind, const void* A, int64_t lda, const void* B,
+                           int64_t ldb, int64_t M, int64_t N, int64_t K,
+                           const GemmPlan& plan, const float* sa, bool per_row_a,
+                           const float* sb, float* out, int32_t* acc_out,
+                           void* split_ws, unsigned int* status, cudaStream_t st);
 
 }  // namespace hlq

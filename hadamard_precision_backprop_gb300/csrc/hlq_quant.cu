@@ -294,7 +294,7 @@ __device__ __forceinline__ void load_pair(const void* src, int64_t idx, float* v
 template <bool kBf16, int kMode, int kOut>
 __global__ void __launch_bounds__(256) hla_kernel(
     const void* __restrict__ src, int64_t T, int64_t C, int rank,
-    unsigned int* __restrict__ amax_slot, void* __restrict__ out,
+    unsigned int* __restrict__ amax_slot, void* __restrict__ out, int64_t out_ld,
     float* __restrict__ scale, unsigned int* __restrict__ status) {
   extern __shared__ __align__(16) uint8_t smem[];
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
@@ -356,7 +356,7 @@ __global__ void __launch_bounds__(256) hla_kernel(
   // Write the tile: column c gets codes [tb0*rank, (tb0+valid_tb)*rank).
   const int64_t valid_tb = imin64(kHlaTB, n_tb - tb0);
   const int64_t seg_bytes = valid_tb * rank * kBytes;
-  const int64_t row_bytes = Tp * kBytes;
+  const int64_t row_bytes = out_ld * kBytes;
   const bool vec = (seg_bytes % 16 == 0) && (row_bytes % 16 == 0) &&
                    ((tb0 * rank * kBytes) % 16 == 0);
   uint8_t* outb = static_cast<uint8_t*>(out);
@@ -452,19 +452,27 @@ __global__ void __launch_bounds__(256) hla_transform_kernel(
 // ---------------------------------------------------------------------------
 // Format conversions (GEMM operand widening and debug read-back).
 // ---------------------------------------------------------------------------
+// int8 codes [rows, cols] -> bf16 codes [rows, out_ld]; 8 codes per thread
+// (cols is a multiple of 8 on the vector path).
 __global__ void widen_i8_to_bf16_kernel(const int8_t* __restrict__ in,
                                         __nv_bfloat16* __restrict__ out,
-                                        int64_t n) {
-  const int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 8;
-  if (i + 8 <= n) {
-    uint2 r = *reinterpret_cast<const uint2*>(in + i);
-    const int8_t* b = reinterpret_cast<const int8_t*>(&r);
+                                        int64_t rows, int64_t cols,
+                                        int64_t out_ld) {
+  const int64_t per_row = (cols + 7) / 8;
+  const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= rows * per_row) return;
+  const int64_t r = idx / per_row, c = (idx % per_row) * 8;
+  const int8_t* src = in + r * cols + c;
+  __nv_bfloat16* dst = out + r * out_ld + c;
+  if (c + 8 <= cols && (cols % 8) == 0) {
+    uint2 v = *reinterpret_cast<const uint2*>(src);
+    const int8_t* b = reinterpret_cast<const int8_t*>(&v);
     __align__(16) __nv_bfloat16 o[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) o[k] = __int2bfloat16_rn(b[k]);
-    *reinterpret_cast<uint4*>(out + i) = *reinterpret_cast<const uint4*>(o);
+    *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(o);
   } else {
-    for (int64_t k = i; k < n; ++k) out[k] = __int2bfloat16_rn(in[k]);
+    for (int k = 0; k < 8 && c + k < cols; ++k) dst[k] = __int2bfloat16_rn(src[k]);
   }
 }
 
@@ -476,10 +484,12 @@ __global__ void decode_e4m3_kernel(const uint8_t* __restrict__ in,
 }
 
 __global__ void decode_bf16_kernel(const __nv_bfloat16* __restrict__ in,
-                                   int8_t* __restrict__ out, int64_t n) {
+                                   int8_t* __restrict__ out, int64_t rows,
+                                   int64_t cols, int64_t ld) {
+  const int64_t n = rows * cols;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
        i += (int64_t)gridDim.x * blockDim.x)
-    out[i] = (int8_t)__bfloat162int_rn(in[i]);
+    out[i] = (int8_t)__bfloat162int_rn(in[(i / cols) * ld + i % cols]);
 }
 
 // ---------------------------------------------------------------------------
@@ -539,8 +549,8 @@ size_t hla_smem_bytes(int rank, bool out_bf16) {
 
 cudaError_t launch_hla(const void* src, bool bf16, int64_t T, int64_t C,
                        int rank, bool amax_only, bool out_bf16,
-                       unsigned int* amax_slot, void* out, float* scale,
-                       unsigned int* status, cudaStream_t st) {
+                       unsigned int* amax_slot, void* out, int64_t out_ld,
+                       float* scale, unsigned int* status, cudaStream_t st) {
   dim3 grid(grid1(C, kHlaCols), grid1(T / 16, kHlaTB));
   const size_t smem = amax_only ? 0 : hla_smem_bytes(rank, out_bf16);
 #define HLA(B, M, O)                                                           \
@@ -550,7 +560,7 @@ cudaError_t launch_hla(const void* src, bool bf16, int64_t T, int64_t C,
                            cudaFuncAttributeMaxDynamicSharedMemorySize,        \
                            (int)smem);                                         \
     hla_kernel<B, M, O><<<grid, 256, smem, st>>>(src, T, C, rank, amax_slot,   \
-                                                 out, scale, status);          \
+                                                 out, out_ld, scale, status);  \
   } while (0)
   if (amax_only) {
     if (bf16) HLA(true, kAmax, 0); else HLA(false, kAmax, 0);
@@ -590,11 +600,12 @@ cudaError_t launch_hla_transform(const void* src, bool bf16, int64_t T,
   return cudaGetLastError();
 }
 
-cudaError_t launch_widen_i8_bf16(const int8_t* in, void* out, int64_t n,
-                                 cudaStream_t st) {
-  if (n == 0) return cudaSuccess;
-  widen_i8_to_bf16_kernel<<<grid1(n, 256 * 8), 256, 0, st>>>(
-      in, static_cast<__nv_bfloat16*>(out), n);
+cudaError_t launch_widen_i8_bf16(const int8_t* in, void* out, int64_t rows,
+                                 int64_t cols, int64_t out_ld, cudaStream_t st) {
+  if (rows * cols == 0) return cudaSuccess;
+  const int64_t n = rows * ((cols + 7) / 8);
+  widen_i8_to_bf16_kernel<<<grid1(n, 256), 256, 0, st>>>(
+      in, static_cast<__nv_bfloat16*>(out), rows, cols, out_ld);
   return cudaGetLastError();
 }
 
@@ -605,11 +616,12 @@ cudaError_t launch_decode_e4m3(const uint8_t* in, int8_t* out, int64_t n,
   return cudaGetLastError();
 }
 
-cudaError_t launch_decode_bf16(const void* in, int8_t* out, int64_t n,
-                               cudaStream_t st) {
+cudaError_t launch_decode_bf16(const void* in, int8_t* out, int64_t rows,
+                               int64_t cols, int64_t ld, cudaStream_t st) {
+  const int64_t n = rows * cols;
   if (n == 0) return cudaSuccess;
   decode_bf16_kernel<<<(unsigned)imin64(grid1(n, 256), 4096), 256, 0, st>>>(
-      static_cast<const __nv_bfloat16*>(in), out, n);
+      static_cast<const __nv_bfloat16*>(in), out, rows, cols, ld);
   return cudaGetLastError();
 }
 

@@ -188,6 +188,32 @@ hlq_status hlq_debug_hla_transform(const void *d_src, int dt, int64_t T,
  */
 hlq_status hlq_read_device_status(uint32_t *flags, int clear, void *stream);
 
+/*
+ * Second-opinion integer GEMM on the CUDA cores (dp4a), for checking the
+ * tensor-core GEMMs at full size: d_acc[m, n] = sum_k A[m, k] * B[n, k] with
+ * A [M, K] and B [N, K] int8 (contraction dim contiguous), int32 sums.
+ * `kind` is 0 or 1 (kept for symmetry with the two GEMMs; both read int8).
+ */
+hlq_status hlq_debug_reference_gemm(int kind, const void *d_a, const void *d_b,
+                                    int64_t M, int64_t N, int64_t K,
+                                    int32_t *d_acc, void *stream);
+
+/*
+ * Launch tracing, for timing without a profiler.  hlq_trace_begin creates
+ * 2*capacity CUDA events (host-side objects, no device memory) and turns
+ * tracing on: every later kernel launch of this library, on any stream, is
+ * bracketed by two events recorded on that stream, up to `capacity` launches
+ * (later ones run untraced).  hlq_trace_end turns tracing off, waits for the
+ * recorded events and returns how many launches were traced; hlq_trace_get
+ * gives launch i's kernel name (static string) and its device time in ms.
+ * hlq_trace_free destroys the events.  Not thread-safe: trace from one host
+ * thread at a time.
+ */
+hlq_status hlq_trace_begin(int capacity);
+hlq_status hlq_trace_end(int *n_launches);
+hlq_status hlq_trace_get(int i, const char **name, float *ms);
+hlq_status hlq_trace_free(void);
+
 /* Static text for a status code. */
 const char *hlq_status_string(int status);
 

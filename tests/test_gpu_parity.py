@@ -205,3 +205,67 @@ def test_seed_changes_codes_deterministically():
     b = hlq.hlq_debug_gx_parts(gy, w, seed=1)["qgy"]
     c = hlq.hlq_debug_gx_parts(gy, w, seed=(1 << 40) + 1)["qgy"]
     assert torch.equal(a, b) and not torch.equal(a, c)
+
+
+# ------------------------------------------- accumulator exactness at the limits
+
+def _lossless_rows(signs, scale, H):
+    """Rows whose 16-blocks transform (by H16) to exactly 7*scale*signs."""
+    T, n = signs.shape
+    out = np.zeros((T, n), np.float64)
+    for b in range(n // 16):
+        out[:, 16 * b:16 * b + 16] = (7.0 * scale * signs[:, 16 * b:16 * b + 16]) @ H / 16.0
+    return out.astype(np.float32)
+
+
+def test_gx_accumulator_exact_at_max_magnitude():
+    """All int4 codes +-7 with rows of qY equal to rows of qW: |acc| reaches
+    49 * Cout, the largest the g_x GEMM admits a chunk to hold."""
+    H = oracle.hadamard16().astype(np.float64)
+    rng = np.random.default_rng(31)
+    T, Cin, Cout = 256, 64, 4096
+    sw = rng.choice([-1.0, 1.0], size=(Cin, Cout))
+    sy = rng.choice([-1.0, 1.0], size=(T, Cout))
+    sy[:Cin] = sw                      # acc[t, t] = 49 * Cout for t < Cin
+    sy[Cin:2 * Cin] = -sw
+    gy = _lossless_rows(sy, 2.0 ** -8, H)
+    wT = _lossless_rows(sw, 2.0 ** -4, H)          # [Cin, Cout]
+    inp = {"g_y": gy, "w": np.ascontiguousarray(wT.T),
+           "x": np.zeros((T, Cin), np.float32)}
+    r, ref = check_gx(inp, "f32", workloads.PER_TENSOR, oracle.RNE, 0)
+    acc = host(r["acc"])
+    assert acc[0, 0] == 49 * Cout and acc[Cin, 0] == -49 * Cout
+
+
+def _hla_lossless(signs, scale, rank=8):
+    """Tokens whose HLA coefficients (rank lowest-sequency rows per 16-token
+    block) are exactly 127*scale*signs; signs [T', C]."""
+    H = oracle.hadamard16().astype(np.float64)
+    sigma = oracle.sequency_order()
+    Tp, C = signs.shape
+    T = Tp // rank * 16
+    x = np.zeros((T, C), np.float64)
+    for b in range(T // 16):
+        c = 127.0 * scale * signs[rank * b:rank * b + rank]        # [rank, C]
+        x[16 * b:16 * b + 16] = (H[sigma[:rank]].T @ c) / 16.0
+    return x.astype(np.float32)
+
+
+def test_gw_accumulator_exact_beyond_2_24():
+    """All int8 codes +-127 with matching signs: acc = 127^2 * T' = 66e6,
+    beyond the 2^24 an fp32 accumulator holds exactly; the chunked drain and
+    any K split must still give the exact integer."""
+    rng = np.random.default_rng(32)
+    T, Cin, Cout, rank = 8192, 32, 48, 8
+    Tp = T // 16 * rank
+    sx = rng.choice([-1.0, 1.0], size=(Tp, Cin))
+    sg = rng.choice([-1.0, 1.0], size=(Tp, Cout))
+    sg[:, :Cin] = sx                     # acc[o, o] = 127^2 * T' for o < Cin
+    x = _hla_lossless(sx, 2.0 ** -3, rank)
+    gy = _hla_lossless(sg, 2.0 ** -9, rank)
+    inp = {"x": x, "g_y": gy, "w": np.zeros((Cout, Cin), np.float32)}
+    check_gw(inp, "f32", rank)
+    xbar, s = hlq.hlq_compress_activation(to_dev(inp, "x", "f32"), rank=rank)
+    r = hlq.hlq_debug_gw_parts(to_dev(inp, "g_y", "f32"), xbar, s, rank=rank)
+    acc = host(r["acc"])
+    assert acc[0, 0] == 127 * 127 * Tp and acc[5, 5] == 127 * 127 * Tp
