@@ -35,7 +35,7 @@ EXPORTS = [
     "hlq_read_device_status", "hlq_status_string", "hlq_version",
     "hlq_debug_hq_transform", "hlq_debug_hla_transform",
     "hlq_trace_begin", "hlq_trace_end", "hlq_trace_get", "hlq_trace_free",
-    "hlq_debug_reference_gemm",
+    "hlq_debug_reference_gemm", "hlq_debug_tc_gemm", "hlq_debug_tc_gemm_ws_bytes",
 ]
 
 _lock = threading.Lock()
@@ -85,6 +85,9 @@ def lib() -> ctypes.CDLL:
             "hlq_debug_hla_transform": (i32, [P, i32, i64, i64, i32, P, P]),
             "hlq_trace_begin": (i32, [i32]),
             "hlq_debug_reference_gemm": (i32, [i32, P, P, i64, i64, i64, P, P]),
+            "hlq_debug_tc_gemm": (i32, [i32, P, i64, P, i64, i64, i64, i64, i32,
+                                        i32, P, P, sz, P]),
+            "hlq_debug_tc_gemm_ws_bytes": (sz, [i64, i64]),
             "hlq_trace_end": (i32, [P]),
             "hlq_trace_get": (i32, [i32, P, P]),
             "hlq_trace_free": (i32, []),
@@ -300,6 +303,22 @@ def hlq_debug_reference_gemm(a, b, stream=None):
     _check(lib().hlq_debug_reference_gemm(0, _ptr(a), _ptr(b), M, N, K,
                                           _ptr(acc), _stream(stream)),
            "hlq_debug_reference_gemm")
+    return acc
+
+
+def hlq_debug_tc_gemm(kind, a, b, bn=0, splits=0, stream=None):
+    """int32 a @ b^T on the tensor cores with an explicit plan.  kind 0: a, b
+    are uint8 E4M3 codes [M, K] / [N, K]; kind 1: bf16 codes."""
+    torch = _torch()
+    _need_cuda_contig(a, b)
+    M, K = a.shape
+    N = b.shape[0]
+    acc = torch.empty((M, N), dtype=torch.int32, device=a.device)
+    nws = int(lib().hlq_debug_tc_gemm_ws_bytes(M, N))
+    ws = torch.empty(max(nws, 256), dtype=torch.uint8, device=a.device)
+    _check(lib().hlq_debug_tc_gemm(kind, _ptr(a), K, _ptr(b), K, M, N, K, bn,
+                                   splits, _ptr(acc), _ptr(ws), ws.numel(),
+                                   _stream(stream)), "hlq_debug_tc_gemm")
     return acc
 
 

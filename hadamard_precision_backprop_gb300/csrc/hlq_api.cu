@@ -425,6 +425,42 @@ hlq_status hlq_debug_reference_gemm(int kind, const void* d_a, const void* d_b,
   return HLQ_OK;
 }
 
+hlq_status hlq_debug_tc_gemm(int kind, const void* d_a, int64_t lda, const void* d_b,
+                             int64_t ldb, int64_t M, int64_t N, int64_t K, int bn,
+                             int splits, int32_t* d_acc, void* d_ws, size_t ws_bytes,
+                             void* stream) {
+  if (kind != 0 && kind != 1) return HLQ_ERR_INVALID_ARG;
+  if (M < 0 || N < 0 || K < 0 || N % 16 || K % 16 || M % 16) return HLQ_ERR_SHAPE;
+  if (bn != 0 && bn != 128 && bn != 256) return HLQ_ERR_INVALID_ARG;
+  if (splits < 0 || splits > 64) return HLQ_ERR_INVALID_ARG;
+  const int esz = kind == 1 ? 2 : 1;
+  if (lda < K || ldb < K || (lda * esz) % 16 || (ldb * esz) % 16) return HLQ_ERR_ALIGN;
+  if (M * N > 0 && (!d_a || !d_b || !d_acc)) return HLQ_ERR_INVALID_ARG;
+  if (!aligned16(d_a) || !aligned16(d_b) || !aligned16(d_acc)) return HLQ_ERR_ALIGN;
+  if (kind == 0 && 49 * K >= ((int64_t)1 << 24)) return HLQ_ERR_OVERFLOW;
+  if (kind == 1 && K * 127 * 127 >= ((int64_t)1 << 31)) return HLQ_ERR_OVERFLOW;
+  if (M * N == 0) return HLQ_OK;
+  const int sms = device_sm_count();
+  if (sms <= 0) return HLQ_ERR_CUDA;
+  GemmPlan plan = plan_gemm_tc(kind, M, N, K, sms, kind == 1 ? 16 : 1);
+  if (bn) plan.bn = bn;
+  if (splits) plan.splits = splits;
+  if (plan.splits > 1 && (!d_ws || ws_bytes < gemm_tc_split_ws_bytes(M, N)))
+    return HLQ_ERR_WORKSPACE;
+  if (plan.splits > 1 && !aligned256(d_ws)) return HLQ_ERR_ALIGN;
+  unsigned int* status = device_status_ptr();
+  if (!status) return HLQ_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  HLQ_LAUNCH(kind == 0 ? "gemm_gx_tc" : "gemm_gw_tc", s,
+             launch_gemm_tc(kind, d_a, lda, d_b, ldb, M, N, K, plan, nullptr, false,
+                            nullptr, nullptr, d_acc, d_ws, status, s));
+  return HLQ_OK;
+}
+
+size_t hlq_debug_tc_gemm_ws_bytes(int64_t M, int64_t N) {
+  return gemm_tc_split_ws_bytes(M, N);
+}
+
 hlq_status hlq_trace_begin(int capacity) {
   if (capacity <= 0 || capacity > (1 << 20)) return HLQ_ERR_INVALID_ARG;
   trace_free();

@@ -5,6 +5,7 @@
 
 #include <cstdint>
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include "hlq.h"
@@ -149,6 +150,71 @@ static __device__ __noinline__ float exact_sum16(const float* v, uint32_t neg_ma
   return __uint_as_float(bits | (negative ? 0x80000000u : 0u));
 }
 
+// Exact 16-point Hadamard transform of v in 64-bit fixed point: every value
+// is m * 2^(p-150) (m its 24-bit significand, p its exponent field, >= 1),
+// so with pmin the smallest p of the non-zero values, n_j = m_j << (p_j - pmin)
+// are integers and y_i = sum_j H[i][j] n_j * 2^(pmin-150) exactly.  bf16
+// inputs have 16 zero low significand bits, which are dropped first.  The
+// sums fit in int64 when the exponent spread is at most 51 (bf16) or 35
+// (fp32) binades; each y_i is then rounded once by the int64 -> fp32
+// conversion and rescaled by an exponent shift.  Returns false (y is then
+// garbage) when the spread is larger or a result would be subnormal.
+template <bool kBf16>
+__device__ __forceinline__ bool fwht16_fixed(const float* v, float* y) {
+  constexpr int kDrop = kBf16 ? 16 : 0;
+  constexpr int kMaxSpread = kBf16 ? 51 : 35;
+  int pmin = 255, pmax = 0;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const uint32_t b = __float_as_uint(v[j]) & 0x7fffffffu;
+    if (b != 0u) {
+      const int p = max((int)(b >> 23), 1);
+      pmin = min(pmin, p);
+      pmax = max(pmax, p);
+    }
+  }
+  if (pmax == 0) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) y[i] = 0.0f;
+    return true;
+  }
+  if (pmax - pmin > kMaxSpread) return false;
+  long long n[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const uint32_t b = __float_as_uint(v[j]);
+    const uint32_t e = (b >> 23) & 0xffu;
+    uint32_t m = b & 0x7fffffu;
+    if (e != 0u) m |= 0x800000u;
+    long long mag = 0;
+    if (m != 0u) mag = (long long)(m >> kDrop) << (max((int)e, 1) - pmin);
+    n[j] = (b >> 31) ? -mag : mag;
+  }
+#pragma unroll
+  for (int h = 1; h < 16; h <<= 1)
+#pragma unroll
+    for (int a = 0; a < 16; ++a)
+      if ((a & h) == 0) {
+        const long long p = n[a], q = n[a + h];
+        n[a] = p + q;
+        n[a + h] = p - q;
+      }
+  const int L = pmin - 150 + kDrop;  // y_i = n_i * 2^L
+  bool ok = true;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    if (n[i] == 0) {
+      y[i] = 0.0f;
+    } else {
+      const uint32_t fb = __float_as_uint(__ll2float_rn(n[i]));
+      const int E = (int)((fb >> 23) & 0xffu) + L;
+      ok &= (E >= 1);
+      y[i] = __uint_as_float(fb + ((uint32_t)L << 23));
+    }
+  }
+  return ok;
+}
+
 // Sylvester H16 row i as a negate mask: bit j set when popcount(i & j) odd.
 __device__ __forceinline__ uint32_t hrow_negmask(int i) {
   uint32_t m = 0;
@@ -224,6 +290,42 @@ __device__ __forceinline__ U4 philox_block(uint64_t seed, uint32_t stream,
                        (uint32_t)seed, (uint32_t)(seed >> 32));
 }
 
+// The ten round keys of a seed, computed once per thread and reused for
+// every block it draws (the key schedule does not depend on the counter).
+struct PhiloxKeys {
+  uint32_t k0[10], k1[10];
+};
+
+__device__ __forceinline__ PhiloxKeys philox_keys(uint64_t seed) {
+  PhiloxKeys k;
+  uint32_t a = (uint32_t)seed, b = (uint32_t)(seed >> 32);
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    k.k0[r] = a;
+    k.k1[r] = b;
+    a += 0x9E3779B9u;
+    b += 0xBB67AE85u;
+  }
+  return k;
+}
+
+__device__ __forceinline__ U4 philox_block_k(const PhiloxKeys& k, uint32_t stream,
+                                             uint64_t q) {
+  uint32_t c0 = (uint32_t)q, c1 = (uint32_t)(q >> 32), c2 = stream, c3 = 0u;
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const unsigned long long p0 = (unsigned long long)0xD2511F53u * c0;
+    const unsigned long long p1 = (unsigned long long)0xCD9E8D57u * c2;
+    const uint32_t n0 = (uint32_t)(p1 >> 32) ^ c1 ^ k.k0[r];
+    const uint32_t n2 = (uint32_t)(p0 >> 32) ^ c3 ^ k.k1[r];
+    c1 = (uint32_t)p1;
+    c3 = (uint32_t)p0;
+    c0 = n0;
+    c2 = n2;
+  }
+  return {c0, c1, c2, c3};
+}
+
 // ---------------------------------------------------------------------------
 // Quantizers.  s == 0 gives code 0.  Division is IEEE round-to-nearest.
 // ---------------------------------------------------------------------------
@@ -245,6 +347,29 @@ __device__ __forceinline__ int quant_rne(float y, float s, int qmax) {
   float r = rintf(x);
   r = fminf(fmaxf(r, -(float)qmax), (float)qmax);
   return (int)r;
+}
+
+// Float-valued forms of the two roundings (integer-valued results, clamped);
+// s == 0 gives 0.
+__device__ __forceinline__ float quant_sr_f(float y, float s, uint32_t word,
+                                            float qmax) {
+  const float x = __fdiv_rn(y, s);
+  const float f = floorf(x);
+  const float frac = x - f;
+  const float u = __uint2float_rn(word >> 8) * 5.9604644775390625e-08f;  // 2^-24
+  const float r = fminf(fmaxf(f + ((u < frac) ? 1.0f : 0.0f), -qmax), qmax);
+  return s == 0.0f ? 0.0f : r;
+}
+
+__device__ __forceinline__ float quant_rne_f(float y, float s, float qmax) {
+  const float r = fminf(fmaxf(rintf(__fdiv_rn(y, s)), -qmax), qmax);
+  return s == 0.0f ? 0.0f : r;
+}
+
+// Two integer-valued floats in [-7, 7] to two E4M3 bytes (exact; a in the
+// low byte).
+__device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
+  return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
 }
 
 // E4M3 byte of an integer in [-7, 7] (exact): |q| = 1.m * 2^e, bias 7.

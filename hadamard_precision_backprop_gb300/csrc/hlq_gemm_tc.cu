@@ -337,15 +337,16 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(
       }
     }
     if (ok && gridDim.z == 1 && m < M) {
-      const float scale = (per_row_a ? sa[m] : sa[0]) * sb[0] * 0.0625f;
+      const float scale = out ? (per_row_a ? sa[m] : sa[0]) * sb[0] * 0.0625f : 0.0f;
       float* orow = out + (size_t)m * N;
 #pragma unroll
       for (int q = 0; q < C::kColsPerThread; q += 4) {
         const int n = nb + q;
         if (n + 4 <= N) {
-          *reinterpret_cast<float4*>(orow + n) =
-              make_float4((float)acc[q] * scale, (float)acc[q + 1] * scale,
-                          (float)acc[q + 2] * scale, (float)acc[q + 3] * scale);
+          if (out)
+            *reinterpret_cast<float4*>(orow + n) =
+                make_float4((float)acc[q] * scale, (float)acc[q + 1] * scale,
+                            (float)acc[q + 2] * scale, (float)acc[q + 3] * scale);
           if (acc_out)
             *reinterpret_cast<int4*>(acc_out + (size_t)m * N + n) =
                 make_int4(acc[q], acc[q + 1], acc[q + 2], acc[q + 3]);
@@ -367,13 +368,12 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(
     if (*last_flag) {
       __threadfence();
       const int rows = min(kBM, M - m0), cols = min(BN, N - n0);
-      const float scale_t = sb[0] * 0.0625f;
+      const float scale_t = out ? sb[0] * 0.0625f : 0.0f;
       for (int idx = threadIdx.x; idx < rows * cols; idx += blockDim.x) {
         const int r = idx / cols, cc = idx % cols;
         const int m = m0 + r, n = n0 + cc;
         const int32_t v = __ldcg(&split_acc[(size_t)m * N + n]);
-        const float scale = (per_row_a ? sa[m] : sa[0]) * scale_t;
-        out[(size_t)m * N + n] = (float)v * scale;
+        if (out) out[(size_t)m * N + n] = (float)v * ((per_row_a ? sa[m] : sa[0]) * scale_t);
         if (acc_out) acc_out[(size_t)m * N + n] = v;
       }
     }
@@ -467,24 +467,22 @@ GemmPlan plan_gemm_tc(int kind, int64_t M, int64_t N, int64_t K, int num_sms,
   p.num_kb = (int)((K + elems - 1) / elems);
   p.chunk_kb = (kind == 1) ? 16 : p.num_kb;  // bf16: 1024 codes per exact chunk
   if (p.chunk_kb < 1) p.chunk_kb = 1;
-  // choose the tile width and split count that fill the GPU best
-  double best = 1e30;
-  for (int bn : {128, 256}) {
-    const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + bn - 1) / bn);
-    for (int s = 1; s <= max_splits; ++s) {
-      if (s > 1 && (p.num_kb + s - 1) / s < 4) break;
-      const int64_t ctas = tiles * s;
-      const int64_t waves = (ctas + num_sms - 1) / num_sms;
-      const int kb_split = (p.num_kb + s - 1) / s;
-      // per CTA: k-blocks of MMA work (proportional to bn), plus the
-      // epilogue / reduction overhead of a split
-      const double cost = (double)waves * ((double)kb_split * bn / 128.0 + 2.0 + (s > 1 ? 2.0 : 0.0));
-      if (cost < best - 1e-9) {
-        best = cost;
-        p.bn = bn;
-        p.splits = s;
-      }
-    }
+  // Tile width: fewer waves of CTAs, a 256-wide tile counted as 1.6 waves of
+  // 128-wide ones (it moves less shared-memory and L2 data per MMA).  K split: only when the tiles
+  // fill less than a third of the SMs, because the int32 reduction through
+  // global atomics costs about as much as the MMAs it parallelises.
+  const int64_t t128 = ((M + kBM - 1) / kBM) * ((N + 127) / 128);
+  const int64_t t256 = ((M + kBM - 1) / kBM) * ((N + 255) / 256);
+  const double w128 = (double)((t128 + num_sms - 1) / num_sms);
+  const double w256 = (double)((t256 + num_sms - 1) / num_sms) * 1.6;
+  p.bn = (w256 <= w128) ? 256 : 128;
+  const int64_t tiles = p.bn == 256 ? t256 : t128;
+  p.splits = 1;
+  if (max_splits > 1 && tiles * 3 < num_sms) {
+    int s = (int)(num_sms / tiles);
+    s = s < max_splits ? s : max_splits;
+    while (s > 1 && (p.num_kb + s - 1) / s < 2 * p.chunk_kb) --s;
+    p.splits = s > 1 ? s : 1;
   }
   return p;
 }

@@ -33,7 +33,6 @@ cudaError_t launch_hla(const void* src, bool bf16, int64_t T, int64_t C,
                        int rank, bool amax_only, bool out_bf16,
                        unsigned int* amax_slot, void* out, int64_t out_ld,
                        float* scale, unsigned int* status, cudaStream_t st);
-size_t hla_smem_bytes(int rank, bool out_bf16);
 
 // Transform only (fp32 coefficients), for bit-exact checks.
 cudaError_t launch_hq_rows_transform(const void* src, bool bf16, int64_t rows,

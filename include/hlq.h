@@ -199,6 +199,22 @@ hlq_status hlq_debug_reference_gemm(int kind, const void *d_a, const void *d_b,
                                     int32_t *d_acc, void *stream);
 
 /*
+ * The tensor-core GEMM alone, with an explicit plan, for checks and tuning:
+ *   d_acc[m, n] = sum_k A[m, k] * B[n, k]   (int32, exact)
+ * kind 0: A, B hold E4M3 bytes of integers in [-7, 7] (the g_x GEMM);
+ * kind 1: A, B hold bf16 values of integers in [-127, 127] (the g_w GEMM).
+ * lda / ldb: row strides in elements (16-byte multiples).  bn: tile width
+ * 128 or 256 (0 = the library's choice); splits: K split count (0 = the
+ * library's choice; > 1 needs d_ws of hlq_debug_tc_gemm_ws_bytes(M, N)).
+ * M, N, K multiples of 16.
+ */
+hlq_status hlq_debug_tc_gemm(int kind, const void *d_a, int64_t lda,
+                             const void *d_b, int64_t ldb, int64_t M, int64_t N,
+                             int64_t K, int bn, int splits, int32_t *d_acc,
+                             void *d_ws, size_t ws_bytes, void *stream);
+size_t hlq_debug_tc_gemm_ws_bytes(int64_t M, int64_t N);
+
+/*
  * Launch tracing, for timing without a profiler.  hlq_trace_begin creates
  * 2*capacity CUDA events (host-side objects, no device memory) and turns
  * tracing on: every later kernel launch of this library, on any stream, is

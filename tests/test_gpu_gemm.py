@@ -1,0 +1,77 @@
+"""The tensor-core GEMMs alone: exact int32 sums for every tile width and
+K split, ragged M/N/K, both operand kinds (E4M3 int4 codes, bf16 int8
+codes), against numpy int64 sums and the CUDA-core reference GEMM."""
+import numpy as np
+import pytest
+import torch
+
+import hadamard_precision_backprop_gb300 as hlq
+from hadamard_precision_backprop_gb300 import build as hbuild
+
+pytestmark = pytest.mark.gpu
+
+# E4M3 (1 sign, 4 exponent bits with bias 7, 3 mantissa bits) bytes of the
+# integers 0..7, written out from the format's definition.
+E4M3_OF = {0: 0x00, 1: 0x38, 2: 0x40, 3: 0x44, 4: 0x48, 5: 0x4A, 6: 0x4C, 7: 0x4E}
+
+
+def e4m3_bytes(codes):
+    mag = np.vectorize(lambda v: E4M3_OF[abs(int(v))])(codes).astype(np.uint8)
+    return np.where(codes < 0, mag | 0x80, mag).astype(np.uint8)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    hbuild.build()
+    hlq.lib()
+
+
+def run(kind, A, B, bn, splits):
+    if kind == 0:
+        a = torch.from_numpy(e4m3_bytes(A)).cuda()
+        b = torch.from_numpy(e4m3_bytes(B)).cuda()
+    else:
+        a = torch.from_numpy(A.astype(np.float32)).cuda().to(torch.bfloat16)
+        b = torch.from_numpy(B.astype(np.float32)).cuda().to(torch.bfloat16)
+    return hlq.hlq_debug_tc_gemm(kind, a, b, bn=bn, splits=splits)
+
+
+@pytest.mark.parametrize("kind,qmax", [(0, 7), (1, 127)])
+@pytest.mark.parametrize("M,N,K", [(128, 128, 128), (16, 32, 16), (272, 400, 208),
+                                   (384, 512, 2048), (1040, 144, 4112)])
+@pytest.mark.parametrize("bn,splits", [(128, 1), (256, 1), (128, 3), (256, 2)])
+def test_tc_gemm_exact(kind, qmax, M, N, K, bn, splits):
+    rng = np.random.default_rng(M * 7 + N * 3 + K + bn + splits)
+    A = rng.integers(-qmax, qmax + 1, (M, K))
+    B = rng.integers(-qmax, qmax + 1, (N, K))
+    want = A.astype(np.int64) @ B.astype(np.int64).T
+    if kind == 0 and splits > 1:
+        pytest.skip("the E4M3 GEMM runs unsplit")
+    got = run(kind, A, B, bn, splits).cpu().numpy()
+    np.testing.assert_array_equal(got.astype(np.int64), want)
+    ref = hlq.hlq_debug_reference_gemm(torch.from_numpy(A.astype(np.int8)).cuda(),
+                                       torch.from_numpy(B.astype(np.int8)).cuda())
+    np.testing.assert_array_equal(ref.cpu().numpy(), got)
+
+
+def test_tc_gemm_bf16_worst_case_magnitude():
+    """Every product 127*127 with one sign: |acc| = 16129*K, far above 2^24,
+    only exact through the chunked drains (and the int32 split reduction)."""
+    M, N, K = 256, 256, 16384
+    A = np.full((M, K), 127, np.int64)
+    A[1::2] = -127
+    B = np.full((N, K), 127, np.int64)
+    for splits in (1, 2, 5):
+        got = run(1, A, B, 128, splits).cpu().numpy()
+        assert got[0, 0] == 16129 * K and got[1, 0] == -16129 * K
+        assert np.all(got[0::2] == 16129 * K) and np.all(got[1::2] == -16129 * K)
+
+
+def test_tc_gemm_e4m3_worst_case_magnitude():
+    M, N, K = 128, 256, 4096
+    A = np.full((M, K), 7, np.int64)
+    A[::3] = -7
+    B = np.full((N, K), -7, np.int64)
+    got = run(0, A, B, 256, 1).cpu().numpy()
+    want = A[:, :1] * B[:, 0][None, :] * K
+    np.testing.assert_array_equal(got, want)
