@@ -36,6 +36,7 @@ EXPORTS = [
     "hlq_debug_hq_transform", "hlq_debug_hla_transform",
     "hlq_trace_begin", "hlq_trace_end", "hlq_trace_get", "hlq_trace_free",
     "hlq_debug_reference_gemm", "hlq_debug_tc_gemm", "hlq_debug_tc_gemm_ws_bytes",
+    "hlq_linear_backward_gx_noalloc", "hlq_noalloc_scratch_bytes",
 ]
 
 _lock = threading.Lock()
@@ -88,6 +89,9 @@ def lib() -> ctypes.CDLL:
             "hlq_debug_tc_gemm": (i32, [i32, P, i64, P, i64, i64, i64, i64, i32,
                                         i32, P, P, sz, P]),
             "hlq_debug_tc_gemm_ws_bytes": (sz, [i64, i64]),
+            "hlq_linear_backward_gx_noalloc": (i32, [P, P, i32, i64, i64, i64, i32,
+                                                     i32, i32, i32, u64, P, P]),
+            "hlq_noalloc_scratch_bytes": (sz, []),
             "hlq_trace_end": (i32, [P]),
             "hlq_trace_get": (i32, [i32, P, P]),
             "hlq_trace_free": (i32, []),
@@ -216,6 +220,27 @@ def hlq_linear_backward_gw(g_y, xbar, xbar_scale, rank: int = 8,
         _ptr(g_y), _dtype_code(g_y), _ptr(xbar), _ptr(xbar_scale), T, Cin,
         Cout, block, rank, _ptr(out), _ptr(ws), ws.numel(), _stream(stream)),
         "hlq_linear_backward_gw")
+    return out
+
+
+def hlq_linear_backward_gx_noalloc(g_y, w, gran_gy: int = PER_TOKEN,
+                                   gran_w: int = PER_TENSOR, rnd: int = SR,
+                                   seed: int = 0, block: int = 16, out=None,
+                                   stream=None):
+    """hlq_linear_backward_gx without a workspace: for callers that cannot
+    allocate device memory, the library uses its own fixed scratch array
+    (see include/hlq.h for the size limit and the sharing rules).  `out`
+    lets such callers pass a preallocated g_x as well."""
+    torch = _torch()
+    _need_cuda_contig(g_y, w)
+    T, Cout = g_y.shape
+    Cin = w.shape[1]
+    if out is None:
+        out = torch.empty((T, Cin), dtype=torch.float32, device=g_y.device)
+    _check(lib().hlq_linear_backward_gx_noalloc(
+        _ptr(g_y), _ptr(w), _dtype_code(g_y), T, Cin, Cout, block, gran_gy,
+        gran_w, rnd, seed, _ptr(out), _stream(stream)),
+        "hlq_linear_backward_gx_noalloc")
     return out
 
 

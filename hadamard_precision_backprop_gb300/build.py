@@ -19,7 +19,8 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libhlq.so")
 
-SOURCES = ["hlq_api.cu", "hlq_quant.cu", "hlq_gemm_simple.cu", "hlq_gemm_tc.cu"]
+SOURCES = ["hlq_api.cu", "hlq_quant.cu", "hlq_gemm_simple.cu", "hlq_gemm_tc.cu",
+           "hlq_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -279,6 +279,19 @@ hlq_status gw_impl(const void* gy, int dt, const int8_t* xbar,
 }
 
 }  // namespace
+
+size_t gx_workspace_bytes(int64_t T, int64_t Cin, int64_t Cout) {
+  return gx_layout(T, Cin, Cout).total;
+}
+
+hlq_status backward_gx_with_ws(const void* gy, const void* w, int dt, int64_t T,
+                               int64_t Cin, int64_t Cout, int block, int gran_gy,
+                               int gran_w, int rnd, uint64_t seed, float* gx,
+                               void* ws, size_t ws_bytes, void* stream) {
+  return gx_impl(gy, w, dt, T, Cin, Cout, block, gran_gy, gran_w, rnd, seed, gx, ws,
+                 ws_bytes, nullptr, nullptr, nullptr, nullptr, nullptr, stream);
+}
+
 }  // namespace hlq
 
 using namespace hlq;

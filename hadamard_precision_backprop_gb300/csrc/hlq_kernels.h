@@ -5,6 +5,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "hlq.h"
+
 namespace hlq {
 
 // HQ of a [rows, cols] tensor along cols (g_y).  amax_only: per-tensor
@@ -83,5 +85,13 @@ cudaError_t launch_gemm_tc(int kind, const void* A, int64_t lda, const void* B,
                            const GemmPlan& plan, const float* sa, bool per_row_a,
                            const float* sb, float* out, int32_t* acc_out,
                            void* split_ws, unsigned int* status, cudaStream_t st);
+
+// The g_x path with a given workspace (the body of hlq_linear_backward_gx)
+// and the workspace it needs.
+size_t gx_workspace_bytes(int64_t T, int64_t Cin, int64_t Cout);
+hlq_status backward_gx_with_ws(const void* gy, const void* w, int dt, int64_t T,
+                               int64_t Cin, int64_t Cout, int block, int gran_gy,
+                               int gran_w, int rnd, uint64_t seed, float* gx,
+                               void* ws, size_t ws_bytes, void* stream);
 
 }  // namespace hlq

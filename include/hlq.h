@@ -230,6 +230,33 @@ hlq_status hlq_trace_end(int *n_launches);
 hlq_status hlq_trace_get(int i, const char **name, float *ms);
 hlq_status hlq_trace_free(void);
 
+/*
+ * hlq_linear_backward_gx for callers that cannot allocate device memory:
+ * code hosted by another runtime that owns all device memory and gives
+ * plugins none, or loops that forbid cudaMalloc/cudaFree (which can
+ * synchronize the device) once running.  It computes exactly what
+ * hlq_linear_backward_gx computes, with the same arguments minus the
+ * workspace, and allocates nothing: its scratch is one fixed device array
+ * of this library of hlq_noalloc_scratch_bytes() bytes (40 MiB), held by
+ * every GPU that loads the library until the process exits.  The paper has
+ * no counterpart to this entry point.
+ *  - Sizes whose scratch (the g_x workspace of hlq_workspace_bytes) exceeds
+ *    that array are refused with HLQ_ERR_WORKSPACE before anything runs.
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
+ *  - All calls share the array, which keeps the last call's contents; each
+ *    call clears what must start at zero.  Calls whose work overlaps on the
+ *    GPU (other streams, other host threads) race on the array: order them
+ *    on one stream or synchronize between them.
+ */
+hlq_status hlq_linear_backward_gx_noalloc(const void *d_gy, const void *d_w, int dt,
+                                          int64_t T, int64_t Cin, int64_t Cout,
+                                          int block, int gran_gy, int gran_w,
+                                          int rnd, uint64_t seed, float *d_gx,
+                                          void *stream);
+size_t hlq_noalloc_scratch_bytes(void);
+
 /* Static text for a status code. */
 const char *hlq_status_string(int status);
 
