@@ -23,7 +23,7 @@ import threading
 PER_TENSOR, PER_TOKEN = 0, 1
 RNE, SR = 0, 1
 F32, BF16 = 0, 1
-OP_COMPRESS_ACTIVATION, OP_BACKWARD_GX, OP_BACKWARD_GW = 0, 1, 2
+OP_COMPRESS_ACTIVATION, OP_BACKWARD_GX, OP_BACKWARD_GW, OP_BACKWARD = 0, 1, 2, 3
 DEV_NONFINITE, DEV_TIMEOUT, DEV_BADCODE = 0x1, 0x2, 0x4
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -37,6 +37,7 @@ EXPORTS = [
     "hlq_trace_begin", "hlq_trace_end", "hlq_trace_get", "hlq_trace_free",
     "hlq_debug_reference_gemm", "hlq_debug_tc_gemm", "hlq_debug_tc_gemm_ws_bytes",
     "hlq_linear_backward_gx_noalloc", "hlq_noalloc_scratch_bytes",
+    "hlq_linear_backward",
 ]
 
 _lock = threading.Lock()
@@ -92,6 +93,8 @@ def lib() -> ctypes.CDLL:
             "hlq_linear_backward_gx_noalloc": (i32, [P, P, i32, i64, i64, i64, i32,
                                                      i32, i32, i32, u64, P, P]),
             "hlq_noalloc_scratch_bytes": (sz, []),
+            "hlq_linear_backward": (i32, [P, P, P, P, i32, i64, i64, i64, i32, i32,
+                                          i32, i32, i32, u64, P, P, P, sz, P]),
             "hlq_trace_end": (i32, [P]),
             "hlq_trace_get": (i32, [i32, P, P]),
             "hlq_trace_free": (i32, []),
@@ -242,6 +245,32 @@ def hlq_linear_backward_gx_noalloc(g_y, w, gran_gy: int = PER_TOKEN,
         gran_w, rnd, seed, _ptr(out), _stream(stream)),
         "hlq_linear_backward_gx_noalloc")
     return out
+
+
+def hlq_linear_backward(g_y, w, xbar, xbar_scale, rank: int = 8,
+                        gran_gy: int = PER_TOKEN, gran_w: int = PER_TENSOR,
+                        rnd: int = SR, seed: int = 0, block: int = 16,
+                        out_gx=None, out_gw=None, ws=None, stream=None):
+    """Both gradients of the layer, the g_x and g_w branches overlapped on
+    the GPU: returns (g_x [T, Cin], g_w [Cout, Cin]) fp32."""
+    torch = _torch()
+    _need_cuda_contig(g_y, w, xbar, xbar_scale)
+    T, Cout = g_y.shape
+    Cin = w.shape[1]
+    if w.shape[0] != Cout or g_y.dtype != w.dtype or xbar.shape[0] != Cin:
+        raise ValueError("shape/dtype mismatch between g_y, w and xbar")
+    if out_gx is None:
+        out_gx = torch.empty((T, Cin), dtype=torch.float32, device=g_y.device)
+    if out_gw is None:
+        out_gw = torch.empty((Cout, Cin), dtype=torch.float32, device=g_y.device)
+    if ws is None:
+        ws = workspace(OP_BACKWARD, T, Cin, Cout, block, rank, g_y.device)
+    _check(lib().hlq_linear_backward(
+        _ptr(g_y), _ptr(w), _ptr(xbar), _ptr(xbar_scale), _dtype_code(g_y), T,
+        Cin, Cout, block, rank, gran_gy, gran_w, rnd, seed, _ptr(out_gx),
+        _ptr(out_gw), _ptr(ws), ws.numel(), _stream(stream)),
+        "hlq_linear_backward")
+    return out_gx, out_gw
 
 
 def hlq_debug_gx_parts(g_y, w, gran_gy=PER_TOKEN, gran_w=PER_TENSOR, rnd=SR,

@@ -65,6 +65,22 @@ inline void trace_after(const char* what, cudaStream_t s) {
   }
 }
 
+// Auxiliary stream per device for hlq_linear_backward's g_w branch.
+cudaStream_t g_aux_stream[kMaxDevices] = {};
+
+cudaStream_t aux_stream() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    return nullptr;
+  if (!g_aux_stream[dev]) {
+    cudaStream_t st = nullptr;
+    if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess)
+      return nullptr;
+    g_aux_stream[dev] = st;
+  }
+  return g_aux_stream[dev];
+}
+
 constexpr size_t kAlign = 256;
 inline size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
@@ -160,7 +176,7 @@ hlq_status gx_impl(const void* gy, const void* w, int dt, int64_t T,
                    int gran_w, int rnd, uint64_t seed, float* gx, void* ws,
                    size_t ws_bytes, int8_t* dbg_qgy, float* dbg_sgy,
                    int8_t* dbg_qw, float* dbg_sw, int32_t* dbg_acc,
-                   void* stream) {
+                   void* stream, bool validate_only = false) {
   hlq_status st = check_common(dt, T, Cin, Cout, block);
   if (st != HLQ_OK) return st;
   if (gran_gy != HLQ_PER_TENSOR && gran_gy != HLQ_PER_TOKEN) return HLQ_ERR_INVALID_ARG;
@@ -177,6 +193,7 @@ hlq_status gx_impl(const void* gy, const void* w, int dt, int64_t T,
   const GxLayout L = gx_layout(T, Cin, Cout);
   if (!ws || ws_bytes < L.total) return HLQ_ERR_WORKSPACE;
   if (!aligned256(ws)) return HLQ_ERR_ALIGN;
+  if (validate_only) return HLQ_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (n_gx == 0) return HLQ_OK;
   if (Cout == 0) {  // empty contraction: g_x = 0
@@ -228,7 +245,7 @@ hlq_status gw_impl(const void* gy, int dt, const int8_t* xbar,
                    const float* xscale, int64_t T, int64_t Cin, int64_t Cout,
                    int block, int rank, float* gw, void* ws, size_t ws_bytes,
                    int8_t* dbg_qg, float* dbg_sg, int32_t* dbg_acc,
-                   void* stream) {
+                   void* stream, bool validate_only = false) {
   hlq_status st = check_common(dt, T, Cin, Cout, block);
   if (st != HLQ_OK) return st;
   if (!rank_ok(rank)) return HLQ_ERR_INVALID_ARG;
@@ -243,6 +260,7 @@ hlq_status gw_impl(const void* gy, int dt, const int8_t* xbar,
   const GwLayout L = gw_layout(T, Cin, Cout, rank);
   if (!ws || ws_bytes < L.total) return HLQ_ERR_WORKSPACE;
   if (!aligned256(ws)) return HLQ_ERR_ALIGN;
+  if (validate_only) return HLQ_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (n_gw == 0) return HLQ_OK;
   if (Tp == 0) {  // no tokens: g_w = 0
@@ -309,6 +327,9 @@ size_t hlq_workspace_bytes(int op, int64_t T, int64_t Cin, int64_t Cout,
       return gx_layout(T, Cin, Cout).total;
     case HLQ_OP_BACKWARD_GW:
       return gw_layout(T, Cin, Cout, rank_ok(rank) ? rank : 16).total;
+    case HLQ_OP_BACKWARD:
+      return gx_layout(T, Cin, Cout).total +
+             gw_layout(T, Cin, Cout, rank_ok(rank) ? rank : 16).total;
     default:
       return 0;
   }
@@ -344,6 +365,58 @@ hlq_status hlq_compress_activation(const void* d_x, int dt, int64_t T,
              launch_hla(d_x, bf16, T, Cin, rank, false, false, amax, d_xbar, Tp,
                         d_xbar_scale, status, s));
   return HLQ_OK;
+}
+
+hlq_status hlq_linear_backward(const void* d_gy, const void* d_w, const int8_t* d_xbar,
+                               const float* d_xbar_scale, int dt, int64_t T,
+                               int64_t Cin, int64_t Cout, int block, int rank,
+                               int gran_gy, int gran_w, int rnd, uint64_t seed,
+                               float* d_gx, float* d_gw, void* d_ws, size_t ws_bytes,
+                               void* stream) {
+  hlq_status st = check_common(dt, T, Cin, Cout, block);
+  if (st != HLQ_OK) return st;
+  if (!rank_ok(rank)) return HLQ_ERR_INVALID_ARG;
+  const size_t gx_bytes = gx_layout(T, Cin, Cout).total;
+  const size_t gw_bytes = gw_layout(T, Cin, Cout, rank).total;
+  if (!d_ws || ws_bytes < gx_bytes + gw_bytes) return HLQ_ERR_WORKSPACE;
+  if (!aligned256(d_ws)) return HLQ_ERR_ALIGN;
+  uint8_t* base = static_cast<uint8_t*>(d_ws);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaStream_t a = aux_stream();
+  if (!a) return HLQ_ERR_CUDA;
+  // validate both branches before forking (nothing enqueued on failure)
+  st = gw_impl(d_gy, dt, d_xbar, d_xbar_scale, T, Cin, Cout, block, rank, d_gw,
+               base + gx_bytes, gw_bytes, nullptr, nullptr, nullptr, nullptr,
+               /*validate_only=*/true);
+  if (st != HLQ_OK) return st;
+  st = gx_impl(d_gy, d_w, dt, T, Cin, Cout, block, gran_gy, gran_w, rnd, seed, d_gx,
+               base, gx_bytes, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
+               /*validate_only=*/true);
+  if (st != HLQ_OK) return st;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  if (cudaEventCreateWithFlags(&fork, cudaEventDisableTiming) != cudaSuccess)
+    return HLQ_ERR_CUDA;
+  if (cudaEventCreateWithFlags(&join, cudaEventDisableTiming) != cudaSuccess) {
+    cudaEventDestroy(fork);
+    return HLQ_ERR_CUDA;
+  }
+  hlq_status r = HLQ_OK;
+  if (cudaEventRecord(fork, s) != cudaSuccess || cudaStreamWaitEvent(a, fork, 0) != cudaSuccess)
+    r = HLQ_ERR_CUDA;
+  if (r == HLQ_OK)  // g_w branch on the auxiliary stream
+    r = gw_impl(d_gy, dt, d_xbar, d_xbar_scale, T, Cin, Cout, block, rank, d_gw,
+                base + gx_bytes, gw_bytes, nullptr, nullptr, nullptr, a, false);
+  if (r == HLQ_OK)  // g_x branch on the caller's stream
+    r = gx_impl(d_gy, d_w, dt, T, Cin, Cout, block, gran_gy, gran_w, rnd, seed, d_gx,
+                base, gx_bytes, nullptr, nullptr, nullptr, nullptr, nullptr, stream,
+                false);
+  // join even after a failure, so the caller's stream never runs ahead of
+  // work already enqueued on the auxiliary stream
+  if (cudaEventRecord(join, a) != cudaSuccess || cudaStreamWaitEvent(s, join, 0) != cudaSuccess)
+    r = HLQ_ERR_CUDA;
+  cudaEventDestroy(fork);
+  cudaEventDestroy(join);
+  return r;
 }
 
 hlq_status hlq_linear_backward_gx(const void* d_gy, const void* d_w, int dt,

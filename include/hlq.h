@@ -67,7 +67,8 @@ typedef enum { HLQ_RNE = 0, HLQ_SR = 1 } hlq_round;
 typedef enum {
     HLQ_OP_COMPRESS_ACTIVATION = 0,
     HLQ_OP_BACKWARD_GX = 1,
-    HLQ_OP_BACKWARD_GW = 2
+    HLQ_OP_BACKWARD_GW = 2,
+    HLQ_OP_BACKWARD = 3 /* hlq_linear_backward: both gradients */
 } hlq_op;
 
 /* Device status flags (hlq_read_device_status). */
@@ -134,6 +135,23 @@ hlq_status hlq_linear_backward_gw(const void *d_gy, int dt, const int8_t *d_xbar
                                   int64_t Cin, int64_t Cout, int block,
                                   int rank, float *d_gw, void *d_ws,
                                   size_t ws_bytes, void *stream);
+
+/*
+ * The whole backward pass of the layer: g_x exactly as hlq_linear_backward_gx
+ * and g_w exactly as hlq_linear_backward_gw, with the two independent
+ * branches overlapped on the GPU.  The g_w branch runs on an auxiliary
+ * stream of the library (one per device, created on first use) forked from
+ * and joined back into `stream` with events, so all work is still ordered
+ * after what precedes the call on `stream` and before what follows it.
+ * Workspace: hlq_workspace_bytes(HLQ_OP_BACKWARD, ...).  Arguments are the
+ * union of the two calls'.
+ */
+hlq_status hlq_linear_backward(const void *d_gy, const void *d_w, const int8_t *d_xbar,
+                               const float *d_xbar_scale, int dt, int64_t T,
+                               int64_t Cin, int64_t Cout, int block, int rank,
+                               int gran_gy, int gran_w, int rnd, uint64_t seed,
+                               float *d_gx, float *d_gw, void *d_ws, size_t ws_bytes,
+                               void *stream);
 
 /*
  * hlq_linear_backward_gx with its intermediates copied out, for bit-exact

@@ -269,3 +269,22 @@ def test_gw_accumulator_exact_beyond_2_24():
     r = hlq.hlq_debug_gw_parts(to_dev(inp, "g_y", "f32"), xbar, s, rank=rank)
     acc = host(r["acc"])
     assert acc[0, 0] == 127 * 127 * Tp and acc[5, 5] == 127 * 127 * Tp
+
+
+@pytest.mark.parametrize("idx", [0, 1, 4])
+def test_combined_backward_matches_separate_calls(idx):
+    """hlq_linear_backward (g_w branch forked onto a second stream) gives
+    bit-identical g_x and g_w to the two separate entry points, and its
+    output is ordered before later work on the caller's stream."""
+    wl = workloads.WORKLOADS[idx]
+    inp = workloads.make_inputs(wl, T=min(wl.T, 1024))
+    x, gy, w = (to_dev(inp, n, wl.dtype) for n in ("x", "g_y", "w"))
+    xbar, sx = hlq.hlq_compress_activation(x, rank=wl.rank)
+    gx1 = hlq.hlq_linear_backward_gx(gy, w, gran_gy=wl.gran_gy, seed=3)
+    gw1 = hlq.hlq_linear_backward_gw(gy, xbar, sx, rank=wl.rank)
+    for _ in range(2):
+        gx2, gw2 = hlq.hlq_linear_backward(gy, w, xbar, sx, rank=wl.rank,
+                                           gran_gy=wl.gran_gy, seed=3)
+        total = gw2.sum() + gx2.sum()   # consumes the outputs on the same stream
+        assert torch.equal(gx1, gx2) and torch.equal(gw1, gw2)
+        assert torch.isfinite(total)
