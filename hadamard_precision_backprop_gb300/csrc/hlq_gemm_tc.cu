@@ -14,8 +14,8 @@
 // int32 registers (49 * K < 2^24 lets the E4M3 path use one chunk; the bf16
 // path uses chunks of 16 k-blocks = 1024 codes, 1024 * 127^2 < 2^24).
 //
-// CTA layout (one 128 x BN output tile; optional split of the K range over
-// gridDim.z, reduced exactly in int32 through a workspace):
+// CTA layout (persistent over 128 x BN output tiles, each optionally split
+// along K with an exact int32 reduction through a workspace):
 //   warp 0      TMA producer (one lane): A and B k-blocks of 128 bytes per
 //               row into a kStages ring of 128B-swizzled smem tiles;
 //   warp 1      TMEM allocator and MMA issuer (one lane), 4 MMAs per k-block
@@ -181,13 +181,17 @@ struct TcCfg {
   static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + 256;
 };
 
+// Persistent: CTA b processes work units b, b + gridDim.x, ... where a unit
+// is (output tile, K split).  The TMA producer and the MMA issuer run through
+// their units without pausing between tiles; a unit's epilogue (stores, or
+// exact int32 atomics for a split unit) overlaps the next unit's MMAs.
 template <int kKind, int BN>
 __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(
     const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-    int M, int N, int num_kb, int chunk_kb, int kb_per_split,
-    const float* __restrict__ sa, int per_row_a, const float* __restrict__ sb,
-    float* __restrict__ out, int32_t* __restrict__ acc_out,
-    int32_t* __restrict__ split_acc, unsigned int* __restrict__ tile_count,
+    int M, int N, int num_kb, int chunk_kb, int kb_per_split, int splits, int tiles_n,
+    int num_units, const float* __restrict__ sa, int per_row_a,
+    const float* __restrict__ sb, float* __restrict__ out, int32_t* __restrict__ acc_out,
+    int32_t* __restrict__ split_acc, unsigned int* __restrict__ slab_count,
     unsigned int* __restrict__ status) {
   using C = TcCfg<BN>;
   extern __shared__ uint8_t smem_raw[];
@@ -199,14 +203,8 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(
   uint64_t* tempty = tfull + 2;       // [2]
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(tempty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
-  int* last_flag = const_cast<int*>(abort_flag) + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m0 = blockIdx.y * kBM, n0 = blockIdx.x * BN;
-  const int kb_begin = blockIdx.z * kb_per_split;
-  const int kb_end = min(num_kb, kb_begin + kb_per_split);
-  const int my_kb = max(0, kb_end - kb_begin);
-  const int num_chunks = (my_kb + chunk_kb - 1) / chunk_kb;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -218,7 +216,6 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(
       mbar_init(&tempty[b], C::kEpiWarps);
     }
     *abort_flag = 0;
-    *last_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
@@ -234,6 +231,15 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
 
+  // unit -> (m0, n0, first k-block, k-blocks)
+  auto unit_coords = [&](int u, int& m0, int& n0, int& kb0, int& nkb) {
+    const int t = u / splits, z = u - t * splits;
+    m0 = (t / tiles_n) * kBM;
+    n0 = (t % tiles_n) * BN;
+    kb0 = z * kb_per_split;
+    nkb = max(0, min(num_kb, kb0 + kb_per_split) - kb0);
+  };
+
   if (warp == 0) {
     if (lane == 0) {
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA))
@@ -241,22 +247,25 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB))
                    : "memory");
       const int elems = kRowBytes / (kKind == 1 ? 2 : 1);
-      int issued = 0;
-      for (int i = 0; i < my_kb; ++i) {
-        const int s = i % kStages;
-        const uint32_t ph = (uint32_t)(i / kStages) & 1u;
-        if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, status)) break;
-        mbar_expect_tx(&full[s], C::kStageBytes);
-        uint8_t* a = smem + s * C::kStageBytes;
-        const int kx = (kb_begin + i) * elems;
-        tma_load_2d(a, &tmA, &full[s], kx, m0);
-        tma_load_2d(a + C::kABytes, &tmB, &full[s], kx, n0);
-        ++issued;
+      int i = 0;  // k-blocks issued by this CTA so far
+      for (int u = blockIdx.x; u < num_units && !*abort_flag; u += gridDim.x) {
+        int m0, n0, kb0, nkb;
+        unit_coords(u, m0, n0, kb0, nkb);
+        for (int j = 0; j < nkb; ++j, ++i) {
+          const int s = i % kStages;
+          const uint32_t ph = (uint32_t)(i / kStages) & 1u;
+          if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, status)) break;
+          mbar_expect_tx(&full[s], C::kStageBytes);
+          uint8_t* a = smem + s * C::kStageBytes;
+          const int kx = (kb0 + j) * elems;
+          tma_load_2d(a, &tmA, &full[s], kx, m0);
+          tma_load_2d(a + C::kABytes, &tmB, &full[s], kx, n0);
+        }
       }
       if (*abort_flag) {  // let the copies already issued land before exit
-        for (int i = max(0, issued - kStages); i < issued; ++i) {
+        for (int k = max(0, i - kStages); k < i; ++k) {
           const unsigned long long t0 = now_ns();
-          while (!mbar_test(&full[i % kStages], (uint32_t)(i / kStages) & 1u) &&
+          while (!mbar_test(&full[k % kStages], (uint32_t)(k / kStages) & 1u) &&
                  now_ns() - t0 < kWaitNs) {
           }
         }
@@ -265,35 +274,40 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t idesc = make_idesc(kKind, kBM, BN);
-      int i = 0;
+      int i = 0, cc = 0;  // k-blocks and accumulation chunks consumed so far
       bool ok = true;
-      for (int c = 0; c < num_chunks && ok; ++c) {
-        const int buf = c & 1;
-        const uint32_t use = (uint32_t)(c >> 1);
-        if (!mbar_wait(&tempty[buf], (use & 1u) ^ 1u, abort_flag, status)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t d = tmem_base + (uint32_t)(buf * BN);
-        const int i_end = min(my_kb, i + chunk_kb);
-        for (int j = 0; i < i_end; ++i, ++j) {
-          const int s = i % kStages;
-          const uint32_t ph = (uint32_t)(i / kStages) & 1u;
-          if (!mbar_wait(&full[s], ph, abort_flag, status)) {
+      for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+        int m0, n0, kb0, nkb;
+        unit_coords(u, m0, n0, kb0, nkb);
+        const int nch = (nkb + chunk_kb - 1) / chunk_kb;
+        for (int c = 0, j = 0; c < nch && ok; ++c, ++cc) {
+          const int buf = cc & 1;
+          const uint32_t use = (uint32_t)(cc >> 1);
+          if (!mbar_wait(&tempty[buf], (use & 1u) ^ 1u, abort_flag, status)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a = saddr(smem + s * C::kStageBytes);
-          const uint32_t b = a + C::kABytes;
+          const uint32_t d = tmem_base + (uint32_t)(buf * BN);
+          const int j_end = min(nkb, j + chunk_kb);
+          for (int jj = 0; j < j_end; ++j, ++jj, ++i) {
+            const int s = i % kStages;
+            const uint32_t ph = (uint32_t)(i / kStages) & 1u;
+            if (!mbar_wait(&full[s], ph, abort_flag, status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a = saddr(smem + s * C::kStageBytes);
+            const uint32_t b = a + C::kABytes;
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_issue<kKind>(d, sw128_desc(a + 32 * k), sw128_desc(b + 32 * k), idesc,
-                             (j > 0 || k > 0) ? 1u : 0u);
-          mma_commit(&empty[s]);
+            for (int k = 0; k < 4; ++k)
+              mma_issue<kKind>(d, sw128_desc(a + 32 * k), sw128_desc(b + 32 * k), idesc,
+                               (jj > 0 || k > 0) ? 1u : 0u);
+            mma_commit(&empty[s]);
+          }
+          if (ok) mma_commit(&tfull[buf]);
         }
-        if (ok) mma_commit(&tfull[buf]);
       }
     }
   } else {
@@ -302,79 +316,90 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(
     const int quarter = warp & 3;  // TMEM lanes this warp may access
     const int colgrp = ew >> 2;
     const int row = quarter * 32 + lane;
-    int32_t acc[C::kColsPerThread];
-#pragma unroll
-    for (int i = 0; i < C::kColsPerThread; ++i) acc[i] = 0;
+    int cc = 0;
     bool ok = true;
-    for (int c = 0; c < num_chunks; ++c) {
-      const int buf = c & 1;
-      const uint32_t use = (uint32_t)(c >> 1);
-      ok = mbar_wait(&tfull[buf], use & 1u, abort_flag, status);
-      ok = __all_sync(0xffffffffu, ok);  // also reconverges the warp
-      if (!ok) break;
-      tc_fence_after();
-      const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) +
-                             (uint32_t)(buf * BN + colgrp * C::kColsPerThread);
+    for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+      int m0, n0, kb0, nkb;
+      unit_coords(u, m0, n0, kb0, nkb);
+      const int nch = (nkb + chunk_kb - 1) / chunk_kb;
+      int32_t acc[C::kColsPerThread];
 #pragma unroll
-      for (int j = 0; j < C::kColsPerThread / 32; ++j) {
-        uint32_t r[32];
-        tmem_ld_x32(taddr + 32 * j, r);
+      for (int q = 0; q < C::kColsPerThread; ++q) acc[q] = 0;
+      for (int c = 0; c < nch; ++c, ++cc) {
+        const int buf = cc & 1;
+        const uint32_t use = (uint32_t)(cc >> 1);
+        ok = mbar_wait(&tfull[buf], use & 1u, abort_flag, status);
+        ok = __all_sync(0xffffffffu, ok);  // also reconverges the warp
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) +
+                               (uint32_t)(buf * BN + colgrp * C::kColsPerThread);
 #pragma unroll
-        for (int q = 0; q < 32; ++q) acc[32 * j + q] += __float2int_rn(__uint_as_float(r[q]));
+        for (int jc = 0; jc < C::kColsPerThread / 32; ++jc) {
+          uint32_t r[32];
+          tmem_ld_x32(taddr + 32 * jc, r);
+#pragma unroll
+          for (int q = 0; q < 32; ++q)
+            acc[32 * jc + q] += __float2int_rn(__uint_as_float(r[q]));
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[buf]);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[buf]);
-    }
-    const int m = m0 + row;
-    const int nb = n0 + colgrp * C::kColsPerThread;
-    if (ok && gridDim.z > 1) {
-      // split K: add this CTA's exact partial into the int32 workspace tile
+      if (!ok) break;
+      const int m = m0 + row;
+      const int nb = n0 + colgrp * C::kColsPerThread;
+      if (splits == 1) {
+        if (m < M) {
+          const float scale =
+              out ? (per_row_a ? sa[m] : sa[0]) * sb[0] * 0.0625f : 0.0f;
+          float* orow = out + (size_t)m * N;
+#pragma unroll
+          for (int q = 0; q < C::kColsPerThread; q += 4) {
+            const int n = nb + q;
+            if (n + 4 <= N) {
+              if (out)
+                *reinterpret_cast<float4*>(orow + n) =
+                    make_float4((float)acc[q] * scale, (float)acc[q + 1] * scale,
+                                (float)acc[q + 2] * scale, (float)acc[q + 3] * scale);
+              if (acc_out)
+                *reinterpret_cast<int4*>(acc_out + (size_t)m * N + n) =
+                    make_int4(acc[q], acc[q + 1], acc[q + 2], acc[q + 3]);
+            }
+          }
+        }
+        continue;
+      }
+      // split unit: add the exact partial; the warp that completes a slab
+      // (its 32 rows x kColsPerThread columns) last dequantizes it
       if (m < M) {
 #pragma unroll
         for (int q = 0; q < C::kColsPerThread; ++q)
           if (nb + q < N) atomicAdd(&split_acc[(size_t)m * N + nb + q], acc[q]);
       }
-    }
-    if (ok && gridDim.z == 1 && m < M) {
-      const float scale = out ? (per_row_a ? sa[m] : sa[0]) * sb[0] * 0.0625f : 0.0f;
-      float* orow = out + (size_t)m * N;
-#pragma unroll
-      for (int q = 0; q < C::kColsPerThread; q += 4) {
-        const int n = nb + q;
-        if (n + 4 <= N) {
-          if (out)
-            *reinterpret_cast<float4*>(orow + n) =
-                make_float4((float)acc[q] * scale, (float)acc[q + 1] * scale,
-                            (float)acc[q + 2] * scale, (float)acc[q + 3] * scale);
-          if (acc_out)
-            *reinterpret_cast<int4*>(acc_out + (size_t)m * N + n) =
-                make_int4(acc[q], acc[q + 1], acc[q + 2], acc[q + 3]);
-        }
-      }
-    }
-  }
-
-  // ---- split K: the last CTA of a tile dequantizes the summed tile ----
-  if (gridDim.z > 1) {
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0 && !*abort_flag) {
-      const unsigned int t = blockIdx.y * gridDim.x + blockIdx.x;
-      const unsigned int prev = atomicAdd(&tile_count[t], 1u);
-      *last_flag = (prev == gridDim.z - 1) ? 1 : 0;
-    }
-    __syncthreads();
-    if (*last_flag) {
       __threadfence();
-      const int rows = min(kBM, M - m0), cols = min(BN, N - n0);
-      const float scale_t = out ? sb[0] * 0.0625f : 0.0f;
-      for (int idx = threadIdx.x; idx < rows * cols; idx += blockDim.x) {
-        const int r = idx / cols, cc = idx % cols;
-        const int m = m0 + r, n = n0 + cc;
-        const int32_t v = __ldcg(&split_acc[(size_t)m * N + n]);
-        if (out) out[(size_t)m * N + n] = (float)v * ((per_row_a ? sa[m] : sa[0]) * scale_t);
-        if (acc_out) acc_out[(size_t)m * N + n] = v;
+      __syncwarp();
+      unsigned int last = 0;
+      if (lane == 0) {
+        const int t = u / splits;
+        last = atomicAdd(&slab_count[(size_t)t * C::kEpiWarps + ew], 1u) ==
+               (unsigned int)(splits - 1);
+      }
+      last = __shfl_sync(0xffffffffu, last, 0);
+      if (last && m < M) {
+        __threadfence();
+        const float scale = out ? (per_row_a ? sa[m] : sa[0]) * sb[0] * 0.0625f : 0.0f;
+        for (int q = 0; q < C::kColsPerThread; q += 4) {
+          const int n = nb + q;
+          if (n + 4 <= N) {
+            const int4 v = __ldcg(reinterpret_cast<const int4*>(split_acc + (size_t)m * N + n));
+            if (out)
+              *reinterpret_cast<float4*>(out + (size_t)m * N + n) =
+                  make_float4((float)v.x * scale, (float)v.y * scale, (float)v.z * scale,
+                              (float)v.w * scale);
+            if (acc_out) *reinterpret_cast<int4*>(acc_out + (size_t)m * N + n) = v;
+          }
+        }
       }
     }
   }
@@ -428,9 +453,9 @@ bool make_map(CUtensorMap* map, const void* ptr, bool bf16, int64_t rows, int64_
 
 template <int kKind, int BN>
 cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, int64_t M, int64_t N,
-                      int num_kb, int chunk_kb, int splits, const float* sa,
+                      int num_kb, int chunk_kb, int splits, int num_sms, const float* sa,
                       bool per_row_a, const float* sb, float* out, int32_t* acc_out,
-                      int32_t* split_acc, unsigned int* tile_count,
+                      int32_t* split_acc, unsigned int* slab_count,
                       unsigned int* status, cudaStream_t st) {
   using C = TcCfg<BN>;
   static bool attr_set[64] = {};
@@ -445,19 +470,24 @@ cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, int64_t M, int
     attr_set[dev] = true;
   }
   const int kb_per_split = (num_kb + splits - 1) / splits;
-  dim3 grid((unsigned)((N + BN - 1) / BN), (unsigned)((M + kBM - 1) / kBM),
-            (unsigned)splits);
+  const int tiles_n = (int)((N + BN - 1) / BN);
+  const int64_t tiles = ((M + kBM - 1) / kBM) * tiles_n;
+  const int64_t units = tiles * splits;
+  if (units > 0x7fffffff) return cudaErrorInvalidValue;
+  const int grid = (int)(units < num_sms ? units : num_sms);
   gemm_tc_kernel<kKind, BN><<<grid, C::kThreads, C::kSmem, st>>>(
-      a, b, (int)M, (int)N, num_kb, chunk_kb, kb_per_split, sa, per_row_a ? 1 : 0, sb,
-      out, acc_out, split_acc, tile_count, status);
+      a, b, (int)M, (int)N, num_kb, chunk_kb, kb_per_split, splits, tiles_n, (int)units,
+      sa, per_row_a ? 1 : 0, sb, out, acc_out, split_acc, slab_count, status);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 size_t gemm_tc_split_ws_bytes(int64_t M, int64_t N) {
+  // int32 partial sums, then one counter per (tile, epilogue warp) slab
+  // (128-wide tiles x 8 slabs covers both tile widths)
   const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + 127) / 128);
-  return (size_t)M * (size_t)N * 4 + (size_t)tiles * 4 + 256;
+  return (size_t)M * (size_t)N * 4 + (size_t)tiles * 8 * 4 + 256;
 }
 
 GemmPlan plan_gemm_tc(int kind, int64_t M, int64_t N, int64_t K, int num_sms,
@@ -499,18 +529,25 @@ cudaError_t launch_gemm_tc(int kind, const void* A, int64_t lda, const void* B,
   if (!make_map(&ma, A, bf16, M, K, lda, kBM)) return cudaErrorInvalidValue;
   if (!make_map(&mb, B, bf16, N, K, ldb, plan.bn)) return cudaErrorInvalidValue;
   int32_t* split_acc = nullptr;
-  unsigned int* tile_count = nullptr;
+  unsigned int* slab_count = nullptr;
   if (plan.splits > 1) {
     split_acc = static_cast<int32_t*>(split_ws);
-    tile_count = reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(split_ws) +
+    slab_count = reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(split_ws) +
                                                  (size_t)M * (size_t)N * 4);
     const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + plan.bn - 1) / plan.bn);
-    cudaError_t e = cudaMemsetAsync(split_ws, 0, (size_t)M * (size_t)N * 4 + (size_t)tiles * 4, st);
+    const int epi_warps = plan.bn / 32;
+    cudaError_t e = cudaMemsetAsync(
+        split_ws, 0, (size_t)M * (size_t)N * 4 + (size_t)tiles * epi_warps * 4, st);
     if (e != cudaSuccess) return e;
   }
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      sms <= 0)
+    return cudaErrorInvalidDevice;
 #define TC(KIND, BN)                                                                  \
-  launch_tc<KIND, BN>(ma, mb, M, N, plan.num_kb, plan.chunk_kb, plan.splits, sa,      \
-                      per_row_a, sb, out, acc_out, split_acc, tile_count, status, st)
+  launch_tc<KIND, BN>(ma, mb, M, N, plan.num_kb, plan.chunk_kb, plan.splits, sms, sa, \
+                      per_row_a, sb, out, acc_out, split_acc, slab_count, status, st)
   if (kind == 0) return plan.bn == 256 ? TC(0, 256) : TC(0, 128);
   return plan.bn == 256 ? TC(1, 256) : TC(1, 128);
 #undef TC

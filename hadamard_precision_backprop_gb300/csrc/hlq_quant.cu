@@ -467,7 +467,7 @@ __device__ __forceinline__ void column_coeffs(float* x, int rank, bool natural,
 
 // Exactness of the two columns of 16 packed bf16 pairs (low half = column
 // 0), by 16-bit SIMD max/min of |bits| as in transform_octet_bf16.
-__device__ __forceinline__ void pair_col_exact_bf16(const uint32_t* p, bool* exact,
+__device__ __forceinline__ void pair_col_exact_bf16(const uint32_t (&p)[16], bool* exact,
                                                     unsigned int* status) {
   uint32_t mx = 0u, mn = 0x7fff7fffu;
 #pragma unroll
@@ -540,9 +540,9 @@ __global__ void __launch_bounds__(256, 2) col_kernel(
     const int64_t b = b0 + bl;
     if (!col_ok || b >= n_blk) continue;
     float v[kCPT][16];
-    if (kBf16) {
+    if constexpr (kBf16) {
       bool exact[2];
-      pair_col_exact_bf16(reinterpret_cast<const uint32_t*>(&raw[half]), exact, status);
+      pair_col_exact_bf16(raw[half].p, exact, status);
       unpack_pair_col<kBf16>(raw[half], v);
 #pragma unroll
       for (int c = 0; c < kCPT; ++c) column_butterfly<kBf16>(v[c], exact[c], R, kHq);
@@ -642,6 +642,107 @@ __global__ void __launch_bounds__(256, 2) col_kernel(
       const int64_t c = col_base + col_tile_col(r);
       if (c < cols) outb[c * row_bytes + off + by] = smem[(size_t)r * row_stride + by];
     }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// HQ of w [Cout, Cin] along Cout (blocks of 16 rows), codes written
+// transposed [Cin, Cout].  w is small next to g_y, so the kernel trades
+// redundant transforms for parallelism: thread (tx, ty) owns column pair tx
+// (64 columns per CTA), block ty / 2 (4 blocks per CTA) and quantizes half
+// of its 16 coefficients (ty % 2), drawing one Philox block per coefficient
+// row for the pair.
+// ---------------------------------------------------------------------------
+constexpr int kWCols = 64;
+constexpr int kWBlocks = 4;
+constexpr int kWRowStride = kWBlocks * 16 + 8;  // bytes; 9 x 8-byte chunks
+
+template <bool kBf16, int kMode>
+__global__ void __launch_bounds__(256) hq_w_kernel(
+    const void* __restrict__ src, int64_t rows, int64_t cols,
+    unsigned int* __restrict__ amax_slot, uint8_t* __restrict__ codes_t,
+    float* __restrict__ scale, int rnd, uint64_t seed, uint32_t stream,
+    unsigned int* __restrict__ status) {
+  __shared__ __align__(16) uint8_t stage[kWCols * kWRowStride];
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  const int bl = ty >> 1, part = ty & 1;
+  const int64_t c0 = (int64_t)blockIdx.x * kWCols + 2 * tx;
+  const int64_t b = (int64_t)blockIdx.y * kWBlocks + bl;
+  const int64_t n_blk = rows >> 4;
+  const bool ok = c0 < cols && b < n_blk;
+  float v[2][16];
+  if (ok) {
+    RawPairCol<kBf16> raw;
+    load_pair_col<kBf16>(src, 16 * b * cols + c0, cols, raw);
+    if constexpr (kBf16) {
+      bool exact[2];
+      pair_col_exact_bf16(raw.p, exact, status);
+      unpack_pair_col<kBf16>(raw, v);
+      column_butterfly<kBf16>(v[0], exact[0], 16, true);
+      column_butterfly<kBf16>(v[1], exact[1], 16, true);
+    } else {
+      unpack_pair_col<kBf16>(raw, v);
+      column_coeffs<kBf16>(v[0], 16, true, status);
+      column_coeffs<kBf16>(v[1], 16, true, status);
+    }
+  }
+  if (kMode == kAmax) {
+    float amax = 0.0f;
+    if (ok && part == 0) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fmaxf(fabsf(v[0][i]), fabsf(v[1][i])));
+    }
+    amax = warp_max(amax);
+    if (tx == 0) atomic_max_nonneg(amax_slot, amax);
+    return;
+  }
+  const float s = __fdiv_rn(__uint_as_float(*amax_slot), 7.0f);
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) scale[0] = s;
+  if (ok) {
+    const PhiloxKeys keys = philox_keys(seed);
+    const bool hi = (c0 & 2) != 0;
+    float h8[2][8];  // this thread's half of the coefficients (static indexing)
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      h8[0][k] = part ? v[0][8 + k] : v[0][k];
+      h8[1][k] = part ? v[1][8 + k] : v[1][k];
+    }
+    uint32_t w[2][2] = {{0u, 0u}, {0u, 0u}};
+#pragma unroll
+    for (int h = 0; h < 8; h += 2) {
+      float q[2][2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int i = 8 * part + h + u;
+        // element (16b+i, c0+c) of the transformed [rows, cols] tensor
+        U4 r = {0u, 0u, 0u, 0u};
+        if (rnd == HLQ_SR)
+          r = philox_block_k(keys, stream, (uint64_t)((16 * b + i) * cols + c0) >> 2);
+        const uint32_t w0 = hi ? r.z : r.x, w1 = hi ? r.w : r.y;
+        const float y0 = h8[0][h + u], y1 = h8[1][h + u];
+        q[u][0] = rnd == HLQ_SR ? quant_sr_f(y0, s, w0, 7.0f) : quant_rne_f(y0, s, 7.0f);
+        q[u][1] = rnd == HLQ_SR ? quant_sr_f(y1, s, w1, 7.0f) : quant_rne_f(y1, s, 7.0f);
+      }
+#pragma unroll
+      for (int c = 0; c < 2; ++c) w[c][h >> 2] |= e4m3x2(q[0][c], q[1][c]) << (8 * (h & 3));
+    }
+#pragma unroll
+    for (int c = 0; c < 2; ++c)
+      *reinterpret_cast<uint2*>(stage + (c * 32 + tx) * kWRowStride + bl * 16 + part * 8) =
+          make_uint2(w[c][0], w[c][1]);
+  }
+  __syncthreads();
+  // row r of the stage = column tile_base + 2 * (r % 32) + r / 32; its
+  // valid_b blocks of 16 codes go to codes_t[col, 16 * b0 ...]
+  const int64_t b0 = (int64_t)blockIdx.y * kWBlocks;
+  const int valid_b = (int)imin64(kWBlocks, n_blk - b0);
+  const int chunks = valid_b * 2;  // 8-byte chunks per row
+  for (int idx = threadIdx.x; idx < kWCols * chunks; idx += blockDim.x) {
+    const int r = idx / chunks, ch = idx % chunks;
+    const int64_t c = (int64_t)blockIdx.x * kWCols + 2 * (r & 31) + (r >> 5);
+    if (c < cols)
+      *reinterpret_cast<uint2*>(codes_t + c * rows + 16 * b0 + ch * 8) =
+          *reinterpret_cast<const uint2*>(stage + r * kWRowStride + ch * 8);
   }
 }
 
@@ -835,12 +936,17 @@ cudaError_t launch_hq_cols(const void* src, bool bf16, int64_t rows,
                            float* scale, int rnd, uint64_t seed,
                            uint32_t stream_id, unsigned int* status,
                            cudaStream_t st) {
-#define COL(B, M)                                                                   \
-  launch_col<B, M, kColHqE4M3>(src, rows, cols, 16, amax_slot, codes_t, rows, scale, \
-                               rnd, seed, stream_id, status, st)
-  if (amax_only) return bf16 ? COL(true, kAmax) : COL(false, kAmax);
-  return bf16 ? COL(true, kQuant) : COL(false, kQuant);
-#undef COL
+  dim3 grid(grid1(cols, kWCols), grid1(rows / 16, kWBlocks));
+#define HQW(B, M)                                                                  \
+  hq_w_kernel<B, M><<<grid, 256, 0, st>>>(src, rows, cols, amax_slot, codes_t, scale, \
+                                          rnd, seed, stream_id, status)
+  if (amax_only) {
+    if (bf16) HQW(true, kAmax); else HQW(false, kAmax);
+  } else {
+    if (bf16) HQW(true, kQuant); else HQW(false, kQuant);
+  }
+#undef HQW
+  return cudaGetLastError();
 }
 
 cudaError_t launch_hla(const void* src, bool bf16, int64_t T, int64_t C,
