@@ -381,20 +381,41 @@ def hlq_trace_begin(capacity: int = 4096):
     _check(lib().hlq_trace_begin(capacity), "hlq_trace_begin")
 
 
-def hlq_trace_end():
-    """Stop tracing; return [(kernel name, ms), ...] in launch order."""
+_trace_n = 0
+
+
+def hlq_trace_end(keep: bool = False):
+    """Stop tracing; return [(kernel name, ms), ...] in launch order.  With
+    keep=True return the number of traced launches and keep the events
+    alive (for graph replays: hlq_trace_read() after each replay, then
+    hlq_trace_free())."""
+    global _trace_n
     L = lib()
     n = ctypes.c_int(0)
     _check(L.hlq_trace_end(ctypes.byref(n)), "hlq_trace_end")
+    _trace_n = n.value
+    if keep:
+        return _trace_n
+    out = hlq_trace_read()
+    L.hlq_trace_free()
+    return out
+
+
+def hlq_trace_read():
+    """Per-launch (name, ms) of the last recording of the traced launches."""
+    L = lib()
     out = []
-    for i in range(n.value):
+    for i in range(_trace_n):
         name = ctypes.c_char_p()
         ms = ctypes.c_float()
         _check(L.hlq_trace_get(i, ctypes.byref(name), ctypes.byref(ms)),
                "hlq_trace_get")
         out.append((name.value.decode(), float(ms.value)))
-    L.hlq_trace_free()
     return out
+
+
+def hlq_trace_free():
+    lib().hlq_trace_free()
 
 
 def hlq_read_device_status(clear: bool = False, stream=None) -> int:

@@ -53,13 +53,16 @@ void trace_free() {
   g_trace = Trace{};
 }
 
+// External records: inside a stream capture they become event-record nodes
+// of the graph, re-recorded at every replay (outside a capture the flag
+// changes nothing).
 inline void trace_before(cudaStream_t s) {
   if (g_trace.on && g_trace.n < g_trace.cap)
-    cudaEventRecord(g_trace.ev[2 * g_trace.n], s);
+    cudaEventRecordWithFlags(g_trace.ev[2 * g_trace.n], s, cudaEventRecordExternal);
 }
 inline void trace_after(const char* what, cudaStream_t s) {
   if (g_trace.on && g_trace.n < g_trace.cap) {
-    cudaEventRecord(g_trace.ev[2 * g_trace.n + 1], s);
+    cudaEventRecordWithFlags(g_trace.ev[2 * g_trace.n + 1], s, cudaEventRecordExternal);
     g_trace.name[g_trace.n] = what;
     ++g_trace.n;
   }

@@ -406,4 +406,19 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
+// Max over the CTA (every thread calls it; blockDim.x a multiple of 32, at
+// most 1024), then one atomicMax per CTA into `slot`.
+__device__ __forceinline__ void cta_max_to_slot(float v, unsigned int* slot) {
+  __shared__ float partial[32];
+  v = warp_max(v);
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  if (lane == 0) partial[w] = v;
+  __syncthreads();
+  if (w == 0) {
+    float m = lane < (int)(blockDim.x >> 5) ? partial[lane] : 0.0f;
+    m = warp_max(m);
+    if (lane == 0) atomic_max_nonneg(slot, m);
+  }
+}
+
 }  // namespace hlq

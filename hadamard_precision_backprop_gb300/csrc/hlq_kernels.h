@@ -3,6 +3,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "hlq.h"
@@ -67,6 +68,11 @@ cudaError_t launch_gemm_simple(const void* A, int fmtA, const void* B,
                                const float* sa, bool per_row_a,
                                const float* sb, float* out, int32_t* acc_out,
                                cudaStream_t st);
+
+// A TMA tensor map over a row-major [rows, cols] bf16 / fp32 matrix with
+// boxes of box_rows x box_cols, no swizzle, zero fill outside the matrix.
+bool make_tile_map_2d(CUtensorMap* map, const void* ptr, bool bf16, int64_t rows,
+                      int64_t cols, int box_cols, int box_rows);
 
 // Tensor-core GEMM (hlq_gemm_tc.cu).  kind 0: E4M3 operands (int4 codes),
 // kind 1: bf16 operands (int8 codes).  A [M, K] (row stride lda elements),

@@ -8,10 +8,10 @@
 //                   Transform" and "Alternative Optimization Technique:
 //                   Hadamard Quantization"; HOT, Approach (layer-wise
 //                   quantizer selection).
-//  col_kernel     : HQ of w [Cout, Cin] along Cout (blocks of 16 rows),
+//  hq_w_kernel    : HQ of w [Cout, Cin] along Cout (blocks of 16 rows),
 //                   written transposed [Cin, Cout] so the contraction dim is
 //                   contiguous for the GEMM.
-//  col_kernel     : HLA along tokens (16-token blocks, the `rank` lowest-
+//  hla_kernel     : HLA along tokens (16-token blocks, the `rank` lowest-
 //                   sequency Walsh rows kept), per-tensor int8 codes with
 //                   round-to-nearest-even, written [C, T'] (token dim
 //                   contiguous).  "HLQ ...", section "Analysis on Hadamard
@@ -32,6 +32,7 @@
 
 #include "hlq_device.cuh"
 #include "hlq_kernels.h"
+#include "hlq_tma.cuh"
 
 namespace hlq {
 
@@ -79,31 +80,55 @@ __device__ __noinline__ void slow_block16(const float* in, float* out, int bf16)
     for (int i = 0; i < 16; ++i) out[i] = exact_sum16(in, hrow_negmask(i));
 }
 
-// Butterfly of one octet in place, given whether its 16-block is exact in the
-// fp32 butterfly (both lanes of the pair agree).  All 32 lanes call this.
+// Butterfly of one octet (the lane pair 2p, 2p+1 holds one 16-block): the
+// fp32 butterfly over lanes, across the pair with one shuffle stage.
+__device__ __forceinline__ void octet_fwht(float* v) {
+  const bool upper = (threadIdx.x & 1) != 0;
+  fwht8(v);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const float o = __shfl_xor_sync(0xffffffffu, v[k], 1);
+    v[k] = upper ? (o - v[k]) : (v[k] + o);
+  }
+}
+
+// Exactly rounded transform of one octet in place.  tier (equal on both
+// lanes of a pair): 0 = the fp32 butterfly is exact (exponent spread <= 12
+// binades for bf16 inputs); 1 = split: values within 12 binades of the
+// block's largest exponent `emax` and the rest are transformed separately
+// (each part is exact) and the two exact results added with one rounding;
+// 2 = out-of-line exact path.  All 32 lanes call this.
 template <bool kBf16>
-__device__ __forceinline__ void octet_butterfly(float* v, bool exact) {
-  const int lane = threadIdx.x & 31;
-  const bool upper = (lane & 1) != 0;
-  // When some block of the warp defeats the fp32 butterfly, gather its 16
-  // inputs first (shuffles stay warp-uniform), then overwrite below.
-  const bool any_slow = !__all_sync(0xffffffffu, exact);
+__device__ __forceinline__ void octet_butterfly(float* v, int tier, uint32_t emax) {
+  const bool upper = (threadIdx.x & 1) != 0;
+  // gather a slow block's 16 inputs first (shuffles stay warp-uniform)
+  const bool any_slow = __any_sync(0xffffffffu, tier == 2);
   float full[16];
   if (any_slow) {
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-      float o = __shfl_xor_sync(0xffffffffu, v[k], 1);
+      const float o = __shfl_xor_sync(0xffffffffu, v[k], 1);
       full[k] = upper ? o : v[k];
       full[8 + k] = upper ? v[k] : o;
     }
   }
-  fwht8(v);
+  if (__any_sync(0xffffffffu, tier == 1)) {
+    float lo[8];
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    float o = __shfl_xor_sync(0xffffffffu, v[k], 1);
-    v[k] = upper ? (o - v[k]) : (v[k] + o);
+    for (int k = 0; k < 8; ++k) {
+      const uint32_t e = max((__float_as_uint(v[k]) >> 23) & 0xffu, 1u);
+      const bool high = tier != 1 || e + 12u >= emax;
+      lo[k] = high ? 0.0f : v[k];
+      v[k] = high ? v[k] : 0.0f;
+    }
+    octet_fwht(v);
+    octet_fwht(lo);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) v[k] += lo[k];  // exact + exact, one rounding
+  } else {
+    octet_fwht(v);
   }
-  if (!exact) {
+  if (tier == 2) {
     float y[16];
     slow_block16(full, y, kBf16 ? 1 : 0);
 #pragma unroll
@@ -111,7 +136,30 @@ __device__ __forceinline__ void octet_butterfly(float* v, bool exact) {
   }
 }
 
-// Transform one octet in place (all 32 lanes must call this together).
+// Tier of a block from its exponent range (emax = largest exponent field,
+// emin = smallest over non-zero values with subnormals as 1, all_zero).
+__device__ __forceinline__ int block_tier_bf16(uint32_t emax, uint32_t emin, bool all_zero) {
+  if (all_zero) return 0;
+  if (emax == 255u) return 2;
+  const uint32_t spread = emax - min(emin, emax);
+  return spread <= 12u ? 0 : (spread <= 25u ? 1 : 2);
+}
+
+// Split of a column for tier 1: x -> (values within 12 binades of emax,
+// the rest).
+__device__ __forceinline__ void split_high_low(const float* x, uint32_t emax, float* hi,
+                                               float* lo) {
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const uint32_t e = max((__float_as_uint(x[j]) >> 23) & 0xffu, 1u);
+    const bool high = e + 12u >= emax;
+    hi[j] = high ? x[j] : 0.0f;
+    lo[j] = high ? 0.0f : x[j];
+  }
+}
+
+// Transform one octet in place (fp32 inputs: the butterfly is never exact
+// for 24-bit significands, so blocks with values take the exact path).
 template <bool kBf16>
 __device__ __forceinline__ void transform_octet(float* v, unsigned int* status) {
   ExpRange er = exp_range_init();
@@ -120,37 +168,34 @@ __device__ __forceinline__ void transform_octet(float* v, unsigned int* status) 
   er.emax = max(er.emax, __shfl_xor_sync(0xffffffffu, er.emax, 1));
   er.emin = min(er.emin, __shfl_xor_sync(0xffffffffu, er.emin, 1));
   if (any_nonfinite(er)) raise_flag(status, HLQ_DEV_NONFINITE);
-  octet_butterfly<kBf16>(v, butterfly_exact<kBf16>(er));
+  octet_butterfly<kBf16>(v, butterfly_exact<kBf16>(er) ? 0 : 2, er.emax);
 }
 
 // The same for eight packed bf16 values: the exponent range comes from
-// two-lane 16-bit SIMD max/min over |bits| (zeros mapped to the largest
-// pattern so that they drop out of the minimum), then the values unpack.
+// 32-bit integer max/min over |bits| (zeros wrap to the largest value under
+// "minus one" and drop out of the minimum), then the values unpack.
 __device__ __forceinline__ void transform_octet_bf16(const uint4& raw, float* v,
                                                      unsigned int* status) {
   const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-  uint32_t mx = 0u, mn = 0x7fff7fffu;
+  uint32_t hi = 0u, lom1 = 0xffffffffu;
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    const uint32_t a = w[k] & 0x7fff7fffu;
-    mx = __vmaxu2(mx, a);
-    mn = __vminu2(mn, a | (__vcmpeq2(a, 0u) & 0x7fff7fffu));
+    const uint32_t a0 = w[k] & 0x7fffu, a1 = (w[k] >> 16) & 0x7fffu;
+    hi = max(hi, max(a0, a1));
+    lom1 = min(lom1, min(a0 - 1u, a1 - 1u));
   }
-  uint32_t hi = max(mx & 0xffffu, mx >> 16);
-  uint32_t lo = min(mn & 0xffffu, mn >> 16);
   hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, 1));
-  lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, 1));
+  lom1 = min(lom1, __shfl_xor_sync(0xffffffffu, lom1, 1));
   const uint32_t emax = hi >> 7;
   if (emax == 255u) raise_flag(status, HLQ_DEV_NONFINITE);
-  const bool all_zero = lo == 0x7fffu;
-  const uint32_t emin = max(lo >> 7, 1u);
-  const bool exact = all_zero || (emax <= 254u && emax - min(emin, emax) <= 12u);
+  const bool all_zero = lom1 == 0xffffffffu;
+  const uint32_t emin = max((lom1 + 1u) >> 7, 1u);
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     v[2 * k] = bf16_lo(w[k]);
     v[2 * k + 1] = bf16_hi(w[k]);
   }
-  octet_butterfly<true>(v, exact);
+  octet_butterfly<true>(v, block_tier_bf16(emax, emin, all_zero), emax);
 }
 
 // Raw octet as loaded from HBM (kept packed while the row sits in registers).
@@ -257,15 +302,34 @@ __global__ void __launch_bounds__(256) hq_rows_kernel(
   const int wid = threadIdx.x >> 5;
   const int warps = blockDim.x >> 5;
   const int64_t row = (int64_t)blockIdx.x * warps + wid;
-  if (row >= rows) return;  // whole warp leaves together
   const int n_oct = (int)(cols >> 3);
   const int iters = (n_oct + 31) >> 5;
   const int64_t base = row * cols;
+  if (kMode == kAmax) {  // per-tensor pre-pass: transform, max, one atomic per CTA
+    float amax = 0.0f;
+    if (row < rows) {  // warp-uniform
+      RawOct<kBf16> cur = load_raw<kBf16>(src, base + lane * 8, lane < n_oct);
+#pragma unroll 1
+      for (int it = 0; it < iters; ++it) {
+        const int nx = it * 32 + lane + 32;
+        RawOct<kBf16> nxt = load_raw<kBf16>(src, base + (int64_t)nx * 8,
+                                            it + 1 < iters && nx < n_oct);
+        float v[8];
+        transform_raw<kBf16>(cur, v, status);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) amax = fmaxf(amax, fabsf(v[k]));
+        cur = nxt;
+      }
+    }
+    cta_max_to_slot(amax, amax_slot);
+    return;
+  }
+  if (row >= rows) return;  // whole warp leaves together
   // staged octet (it, lane): float4 halves at [(2*it + h) * 32 + lane]
   float4* my = srow + (size_t)wid * iters * 64;
 
   float amax = 0.0f;
-  if (kMode == kAmax || kPerToken) {
+  if (kPerToken) {
     RawOct<kBf16> cur = load_raw<kBf16>(src, base + lane * 8, lane < n_oct);
 #pragma unroll 1
     for (int it = 0; it < iters; ++it) {
@@ -284,10 +348,6 @@ __global__ void __launch_bounds__(256) hq_rows_kernel(
       cur = nxt;
     }
     amax = warp_max(amax);
-    if (kMode == kAmax) {
-      if (lane == 0) atomic_max_nonneg(amax_slot, amax);
-      return;
-    }
   } else {
     amax = __uint_as_float(*amax_slot);
   }
@@ -324,20 +384,25 @@ __global__ void __launch_bounds__(256) hq_rows_kernel(
 }
 
 // ---------------------------------------------------------------------------
-// Column transforms: w (HQ along Cout, blocks of 16 rows, all 16 Sylvester
-// rows, int4 codes) and x / g_y (HLA along tokens, blocks of 16 tokens, the
-// `rank` lowest-sequency rows, int8 codes).  Both write [C, X] with the
-// transformed dim contiguous (X = Cout for w, T' for HLA).
-//
-// Thread: kCPT = 2 adjacent columns of one 16-row block (4-byte bf16 /
-// 8-byte fp32 loads, a warp reads 128/256 contiguous bytes per row).  CTA:
-// 32 x 8 threads = 64 columns x 16 blocks (two per warp), codes staged in
-// shared memory so every output row segment leaves as 16-byte stores.
+// Column transforms (the 16 values of a block lie in one column, 16 rows
+// apart): helpers shared by the w and HLA kernels and the transform-only
+// debug kernel.
 // ---------------------------------------------------------------------------
-enum ColOut { kColHqE4M3 = 0, kColI8 = 1, kColBf16 = 2 };
-constexpr int kCPT = 2;               // columns per thread
-constexpr int kColCols = 32 * kCPT;   // columns per CTA tile
-constexpr int kColBlocks = 16;
+enum ColOut { kColI8 = 1, kColBf16 = 2 };
+
+// Store `n` bytes (1, 2, 4, 8, 16 or 32) of packed codes.
+__device__ __forceinline__ void store_chunk(uint8_t* dst, const uint32_t* p, int n) {
+  if (n >= 16) {
+    *reinterpret_cast<uint4*>(dst) = make_uint4(p[0], p[1], p[2], p[3]);
+    if (n == 32) *reinterpret_cast<uint4*>(dst + 16) = make_uint4(p[4], p[5], p[6], p[7]);
+  } else if (n == 8) {
+    *reinterpret_cast<uint2*>(dst) = make_uint2(p[0], p[1]);
+  } else if (n == 4) {
+    *reinterpret_cast<uint32_t*>(dst) = p[0];
+  } else {
+    for (int i = 0; i < n; ++i) dst[i] = (uint8_t)(p[i >> 2] >> (8 * (i & 3)));
+  }
+}
 
 template <bool kBf16>
 __device__ __forceinline__ void load_pair(const void* src, int64_t idx, float* v) {
@@ -419,39 +484,41 @@ __device__ __forceinline__ void load_quad(const void* src, int64_t idx, float* v
   }
 }
 
-// Exactly rounded coefficients of one 16-value column, in place, given
-// whether the fp32 butterfly is exact for it: the `rank` kept rows in
-// sequency order in x[0..rank), or all 16 in Sylvester order when `natural`.
+// Exactly rounded coefficients of one 16-value column, in place, given its
+// tier (0 fast, 1 split, 2 out-of-line exact; see octet_butterfly): the
+// `rank` kept rows in sequency order in x[0..rank), or all 16 in Sylvester
+// order when `natural`.
 template <bool kBf16>
-__device__ __forceinline__ void column_butterfly(float* x, bool exact, int rank,
-                                                 bool natural) {
-  if (exact) {
-    float t[16];
+__device__ __forceinline__ void column_butterfly(float* x, int tier, uint32_t emax,
+                                                 int rank, bool natural) {
+  float t[16];
+  if (tier == 0) {
 #pragma unroll
     for (int j = 0; j < 16; ++j) t[j] = x[j];
     fwht16(t);
-    if (natural) {
+  } else if (tier == 1) {
+    float lo[16];
+    split_high_low(x, emax, t, lo);
+    fwht16(t);
+    fwht16(lo);
 #pragma unroll
-      for (int i = 0; i < 16; ++i) x[i] = t[i];
-    } else {
-#pragma unroll
-      for (int k = 0; k < 16; ++k)
-        if (k < rank) x[k] = t[sequency_row(k)];
-    }
+    for (int j = 0; j < 16; ++j) t[j] += lo[j];  // exact + exact, one rounding
   } else {
     // rare: these two arrays live in local memory for the out-of-line call
     float in[16], o[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j) in[j] = x[j];
     slow_block16(in, o, kBf16 ? 1 : 0);
-    if (natural) {
 #pragma unroll
-      for (int i = 0; i < 16; ++i) x[i] = o[i];
-    } else {
+    for (int j = 0; j < 16; ++j) t[j] = o[j];
+  }
+  if (natural) {
 #pragma unroll
-      for (int k = 0; k < 16; ++k)
-        if (k < rank) x[k] = o[sequency_row(k)];
-    }
+    for (int i = 0; i < 16; ++i) x[i] = t[i];
+  } else {
+#pragma unroll
+    for (int k = 0; k < 16; ++k)
+      if (k < rank) x[k] = t[sequency_row(k)];
   }
 }
 
@@ -462,186 +529,357 @@ __device__ __forceinline__ void column_coeffs(float* x, int rank, bool natural,
 #pragma unroll
   for (int j = 0; j < 16; ++j) exp_range_add(er, x[j]);
   if (any_nonfinite(er)) raise_flag(status, HLQ_DEV_NONFINITE);
-  column_butterfly<kBf16>(x, butterfly_exact<kBf16>(er), rank, natural);
+  column_butterfly<kBf16>(x, butterfly_exact<kBf16>(er) ? 0 : 2, er.emax, rank, natural);
 }
 
-// Exactness of the two columns of 16 packed bf16 pairs (low half = column
-// 0), by 16-bit SIMD max/min of |bits| as in transform_octet_bf16.
-__device__ __forceinline__ void pair_col_exact_bf16(const uint32_t (&p)[16], bool* exact,
+// Tiers (as in octet_butterfly) of the two columns of 16 packed bf16 pairs
+// (low half = column 0), from the largest |bits| and the smallest non-zero
+// |bits| of each column, kept in place in their half of the word (plain
+// 32-bit integer max/min; a zero minus one wraps to the largest value and
+// drops out of the minimum).
+__device__ __forceinline__ void pair_col_tiers_bf16(const uint32_t (&p)[16], int* tier,
+                                                    uint32_t* emax_out,
                                                     unsigned int* status) {
-  uint32_t mx = 0u, mn = 0x7fff7fffu;
+  uint32_t mx0 = 0u, mx1 = 0u, mn0 = 0xffffffffu, mn1 = 0xffffffffu;
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
-    const uint32_t a = p[j] & 0x7fff7fffu;
-    mx = __vmaxu2(mx, a);
-    mn = __vminu2(mn, a | (__vcmpeq2(a, 0u) & 0x7fff7fffu));
+    const uint32_t a0 = p[j] & 0x7fffu, a1 = p[j] & 0x7fff0000u;
+    mx0 = max(mx0, a0);
+    mx1 = max(mx1, a1);
+    mn0 = min(mn0, a0 - 1u);
+    mn1 = min(mn1, a1 - 1u);
   }
+  const uint32_t hi[2] = {mx0, mx1 >> 16};
+  const uint32_t lo[2] = {mn0 + 1u, mn1 == 0xffffffffu ? 0u : (mn1 + 1u) >> 16};
 #pragma unroll
   for (int c = 0; c < 2; ++c) {
-    const uint32_t hi = (mx >> (16 * c)) & 0xffffu, lo = (mn >> (16 * c)) & 0xffffu;
-    const uint32_t emax = hi >> 7, emin = max(lo >> 7, 1u);
+    const uint32_t emax = hi[c] >> 7, emin = max(lo[c] >> 7, 1u);
     if (emax == 255u) raise_flag(status, HLQ_DEV_NONFINITE);
-    exact[c] = lo == 0x7fffu || (emax <= 254u && emax - min(emin, emax) <= 12u);
+    tier[c] = block_tier_bf16(emax, emin, lo[c] == 0u);
+    emax_out[c] = emax;
   }
 }
 
-// Shared-memory staging of a column tile: local row r = c * 32 + tx holds
-// the codes of global column tile_base + kCPT * tx + c; a row is kColBlocks
-// chunks of R codes plus one pad chunk (an odd number of chunks), so the 32
-// chunk stores of a warp (consecutive rows) fall in distinct banks.
-__device__ __forceinline__ int col_tile_col(int r) { return kCPT * (r & 31) + (r >> 5); }
 
-// Store `n` bytes (4, 8, 16 or 32) of packed codes.
-__device__ __forceinline__ void store_chunk(uint8_t* dst, const uint32_t* p, int n) {
-  if (n >= 16) {
-    *reinterpret_cast<uint4*>(dst) = make_uint4(p[0], p[1], p[2], p[3]);
-    if (n == 32) *reinterpret_cast<uint4*>(dst + 16) = make_uint4(p[4], p[5], p[6], p[7]);
-  } else if (n == 8) {
-    *reinterpret_cast<uint2*>(dst) = make_uint2(p[0], p[1]);
-  } else if (n == 4) {
-    *reinterpret_cast<uint32_t*>(dst) = p[0];
-  } else {
-    for (int i = 0; i < n; ++i) dst[i] = (uint8_t)(p[i >> 2] >> (8 * (i & 3)));
+// ---------------------------------------------------------------------------
+// HLA along tokens (a1, a5, and their amax pre-pass).
+//
+// The Sylvester rows of sequency < R are H_R applied to sums over runs of
+// L = 16/R consecutive tokens (H16[L*i][j] = H_R[i][j/L]), so coefficient k
+// is Z[sigma(k)/L] with Z = H_R . (run sums): for R = 8 that is 8 pair sums
+// and an 8-point butterfly instead of a 16-point one.  Both are stages of the
+// 16-point butterfly, so the fp32 exactness rule applies unchanged; blocks
+// that defeat it take the out-of-line exact path on all 16 inputs.
+//
+// Thread = 2 adjacent columns (one 4-byte bf16 pair per row); a warp holds
+// 64 columns; each warp walks kHlaBW consecutive 16-token blocks with the
+// next block's 16 loads in flight while the current one is transformed.
+// CTA = 8 warps = 64 columns x 8*kHlaBW blocks; codes staged in shared
+// memory leave as contiguous row segments of 8*kHlaBW*R codes.
+// ---------------------------------------------------------------------------
+constexpr int kHlaBW = 4;                 // blocks per warp
+constexpr int kHlaBlocks = 8 * kHlaBW;    // blocks per CTA
+constexpr int kHlaCols = 64;
+
+// Column c (0: low, 1: high half of each pair) of a raw block, as fp32.
+__device__ __forceinline__ float col_val(const RawPairCol<true>& r, int c, int j) {
+  return c ? bf16_hi(r.p[j]) : bf16_lo(r.p[j]);
+}
+__device__ __forceinline__ float col_val(const RawPairCol<false>& r, int c, int j) {
+  return c ? r.p[j].y : r.p[j].x;
+}
+
+template <int kR>
+__device__ __forceinline__ void hla_fast(const float* x, float* coef) {
+  constexpr int L = 16 / kR;
+  float z[kR];
+#pragma unroll
+  for (int m = 0; m < kR; ++m) {
+    float acc = x[m * L];
+#pragma unroll
+    for (int t = 1; t < L; ++t) acc += x[m * L + t];
+    z[m] = acc;
   }
+  // butterfly: the pair sums above are the first log2(L) stages; for the
+  // remaining ones the order matches fwht16's on the full block
+#pragma unroll
+  for (int h = 1; h < kR; h <<= 1)
+#pragma unroll
+    for (int a = 0; a < kR; ++a)
+      if ((a & h) == 0) {
+        const float p = z[a], q = z[a + h];
+        z[a] = p + q;
+        z[a + h] = p - q;
+      }
+#pragma unroll
+  for (int k = 0; k < kR; ++k) coef[k] = z[sequency_row(k) / L];
 }
 
 template <bool kBf16, int kMode, int kOut, int kR>
-__global__ void __launch_bounds__(256, 2) col_kernel(
-    const void* __restrict__ src, int64_t rows, int64_t cols,
+__global__ void __launch_bounds__(256, 2) hla_kernel(
+    const void* __restrict__ src, int64_t T, int64_t C,
     unsigned int* __restrict__ amax_slot, void* __restrict__ out, int64_t out_ld,
-    float* __restrict__ scale, int rnd, uint64_t seed, uint32_t stream,
-    unsigned int* __restrict__ status) {
+    float* __restrict__ scale, unsigned int* __restrict__ status) {
   extern __shared__ __align__(16) uint8_t smem[];
-  constexpr bool kHq = kOut == kColHqE4M3;
   constexpr int kBytes = kOut == kColBf16 ? 2 : 1;
-  constexpr int R = kHq ? 16 : kR;  // codes per block per column
-  constexpr int chunk = R * kBytes;   // bytes per block per column
-  constexpr int row_stride = (kColBlocks + 1) * chunk;
+  constexpr int chunk = kR * kBytes;                      // bytes / block / column
+  constexpr int row_stride = (kHlaBlocks + 1) * chunk;    // odd number of chunks
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-  const int64_t n_blk = rows >> 4;
-  const int64_t c0 = (int64_t)blockIdx.x * kColCols + kCPT * tx;
-  const int64_t b0 = (int64_t)blockIdx.y * kColBlocks;
-  const bool col_ok = c0 < cols;
+  const int64_t n_blk = T >> 4;
+  const int64_t c0 = (int64_t)blockIdx.x * kHlaCols + 2 * tx;
+  const int64_t b_cta = (int64_t)blockIdx.y * kHlaBlocks;
+  const int64_t b_first = b_cta + ty * kHlaBW;
+  const bool col_ok = c0 < C;
+  const int nb = col_ok ? (int)imin64(kHlaBW, n_blk - b_first) : 0;
 
   float s = 0.0f;
-  if (kMode == kQuant)
-    s = __fdiv_rn(__uint_as_float(*amax_slot), kHq ? 7.0f : 127.0f);
+  if (kMode == kQuant) s = __fdiv_rn(__uint_as_float(*amax_slot), 127.0f);
   float amax = 0.0f;
-  // both blocks of this thread are fetched before either is transformed
-  RawPairCol<kBf16> raw[2];
-#pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    const int64_t b = b0 + ty + 8 * half;
-    if (col_ok && b < n_blk) load_pair_col<kBf16>(src, 16 * b * cols + c0, cols, raw[half]);
-  }
-#pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    const int bl = ty + 8 * half;
-    const int64_t b = b0 + bl;
-    if (!col_ok || b >= n_blk) continue;
-    float v[kCPT][16];
+  RawPairCol<kBf16> cur, nxt;
+  if (nb > 0) load_pair_col<kBf16>(src, 16 * b_first * C + c0, C, cur);
+#pragma unroll 1
+  for (int i = 0; i < nb; ++i) {
+    if (i + 1 < nb) load_pair_col<kBf16>(src, 16 * (b_first + i + 1) * C + c0, C, nxt);
+    int tier[2];
+    uint32_t emax[2];
     if constexpr (kBf16) {
-      bool exact[2];
-      pair_col_exact_bf16(raw[half].p, exact, status);
-      unpack_pair_col<kBf16>(raw[half], v);
-#pragma unroll
-      for (int c = 0; c < kCPT; ++c) column_butterfly<kBf16>(v[c], exact[c], R, kHq);
+      pair_col_tiers_bf16(cur.p, tier, emax, status);
     } else {
-      unpack_pair_col<kBf16>(raw[half], v);
 #pragma unroll
-      for (int c = 0; c < kCPT; ++c) column_coeffs<kBf16>(v[c], R, kHq, status);
-    }
-    if (kMode == kAmax) {
+      for (int c = 0; c < 2; ++c) {
+        ExpRange er = exp_range_init();
 #pragma unroll
-      for (int c = 0; c < kCPT; ++c)
-#pragma unroll
-        for (int k = 0; k < 16; ++k)
-          if (k < R) amax = fmaxf(amax, fabsf(v[c][k]));
-      continue;
-    }
-    if (kHq) {
-      // element (16b+i, c0+c) of the transformed [rows, cols] tensor; the
-      // thread's columns lie in one Philox block of four (cols % 4 == 0)
-      uint32_t w[kCPT][4];
-#pragma unroll
-      for (int c = 0; c < kCPT; ++c)
-#pragma unroll
-        for (int k = 0; k < 4; ++k) w[c][k] = 0u;
-      const PhiloxKeys keys = philox_keys(seed);
-#pragma unroll
-      for (int i = 0; i < 16; i += 2) {
-        float q[2][kCPT];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          U4 r = {0u, 0u, 0u, 0u};
-          if (rnd == HLQ_SR)
-            r = philox_block_k(keys, stream, (uint64_t)((16 * b + i + h) * cols + c0) >> 2);
-          const bool hi = (c0 & 2) != 0;
-          const uint32_t words[2] = {hi ? r.z : r.x, hi ? r.w : r.y};
-#pragma unroll
-          for (int c = 0; c < kCPT; ++c)
-            q[h][c] = (rnd == HLQ_SR) ? quant_sr_f(v[c][i + h], s, words[c], 7.0f)
-                                      : quant_rne_f(v[c][i + h], s, 7.0f);
-        }
-#pragma unroll
-        for (int c = 0; c < kCPT; ++c)
-          w[c][i >> 2] |= e4m3x2(q[0][c], q[1][c]) << (8 * (i & 3));
+        for (int j = 0; j < 16; ++j) exp_range_add(er, col_val(cur, c, j));
+        if (any_nonfinite(er)) raise_flag(status, HLQ_DEV_NONFINITE);
+        tier[c] = butterfly_exact<false>(er) ? 0 : 2;
+        emax[c] = er.emax;
       }
+    }
+    const int bl = ty * kHlaBW + i;  // block within the CTA tile
 #pragma unroll
-      for (int c = 0; c < kCPT; ++c)
-        *reinterpret_cast<uint4*>(smem + (size_t)(c * 32 + tx) * row_stride + bl * 16) =
-            make_uint4(w[c][0], w[c][1], w[c][2], w[c][3]);
-    } else {
+    for (int c = 0; c < 2; ++c) {  // one column at a time keeps few values live
+      float coef[kR];
+      float xv[16];
 #pragma unroll
-      for (int c = 0; c < kCPT; ++c) {
+      for (int j = 0; j < 16; ++j) xv[j] = col_val(cur, c, j);
+      if (tier[c] == 0) {
+        hla_fast<kR>(xv, coef);
+      } else if (tier[c] == 1) {
+        float hi[16], lo[16], ch[kR];
+        split_high_low(xv, emax[c], hi, lo);
+        hla_fast<kR>(hi, coef);
+        hla_fast<kR>(lo, ch);
+#pragma unroll
+        for (int k = 0; k < kR; ++k) coef[k] += ch[k];  // exact + exact, one rounding
+      } else {
+        float in[16], o[16];  // rare: local memory for the out-of-line call
+#pragma unroll
+        for (int j = 0; j < 16; ++j) in[j] = xv[j];
+        slow_block16(in, o, kBf16 ? 1 : 0);
+#pragma unroll
+        for (int k = 0; k < kR; ++k) coef[k] = o[sequency_row(k)];
+      }
+      if (kMode == kAmax) {
+#pragma unroll
+        for (int k = 0; k < kR; ++k) amax = fmaxf(amax, fabsf(coef[k]));
+      } else {
         uint32_t p[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          if (k < R) {
-            const int q = quant_rne(v[c][k], s, 127);
-            if (kOut == kColBf16) {
-              const uint32_t h = __bfloat16_as_ushort(__int2bfloat16_rn(q));
-              p[k >> 1] |= h << (16 * (k & 1));
-            } else {
-              p[k >> 2] |= ((uint32_t)q & 0xffu) << (8 * (k & 3));
-            }
+        for (int k = 0; k < kR; ++k) {
+          const float q = quant_rne_f(coef[k], s, 127.0f);
+          if (kOut == kColBf16) {
+            p[k >> 1] |= (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(q)) << (16 * (k & 1));
+          } else {
+            p[k >> 2] |= ((uint32_t)(int)q & 0xffu) << (8 * (k & 3));
           }
         }
         store_chunk(smem + (size_t)(c * 32 + tx) * row_stride + bl * chunk, p, chunk);
       }
     }
+    cur = nxt;
   }
   if (kMode == kAmax) {
-    amax = warp_max(amax);
-    if (tx == 0) atomic_max_nonneg(amax_slot, amax);
+    cta_max_to_slot(amax, amax_slot);
     return;
   }
   if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) scale[0] = s;
   __syncthreads();
-  const int64_t valid_b = imin64(kColBlocks, n_blk - b0);
+  // stage row r holds column tile_base + 2 * (r % 32) + r / 32
+  const int64_t valid_b = imin64(kHlaBlocks, n_blk - b_cta);
   const int64_t seg_bytes = valid_b * chunk;
   const int64_t row_bytes = out_ld * kBytes;
-  const int64_t off = b0 * chunk;
-  const bool vec = (seg_bytes % 16 == 0) && (row_bytes % 16 == 0) && (off % 16 == 0) &&
-                   (chunk % 16 == 0 || (kColBlocks * chunk) % 16 == 0);
+  const int64_t off = b_cta * chunk;
   uint8_t* outb = static_cast<uint8_t*>(out);
-  const int64_t col_base = (int64_t)blockIdx.x * kColCols;
-  if (vec && chunk >= 16) {
+  const int64_t col_base = (int64_t)blockIdx.x * kHlaCols;
+  // copy width: the widest that divides the shared row stride (so every
+  // shared-memory row start is aligned), the segment, the output row
+  // stride and the segment offset
+  if (row_stride % 16 == 0 && seg_bytes % 16 == 0 && row_bytes % 16 == 0 && off % 16 == 0) {
     const int chunks = (int)(seg_bytes / 16);
-    for (int idx = threadIdx.x; idx < kColCols * chunks; idx += blockDim.x) {
+    for (int idx = threadIdx.x; idx < kHlaCols * chunks; idx += blockDim.x) {
       const int r = idx / chunks, ch = idx % chunks;
-      const int64_t c = col_base + col_tile_col(r);
-      if (c < cols)
+      const int64_t c = col_base + 2 * (r & 31) + (r >> 5);
+      if (c < C)
         *reinterpret_cast<uint4*>(outb + c * row_bytes + off + ch * 16) =
             *reinterpret_cast<const uint4*>(smem + (size_t)r * row_stride + ch * 16);
     }
+  } else if (row_stride % 8 == 0 && seg_bytes % 8 == 0 && row_bytes % 8 == 0 &&
+             off % 8 == 0) {
+    const int chunks = (int)(seg_bytes / 8);
+    for (int idx = threadIdx.x; idx < kHlaCols * chunks; idx += blockDim.x) {
+      const int r = idx / chunks, ch = idx % chunks;
+      const int64_t c = col_base + 2 * (r & 31) + (r >> 5);
+      if (c < C)
+        *reinterpret_cast<uint2*>(outb + c * row_bytes + off + ch * 8) =
+            *reinterpret_cast<const uint2*>(smem + (size_t)r * row_stride + ch * 8);
+    }
   } else {
-    for (int64_t idx = threadIdx.x; idx < (int64_t)kColCols * seg_bytes; idx += blockDim.x) {
+    for (int64_t idx = threadIdx.x; idx < (int64_t)kHlaCols * seg_bytes; idx += blockDim.x) {
       const int r = (int)(idx / seg_bytes);
       const int by = (int)(idx % seg_bytes);
-      const int64_t c = col_base + col_tile_col(r);
-      if (c < cols) outb[c * row_bytes + off + by] = smem[(size_t)r * row_stride + by];
+      const int64_t c = col_base + 2 * (r & 31) + (r >> 5);
+      if (c < C) outb[c * row_bytes + off + by] = smem[(size_t)r * row_stride + by];
     }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// HLA through TMA-staged tiles.  A CTA owns 256 columns x kTmaBlocks
+// consecutive 16-token blocks; thread 0 starts one TMA copy per block (box
+// 16 rows x 256 columns) into its own shared-memory stage as soon as the
+// barriers exist, so a CTA's whole input is in flight at once; 128 threads
+// then take two columns each and process the blocks in order as they land,
+// reading their 16 values per column out of shared memory (one 32-bit word
+// per lane per row: conflict-free).
+// ---------------------------------------------------------------------------
+constexpr int kTmaCols = 256;
+constexpr int kTmaBlocks = 1;
+
+template <bool kBf16>
+__device__ __forceinline__ void read_pair_col(const uint8_t* stage, int t,
+                                              RawPairCol<kBf16>& r) {
+  if constexpr (kBf16) {
+    const uint32_t* p = reinterpret_cast<const uint32_t*>(stage);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) r.p[j] = p[j * (kTmaCols / 2) + t];
+  } else {
+    const float2* p = reinterpret_cast<const float2*>(stage);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) r.p[j] = p[j * (kTmaCols / 2) + t];
+  }
+}
+
+template <bool kBf16, int kMode, int kOut, int kR>
+__global__ void __launch_bounds__(128 * kTmaBlocks) hla_tma_kernel(
+    const __grid_constant__ CUtensorMap tm, int64_t T, int64_t C,
+    unsigned int* __restrict__ amax_slot, void* __restrict__ out, int64_t out_ld,
+    float* __restrict__ scale, unsigned int* __restrict__ status) {
+  constexpr int kStage = 16 * kTmaCols * (kBf16 ? 2 : 4);
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kTmaBlocks * kStage);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(full + kTmaBlocks);
+  constexpr int kBytes = kOut == kColBf16 ? 2 : 1;
+
+  // thread (t, i): column pair t of block i of the tile
+  const int t = threadIdx.x & 127, i = threadIdx.x >> 7;
+  const int64_t n_blk = T >> 4;
+  const int64_t b0 = (int64_t)blockIdx.y * kTmaBlocks;
+  const int nb = (int)imin64(kTmaBlocks, n_blk - b0);
+  const int64_t col0 = (int64_t)blockIdx.x * kTmaCols;
+  if (threadIdx.x == 0) {
+    for (int k = 0; k < kTmaBlocks; ++k) mbar_init(&full[k], 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    for (int k = 0; k < nb; ++k) {
+      mbar_expect_tx(&full[k], kStage);
+      tma_load_2d(smem + k * kStage, &tm, &full[k], (int)col0, (int)(16 * (b0 + k)));
+    }
+  }
+  __syncthreads();
+
+  const int64_t c0 = col0 + 2 * t;
+  const bool col_ok = c0 < C;
+  float s = 0.0f;
+  if (kMode == kQuant) s = __fdiv_rn(__uint_as_float(*amax_slot), 127.0f);
+  float amax = 0.0f;
+  uint8_t* outb = static_cast<uint8_t*>(out);
+  bool ok = true;
+  if (i < nb) {
+    ok = mbar_wait(&full[i], 0u, abort_flag, status);
+  }
+  if (i < nb && ok && col_ok) {
+    RawPairCol<kBf16> cur;
+    read_pair_col<kBf16>(smem + i * kStage, t, cur);
+    int tier[2];
+    uint32_t emax[2];
+    if constexpr (kBf16) {
+      pair_col_tiers_bf16(cur.p, tier, emax, status);
+    } else {
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        ExpRange er = exp_range_init();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) exp_range_add(er, col_val(cur, c, j));
+        if (any_nonfinite(er)) raise_flag(status, HLQ_DEV_NONFINITE);
+        tier[c] = butterfly_exact<false>(er) ? 0 : 2;
+        emax[c] = er.emax;
+      }
+    }
+    const int64_t b = b0 + i;
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      float coef[kR];
+      float xv[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) xv[j] = col_val(cur, c, j);
+      if (tier[c] == 0) {
+        hla_fast<kR>(xv, coef);
+      } else if (tier[c] == 1) {
+        float hi[16], lo[16], ch[kR];
+        split_high_low(xv, emax[c], hi, lo);
+        hla_fast<kR>(hi, coef);
+        hla_fast<kR>(lo, ch);
+#pragma unroll
+        for (int k = 0; k < kR; ++k) coef[k] += ch[k];  // exact + exact, one rounding
+      } else {
+        float in[16], o[16];  // rare: local memory for the out-of-line call
+#pragma unroll
+        for (int j = 0; j < 16; ++j) in[j] = xv[j];
+        slow_block16(in, o, kBf16 ? 1 : 0);
+#pragma unroll
+        for (int k = 0; k < kR; ++k) coef[k] = o[sequency_row(k)];
+      }
+      if (kMode == kAmax) {
+#pragma unroll
+        for (int k = 0; k < kR; ++k) amax = fmaxf(amax, fabsf(coef[k]));
+      } else {
+        uint32_t p[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+#pragma unroll
+        for (int k = 0; k < kR; ++k) {
+          const float q = quant_rne_f(coef[k], s, 127.0f);
+          if (kOut == kColBf16)
+            p[k >> 1] |= (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(q)) << (16 * (k & 1));
+          else
+            p[k >> 2] |= ((uint32_t)(int)q & 0xffu) << (8 * (k & 3));
+        }
+        store_chunk(outb + ((c0 + c) * out_ld + b * kR) * kBytes, p, kR * kBytes);
+      }
+    }
+  }
+  if (threadIdx.x == 0 && *abort_flag) {  // let every copy land before exit
+    for (int k = 0; k < nb; ++k) {
+      const unsigned long long t0 = now_ns();
+      while (!mbar_test(&full[k], 0u) && now_ns() - t0 < kWaitNs) {
+      }
+    }
+  }
+  if (kMode == kAmax) {
+    cta_max_to_slot(amax, amax_slot);
+  } else if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
+    scale[0] = s;
   }
 }
 
@@ -675,11 +913,12 @@ __global__ void __launch_bounds__(256) hq_w_kernel(
     RawPairCol<kBf16> raw;
     load_pair_col<kBf16>(src, 16 * b * cols + c0, cols, raw);
     if constexpr (kBf16) {
-      bool exact[2];
-      pair_col_exact_bf16(raw.p, exact, status);
+      int tier[2];
+      uint32_t emax[2];
+      pair_col_tiers_bf16(raw.p, tier, emax, status);
       unpack_pair_col<kBf16>(raw, v);
-      column_butterfly<kBf16>(v[0], exact[0], 16, true);
-      column_butterfly<kBf16>(v[1], exact[1], 16, true);
+      column_butterfly<kBf16>(v[0], tier[0], emax[0], 16, true);
+      column_butterfly<kBf16>(v[1], tier[1], emax[1], 16, true);
     } else {
       unpack_pair_col<kBf16>(raw, v);
       column_coeffs<kBf16>(v[0], 16, true, status);
@@ -692,8 +931,7 @@ __global__ void __launch_bounds__(256) hq_w_kernel(
 #pragma unroll
       for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fmaxf(fabsf(v[0][i]), fabsf(v[1][i])));
     }
-    amax = warp_max(amax);
-    if (tx == 0) atomic_max_nonneg(amax_slot, amax);
+    cta_max_to_slot(amax, amax_slot);
     return;
   }
   const float s = __fdiv_rn(__uint_as_float(*amax_slot), 7.0f);
@@ -851,6 +1089,22 @@ __global__ void decode_bf16_kernel(const __nv_bfloat16* __restrict__ in,
 // ---------------------------------------------------------------------------
 // Host-side launchers.
 // ---------------------------------------------------------------------------
+// Raise a kernel's dynamic shared-memory limit once per device (the call is
+// not free, and launches come in the microseconds).
+// (one cache per kernel: the kernel is a template argument)
+template <auto kKernel>
+static cudaError_t ensure_smem_limit(size_t bytes) {
+  static int done[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (done[dev] >= (int)bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(kKernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess) done[dev] = (int)bytes;
+  return e;
+}
+
 static inline unsigned grid1(int64_t n, int per) {
   return (unsigned)((n + per - 1) / per);
 }
@@ -870,9 +1124,9 @@ cudaError_t launch_hq_rows(const void* src, bool bf16, int64_t rows,
   const size_t smem = stage ? row_bytes * warps : 0;
 #define HQR(B, M, P)                                                              \
   do {                                                                            \
-    if (smem > 48 * 1024)                                                         \
-      cudaFuncSetAttribute(hq_rows_kernel<B, M, P>,                               \
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024); \
+    if (smem > 48 * 1024 &&                                                       \
+        ensure_smem_limit<hq_rows_kernel<B, M, P>>(160 * 1024) != cudaSuccess)    \
+      return cudaGetLastError();                                                  \
     hq_rows_kernel<B, M, P><<<grid, threads, smem, st>>>(                         \
         src, rows, cols, amax_slot, codes, scales, rnd, seed, stream_id, status,  \
         stage ? 1 : 0);                                                           \
@@ -886,48 +1140,6 @@ cudaError_t launch_hq_rows(const void* src, bool bf16, int64_t rows,
   }
 #undef HQR
   return cudaGetLastError();
-}
-
-template <bool B, int M, int O, int R>
-static cudaError_t launch_col_r(const void* src, int64_t rows, int64_t cols,
-                                unsigned int* amax_slot, void* out, int64_t out_ld,
-                                float* scale, int rnd, uint64_t seed, uint32_t stream_id,
-                                unsigned int* status, cudaStream_t st) {
-  constexpr int RR = O == kColHqE4M3 ? 16 : R;
-  const size_t smem =
-      M == kAmax ? 0 : (size_t)kColCols * (kColBlocks + 1) * RR * (O == kColBf16 ? 2 : 1);
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(
-        col_kernel<B, M, O, R>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-  }
-  dim3 grid(grid1(cols, kColCols), grid1(rows / 16, kColBlocks));
-  col_kernel<B, M, O, R><<<grid, 256, smem, st>>>(src, rows, cols, amax_slot, out,
-                                                  out_ld, scale, rnd, seed, stream_id,
-                                                  status);
-  return cudaGetLastError();
-}
-
-template <bool B, int M, int O>
-static cudaError_t launch_col(const void* src, int64_t rows, int64_t cols, int rank,
-                              unsigned int* amax_slot, void* out, int64_t out_ld,
-                              float* scale, int rnd, uint64_t seed, uint32_t stream_id,
-                              unsigned int* status, cudaStream_t st) {
-#define LCR(R) \
-  launch_col_r<B, M, O, R>(src, rows, cols, amax_slot, out, out_ld, scale, rnd, seed, \
-                           stream_id, status, st)
-  if constexpr (O == kColHqE4M3) {
-    return LCR(16);
-  } else {
-    switch (rank) {
-      case 1: return LCR(1);
-      case 2: return LCR(2);
-      case 4: return LCR(4);
-      case 8: return LCR(8);
-      default: return LCR(16);
-    }
-  }
-#undef LCR
 }
 
 cudaError_t launch_hq_cols(const void* src, bool bf16, int64_t rows,
@@ -949,17 +1161,61 @@ cudaError_t launch_hq_cols(const void* src, bool bf16, int64_t rows,
   return cudaGetLastError();
 }
 
+template <bool B, int M, int O, int R>
+static cudaError_t launch_hla_r(const void* src, int64_t T, int64_t C,
+                                unsigned int* amax_slot, void* out, int64_t out_ld,
+                                float* scale, unsigned int* status, cudaStream_t st) {
+  // TMA-staged path: chunk stores of R codes need R-code-aligned rows
+  const int chunk = R * (O == kColBf16 ? 2 : 1);
+  const bool chunk_ok = (chunk == 1 || chunk == 2 || chunk % 4 == 0) &&
+                        (out_ld * (O == kColBf16 ? 2 : 1)) % (chunk >= 16 ? 16 : chunk) == 0;
+  CUtensorMap tm;
+  if (chunk_ok && make_tile_map_2d(&tm, src, B, T, C, kTmaCols, 16)) {
+    const size_t smem = 128 + (size_t)kTmaBlocks * 16 * kTmaCols * (B ? 2 : 4) +
+                        kTmaBlocks * 8 + 16;
+    cudaError_t e = ensure_smem_limit<hla_tma_kernel<B, M, O, R>>(smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid(grid1(C, kTmaCols), grid1(T / 16, kTmaBlocks));
+    hla_tma_kernel<B, M, O, R><<<grid, 128 * kTmaBlocks, smem, st>>>(
+        tm, T, C, amax_slot, out, out_ld, scale, status);
+    return cudaGetLastError();
+  }
+  const size_t smem =
+      M == kAmax ? 0 : (size_t)kHlaCols * (kHlaBlocks + 1) * R * (O == kColBf16 ? 2 : 1);
+  if (smem > 48 * 1024) {
+    cudaError_t e = ensure_smem_limit<hla_kernel<B, M, O, R>>(smem);
+    if (e != cudaSuccess) return e;
+  }
+  dim3 grid(grid1(C, kHlaCols), grid1(T / 16, kHlaBlocks));
+  hla_kernel<B, M, O, R><<<grid, 256, smem, st>>>(src, T, C, amax_slot, out, out_ld,
+                                                  scale, status);
+  return cudaGetLastError();
+}
+
+template <bool B, int M, int O>
+static cudaError_t launch_hla_o(const void* src, int64_t T, int64_t C, int rank,
+                                unsigned int* amax_slot, void* out, int64_t out_ld,
+                                float* scale, unsigned int* status, cudaStream_t st) {
+#define LHR(R) launch_hla_r<B, M, O, R>(src, T, C, amax_slot, out, out_ld, scale, status, st)
+  switch (rank) {
+    case 1: return LHR(1);
+    case 2: return LHR(2);
+    case 4: return LHR(4);
+    case 8: return LHR(8);
+    default: return LHR(16);
+  }
+#undef LHR
+}
+
 cudaError_t launch_hla(const void* src, bool bf16, int64_t T, int64_t C,
                        int rank, bool amax_only, bool out_bf16,
                        unsigned int* amax_slot, void* out, int64_t out_ld,
                        float* scale, unsigned int* status, cudaStream_t st) {
-#define COL(B, M, O)                                                                  \
-  launch_col<B, M, O>(src, T, C, rank, amax_slot, out, out_ld, scale, HLQ_RNE, 0, 0, \
-                      status, st)
-  if (amax_only) return bf16 ? COL(true, kAmax, kColI8) : COL(false, kAmax, kColI8);
-  if (out_bf16) return bf16 ? COL(true, kQuant, kColBf16) : COL(false, kQuant, kColBf16);
-  return bf16 ? COL(true, kQuant, kColI8) : COL(false, kQuant, kColI8);
-#undef COL
+#define LHO(B, M, O) launch_hla_o<B, M, O>(src, T, C, rank, amax_slot, out, out_ld, scale, status, st)
+  if (amax_only) return bf16 ? LHO(true, kAmax, kColI8) : LHO(false, kAmax, kColI8);
+  if (out_bf16) return bf16 ? LHO(true, kQuant, kColBf16) : LHO(false, kQuant, kColBf16);
+  return bf16 ? LHO(true, kQuant, kColI8) : LHO(false, kQuant, kColI8);
+#undef LHO
 }
 
 cudaError_t launch_hq_rows_transform(const void* src, bool bf16, int64_t rows,

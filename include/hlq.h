@@ -241,7 +241,10 @@ size_t hlq_debug_tc_gemm_ws_bytes(int64_t M, int64_t N);
  * recorded events and returns how many launches were traced; hlq_trace_get
  * gives launch i's kernel name (static string) and its device time in ms.
  * hlq_trace_free destroys the events.  Not thread-safe: trace from one host
- * thread at a time.
+ * thread at a time.  Launches traced while their stream is being captured
+ * into a CUDA graph record their events as external event nodes: every
+ * replay of the graph re-records them, and hlq_trace_get (after the replay
+ * has finished) returns that replay's times.
  */
 hlq_status hlq_trace_begin(int capacity);
 hlq_status hlq_trace_end(int *n_launches);
