@@ -4,6 +4,7 @@
 #pragma once
 
 #include <cstdint>
+#include <utility>
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
@@ -11,6 +12,35 @@
 #include "hlq.h"
 
 namespace hlq {
+
+// Programmatic dependent launch: the hot kernels are launched with the
+// programmatic-serialization attribute (launch_pdl), let the next kernel in
+// the stream start launching at once (pdl_trigger), and wait for the
+// previous kernel's completion and memory (pdl_wait) before they touch
+// global memory.  Both are no-ops for a kernel launched without the
+// attribute.
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+template <typename... Exp, typename... Act>
+static cudaError_t launch_pdl(void (*kernel)(Exp...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t st, Act&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Act>(args)...);
+}
 
 // Device status word (HLQ_DEV_* flags): every kernel that can detect a
 // device-side condition takes its address; hlq_read_device_status reads it.

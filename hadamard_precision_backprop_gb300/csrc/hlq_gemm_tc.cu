@@ -167,6 +167,10 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
+  // the prologue above overlaps the previous kernel; operands, scales and
+  // outputs are touched only after it has completed
+  pdl_trigger();
+  pdl_wait();
 
   // unit -> (m0, n0, first k-block, k-blocks)
   auto unit_coords = [&](int u, int& m0, int& n0, int& kb0, int& nkb) {
@@ -412,9 +416,11 @@ cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, int64_t M, int
   const int64_t units = tiles * splits;
   if (units > 0x7fffffff) return cudaErrorInvalidValue;
   const int grid = (int)(units < num_sms ? units : num_sms);
-  gemm_tc_kernel<kKind, BN><<<grid, C::kThreads, C::kSmem, st>>>(
-      a, b, (int)M, (int)N, num_kb, chunk_kb, kb_per_split, splits, tiles_n, (int)units,
-      sa, per_row_a ? 1 : 0, sb, out, acc_out, split_acc, slab_count, status);
+  cudaError_t le = launch_pdl(
+      gemm_tc_kernel<kKind, BN>, dim3(grid), dim3(C::kThreads), C::kSmem, st, a, b, (int)M,
+      (int)N, num_kb, chunk_kb, kb_per_split, splits, tiles_n, (int)units, sa,
+      per_row_a ? 1 : 0, sb, out, acc_out, split_acc, slab_count, status);
+  if (le != cudaSuccess) return le;
   return cudaGetLastError();
 }
 

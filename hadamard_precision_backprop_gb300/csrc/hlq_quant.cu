@@ -297,6 +297,8 @@ __global__ void __launch_bounds__(256) hq_rows_kernel(
     unsigned int* __restrict__ amax_slot, uint8_t* __restrict__ codes,
     float* __restrict__ scales, int rnd, uint64_t seed, uint32_t stream,
     unsigned int* __restrict__ status, int stage) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ float4 srow[];
   const int lane = threadIdx.x & 31;
   const int wid = threadIdx.x >> 5;
@@ -620,6 +622,8 @@ __global__ void __launch_bounds__(256, 2) hla_kernel(
     const void* __restrict__ src, int64_t T, int64_t C,
     unsigned int* __restrict__ amax_slot, void* __restrict__ out, int64_t out_ld,
     float* __restrict__ scale, unsigned int* __restrict__ status) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ __align__(16) uint8_t smem[];
   constexpr int kBytes = kOut == kColBf16 ? 2 : 1;
   constexpr int chunk = kR * kBytes;                      // bytes / block / column
@@ -788,11 +792,15 @@ __global__ void __launch_bounds__(128 * kTmaBlocks) hla_tma_kernel(
   const int64_t b0 = (int64_t)blockIdx.y * kTmaBlocks;
   const int nb = (int)imin64(kTmaBlocks, n_blk - b0);
   const int64_t col0 = (int64_t)blockIdx.x * kTmaCols;
+  pdl_trigger();
   if (threadIdx.x == 0) {
     for (int k = 0; k < kTmaBlocks; ++k) mbar_init(&full[k], 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  pdl_wait();  // the input and the amax slot come from earlier kernels
+  if (threadIdx.x == 0) {
     for (int k = 0; k < nb; ++k) {
       mbar_expect_tx(&full[k], kStage);
       tma_load_2d(smem + k * kStage, &tm, &full[k], (int)col0, (int)(16 * (b0 + k)));
@@ -901,6 +909,8 @@ __global__ void __launch_bounds__(256) hq_w_kernel(
     unsigned int* __restrict__ amax_slot, uint8_t* __restrict__ codes_t,
     float* __restrict__ scale, int rnd, uint64_t seed, uint32_t stream,
     unsigned int* __restrict__ status) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ __align__(16) uint8_t stage[kWCols * kWRowStride];
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
   const int bl = ty >> 1, part = ty & 1;
@@ -1052,6 +1062,8 @@ __global__ void widen_i8_to_bf16_kernel(const int8_t* __restrict__ in,
                                         __nv_bfloat16* __restrict__ out,
                                         int64_t rows, int64_t cols,
                                         int64_t out_ld) {
+  pdl_trigger();
+  pdl_wait();
   const int64_t per_row = (cols + 7) / 8;
   const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= rows * per_row) return;
@@ -1127,9 +1139,9 @@ cudaError_t launch_hq_rows(const void* src, bool bf16, int64_t rows,
     if (smem > 48 * 1024 &&                                                       \
         ensure_smem_limit<hq_rows_kernel<B, M, P>>(160 * 1024) != cudaSuccess)    \
       return cudaGetLastError();                                                  \
-    hq_rows_kernel<B, M, P><<<grid, threads, smem, st>>>(                         \
-        src, rows, cols, amax_slot, codes, scales, rnd, seed, stream_id, status,  \
-        stage ? 1 : 0);                                                           \
+    launch_pdl(hq_rows_kernel<B, M, P>, grid, dim3(threads), smem, st, src, rows,  \
+               cols, amax_slot, codes, scales, rnd, seed, stream_id, status,       \
+               stage ? 1 : 0);                                                    \
   } while (0)
   if (amax_only) {
     if (bf16) HQR(true, kAmax, false); else HQR(false, kAmax, false);
@@ -1150,8 +1162,8 @@ cudaError_t launch_hq_cols(const void* src, bool bf16, int64_t rows,
                            cudaStream_t st) {
   dim3 grid(grid1(cols, kWCols), grid1(rows / 16, kWBlocks));
 #define HQW(B, M)                                                                  \
-  hq_w_kernel<B, M><<<grid, 256, 0, st>>>(src, rows, cols, amax_slot, codes_t, scale, \
-                                          rnd, seed, stream_id, status)
+  launch_pdl(hq_w_kernel<B, M>, grid, dim3(256), 0, st, src, rows, cols, amax_slot, \
+             codes_t, scale, rnd, seed, stream_id, status)
   if (amax_only) {
     if (bf16) HQW(true, kAmax); else HQW(false, kAmax);
   } else {
@@ -1176,8 +1188,8 @@ static cudaError_t launch_hla_r(const void* src, int64_t T, int64_t C,
     cudaError_t e = ensure_smem_limit<hla_tma_kernel<B, M, O, R>>(smem);
     if (e != cudaSuccess) return e;
     dim3 grid(grid1(C, kTmaCols), grid1(T / 16, kTmaBlocks));
-    hla_tma_kernel<B, M, O, R><<<grid, 128 * kTmaBlocks, smem, st>>>(
-        tm, T, C, amax_slot, out, out_ld, scale, status);
+    launch_pdl(hla_tma_kernel<B, M, O, R>, grid, dim3(128 * kTmaBlocks), smem, st, tm, T,
+               C, amax_slot, out, out_ld, scale, status);
     return cudaGetLastError();
   }
   const size_t smem =
@@ -1187,7 +1199,7 @@ static cudaError_t launch_hla_r(const void* src, int64_t T, int64_t C,
     if (e != cudaSuccess) return e;
   }
   dim3 grid(grid1(C, kHlaCols), grid1(T / 16, kHlaBlocks));
-  hla_kernel<B, M, O, R><<<grid, 256, smem, st>>>(src, T, C, amax_slot, out, out_ld,
+  launch_pdl(hla_kernel<B, M, O, R>, grid, dim3(256), smem, st, src, T, C, amax_slot, out, out_ld,
                                                   scale, status);
   return cudaGetLastError();
 }
@@ -1249,8 +1261,8 @@ cudaError_t launch_widen_i8_bf16(const int8_t* in, void* out, int64_t rows,
                                  int64_t cols, int64_t out_ld, cudaStream_t st) {
   if (rows * cols == 0) return cudaSuccess;
   const int64_t n = rows * ((cols + 7) / 8);
-  widen_i8_to_bf16_kernel<<<grid1(n, 256), 256, 0, st>>>(
-      in, static_cast<__nv_bfloat16*>(out), rows, cols, out_ld);
+  launch_pdl(widen_i8_to_bf16_kernel, dim3(grid1(n, 256)), dim3(256), 0, st, in,
+             static_cast<__nv_bfloat16*>(out), rows, cols, out_ld);
   return cudaGetLastError();
 }
 
