@@ -493,15 +493,32 @@ def run_ours(args, wl, rank, world, local_rank):
     return 0
 
 
+def kernel_sources_digest():
+    """sha256 over the CUDA sources, so that DRAM counters taken from an older
+    build of the kernels are not reported against the current ones."""
+    import hashlib
+    d = os.path.join(ROOT, "hadamard_precision_backprop_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(d)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            h.update(name.encode())
+            with open(os.path.join(d, name), "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()
+
+
 def load_traffic(kernel, wl):
-    """DRAM bytes per launch of `kernel` from the committed ncu summary of the
-    current kernels, or None when no capture of this kernel exists."""
+    """DRAM bytes (read + write) per launch of `kernel` from the committed ncu
+    capture summary, or None when there is no capture of this kernel on this
+    workload or the kernel sources changed after it was taken."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         d = json.load(f)
-    v = d.get(wl.name, {}).get(kernel)
+    if d.get("sources_sha256") != kernel_sources_digest():
+        return None
+    v = d.get("workloads", {}).get(wl.name, {}).get(kernel)
     return None if v is None else v.get("dram_bytes_per_launch")
 
 
