@@ -1,6 +1,7 @@
 // hlq_api.cu -- the C ABI of libhlq (declared in include/hlq.h): argument
 // validation, workspace layout and the launch sequence of each step.
 #include <cstdint>
+#include <mutex>
 #include <cstring>
 #include <cuda_runtime.h>
 
@@ -53,35 +54,46 @@ void trace_free() {
   g_trace = Trace{};
 }
 
-// External records: inside a stream capture they become event-record nodes
-// of the graph, re-recorded at every replay (outside a capture the flag
-// changes nothing).
+// Inside a stream capture the records are external, so that they become
+// event-record nodes of the graph, re-recorded at every replay; outside a
+// capture they are plain records (the external flag is refused there).
+inline void trace_record(cudaEvent_t ev, cudaStream_t s) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+    cudaEventRecordWithFlags(ev, s, cudaEventRecordExternal);
+  else
+    cudaEventRecord(ev, s);
+}
 inline void trace_before(cudaStream_t s) {
-  if (g_trace.on && g_trace.n < g_trace.cap)
-    cudaEventRecordWithFlags(g_trace.ev[2 * g_trace.n], s, cudaEventRecordExternal);
+  if (g_trace.on && g_trace.n < g_trace.cap) trace_record(g_trace.ev[2 * g_trace.n], s);
 }
 inline void trace_after(const char* what, cudaStream_t s) {
   if (g_trace.on && g_trace.n < g_trace.cap) {
-    cudaEventRecordWithFlags(g_trace.ev[2 * g_trace.n + 1], s, cudaEventRecordExternal);
+    trace_record(g_trace.ev[2 * g_trace.n + 1], s);
     g_trace.name[g_trace.n] = what;
     ++g_trace.n;
   }
 }
 
-// Auxiliary stream per device for hlq_linear_backward's g_w branch.
-cudaStream_t g_aux_stream[kMaxDevices] = {};
+// Auxiliary streams per device for hlq_linear_backward: 0 runs the g_w
+// branch, 1 the HQ of w.  Created on first use, kept for the process.
+constexpr int kAuxStreams = 2;
+cudaStream_t g_aux_stream[kMaxDevices][kAuxStreams] = {};
+std::mutex g_aux_mutex;
 
-cudaStream_t aux_stream() {
+cudaStream_t aux_stream(int which) {
   int dev = 0;
+  if (which < 0 || which >= kAuxStreams) return nullptr;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
     return nullptr;
-  if (!g_aux_stream[dev]) {
+  std::lock_guard<std::mutex> lock(g_aux_mutex);
+  if (!g_aux_stream[dev][which]) {
     cudaStream_t st = nullptr;
     if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess)
       return nullptr;
-    g_aux_stream[dev] = st;
+    g_aux_stream[dev][which] = st;
   }
-  return g_aux_stream[dev];
+  return g_aux_stream[dev][which];
 }
 
 constexpr size_t kAlign = 256;
@@ -157,7 +169,6 @@ hlq_status check_common(int dt, int64_t T, int64_t Cin, int64_t Cout,
   return HLQ_OK;
 }
 
-hlq_status cuda_status(cudaError_t e) { return e == cudaSuccess ? HLQ_OK : HLQ_ERR_CUDA; }
 
 #define HLQ_TRY(expr)                                  \
   do {                                                 \
@@ -174,12 +185,40 @@ hlq_status cuda_status(cudaError_t e) { return e == cudaSuccess ? HLQ_OK : HLQ_E
     trace_after(name, s);                              \
   } while (0)
 
+// HQ of w (amax pass, then quantization to transposed E4M3 codes).
+hlq_status hq_w_launches(const void* w, bool bf16, int64_t Cout, int64_t Cin,
+                         unsigned int* amax, uint8_t* qw, float* sw, int rnd, uint64_t seed,
+                         unsigned int* status, cudaStream_t s) {
+  HLQ_LAUNCH("hq_cols_amax", s,
+             launch_hq_cols(w, bf16, Cout, Cin, true, amax, nullptr, nullptr, rnd, seed, 1,
+                            status, s));
+  HLQ_LAUNCH("hq_cols_quant", s,
+             launch_hq_cols(w, bf16, Cout, Cin, false, amax, qw, sw, rnd, seed, 1, status,
+                            s));
+  return HLQ_OK;
+}
+
+// HQ of g_y (an amax pass first for a per-tensor scale).
+hlq_status hq_gy_launches(const void* gy, bool bf16, int64_t T, int64_t Cout, bool per_token,
+                          unsigned int* amax, uint8_t* qy, float* sgy, int rnd,
+                          uint64_t seed, unsigned int* status, cudaStream_t s) {
+  if (!per_token)
+    HLQ_LAUNCH("hq_rows_amax", s,
+               launch_hq_rows(gy, bf16, T, Cout, false, true, amax, nullptr, nullptr, rnd,
+                              seed, 0, status, s));
+  HLQ_LAUNCH("hq_rows_quant", s,
+             launch_hq_rows(gy, bf16, T, Cout, per_token, false, amax, qy, sgy, rnd, seed, 0,
+                            status, s));
+  return HLQ_OK;
+}
+
 hlq_status gx_impl(const void* gy, const void* w, int dt, int64_t T,
                    int64_t Cin, int64_t Cout, int block, int gran_gy,
                    int gran_w, int rnd, uint64_t seed, float* gx, void* ws,
                    size_t ws_bytes, int8_t* dbg_qgy, float* dbg_sgy,
                    int8_t* dbg_qw, float* dbg_sw, int32_t* dbg_acc,
-                   void* stream, bool validate_only = false) {
+                   void* stream, bool validate_only = false,
+                   cudaStream_t w_stream = nullptr) {
   hlq_status st = check_common(dt, T, Cin, Cout, block);
   if (st != HLQ_OK) return st;
   if (gran_gy != HLQ_PER_TENSOR && gran_gy != HLQ_PER_TOKEN) return HLQ_ERR_INVALID_ARG;
@@ -215,20 +254,37 @@ hlq_status gx_impl(const void* gy, const void* w, int dt, int64_t T,
   const bool bf16 = dt == HLQ_BF16;
   const bool per_token = gran_gy == HLQ_PER_TOKEN;
 
+  // amax[0]: g_y, amax[1]: w
   HLQ_TRY(cudaMemsetAsync(amax, 0, 8, s));
-  if (!per_token)
-    HLQ_LAUNCH("hq_rows_amax", s,
-               launch_hq_rows(gy, bf16, T, Cout, false, true, amax, nullptr,
-                              nullptr, rnd, seed, 0, status, s));
-  HLQ_LAUNCH("hq_rows_quant", s,
-             launch_hq_rows(gy, bf16, T, Cout, per_token, false, amax, qy, sgy,
-                            rnd, seed, 0, status, s));
-  HLQ_LAUNCH("hq_cols_amax", s,
-             launch_hq_cols(w, bf16, Cout, Cin, true, amax + 1, nullptr, nullptr,
-                            rnd, seed, 1, status, s));
-  HLQ_LAUNCH("hq_cols_quant", s,
-             launch_hq_cols(w, bf16, Cout, Cin, false, amax + 1, qw, sw, rnd,
-                            seed, 1, status, s));
+  // HQ of w: on `w_stream` when given (forked here, joined before the GEMM),
+  // so that the small, latency-bound transform of w overlaps the HQ of g_y
+  cudaStream_t sw_st = s;
+  cudaEvent_t w_fork = nullptr, w_done = nullptr;
+  if (w_stream && w_stream != s) {
+    if (cudaEventCreateWithFlags(&w_fork, cudaEventDisableTiming) != cudaSuccess)
+      return HLQ_ERR_CUDA;
+    if (cudaEventCreateWithFlags(&w_done, cudaEventDisableTiming) != cudaSuccess) {
+      cudaEventDestroy(w_fork);
+      return HLQ_ERR_CUDA;
+    }
+    sw_st = w_stream;
+  }
+  hlq_status r = HLQ_OK;
+  if (w_fork && (cudaEventRecord(w_fork, s) != cudaSuccess ||
+                 cudaStreamWaitEvent(sw_st, w_fork, 0) != cudaSuccess))
+    r = HLQ_ERR_CUDA;
+  if (r == HLQ_OK)
+    r = hq_w_launches(w, bf16, Cout, Cin, amax + 1, qw, sw, rnd, seed, status, sw_st);
+  if (r == HLQ_OK)
+    r = hq_gy_launches(gy, bf16, T, Cout, per_token, amax, qy, sgy, rnd, seed, status, s);
+  if (w_fork) {  // join even after a failure: `s` never runs ahead of `w_stream`
+    if (cudaEventRecord(w_done, sw_st) != cudaSuccess ||
+        cudaStreamWaitEvent(s, w_done, 0) != cudaSuccess)
+      r = HLQ_ERR_CUDA;
+    cudaEventDestroy(w_fork);
+    cudaEventDestroy(w_done);
+  }
+  if (r != HLQ_OK) return r;
   const int sms = device_sm_count();
   if (sms <= 0) return HLQ_ERR_CUDA;
   const GemmPlan plan = plan_gemm_tc(0, T, Cin, Cout, sms, 1);
@@ -385,8 +441,8 @@ hlq_status hlq_linear_backward(const void* d_gy, const void* d_w, const int8_t* 
   if (!aligned256(d_ws)) return HLQ_ERR_ALIGN;
   uint8_t* base = static_cast<uint8_t*>(d_ws);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaStream_t a = aux_stream();
-  if (!a) return HLQ_ERR_CUDA;
+  cudaStream_t a = aux_stream(0), aw = aux_stream(1);
+  if (!a || !aw) return HLQ_ERR_CUDA;
   // validate both branches before forking (nothing enqueued on failure)
   st = gw_impl(d_gy, dt, d_xbar, d_xbar_scale, T, Cin, Cout, block, rank, d_gw,
                base + gx_bytes, gw_bytes, nullptr, nullptr, nullptr, nullptr,
@@ -409,10 +465,10 @@ hlq_status hlq_linear_backward(const void* d_gy, const void* d_w, const int8_t* 
   if (r == HLQ_OK)  // g_w branch on the auxiliary stream
     r = gw_impl(d_gy, dt, d_xbar, d_xbar_scale, T, Cin, Cout, block, rank, d_gw,
                 base + gx_bytes, gw_bytes, nullptr, nullptr, nullptr, a, false);
-  if (r == HLQ_OK)  // g_x branch on the caller's stream
+  if (r == HLQ_OK)  // g_x branch on the caller's stream, its HQ of w on a third
     r = gx_impl(d_gy, d_w, dt, T, Cin, Cout, block, gran_gy, gran_w, rnd, seed, d_gx,
                 base, gx_bytes, nullptr, nullptr, nullptr, nullptr, nullptr, stream,
-                false);
+                false, aw);
   // join even after a failure, so the caller's stream never runs ahead of
   // work already enqueued on the auxiliary stream
   if (cudaEventRecord(join, a) != cudaSuccess || cudaStreamWaitEvent(s, join, 0) != cudaSuccess)
