@@ -582,6 +582,7 @@ hlq_status hlq_debug_tc_gemm(int kind, const void* d_a, int64_t lda, const void*
   if (cluster_m && !gemm_tc_cluster_supported(bn ? bn : 128, cluster_m, cluster_n))
     return HLQ_ERR_INVALID_ARG;
   if (cluster_m * cluster_n > 1 && splits > 1) return HLQ_ERR_INVALID_ARG;
+  if (kind == 0 && splits > 1) return HLQ_ERR_INVALID_ARG;  // E4M3 GEMM runs unsplit
   const int esz = kind == 1 ? 2 : 1;
   if (lda < K || ldb < K || (lda * esz) % 16 || (ldb * esz) % 16) return HLQ_ERR_ALIGN;
   if (M * N > 0 && (!d_a || !d_b || !d_acc)) return HLQ_ERR_INVALID_ARG;

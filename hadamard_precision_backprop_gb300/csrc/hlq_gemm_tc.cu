@@ -31,6 +31,7 @@
 //               chunk, then dequantize and store fp32 rows.
 // Every mbarrier wait is bounded (HLQ_DEV_TIMEOUT, then the CTA winds down).
 #include <cstdint>
+#include <cstring>
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -133,7 +134,10 @@ struct TcCfg {
   static constexpr uint32_t kBBytes = BN * kRowBytes;
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;
   static constexpr uint32_t kTmemCols = 2 * BN;           // two accumulators
-  static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + 256;
+  // epilogue staging: one 32 x 32 fp32 box (128B-swizzled) per epilogue warp
+  static constexpr uint32_t kStageOutBytes = 32 * 32 * 4;
+  static constexpr size_t kSmem =
+      1024 + (size_t)kStages * kStageBytes + (size_t)kEpiWarps * kStageOutBytes + 256;
   static_assert(kSmem <= 232448, "227 KB of shared memory per CTA");
 };
 
@@ -147,6 +151,7 @@ struct TcCfg {
 template <int kKind, int BN, int kCm, int kCn>
 __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(
     const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+    const __grid_constant__ CUtensorMap tmOut, const __grid_constant__ CUtensorMap tmAcc,
     int M, int N, int num_kb, int chunk_kb, int kb_per_split, int splits, int tiles_n,
     int num_units, const float* __restrict__ sa, int per_row_a,
     const float* __restrict__ sb, float* __restrict__ out, int32_t* __restrict__ acc_out,
@@ -160,7 +165,8 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * C::kStageBytes);
+  uint8_t* stage_out = smem + kStages * C::kStageBytes;  // [kEpiWarps][4 KB]
+  uint64_t* full = reinterpret_cast<uint64_t*>(stage_out + C::kEpiWarps * C::kStageOutBytes);
   uint64_t* empty = full + kStages;
   uint64_t* tfull = empty + kStages;  // [2]
   uint64_t* tempty = tfull + 2;       // [2]
@@ -317,11 +323,72 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(
     const int quarter = warp & 3;  // TMEM lanes this warp may access
     const int colgrp = ew >> 2;
     const int row = quarter * 32 + lane;
+    uint8_t* stg = stage_out + ew * C::kStageOutBytes;
+    // One 32 x 32 box of 32-bit values (this thread's row, 32 columns)
+    // through the warp's staging buffer (128B swizzle: 16-byte chunk c of row
+    // r at c ^ (r % 8), conflict-free) and a TMA store, which clips rows >= M
+    // and columns >= N.
+    auto store_box = [&](const CUtensorMap* map, int x, int y, const uint32_t (&v)[32]) {
+      if (lane == 0) tma_store_wait_read();  // the previous box has been read
+      __syncwarp();
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<uint4*>(stg + lane * 128 + ((c ^ (lane & 7)) << 4)) =
+            make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) tma_store_2d(map, x, y, stg);
+    };
+    auto dequant_scale = [&](int m) {
+      return (out && m < M) ? (per_row_a ? sa[m] : sa[0]) * sb[0] * 0.0625f : 0.0f;
+    };
     int cc = 0;
     bool ok = true;
     for (int u = first_unit; u < num_units && ok; u += unit_step) {
       int m0, n0, kb0, nkb;
       unit_coords(u, m0, n0, kb0, nkb);
+      const int m = m0 + row;
+      const int nb = n0 + colgrp * C::kColsPerThread;
+      const int y = m0 + quarter * 32;
+      if constexpr (kKind == 0) {
+        // one accumulation chunk, never split: stream each 32-column TMEM
+        // slice straight into a store box
+        const int buf = cc & 1;
+        const uint32_t use = (uint32_t)(cc >> 1);
+        ++cc;
+        ok = mbar_wait(&tfull[buf], use & 1u, abort_flag, status);
+        ok = __all_sync(0xffffffffu, ok);  // also reconverges the warp
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) +
+                               (uint32_t)(buf * BN + colgrp * C::kColsPerThread);
+        const float scale = dequant_scale(m);
+#pragma unroll
+        for (int jc = 0; jc < C::kColsPerThread / 32; ++jc) {
+          uint32_t r[32];
+          tmem_ld_x32(taddr + 32 * jc, r);
+          if (jc == C::kColsPerThread / 32 - 1) {  // accumulator read out: release it
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[buf]);
+          }
+          const int x = nb + 32 * jc;
+          if (x >= N) continue;
+          if (acc_out) {
+            uint32_t v[32];
+#pragma unroll
+            for (int q = 0; q < 32; ++q) v[q] = (uint32_t)__float2int_rn(__uint_as_float(r[q]));
+            store_box(&tmAcc, x, y, v);
+          }
+          if (out) {
+#pragma unroll
+            for (int q = 0; q < 32; ++q)
+              r[q] = __float_as_uint((float)__float2int_rn(__uint_as_float(r[q])) * scale);
+            store_box(&tmOut, x, y, r);
+          }
+        }
+        continue;
+      }
       const int nch = (nkb + chunk_kb - 1) / chunk_kb;
       int32_t acc[C::kColsPerThread];
 #pragma unroll
@@ -348,25 +415,22 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(
         if (lane == 0) mbar_arrive(&tempty[buf]);
       }
       if (!ok) break;
-      const int m = m0 + row;
-      const int nb = n0 + colgrp * C::kColsPerThread;
       if (splits == 1) {
-        if (m < M) {
-          const float scale =
-              out ? (per_row_a ? sa[m] : sa[0]) * sb[0] * 0.0625f : 0.0f;
-          float* orow = out + (size_t)m * N;
+        const float scale = dequant_scale(m);
 #pragma unroll
-          for (int q = 0; q < C::kColsPerThread; q += 4) {
-            const int n = nb + q;
-            if (n + 4 <= N) {
-              if (out)
-                *reinterpret_cast<float4*>(orow + n) =
-                    make_float4((float)acc[q] * scale, (float)acc[q + 1] * scale,
-                                (float)acc[q + 2] * scale, (float)acc[q + 3] * scale);
-              if (acc_out)
-                *reinterpret_cast<int4*>(acc_out + (size_t)m * N + n) =
-                    make_int4(acc[q], acc[q + 1], acc[q + 2], acc[q + 3]);
-            }
+        for (int jc = 0; jc < C::kColsPerThread / 32; ++jc) {
+          const int x = nb + 32 * jc;
+          if (x >= N) break;
+          uint32_t v[32];
+          if (acc_out) {
+#pragma unroll
+            for (int q = 0; q < 32; ++q) v[q] = (uint32_t)acc[32 * jc + q];
+            store_box(&tmAcc, x, y, v);
+          }
+          if (out) {
+#pragma unroll
+            for (int q = 0; q < 32; ++q) v[q] = __float_as_uint((float)acc[32 * jc + q] * scale);
+            store_box(&tmOut, x, y, v);
           }
         }
         continue;
@@ -403,6 +467,7 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(
         }
       }
     }
+    if (lane == 0) tma_store_wait_all();  // boxes written before the CTA exits
   }
 
   tc_fence_before();
@@ -454,8 +519,24 @@ bool make_map(CUtensorMap* map, const void* ptr, bool bf16, int64_t rows, int64_
   return r == CUDA_SUCCESS;
 }
 
+// Output [rows, cols] of 32-bit elements (fp32 or int32), stored in 32 x 32
+// boxes with the 128-byte swizzle of the epilogue's staging buffers.
+bool make_out_map(CUtensorMap* map, const void* ptr, bool is_int, int64_t rows,
+                  int64_t cols) {
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(cols * 4)};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, is_int ? CU_TENSOR_MAP_DATA_TYPE_INT32 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                        2, const_cast<void*>(ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 template <int kKind, int BN, int kCm, int kCn>
-cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, int64_t M, int64_t N,
+cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& mo,
+                      const CUtensorMap& macc, int64_t M, int64_t N,
                       int num_kb, int chunk_kb, int splits, int num_sms, const float* sa,
                       bool per_row_a, const float* sb, float* out, int32_t* acc_out,
                       int32_t* split_acc, unsigned int* slab_count,
@@ -521,7 +602,8 @@ cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, int64_t M, int
   }
   cfg.attrs = attr;
   cfg.numAttrs = na;
-  cudaError_t le = cudaLaunchKernelEx(&cfg, kernel, a, b, (int)M, (int)N, num_kb, chunk_kb,
+  cudaError_t le = cudaLaunchKernelEx(&cfg, kernel, a, b, mo, macc, (int)M, (int)N, num_kb,
+                                      chunk_kb,
                                       kb_per_split, splits, (int)blocks_n, (int)units, sa,
                                       per_row_a ? 1 : 0, sb, out, acc_out, split_acc,
                                       slab_count, status);
@@ -605,11 +687,15 @@ cudaError_t launch_gemm_tc(int kind, const void* A, int64_t lda, const void* B,
   if (!get_encode()) return cudaErrorNotSupported;
   const bool bf16 = kind == 1;
   if (!gemm_tc_cluster_supported(plan.bn, plan.cm, plan.cn) ||
-      (plan.splits > 1 && plan.cm * plan.cn > 1))
+      (plan.splits > 1 && (plan.cm * plan.cn > 1 || kind == 0)))
     return cudaErrorInvalidValue;
-  CUtensorMap ma, mb;
+  CUtensorMap ma, mb, mo, macc;
   if (!make_map(&ma, A, bf16, M, K, lda, kBM / plan.cn)) return cudaErrorInvalidValue;
   if (!make_map(&mb, B, bf16, N, K, ldb, plan.bn / plan.cm)) return cudaErrorInvalidValue;
+  memset(&mo, 0, sizeof(mo));
+  memset(&macc, 0, sizeof(macc));
+  if (out && !make_out_map(&mo, out, false, M, N)) return cudaErrorInvalidValue;
+  if (acc_out && !make_out_map(&macc, acc_out, true, M, N)) return cudaErrorInvalidValue;
   int32_t* split_acc = nullptr;
   unsigned int* slab_count = nullptr;
   if (plan.splits > 1) {
@@ -628,7 +714,8 @@ cudaError_t launch_gemm_tc(int kind, const void* A, int64_t lda, const void* B,
       sms <= 0)
     return cudaErrorInvalidDevice;
 #define TC(KIND, BN, CM, CN)                                                          \
-  launch_tc<KIND, BN, CM, CN>(ma, mb, M, N, plan.num_kb, plan.chunk_kb, plan.splits,  \
+  launch_tc<KIND, BN, CM, CN>(ma, mb, mo, macc, M, N, plan.num_kb, plan.chunk_kb,      \
+                              plan.splits,                                            \
                               sms, sa, per_row_a, sb, out, acc_out, split_acc,        \
                               slab_count, status, st)
 #define TC_SHAPES(KIND, BN)                                   \

@@ -226,8 +226,8 @@ hlq_status hlq_debug_reference_gemm(int kind, const void *d_a, const void *d_b,
  * library's choice; > 1 needs d_ws of hlq_debug_tc_gemm_ws_bytes(M, N)).
  * cluster_m x cluster_n: thread-block cluster of tiles sharing operand tiles
  * by TMA multicast, one of 1x1, 2x1, 4x1, 2x2 (0 x 0 = the library's choice;
- * a K split forces 1x1).  M, N, K multiples of 16.  An unsupported plan is
- * HLQ_ERR_INVALID_ARG.
+ * a K split forces 1x1; kind 0 runs unsplit).  M, N, K multiples of 16.  An
+ * unsupported plan is HLQ_ERR_INVALID_ARG.
  */
 hlq_status hlq_debug_tc_gemm(int kind, const void *d_a, int64_t lda,
                              const void *d_b, int64_t ldb, int64_t M, int64_t N,

@@ -131,6 +131,7 @@ def test_tc_gemm_plan_validation(L):
     assert call(cm=4, cn=2) == 1
     assert call(cm=1, cn=0) == 1
     assert call(cm=2, splits=2) == 1          # a K split runs unclustered
+    assert call(kind=0, splits=2) == 1        # the E4M3 GEMM runs unsplit
     assert call(M=200) == 2
 
 
