@@ -12,8 +12,10 @@ Cin = 768, Cout = 2304, bf16 inputs, per-token g_y quantizer.
 Prints one JSON line (rank 0).  `value` is microseconds per layer step
 (lower is better), device-timed with CUDA events on the launching stream,
 inputs resident in HBM, L2 flushed (256 MiB write) before every timed step.
-`e2e` is the same through host buffers (pinned host -> device copies of
-x, g_y, w and device -> host copies of g_x, g_w inside the timed region).
+`e2e` is the same step through libhlq's host-buffer entry
+(hlq_layer_step_host): pinned host -> device copies of x, g_y, w and
+device -> host copies of g_x, g_w inside the timed region, pipelined with the
+kernels by the library.
 `roofline` is for the kernel with the largest device time, from per-launch
 CUDA events recorded by libhlq's tracing hooks; `cpu_baseline` times the CPU
 oracle on a bounded token sample on this host.
@@ -403,17 +405,18 @@ def run_ours(args, wl, rank, world, local_rank):
     ms_eager = statistics.mean(a.elapsed_time(b) for a, b in eager)
 
     # ---- end to end through host buffers ---------------------------------
+    # libhlq's host-buffer entry: pinned inputs in, gradients back out, the
+    # copies pipelined with the kernels inside the call
     h_gx = torch.empty((T, Cin), dtype=torch.float32).pin_memory()
     h_gw = torch.empty((Cout, Cin), dtype=torch.float32).pin_memory()
-    d_x, d_gy, d_w = torch.empty_like(x), torch.empty_like(gy), torch.empty_like(w)
+    dt_code = hlq.BF16 if wl.dtype == "bf16" else hlq.F32
+    ws_host = torch.empty(max(hlq.hlq_layer_step_host_workspace_bytes(
+        dt_code, T, Cin, Cout, 16, wl.rank), 256), dtype=torch.uint8, device=dev)
 
     def e2e_step():
-        d_x.copy_(h_x, non_blocking=True)
-        d_gy.copy_(h_gy, non_blocking=True)
-        d_w.copy_(h_w, non_blocking=True)
-        step(d_x, d_gy, d_w)
-        h_gx.copy_(gx, non_blocking=True)
-        h_gw.copy_(gw, non_blocking=True)
+        hlq.hlq_layer_step_host(h_x, h_gy, h_w, xbar, sx, rank=wl.rank,
+                                gran_gy=wl.gran_gy, gran_w=wl.gran_w, rnd=hlq.SR,
+                                seed=wl.seed, out_gx=h_gx, out_gw=h_gw, ws=ws_host)
 
     for _ in range(args.warmup):
         e2e_step()

@@ -38,6 +38,8 @@ EXPORTS = [
     "hlq_debug_reference_gemm", "hlq_debug_tc_gemm", "hlq_debug_tc_gemm_ws_bytes",
     "hlq_linear_backward_gx_noalloc", "hlq_noalloc_scratch_bytes",
     "hlq_linear_backward",
+    "hlq_layer_step_host",
+    "hlq_layer_step_host_workspace_bytes",
 ]
 
 _lock = threading.Lock()
@@ -95,6 +97,9 @@ def lib() -> ctypes.CDLL:
             "hlq_noalloc_scratch_bytes": (sz, []),
             "hlq_linear_backward": (i32, [P, P, P, P, i32, i64, i64, i64, i32, i32,
                                           i32, i32, i32, u64, P, P, P, sz, P]),
+            "hlq_layer_step_host": (i32, [P, P, P, i32, i64, i64, i64, i32, i32, i32,
+                                          i32, i32, u64, P, P, P, P, i64, P, sz, P]),
+            "hlq_layer_step_host_workspace_bytes": (sz, [i32, i64, i64, i64, i32, i32]),
             "hlq_trace_end": (i32, [P]),
             "hlq_trace_get": (i32, [i32, P, P]),
             "hlq_trace_free": (i32, []),
@@ -270,6 +275,49 @@ def hlq_linear_backward(g_y, w, xbar, xbar_scale, rank: int = 8,
         Cin, Cout, block, rank, gran_gy, gran_w, rnd, seed, _ptr(out_gx),
         _ptr(out_gw), _ptr(ws), ws.numel(), _stream(stream)),
         "hlq_linear_backward")
+    return out_gx, out_gw
+
+
+def _need_cpu_contig(*ts):
+    for t in ts:
+        if t is not None and (t.is_cuda or not t.is_contiguous()):
+            raise ValueError("host tensors must be contiguous CPU tensors")
+
+
+def hlq_layer_step_host_workspace_bytes(dtype_code: int, T: int, Cin: int, Cout: int,
+                                        block: int = 16, rank: int = 8) -> int:
+    return int(lib().hlq_layer_step_host_workspace_bytes(dtype_code, T, Cin, Cout, block,
+                                                         rank))
+
+
+def hlq_layer_step_host(x, g_y, w, xbar, xbar_scale, rank: int = 8,
+                        gran_gy: int = PER_TOKEN, gran_w: int = PER_TENSOR,
+                        rnd: int = SR, seed: int = 0, block: int = 16,
+                        out_gx=None, out_gw=None, ws=None, chunk_tokens: int = 0,
+                        stream=None):
+    """One layer step from host tensors (x, g_y, w on the CPU, pinned for
+    speed): compresses x into the device buffers xbar / xbar_scale and
+    returns host (g_x, g_w) fp32.  Asynchronous on `stream`: synchronize it
+    before reading the results."""
+    torch = _torch()
+    _need_cpu_contig(x, g_y, w, out_gx, out_gw)
+    _need_cuda_contig(xbar, xbar_scale)
+    T, Cout = g_y.shape
+    Cin = w.shape[1]
+    if w.shape[0] != Cout or tuple(x.shape) != (T, Cin) or not (x.dtype == g_y.dtype == w.dtype):
+        raise ValueError("shape/dtype mismatch between x, g_y and w")
+    if out_gx is None:
+        out_gx = torch.empty((T, Cin), dtype=torch.float32).pin_memory()
+    if out_gw is None:
+        out_gw = torch.empty((Cout, Cin), dtype=torch.float32).pin_memory()
+    dt = _dtype_code(g_y)
+    if ws is None:
+        n = hlq_layer_step_host_workspace_bytes(dt, T, Cin, Cout, block, rank)
+        ws = torch.empty(max(n, 256), dtype=torch.uint8, device=xbar.device)
+    _check(lib().hlq_layer_step_host(
+        _ptr(x), _ptr(g_y), _ptr(w), dt, T, Cin, Cout, block, rank, gran_gy, gran_w,
+        rnd, seed, _ptr(out_gx), _ptr(out_gw), _ptr(xbar), _ptr(xbar_scale),
+        chunk_tokens, _ptr(ws), ws.numel(), _stream(stream)), "hlq_layer_step_host")
     return out_gx, out_gw
 
 

@@ -75,9 +75,10 @@ inline void trace_after(const char* what, cudaStream_t s) {
   }
 }
 
-// Auxiliary streams per device for hlq_linear_backward: 0 runs the g_w
-// branch, 1 the HQ of w.  Created on first use, kept for the process.
-constexpr int kAuxStreams = 2;
+// Auxiliary streams per device: 0 runs the g_w branch, 1 the HQ of w, 2 the
+// host-to-device and 3 the device-to-host copies of hlq_layer_step_host.
+// Created on first use, kept for the process.
+constexpr int kAuxStreams = 4;
 cudaStream_t g_aux_stream[kMaxDevices][kAuxStreams] = {};
 std::mutex g_aux_mutex;
 
@@ -300,6 +301,51 @@ hlq_status gx_impl(const void* gy, const void* w, int dt, int64_t T,
   return HLQ_OK;
 }
 
+// ACBP: HLA of x along tokens, per-tensor amax pass, int8 codes [Cin, T'].
+hlq_status compress_launches(const void* x, bool bf16, int64_t T, int64_t Cin, int rank,
+                             int8_t* xbar, float* xscale, unsigned int* amax,
+                             unsigned int* status, cudaStream_t s) {
+  const int64_t Tp = T / 16 * rank;
+  HLQ_TRY(cudaMemsetAsync(amax, 0, 4, s));
+  HLQ_LAUNCH("hla_x_amax", s,
+             launch_hla(x, bf16, T, Cin, rank, true, false, amax, nullptr, 0, nullptr,
+                        status, s));
+  HLQ_LAUNCH("hla_x_quant", s,
+             launch_hla(x, bf16, T, Cin, rank, false, false, amax, xbar, Tp, xscale, status,
+                        s));
+  return HLQ_OK;
+}
+
+// HLA of g_y: per-tensor amax pass, then int8 codes stored as bf16 [Cout, ld].
+hlq_status hla_gy_launches(const void* gy, bool bf16, int64_t T, int64_t Cout, int rank,
+                           unsigned int* amax, void* qg, int64_t ld, float* sg,
+                           unsigned int* status, cudaStream_t s) {
+  HLQ_TRY(cudaMemsetAsync(amax, 0, 4, s));
+  HLQ_LAUNCH("hla_gy_amax", s,
+             launch_hla(gy, bf16, T, Cout, rank, true, true, amax, nullptr, 0, nullptr,
+                        status, s));
+  HLQ_LAUNCH("hla_gy_quant", s,
+             launch_hla(gy, bf16, T, Cout, rank, false, true, amax, qg, ld, sg, status, s));
+  return HLQ_OK;
+}
+
+// ACBP buffer widened to bf16, then the g_w GEMM with its dequantization.
+hlq_status gw_gemm_launches(const int8_t* xbar, const float* xscale, int64_t Cin,
+                            int64_t Cout, int64_t Tp, const GwLayout& L, uint8_t* base,
+                            float* gw, int32_t* dbg_acc, unsigned int* status,
+                            cudaStream_t s) {
+  void* xw = base + L.xw;
+  const float* sg = reinterpret_cast<const float*>(base + L.sg);
+  HLQ_LAUNCH("widen_xbar", s, launch_widen_i8_bf16(xbar, xw, Cin, Tp, L.ld, s));
+  const int sms = device_sm_count();
+  if (sms <= 0) return HLQ_ERR_CUDA;
+  const GemmPlan plan = plan_gemm_tc(1, Cout, Cin, Tp, sms, 16);
+  HLQ_LAUNCH("gemm_gw_tc", s,
+             launch_gemm_tc(1, base + L.qg, L.ld, xw, L.ld, Cout, Cin, Tp, plan, sg, false,
+                            xscale, gw, dbg_acc, base + L.split, status, s));
+  return HLQ_OK;
+}
+
 hlq_status gw_impl(const void* gy, int dt, const int8_t* xbar,
                    const float* xscale, int64_t T, int64_t Cin, int64_t Cout,
                    int block, int rank, float* gw, void* ws, size_t ws_bytes,
@@ -335,25 +381,54 @@ hlq_status gw_impl(const void* gy, int dt, const int8_t* xbar,
   void* qg = base + L.qg;
   const bool bf16 = dt == HLQ_BF16;
 
-  HLQ_TRY(cudaMemsetAsync(amax, 0, 4, s));
-  void* xw = base + L.xw;
-  HLQ_LAUNCH("hla_gy_amax", s,
-             launch_hla(gy, bf16, T, Cout, rank, true, true, amax, nullptr, 0,
-                        nullptr, status, s));
-  HLQ_LAUNCH("hla_gy_quant", s,
-             launch_hla(gy, bf16, T, Cout, rank, false, true, amax, qg, L.ld,
-                        sg, status, s));
-  HLQ_LAUNCH("widen_xbar", s, launch_widen_i8_bf16(xbar, xw, Cin, Tp, L.ld, s));
-  const int sms = device_sm_count();
-  if (sms <= 0) return HLQ_ERR_CUDA;
-  const GemmPlan plan = plan_gemm_tc(1, Cout, Cin, Tp, sms, 16);
-  HLQ_LAUNCH("gemm_gw_tc", s,
-             launch_gemm_tc(1, qg, L.ld, xw, L.ld, Cout, Cin, Tp, plan, sg, false,
-                            xscale, gw, dbg_acc, base + L.split, status, s));
+  st = hla_gy_launches(gy, bf16, T, Cout, rank, amax, qg, L.ld, sg, status, s);
+  if (st != HLQ_OK) return st;
+  st = gw_gemm_launches(xbar, xscale, Cin, Cout, Tp, L, base, gw, dbg_acc, status, s);
+  if (st != HLQ_OK) return st;
   if (dbg_qg) HLQ_TRY(launch_decode_bf16(qg, dbg_qg, Cout, Tp, L.ld, s));
   if (dbg_sg) HLQ_TRY(cudaMemcpyAsync(dbg_sg, sg, 4, cudaMemcpyDeviceToDevice, s));
   return HLQ_OK;
 }
+
+
+// Workspace of hlq_layer_step_host: device copies of the inputs and outputs,
+// then the workspaces of the compression and of the two gradient branches.
+struct StepLayout {
+  size_t x, gy, w, gx, gw, cws, gxws, gwws, total;
+};
+
+StepLayout step_layout(int dt, int64_t T, int64_t Cin, int64_t Cout, int rank) {
+  const size_t esz = dt == HLQ_BF16 ? 2 : 4;
+  StepLayout L{};
+  size_t o = 0;
+  L.x = o;    o += align_up((size_t)T * (size_t)Cin * esz);
+  L.gy = o;   o += align_up((size_t)T * (size_t)Cout * esz);
+  L.w = o;    o += align_up((size_t)Cout * (size_t)Cin * esz);
+  L.gx = o;   o += align_up((size_t)T * (size_t)Cin * 4);
+  L.gw = o;   o += align_up((size_t)Cout * (size_t)Cin * 4);
+  L.cws = o;  o += align_up(compress_ws(T, Cin));
+  L.gxws = o; o += gx_layout(T, Cin, Cout).total;
+  L.gwws = o; o += gw_layout(T, Cin, Cout, rank).total;
+  L.total = o;
+  return L;
+}
+
+// Events of one hlq_layer_step_host call (destroyed when it returns; the
+// runtime keeps pending ones alive until they complete).
+struct EventSet {
+  cudaEvent_t ev[72] = {};
+  int n = 0;
+  cudaEvent_t make() {
+    if (n >= 72) return nullptr;
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return nullptr;
+    ev[n++] = e;
+    return e;
+  }
+  ~EventSet() {
+    for (int i = 0; i < n; ++i) cudaEventDestroy(ev[i]);
+  }
+};
 
 }  // namespace
 
@@ -414,16 +489,8 @@ hlq_status hlq_compress_activation(const void* d_x, int dt, int64_t T,
   }
   unsigned int* status = device_status_ptr();
   if (!status) return HLQ_ERR_CUDA;
-  unsigned int* amax = static_cast<unsigned int*>(d_ws);
-  const bool bf16 = dt == HLQ_BF16;
-  HLQ_TRY(cudaMemsetAsync(amax, 0, 4, s));
-  HLQ_LAUNCH("hla_x_amax", s,
-             launch_hla(d_x, bf16, T, Cin, rank, true, false, amax, nullptr, 0,
-                        nullptr, status, s));
-  HLQ_LAUNCH("hla_x_quant", s,
-             launch_hla(d_x, bf16, T, Cin, rank, false, false, amax, d_xbar, Tp,
-                        d_xbar_scale, status, s));
-  return HLQ_OK;
+  return compress_launches(d_x, dt == HLQ_BF16, T, Cin, rank, d_xbar, d_xbar_scale,
+                           static_cast<unsigned int*>(d_ws), status, s);
 }
 
 hlq_status hlq_linear_backward(const void* d_gy, const void* d_w, const int8_t* d_xbar,
@@ -475,6 +542,205 @@ hlq_status hlq_linear_backward(const void* d_gy, const void* d_w, const int8_t* 
     r = HLQ_ERR_CUDA;
   cudaEventDestroy(fork);
   cudaEventDestroy(join);
+  return r;
+}
+
+size_t hlq_layer_step_host_workspace_bytes(int dt, int64_t T, int64_t Cin, int64_t Cout,
+                                           int block, int rank) {
+  (void)block;
+  if (T < 0 || Cin < 0 || Cout < 0 || (dt != HLQ_F32 && dt != HLQ_BF16)) return 0;
+  return step_layout(dt, T, Cin, Cout, rank_ok(rank) ? rank : 16).total;
+}
+
+hlq_status hlq_layer_step_host(const void* h_x, const void* h_gy, const void* h_w, int dt,
+                               int64_t T, int64_t Cin, int64_t Cout, int block, int rank,
+                               int gran_gy, int gran_w, int rnd, uint64_t seed, float* h_gx,
+                               float* h_gw, int8_t* d_xbar, float* d_xbar_scale,
+                               int64_t chunk_tokens, void* d_ws, size_t ws_bytes,
+                               void* stream) {
+  hlq_status st = check_common(dt, T, Cin, Cout, block);
+  if (st != HLQ_OK) return st;
+  if (!rank_ok(rank) || chunk_tokens < 0) return HLQ_ERR_INVALID_ARG;
+  if ((T * Cin > 0 && (!h_x || !h_gx)) || (T * Cout > 0 && !h_gy) ||
+      (Cout * Cin > 0 && (!h_w || !h_gw)))
+    return HLQ_ERR_INVALID_ARG;
+  const StepLayout L = step_layout(dt, T, Cin, Cout, rank);
+  if (!d_ws || ws_bytes < L.total) return HLQ_ERR_WORKSPACE;
+  if (!aligned256(d_ws)) return HLQ_ERR_ALIGN;
+  uint8_t* base = static_cast<uint8_t*>(d_ws);
+  void* x = base + L.x;
+  void* gy = base + L.gy;
+  void* w = base + L.w;
+  float* gx = reinterpret_cast<float*>(base + L.gx);
+  float* gw = reinterpret_cast<float*>(base + L.gw);
+  const size_t gx_bytes = gx_layout(T, Cin, Cout).total;
+  const size_t gw_bytes = gw_layout(T, Cin, Cout, rank).total;
+  // validate every device step before anything is enqueued
+  st = gx_impl(gy, w, dt, T, Cin, Cout, block, gran_gy, gran_w, rnd, seed, gx, base + L.gxws,
+               gx_bytes, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, true);
+  if (st != HLQ_OK) return st;
+  st = gw_impl(gy, dt, d_xbar, d_xbar_scale, T, Cin, Cout, block, rank, gw, base + L.gwws,
+               gw_bytes, nullptr, nullptr, nullptr, nullptr, true);
+  if (st != HLQ_OK) return st;
+  if (!d_xbar_scale) return HLQ_ERR_INVALID_ARG;
+  if (!aligned16(d_xbar)) return HLQ_ERR_ALIGN;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t esz = dt == HLQ_BF16 ? 2 : 4;
+  const int64_t Tp = T / 16 * rank;
+  auto h2d = [](void* d, const void* h, size_t n, cudaStream_t q) {
+    return n ? cudaMemcpyAsync(d, h, n, cudaMemcpyHostToDevice, q) : cudaSuccess;
+  };
+  auto d2h = [](void* h, const void* d, size_t n, cudaStream_t q) {
+    return n ? cudaMemcpyAsync(h, d, n, cudaMemcpyDeviceToHost, q) : cudaSuccess;
+  };
+  if (T == 0 || Cin == 0 || Cout == 0) {  // degenerate sizes: one stream, in order
+    HLQ_TRY(h2d(x, h_x, (size_t)(T * Cin) * esz, s));
+    HLQ_TRY(h2d(gy, h_gy, (size_t)(T * Cout) * esz, s));
+    HLQ_TRY(h2d(w, h_w, (size_t)(Cout * Cin) * esz, s));
+    st = hlq_compress_activation(x, dt, T, Cin, block, rank, d_xbar, d_xbar_scale,
+                                 base + L.cws, compress_ws(T, Cin), stream);
+    if (st != HLQ_OK) return st;
+    st = hlq_linear_backward_gx(gy, w, dt, T, Cin, Cout, block, gran_gy, gran_w, rnd, seed,
+                                gx, base + L.gxws, gx_bytes, stream);
+    if (st != HLQ_OK) return st;
+    st = hlq_linear_backward_gw(gy, dt, d_xbar, d_xbar_scale, T, Cin, Cout, block, rank, gw,
+                                base + L.gwws, gw_bytes, stream);
+    if (st != HLQ_OK) return st;
+    HLQ_TRY(d2h(h_gx, gx, (size_t)(T * Cin) * 4, s));
+    HLQ_TRY(d2h(h_gw, gw, (size_t)(Cout * Cin) * 4, s));
+    return HLQ_OK;
+  }
+
+  // chunks of g_y rows: multiples of 128 (GEMM tiles), ~16 MB each, <= 64
+  int64_t ch = chunk_tokens;
+  if (ch == 0) ch = (int64_t)((16u << 20) / ((size_t)Cout * esz));
+  ch = (ch + 127) / 128 * 128;
+  if (ch < 128) ch = 128;
+  if ((T + ch - 1) / ch > 64) ch = ((T + 63) / 64 + 127) / 128 * 128;
+  const int nc = (int)((T + ch - 1) / ch);
+
+  cudaStream_t a_gw = aux_stream(0), a_w = aux_stream(1), cin = aux_stream(2),
+               cout = aux_stream(3);
+  if (!a_gw || !a_w || !cin || !cout) return HLQ_ERR_CUDA;
+  unsigned int* status = device_status_ptr();
+  if (!status) return HLQ_ERR_CUDA;
+  const int sms = device_sm_count();
+  if (sms <= 0) return HLQ_ERR_CUDA;
+
+  EventSet E;
+  cudaEvent_t fork = E.make(), w_in = E.make(), x_in = E.make(), w_done = E.make(),
+              gw_done = E.make(), out_done = E.make();
+  cudaEvent_t gy_in[64], gx_done[64];
+  for (int c = 0; c < nc; ++c) {
+    gy_in[c] = E.make();
+    gx_done[c] = E.make();
+  }
+  if (!fork || !w_in || !x_in || !w_done || !gw_done || !out_done || !gy_in[nc - 1] ||
+      !gx_done[nc - 1])
+    return HLQ_ERR_CUDA;
+
+  const bool bf16 = dt == HLQ_BF16;
+  const bool per_token = gran_gy == HLQ_PER_TOKEN;
+  uint8_t* gxb = base + L.gxws;
+  const GxLayout GL = gx_layout(T, Cin, Cout);
+  unsigned int* gx_amax = reinterpret_cast<unsigned int*>(gxb + GL.amax);
+  float* sgy = reinterpret_cast<float*>(gxb + GL.sgy);
+  float* sw = reinterpret_cast<float*>(gxb + GL.sw);
+  uint8_t* qy = gxb + GL.qy;
+  uint8_t* qw = gxb + GL.qw;
+  uint8_t* gwb = base + L.gwws;
+  const GwLayout WL = gw_layout(T, Cin, Cout, rank);
+  unsigned int* gw_amax = reinterpret_cast<unsigned int*>(gwb + WL.amax);
+  float* sg = reinterpret_cast<float*>(gwb + WL.sg);
+
+  hlq_status r = HLQ_OK;
+  auto fail = [&](cudaError_t e) {
+    if (e != cudaSuccess && r == HLQ_OK) r = HLQ_ERR_CUDA;
+  };
+  fail(cudaEventRecord(fork, s));
+  // copy-in stream: w (first needed), the g_y chunks, then x
+  fail(cudaStreamWaitEvent(cin, fork, 0));
+  fail(h2d(w, h_w, (size_t)(Cout * Cin) * esz, cin));
+  fail(cudaEventRecord(w_in, cin));
+  for (int c = 0; c < nc; ++c) {
+    const int64_t r0 = c * ch, rows = (r0 + ch <= T ? ch : T - r0);
+    fail(h2d(static_cast<uint8_t*>(gy) + (size_t)r0 * Cout * esz,
+             static_cast<const uint8_t*>(h_gy) + (size_t)r0 * Cout * esz,
+             (size_t)rows * Cout * esz, cin));
+    fail(cudaEventRecord(gy_in[c], cin));
+  }
+  fail(h2d(x, h_x, (size_t)(T * Cin) * esz, cin));
+  fail(cudaEventRecord(x_in, cin));
+  // HQ of w
+  fail(cudaStreamWaitEvent(a_w, w_in, 0));
+  fail(cudaMemsetAsync(gx_amax + 1, 0, 4, a_w));
+  if (r == HLQ_OK) r = hq_w_launches(w, bf16, Cout, Cin, gx_amax + 1, qw, sw, rnd, seed, status, a_w);
+  fail(cudaEventRecord(w_done, a_w));
+  // g_x branch on the caller's stream, chunk by chunk
+  fail(cudaMemsetAsync(gx_amax, 0, 4, s));
+  auto gemm_chunk = [&](int c) {
+    const int64_t r0 = c * ch, rows = (r0 + ch <= T ? ch : T - r0);
+    const GemmPlan plan = plan_gemm_tc(0, rows, Cin, Cout, sms, 1);
+    if (r == HLQ_OK) {
+      trace_before(s);
+      fail(launch_gemm_tc(0, qy + (size_t)r0 * Cout, Cout, qw, Cout, rows, Cin, Cout, plan,
+                          per_token ? sgy + r0 : sgy, per_token, sw, gx + (size_t)r0 * Cin,
+                          nullptr, nullptr, status, s));
+      trace_after("gemm_gx_tc", s);
+    }
+    fail(cudaEventRecord(gx_done[c], s));
+  };
+  for (int c = 0; c < nc && r == HLQ_OK; ++c) {
+    const int64_t r0 = c * ch, rows = (r0 + ch <= T ? ch : T - r0);
+    fail(cudaStreamWaitEvent(s, gy_in[c], 0));
+    const uint8_t* gyc = static_cast<const uint8_t*>(gy) + (size_t)r0 * Cout * esz;
+    if (per_token) {
+      trace_before(s);
+      fail(launch_hq_rows(gyc, bf16, rows, Cout, true, false, gx_amax, qy + (size_t)r0 * Cout,
+                          sgy + r0, rnd, seed, 0, status, s, r0));
+      trace_after("hq_rows_quant", s);
+      if (c == 0) fail(cudaStreamWaitEvent(s, w_done, 0));
+      gemm_chunk(c);
+    } else {
+      trace_before(s);
+      fail(launch_hq_rows(gyc, bf16, rows, Cout, false, true, gx_amax, nullptr, nullptr, rnd,
+                          seed, 0, status, s, r0));
+      trace_after("hq_rows_amax", s);
+    }
+  }
+  if (!per_token && r == HLQ_OK) {  // the per-tensor scale needs all of g_y
+    trace_before(s);
+    fail(launch_hq_rows(gy, bf16, T, Cout, false, false, gx_amax, qy, sgy, rnd, seed, 0,
+                        status, s, 0));
+    trace_after("hq_rows_quant", s);
+    fail(cudaStreamWaitEvent(s, w_done, 0));
+    for (int c = 0; c < nc; ++c) gemm_chunk(c);
+  }
+  // g_w branch: HLA of g_y once all of it is in, then x's compression
+  fail(cudaStreamWaitEvent(a_gw, gy_in[nc - 1], 0));
+  if (r == HLQ_OK)
+    r = hla_gy_launches(gy, bf16, T, Cout, rank, gw_amax, gwb + WL.qg, WL.ld, sg, status, a_gw);
+  fail(cudaStreamWaitEvent(a_gw, x_in, 0));
+  if (r == HLQ_OK)
+    r = compress_launches(x, bf16, T, Cin, rank, d_xbar, d_xbar_scale,
+                          reinterpret_cast<unsigned int*>(base + L.cws), status, a_gw);
+  if (r == HLQ_OK)
+    r = gw_gemm_launches(d_xbar, d_xbar_scale, Cin, Cout, Tp, WL, gwb, gw, nullptr, status,
+                         a_gw);
+  fail(cudaEventRecord(gw_done, a_gw));
+  // copy-out stream: g_x chunk by chunk as they finish, then g_w
+  for (int c = 0; c < nc; ++c) {
+    const int64_t r0 = c * ch, rows = (r0 + ch <= T ? ch : T - r0);
+    fail(cudaStreamWaitEvent(cout, gx_done[c], 0));
+    fail(d2h(h_gx + (size_t)r0 * Cin, gx + (size_t)r0 * Cin, (size_t)rows * Cin * 4, cout));
+  }
+  fail(cudaStreamWaitEvent(cout, gw_done, 0));
+  fail(d2h(h_gw, gw, (size_t)(Cout * Cin) * 4, cout));
+  fail(cudaEventRecord(out_done, cout));
+  // join every stream back into the caller's (also after a failure)
+  fail(cudaStreamWaitEvent(s, out_done, 0));
+  fail(cudaStreamWaitEvent(s, w_done, 0));
   return r;
 }
 

@@ -12,13 +12,15 @@ namespace hlq {
 
 // HQ of a [rows, cols] tensor along cols (g_y).  amax_only: per-tensor
 // pre-pass into *amax_slot.  Otherwise writes E4M3 codes [rows, cols] and
-// scales ([rows] if per_token else [1], from *amax_slot).
+// scales ([rows] if per_token else [1], from *amax_slot).  The rows may be
+// rows row0 .. of a larger tensor (pointers already offset): the random
+// words are drawn for their element indices in that tensor.
 cudaError_t launch_hq_rows(const void* src, bool bf16, int64_t rows,
                            int64_t cols, bool per_token, bool amax_only,
                            unsigned int* amax_slot, uint8_t* codes,
                            float* scales, int rnd, uint64_t seed,
                            uint32_t stream_id, unsigned int* status,
-                           cudaStream_t st);
+                           cudaStream_t st, int64_t row0 = 0);
 
 // HQ of a [rows, cols] tensor along rows (w), codes written transposed
 // [cols, rows] (E4M3), per-tensor scale from *amax_slot.

@@ -244,14 +244,17 @@ __device__ __forceinline__ void unpack(const RawOct<false>& r, float* v) {
   v[4] = r.b.x; v[5] = r.b.y; v[6] = r.b.z; v[7] = r.b.w;
 }
 
-// Quantize one transformed octet (elements e0 .. e0+7) to E4M3 int4 codes.
+// Quantize one transformed octet (elements e0 .. e0+7 of `codes`) to E4M3
+// int4 codes; the random words are those of elements e_off + e0 .. of the
+// whole tensor.
 __device__ __forceinline__ void quantize_octet(const float* v, float s, int rnd,
                                                const PhiloxKeys& keys, uint32_t stream,
-                                               int64_t e0, uint8_t* codes) {
+                                               int64_t e0, int64_t e_off, uint8_t* codes) {
   float r[8];
   if (rnd == HLQ_SR) {
-    const U4 a = philox_block_k(keys, stream, (uint64_t)e0 >> 2);
-    const U4 b = philox_block_k(keys, stream, ((uint64_t)e0 >> 2) + 1);
+    const uint64_t q = (uint64_t)(e_off + e0) >> 2;
+    const U4 a = philox_block_k(keys, stream, q);
+    const U4 b = philox_block_k(keys, stream, q + 1);
     r[0] = quant_sr_f(v[0], s, a.x, 7.0f);
     r[1] = quant_sr_f(v[1], s, a.y, 7.0f);
     r[2] = quant_sr_f(v[2], s, a.z, 7.0f);
@@ -296,7 +299,7 @@ __global__ void __launch_bounds__(256) hq_rows_kernel(
     const void* __restrict__ src, int64_t rows, int64_t cols,
     unsigned int* __restrict__ amax_slot, uint8_t* __restrict__ codes,
     float* __restrict__ scales, int rnd, uint64_t seed, uint32_t stream,
-    unsigned int* __restrict__ status, int stage) {
+    unsigned int* __restrict__ status, int stage, int64_t e_off) {
   pdl_trigger();
   pdl_wait();
   extern __shared__ float4 srow[];
@@ -367,7 +370,7 @@ __global__ void __launch_bounds__(256) hq_rows_kernel(
       if (oct >= n_oct) break;
       const float4 a = my[(2 * it) * 32 + lane], b = my[(2 * it + 1) * 32 + lane];
       const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-      quantize_octet(v, s, rnd, keys, stream, base + (int64_t)oct * 8, codes);
+      quantize_octet(v, s, rnd, keys, stream, base + (int64_t)oct * 8, e_off, codes);
     }
     return;
   }
@@ -380,7 +383,7 @@ __global__ void __launch_bounds__(256) hq_rows_kernel(
                                         it + 1 < iters && nx < n_oct);
     float v[8];
     transform_raw<kBf16>(cur, v, status);
-    if (oct < n_oct) quantize_octet(v, s, rnd, keys, stream, base + (int64_t)oct * 8, codes);
+    if (oct < n_oct) quantize_octet(v, s, rnd, keys, stream, base + (int64_t)oct * 8, e_off, codes);
     cur = nxt;
   }
 }
@@ -1126,7 +1129,8 @@ cudaError_t launch_hq_rows(const void* src, bool bf16, int64_t rows,
                            unsigned int* amax_slot, uint8_t* codes,
                            float* scales, int rnd, uint64_t seed,
                            uint32_t stream_id, unsigned int* status,
-                           cudaStream_t st) {
+                           cudaStream_t st, int64_t row0) {
+  if (rows == 0) return cudaSuccess;
   const int threads = 256, warps = threads / 32;
   dim3 grid(grid1(rows, warps));
   // per-token rows wait transformed (fp32) in shared memory between the two
@@ -1141,7 +1145,7 @@ cudaError_t launch_hq_rows(const void* src, bool bf16, int64_t rows,
       return cudaGetLastError();                                                  \
     launch_pdl(hq_rows_kernel<B, M, P>, grid, dim3(threads), smem, st, src, rows,  \
                cols, amax_slot, codes, scales, rnd, seed, stream_id, status,       \
-               stage ? 1 : 0);                                                    \
+               stage ? 1 : 0, row0 * cols);                                       \
   } while (0)
   if (amax_only) {
     if (bf16) HQR(true, kAmax, false); else HQR(false, kAmax, false);

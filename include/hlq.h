@@ -138,11 +138,11 @@ hlq_status hlq_linear_backward_gw(const void *d_gy, int dt, const int8_t *d_xbar
 
 /*
  * The whole backward pass of the layer: g_x exactly as hlq_linear_backward_gx
- * and g_w exactly as hlq_linear_backward_gw, with the two independent
- * branches overlapped on the GPU.  The g_w branch runs on an auxiliary
- * stream of the library (one per device, created on first use) forked from
- * and joined back into `stream` with events, so all work is still ordered
- * after what precedes the call on `stream` and before what follows it.
+ * and g_w exactly as hlq_linear_backward_gw, with the independent branches
+ * overlapped on the GPU.  The g_w branch and the HQ of w run on auxiliary
+ * streams of the library (per device, created on first use) forked from and
+ * joined back into `stream` with events, so all work is still ordered after
+ * what precedes the call on `stream` and before what follows it.
  * Workspace: hlq_workspace_bytes(HLQ_OP_BACKWARD, ...).  Arguments are the
  * union of the two calls'.
  */
@@ -237,6 +237,41 @@ hlq_status hlq_debug_tc_gemm(int kind, const void *d_a, int64_t lda,
 size_t hlq_debug_tc_gemm_ws_bytes(int64_t M, int64_t N);
 
 /*
+ * One layer step from HOST buffers, every host<->device copy inside the
+ * call: the ACBP compression of x (as hlq_compress_activation) and both
+ * gradients (as hlq_linear_backward), results copied back to the host.
+ * This entry has no counterpart in the pages (they run inside a training
+ * framework with device-resident tensors); it serves callers whose data
+ * lives in host memory, and it overlaps the copies with the computation:
+ * g_y goes up in chunks of `chunk_tokens` rows (a multiple of 128; 0 = the
+ * library's choice, ~16 MB of g_y per chunk) on a copy stream, the HQ of
+ * each chunk and its g_x GEMM start as soon as it has landed, each g_x chunk
+ * goes back to the host on a second copy stream while later chunks compute,
+ * and the g_w branch (HLA of g_y, then the compression of x, the widening
+ * and the g_w GEMM) runs alongside.  Results are bit-identical to the
+ * device entry points on the same inputs.
+ *   h_x [T, Cin], h_gy [T, Cout], h_w [Cout, Cin]: host, dtype dt;
+ *   h_gx [T, Cin], h_gw [Cout, Cin]: host fp32 outputs;
+ *   d_xbar [Cin, T'] int8 and d_xbar_scale [1]: device, filled by the call
+ *   (the stored activation of the step);
+ *   d_ws: device workspace of hlq_layer_step_host_workspace_bytes(...),
+ *   which also holds the device copies of the inputs and outputs.
+ * Host buffers should be page-locked (cudaHostAlloc / cudaHostRegister):
+ * pageable memory works but the copies are then staged and slower.  The call
+ * is asynchronous on `stream`: the host buffers must stay valid, and h_gx /
+ * h_gw are complete, only once `stream` has reached the end of the call.
+ * Arguments are validated as for the device entry points (host pointers
+ * non-null when their tensor is non-empty; chunk_tokens >= 0).
+ */
+hlq_status hlq_layer_step_host(const void *h_x, const void *h_gy, const void *h_w,
+                               int dt, int64_t T, int64_t Cin, int64_t Cout,
+                               int block, int rank, int gran_gy, int gran_w,
+                               int rnd, uint64_t seed, float *h_gx, float *h_gw,
+                               int8_t *d_xbar, float *d_xbar_scale,
+                               int64_t chunk_tokens, void *d_ws, size_t ws_bytes,
+                               void *stream);
+size_t hlq_layer_step_host_workspace_bytes(int dt, int64_t T, int64_t Cin,
+                                           int64_t Cout, int block, int rank);/*
  * Launch tracing, for timing without a profiler.  hlq_trace_begin creates
  * 2*capacity CUDA events (host-side objects, no device memory) and turns
  * tracing on: every later kernel launch of this library, on any stream, is

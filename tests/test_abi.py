@@ -135,6 +135,35 @@ def test_tc_gemm_plan_validation(L):
     assert call(M=200) == 2
 
 
+def test_step_host_validation_and_workspace(L):
+    f = L.hlq_layer_step_host
+    nb = L.hlq_layer_step_host_workspace_bytes
+    assert nb(1, 256, 64, 128, 16, 8) > 0 and nb(1, 256, 64, 128, 16, 8) % 256 == 0
+    assert nb(0, 256, 64, 128, 16, 8) > nb(1, 256, 64, 128, 16, 8)  # fp32 inputs
+    assert nb(7, 256, 64, 128, 16, 8) == 0 and nb(1, -16, 64, 128, 16, 8) == 0
+
+    def call(**kw):
+        a = dict(hx=FAKE, hgy=FAKE, hw=FAKE, dt=1, T=256, Cin=64, Cout=128, block=16,
+                 rank=8, gran_gy=1, gran_w=0, rnd=1, seed=0, hgx=FAKE, hgw=FAKE,
+                 xbar=FAKE, xs=FAKE, chunk=0, ws=FAKE_WS, ws_bytes=1 << 30)
+        a.update(kw)
+        return f(a["hx"], a["hgy"], a["hw"], a["dt"], a["T"], a["Cin"], a["Cout"],
+                 a["block"], a["rank"], a["gran_gy"], a["gran_w"], a["rnd"], a["seed"],
+                 a["hgx"], a["hgw"], a["xbar"], a["xs"], a["chunk"], a["ws"],
+                 a["ws_bytes"], None)
+
+    assert call(hx=None) == 1
+    assert call(hgw=None) == 1
+    assert call(chunk=-1) == 1
+    assert call(rank=3) == 1
+    assert call(T=17) == 2
+    assert call(ws_bytes=4096) == 5
+    assert call(ws=FAKE_WS + 128) == 3
+    assert call(xbar=FAKE + 4) == 3
+    assert call(xs=None) == 1
+    assert call(gran_w=1) == 4
+
+
 def test_read_status_rejects_null(L):
     assert L.hlq_read_device_status(None, 0, None) == 1
 
