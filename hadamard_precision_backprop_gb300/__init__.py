@@ -90,7 +90,7 @@ def lib() -> ctypes.CDLL:
             "hlq_trace_begin": (i32, [i32]),
             "hlq_debug_reference_gemm": (i32, [i32, P, P, i64, i64, i64, P, P]),
             "hlq_debug_tc_gemm": (i32, [i32, P, i64, P, i64, i64, i64, i64, i32,
-                                        i32, i32, i32, P, P, sz, P]),
+                                        i32, P, P, sz, P]),
             "hlq_debug_tc_gemm_ws_bytes": (sz, [i64, i64]),
             "hlq_linear_backward_gx_noalloc": (i32, [P, P, i32, i64, i64, i64, i32,
                                                      i32, i32, i32, u64, P, P]),
@@ -408,11 +408,9 @@ def hlq_debug_reference_gemm(a, b, stream=None):
     return acc
 
 
-def hlq_debug_tc_gemm(kind, a, b, bn=0, splits=0, cluster=(0, 0), stream=None):
+def hlq_debug_tc_gemm(kind, a, b, bn=0, splits=0, stream=None):
     """int32 a @ b^T on the tensor cores with an explicit plan.  kind 0: a, b
-    are uint8 E4M3 codes [M, K] / [N, K]; kind 1: bf16 codes.  cluster:
-    (CTAs along M, CTAs along N) sharing operand tiles, (0, 0) = library's
-    choice."""
+    are uint8 E4M3 codes [M, K] / [N, K]; kind 1: bf16 codes."""
     torch = _torch()
     _need_cuda_contig(a, b)
     M, K = a.shape
@@ -421,8 +419,7 @@ def hlq_debug_tc_gemm(kind, a, b, bn=0, splits=0, cluster=(0, 0), stream=None):
     nws = int(lib().hlq_debug_tc_gemm_ws_bytes(M, N))
     ws = torch.empty(max(nws, 256), dtype=torch.uint8, device=a.device)
     _check(lib().hlq_debug_tc_gemm(kind, _ptr(a), K, _ptr(b), K, M, N, K, bn,
-                                   splits, int(cluster[0]), int(cluster[1]),
-                                   _ptr(acc), _ptr(ws), ws.numel(),
+                                   splits, _ptr(acc), _ptr(ws), ws.numel(),
                                    _stream(stream)), "hlq_debug_tc_gemm")
     return acc
 

@@ -838,16 +838,12 @@ hlq_status hlq_debug_reference_gemm(int kind, const void* d_a, const void* d_b,
 
 hlq_status hlq_debug_tc_gemm(int kind, const void* d_a, int64_t lda, const void* d_b,
                              int64_t ldb, int64_t M, int64_t N, int64_t K, int bn,
-                             int splits, int cluster_m, int cluster_n, int32_t* d_acc,
-                             void* d_ws, size_t ws_bytes, void* stream) {
+                             int splits, int32_t* d_acc, void* d_ws, size_t ws_bytes,
+                             void* stream) {
   if (kind != 0 && kind != 1) return HLQ_ERR_INVALID_ARG;
   if (M < 0 || N < 0 || K < 0 || N % 16 || K % 16 || M % 16) return HLQ_ERR_SHAPE;
   if (bn != 0 && bn != 128 && bn != 256) return HLQ_ERR_INVALID_ARG;
   if (splits < 0 || splits > 64) return HLQ_ERR_INVALID_ARG;
-  if ((cluster_m == 0) != (cluster_n == 0)) return HLQ_ERR_INVALID_ARG;
-  if (cluster_m && !gemm_tc_cluster_supported(bn ? bn : 128, cluster_m, cluster_n))
-    return HLQ_ERR_INVALID_ARG;
-  if (cluster_m * cluster_n > 1 && splits > 1) return HLQ_ERR_INVALID_ARG;
   if (kind == 0 && splits > 1) return HLQ_ERR_INVALID_ARG;  // E4M3 GEMM runs unsplit
   const int esz = kind == 1 ? 2 : 1;
   if (lda < K || ldb < K || (lda * esz) % 16 || (ldb * esz) % 16) return HLQ_ERR_ALIGN;
@@ -861,11 +857,6 @@ hlq_status hlq_debug_tc_gemm(int kind, const void* d_a, int64_t lda, const void*
   GemmPlan plan = plan_gemm_tc(kind, M, N, K, sms, kind == 1 ? 16 : 1);
   if (bn) plan.bn = bn;
   if (splits) plan.splits = splits;
-  if (cluster_m) {
-    plan.cm = cluster_m;
-    plan.cn = cluster_n;
-  }
-  if (plan.splits > 1) plan.cm = plan.cn = 1;
   if (plan.splits > 1 && (!d_ws || ws_bytes < gemm_tc_split_ws_bytes(M, N)))
     return HLQ_ERR_WORKSPACE;
   if (plan.splits > 1 && !aligned256(d_ws)) return HLQ_ERR_ALIGN;

@@ -14,13 +14,6 @@
 // int32 registers (49 * K < 2^24 lets the E4M3 path use one chunk; the bf16
 // path uses chunks of 16 k-blocks = 1024 codes, 1024 * 127^2 < 2^24).
 //
-// Operand feed: every CTA re-reads its A and B tiles from L2, and at GB300's
-// tensor rate that L2 -> shared-memory traffic, not the MMAs, bounds the
-// unclustered kernel.  With a cluster of kCm x kCn CTAs (kCm along M, kCn
-// along N, all on one k-block schedule) each CTA fetches 1/kCn of its A tile
-// and 1/kCm of its B tile and multicasts the slice to the CTAs that share it,
-// so a CTA pulls A/kCn + B/kCm bytes per k-block instead of A + B.
-//
 // CTA layout (persistent over 128 x BN output tiles, each optionally split
 // along K with an exact int32 reduction through a workspace):
 //   warp 0      TMA producer (one lane): A and B k-blocks of 128 bytes per
@@ -113,14 +106,6 @@ __device__ __forceinline__ void tmem_ld_x32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-__device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster"
-      ".b64 [%0], %1;" ::"r"(saddr(bar)),
-      "h"(mask)
-      : "memory");
-}
-
 // The mainloop is bound by the latency of a TMA round trip (L2 -> shared
 // memory, MMA, release), so the ring holds as many stages as shared memory
 // allows: 6 of 32 KB for 128-wide tiles, 4 of 48 KB for 256-wide ones.
@@ -141,14 +126,11 @@ struct TcCfg {
   static_assert(kSmem <= 232448, "227 KB of shared memory per CTA");
 };
 
-// Persistent: CTA (or cluster) b processes work units b, b + grid, ...
-// where a unit is (output tile, K split), or for a cluster the kCm x kCn
-// block of tiles it covers (no K split).  The TMA producer and the MMA
-// issuer run through their units without pausing between tiles; a unit's
-// epilogue (stores, or exact int32 atomics for a split unit) overlaps the
-// next unit's MMAs.  `tiles_n` counts tiles along N, in cluster blocks when
-// clustered.
-template <int kKind, int BN, int kCm, int kCn>
+// Persistent: CTA b processes work units b, b + gridDim.x, ... where a unit
+// is (output tile, K split).  The TMA producer and the MMA issuer run through
+// their units without pausing between tiles; a unit's epilogue (stores, or
+// exact int32 atomics for a split unit) overlaps the next unit's MMAs.
+template <int kKind, int BN>
 __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(
     const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
     const __grid_constant__ CUtensorMap tmOut, const __grid_constant__ CUtensorMap tmAcc,
@@ -159,9 +141,6 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(
     unsigned int* __restrict__ status) {
   using C = TcCfg<BN>;
   constexpr int kStages = C::kStages;
-  constexpr int kCs = kCm * kCn;                       // CTAs per cluster
-  constexpr int kARows = kBM / kCn, kBRows = BN / kCm;  // rows fetched per CTA
-  static_assert(kARows % 8 == 0 && kBRows % 8 == 0, "slices of 8-row swizzle atoms");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -174,16 +153,12 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // position in the cluster: rm along M, rn along N
-  const int crank = kCs > 1 ? (int)cluster_rank() : 0;
-  const int rm = crank % kCm, rn = crank / kCm;
-  const int first_unit = kCs > 1 ? (int)cluster_index() : (int)blockIdx.x;
-  const int unit_step = kCs > 1 ? (int)cluster_count() : (int)gridDim.x;
+  const int first_unit = (int)blockIdx.x, unit_step = (int)gridDim.x;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kCs);  // one MMA commit from every CTA of the cluster
+      mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
@@ -202,7 +177,6 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(
   }
   tc_fence_before();
   __syncthreads();
-  if (kCs > 1) cluster_sync_all();  // peers' barriers exist before any multicast
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
   // the prologue above overlaps the previous kernel; operands, scales and
@@ -213,17 +187,11 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(
   // unit -> (m0, n0, first k-block, k-blocks)
   auto unit_coords = [&](int u, int& m0, int& n0, int& kb0, int& nkb) {
     const int t = u / splits, z = u - t * splits;
-    m0 = ((t / tiles_n) * kCm + rm) * kBM;
-    n0 = ((t % tiles_n) * kCn + rn) * BN;
+    m0 = (t / tiles_n) * kBM;
+    n0 = (t % tiles_n) * BN;
     kb0 = z * kb_per_split;
     nkb = max(0, min(num_kb, kb0 + kb_per_split) - kb0);
   };
-  // CTAs that share this CTA's A tile (same rm) and B tile (same rn)
-  uint16_t mask_a = 0, mask_b = 0;
-#pragma unroll
-  for (int j = 0; j < kCn; ++j) mask_a |= (uint16_t)(1u << (rm + kCm * j));
-#pragma unroll
-  for (int i = 0; i < kCm; ++i) mask_b |= (uint16_t)(1u << (i + kCm * rn));
 
   if (warp == 0) {
     if (lane == 0) {
@@ -239,31 +207,13 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(
         for (int j = 0; j < nkb; ++j, ++i) {
           const int s = i % kStages;
           const uint32_t ph = (uint32_t)(i / kStages) & 1u;
-          // clustered: free only once every CTA of the cluster has consumed it
           if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, status)) break;
-          mbar_expect_tx(&full[s], C::kStageBytes);  // whole A and B tiles arrive
+          mbar_expect_tx(&full[s], C::kStageBytes);
           uint8_t* a = smem + s * C::kStageBytes;
-          uint8_t* b = a + C::kABytes;
           const int kx = (kb0 + j) * elems;
-          if (kCn == 1)
-            tma_load_2d(a, &tmA, &full[s], kx, m0);
-          else
-            tma_load_2d_mc(a + rn * kARows * kRowBytes, &tmA, &full[s], kx,
-                           m0 + rn * kARows, mask_a);
-          if (kCm == 1)
-            tma_load_2d(b, &tmB, &full[s], kx, n0);
-          else
-            tma_load_2d_mc(b + rm * kBRows * kRowBytes, &tmB, &full[s], kx,
-                           n0 + rm * kBRows, mask_b);
+          tma_load_2d(a, &tmA, &full[s], kx, m0);
+          tma_load_2d(a + C::kABytes, &tmB, &full[s], kx, n0);
         }
-      }
-      if (kCs > 1 && !*abort_flag) {
-        // the last stages' releases carry the peers' final MMA commits: wait
-        // for them so that no arrival targets this CTA after it exits
-        for (int k = max(0, i - kStages); k < i; ++k)
-          if (!mbar_wait(&empty[k % kStages], (uint32_t)(k / kStages) & 1u, abort_flag,
-                         status))
-            break;
       }
       if (*abort_flag) {  // let the copies already issued land before exit
         for (int k = max(0, i - kStages); k < i; ++k) {
@@ -279,7 +229,6 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(
       constexpr uint32_t idesc = make_idesc(kKind, kBM, BN);
       int i = 0, cc = 0;  // k-blocks and accumulation chunks consumed so far
       bool ok = true;
-      const uint16_t mask_all = (uint16_t)((1u << kCs) - 1u);
       for (int u = first_unit; u < num_units && ok; u += unit_step) {
         int m0, n0, kb0, nkb;
         unit_coords(u, m0, n0, kb0, nkb);
@@ -308,10 +257,7 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(
             for (int k = 0; k < 4; ++k)
               mma_issue<kKind>(d, sw128_desc(a + 32 * k), sw128_desc(b + 32 * k), idesc,
                                (jj > 0 || k > 0) ? 1u : 0u);
-            if (kCs == 1)
-              mma_commit(&empty[s]);
-            else
-              mma_commit_mc(&empty[s], mask_all);
+            mma_commit(&empty[s]);
           }
           if (ok) mma_commit(&tfull[buf]);
         }
@@ -472,8 +418,6 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(
 
   tc_fence_before();
   __syncthreads();
-  // no CTA leaves while a peer may still multicast into it or signal it
-  if (kCs > 1) cluster_sync_all();
   if (*abort_flag) {  // let in-flight tensor-core work finish before freeing TMEM
     const unsigned long long t0 = now_ns();
     while (now_ns() - t0 < 1000000ull) {
@@ -534,79 +478,34 @@ bool make_out_map(CUtensorMap* map, const void* ptr, bool is_int, int64_t rows,
   return r == CUDA_SUCCESS;
 }
 
-template <int kKind, int BN, int kCm, int kCn>
+template <int kKind, int BN>
 cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& mo,
-                      const CUtensorMap& macc, int64_t M, int64_t N,
-                      int num_kb, int chunk_kb, int splits, int num_sms, const float* sa,
-                      bool per_row_a, const float* sb, float* out, int32_t* acc_out,
-                      int32_t* split_acc, unsigned int* slab_count,
-                      unsigned int* status, cudaStream_t st) {
+                      const CUtensorMap& macc, int64_t M, int64_t N, int num_kb, int chunk_kb,
+                      int splits, int num_sms, const float* sa, bool per_row_a,
+                      const float* sb, float* out, int32_t* acc_out, int32_t* split_acc,
+                      unsigned int* slab_count, unsigned int* status, cudaStream_t st) {
   using C = TcCfg<BN>;
-  constexpr int kCs = kCm * kCn;
-  auto kernel = gemm_tc_kernel<kKind, BN, kCm, kCn>;
-  // per device: smem attribute set, and how many clusters fit at once
-  static int max_clusters[64] = {};
+  auto kernel = gemm_tc_kernel<kKind, BN>;
+  static bool attr_set[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (max_clusters[dev] == 0) {
+  if (!attr_set[dev]) {
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)C::kSmem);
     if (e != cudaSuccess) return e;
-    int n = num_sms;
-    if (kCs > 1) {
-      cudaLaunchConfig_t cfg = {};
-      cudaLaunchAttribute attr[1];
-      cfg.gridDim = dim3(kCs * (num_sms / kCs));
-      cfg.blockDim = dim3(C::kThreads);
-      cfg.dynamicSmemBytes = C::kSmem;
-      attr[0].id = cudaLaunchAttributeClusterDimension;
-      attr[0].val.clusterDim.x = kCs;
-      attr[0].val.clusterDim.y = 1;
-      attr[0].val.clusterDim.z = 1;
-      cfg.attrs = attr;
-      cfg.numAttrs = 1;
-      e = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
-      if (e != cudaSuccess) return e;
-      if (n <= 0) return cudaErrorInvalidConfiguration;
-    }
-    max_clusters[dev] = n;
+    attr_set[dev] = true;
   }
-  if (kCs > 1 && splits != 1) return cudaErrorInvalidValue;
   const int kb_per_split = (num_kb + splits - 1) / splits;
-  const int64_t tiles_m = (M + kBM - 1) / kBM;
-  const int64_t tiles_n = (N + BN - 1) / BN;
-  // clustered: units are kCm x kCn blocks of tiles (edges padded with tiles
-  // that read zeros and store nothing)
-  const int64_t blocks_n = (tiles_n + kCn - 1) / kCn;
-  const int64_t units = ((tiles_m + kCm - 1) / kCm) * blocks_n * splits;
+  const int tiles_n = (int)((N + BN - 1) / BN);
+  const int64_t units = ((M + kBM - 1) / kBM) * tiles_n * splits;
   if (units > 0x7fffffff) return cudaErrorInvalidValue;
-  const int64_t groups = units < max_clusters[dev] ? units : max_clusters[dev];
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[2];
-  cfg.gridDim = dim3((unsigned)(groups * kCs));
-  cfg.blockDim = dim3(C::kThreads);
-  cfg.dynamicSmemBytes = C::kSmem;
-  cfg.stream = st;
-  int na = 0;
-  attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[na].val.programmaticStreamSerializationAllowed = 1;
-  ++na;
-  if (kCs > 1) {
-    attr[na].id = cudaLaunchAttributeClusterDimension;
-    attr[na].val.clusterDim.x = kCs;
-    attr[na].val.clusterDim.y = 1;
-    attr[na].val.clusterDim.z = 1;
-    ++na;
-  }
-  cfg.attrs = attr;
-  cfg.numAttrs = na;
-  cudaError_t le = cudaLaunchKernelEx(&cfg, kernel, a, b, mo, macc, (int)M, (int)N, num_kb,
-                                      chunk_kb,
-                                      kb_per_split, splits, (int)blocks_n, (int)units, sa,
-                                      per_row_a ? 1 : 0, sb, out, acc_out, split_acc,
-                                      slab_count, status);
+  const int grid = (int)(units < num_sms ? units : num_sms);
+  cudaError_t le = launch_pdl(kernel, dim3(grid), dim3(C::kThreads), C::kSmem, st, a, b, mo,
+                              macc, (int)M, (int)N, num_kb, chunk_kb, kb_per_split, splits,
+                              tiles_n, (int)units, sa, per_row_a ? 1 : 0, sb, out, acc_out,
+                              split_acc, slab_count, status);
   if (le != cudaSuccess) return le;
   return cudaGetLastError();
 }
@@ -636,12 +535,6 @@ size_t gemm_tc_split_ws_bytes(int64_t M, int64_t N) {
   return (size_t)M * (size_t)N * 4 + (size_t)tiles * 8 * 4 + 256;
 }
 
-bool gemm_tc_cluster_supported(int bn, int cm, int cn) {
-  if (bn != 128 && bn != 256) return false;
-  return (cm == 1 && cn == 1) || (cm == 2 && cn == 1) || (cm == 4 && cn == 1) ||
-         (cm == 2 && cn == 2);
-}
-
 GemmPlan plan_gemm_tc(int kind, int64_t M, int64_t N, int64_t K, int num_sms,
                       int max_splits) {
   GemmPlan p{};
@@ -652,24 +545,18 @@ GemmPlan plan_gemm_tc(int kind, int64_t M, int64_t N, int64_t K, int num_sms,
   if (num_sms < 1) num_sms = 1;
   const int64_t tiles_m = (M + kBM - 1) / kBM;
   // Tile width: fewer waves of CTAs, a 256-wide tile counted as 1.6 waves of
-  // 128-wide ones (it moves less data per MMA).  No cluster: measured on
-  // GB300 at every workload shape, multicasting shared operand tiles across
-  // a cluster never beat independent CTAs (the mainloop waits on TMA
-  // latency, and each CTA still receives its whole tiles), and lock-step
-  // clusters lose to stragglers.
+  // 128-wide ones (it moves less data per MMA).
   const int64_t t128 = tiles_m * ((N + 127) / 128);
   const int64_t t256 = tiles_m * ((N + 255) / 256);
   const double w128 = (double)((t128 + num_sms - 1) / num_sms);
   const double w256 = (double)((t256 + num_sms - 1) / num_sms) * 1.6;
   p.bn = (w256 <= w128) ? 256 : 128;
-  p.cm = p.cn = 1;
-  // K split (unclustered): only when the tiles fill less than a third of the
+  // K split: only when the tiles fill less than a third of the
   // SMs, because the int32 reduction through global atomics costs about as
   // much as the MMAs it parallelises.
   p.splits = 1;
   if (max_splits > 1 && t128 * 3 < num_sms) {
     p.bn = 128;
-    p.cm = p.cn = 1;
     int s = (int)(num_sms / t128);
     s = s < max_splits ? s : max_splits;
     while (s > 1 && (p.num_kb + s - 1) / s < 2 * p.chunk_kb) --s;
@@ -686,12 +573,11 @@ cudaError_t launch_gemm_tc(int kind, const void* A, int64_t lda, const void* B,
   if (M == 0 || N == 0) return cudaSuccess;
   if (!get_encode()) return cudaErrorNotSupported;
   const bool bf16 = kind == 1;
-  if (!gemm_tc_cluster_supported(plan.bn, plan.cm, plan.cn) ||
-      (plan.splits > 1 && (plan.cm * plan.cn > 1 || kind == 0)))
+  if ((plan.bn != 128 && plan.bn != 256) || (plan.splits > 1 && kind == 0))
     return cudaErrorInvalidValue;
   CUtensorMap ma, mb, mo, macc;
-  if (!make_map(&ma, A, bf16, M, K, lda, kBM / plan.cn)) return cudaErrorInvalidValue;
-  if (!make_map(&mb, B, bf16, N, K, ldb, plan.bn / plan.cm)) return cudaErrorInvalidValue;
+  if (!make_map(&ma, A, bf16, M, K, lda, kBM)) return cudaErrorInvalidValue;
+  if (!make_map(&mb, B, bf16, N, K, ldb, plan.bn)) return cudaErrorInvalidValue;
   memset(&mo, 0, sizeof(mo));
   memset(&macc, 0, sizeof(macc));
   if (out && !make_out_map(&mo, out, false, M, N)) return cudaErrorInvalidValue;
@@ -713,27 +599,12 @@ cudaError_t launch_gemm_tc(int kind, const void* A, int64_t lda, const void* B,
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
       sms <= 0)
     return cudaErrorInvalidDevice;
-#define TC(KIND, BN, CM, CN)                                                          \
-  launch_tc<KIND, BN, CM, CN>(ma, mb, mo, macc, M, N, plan.num_kb, plan.chunk_kb,      \
-                              plan.splits,                                            \
-                              sms, sa, per_row_a, sb, out, acc_out, split_acc,        \
-                              slab_count, status, st)
-#define TC_SHAPES(KIND, BN)                                   \
-  if (plan.cm == 1 && plan.cn == 1) return TC(KIND, BN, 1, 1); \
-  if (plan.cm == 2 && plan.cn == 1) return TC(KIND, BN, 2, 1); \
-  if (plan.cm == 4 && plan.cn == 1) return TC(KIND, BN, 4, 1); \
-  return TC(KIND, BN, 2, 2);
-  if (kind == 0) {
-    if (plan.bn == 256) {
-      TC_SHAPES(0, 256)
-    }
-    TC_SHAPES(0, 128)
-  }
-  if (plan.bn == 256) {
-    TC_SHAPES(1, 256)
-  }
-  TC_SHAPES(1, 128)
-#undef TC_SHAPES
+#define TC(KIND, BN)                                                                  \
+  launch_tc<KIND, BN>(ma, mb, mo, macc, M, N, plan.num_kb, plan.chunk_kb, plan.splits,  \
+                      sms, sa, per_row_a, sb, out, acc_out, split_acc, slab_count,      \
+                      status, st)
+  if (kind == 0) return plan.bn == 256 ? TC(0, 256) : TC(0, 128);
+  return plan.bn == 256 ? TC(1, 256) : TC(1, 128);
 #undef TC
 }
 

@@ -81,13 +81,10 @@ bool make_tile_map_2d(CUtensorMap* map, const void* ptr, bool bf16, int64_t rows
 // B [N, K] (ldb); out [M, N] fp32 = acc * sa[m or 0] * sb[0] / 16.
 struct GemmPlan {
   int bn = 128;      // tile width (128 or 256)
-  int splits = 1;    // K split count (int32 workspace reduction), unclustered
+  int splits = 1;    // K split count (int32 workspace reduction)
   int num_kb = 0;    // k-blocks of 128 bytes
   int chunk_kb = 0;  // k-blocks per exact fp32 accumulation chunk
-  int cm = 1;        // cluster shape: CTAs along M sharing B tiles
-  int cn = 1;        //                CTAs along N sharing A tiles
 };
-bool gemm_tc_cluster_supported(int bn, int cm, int cn);
 GemmPlan plan_gemm_tc(int kind, int64_t M, int64_t N, int64_t K, int num_sms,
                       int max_splits);
 size_t gemm_tc_split_ws_bytes(int64_t M, int64_t N);

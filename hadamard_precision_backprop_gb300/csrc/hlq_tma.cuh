@@ -74,19 +74,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map,
       : "memory");
 }
 
-// Multicast form: the tile lands at `dst`'s shared-memory offset in every CTA
-// of the cluster whose rank bit is set in `mask`, and completes its bytes on
-// the mbarrier at `bar`'s offset in each of them.
-__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* map,
-                                               uint64_t* bar, int x, int y,
-                                               uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(saddr(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(saddr(bar)), "h"(mask)
-      : "memory");
-}
-
 // Tiled store of a shared-memory box to global memory (the box layout of the
 // tensor map, swizzle included); parts outside the tensor are not written.
 // Completion is tracked per thread in bulk groups: commit after issuing,
@@ -111,29 +98,6 @@ __device__ __forceinline__ void tma_store_wait_all() {
 // (TMA) reads of them.
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ uint32_t cluster_index() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ uint32_t cluster_count() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
-  return r;
-}
-// All threads of every CTA of the cluster; orders prior shared-memory writes
-// (barrier inits included) before what follows in every CTA.
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile(
-      "barrier.cluster.arrive.release.aligned;\n\t"
-      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 }  // namespace hlq

@@ -223,17 +223,14 @@ hlq_status hlq_debug_reference_gemm(int kind, const void *d_a, const void *d_b,
  * kind 1: A, B hold bf16 values of integers in [-127, 127] (the g_w GEMM).
  * lda / ldb: row strides in elements (16-byte multiples).  bn: tile width
  * 128 or 256 (0 = the library's choice); splits: K split count (0 = the
- * library's choice; > 1 needs d_ws of hlq_debug_tc_gemm_ws_bytes(M, N)).
- * cluster_m x cluster_n: thread-block cluster of tiles sharing operand tiles
- * by TMA multicast, one of 1x1, 2x1, 4x1, 2x2 (0 x 0 = the library's choice;
- * a K split forces 1x1; kind 0 runs unsplit).  M, N, K multiples of 16.  An
- * unsupported plan is HLQ_ERR_INVALID_ARG.
+ * library's choice; > 1 needs d_ws of hlq_debug_tc_gemm_ws_bytes(M, N);
+ * kind 0 runs unsplit).  M, N, K multiples of 16.  An unsupported plan is
+ * HLQ_ERR_INVALID_ARG.
  */
 hlq_status hlq_debug_tc_gemm(int kind, const void *d_a, int64_t lda,
                              const void *d_b, int64_t ldb, int64_t M, int64_t N,
-                             int64_t K, int bn, int splits, int cluster_m,
-                             int cluster_n, int32_t *d_acc, void *d_ws,
-                             size_t ws_bytes, void *stream);
+                             int64_t K, int bn, int splits, int32_t *d_acc,
+                             void *d_ws, size_t ws_bytes, void *stream);
 size_t hlq_debug_tc_gemm_ws_bytes(int64_t M, int64_t N);
 
 /*

@@ -120,17 +120,13 @@ def test_compress_argument_validation(L):
 def test_tc_gemm_plan_validation(L):
     f = L.hlq_debug_tc_gemm
 
-    def call(bn=128, splits=1, cm=1, cn=1, kind=1, M=256, N=256, K=256):
-        return f(kind, FAKE, K, FAKE, K, M, N, K, bn, splits, cm, cn, FAKE,
-                 FAKE_WS, 1 << 30, None)
+    def call(bn=128, splits=1, kind=1, M=256, N=256, K=256):
+        return f(kind, FAKE, K, FAKE, K, M, N, K, bn, splits, FAKE, FAKE_WS, 1 << 30,
+                 None)
 
     assert call(bn=64) == 1
     assert call(kind=2) == 1
     assert call(splits=65) == 1
-    assert call(cm=3) == 1                    # cluster shapes: 1x1 2x1 4x1 2x2
-    assert call(cm=4, cn=2) == 1
-    assert call(cm=1, cn=0) == 1
-    assert call(cm=2, splits=2) == 1          # a K split runs unclustered
     assert call(kind=0, splits=2) == 1        # the E4M3 GEMM runs unsplit
     assert call(M=200) == 2
 

@@ -1,5 +1,5 @@
-"""The tensor-core GEMMs alone: exact int32 sums for every tile width, K
-split and cluster shape, ragged M/N/K, both operand kinds (E4M3 int4 codes, bf16 int8
+"""The tensor-core GEMMs alone: exact int32 sums for every tile width and
+K split, ragged M/N/K, both operand kinds (E4M3 int4 codes, bf16 int8
 codes), against numpy int64 sums and the CUDA-core reference GEMM."""
 import numpy as np
 import pytest
@@ -29,14 +29,14 @@ def _lib():
     hlq.lib()
 
 
-def run(kind, A, B, bn, splits, cluster=(1, 1)):
+def run(kind, A, B, bn, splits):
     if kind == 0:
         a = torch.from_numpy(e4m3_bytes(A)).cuda()
         b = torch.from_numpy(e4m3_bytes(B)).cuda()
     else:
         a = torch.from_numpy(A.astype(np.float32)).cuda().to(torch.bfloat16)
         b = torch.from_numpy(B.astype(np.float32)).cuda().to(torch.bfloat16)
-    return hlq.hlq_debug_tc_gemm(kind, a, b, bn=bn, splits=splits, cluster=cluster)
+    return hlq.hlq_debug_tc_gemm(kind, a, b, bn=bn, splits=splits)
 
 
 @pytest.mark.parametrize("kind,qmax", [(0, 7), (1, 127)])
@@ -57,31 +57,15 @@ def test_tc_gemm_exact(kind, qmax, M, N, K, bn, splits):
     np.testing.assert_array_equal(ref.cpu().numpy(), got)
 
 
-@pytest.mark.parametrize("kind,qmax", [(0, 7), (1, 127)])
-@pytest.mark.parametrize("M,N,K", [(16, 32, 16), (272, 400, 208), (1040, 144, 4112),
-                                   (400, 784, 1024)])
-@pytest.mark.parametrize("bn,cluster", [(128, (2, 1)), (128, (4, 1)), (128, (2, 2)),
-                                        (256, (2, 1)), (256, (4, 1)), (256, (2, 2))])
-def test_tc_gemm_cluster_multicast_exact(kind, qmax, M, N, K, bn, cluster):
-    """Clustered CTAs fetch slices of the shared A / B tiles and multicast
-    them; ragged edges add padding tiles that read zeros and store nothing."""
-    rng = np.random.default_rng(M * 5 + N + K * 3 + bn + 11 * cluster[0] + 17 * cluster[1])
-    A = rng.integers(-qmax, qmax + 1, (M, K))
-    B = rng.integers(-qmax, qmax + 1, (N, K))
-    want = A.astype(np.int64) @ B.astype(np.int64).T
-    got = run(kind, A, B, bn, 1, cluster).cpu().numpy()
-    np.testing.assert_array_equal(got.astype(np.int64), want)
-
-
 def test_tc_gemm_library_plan_exact():
-    """The plan the library picks for the workload shapes (tile width,
-    cluster shape, K split), on operands cut to a few tiles per dimension."""
+    """The plan the library picks for the workload shapes (tile width, K
+    split), at full size, checked on sampled rows."""
     for kind, qmax, M, N, K in [(0, 7, 12608, 768, 2304), (1, 127, 2304, 768, 6304),
                                 (1, 127, 256, 2304, 25088)]:
         rng = np.random.default_rng(M + N + K)
         A = rng.integers(-qmax, qmax + 1, (M, K))
         B = rng.integers(-qmax, qmax + 1, (N, K))
-        got = run(kind, A, B, 0, 0, (0, 0)).cpu().numpy().astype(np.int64)
+        got = run(kind, A, B, 0, 0).cpu().numpy().astype(np.int64)
         rows = rng.choice(M, 64, replace=False)
         np.testing.assert_array_equal(got[rows], A[rows].astype(np.int64) @ B.astype(np.int64).T)
 
@@ -93,8 +77,8 @@ def test_tc_gemm_bf16_worst_case_magnitude():
     A = np.full((M, K), 127, np.int64)
     A[1::2] = -127
     B = np.full((N, K), 127, np.int64)
-    for splits, cluster in ((1, (1, 1)), (2, (1, 1)), (5, (1, 1)), (1, (2, 2))):
-        got = run(1, A, B, 128, splits, cluster).cpu().numpy()
+    for splits in (1, 2, 5):
+        got = run(1, A, B, 128, splits).cpu().numpy()
         assert got[0, 0] == 16129 * K and got[1, 0] == -16129 * K
         assert np.all(got[0::2] == 16129 * K) and np.all(got[1::2] == -16129 * K)
 
@@ -105,6 +89,5 @@ def test_tc_gemm_e4m3_worst_case_magnitude():
     A[::3] = -7
     B = np.full((N, K), -7, np.int64)
     want = A[:, :1] * B[:, 0][None, :] * K
-    for cluster in ((1, 1), (4, 1)):
-        got = run(0, A, B, 256, 1, cluster).cpu().numpy()
-        np.testing.assert_array_equal(got, want)
+    got = run(0, A, B, 256, 1).cpu().numpy()
+    np.testing.assert_array_equal(got, want)
