@@ -72,6 +72,7 @@ def _load():
                                                P, P]),
                 "orc_amax": (ctypes.c_float, [P, i64]),
                 "orc_int8_quantize": (i32, [P, i64, P, P]),
+                "orc_rne_quantize": (i32, [P, i64, i32, P, P]),
                 "orc_pack_int4": (i32, [P, i64, P]),
                 "orc_gemm_i64": (None, [P, P, i64, i64, i64, P]),
                 "orc_dequant_gx": (None, [P, P, i32, ctypes.c_float, i64, i64, P]),
@@ -215,6 +216,16 @@ def int8_quantize(v):
     return codes, np.float32(s[0])
 
 
+def rne_quantize(v, qmax: int):
+    """Per-tensor RNE quantizer with qmax 127 (int8) or 7 (int4)."""
+    v = _f32(v)
+    codes = np.empty(v.shape, dtype=np.int8)
+    s = np.zeros(1, dtype=np.float32)
+    _check(_load().orc_rne_quantize(_p(v), v.size, int(qmax), _p(codes), _p(s)),
+           "rne_quantize")
+    return codes, np.float32(s[0])
+
+
 def pack_int4(codes) -> np.ndarray:
     c = np.ascontiguousarray(codes, dtype=np.int8)
     packed = np.empty(c.shape[:-1] + (c.shape[-1] // 2,), dtype=np.uint8)
@@ -278,11 +289,12 @@ def gx_path(g_y, w, gran_gy=PER_TOKEN, rnd=SR, seed=0, rows=None):
                 g_x=g_x, rows=sel)
 
 
-def compress_activation(x, rank=8):
-    """ACBP at forward time: x [T, Cin] -> int8 codes [Cin, T*rank/16] and
-    the per-tensor scale."""
+def compress_activation(x, rank=8, bits=8):
+    """ACBP at forward time: x [T, Cin] -> codes [Cin, T*rank/16] (int8
+    values: [-127, 127] for bits=8, [-7, 7] for bits=4; pack_int4 gives the
+    stored nibbles of the latter) and the per-tensor scale."""
     Xb = hla_transform(x, rank)
-    q, s = int8_quantize(Xb)
+    q, s = rne_quantize(Xb, 127 if bits == 8 else 7)
     return q, s
 
 

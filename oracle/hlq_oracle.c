@@ -512,10 +512,14 @@ float orc_amax(const float *v, int64_t n)
     return amax;
 }
 
-/* int8 quantizer with one scale per tensor, s = RN_f32(amax / 127),
- * round to nearest even, clamp to [-127, 127] (the HLA operands). */
-int orc_int8_quantize(const float *v, int64_t n, int8_t *codes, float *scale)
+/* Round-to-nearest-even quantizer with one scale per tensor:
+ * s = RN_f32(amax / qmax), codes clamp(rint(RN_f32(v / s)), -qmax, qmax).
+ * qmax = 127 gives the int8 HLA operands; qmax = 7 the int4 form of the
+ * stored activation (HLQ TL;DR, "int4 activation-compression strategy"). */
+int orc_rne_quantize(const float *v, int64_t n, int qmax, int8_t *codes, float *scale)
 {
+    if (qmax != 7 && qmax != 127)
+        return ORC_ERR_ARG;
     float amax = 0.0f;
     for (int64_t i = 0; i < n; ++i) {
         if (!is_finite_f32(v[i]))
@@ -523,11 +527,17 @@ int orc_int8_quantize(const float *v, int64_t n, int8_t *codes, float *scale)
         if (fabsf(v[i]) > amax)
             amax = fabsf(v[i]);
     }
-    float s = amax / 127.0f;
+    float s = amax / (float)qmax;
     *scale = s;
     for (int64_t i = 0; i < n; ++i)
-        codes[i] = (int8_t)quant_one(v[i], s, 127, ORC_RNE, 0);
+        codes[i] = (int8_t)quant_one(v[i], s, qmax, ORC_RNE, 0);
     return ORC_OK;
+}
+
+/* int8 quantizer of the HLA operands: orc_rne_quantize with qmax = 127. */
+int orc_int8_quantize(const float *v, int64_t n, int8_t *codes, float *scale)
+{
+    return orc_rne_quantize(v, n, 127, codes, scale);
 }
 
 /* Nibble packing of int4 codes (two's complement; element 2k in the low

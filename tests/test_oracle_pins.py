@@ -275,6 +275,49 @@ def test_int8_rne_bound():
     assert np.all(np.abs(q[ok] - x[ok]) <= 0.5)
 
 
+def test_int4_acbp_rne_bound_ties_and_int8_equivalence():
+    """The int4 storage form of the stored activation: RNE with qmax 7
+    (HLQ TL;DR, int4 activation compression).  Error <= s/2 off the clamp,
+    exact ties to even, scale RN(amax/7), and qmax 127 is the int8 path."""
+    rng = np.random.default_rng(21)
+    v = rng.standard_normal(4000).astype(np.float32)
+    q, s = oracle.rne_quantize(v, 7)
+    assert s == np.float32(np.max(np.abs(v))) / np.float32(7.0)
+    x = v / s
+    assert np.all(np.abs(q) <= 7)
+    ok = np.abs(x) <= 7
+    assert np.all(np.abs(q[ok] - x[ok]) <= 0.5)
+    assert np.all(q[~ok] == np.sign(x[~ok]) * 7)
+    t = np.array([7.0, 0.5, 1.5, 2.5, -0.5, -3.5, 6.5, -6.5], np.float32)
+    q, s = oracle.rne_quantize(t, 7)
+    assert s == 1.0 and list(q) == [7, 0, 2, 2, 0, -4, 6, -6]
+    q127, s127 = oracle.rne_quantize(v, 127)
+    q8, s8 = oracle.int8_quantize(v)
+    assert s127 == s8 and np.array_equal(q127, q8)
+    with pytest.raises(ValueError):
+        oracle.rne_quantize(v, 15)
+
+
+def test_int4_acbp_lossless_gw():
+    """With every HLA coefficient of x an integer multiple of amax/7, the
+    int4 stored activation loses nothing: g_w equals g_y^T x."""
+    rng = np.random.default_rng(22)
+    T, Cin, Cout = 64, 20, 24
+    gy = np.repeat(rng.integers(-3, 4, (T // 2, Cout)), 2, 0).astype(np.float64)
+    x = np.repeat(rng.integers(-1, 2, (T // 2, Cin)), 2, 0).astype(np.float64)
+    gy[:16, 0] = 127 / 16.0 * 2
+    x[:16, 0] = 7 / 16.0 * 2          # amax of the HLA of x: 7 * 2^-2
+    gy = (gy * 2.0 ** -7).astype(np.float32)
+    x = (x * 2.0 ** -2).astype(np.float32)
+    q, s = oracle.compress_activation(x, 8, bits=4)
+    assert np.all(np.abs(q) <= 7)
+    Xb = oracle.hla_transform(x, 8)
+    assert np.array_equal(q.astype(np.float64) * s, Xb)
+    r = oracle.gw_path(gy, q, s, 8)
+    want = gy.astype(np.float64).T @ x.astype(np.float64)
+    assert np.allclose(r["g_w"], want, rtol=1e-12, atol=1e-15)
+
+
 def test_clamp_when_scale_rounds_down():
     # amax/7 rounded to fp32 can be below the true quotient, so amax/s > 7
     for amax in np.float32([1.0, 3.0, 5.0, 0.1, 1e-3, 123.456]):
