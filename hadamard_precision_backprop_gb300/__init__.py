@@ -73,17 +73,17 @@ def lib() -> ctypes.CDLL:
                                 ctypes.c_uint64, ctypes.c_size_t)
         sig = {
             "hlq_workspace_bytes": (sz, [i32, i64, i64, i64, i32, i32]),
-            "hlq_compress_activation": (i32, [P, i32, i64, i64, i32, i32, P, P,
-                                              P, sz, P]),
+            "hlq_compress_activation": (i32, [P, i32, i64, i64, i32, i32, i32, P,
+                                              P, P, sz, P]),
             "hlq_linear_backward_gx": (i32, [P, P, i32, i64, i64, i64, i32, i32,
                                              i32, i32, u64, P, P, sz, P]),
             "hlq_linear_backward_gw": (i32, [P, i32, P, P, i64, i64, i64, i32,
-                                             i32, P, P, sz, P]),
+                                             i32, i32, P, P, sz, P]),
             "hlq_debug_gx_parts": (i32, [P, P, i32, i64, i64, i64, i32, i32,
                                          i32, i32, u64, P, P, sz, P, P, P, P,
                                          P, P]),
             "hlq_debug_gw_parts": (i32, [P, i32, P, P, i64, i64, i64, i32, i32,
-                                         P, P, sz, P, P, P, P]),
+                                         i32, P, P, sz, P, P, P, P]),
             "hlq_read_device_status": (i32, [P, i32, P]),
             "hlq_debug_hq_transform": (i32, [P, i32, i64, i64, i32, P, P]),
             "hlq_debug_hla_transform": (i32, [P, i32, i64, i64, i32, P, P]),
@@ -96,9 +96,9 @@ def lib() -> ctypes.CDLL:
                                                      i32, i32, i32, u64, P, P]),
             "hlq_noalloc_scratch_bytes": (sz, []),
             "hlq_linear_backward": (i32, [P, P, P, P, i32, i64, i64, i64, i32, i32,
-                                          i32, i32, i32, u64, P, P, P, sz, P]),
+                                          i32, i32, i32, i32, u64, P, P, P, sz, P]),
             "hlq_layer_step_host": (i32, [P, P, P, i32, i64, i64, i64, i32, i32, i32,
-                                          i32, i32, u64, P, P, P, P, i64, P, sz, P]),
+                                          i32, i32, i32, u64, P, P, P, P, i64, P, sz, P]),
             "hlq_layer_step_host_workspace_bytes": (sz, [i32, i64, i64, i64, i32, i32]),
             "hlq_trace_end": (i32, [P]),
             "hlq_trace_get": (i32, [i32, P, P]),
@@ -172,22 +172,32 @@ def workspace(op, T, Cin, Cout, block=16, rank=8, device=None):
                        device=device or torch.cuda.current_device())
 
 
+def xbar_shape(T: int, Cin: int, rank: int = 8, xbar_bits: int = 8):
+    """Shape of the ACBP buffer: [Cin, T'] int8 codes, or [Cin, T'/2] bytes
+    of packed int4 codes."""
+    Tp = T // 16 * rank
+    return (Cin, Tp if xbar_bits == 8 else Tp // 2)
+
+
 def hlq_compress_activation(x, rank: int = 8, block: int = 16, out=None,
-                            scale=None, ws=None, stream=None):
-    """ACBP: x [T, Cin] -> (int8 codes [Cin, T*rank/16], fp32 scale [1])."""
+                            scale=None, ws=None, xbar_bits: int = 8, stream=None):
+    """ACBP: x [T, Cin] -> (codes, fp32 scale [1]); codes are int8
+    [Cin, T*rank/16] (xbar_bits 8) or uint8 [Cin, T*rank/32] holding two int4
+    codes per byte (xbar_bits 4)."""
     torch = _torch()
     _need_cuda_contig(x)
     T, Cin = x.shape
-    Tp = T // 16 * rank
     if out is None:
-        out = torch.empty((Cin, Tp), dtype=torch.int8, device=x.device)
+        out = torch.empty(xbar_shape(T, Cin, rank, xbar_bits),
+                          dtype=torch.int8 if xbar_bits == 8 else torch.uint8,
+                          device=x.device)
     if scale is None:
         scale = torch.empty(1, dtype=torch.float32, device=x.device)
     if ws is None:
         ws = workspace(OP_COMPRESS_ACTIVATION, T, Cin, 16, block, rank, x.device)
     _check(lib().hlq_compress_activation(
-        _ptr(x), _dtype_code(x), T, Cin, block, rank, _ptr(out), _ptr(scale),
-        _ptr(ws), ws.numel(), _stream(stream)), "hlq_compress_activation")
+        _ptr(x), _dtype_code(x), T, Cin, block, rank, xbar_bits, _ptr(out),
+        _ptr(scale), _ptr(ws), ws.numel(), _stream(stream)), "hlq_compress_activation")
     return out, scale
 
 
@@ -214,7 +224,8 @@ def hlq_linear_backward_gx(g_y, w, gran_gy: int = PER_TOKEN,
 
 
 def hlq_linear_backward_gw(g_y, xbar, xbar_scale, rank: int = 8,
-                           block: int = 16, out=None, ws=None, stream=None):
+                           block: int = 16, out=None, ws=None, xbar_bits: int = 8,
+                           stream=None):
     """g_w [Cout, Cin] (fp32) from g_y [T, Cout] and the ACBP buffer."""
     torch = _torch()
     _need_cuda_contig(g_y, xbar, xbar_scale)
@@ -226,7 +237,7 @@ def hlq_linear_backward_gw(g_y, xbar, xbar_scale, rank: int = 8,
         ws = workspace(OP_BACKWARD_GW, T, Cin, Cout, block, rank, g_y.device)
     _check(lib().hlq_linear_backward_gw(
         _ptr(g_y), _dtype_code(g_y), _ptr(xbar), _ptr(xbar_scale), T, Cin,
-        Cout, block, rank, _ptr(out), _ptr(ws), ws.numel(), _stream(stream)),
+        Cout, block, rank, xbar_bits, _ptr(out), _ptr(ws), ws.numel(), _stream(stream)),
         "hlq_linear_backward_gw")
     return out
 
@@ -255,7 +266,8 @@ def hlq_linear_backward_gx_noalloc(g_y, w, gran_gy: int = PER_TOKEN,
 def hlq_linear_backward(g_y, w, xbar, xbar_scale, rank: int = 8,
                         gran_gy: int = PER_TOKEN, gran_w: int = PER_TENSOR,
                         rnd: int = SR, seed: int = 0, block: int = 16,
-                        out_gx=None, out_gw=None, ws=None, stream=None):
+                        out_gx=None, out_gw=None, ws=None, xbar_bits: int = 8,
+                        stream=None):
     """Both gradients of the layer, the g_x and g_w branches overlapped on
     the GPU: returns (g_x [T, Cin], g_w [Cout, Cin]) fp32."""
     torch = _torch()
@@ -272,7 +284,7 @@ def hlq_linear_backward(g_y, w, xbar, xbar_scale, rank: int = 8,
         ws = workspace(OP_BACKWARD, T, Cin, Cout, block, rank, g_y.device)
     _check(lib().hlq_linear_backward(
         _ptr(g_y), _ptr(w), _ptr(xbar), _ptr(xbar_scale), _dtype_code(g_y), T,
-        Cin, Cout, block, rank, gran_gy, gran_w, rnd, seed, _ptr(out_gx),
+        Cin, Cout, block, rank, xbar_bits, gran_gy, gran_w, rnd, seed, _ptr(out_gx),
         _ptr(out_gw), _ptr(ws), ws.numel(), _stream(stream)),
         "hlq_linear_backward")
     return out_gx, out_gw
@@ -294,7 +306,7 @@ def hlq_layer_step_host(x, g_y, w, xbar, xbar_scale, rank: int = 8,
                         gran_gy: int = PER_TOKEN, gran_w: int = PER_TENSOR,
                         rnd: int = SR, seed: int = 0, block: int = 16,
                         out_gx=None, out_gw=None, ws=None, chunk_tokens: int = 0,
-                        stream=None):
+                        xbar_bits: int = 8, stream=None):
     """One layer step from host tensors (x, g_y, w on the CPU, pinned for
     speed): compresses x into the device buffers xbar / xbar_scale and
     returns host (g_x, g_w) fp32.  Asynchronous on `stream`: synchronize it
@@ -315,7 +327,8 @@ def hlq_layer_step_host(x, g_y, w, xbar, xbar_scale, rank: int = 8,
         n = hlq_layer_step_host_workspace_bytes(dt, T, Cin, Cout, block, rank)
         ws = torch.empty(max(n, 256), dtype=torch.uint8, device=xbar.device)
     _check(lib().hlq_layer_step_host(
-        _ptr(x), _ptr(g_y), _ptr(w), dt, T, Cin, Cout, block, rank, gran_gy, gran_w,
+        _ptr(x), _ptr(g_y), _ptr(w), dt, T, Cin, Cout, block, rank, xbar_bits, gran_gy,
+        gran_w,
         rnd, seed, _ptr(out_gx), _ptr(out_gw), _ptr(xbar), _ptr(xbar_scale),
         chunk_tokens, _ptr(ws), ws.numel(), _stream(stream)), "hlq_layer_step_host")
     return out_gx, out_gw
@@ -347,7 +360,8 @@ def hlq_debug_gx_parts(g_y, w, gran_gy=PER_TOKEN, gran_w=PER_TENSOR, rnd=SR,
     return r
 
 
-def hlq_debug_gw_parts(g_y, xbar, xbar_scale, rank=8, block=16, stream=None):
+def hlq_debug_gw_parts(g_y, xbar, xbar_scale, rank=8, block=16, xbar_bits=8,
+                       stream=None):
     """g_w plus its intermediates: dict(g_w, qg, sg, acc)."""
     torch = _torch()
     _need_cuda_contig(g_y, xbar, xbar_scale)
@@ -364,7 +378,7 @@ def hlq_debug_gw_parts(g_y, xbar, xbar_scale, rank=8, block=16, stream=None):
     ws = workspace(OP_BACKWARD_GW, T, Cin, Cout, block, rank, dev)
     _check(lib().hlq_debug_gw_parts(
         _ptr(g_y), _dtype_code(g_y), _ptr(xbar), _ptr(xbar_scale), T, Cin,
-        Cout, block, rank, _ptr(r["g_w"]), _ptr(ws), ws.numel(), _ptr(r["qg"]),
+        Cout, block, rank, xbar_bits, _ptr(r["g_w"]), _ptr(ws), ws.numel(), _ptr(r["qg"]),
         _ptr(r["sg"]), _ptr(r["acc"]), _stream(stream)), "hlq_debug_gw_parts")
     return r
 

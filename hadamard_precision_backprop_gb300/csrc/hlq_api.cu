@@ -157,6 +157,14 @@ bool rank_ok(int rank) {
   return rank == 1 || rank == 2 || rank == 4 || rank == 8 || rank == 16;
 }
 
+// Storage of the ACBP buffer: 8 (int8 codes [Cin, T']) or 4 (int4 codes packed
+// two per byte [Cin, T'/2], even ranks only).
+hlq_status xbar_bits_check(int bits, int rank) {
+  if (bits != 8 && bits != 4) return HLQ_ERR_INVALID_ARG;
+  if (bits == 4 && rank < 2) return HLQ_ERR_UNSUPPORTED;
+  return HLQ_OK;
+}
+
 hlq_status check_common(int dt, int64_t T, int64_t Cin, int64_t Cout,
                         int block) {
   if (dt != HLQ_F32 && dt != HLQ_BF16) return HLQ_ERR_INVALID_ARG;
@@ -301,18 +309,19 @@ hlq_status gx_impl(const void* gy, const void* w, int dt, int64_t T,
   return HLQ_OK;
 }
 
-// ACBP: HLA of x along tokens, per-tensor amax pass, int8 codes [Cin, T'].
+// ACBP: HLA of x along tokens, per-tensor amax pass, int8 codes [Cin, T'] or
+// packed int4 codes (bits 4).
 hlq_status compress_launches(const void* x, bool bf16, int64_t T, int64_t Cin, int rank,
-                             int8_t* xbar, float* xscale, unsigned int* amax,
+                             int bits, int8_t* xbar, float* xscale, unsigned int* amax,
                              unsigned int* status, cudaStream_t s) {
   const int64_t Tp = T / 16 * rank;
   HLQ_TRY(cudaMemsetAsync(amax, 0, 4, s));
   HLQ_LAUNCH("hla_x_amax", s,
-             launch_hla(x, bf16, T, Cin, rank, true, false, amax, nullptr, 0, nullptr,
+             launch_hla(x, bf16, T, Cin, rank, true, kHlaOutI8, amax, nullptr, 0, nullptr,
                         status, s));
   HLQ_LAUNCH("hla_x_quant", s,
-             launch_hla(x, bf16, T, Cin, rank, false, false, amax, xbar, Tp, xscale, status,
-                        s));
+             launch_hla(x, bf16, T, Cin, rank, false, bits == 4 ? kHlaOutI4 : kHlaOutI8, amax,
+                        xbar, Tp, xscale, status, s));
   return HLQ_OK;
 }
 
@@ -322,21 +331,27 @@ hlq_status hla_gy_launches(const void* gy, bool bf16, int64_t T, int64_t Cout, i
                            unsigned int* status, cudaStream_t s) {
   HLQ_TRY(cudaMemsetAsync(amax, 0, 4, s));
   HLQ_LAUNCH("hla_gy_amax", s,
-             launch_hla(gy, bf16, T, Cout, rank, true, true, amax, nullptr, 0, nullptr,
+             launch_hla(gy, bf16, T, Cout, rank, true, kHlaOutBf16, amax, nullptr, 0, nullptr,
                         status, s));
   HLQ_LAUNCH("hla_gy_quant", s,
-             launch_hla(gy, bf16, T, Cout, rank, false, true, amax, qg, ld, sg, status, s));
+             launch_hla(gy, bf16, T, Cout, rank, false, kHlaOutBf16, amax, qg, ld, sg, status,
+                        s));
   return HLQ_OK;
 }
 
 // ACBP buffer widened to bf16, then the g_w GEMM with its dequantization.
-hlq_status gw_gemm_launches(const int8_t* xbar, const float* xscale, int64_t Cin,
+hlq_status gw_gemm_launches(const int8_t* xbar, int bits, const float* xscale, int64_t Cin,
                             int64_t Cout, int64_t Tp, const GwLayout& L, uint8_t* base,
                             float* gw, int32_t* dbg_acc, unsigned int* status,
                             cudaStream_t s) {
   void* xw = base + L.xw;
   const float* sg = reinterpret_cast<const float*>(base + L.sg);
-  HLQ_LAUNCH("widen_xbar", s, launch_widen_i8_bf16(xbar, xw, Cin, Tp, L.ld, s));
+  if (bits == 4)
+    HLQ_LAUNCH("widen_xbar", s,
+               launch_widen_i4_bf16(reinterpret_cast<const uint8_t*>(xbar), xw, Cin, Tp, L.ld,
+                                    s));
+  else
+    HLQ_LAUNCH("widen_xbar", s, launch_widen_i8_bf16(xbar, xw, Cin, Tp, L.ld, s));
   const int sms = device_sm_count();
   if (sms <= 0) return HLQ_ERR_CUDA;
   const GemmPlan plan = plan_gemm_tc(1, Cout, Cin, Tp, sms, 16);
@@ -346,7 +361,7 @@ hlq_status gw_gemm_launches(const int8_t* xbar, const float* xscale, int64_t Cin
   return HLQ_OK;
 }
 
-hlq_status gw_impl(const void* gy, int dt, const int8_t* xbar,
+hlq_status gw_impl(const void* gy, int dt, const int8_t* xbar, int bits,
                    const float* xscale, int64_t T, int64_t Cin, int64_t Cout,
                    int block, int rank, float* gw, void* ws, size_t ws_bytes,
                    int8_t* dbg_qg, float* dbg_sg, int32_t* dbg_acc,
@@ -354,6 +369,8 @@ hlq_status gw_impl(const void* gy, int dt, const int8_t* xbar,
   hlq_status st = check_common(dt, T, Cin, Cout, block);
   if (st != HLQ_OK) return st;
   if (!rank_ok(rank)) return HLQ_ERR_INVALID_ARG;
+  st = xbar_bits_check(bits, rank);
+  if (st != HLQ_OK) return st;
   const int64_t Tp = T / 16 * rank;
   const int64_t n_gw = Cout * Cin;
   if (n_gw > 0 && !gw) return HLQ_ERR_INVALID_ARG;
@@ -361,7 +378,8 @@ hlq_status gw_impl(const void* gy, int dt, const int8_t* xbar,
   if (Cin * Tp > 0 && !xbar) return HLQ_ERR_INVALID_ARG;
   if (!xscale) return HLQ_ERR_INVALID_ARG;
   if (!aligned16(gy) || !aligned16(xbar) || !aligned16(gw)) return HLQ_ERR_ALIGN;
-  if (Tp * 127 * 127 >= ((int64_t)1 << 31)) return HLQ_ERR_OVERFLOW;
+  // |acc| <= T' * 127 * qmax_x must stay below 2^31
+  if (Tp * 127 * (bits == 4 ? 7 : 127) >= ((int64_t)1 << 31)) return HLQ_ERR_OVERFLOW;
   const GwLayout L = gw_layout(T, Cin, Cout, rank);
   if (!ws || ws_bytes < L.total) return HLQ_ERR_WORKSPACE;
   if (!aligned256(ws)) return HLQ_ERR_ALIGN;
@@ -383,7 +401,7 @@ hlq_status gw_impl(const void* gy, int dt, const int8_t* xbar,
 
   st = hla_gy_launches(gy, bf16, T, Cout, rank, amax, qg, L.ld, sg, status, s);
   if (st != HLQ_OK) return st;
-  st = gw_gemm_launches(xbar, xscale, Cin, Cout, Tp, L, base, gw, dbg_acc, status, s);
+  st = gw_gemm_launches(xbar, bits, xscale, Cin, Cout, Tp, L, base, gw, dbg_acc, status, s);
   if (st != HLQ_OK) return st;
   if (dbg_qg) HLQ_TRY(launch_decode_bf16(qg, dbg_qg, Cout, Tp, L.ld, s));
   if (dbg_sg) HLQ_TRY(cudaMemcpyAsync(dbg_sg, sg, 4, cudaMemcpyDeviceToDevice, s));
@@ -470,12 +488,14 @@ size_t hlq_workspace_bytes(int op, int64_t T, int64_t Cin, int64_t Cout,
 }
 
 hlq_status hlq_compress_activation(const void* d_x, int dt, int64_t T,
-                                   int64_t Cin, int block, int rank,
+                                   int64_t Cin, int block, int rank, int xbar_bits,
                                    int8_t* d_xbar, float* d_xbar_scale,
                                    void* d_ws, size_t ws_bytes, void* stream) {
   hlq_status st = check_common(dt, T, Cin, 16, block);
   if (st != HLQ_OK) return st;
   if (!rank_ok(rank)) return HLQ_ERR_INVALID_ARG;
+  st = xbar_bits_check(xbar_bits, rank);
+  if (st != HLQ_OK) return st;
   const int64_t Tp = T / 16 * rank;
   if (!d_xbar_scale) return HLQ_ERR_INVALID_ARG;
   if (Cin * Tp > 0 && (!d_x || !d_xbar)) return HLQ_ERR_INVALID_ARG;
@@ -489,14 +509,14 @@ hlq_status hlq_compress_activation(const void* d_x, int dt, int64_t T,
   }
   unsigned int* status = device_status_ptr();
   if (!status) return HLQ_ERR_CUDA;
-  return compress_launches(d_x, dt == HLQ_BF16, T, Cin, rank, d_xbar, d_xbar_scale,
-                           static_cast<unsigned int*>(d_ws), status, s);
+  return compress_launches(d_x, dt == HLQ_BF16, T, Cin, rank, xbar_bits, d_xbar,
+                           d_xbar_scale, static_cast<unsigned int*>(d_ws), status, s);
 }
 
 hlq_status hlq_linear_backward(const void* d_gy, const void* d_w, const int8_t* d_xbar,
                                const float* d_xbar_scale, int dt, int64_t T,
                                int64_t Cin, int64_t Cout, int block, int rank,
-                               int gran_gy, int gran_w, int rnd, uint64_t seed,
+                               int xbar_bits, int gran_gy, int gran_w, int rnd, uint64_t seed,
                                float* d_gx, float* d_gw, void* d_ws, size_t ws_bytes,
                                void* stream) {
   hlq_status st = check_common(dt, T, Cin, Cout, block);
@@ -511,7 +531,7 @@ hlq_status hlq_linear_backward(const void* d_gy, const void* d_w, const int8_t* 
   cudaStream_t a = aux_stream(0), aw = aux_stream(1);
   if (!a || !aw) return HLQ_ERR_CUDA;
   // validate both branches before forking (nothing enqueued on failure)
-  st = gw_impl(d_gy, dt, d_xbar, d_xbar_scale, T, Cin, Cout, block, rank, d_gw,
+  st = gw_impl(d_gy, dt, d_xbar, xbar_bits, d_xbar_scale, T, Cin, Cout, block, rank, d_gw,
                base + gx_bytes, gw_bytes, nullptr, nullptr, nullptr, nullptr,
                /*validate_only=*/true);
   if (st != HLQ_OK) return st;
@@ -530,7 +550,7 @@ hlq_status hlq_linear_backward(const void* d_gy, const void* d_w, const int8_t* 
   if (cudaEventRecord(fork, s) != cudaSuccess || cudaStreamWaitEvent(a, fork, 0) != cudaSuccess)
     r = HLQ_ERR_CUDA;
   if (r == HLQ_OK)  // g_w branch on the auxiliary stream
-    r = gw_impl(d_gy, dt, d_xbar, d_xbar_scale, T, Cin, Cout, block, rank, d_gw,
+    r = gw_impl(d_gy, dt, d_xbar, xbar_bits, d_xbar_scale, T, Cin, Cout, block, rank, d_gw,
                 base + gx_bytes, gw_bytes, nullptr, nullptr, nullptr, a, false);
   if (r == HLQ_OK)  // g_x branch on the caller's stream, its HQ of w on a third
     r = gx_impl(d_gy, d_w, dt, T, Cin, Cout, block, gran_gy, gran_w, rnd, seed, d_gx,
@@ -554,7 +574,8 @@ size_t hlq_layer_step_host_workspace_bytes(int dt, int64_t T, int64_t Cin, int64
 
 hlq_status hlq_layer_step_host(const void* h_x, const void* h_gy, const void* h_w, int dt,
                                int64_t T, int64_t Cin, int64_t Cout, int block, int rank,
-                               int gran_gy, int gran_w, int rnd, uint64_t seed, float* h_gx,
+                               int xbar_bits, int gran_gy, int gran_w, int rnd, uint64_t seed,
+                               float* h_gx,
                                float* h_gw, int8_t* d_xbar, float* d_xbar_scale,
                                int64_t chunk_tokens, void* d_ws, size_t ws_bytes,
                                void* stream) {
@@ -579,8 +600,8 @@ hlq_status hlq_layer_step_host(const void* h_x, const void* h_gy, const void* h_
   st = gx_impl(gy, w, dt, T, Cin, Cout, block, gran_gy, gran_w, rnd, seed, gx, base + L.gxws,
                gx_bytes, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, true);
   if (st != HLQ_OK) return st;
-  st = gw_impl(gy, dt, d_xbar, d_xbar_scale, T, Cin, Cout, block, rank, gw, base + L.gwws,
-               gw_bytes, nullptr, nullptr, nullptr, nullptr, true);
+  st = gw_impl(gy, dt, d_xbar, xbar_bits, d_xbar_scale, T, Cin, Cout, block, rank, gw,
+               base + L.gwws, gw_bytes, nullptr, nullptr, nullptr, nullptr, true);
   if (st != HLQ_OK) return st;
   if (!d_xbar_scale) return HLQ_ERR_INVALID_ARG;
   if (!aligned16(d_xbar)) return HLQ_ERR_ALIGN;
@@ -598,13 +619,14 @@ hlq_status hlq_layer_step_host(const void* h_x, const void* h_gy, const void* h_
     HLQ_TRY(h2d(x, h_x, (size_t)(T * Cin) * esz, s));
     HLQ_TRY(h2d(gy, h_gy, (size_t)(T * Cout) * esz, s));
     HLQ_TRY(h2d(w, h_w, (size_t)(Cout * Cin) * esz, s));
-    st = hlq_compress_activation(x, dt, T, Cin, block, rank, d_xbar, d_xbar_scale,
+    st = hlq_compress_activation(x, dt, T, Cin, block, rank, xbar_bits, d_xbar, d_xbar_scale,
                                  base + L.cws, compress_ws(T, Cin), stream);
     if (st != HLQ_OK) return st;
     st = hlq_linear_backward_gx(gy, w, dt, T, Cin, Cout, block, gran_gy, gran_w, rnd, seed,
                                 gx, base + L.gxws, gx_bytes, stream);
     if (st != HLQ_OK) return st;
-    st = hlq_linear_backward_gw(gy, dt, d_xbar, d_xbar_scale, T, Cin, Cout, block, rank, gw,
+    st = hlq_linear_backward_gw(gy, dt, d_xbar, d_xbar_scale, T, Cin, Cout, block, rank,
+                                xbar_bits, gw,
                                 base + L.gwws, gw_bytes, stream);
     if (st != HLQ_OK) return st;
     HLQ_TRY(d2h(h_gx, gx, (size_t)(T * Cin) * 4, s));
@@ -723,10 +745,11 @@ hlq_status hlq_layer_step_host(const void* h_x, const void* h_gy, const void* h_
     r = hla_gy_launches(gy, bf16, T, Cout, rank, gw_amax, gwb + WL.qg, WL.ld, sg, status, a_gw);
   fail(cudaStreamWaitEvent(a_gw, x_in, 0));
   if (r == HLQ_OK)
-    r = compress_launches(x, bf16, T, Cin, rank, d_xbar, d_xbar_scale,
+    r = compress_launches(x, bf16, T, Cin, rank, xbar_bits, d_xbar, d_xbar_scale,
                           reinterpret_cast<unsigned int*>(base + L.cws), status, a_gw);
   if (r == HLQ_OK)
-    r = gw_gemm_launches(d_xbar, d_xbar_scale, Cin, Cout, Tp, WL, gwb, gw, nullptr, status,
+    r = gw_gemm_launches(d_xbar, xbar_bits, d_xbar_scale, Cin, Cout, Tp, WL, gwb, gw, nullptr,
+                         status,
                          a_gw);
   fail(cudaEventRecord(gw_done, a_gw));
   // copy-out stream: g_x chunk by chunk as they finish, then g_w
@@ -758,9 +781,9 @@ hlq_status hlq_linear_backward_gw(const void* d_gy, int dt,
                                   const int8_t* d_xbar,
                                   const float* d_xbar_scale, int64_t T,
                                   int64_t Cin, int64_t Cout, int block,
-                                  int rank, float* d_gw, void* d_ws,
+                                  int rank, int xbar_bits, float* d_gw, void* d_ws,
                                   size_t ws_bytes, void* stream) {
-  return gw_impl(d_gy, dt, d_xbar, d_xbar_scale, T, Cin, Cout, block, rank,
+  return gw_impl(d_gy, dt, d_xbar, xbar_bits, d_xbar_scale, T, Cin, Cout, block, rank,
                  d_gw, d_ws, ws_bytes, nullptr, nullptr, nullptr, stream);
 }
 
@@ -778,10 +801,10 @@ hlq_status hlq_debug_gx_parts(const void* d_gy, const void* d_w, int dt,
 hlq_status hlq_debug_gw_parts(const void* d_gy, int dt, const int8_t* d_xbar,
                               const float* d_xbar_scale, int64_t T,
                               int64_t Cin, int64_t Cout, int block, int rank,
-                              float* d_gw, void* d_ws, size_t ws_bytes,
+                              int xbar_bits, float* d_gw, void* d_ws, size_t ws_bytes,
                               int8_t* d_qg, float* d_sg, int32_t* d_acc,
                               void* stream) {
-  return gw_impl(d_gy, dt, d_xbar, d_xbar_scale, T, Cin, Cout, block, rank,
+  return gw_impl(d_gy, dt, d_xbar, xbar_bits, d_xbar_scale, T, Cin, Cout, block, rank,
                  d_gw, d_ws, ws_bytes, d_qg, d_sg, d_acc, stream);
 }
 

@@ -31,11 +31,15 @@ cudaError_t launch_hq_cols(const void* src, bool bf16, int64_t rows,
                            uint32_t stream_id, unsigned int* status,
                            cudaStream_t st);
 
-// HLA of src [T, C] along tokens -> codes [C, T*rank/16] (int8, or bf16
-// values when out_bf16), per-tensor scale from *amax_slot.
+// Output formats of launch_hla: int8 codes, their bf16 values, or int4
+// codes packed two per byte (even ranks only).
+constexpr int kHlaOutI8 = 0, kHlaOutBf16 = 1, kHlaOutI4 = 2;
+
+// HLA of src [T, C] along tokens -> codes [C, T*rank/16] in `out_fmt`,
+// per-tensor scale RN(amax/qmax) from *amax_slot (qmax 7 for int4, else 127).
 // out_ld: row stride of `out` in codes (>= T*rank/16).
 cudaError_t launch_hla(const void* src, bool bf16, int64_t T, int64_t C,
-                       int rank, bool amax_only, bool out_bf16,
+                       int rank, bool amax_only, int out_fmt,
                        unsigned int* amax_slot, void* out, int64_t out_ld,
                        float* scale, unsigned int* status, cudaStream_t st);
 
@@ -51,6 +55,8 @@ cudaError_t launch_hla_transform(const void* src, bool bf16, int64_t T,
                                  unsigned int* status, cudaStream_t st);
 
 // in [rows, cols] int8 (row stride cols) -> out [rows, out_ld] bf16.
+cudaError_t launch_widen_i4_bf16(const uint8_t* in, void* out, int64_t rows, int64_t cols,
+                                 int64_t out_ld, cudaStream_t st);
 cudaError_t launch_widen_i8_bf16(const int8_t* in, void* out, int64_t rows,
                                  int64_t cols, int64_t out_ld, cudaStream_t st);
 cudaError_t launch_decode_e4m3(const uint8_t* in, int8_t* out, int64_t n,

@@ -393,7 +393,28 @@ __global__ void __launch_bounds__(256) hq_rows_kernel(
 // apart): helpers shared by the w and HLA kernels and the transform-only
 // debug kernel.
 // ---------------------------------------------------------------------------
-enum ColOut { kColI8 = 1, kColBf16 = 2 };
+enum ColOut { kColI8 = 1, kColBf16 = 2, kColI4 = 3 };
+
+// Code storage of an HLA output format: bytes per code as num / den (int4
+// codes are packed two per byte, code 2k in the low nibble), and the
+// symmetric code range.
+template <int kOut>
+struct ColFmt {
+  static constexpr int kNum = kOut == kColBf16 ? 2 : 1;
+  static constexpr int kDen = kOut == kColI4 ? 2 : 1;
+  static constexpr float kQmax = kOut == kColI4 ? 7.0f : 127.0f;
+};
+
+// Pack code k (an integer-valued float) of a column's block into p.
+template <int kOut>
+__device__ __forceinline__ void pack_code(uint32_t* p, int k, float q) {
+  if (kOut == kColBf16)
+    p[k >> 1] |= (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(q)) << (16 * (k & 1));
+  else if (kOut == kColI4)
+    p[k >> 3] |= ((uint32_t)(int)q & 0xfu) << (4 * (k & 7));
+  else
+    p[k >> 2] |= ((uint32_t)(int)q & 0xffu) << (8 * (k & 3));
+}
 
 // Store `n` bytes (1, 2, 4, 8, 16 or 32) of packed codes.
 __device__ __forceinline__ void store_chunk(uint8_t* dst, const uint32_t* p, int n) {
@@ -628,8 +649,9 @@ __global__ void __launch_bounds__(256, 2) hla_kernel(
   pdl_trigger();
   pdl_wait();
   extern __shared__ __align__(16) uint8_t smem[];
-  constexpr int kBytes = kOut == kColBf16 ? 2 : 1;
-  constexpr int chunk = kR * kBytes;                      // bytes / block / column
+  using F = ColFmt<kOut>;
+  constexpr int chunk = kR * F::kNum / F::kDen;           // bytes / block / column
+  static_assert(chunk >= 1, "int4 codes need an even rank");
   constexpr int row_stride = (kHlaBlocks + 1) * chunk;    // odd number of chunks
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
   const int64_t n_blk = T >> 4;
@@ -640,7 +662,7 @@ __global__ void __launch_bounds__(256, 2) hla_kernel(
   const int nb = col_ok ? (int)imin64(kHlaBW, n_blk - b_first) : 0;
 
   float s = 0.0f;
-  if (kMode == kQuant) s = __fdiv_rn(__uint_as_float(*amax_slot), 127.0f);
+  if (kMode == kQuant) s = __fdiv_rn(__uint_as_float(*amax_slot), ColFmt<kOut>::kQmax);
   float amax = 0.0f;
   RawPairCol<kBf16> cur, nxt;
   if (nb > 0) load_pair_col<kBf16>(src, 16 * b_first * C + c0, C, cur);
@@ -692,14 +714,7 @@ __global__ void __launch_bounds__(256, 2) hla_kernel(
       } else {
         uint32_t p[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
 #pragma unroll
-        for (int k = 0; k < kR; ++k) {
-          const float q = quant_rne_f(coef[k], s, 127.0f);
-          if (kOut == kColBf16) {
-            p[k >> 1] |= (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(q)) << (16 * (k & 1));
-          } else {
-            p[k >> 2] |= ((uint32_t)(int)q & 0xffu) << (8 * (k & 3));
-          }
-        }
+        for (int k = 0; k < kR; ++k) pack_code<kOut>(p, k, quant_rne_f(coef[k], s, F::kQmax));
         store_chunk(smem + (size_t)(c * 32 + tx) * row_stride + bl * chunk, p, chunk);
       }
     }
@@ -714,7 +729,7 @@ __global__ void __launch_bounds__(256, 2) hla_kernel(
   // stage row r holds column tile_base + 2 * (r % 32) + r / 32
   const int64_t valid_b = imin64(kHlaBlocks, n_blk - b_cta);
   const int64_t seg_bytes = valid_b * chunk;
-  const int64_t row_bytes = out_ld * kBytes;
+  const int64_t row_bytes = out_ld * F::kNum / F::kDen;
   const int64_t off = b_cta * chunk;
   uint8_t* outb = static_cast<uint8_t*>(out);
   const int64_t col_base = (int64_t)blockIdx.x * kHlaCols;
@@ -782,12 +797,14 @@ __global__ void __launch_bounds__(128 * kTmaBlocks) hla_tma_kernel(
     unsigned int* __restrict__ amax_slot, void* __restrict__ out, int64_t out_ld,
     float* __restrict__ scale, unsigned int* __restrict__ status) {
   constexpr int kStage = 16 * kTmaCols * (kBf16 ? 2 : 4);
+  using F = ColFmt<kOut>;
+  constexpr int kChunk = kR * F::kNum / F::kDen;  // code bytes / block / column
+  static_assert(kChunk >= 1, "int4 codes need an even rank");
   extern __shared__ __align__(128) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kTmaBlocks * kStage);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(full + kTmaBlocks);
-  constexpr int kBytes = kOut == kColBf16 ? 2 : 1;
 
   // thread (t, i): column pair t of block i of the tile
   const int t = threadIdx.x & 127, i = threadIdx.x >> 7;
@@ -814,7 +831,7 @@ __global__ void __launch_bounds__(128 * kTmaBlocks) hla_tma_kernel(
   const int64_t c0 = col0 + 2 * t;
   const bool col_ok = c0 < C;
   float s = 0.0f;
-  if (kMode == kQuant) s = __fdiv_rn(__uint_as_float(*amax_slot), 127.0f);
+  if (kMode == kQuant) s = __fdiv_rn(__uint_as_float(*amax_slot), ColFmt<kOut>::kQmax);
   float amax = 0.0f;
   uint8_t* outb = static_cast<uint8_t*>(out);
   bool ok = true;
@@ -869,14 +886,8 @@ __global__ void __launch_bounds__(128 * kTmaBlocks) hla_tma_kernel(
       } else {
         uint32_t p[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
 #pragma unroll
-        for (int k = 0; k < kR; ++k) {
-          const float q = quant_rne_f(coef[k], s, 127.0f);
-          if (kOut == kColBf16)
-            p[k >> 1] |= (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(q)) << (16 * (k & 1));
-          else
-            p[k >> 2] |= ((uint32_t)(int)q & 0xffu) << (8 * (k & 3));
-        }
-        store_chunk(outb + ((c0 + c) * out_ld + b * kR) * kBytes, p, kR * kBytes);
+        for (int k = 0; k < kR; ++k) pack_code<kOut>(p, k, quant_rne_f(coef[k], s, F::kQmax));
+        store_chunk(outb + ((c0 + c) * out_ld + b * kR) * F::kNum / F::kDen, p, kChunk);
       }
     }
   }
@@ -1182,9 +1193,10 @@ static cudaError_t launch_hla_r(const void* src, int64_t T, int64_t C,
                                 unsigned int* amax_slot, void* out, int64_t out_ld,
                                 float* scale, unsigned int* status, cudaStream_t st) {
   // TMA-staged path: chunk stores of R codes need R-code-aligned rows
-  const int chunk = R * (O == kColBf16 ? 2 : 1);
+  using F = ColFmt<O>;
+  const int chunk = R * F::kNum / F::kDen;
   const bool chunk_ok = (chunk == 1 || chunk == 2 || chunk % 4 == 0) &&
-                        (out_ld * (O == kColBf16 ? 2 : 1)) % (chunk >= 16 ? 16 : chunk) == 0;
+                        (out_ld * F::kNum / F::kDen) % (chunk >= 16 ? 16 : chunk) == 0;
   CUtensorMap tm;
   if (chunk_ok && make_tile_map_2d(&tm, src, B, T, C, kTmaCols, 16)) {
     const size_t smem = 128 + (size_t)kTmaBlocks * 16 * kTmaCols * (B ? 2 : 4) +
@@ -1196,8 +1208,7 @@ static cudaError_t launch_hla_r(const void* src, int64_t T, int64_t C,
                C, amax_slot, out, out_ld, scale, status);
     return cudaGetLastError();
   }
-  const size_t smem =
-      M == kAmax ? 0 : (size_t)kHlaCols * (kHlaBlocks + 1) * R * (O == kColBf16 ? 2 : 1);
+  const size_t smem = M == kAmax ? 0 : (size_t)kHlaCols * (kHlaBlocks + 1) * chunk;
   if (smem > 48 * 1024) {
     cudaError_t e = ensure_smem_limit<hla_kernel<B, M, O, R>>(smem);
     if (e != cudaSuccess) return e;
@@ -1213,23 +1224,35 @@ static cudaError_t launch_hla_o(const void* src, int64_t T, int64_t C, int rank,
                                 unsigned int* amax_slot, void* out, int64_t out_ld,
                                 float* scale, unsigned int* status, cudaStream_t st) {
 #define LHR(R) launch_hla_r<B, M, O, R>(src, T, C, amax_slot, out, out_ld, scale, status, st)
-  switch (rank) {
-    case 1: return LHR(1);
-    case 2: return LHR(2);
-    case 4: return LHR(4);
-    case 8: return LHR(8);
-    default: return LHR(16);
+  if constexpr (O == kColI4) {  // two codes per byte: even ranks only
+    switch (rank) {
+      case 2: return LHR(2);
+      case 4: return LHR(4);
+      case 8: return LHR(8);
+      case 16: return LHR(16);
+      default: return cudaErrorInvalidValue;
+    }
+  } else {
+    switch (rank) {
+      case 1: return LHR(1);
+      case 2: return LHR(2);
+      case 4: return LHR(4);
+      case 8: return LHR(8);
+      default: return LHR(16);
+    }
   }
 #undef LHR
 }
 
 cudaError_t launch_hla(const void* src, bool bf16, int64_t T, int64_t C,
-                       int rank, bool amax_only, bool out_bf16,
+                       int rank, bool amax_only, int out_fmt,
                        unsigned int* amax_slot, void* out, int64_t out_ld,
                        float* scale, unsigned int* status, cudaStream_t st) {
 #define LHO(B, M, O) launch_hla_o<B, M, O>(src, T, C, rank, amax_slot, out, out_ld, scale, status, st)
   if (amax_only) return bf16 ? LHO(true, kAmax, kColI8) : LHO(false, kAmax, kColI8);
-  if (out_bf16) return bf16 ? LHO(true, kQuant, kColBf16) : LHO(false, kQuant, kColBf16);
+  if (out_fmt == kHlaOutBf16)
+    return bf16 ? LHO(true, kQuant, kColBf16) : LHO(false, kQuant, kColBf16);
+  if (out_fmt == kHlaOutI4) return bf16 ? LHO(true, kQuant, kColI4) : LHO(false, kQuant, kColI4);
   return bf16 ? LHO(true, kQuant, kColI8) : LHO(false, kQuant, kColI8);
 #undef LHO
 }
@@ -1258,6 +1281,46 @@ cudaError_t launch_hla_transform(const void* src, bool bf16, int64_t T,
   dim3 grid(grid1(C / 4, 128), (unsigned)(T / 16));
   if (bf16) col_transform_kernel<true><<<grid, 128, 0, st>>>(src, T, C, rank, 0, out, status);
   else col_transform_kernel<false><<<grid, 128, 0, st>>>(src, T, C, rank, 0, out, status);
+  return cudaGetLastError();
+}
+
+// Packed int4 codes [rows, cols/2 bytes] (code 2k in the low nibble) to
+// bf16 rows with stride out_ld; 8 codes per thread.
+__global__ void widen_i4_to_bf16_kernel(const uint8_t* __restrict__ in,
+                                        __nv_bfloat16* __restrict__ out, int64_t rows,
+                                        int64_t cols, int64_t out_ld) {
+  pdl_trigger();
+  pdl_wait();
+  const int64_t per_row = (cols + 7) / 8;
+  const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= rows * per_row) return;
+  const int64_t r = idx / per_row, c = (idx % per_row) * 8;
+  const uint8_t* src = in + (r * cols + c) / 2;
+  __nv_bfloat16* dst = out + r * out_ld + c;
+  auto code = [&](int k) {  // sign-extended nibble k of the run
+    const int v = (src[k >> 1] >> (4 * (k & 1))) & 0xf;
+    return v >= 8 ? v - 16 : v;
+  };
+  if (c + 8 <= cols && (cols % 8) == 0) {
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(src);
+    __align__(16) __nv_bfloat16 o[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int v = (int)((w >> (4 * k)) & 0xfu);
+      o[k] = __int2bfloat16_rn(v >= 8 ? v - 16 : v);
+    }
+    *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(o);
+  } else {
+    for (int k = 0; k < 8 && c + k < cols; ++k) dst[k] = __int2bfloat16_rn(code(k));
+  }
+}
+
+cudaError_t launch_widen_i4_bf16(const uint8_t* in, void* out, int64_t rows, int64_t cols,
+                                 int64_t out_ld, cudaStream_t st) {
+  if (rows * cols == 0) return cudaSuccess;
+  const int64_t n = rows * ((cols + 7) / 8);
+  launch_pdl(widen_i4_to_bf16_kernel, dim3(grid1(n, 256)), dim3(256), 0, st, in,
+             static_cast<__nv_bfloat16*>(out), rows, cols, out_ld);
   return cudaGetLastError();
 }
 

@@ -85,16 +85,22 @@ size_t hlq_workspace_bytes(int op, int64_t T, int64_t Cin, int64_t Cout,
 
 /*
  * ACBP at forward time (HOT, Approach: stored activations compressed when
- * the forward pass runs; HLQ TL;DR: "activation-compression").
- * x [T, Cin] (dtype dt) -> d_xbar [Cin, T'] int8 codes (token dim
- * contiguous) and d_xbar_scale [1] fp32:
+ * the forward pass runs; HLQ TL;DR: "activation-compression", "int4
+ * activation-compression strategy").
+ * x [T, Cin] (dtype dt) -> d_xbar codes (token dim contiguous) and
+ * d_xbar_scale [1] fp32:
  *   Xbar[c, rank*b + k] = RN_f32( sum_j H16[sigma(k)][j] x[16b + j, c] )
- *   s = RN_f32(max|Xbar| / 127),  code = clamp(rne(RN_f32(Xbar / s)), +-127)
+ *   s = RN_f32(max|Xbar| / qmax),  code = clamp(rne(RN_f32(Xbar / s)), +-qmax)
  * where sigma(k) is the Sylvester row of sequency k (the rank lowest-
  * sequency Walsh rows are kept).  s == 0 gives all-zero codes.
+ * xbar_bits 8: qmax 127, d_xbar [Cin, T'] int8 codes.
+ * xbar_bits 4: qmax 7, d_xbar [Cin, T'/2] bytes, two's-complement int4 codes
+ *   packed two per byte (code 2k in the low nibble, 2k+1 in the high one);
+ *   even ranks only (HLQ_ERR_UNSUPPORTED for rank 1).
+ * Other xbar_bits: HLQ_ERR_INVALID_ARG.
  */
 hlq_status hlq_compress_activation(const void *d_x, int dt, int64_t T,
-                                   int64_t Cin, int block, int rank,
+                                   int64_t Cin, int block, int rank, int xbar_bits,
                                    int8_t *d_xbar, float *d_xbar_scale,
                                    void *d_ws, size_t ws_bytes, void *stream);
 
@@ -128,12 +134,13 @@ hlq_status hlq_linear_backward_gx(const void *d_gy, const void *d_w, int dt,
  *   acc[o, i] = sum_t' qG[o, t'] qX[i, t']  (exact integer),
  *   g_w[o, i] = acc * s_g * s_x / 16   (fp32).
  * d_xbar / d_xbar_scale come from hlq_compress_activation with the same T,
- * Cin and rank.  Needs T' * 127^2 < 2^31.
+ * Cin, rank and xbar_bits (the qX codes are then in [-127, 127] or [-7, 7]).
+ * Needs T' * 127 * qmax_x < 2^31.
  */
 hlq_status hlq_linear_backward_gw(const void *d_gy, int dt, const int8_t *d_xbar,
                                   const float *d_xbar_scale, int64_t T,
                                   int64_t Cin, int64_t Cout, int block,
-                                  int rank, float *d_gw, void *d_ws,
+                                  int rank, int xbar_bits, float *d_gw, void *d_ws,
                                   size_t ws_bytes, void *stream);
 
 /*
@@ -149,7 +156,7 @@ hlq_status hlq_linear_backward_gw(const void *d_gy, int dt, const int8_t *d_xbar
 hlq_status hlq_linear_backward(const void *d_gy, const void *d_w, const int8_t *d_xbar,
                                const float *d_xbar_scale, int dt, int64_t T,
                                int64_t Cin, int64_t Cout, int block, int rank,
-                               int gran_gy, int gran_w, int rnd, uint64_t seed,
+                               int xbar_bits, int gran_gy, int gran_w, int rnd, uint64_t seed,
                                float *d_gx, float *d_gw, void *d_ws, size_t ws_bytes,
                                void *stream);
 
@@ -175,8 +182,8 @@ hlq_status hlq_debug_gx_parts(const void *d_gy, const void *d_w, int dt,
  */
 hlq_status hlq_debug_gw_parts(const void *d_gy, int dt, const int8_t *d_xbar,
                               const float *d_xbar_scale, int64_t T, int64_t Cin,
-                              int64_t Cout, int block, int rank, float *d_gw,
-                              void *d_ws, size_t ws_bytes, int8_t *d_qg,
+                              int64_t Cout, int block, int rank, int xbar_bits,
+                              float *d_gw, void *d_ws, size_t ws_bytes, int8_t *d_qg,
                               float *d_sg, int32_t *d_acc, void *stream);
 
 /*
@@ -249,8 +256,9 @@ size_t hlq_debug_tc_gemm_ws_bytes(int64_t M, int64_t N);
  * device entry points on the same inputs.
  *   h_x [T, Cin], h_gy [T, Cout], h_w [Cout, Cin]: host, dtype dt;
  *   h_gx [T, Cin], h_gw [Cout, Cin]: host fp32 outputs;
- *   d_xbar [Cin, T'] int8 and d_xbar_scale [1]: device, filled by the call
- *   (the stored activation of the step);
+ *   d_xbar (int8 [Cin, T'] or packed int4 [Cin, T'/2], per xbar_bits as in
+ *   hlq_compress_activation) and d_xbar_scale [1]: device, filled by the
+ *   call (the stored activation of the step);
  *   d_ws: device workspace of hlq_layer_step_host_workspace_bytes(...),
  *   which also holds the device copies of the inputs and outputs.
  * Host buffers should be page-locked (cudaHostAlloc / cudaHostRegister):
@@ -262,13 +270,15 @@ size_t hlq_debug_tc_gemm_ws_bytes(int64_t M, int64_t N);
  */
 hlq_status hlq_layer_step_host(const void *h_x, const void *h_gy, const void *h_w,
                                int dt, int64_t T, int64_t Cin, int64_t Cout,
-                               int block, int rank, int gran_gy, int gran_w,
-                               int rnd, uint64_t seed, float *h_gx, float *h_gw,
+                               int block, int rank, int xbar_bits, int gran_gy,
+                               int gran_w, int rnd, uint64_t seed, float *h_gx, float *h_gw,
                                int8_t *d_xbar, float *d_xbar_scale,
                                int64_t chunk_tokens, void *d_ws, size_t ws_bytes,
                                void *stream);
 size_t hlq_layer_step_host_workspace_bytes(int dt, int64_t T, int64_t Cin,
-                                           int64_t Cout, int block, int rank);/*
+                                           int64_t Cout, int block, int rank);
+
+/*
  * Launch tracing, for timing without a profiler.  hlq_trace_begin creates
  * 2*capacity CUDA events (host-side objects, no device memory) and turns
  * tracing on: every later kernel launch of this library, on any stream, is

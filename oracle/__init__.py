@@ -289,6 +289,30 @@ def gx_path(g_y, w, gran_gy=PER_TOKEN, rnd=SR, seed=0, rows=None):
                 g_x=g_x, rows=sel)
 
 
+def hq_mse(Y, gran: int) -> float:
+    """Mean squared error of the int4 HQ quantizer with round-to-nearest-even
+    on transformed values Y [T, Cout] at granularity `gran`: mean over all
+    elements of (q * s - Y)^2, each term exact in fp64 before squaring."""
+    q, s = hq_quantize(Y, gran, RNE, 0, STREAM_GY)
+    sc = (np.asarray(s, np.float64)[:, None] if gran == PER_TOKEN
+          else np.float64(s[0]))
+    err = q.astype(np.float64) * sc - np.asarray(Y, np.float64)
+    return float(np.mean(err * err))
+
+
+def lqs_select(g_y, threshold: float = 1.5):
+    """Layer-wise quantizer selection for the HQ of g_y (HOT summary page,
+    Approach: per-token or per-tensor quantizer chosen per layer; Limitations:
+    a calibration set and a 50 % MSE-difference threshold): per-token iff the
+    per-tensor MSE exceeds the per-token MSE by more than 50 %.  Returns
+    (choice, mse_per_tensor, mse_per_token)."""
+    Y = hq_transform(g_y, axis=0)
+    m_tensor = hq_mse(Y, PER_TENSOR)
+    m_token = hq_mse(Y, PER_TOKEN)
+    choice = PER_TOKEN if m_tensor > threshold * m_token else PER_TENSOR
+    return choice, m_tensor, m_token
+
+
 def compress_activation(x, rank=8, bits=8):
     """ACBP at forward time: x [T, Cin] -> codes [Cin, T*rank/16] (int8
     values: [-127, 127] for bits=8, [-7, 7] for bits=4; pack_int4 gives the

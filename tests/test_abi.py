@@ -70,12 +70,12 @@ def gx(L, **kw):
 
 def gw(L, **kw):
     a = dict(gy=FAKE, dt=1, xbar=FAKE, xs=FAKE, T=256, Cin=64, Cout=128,
-             block=16, rank=8, gw=FAKE, ws=FAKE_WS, ws_bytes=1 << 30,
+             block=16, rank=8, bits=8, gw=FAKE, ws=FAKE_WS, ws_bytes=1 << 30,
              stream=None)
     a.update(kw)
     return L.hlq_linear_backward_gw(
         a["gy"], a["dt"], a["xbar"], a["xs"], a["T"], a["Cin"], a["Cout"],
-        a["block"], a["rank"], a["gw"], a["ws"], a["ws_bytes"], a["stream"])
+        a["block"], a["rank"], a["bits"], a["gw"], a["ws"], a["ws_bytes"], a["stream"])
 
 
 def test_gx_argument_validation(L):
@@ -105,16 +105,21 @@ def test_gw_argument_validation(L):
     assert gw(L, xbar=FAKE + 1) == 3
     assert gw(L, ws_bytes=0) == 5
     assert gw(L, T=266304) == 6               # T' * 127^2 >= 2^31
+    assert gw(L, bits=6) == 1                 # ACBP storage: 8 or 4 bits
+    assert gw(L, bits=4, rank=1) == 4         # int4 codes pack two per byte
+    assert gw(L, bits=4, T=266304) != 6       # T' * 127 * 7 < 2^31 still
 
 
 def test_compress_argument_validation(L):
     f = L.hlq_compress_activation
-    assert f(FAKE, 1, 256, 64, 15, 8, FAKE, FAKE, FAKE_WS, 1 << 20, None) == 1
-    assert f(FAKE, 1, 256, 64, 16, 5, FAKE, FAKE, FAKE_WS, 1 << 20, None) == 1
-    assert f(FAKE, 1, 250, 64, 16, 8, FAKE, FAKE, FAKE_WS, 1 << 20, None) == 2
-    assert f(FAKE, 1, 256, 64, 16, 8, FAKE, None, FAKE_WS, 1 << 20, None) == 1
-    assert f(FAKE + 2, 1, 256, 64, 16, 8, FAKE, FAKE, FAKE_WS, 1 << 20, None) == 3
-    assert f(FAKE, 1, 256, 64, 16, 8, FAKE, FAKE, FAKE_WS, 0, None) == 5
+    assert f(FAKE, 1, 256, 64, 15, 8, 8, FAKE, FAKE, FAKE_WS, 1 << 20, None) == 1
+    assert f(FAKE, 1, 256, 64, 16, 5, 8, FAKE, FAKE, FAKE_WS, 1 << 20, None) == 1
+    assert f(FAKE, 1, 250, 64, 16, 8, 8, FAKE, FAKE, FAKE_WS, 1 << 20, None) == 2
+    assert f(FAKE, 1, 256, 64, 16, 8, 8, FAKE, None, FAKE_WS, 1 << 20, None) == 1
+    assert f(FAKE + 2, 1, 256, 64, 16, 8, 8, FAKE, FAKE, FAKE_WS, 1 << 20, None) == 3
+    assert f(FAKE, 1, 256, 64, 16, 8, 8, FAKE, FAKE, FAKE_WS, 0, None) == 5
+    assert f(FAKE, 1, 256, 64, 16, 8, 2, FAKE, FAKE, FAKE_WS, 1 << 20, None) == 1
+    assert f(FAKE, 1, 256, 64, 16, 1, 4, FAKE, FAKE, FAKE_WS, 1 << 20, None) == 4
 
 
 def test_tc_gemm_plan_validation(L):
@@ -140,11 +145,12 @@ def test_step_host_validation_and_workspace(L):
 
     def call(**kw):
         a = dict(hx=FAKE, hgy=FAKE, hw=FAKE, dt=1, T=256, Cin=64, Cout=128, block=16,
-                 rank=8, gran_gy=1, gran_w=0, rnd=1, seed=0, hgx=FAKE, hgw=FAKE,
+                 rank=8, bits=8, gran_gy=1, gran_w=0, rnd=1, seed=0, hgx=FAKE, hgw=FAKE,
                  xbar=FAKE, xs=FAKE, chunk=0, ws=FAKE_WS, ws_bytes=1 << 30)
         a.update(kw)
         return f(a["hx"], a["hgy"], a["hw"], a["dt"], a["T"], a["Cin"], a["Cout"],
-                 a["block"], a["rank"], a["gran_gy"], a["gran_w"], a["rnd"], a["seed"],
+                 a["block"], a["rank"], a["bits"], a["gran_gy"], a["gran_w"], a["rnd"],
+                 a["seed"],
                  a["hgx"], a["hgw"], a["xbar"], a["xs"], a["chunk"], a["ws"],
                  a["ws_bytes"], None)
 
@@ -158,6 +164,7 @@ def test_step_host_validation_and_workspace(L):
     assert call(xbar=FAKE + 4) == 3
     assert call(xs=None) == 1
     assert call(gran_w=1) == 4
+    assert call(bits=5) == 1
 
 
 def test_read_status_rejects_null(L):

@@ -318,6 +318,40 @@ def test_int4_acbp_lossless_gw():
     assert np.allclose(r["g_w"], want, rtol=1e-12, atol=1e-15)
 
 
+def test_lqs_mse_bounds_and_known_choices():
+    """Layer-wise quantizer selection: MSE of RNE codes is bounded by s^2/4
+    per element (no value clamps with RNE when s = RN(amax/7) rounds up, and
+    a clamped value errs by at most s/2 + ulp); values on the code grid give
+    zero error; a token a few times larger than the rest makes the
+    per-tensor scale too coarse for the others (per-token chosen), while a
+    huge one dominates both means (its own error is the same either way);
+    identical tokens make both equal (per-tensor kept)."""
+    rng = np.random.default_rng(31)
+    g = rng.standard_normal((64, 128)).astype(np.float32)
+    Y = oracle.hq_transform(g, axis=0)
+    for gran in (oracle.PER_TENSOR, oracle.PER_TOKEN):
+        _, s = oracle.hq_quantize(Y, gran, oracle.RNE, 0, 0)
+        s2 = (np.asarray(s, np.float64) ** 2).mean() if gran == oracle.PER_TOKEN else float(s[0]) ** 2
+        m = oracle.hq_mse(Y, gran)
+        assert 0 < m <= s2 / 4 * (1 + 1e-6)
+    # on the grid: Y = k * s exactly for every element -> zero error
+    grid = np.tile(np.arange(-7, 8, dtype=np.float32), (4, 1)) * np.float32(0.25)
+    assert oracle.hq_mse(grid, oracle.PER_TENSOR) == 0.0
+    g2 = rng.standard_normal((64, 128)).astype(np.float32)
+    g2[5] *= 4.0
+    choice, mt, mk = oracle.lqs_select(g2)
+    assert choice == oracle.PER_TOKEN and mt > 1.5 * mk
+    g2[5] *= 250.0
+    choice, mt, mk = oracle.lqs_select(g2)
+    assert choice == oracle.PER_TENSOR and mk <= mt <= 1.5 * mk
+    # identical tokens: per-token scales all equal the per-tensor one
+    g3 = np.tile(rng.standard_normal((1, 128)).astype(np.float32), (32, 1))
+    choice, mt, mk = oracle.lqs_select(g3)
+    assert mt == mk and choice == oracle.PER_TENSOR
+    choice, mt, mk = oracle.lqs_select(np.zeros((16, 32), np.float32))
+    assert mt == mk == 0.0 and choice == oracle.PER_TENSOR
+
+
 def test_clamp_when_scale_rounds_down():
     # amax/7 rounded to fp32 can be below the true quotient, so amax/s > 7
     for amax in np.float32([1.0, 3.0, 5.0, 0.1, 1e-3, 123.456]):
