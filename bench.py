@@ -468,6 +468,9 @@ def run_ours(args, wl, rank, world, local_rank):
                 "traffic": traffic, "peak_source": peaks["source"]}
 
     us = ms * 1e3 / world                 # job-wide us per layer step
+    gemm_ops = 2 * T * Cin * Cout + 2 * Cout * Cin * Tp
+    gemm_bitops = 2 * T * Cin * Cout * 4 + 2 * Cout * Cin * Tp * 8
+    gemm_s = sum(v[1] for k, v in per_kernel.items() if k.startswith("gemm")) / args.steps / 1e3
     fwd_ms = sum(v[1] for k, v in per_kernel.items()
                  if k.startswith("hla_x")) / args.steps
     bwd_ms = ms - fwd_ms
@@ -480,6 +483,11 @@ def run_ours(args, wl, rank, world, local_rank):
         "backward_us": bwd_ms * 1e3,
         "forward_acbp_us": fwd_ms * 1e3,
         "effective_tops": 4 * T * Cin * Cout / (bwd_ms / 1e3) / 1e12,
+        # integer ops the two GEMMs execute (reduced K = T' on the g_w side),
+        # per second of their traced time; and those ops x operand bits
+        "gemm_int_tops": gemm_ops / gemm_s / 1e12 if gemm_s > 0 else None,
+        "gemm_tbops": gemm_bitops / gemm_s / 1e12 if gemm_s > 0 else None,
+        "acbp_stored_bytes": acbp_bytes(T, Cin, wl.rank, e),
         "timing": timing,
         "ms_per_step_eager": ms_eager,
         "roofline": roofline,
@@ -508,6 +516,17 @@ def kernel_sources_digest():
             with open(os.path.join(d, name), "rb") as f:
                 h.update(f.read())
     return h.hexdigest()
+
+
+def acbp_bytes(T, Cin, rank, e):
+    """Bytes of the activation kept for the backward pass: x itself, or the
+    ACBP buffer with int8 or packed int4 codes (plus its 4-byte scale)."""
+    Tp = T // 16 * rank
+    raw = T * Cin * e
+    i8 = Cin * Tp + 4
+    i4 = Cin * Tp // 2 + 4
+    return {"x": raw, "int8": i8, "int4": i4,
+            "saved_int8": 1 - i8 / raw, "saved_int4": 1 - i4 / raw}
 
 
 def load_traffic(kernel, wl):

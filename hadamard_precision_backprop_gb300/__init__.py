@@ -24,6 +24,7 @@ PER_TENSOR, PER_TOKEN = 0, 1
 RNE, SR = 0, 1
 F32, BF16 = 0, 1
 OP_COMPRESS_ACTIVATION, OP_BACKWARD_GX, OP_BACKWARD_GW, OP_BACKWARD = 0, 1, 2, 3
+OP_SELECT_GRANULARITY = 4
 DEV_NONFINITE, DEV_TIMEOUT, DEV_BADCODE = 0x1, 0x2, 0x4
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -40,6 +41,7 @@ EXPORTS = [
     "hlq_linear_backward",
     "hlq_layer_step_host",
     "hlq_layer_step_host_workspace_bytes",
+    "hlq_select_gy_granularity",
 ]
 
 _lock = threading.Lock()
@@ -100,6 +102,8 @@ def lib() -> ctypes.CDLL:
             "hlq_layer_step_host": (i32, [P, P, P, i32, i64, i64, i64, i32, i32, i32,
                                           i32, i32, i32, u64, P, P, P, P, i64, P, sz, P]),
             "hlq_layer_step_host_workspace_bytes": (sz, [i32, i64, i64, i64, i32, i32]),
+            "hlq_select_gy_granularity": (i32, [P, i32, i64, i64, i32, ctypes.c_double,
+                                                P, P, P, sz, P]),
             "hlq_trace_end": (i32, [P]),
             "hlq_trace_get": (i32, [i32, P, P]),
             "hlq_trace_free": (i32, []),
@@ -332,6 +336,23 @@ def hlq_layer_step_host(x, g_y, w, xbar, xbar_scale, rank: int = 8,
         rnd, seed, _ptr(out_gx), _ptr(out_gw), _ptr(xbar), _ptr(xbar_scale),
         chunk_tokens, _ptr(ws), ws.numel(), _stream(stream)), "hlq_layer_step_host")
     return out_gx, out_gw
+
+
+def hlq_select_gy_granularity(g_y, threshold: float = 1.5, block: int = 16,
+                              stream=None):
+    """Layer-wise quantizer selection on a calibration sample g_y [T, Cout]:
+    returns device tensors (mse [2] fp64: per tensor, per token; choice [1]
+    int32: PER_TOKEN or PER_TENSOR)."""
+    torch = _torch()
+    _need_cuda_contig(g_y)
+    T, Cout = g_y.shape
+    mse = torch.empty(2, dtype=torch.float64, device=g_y.device)
+    choice = torch.empty(1, dtype=torch.int32, device=g_y.device)
+    ws = workspace(OP_SELECT_GRANULARITY, T, 16, Cout, block, 8, g_y.device)
+    _check(lib().hlq_select_gy_granularity(
+        _ptr(g_y), _dtype_code(g_y), T, Cout, block, float(threshold), _ptr(mse),
+        _ptr(choice), _ptr(ws), ws.numel(), _stream(stream)), "hlq_select_gy_granularity")
+    return mse, choice
 
 
 def hlq_debug_gx_parts(g_y, w, gran_gy=PER_TOKEN, gran_w=PER_TENSOR, rnd=SR,

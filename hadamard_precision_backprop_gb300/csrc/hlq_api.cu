@@ -482,6 +482,8 @@ size_t hlq_workspace_bytes(int op, int64_t T, int64_t Cin, int64_t Cout,
     case HLQ_OP_BACKWARD:
       return gx_layout(T, Cin, Cout).total +
              gw_layout(T, Cin, Cout, rank_ok(rank) ? rank : 16).total;
+    case HLQ_OP_SELECT_GRANULARITY:
+      return kAlign;  // amax slot at 0, two fp64 sums at 16
     default:
       return 0;
   }
@@ -563,6 +565,37 @@ hlq_status hlq_linear_backward(const void* d_gy, const void* d_w, const int8_t* 
   cudaEventDestroy(fork);
   cudaEventDestroy(join);
   return r;
+}
+
+hlq_status hlq_select_gy_granularity(const void* d_gy, int dt, int64_t T, int64_t Cout,
+                                     int block, double threshold, double* d_mse,
+                                     int32_t* d_choice, void* d_ws, size_t ws_bytes,
+                                     void* stream) {
+  hlq_status st = check_common(dt, T, 16, Cout, block);
+  if (st != HLQ_OK) return st;
+  if (!d_mse || !d_choice || !(threshold >= 0.0)) return HLQ_ERR_INVALID_ARG;
+  if (T * Cout > 0 && !d_gy) return HLQ_ERR_INVALID_ARG;
+  if (!aligned16(d_gy) || reinterpret_cast<uintptr_t>(d_mse) % 8 ||
+      reinterpret_cast<uintptr_t>(d_choice) % 4)
+    return HLQ_ERR_ALIGN;
+  if (!d_ws || ws_bytes < kAlign) return HLQ_ERR_WORKSPACE;
+  if (!aligned256(d_ws)) return HLQ_ERR_ALIGN;
+  unsigned int* status = device_status_ptr();
+  if (!status) return HLQ_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* base = static_cast<uint8_t*>(d_ws);
+  unsigned int* amax = reinterpret_cast<unsigned int*>(base);
+  double* sums = reinterpret_cast<double*>(base + 16);
+  const bool bf16 = dt == HLQ_BF16;
+  HLQ_TRY(cudaMemsetAsync(base, 0, 32, s));
+  if (T * Cout > 0)
+    HLQ_LAUNCH("hq_rows_amax", s,
+               launch_hq_rows(d_gy, bf16, T, Cout, false, true, amax, nullptr, nullptr,
+                              HLQ_RNE, 0, 0, status, s));
+  HLQ_LAUNCH("hq_mse", s,
+             launch_hq_mse(d_gy, bf16, T, Cout, amax, sums, threshold, d_mse, d_choice,
+                           status, s));
+  return HLQ_OK;
 }
 
 size_t hlq_layer_step_host_workspace_bytes(int dt, int64_t T, int64_t Cin, int64_t Cout,

@@ -24,6 +24,14 @@ cudaError_t launch_hq_rows(const void* src, bool bf16, int64_t rows,
 
 // HQ of a [rows, cols] tensor along rows (w), codes written transposed
 // [cols, rows] (E4M3), per-tensor scale from *amax_slot.
+// Layer-wise quantizer selection: RNE int4 HQ errors of g_y per tensor
+// (scale from *amax_slot) and per token added into sums[0..1] (zeroed by the
+// caller), then mse[g] = sums[g] / (rows * cols) and *choice.
+cudaError_t launch_hq_mse(const void* src, bool bf16, int64_t rows, int64_t cols,
+                          const unsigned int* amax_slot, double* sums, double threshold,
+                          double* mse, int32_t* choice, unsigned int* status,
+                          cudaStream_t st);
+
 cudaError_t launch_hq_cols(const void* src, bool bf16, int64_t rows,
                            int64_t cols, bool amax_only,
                            unsigned int* amax_slot, uint8_t* codes_t,

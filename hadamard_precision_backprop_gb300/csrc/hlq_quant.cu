@@ -1012,6 +1012,78 @@ __global__ void __launch_bounds__(256) hq_w_kernel(
 // Transform-only kernels (debug read-back of the exactly rounded Hadamard
 // coefficients; same device functions as the quantizing kernels).
 // ---------------------------------------------------------------------------
+// Quantization error of the int4 HQ of g_y with RNE codes, per tensor and
+// per token at once (layer-wise quantizer selection): one warp per row; the
+// row's transformed values give its amax (per-token scale), then a second
+// transform of the row (it is still in L1/L2) gives both errors
+// (q * s - Y)^2, exact differences in fp64, summed per warp and added into
+// sums[0] (per tensor, scale from *amax_slot) and sums[1] (per token).
+template <bool kBf16>
+__global__ void __launch_bounds__(256) hq_mse_kernel(const void* __restrict__ src,
+                                                     int64_t rows, int64_t cols,
+                                                     const unsigned int* __restrict__ amax_slot,
+                                                     double* __restrict__ sums,
+                                                     unsigned int* __restrict__ status) {
+  pdl_trigger();
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (row >= rows) return;  // whole warp leaves together
+  const int n_oct = (int)(cols >> 3);
+  const int iters = (n_oct + 31) >> 5;
+  const int64_t base = row * cols;
+  float amax = 0.0f;
+  for (int it = 0; it < iters; ++it) {
+    const int oct = it * 32 + lane;
+    float v[8];
+    transform_raw<kBf16>(load_raw<kBf16>(src, base + (int64_t)oct * 8, oct < n_oct), v, status);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) amax = fmaxf(amax, fabsf(v[k]));
+  }
+  amax = warp_max(amax);
+  const float st = __fdiv_rn(amax, 7.0f);
+  const float sg = __fdiv_rn(__uint_as_float(*amax_slot), 7.0f);
+  double et = 0.0, eg = 0.0;
+  for (int it = 0; it < iters; ++it) {
+    const int oct = it * 32 + lane;
+    float v[8];
+    transform_raw<kBf16>(load_raw<kBf16>(src, base + (int64_t)oct * 8, oct < n_oct), v, status);
+    if (oct >= n_oct) continue;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const double dt = (double)quant_rne_f(v[k], st, 7.0f) * st - (double)v[k];
+      const double dg = (double)quant_rne_f(v[k], sg, 7.0f) * sg - (double)v[k];
+      et += dt * dt;
+      eg += dg * dg;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    et += __shfl_xor_sync(0xffffffffu, et, o);
+    eg += __shfl_xor_sync(0xffffffffu, eg, o);
+  }
+  if (lane == 0) {
+    atomicAdd(&sums[0], eg);
+    atomicAdd(&sums[1], et);
+  }
+}
+
+// mse[g] = sums[g] / n; choice = per-token iff mse[0] > threshold * mse[1].
+__global__ void lqs_finalize_kernel(const double* __restrict__ sums, int64_t n,
+                                    double threshold, double* __restrict__ mse,
+                                    int32_t* __restrict__ choice) {
+  pdl_trigger();
+  pdl_wait();
+  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  const double mt = n > 0 ? sums[0] / (double)n : 0.0;
+  const double mk = n > 0 ? sums[1] / (double)n : 0.0;
+  mse[0] = mt;
+  mse[1] = mk;
+  *choice = mt > threshold * mk ? HLQ_PER_TOKEN : HLQ_PER_TENSOR;
+}
+
+
+// ---------------------------------------------------------------------------
 template <bool kBf16>
 __global__ void __launch_bounds__(256) hq_rows_transform_kernel(
     const void* __restrict__ src, int64_t rows, int64_t cols,
@@ -1166,6 +1238,25 @@ cudaError_t launch_hq_rows(const void* src, bool bf16, int64_t rows,
     if (bf16) HQR(true, kQuant, false); else HQR(false, kQuant, false);
   }
 #undef HQR
+  return cudaGetLastError();
+}
+
+cudaError_t launch_hq_mse(const void* src, bool bf16, int64_t rows, int64_t cols,
+                          const unsigned int* amax_slot, double* sums, double threshold,
+                          double* mse, int32_t* choice, unsigned int* status,
+                          cudaStream_t st) {
+  if (rows > 0) {
+    if (bf16)
+      launch_pdl(hq_mse_kernel<true>, dim3(grid1(rows, 8)), dim3(256), 0, st, src, rows,
+                 cols, amax_slot, sums, status);
+    else
+      launch_pdl(hq_mse_kernel<false>, dim3(grid1(rows, 8)), dim3(256), 0, st, src, rows,
+                 cols, amax_slot, sums, status);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  launch_pdl(lqs_finalize_kernel, dim3(1), dim3(32), 0, st, (const double*)sums,
+             rows * cols, threshold, mse, choice);
   return cudaGetLastError();
 }
 

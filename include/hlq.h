@@ -68,7 +68,8 @@ typedef enum {
     HLQ_OP_COMPRESS_ACTIVATION = 0,
     HLQ_OP_BACKWARD_GX = 1,
     HLQ_OP_BACKWARD_GW = 2,
-    HLQ_OP_BACKWARD = 3 /* hlq_linear_backward: both gradients */
+    HLQ_OP_BACKWARD = 3, /* hlq_linear_backward: both gradients */
+    HLQ_OP_SELECT_GRANULARITY = 4 /* hlq_select_gy_granularity */
 } hlq_op;
 
 /* Device status flags (hlq_read_device_status). */
@@ -239,6 +240,28 @@ hlq_status hlq_debug_tc_gemm(int kind, const void *d_a, int64_t lda,
                              int64_t K, int bn, int splits, int32_t *d_acc,
                              void *d_ws, size_t ws_bytes, void *stream);
 size_t hlq_debug_tc_gemm_ws_bytes(int64_t M, int64_t N);
+
+/*
+ * Layer-wise quantizer selection for the HQ of g_y (HOT summary page,
+ * Approach: per-token or per-tensor quantizer chosen per layer; Limitations:
+ * chosen on a calibration set with a 50 % MSE-difference threshold).  On a
+ * calibration sample d_gy [T, Cout] (dtype dt): Y = the 16-point Hadamard
+ * transform along Cout as in hlq_linear_backward_gx, quantized to int4 with
+ * round-to-nearest-even codes at both granularities,
+ *   d_mse[0] = mean over all T*Cout elements of (q*s - Y)^2, per tensor,
+ *   d_mse[1] = the same per token (fp64, each difference exact),
+ *   *d_choice = HLQ_PER_TOKEN if d_mse[0] > threshold * d_mse[1] else
+ *               HLQ_PER_TENSOR  (threshold 1.5 reads "50 %").
+ * d_mse: 2 doubles (8-byte aligned), d_choice: 1 int32, both device memory.
+ * Workspace: hlq_workspace_bytes(HLQ_OP_SELECT_GRANULARITY, ...).  The sums
+ * are accumulated with atomics, so the last bits of d_mse may differ
+ * between runs; the choice differs only within that rounding of the
+ * threshold.
+ */
+hlq_status hlq_select_gy_granularity(const void *d_gy, int dt, int64_t T,
+                                     int64_t Cout, int block, double threshold,
+                                     double *d_mse, int32_t *d_choice, void *d_ws,
+                                     size_t ws_bytes, void *stream);
 
 /*
  * One layer step from HOST buffers, every host<->device copy inside the
