@@ -167,6 +167,25 @@ def test_step_host_validation_and_workspace(L):
     assert call(bits=5) == 1
 
 
+def test_select_granularity_validation(L):
+    f = L.hlq_select_gy_granularity
+    assert L.hlq_workspace_bytes(4, 256, 16, 128, 16, 8) == 256
+
+    def call(gy=FAKE, T=256, Cout=128, block=16, thr=1.5, mse=FAKE, ch=FAKE,
+             ws=FAKE_WS, ws_bytes=256):
+        return f(gy, 1, T, Cout, block, thr, mse, ch, ws, ws_bytes, None)
+
+    assert call(mse=None) == 1
+    assert call(ch=None) == 1
+    assert call(thr=-1.0) == 1
+    assert call(thr=float("nan")) == 1
+    assert call(T=20) == 2
+    assert call(mse=FAKE + 4) == 3
+    assert call(gy=FAKE + 2) == 3
+    assert call(ws_bytes=128) == 5
+    assert call(block=8) == 1
+
+
 def test_read_status_rejects_null(L):
     assert L.hlq_read_device_status(None, 0, None) == 1
 
