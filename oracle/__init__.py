@@ -32,6 +32,7 @@ _lib = None
 PER_TENSOR, PER_TOKEN = 0, 1
 RNE, SR = 0, 1
 STREAM_GY, STREAM_W = 0, 1
+STREAM_GY_T, STREAM_X_T = 2, 3        # the along-tokens HQ of the g_w ablation
 
 
 def build(force: bool = False) -> str:
@@ -311,6 +312,28 @@ def lqs_select(g_y, threshold: float = 1.5):
     m_token = hq_mse(Y, PER_TOKEN)
     choice = PER_TOKEN if m_tensor > threshold * m_token else PER_TENSOR
     return choice, m_tensor, m_token
+
+
+def gw_hq_path(g_y, x, rnd=SR, seed=0, rows=None):
+    """Ablation of the weight-gradient path (HOT summary page, ablation
+    table: "Hadamard transformation with 4-bit quantization on the
+    weight-gradient path" in place of HLA + int8): g_y and x are both
+    transformed along tokens in blocks of 16 (the g_w contraction dim),
+    quantized to int4 per tensor (SR on Philox streams 2 and 3, element
+    index t*C + c of the transformed [T, C] tensor), and
+    g_w = (1/16) acc * s_g * s_x with acc = qGᵀ qX exact over T.
+    Returns qG [Cout, T], s_g, qX [Cin, T], s_x, acc, g_w (``rows``: output
+    channels to compute)."""
+    Yg = hq_transform(g_y, axis=1)                   # along tokens
+    qg, s_g = hq_quantize(Yg, PER_TENSOR, rnd, seed, STREAM_GY_T)
+    Yx = hq_transform(x, axis=1)
+    qx, s_x = hq_quantize(Yx, PER_TENSOR, rnd, seed, STREAM_X_T)
+    qG = np.ascontiguousarray(qg.T)                  # [Cout, T]
+    qX = np.ascontiguousarray(qx.T)                  # [Cin, T]
+    sel = np.arange(qG.shape[0]) if rows is None else np.asarray(rows)
+    acc = gemm_i64(qG[sel], qX)
+    g_w = dequant_gw(acc, s_g[0], s_x[0])
+    return dict(qG=qG, s_g=s_g, qX=qX, s_x=s_x, acc=acc, g_w=g_w, rows=sel)
 
 
 def compress_activation(x, rank=8, bits=8):

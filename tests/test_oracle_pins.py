@@ -352,6 +352,32 @@ def test_lqs_mse_bounds_and_known_choices():
     assert mt == mk == 0.0 and choice == oracle.PER_TENSOR
 
 
+def test_gw_hq_ablation_transform_orientation_and_lossless_case():
+    """The along-tokens HQ of the g_w ablation: with quantization off,
+    (1/16) (H g_y)^T (H x) over 16-token blocks equals g_y^T x (Hadamard
+    orthogonality along the contraction dim); and with block-constant
+    inputs on a 2^-4 grid (coefficient 0 = 16 v, all others 0, amax 7, s = 1)
+    the int4 path is lossless."""
+    rng = np.random.default_rng(41)
+    T, Cin, Cout = 64, 24, 40
+    gy = rng.standard_normal((T, Cout))
+    x = rng.standard_normal((T, Cin))
+    Yg = oracle.hq_transform_f64(gy, axis=1)
+    Yx = oracle.hq_transform_f64(x, axis=1)
+    assert np.allclose(Yg.T @ Yx / 16.0, gy.T @ x, rtol=1e-12, atol=1e-12)
+    kg = np.repeat(rng.integers(-7, 8, (T // 16, Cout)), 16, 0)
+    kx = np.repeat(rng.integers(-7, 8, (T // 16, Cin)), 16, 0)
+    kg[:16, 0] = 7
+    kx[:16, 0] = -7
+    g32 = (kg * 2.0 ** -4).astype(np.float32)
+    x32 = (kx * 2.0 ** -4).astype(np.float32)
+    for rnd in (oracle.RNE, oracle.SR):
+        r = oracle.gw_hq_path(g32, x32, rnd=rnd, seed=9)
+        assert r["s_g"][0] == 1.0 and r["s_x"][0] == 1.0
+        want = g32.astype(np.float64).T @ x32.astype(np.float64)
+        assert np.allclose(r["g_w"], want, rtol=1e-12, atol=1e-15)
+
+
 def test_clamp_when_scale_rounds_down():
     # amax/7 rounded to fp32 can be below the true quotient, so amax/s > 7
     for amax in np.float32([1.0, 3.0, 5.0, 0.1, 1e-3, 123.456]):
