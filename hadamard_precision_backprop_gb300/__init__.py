@@ -24,7 +24,7 @@ PER_TENSOR, PER_TOKEN = 0, 1
 RNE, SR = 0, 1
 F32, BF16 = 0, 1
 OP_COMPRESS_ACTIVATION, OP_BACKWARD_GX, OP_BACKWARD_GW, OP_BACKWARD = 0, 1, 2, 3
-OP_SELECT_GRANULARITY = 4
+OP_SELECT_GRANULARITY, OP_ABLATION_GW_HQ = 4, 5
 DEV_NONFINITE, DEV_TIMEOUT, DEV_BADCODE = 0x1, 0x2, 0x4
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -42,6 +42,7 @@ EXPORTS = [
     "hlq_layer_step_host",
     "hlq_layer_step_host_workspace_bytes",
     "hlq_select_gy_granularity",
+    "hlq_ablation_gw_hq",
 ]
 
 _lock = threading.Lock()
@@ -104,6 +105,8 @@ def lib() -> ctypes.CDLL:
             "hlq_layer_step_host_workspace_bytes": (sz, [i32, i64, i64, i64, i32, i32]),
             "hlq_select_gy_granularity": (i32, [P, i32, i64, i64, i32, ctypes.c_double,
                                                 P, P, P, sz, P]),
+            "hlq_ablation_gw_hq": (i32, [P, P, i32, i64, i64, i64, i32, i32, u64, P, P, P,
+                                         sz, P]),
             "hlq_trace_end": (i32, [P]),
             "hlq_trace_get": (i32, [i32, P, P]),
             "hlq_trace_free": (i32, []),
@@ -353,6 +356,26 @@ def hlq_select_gy_granularity(g_y, threshold: float = 1.5, block: int = 16,
         _ptr(g_y), _dtype_code(g_y), T, Cout, block, float(threshold), _ptr(mse),
         _ptr(choice), _ptr(ws), ws.numel(), _stream(stream)), "hlq_select_gy_granularity")
     return mse, choice
+
+
+def hlq_ablation_gw_hq(g_y, x, rnd: int = SR, seed: int = 0, block: int = 16,
+                       with_acc: bool = False, stream=None):
+    """g_w [Cout, Cin] through HQ along tokens (the ablation of the g_w path);
+    with_acc also returns the int32 accumulator."""
+    torch = _torch()
+    _need_cuda_contig(g_y, x)
+    T, Cout = g_y.shape
+    Cin = x.shape[1]
+    if x.shape[0] != T or x.dtype != g_y.dtype:
+        raise ValueError("shape/dtype mismatch between g_y and x")
+    gw = torch.empty((Cout, Cin), dtype=torch.float32, device=g_y.device)
+    acc = (torch.empty((Cout, Cin), dtype=torch.int32, device=g_y.device)
+           if with_acc else None)
+    ws = workspace(OP_ABLATION_GW_HQ, T, Cin, Cout, block, 8, g_y.device)
+    _check(lib().hlq_ablation_gw_hq(
+        _ptr(g_y), _ptr(x), _dtype_code(g_y), T, Cin, Cout, block, rnd, seed, _ptr(gw),
+        _ptr(acc), _ptr(ws), ws.numel(), _stream(stream)), "hlq_ablation_gw_hq")
+    return (gw, acc) if with_acc else gw
 
 
 def hlq_debug_gx_parts(g_y, w, gran_gy=PER_TOKEN, gran_w=PER_TENSOR, rnd=SR,

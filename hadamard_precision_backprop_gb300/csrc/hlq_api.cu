@@ -484,6 +484,9 @@ size_t hlq_workspace_bytes(int op, int64_t T, int64_t Cin, int64_t Cout,
              gw_layout(T, Cin, Cout, rank_ok(rank) ? rank : 16).total;
     case HLQ_OP_SELECT_GRANULARITY:
       return kAlign;  // amax slot at 0, two fp64 sums at 16
+    case HLQ_OP_ABLATION_GW_HQ:
+      // amax slots, the two scales, codes [Cout, T] and [Cin, T]
+      return 2 * kAlign + align_up((size_t)Cout * (size_t)T) + align_up((size_t)Cin * (size_t)T);
     default:
       return 0;
   }
@@ -595,6 +598,59 @@ hlq_status hlq_select_gy_granularity(const void* d_gy, int dt, int64_t T, int64_
   HLQ_LAUNCH("hq_mse", s,
              launch_hq_mse(d_gy, bf16, T, Cout, amax, sums, threshold, d_mse, d_choice,
                            status, s));
+  return HLQ_OK;
+}
+
+hlq_status hlq_ablation_gw_hq(const void* d_gy, const void* d_x, int dt, int64_t T,
+                              int64_t Cin, int64_t Cout, int block, int rnd, uint64_t seed,
+                              float* d_gw, int32_t* d_acc, void* d_ws, size_t ws_bytes,
+                              void* stream) {
+  hlq_status st = check_common(dt, T, Cin, Cout, block);
+  if (st != HLQ_OK) return st;
+  if (rnd != HLQ_RNE && rnd != HLQ_SR) return HLQ_ERR_INVALID_ARG;
+  if ((T * Cout > 0 && !d_gy) || (T * Cin > 0 && !d_x) || (Cout * Cin > 0 && !d_gw))
+    return HLQ_ERR_INVALID_ARG;
+  if (!aligned16(d_gy) || !aligned16(d_x) || !aligned16(d_gw) || !aligned16(d_acc))
+    return HLQ_ERR_ALIGN;
+  if (49 * T >= ((int64_t)1 << 24)) return HLQ_ERR_OVERFLOW;
+  const size_t need = hlq_workspace_bytes(HLQ_OP_ABLATION_GW_HQ, T, Cin, Cout, block, 8);
+  if (!d_ws || ws_bytes < need) return HLQ_ERR_WORKSPACE;
+  if (!aligned256(d_ws)) return HLQ_ERR_ALIGN;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (Cout * Cin == 0) return HLQ_OK;
+  if (T == 0) {  // empty contraction
+    HLQ_TRY(cudaMemsetAsync(d_gw, 0, (size_t)(Cout * Cin) * 4, s));
+    if (d_acc) HLQ_TRY(cudaMemsetAsync(d_acc, 0, (size_t)(Cout * Cin) * 4, s));
+    return HLQ_OK;
+  }
+  unsigned int* status = device_status_ptr();
+  if (!status) return HLQ_ERR_CUDA;
+  uint8_t* base = static_cast<uint8_t*>(d_ws);
+  unsigned int* amax = reinterpret_cast<unsigned int*>(base);      // [0] g_y, [1] x
+  float* sg = reinterpret_cast<float*>(base + kAlign);
+  float* sx = sg + 4;
+  uint8_t* qg = base + 2 * kAlign;                                 // [Cout, T]
+  uint8_t* qx = qg + align_up((size_t)Cout * (size_t)T);           // [Cin, T]
+  const bool bf16 = dt == HLQ_BF16;
+  HLQ_TRY(cudaMemsetAsync(amax, 0, 8, s));
+  HLQ_LAUNCH("hq_tok_gy_amax", s,
+             launch_hq_cols(d_gy, bf16, T, Cout, true, amax, nullptr, nullptr, rnd, seed, 2,
+                            status, s));
+  HLQ_LAUNCH("hq_tok_gy_quant", s,
+             launch_hq_cols(d_gy, bf16, T, Cout, false, amax, qg, sg, rnd, seed, 2, status,
+                            s));
+  HLQ_LAUNCH("hq_tok_x_amax", s,
+             launch_hq_cols(d_x, bf16, T, Cin, true, amax + 1, nullptr, nullptr, rnd, seed, 3,
+                            status, s));
+  HLQ_LAUNCH("hq_tok_x_quant", s,
+             launch_hq_cols(d_x, bf16, T, Cin, false, amax + 1, qx, sx, rnd, seed, 3, status,
+                            s));
+  const int sms = device_sm_count();
+  if (sms <= 0) return HLQ_ERR_CUDA;
+  const GemmPlan plan = plan_gemm_tc(0, Cout, Cin, T, sms, 1);
+  HLQ_LAUNCH("gemm_gw_hq_tc", s,
+             launch_gemm_tc(0, qg, T, qx, T, Cout, Cin, T, plan, sg, false, sx, d_gw, d_acc,
+                            nullptr, status, s));
   return HLQ_OK;
 }
 

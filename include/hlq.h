@@ -69,7 +69,8 @@ typedef enum {
     HLQ_OP_BACKWARD_GX = 1,
     HLQ_OP_BACKWARD_GW = 2,
     HLQ_OP_BACKWARD = 3, /* hlq_linear_backward: both gradients */
-    HLQ_OP_SELECT_GRANULARITY = 4 /* hlq_select_gy_granularity */
+    HLQ_OP_SELECT_GRANULARITY = 4, /* hlq_select_gy_granularity */
+    HLQ_OP_ABLATION_GW_HQ = 5      /* hlq_ablation_gw_hq */
 } hlq_op;
 
 /* Device status flags (hlq_read_device_status). */
@@ -262,6 +263,24 @@ hlq_status hlq_select_gy_granularity(const void *d_gy, int dt, int64_t T,
                                      int64_t Cout, int block, double threshold,
                                      double *d_mse, int32_t *d_choice, void *d_ws,
                                      size_t ws_bytes, void *stream);
+
+/*
+ * Ablation of the weight-gradient path, for numerical-error studies (HOT
+ * summary page, ablation table: "Hadamard transformation with 4-bit
+ * quantization on the weight-gradient path" in place of HLA + int8): g_y and
+ * x are both transformed along tokens in blocks of 16 (the contraction dim
+ * of g_w), quantized to int4 per tensor exactly as the HQ of w in
+ * hlq_linear_backward_gx (SR on Philox streams 2 for g_y and 3 for x, element
+ * e = t*C + c of the transformed [T, C] tensor), and
+ *   acc[o, i] = sum_t qG[t, o] qX[t, i]  (exact),  g_w = acc * s_g * s_x / 16.
+ * d_gy [T, Cout], d_x [T, Cin] (dtype dt) -> d_gw [Cout, Cin] fp32; d_acc
+ * [Cout, Cin] int32 may be NULL (else it receives acc).  Needs 49 * T < 2^24.
+ * Workspace: hlq_workspace_bytes(HLQ_OP_ABLATION_GW_HQ, ...).
+ */
+hlq_status hlq_ablation_gw_hq(const void *d_gy, const void *d_x, int dt, int64_t T,
+                              int64_t Cin, int64_t Cout, int block, int rnd,
+                              uint64_t seed, float *d_gw, int32_t *d_acc, void *d_ws,
+                              size_t ws_bytes, void *stream);
 
 /*
  * One layer step from HOST buffers, every host<->device copy inside the

@@ -186,6 +186,22 @@ def test_select_granularity_validation(L):
     assert call(block=8) == 1
 
 
+def test_ablation_gw_hq_validation(L):
+    f = L.hlq_ablation_gw_hq
+
+    def call(gy=FAKE, x=FAKE, T=256, rnd=1, gw=FAKE, ws=FAKE_WS, ws_bytes=1 << 30):
+        return f(gy, x, 1, T, 64, 128, 16, rnd, 0, gw, None, ws, ws_bytes, None)
+
+    need = L.hlq_workspace_bytes(5, 256, 64, 128, 16, 8)
+    assert need == 512 + 128 * 256 + 64 * 256
+    assert call(x=None) == 1
+    assert call(rnd=3) == 1
+    assert call(T=40) == 2
+    assert call(gw=FAKE + 8) == 3
+    assert call(T=342400) == 6                 # 49 * T >= 2^24
+    assert call(ws_bytes=need - 256) == 5
+
+
 def test_read_status_rejects_null(L):
     assert L.hlq_read_device_status(None, 0, None) == 1
 
