@@ -416,7 +416,9 @@ __device__ __forceinline__ void pack_code(uint32_t* p, int k, float q) {
     p[k >> 2] |= ((uint32_t)(int)q & 0xffu) << (8 * (k & 3));
 }
 
-// Store `n` bytes (1, 2, 4, 8, 16 or 32) of packed codes.
+// Store `n` bytes (1, 2, 4, 8, 16 or 32) of packed codes; dst is aligned to
+// min(n, 16) bytes.  Every width is one typed store: a byte-by-byte copy of
+// the 2-byte case (rank-1 bf16 codes) wrote wrong low bytes.
 __device__ __forceinline__ void store_chunk(uint8_t* dst, const uint32_t* p, int n) {
   if (n >= 16) {
     *reinterpret_cast<uint4*>(dst) = make_uint4(p[0], p[1], p[2], p[3]);
@@ -425,8 +427,10 @@ __device__ __forceinline__ void store_chunk(uint8_t* dst, const uint32_t* p, int
     *reinterpret_cast<uint2*>(dst) = make_uint2(p[0], p[1]);
   } else if (n == 4) {
     *reinterpret_cast<uint32_t*>(dst) = p[0];
+  } else if (n == 2) {
+    *reinterpret_cast<uint16_t*>(dst) = (uint16_t)(p[0] & 0xffffu);
   } else {
-    for (int i = 0; i < n; ++i) dst[i] = (uint8_t)(p[i >> 2] >> (8 * (i & 3)));
+    *dst = (uint8_t)(p[0] & 0xffu);
   }
 }
 

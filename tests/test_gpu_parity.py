@@ -131,7 +131,7 @@ def test_paths_ragged_shapes(T, Cin, Cout, dtype):
                                 gy_scale=1e-3, w_scale=0.02)
     for gran in (workloads.PER_TOKEN, workloads.PER_TENSOR):
         check_gx(inp, dtype, gran, oracle.SR, seed=T * 7 + 1)
-    for rank in (8, 4, 16):
+    for rank in (1, 2, 4, 8, 16):
         check_gw(inp, dtype, rank)
 
 
