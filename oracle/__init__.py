@@ -79,6 +79,7 @@ def _load():
                 "orc_dequant_gx": (None, [P, P, i32, ctypes.c_float, i64, i64, P]),
                 "orc_dequant_gw": (None, [P, ctypes.c_float, ctypes.c_float,
                                           i64, i64, P]),
+                "orc_dequant_gw_cols": (None, [P, ctypes.c_float, P, i64, i64, P]),
             }
             for name, (res, args) in sig.items():
                 f = getattr(lib, name)
@@ -257,10 +258,18 @@ def dequant_gx(acc, s_gy, gran_gy: int, s_w) -> np.ndarray:
 
 
 def dequant_gw(acc, s_g, s_x) -> np.ndarray:
+    """g_w = acc * s_g * s_x / 16; s_x a scalar (per tensor) or one scale per
+    input channel (column of g_w)."""
     acc = np.ascontiguousarray(acc, dtype=np.int64)
     Cout, Cin = acc.shape
     out = np.empty((Cout, Cin), dtype=np.float64)
-    _load().orc_dequant_gw(_p(acc), float(s_g), float(s_x), Cout, Cin, _p(out))
+    if np.size(s_x) == 1 and Cin != 1:
+        sx0 = float(np.asarray(s_x, dtype=np.float32).reshape(-1)[0])
+        _load().orc_dequant_gw(_p(acc), float(s_g), sx0, Cout, Cin, _p(out))
+    else:
+        sx = _f32(s_x).reshape(-1)
+        assert sx.size == Cin
+        _load().orc_dequant_gw_cols(_p(acc), float(s_g), _p(sx), Cout, Cin, _p(out))
     return out
 
 
@@ -336,19 +345,34 @@ def gw_hq_path(g_y, x, rnd=SR, seed=0, rows=None):
     return dict(qG=qG, s_g=s_g, qX=qX, s_x=s_x, acc=acc, g_w=g_w, rows=sel)
 
 
-def compress_activation(x, rank=8, bits=8):
+def compress_activation(x, rank=8, bits=8, per_channel=False):
     """ACBP at forward time: x [T, Cin] -> codes [Cin, T*rank/16] (int8
     values: [-127, 127] for bits=8, [-7, 7] for bits=4; pack_int4 gives the
-    stored nibbles of the latter) and the per-tensor scale."""
+    stored nibbles of the latter) and the per-tensor scale.
+
+    per_channel: one scale per input channel instead (a row of the code
+    matrix; the reading of "per-token vs per-tensor" granularity carried to
+    the stored activation, whose token dim is the g_w contraction dim, so
+    only a per-channel scale factors out of the integer GEMM).  Each row is
+    quantized on its own with the same RNE rule; returns an fp32 array
+    [Cin] of scales."""
     Xb = hla_transform(x, rank)
-    q, s = rne_quantize(Xb, 127 if bits == 8 else 7)
+    qmax = 127 if bits == 8 else 7
+    if not per_channel:
+        return rne_quantize(Xb, qmax)
+    q = np.empty(Xb.shape, dtype=np.int8)
+    s = np.empty(Xb.shape[0], dtype=np.float32)
+    for c in range(Xb.shape[0]):
+        q[c], s[c] = rne_quantize(Xb[c], qmax)
     return q, s
 
 
 def gw_path(g_y, xbar_codes, s_x, rank=8, rows=None):
     """Weight-gradient path g_w = (1/16) gbar_y^T xbar with HLA + int8.
 
-    g_y [T, Cout]; xbar_codes [Cin, T'] int8; s_x fp32.  Returns qG
+    g_y [T, Cout]; xbar_codes [Cin, T'] int8; s_x fp32 (a scalar, or one
+    scale per input channel from compress_activation(per_channel=True)).
+    Returns qG
     [Cout, T'] int8, s_g, acc [Cout, Cin] int64 and g_w [Cout, Cin] fp64
     (``rows`` restricts acc/g_w to those output channels)."""
     Gb = hla_transform(g_y, rank)

@@ -591,3 +591,16 @@ void orc_dequant_gw(const int64_t *acc, float s_g, float s_x, int64_t Cout,
             g_w[o * Cin + i] = (double)acc[o * Cin + i] * (double)s_g *
                                (double)s_x / 16.0;
 }
+
+/* Per-channel scales of the stored activation: g_w[o, i] = acc[o, i] * s_g *
+ * s_x[i] / 16 (fp64).  A scale per input channel i is a scale per column of
+ * g_w, so it factors out of the contraction over tokens exactly like the
+ * per-tensor one. */
+void orc_dequant_gw_cols(const int64_t *acc, float s_g, const float *s_x,
+                         int64_t Cout, int64_t Cin, double *g_w)
+{
+    for (int64_t o = 0; o < Cout; ++o)
+        for (int64_t i = 0; i < Cin; ++i)
+            g_w[o * Cin + i] = (double)acc[o * Cin + i] * (double)s_g *
+                               (double)s_x[i] / 16.0;
+}

@@ -529,3 +529,87 @@ def test_gw_path_lossless_equals_gyT_x():
     assert np.array_equal(r["qG"].astype(np.float64) * r["s_g"], r["Gb"])
     want = gy.astype(np.float64).T @ x.astype(np.float64)
     assert np.allclose(r["g_w"], want, rtol=1e-12, atol=1e-15)
+
+
+# ----------------------------------------- per-channel scales of the ACBP
+
+def _per_channel_lossless_x(rng, T, Cin, exps):
+    """x whose HLA (rank 8) coefficients in channel c are integer multiples
+    of 2^(e_c - 1) with maximum exactly 127 * 2^(e_c - 1): token pairs equal
+    (only the kept even Sylvester rows are non-zero) and a spike block."""
+    x = np.repeat(rng.integers(-3, 4, (T // 2, Cin)), 2, 0).astype(np.float64)
+    x[:16, :] = 127 / 16.0 * 2
+    return (x * 2.0 ** (np.asarray(exps, dtype=np.float64)[None, :] - 2)).astype(np.float32)
+
+
+def test_per_channel_acbp_lossless_gw_with_outlier_channels():
+    """Channels of very different magnitude (outlier channels 2^6 larger):
+    one scale per channel keeps every channel on its own code grid, so the
+    stored activation is lossless and g_w equals g_y^T x; one scale for the
+    whole tensor is not (the small channels lose their low bits).  Cin !=
+    Cout, so a scale applied along the wrong axis of g_w fails."""
+    rng = np.random.default_rng(23)
+    T, Cin, Cout = 64, 20, 24
+    exps = np.zeros(Cin, dtype=np.int64)
+    exps[[3, 11]] = 6
+    exps[[5, 17]] = -3
+    x = _per_channel_lossless_x(rng, T, Cin, exps)
+    gy = np.repeat(rng.integers(-3, 4, (T // 2, Cout)), 2, 0).astype(np.float64)
+    gy[:16, 0] = 127 / 16.0 * 2
+    gy = (gy * 2.0 ** -7).astype(np.float32)
+    q, s = oracle.compress_activation(x, 8, per_channel=True)
+    assert s.shape == (Cin,)
+    assert np.array_equal(s.astype(np.float64), 2.0 ** (exps - 1.0))
+    Xb = oracle.hla_transform(x, 8)
+    assert np.array_equal(q.astype(np.float64) * s.astype(np.float64)[:, None], Xb)
+    want = gy.astype(np.float64).T @ x.astype(np.float64)
+    r = oracle.gw_path(gy, q, s, 8)
+    assert np.allclose(r["g_w"], want, rtol=1e-12, atol=1e-15)
+    qt, st = oracle.compress_activation(x, 8)
+    rt = oracle.gw_path(gy, qt, st, 8)
+    small = exps < 0
+    assert not np.allclose(rt["g_w"][:, small], want[:, small], rtol=1e-6, atol=0)
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+def test_per_channel_equal_maxima_reduce_to_per_tensor(bits):
+    """When every channel's largest coefficient is the same number, the
+    per-channel scales all equal the per-tensor scale and the codes and g_w
+    are those of the per-tensor quantizer, bit for bit."""
+    rng = np.random.default_rng(24)
+    T, Cin, Cout = 64, 32, 16
+    x = rng.standard_normal((T, Cin)).astype(np.float32)
+    x[:16, :] = 40.0          # block 0: DC coefficient 640 in every channel
+    gy = rng.standard_normal((T, Cout)).astype(np.float32)
+    qc, sc = oracle.compress_activation(x, 8, bits=bits, per_channel=True)
+    qt, st = oracle.compress_activation(x, 8, bits=bits)
+    assert np.all(sc == st)
+    assert np.array_equal(qc, qt)
+    rc = oracle.gw_path(gy, qc, sc, 8)
+    rt = oracle.gw_path(gy, qt, st, 8)
+    assert np.array_equal(rc["acc"], rt["acc"])
+    assert np.array_equal(rc["g_w"], rt["g_w"])
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+def test_per_channel_rne_bound_per_row(bits):
+    """Outlier channels (1 % of channels x50): each channel's scale is
+    RN(amax_c / qmax) of its own coefficients, its largest code is +-qmax,
+    and every code is within half a step of its coefficient (own scale),
+    which is never coarser than the per-tensor step."""
+    rng = np.random.default_rng(25)
+    T, Cin = 128, 200
+    x = rng.standard_normal((T, Cin))
+    x[:, rng.choice(Cin, 2, replace=False)] *= 50.0
+    x = x.astype(np.float32)
+    qmax = 127 if bits == 8 else 7
+    q, s = oracle.compress_activation(x, 8, bits=bits, per_channel=True)
+    _, st = oracle.compress_activation(x, 8, bits=bits)
+    Xb = oracle.hla_transform(x, 8).astype(np.float64)
+    amax_c = np.max(np.abs(Xb), axis=1)
+    assert np.array_equal(s, (amax_c / qmax).astype(np.float32))
+    assert np.all(np.max(np.abs(q.astype(np.int64)), axis=1) == qmax)
+    err = np.abs(q.astype(np.float64) * s.astype(np.float64)[:, None] - Xb)
+    ulp = np.spacing(amax_c.astype(np.float32)).astype(np.float64)
+    assert np.all(err <= s.astype(np.float64)[:, None] / 2 + ulp[:, None])
+    assert np.all(s <= st)
