@@ -86,23 +86,38 @@ size_t hlq_workspace_bytes(int op, int64_t T, int64_t Cin, int64_t Cout,
                            int block, int rank);
 
 /*
+ * Format word of the stored activation (xbar_fmt): the code width, 8 or 4,
+ * optionally OR'ed with HLQ_XBAR_PER_CHANNEL for one scale per input
+ * channel (d_xbar_scale [Cin]) instead of one per tensor (d_xbar_scale [1]).
+ * The per-channel scale is the per-layer granularity choice of HOT
+ * (Approach) carried to the stored activation: its token dim is the g_w
+ * contraction dim, so the scale that still factors out of the integer GEMM
+ * is one per channel, i.e. per column of g_w.
+ */
+#define HLQ_XBAR_INT8 8
+#define HLQ_XBAR_INT4 4
+#define HLQ_XBAR_PER_CHANNEL 0x100
+
+/*
  * ACBP at forward time (HOT, Approach: stored activations compressed when
- * the forward pass runs; HLQ TL;DR: "activation-compression", "int4
- * activation-compression strategy").
+ * the forward pass runs; HLQ TL;DR: int4 activation compression, ACBP).
  * x [T, Cin] (dtype dt) -> d_xbar codes (token dim contiguous) and
- * d_xbar_scale [1] fp32:
+ * d_xbar_scale fp32 ([1], or [Cin] with HLQ_XBAR_PER_CHANNEL):
  *   Xbar[c, rank*b + k] = RN_f32( sum_j H16[sigma(k)][j] x[16b + j, c] )
  *   s = RN_f32(max|Xbar| / qmax),  code = clamp(rne(RN_f32(Xbar / s)), +-qmax)
  * where sigma(k) is the Sylvester row of sequency k (the rank lowest-
- * sequency Walsh rows are kept).  s == 0 gives all-zero codes.
- * xbar_bits 8: qmax 127, d_xbar [Cin, T'] int8 codes.
- * xbar_bits 4: qmax 7, d_xbar [Cin, T'/2] bytes, two's-complement int4 codes
+ * sequency Walsh rows are kept) and the max runs over the tensor, or over
+ * row c of Xbar for the scale s_c of channel c.  s == 0 gives all-zero codes.
+ * Code width 8: qmax 127, d_xbar [Cin, T'] int8 codes.
+ * Code width 4: qmax 7, d_xbar [Cin, T'/2] bytes, two's-complement int4 codes
  *   packed two per byte (code 2k in the low nibble, 2k+1 in the high one);
  *   even ranks only (HLQ_ERR_UNSUPPORTED for rank 1).
- * Other xbar_bits: HLQ_ERR_INVALID_ARG.
+ * Another width or unknown flag bits: HLQ_ERR_INVALID_ARG.
+ * Workspace: hlq_workspace_bytes(HLQ_OP_COMPRESS_ACTIVATION, ...), which
+ * grows with Cin (one amax slot per channel).
  */
 hlq_status hlq_compress_activation(const void *d_x, int dt, int64_t T,
-                                   int64_t Cin, int block, int rank, int xbar_bits,
+                                   int64_t Cin, int block, int rank, int xbar_fmt,
                                    int8_t *d_xbar, float *d_xbar_scale,
                                    void *d_ws, size_t ws_bytes, void *stream);
 
@@ -134,15 +149,16 @@ hlq_status hlq_linear_backward_gx(const void *d_gy, const void *d_w, int dt,
  *   gbar_y = HLA of g_y along tokens as in hlq_compress_activation,
  *   s_g = RN(amax/127) per tensor, int8 codes by round-to-nearest-even,
  *   acc[o, i] = sum_t' qG[o, t'] qX[i, t']  (exact integer),
- *   g_w[o, i] = acc * s_g * s_x / 16   (fp32).
+ *   g_w[o, i] = acc * s_g * s_x / 16   (fp32),
+ * s_x the tensor scale, or s_x[i] with HLQ_XBAR_PER_CHANNEL in xbar_fmt.
  * d_xbar / d_xbar_scale come from hlq_compress_activation with the same T,
- * Cin, rank and xbar_bits (the qX codes are then in [-127, 127] or [-7, 7]).
+ * Cin, rank and xbar_fmt (the qX codes are then in [-127, 127] or [-7, 7]).
  * Needs T' * 127 * qmax_x < 2^31.
  */
 hlq_status hlq_linear_backward_gw(const void *d_gy, int dt, const int8_t *d_xbar,
                                   const float *d_xbar_scale, int64_t T,
                                   int64_t Cin, int64_t Cout, int block,
-                                  int rank, int xbar_bits, float *d_gw, void *d_ws,
+                                  int rank, int xbar_fmt, float *d_gw, void *d_ws,
                                   size_t ws_bytes, void *stream);
 
 /*
@@ -158,7 +174,7 @@ hlq_status hlq_linear_backward_gw(const void *d_gy, int dt, const int8_t *d_xbar
 hlq_status hlq_linear_backward(const void *d_gy, const void *d_w, const int8_t *d_xbar,
                                const float *d_xbar_scale, int dt, int64_t T,
                                int64_t Cin, int64_t Cout, int block, int rank,
-                               int xbar_bits, int gran_gy, int gran_w, int rnd, uint64_t seed,
+                               int xbar_fmt, int gran_gy, int gran_w, int rnd, uint64_t seed,
                                float *d_gx, float *d_gw, void *d_ws, size_t ws_bytes,
                                void *stream);
 
@@ -184,7 +200,7 @@ hlq_status hlq_debug_gx_parts(const void *d_gy, const void *d_w, int dt,
  */
 hlq_status hlq_debug_gw_parts(const void *d_gy, int dt, const int8_t *d_xbar,
                               const float *d_xbar_scale, int64_t T, int64_t Cin,
-                              int64_t Cout, int block, int rank, int xbar_bits,
+                              int64_t Cout, int block, int rank, int xbar_fmt,
                               float *d_gw, void *d_ws, size_t ws_bytes, int8_t *d_qg,
                               float *d_sg, int32_t *d_acc, void *stream);
 
@@ -266,8 +282,11 @@ hlq_status hlq_select_gy_granularity(const void *d_gy, int dt, int64_t T,
 
 /*
  * Ablation of the weight-gradient path, for numerical-error studies (HOT
- * summary page, ablation table: "Hadamard transformation with 4-bit
- * quantization on the weight-gradient path" in place of HLA + int8): g_y and
+ * summary page, ablation table: Hadamard-transformed 4-bit quantization on
+ * one gradient path; as printed the table names the two paths the other way
+ * round from the method's own assignment of HQ to g_x and HLA to g_w, so its
+ * path labels are read as swapped, and this is that row on the weight-
+ * gradient path, in place of HLA + int8): g_y and
  * x are both transformed along tokens in blocks of 16 (the contraction dim
  * of g_w), quantized to int4 per tensor exactly as the HQ of w in
  * hlq_linear_backward_gx (SR on Philox streams 2 for g_y and 3 for x, element
@@ -298,8 +317,8 @@ hlq_status hlq_ablation_gw_hq(const void *d_gy, const void *d_x, int dt, int64_t
  * device entry points on the same inputs.
  *   h_x [T, Cin], h_gy [T, Cout], h_w [Cout, Cin]: host, dtype dt;
  *   h_gx [T, Cin], h_gw [Cout, Cin]: host fp32 outputs;
- *   d_xbar (int8 [Cin, T'] or packed int4 [Cin, T'/2], per xbar_bits as in
- *   hlq_compress_activation) and d_xbar_scale [1]: device, filled by the
+ *   d_xbar (int8 [Cin, T'] or packed int4 [Cin, T'/2], per xbar_fmt as in
+ *   hlq_compress_activation) and d_xbar_scale [1] or [Cin]: device, filled by the
  *   call (the stored activation of the step);
  *   d_ws: device workspace of hlq_layer_step_host_workspace_bytes(...),
  *   which also holds the device copies of the inputs and outputs.
@@ -312,7 +331,7 @@ hlq_status hlq_ablation_gw_hq(const void *d_gy, const void *d_x, int dt, int64_t
  */
 hlq_status hlq_layer_step_host(const void *h_x, const void *h_gy, const void *h_w,
                                int dt, int64_t T, int64_t Cin, int64_t Cout,
-                               int block, int rank, int xbar_bits, int gran_gy,
+                               int block, int rank, int xbar_fmt, int gran_gy,
                                int gran_w, int rnd, uint64_t seed, float *h_gx, float *h_gw,
                                int8_t *d_xbar, float *d_xbar_scale,
                                int64_t chunk_tokens, void *d_ws, size_t ws_bytes,

@@ -325,8 +325,10 @@ def lqs_select(g_y, threshold: float = 1.5):
 
 def gw_hq_path(g_y, x, rnd=SR, seed=0, rows=None):
     """Ablation of the weight-gradient path (HOT summary page, ablation
-    table: "Hadamard transformation with 4-bit quantization on the
-    weight-gradient path" in place of HLA + int8): g_y and x are both
+    table: Hadamard-transformed 4-bit quantization on a gradient path, the
+    table's path labels read as swapped since as printed they contradict the
+    method's assignment of HQ to g_x and HLA to g_w; here on the
+    weight-gradient path in place of HLA + int8): g_y and x are both
     transformed along tokens in blocks of 16 (the g_w contraction dim),
     quantized to int4 per tensor (SR on Philox streams 2 and 3, element
     index t*C + c of the transformed [T, C] tensor), and
@@ -343,6 +345,30 @@ def gw_hq_path(g_y, x, rnd=SR, seed=0, rows=None):
     acc = gemm_i64(qG[sel], qX)
     g_w = dequant_gw(acc, s_g[0], s_x[0])
     return dict(qG=qG, s_g=s_g, qX=qX, s_x=s_x, acc=acc, g_w=g_w, rows=sel)
+
+
+def gx_hla_path(g_y, w, rank=8, rows=None):
+    """Ablation of the activation-gradient path (HOT summary page, ablation
+    table: internal HLA on a gradient path, the table's path labels read as
+    swapped as for gw_hq_path; here on the activation-gradient path, with
+    the int8 quantizer HLA is paired with on the g_w path): the
+    contraction dim of g_x = g_y . w is Cout, so g_y (along its rows) and w
+    (along its first dim) both keep the `rank` lowest-sequency Walsh rows of
+    each 16-block of Cout,
+      Gb[t, r*b + k] = RN_f32(sum_j H16[sigma(k)][j] g_y[t, 16b + j]),
+      Wb[i, r*b + k] = RN_f32(sum_j H16[sigma(k)][j] w[16b + j, i]),
+    per-tensor RNE int8 codes, acc = qG . qW^T exact over Cout*rank/16, and
+    g_x = acc * s_g * s_w / 16.  Returns Gb, qG [T, Cout'], s_g, Wb, qW
+    [Cin, Cout'], s_w, acc [T, Cin], g_x (``rows``: tokens to compute)."""
+    Gb = hla_transform(np.ascontiguousarray(_f32(g_y).T), rank)   # [T, Cout']
+    Wb = hla_transform(w, rank)                                    # [Cin, Cout']
+    qG, s_g = int8_quantize(Gb)
+    qW, s_w = int8_quantize(Wb)
+    sel = np.arange(qG.shape[0]) if rows is None else np.asarray(rows)
+    acc = gemm_i64(qG[sel], qW)
+    g_x = dequant_gx(acc, np.array([s_g], np.float32), PER_TENSOR, s_w)
+    return dict(Gb=Gb, qG=qG, s_g=s_g, Wb=Wb, qW=qW, s_w=s_w, acc=acc, g_x=g_x,
+                rows=sel)
 
 
 def compress_activation(x, rank=8, bits=8, per_channel=False):

@@ -515,7 +515,7 @@ float orc_amax(const float *v, int64_t n)
 /* Round-to-nearest-even quantizer with one scale per tensor:
  * s = RN_f32(amax / qmax), codes clamp(rint(RN_f32(v / s)), -qmax, qmax).
  * qmax = 127 gives the int8 HLA operands; qmax = 7 the int4 form of the
- * stored activation (HLQ TL;DR, "int4 activation-compression strategy"). */
+ * stored activation (HLQ TL;DR: int4 activation compression). */
 int orc_rne_quantize(const float *v, int64_t n, int qmax, int8_t *codes, float *scale)
 {
     if (qmax != 7 && qmax != 127)

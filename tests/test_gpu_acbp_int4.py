@@ -1,5 +1,5 @@
-"""int4 storage of the stored activation (HLQ TL;DR, "int4 activation-
-compression strategy (ACBP)"): the compressed x as two's-complement int4
+"""int4 storage of the stored activation (HLQ TL;DR: int4 activation
+compression, ACBP): the compressed x as two's-complement int4
 codes packed two per byte, then the g_w path reading it.  Codes (as packed
 bytes), scales and integer accumulators bit-exact against the oracle, g_w
 within 1e-5 of the oracle's fp64 dequant; the combined and host-buffer

@@ -613,3 +613,57 @@ def test_per_channel_rne_bound_per_row(bits):
     ulp = np.spacing(amax_c.astype(np.float32)).astype(np.float64)
     assert np.all(err <= s.astype(np.float64)[:, None] / 2 + ulp[:, None])
     assert np.all(s <= st)
+
+
+# ------------------------------------- ablation: HLA on the g_x contraction
+
+@pytest.mark.parametrize("rank", [1, 2, 4, 8])
+def test_gx_hla_ablation_lossless_equals_gy_w(rank):
+    """g_y constant on groups of 16/rank consecutive output channels lies in
+    the span of the rank lowest-sequency Walsh rows, so the low-rank product
+    over Cout is exact; with every kept coefficient on its int8 grid (spike
+    blocks set both maxima to 127 * s) g_x equals g_y . w.  Keeping other
+    Walsh rows (e.g. the first rank rows in Sylvester order) breaks it, and
+    T, Cin, Cout all differ, so a transposed operand fails too."""
+    rng = np.random.default_rng(26)
+    T, Cin, Cout = 48, 40, 64
+    L = 16 // rank
+    gy = np.repeat(rng.integers(-3, 4, (T, Cout // L)), L, 1).astype(np.float64)
+    gy[0, :16] = 127 / 16.0 * 2              # DC coefficient 127 * 2 of block 0
+    w = rng.integers(-3, 4, (Cout, Cin)).astype(np.float64)
+    w[:16, 0] = 127 / 16.0                   # DC coefficient 127
+    gy = (gy * 2.0 ** -7).astype(np.float32)
+    w = (w * 2.0 ** -2).astype(np.float32)
+    r = oracle.gx_hla_path(gy, w, rank)
+    assert r["qG"].shape == (T, Cout // 16 * rank) and r["qW"].shape == (Cin, Cout // 16 * rank)
+    assert np.array_equal(r["qG"].astype(np.float64) * r["s_g"], r["Gb"])
+    assert np.array_equal(r["qW"].astype(np.float64) * r["s_w"], r["Wb"])
+    want = gy.astype(np.float64) @ w.astype(np.float64)
+    assert np.allclose(r["g_x"], want, rtol=1e-12, atol=1e-15)
+    if rank < 16:   # the same data but generic within the groups is not exact
+        gy2 = gy.copy()
+        gy2[:, 1::2] += np.float32(2.0 ** -7)
+        r2 = oracle.gx_hla_path(gy2, w, rank)
+        want2 = gy2.astype(np.float64) @ w.astype(np.float64)
+        assert not np.allclose(r2["g_x"], want2, rtol=1e-9, atol=0)
+
+
+def test_gx_hla_ablation_full_rank_quant_off_is_gy_w():
+    """Rank 16 keeps every Walsh row: the exactly rounded transforms of both
+    operands, multiplied in fp64 and divided by 16, give g_y . w to fp32
+    rounding of the coefficients (H16 H16^T = 16 I)."""
+    rng = np.random.default_rng(27)
+    T, Cin, Cout = 32, 24, 48
+    gy = rng.standard_normal((T, Cout)).astype(np.float32)
+    w = rng.standard_normal((Cout, Cin)).astype(np.float32)
+    r = oracle.gx_hla_path(gy, w, 16)
+    got = r["Gb"].astype(np.float64) @ r["Wb"].astype(np.float64).T / 16.0
+    want = gy.astype(np.float64) @ w.astype(np.float64)
+    assert np.allclose(got, want, rtol=1e-5, atol=1e-5)
+    # and the permutation of the kept rows is the same on both operands:
+    # Sylvester order of g_y's rows against sequency order of w's would not
+    # reproduce the product
+    H = H_SCIPY.astype(np.float64)
+    Gs = (gy.astype(np.float64).reshape(T, Cout // 16, 16) @ H.T).reshape(T, Cout)
+    bad = Gs @ r["Wb"].astype(np.float64).T / 16.0
+    assert not np.allclose(bad, want, rtol=1e-3, atol=1e-3)
