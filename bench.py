@@ -63,6 +63,9 @@ def parse_args():
     p.add_argument("--serial", action="store_true",
                    help="time the g_x and g_w branches one after the other "
                         "instead of concurrently (hlq_linear_backward)")
+    p.add_argument("--no-variants", action="store_true",
+                   help="skip the timings of the optional paths (int4 / "
+                        "per-channel ACBP, quantizer selection, ablations)")
     return p.parse_args()
 
 
@@ -404,6 +407,83 @@ def run_ours(args, wl, rank, world, local_rank):
     torch.cuda.synchronize()
     ms_eager = statistics.mean(a.elapsed_time(b) for a, b in eager)
 
+    # ---- the optional paths, each timed alone on the same inputs ----------
+    # (graph replay, L2 flushed before each replay, mean over the steps)
+    def time_replays(fn):
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            fn()
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        for _ in range(args.warmup):
+            g.replay()
+        ts = []
+        for _ in range(args.steps):
+            flush.fill_(1)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+            ts.append((a, b))
+        torch.cuda.synchronize()
+        return statistics.mean(a.elapsed_time(b) for a, b in ts) * 1e3
+
+    variants = {}
+    if not args.no_variants and world == 1:
+        xb4 = torch.empty(hlq.xbar_shape(T, Cin, wl.rank, 4), dtype=torch.uint8, device=dev)
+        sxc = torch.empty(Cin, dtype=torch.float32, device=dev)
+        mse = torch.empty(2, dtype=torch.float64, device=dev)
+        choice = torch.empty(1, dtype=torch.int32, device=dev)
+        ws_sel = hlq.workspace(hlq.OP_SELECT_GRANULARITY, T, Cin, Cout, 16, 8, dev)
+        ws_agw = hlq.workspace(hlq.OP_ABLATION_GW_HQ, T, Cin, Cout, 16, 8, dev)
+        ws_agx = hlq.workspace(hlq.OP_ABLATION_GX_HLA, T, Cin, Cout, 16, wl.rank, dev)
+        gw_a = torch.empty((Cout, Cin), dtype=torch.float32, device=dev)
+        gx_a = torch.empty((T, Cin), dtype=torch.float32, device=dev)
+
+        def step_int4():
+            hlq.hlq_compress_activation(x, rank=wl.rank, out=xb4, scale=sx, ws=ws0,
+                                        xbar_bits=4)
+            hlq.hlq_linear_backward(gy, w, xb4, sx, rank=wl.rank, gran_gy=wl.gran_gy,
+                                    gran_w=wl.gran_w, rnd=hlq.SR, seed=wl.seed,
+                                    out_gx=gx, out_gw=gw, ws=ws1, xbar_bits=4)
+
+        def step_per_channel():
+            hlq.hlq_compress_activation(x, rank=wl.rank, out=xbar, scale=sxc, ws=ws0,
+                                        xbar_per_channel=True)
+            hlq.hlq_linear_backward(gy, w, xbar, sxc, rank=wl.rank, gran_gy=wl.gran_gy,
+                                    gran_w=wl.gran_w, rnd=hlq.SR, seed=wl.seed,
+                                    out_gx=gx, out_gw=gw, ws=ws1, xbar_per_channel=True)
+
+        def select():
+            hlq.hlq_select_gy_granularity(gy, mse=mse, choice=choice, ws=ws_sel)
+
+        def ablation_gw():
+            hlq.hlq_ablation_gw_hq(gy, x, rnd=hlq.SR, seed=wl.seed, out=gw_a, ws=ws_agw)
+
+        def ablation_gx():
+            hlq.hlq_ablation_gx_hla(gy, w, rank=wl.rank, out=gx_a, ws=ws_agx)
+
+        for name, fn, what in [
+                ("acbp_int4_step", step_int4,
+                 "whole step with the stored activation as packed int4 codes"),
+                ("acbp_per_channel_step", step_per_channel,
+                 "whole step with one scale per input channel of the stored activation"),
+                ("select_gy_granularity", select,
+                 "per-token vs per-tensor choice from the int4 RNE MSE of g_y"),
+                ("ablation_gw_hq", ablation_gw,
+                 "g_w through HQ along tokens and an int4 GEMM over T"),
+                ("ablation_gx_hla", ablation_gx,
+                 "g_x through HLA along Cout and an int8 GEMM over Cout*rank/16")]:
+            try:
+                variants[name] = {"us": time_replays(fn), "what": what}
+            except Exception as exc:  # report, do not fail the main line
+                variants[name] = {"us": None, "error": f"{type(exc).__name__}: {exc}"}
+        torch.cuda.synchronize()
+
     # ---- end to end through host buffers ---------------------------------
     # libhlq's host-buffer entry: pinned inputs in, gradients back out, the
     # copies pipelined with the kernels inside the call
@@ -493,6 +573,7 @@ def run_ours(args, wl, rank, world, local_rank):
         "roofline": roofline,
         "kernels": kernels,
         "gpu_launches": len(launches),
+        "variants": variants,
         "clocks": clk,
         "e2e": {"value": e2e * 1e3 / world, "unit": UNIT,
                 "h2d_bytes_per_step": (x.numel() + gy.numel() + w.numel()) * e,

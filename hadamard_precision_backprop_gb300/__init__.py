@@ -24,7 +24,8 @@ PER_TENSOR, PER_TOKEN = 0, 1
 RNE, SR = 0, 1
 F32, BF16 = 0, 1
 OP_COMPRESS_ACTIVATION, OP_BACKWARD_GX, OP_BACKWARD_GW, OP_BACKWARD = 0, 1, 2, 3
-OP_SELECT_GRANULARITY, OP_ABLATION_GW_HQ = 4, 5
+OP_SELECT_GRANULARITY, OP_ABLATION_GW_HQ, OP_ABLATION_GX_HLA = 4, 5, 6
+XBAR_INT8, XBAR_INT4, XBAR_PER_CHANNEL = 8, 4, 0x100   # format word of the stored activation
 DEV_NONFINITE, DEV_TIMEOUT, DEV_BADCODE = 0x1, 0x2, 0x4
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -43,6 +44,7 @@ EXPORTS = [
     "hlq_layer_step_host_workspace_bytes",
     "hlq_select_gy_granularity",
     "hlq_ablation_gw_hq",
+    "hlq_ablation_gx_hla",
 ]
 
 _lock = threading.Lock()
@@ -107,6 +109,8 @@ def lib() -> ctypes.CDLL:
                                                 P, P, P, sz, P]),
             "hlq_ablation_gw_hq": (i32, [P, P, i32, i64, i64, i64, i32, i32, u64, P, P, P,
                                          sz, P]),
+            "hlq_ablation_gx_hla": (i32, [P, P, i32, i64, i64, i64, i32, i32, P, P, P, sz,
+                                          P]),
             "hlq_trace_end": (i32, [P]),
             "hlq_trace_get": (i32, [i32, P, P]),
             "hlq_trace_free": (i32, []),
@@ -179,6 +183,18 @@ def workspace(op, T, Cin, Cout, block=16, rank=8, device=None):
                        device=device or torch.cuda.current_device())
 
 
+def _xbar_fmt(xbar_bits: int, per_channel: bool) -> int:
+    """Format word of the stored activation: code bits, plus the per-channel
+    flag."""
+    return int(xbar_bits) | (XBAR_PER_CHANNEL if per_channel else 0)
+
+
+def _check_xbar_scale(xbar_scale, Cin: int, per_channel: bool):
+    need = Cin if per_channel else 1
+    if xbar_scale.dtype != _torch().float32 or xbar_scale.numel() < need:
+        raise ValueError(f"xbar_scale must hold {need} fp32 value(s)")
+
+
 def xbar_shape(T: int, Cin: int, rank: int = 8, xbar_bits: int = 8):
     """Shape of the ACBP buffer: [Cin, T'] int8 codes, or [Cin, T'/2] bytes
     of packed int4 codes."""
@@ -187,10 +203,11 @@ def xbar_shape(T: int, Cin: int, rank: int = 8, xbar_bits: int = 8):
 
 
 def hlq_compress_activation(x, rank: int = 8, block: int = 16, out=None,
-                            scale=None, ws=None, xbar_bits: int = 8, stream=None):
-    """ACBP: x [T, Cin] -> (codes, fp32 scale [1]); codes are int8
-    [Cin, T*rank/16] (xbar_bits 8) or uint8 [Cin, T*rank/32] holding two int4
-    codes per byte (xbar_bits 4)."""
+                            scale=None, ws=None, xbar_bits: int = 8, stream=None,
+                            xbar_per_channel: bool = False):
+    """ACBP: x [T, Cin] -> (codes, fp32 scale [1], or [Cin] with
+    xbar_per_channel); codes are int8 [Cin, T*rank/16] (xbar_bits 8) or uint8
+    [Cin, T*rank/32] holding two int4 codes per byte (xbar_bits 4)."""
     torch = _torch()
     _need_cuda_contig(x)
     T, Cin = x.shape
@@ -199,11 +216,14 @@ def hlq_compress_activation(x, rank: int = 8, block: int = 16, out=None,
                           dtype=torch.int8 if xbar_bits == 8 else torch.uint8,
                           device=x.device)
     if scale is None:
-        scale = torch.empty(1, dtype=torch.float32, device=x.device)
+        scale = torch.empty(Cin if xbar_per_channel else 1, dtype=torch.float32,
+                            device=x.device)
+    _check_xbar_scale(scale, Cin, xbar_per_channel)
     if ws is None:
         ws = workspace(OP_COMPRESS_ACTIVATION, T, Cin, 16, block, rank, x.device)
     _check(lib().hlq_compress_activation(
-        _ptr(x), _dtype_code(x), T, Cin, block, rank, xbar_bits, _ptr(out),
+        _ptr(x), _dtype_code(x), T, Cin, block, rank,
+        _xbar_fmt(xbar_bits, xbar_per_channel), _ptr(out),
         _ptr(scale), _ptr(ws), ws.numel(), _stream(stream)), "hlq_compress_activation")
     return out, scale
 
@@ -232,19 +252,21 @@ def hlq_linear_backward_gx(g_y, w, gran_gy: int = PER_TOKEN,
 
 def hlq_linear_backward_gw(g_y, xbar, xbar_scale, rank: int = 8,
                            block: int = 16, out=None, ws=None, xbar_bits: int = 8,
-                           stream=None):
+                           stream=None, xbar_per_channel: bool = False):
     """g_w [Cout, Cin] (fp32) from g_y [T, Cout] and the ACBP buffer."""
     torch = _torch()
     _need_cuda_contig(g_y, xbar, xbar_scale)
     T, Cout = g_y.shape
     Cin = xbar.shape[0]
+    _check_xbar_scale(xbar_scale, Cin, xbar_per_channel)
     if out is None:
         out = torch.empty((Cout, Cin), dtype=torch.float32, device=g_y.device)
     if ws is None:
         ws = workspace(OP_BACKWARD_GW, T, Cin, Cout, block, rank, g_y.device)
     _check(lib().hlq_linear_backward_gw(
         _ptr(g_y), _dtype_code(g_y), _ptr(xbar), _ptr(xbar_scale), T, Cin,
-        Cout, block, rank, xbar_bits, _ptr(out), _ptr(ws), ws.numel(), _stream(stream)),
+        Cout, block, rank, _xbar_fmt(xbar_bits, xbar_per_channel), _ptr(out), _ptr(ws),
+        ws.numel(), _stream(stream)),
         "hlq_linear_backward_gw")
     return out
 
@@ -274,7 +296,7 @@ def hlq_linear_backward(g_y, w, xbar, xbar_scale, rank: int = 8,
                         gran_gy: int = PER_TOKEN, gran_w: int = PER_TENSOR,
                         rnd: int = SR, seed: int = 0, block: int = 16,
                         out_gx=None, out_gw=None, ws=None, xbar_bits: int = 8,
-                        stream=None):
+                        stream=None, xbar_per_channel: bool = False):
     """Both gradients of the layer, the g_x and g_w branches overlapped on
     the GPU: returns (g_x [T, Cin], g_w [Cout, Cin]) fp32."""
     torch = _torch()
@@ -283,6 +305,7 @@ def hlq_linear_backward(g_y, w, xbar, xbar_scale, rank: int = 8,
     Cin = w.shape[1]
     if w.shape[0] != Cout or g_y.dtype != w.dtype or xbar.shape[0] != Cin:
         raise ValueError("shape/dtype mismatch between g_y, w and xbar")
+    _check_xbar_scale(xbar_scale, Cin, xbar_per_channel)
     if out_gx is None:
         out_gx = torch.empty((T, Cin), dtype=torch.float32, device=g_y.device)
     if out_gw is None:
@@ -291,7 +314,8 @@ def hlq_linear_backward(g_y, w, xbar, xbar_scale, rank: int = 8,
         ws = workspace(OP_BACKWARD, T, Cin, Cout, block, rank, g_y.device)
     _check(lib().hlq_linear_backward(
         _ptr(g_y), _ptr(w), _ptr(xbar), _ptr(xbar_scale), _dtype_code(g_y), T,
-        Cin, Cout, block, rank, xbar_bits, gran_gy, gran_w, rnd, seed, _ptr(out_gx),
+        Cin, Cout, block, rank, _xbar_fmt(xbar_bits, xbar_per_channel), gran_gy,
+        gran_w, rnd, seed, _ptr(out_gx),
         _ptr(out_gw), _ptr(ws), ws.numel(), _stream(stream)),
         "hlq_linear_backward")
     return out_gx, out_gw
@@ -313,7 +337,7 @@ def hlq_layer_step_host(x, g_y, w, xbar, xbar_scale, rank: int = 8,
                         gran_gy: int = PER_TOKEN, gran_w: int = PER_TENSOR,
                         rnd: int = SR, seed: int = 0, block: int = 16,
                         out_gx=None, out_gw=None, ws=None, chunk_tokens: int = 0,
-                        xbar_bits: int = 8, stream=None):
+                        xbar_bits: int = 8, stream=None, xbar_per_channel: bool = False):
     """One layer step from host tensors (x, g_y, w on the CPU, pinned for
     speed): compresses x into the device buffers xbar / xbar_scale and
     returns host (g_x, g_w) fp32.  Asynchronous on `stream`: synchronize it
@@ -323,6 +347,7 @@ def hlq_layer_step_host(x, g_y, w, xbar, xbar_scale, rank: int = 8,
     _need_cuda_contig(xbar, xbar_scale)
     T, Cout = g_y.shape
     Cin = w.shape[1]
+    _check_xbar_scale(xbar_scale, Cin, xbar_per_channel)
     if w.shape[0] != Cout or tuple(x.shape) != (T, Cin) or not (x.dtype == g_y.dtype == w.dtype):
         raise ValueError("shape/dtype mismatch between x, g_y and w")
     if out_gx is None:
@@ -334,24 +359,27 @@ def hlq_layer_step_host(x, g_y, w, xbar, xbar_scale, rank: int = 8,
         n = hlq_layer_step_host_workspace_bytes(dt, T, Cin, Cout, block, rank)
         ws = torch.empty(max(n, 256), dtype=torch.uint8, device=xbar.device)
     _check(lib().hlq_layer_step_host(
-        _ptr(x), _ptr(g_y), _ptr(w), dt, T, Cin, Cout, block, rank, xbar_bits, gran_gy,
-        gran_w,
+        _ptr(x), _ptr(g_y), _ptr(w), dt, T, Cin, Cout, block, rank,
+        _xbar_fmt(xbar_bits, xbar_per_channel), gran_gy, gran_w,
         rnd, seed, _ptr(out_gx), _ptr(out_gw), _ptr(xbar), _ptr(xbar_scale),
         chunk_tokens, _ptr(ws), ws.numel(), _stream(stream)), "hlq_layer_step_host")
     return out_gx, out_gw
 
 
 def hlq_select_gy_granularity(g_y, threshold: float = 1.5, block: int = 16,
-                              stream=None):
+                              stream=None, mse=None, choice=None, ws=None):
     """Layer-wise quantizer selection on a calibration sample g_y [T, Cout]:
     returns device tensors (mse [2] fp64: per tensor, per token; choice [1]
-    int32: PER_TOKEN or PER_TENSOR)."""
+    int32: PER_TOKEN or PER_TENSOR); mse / choice / ws may be preallocated."""
     torch = _torch()
     _need_cuda_contig(g_y)
     T, Cout = g_y.shape
-    mse = torch.empty(2, dtype=torch.float64, device=g_y.device)
-    choice = torch.empty(1, dtype=torch.int32, device=g_y.device)
-    ws = workspace(OP_SELECT_GRANULARITY, T, 16, Cout, block, 8, g_y.device)
+    if mse is None:
+        mse = torch.empty(2, dtype=torch.float64, device=g_y.device)
+    if choice is None:
+        choice = torch.empty(1, dtype=torch.int32, device=g_y.device)
+    if ws is None:
+        ws = workspace(OP_SELECT_GRANULARITY, T, 16, Cout, block, 8, g_y.device)
     _check(lib().hlq_select_gy_granularity(
         _ptr(g_y), _dtype_code(g_y), T, Cout, block, float(threshold), _ptr(mse),
         _ptr(choice), _ptr(ws), ws.numel(), _stream(stream)), "hlq_select_gy_granularity")
@@ -359,7 +387,7 @@ def hlq_select_gy_granularity(g_y, threshold: float = 1.5, block: int = 16,
 
 
 def hlq_ablation_gw_hq(g_y, x, rnd: int = SR, seed: int = 0, block: int = 16,
-                       with_acc: bool = False, stream=None):
+                       with_acc: bool = False, stream=None, out=None, ws=None):
     """g_w [Cout, Cin] through HQ along tokens (the ablation of the g_w path);
     with_acc also returns the int32 accumulator."""
     torch = _torch()
@@ -368,14 +396,38 @@ def hlq_ablation_gw_hq(g_y, x, rnd: int = SR, seed: int = 0, block: int = 16,
     Cin = x.shape[1]
     if x.shape[0] != T or x.dtype != g_y.dtype:
         raise ValueError("shape/dtype mismatch between g_y and x")
-    gw = torch.empty((Cout, Cin), dtype=torch.float32, device=g_y.device)
+    gw = (torch.empty((Cout, Cin), dtype=torch.float32, device=g_y.device)
+          if out is None else out)
     acc = (torch.empty((Cout, Cin), dtype=torch.int32, device=g_y.device)
            if with_acc else None)
-    ws = workspace(OP_ABLATION_GW_HQ, T, Cin, Cout, block, 8, g_y.device)
+    if ws is None:
+        ws = workspace(OP_ABLATION_GW_HQ, T, Cin, Cout, block, 8, g_y.device)
     _check(lib().hlq_ablation_gw_hq(
         _ptr(g_y), _ptr(x), _dtype_code(g_y), T, Cin, Cout, block, rnd, seed, _ptr(gw),
         _ptr(acc), _ptr(ws), ws.numel(), _stream(stream)), "hlq_ablation_gw_hq")
     return (gw, acc) if with_acc else gw
+
+
+def hlq_ablation_gx_hla(g_y, w, rank: int = 8, block: int = 16, with_acc: bool = False,
+                        stream=None, out=None, ws=None):
+    """g_x [T, Cin] through HLA along Cout with int8 codes (the ablation of
+    the g_x path); with_acc also returns the int32 accumulator."""
+    torch = _torch()
+    _need_cuda_contig(g_y, w)
+    T, Cout = g_y.shape
+    Cin = w.shape[1]
+    if w.shape[0] != Cout or w.dtype != g_y.dtype:
+        raise ValueError("shape/dtype mismatch between g_y and w")
+    gx = (torch.empty((T, Cin), dtype=torch.float32, device=g_y.device)
+          if out is None else out)
+    acc = (torch.empty((T, Cin), dtype=torch.int32, device=g_y.device)
+           if with_acc else None)
+    if ws is None:
+        ws = workspace(OP_ABLATION_GX_HLA, T, Cin, Cout, block, rank, g_y.device)
+    _check(lib().hlq_ablation_gx_hla(
+        _ptr(g_y), _ptr(w), _dtype_code(g_y), T, Cin, Cout, block, rank, _ptr(gx),
+        _ptr(acc), _ptr(ws), ws.numel(), _stream(stream)), "hlq_ablation_gx_hla")
+    return (gx, acc) if with_acc else gx
 
 
 def hlq_debug_gx_parts(g_y, w, gran_gy=PER_TOKEN, gran_w=PER_TENSOR, rnd=SR,
@@ -405,12 +457,13 @@ def hlq_debug_gx_parts(g_y, w, gran_gy=PER_TOKEN, gran_w=PER_TENSOR, rnd=SR,
 
 
 def hlq_debug_gw_parts(g_y, xbar, xbar_scale, rank=8, block=16, xbar_bits=8,
-                       stream=None):
+                       stream=None, xbar_per_channel=False):
     """g_w plus its intermediates: dict(g_w, qg, sg, acc)."""
     torch = _torch()
     _need_cuda_contig(g_y, xbar, xbar_scale)
     T, Cout = g_y.shape
     Cin = xbar.shape[0]
+    _check_xbar_scale(xbar_scale, Cin, xbar_per_channel)
     Tp = T // 16 * rank
     dev = g_y.device
     r = dict(
@@ -422,7 +475,8 @@ def hlq_debug_gw_parts(g_y, xbar, xbar_scale, rank=8, block=16, xbar_bits=8,
     ws = workspace(OP_BACKWARD_GW, T, Cin, Cout, block, rank, dev)
     _check(lib().hlq_debug_gw_parts(
         _ptr(g_y), _dtype_code(g_y), _ptr(xbar), _ptr(xbar_scale), T, Cin,
-        Cout, block, rank, xbar_bits, _ptr(r["g_w"]), _ptr(ws), ws.numel(), _ptr(r["qg"]),
+        Cout, block, rank, _xbar_fmt(xbar_bits, xbar_per_channel), _ptr(r["g_w"]), _ptr(ws),
+        ws.numel(), _ptr(r["qg"]),
         _ptr(r["sg"]), _ptr(r["acc"]), _stream(stream)), "hlq_debug_gw_parts")
     return r
 

@@ -138,6 +138,26 @@ GwLayout gw_layout(int64_t T, int64_t Cin, int64_t Cout, int rank) {
   return L;
 }
 
+// Workspace of the g_x HLA ablation: two amax slots, the two scales, bf16
+// codes of g_y [T, ld] and of w [Cin, ld] (ld = Cout' rounded up to 8 codes
+// for 16-byte rows).
+struct GxHlaLayout {
+  size_t amax, s, qg, qw, total;
+  int64_t ld;
+};
+GxHlaLayout gx_hla_layout(int64_t T, int64_t Cin, int64_t Cout, int rank) {
+  GxHlaLayout L{};
+  const int64_t Kp = Cout / 16 * rank;
+  L.ld = (Kp + 7) / 8 * 8;
+  size_t o = 0;
+  L.amax = o; o += kAlign;
+  L.s = o;    o += kAlign;
+  L.qg = o;   o += align_up((size_t)T * (size_t)L.ld * 2);
+  L.qw = o;   o += align_up((size_t)Cin * (size_t)L.ld * 2);
+  L.total = o;
+  return L;
+}
+
 int device_sm_count() {
   static int count[kMaxDevices] = {};
   int dev = 0;
@@ -151,15 +171,23 @@ int device_sm_count() {
   return count[dev];
 }
 
-size_t compress_ws(int64_t, int64_t) { return kAlign; }
+// amax slot(s): one for the tensor, or one per channel
+size_t compress_ws(int64_t, int64_t Cin) {
+  return kAlign + align_up((size_t)(Cin > 0 ? Cin : 0) * 4);
+}
 
 bool rank_ok(int rank) {
   return rank == 1 || rank == 2 || rank == 4 || rank == 8 || rank == 16;
 }
 
-// Storage of the ACBP buffer: 8 (int8 codes [Cin, T']) or 4 (int4 codes packed
-// two per byte [Cin, T'/2], even ranks only).
-hlq_status xbar_bits_check(int bits, int rank) {
+// Format of the ACBP buffer: code bits 8 (int8 codes [Cin, T']) or 4 (int4
+// codes packed two per byte [Cin, T'/2], even ranks only), optionally with
+// HLQ_XBAR_PER_CHANNEL (scales [Cin] instead of [1]).
+inline int xbar_code_bits(int fmt) { return fmt & 0xff; }
+inline bool xbar_per_channel(int fmt) { return (fmt & HLQ_XBAR_PER_CHANNEL) != 0; }
+hlq_status xbar_fmt_check(int fmt, int rank) {
+  if (fmt & ~(0xff | HLQ_XBAR_PER_CHANNEL)) return HLQ_ERR_INVALID_ARG;
+  const int bits = xbar_code_bits(fmt);
   if (bits != 8 && bits != 4) return HLQ_ERR_INVALID_ARG;
   if (bits == 4 && rank < 2) return HLQ_ERR_UNSUPPORTED;
   return HLQ_OK;
@@ -310,18 +338,20 @@ hlq_status gx_impl(const void* gy, const void* w, int dt, int64_t T,
 }
 
 // ACBP: HLA of x along tokens, per-tensor amax pass, int8 codes [Cin, T'] or
-// packed int4 codes (bits 4).
+// packed int4 codes (4 code bits); per-channel scales with HLQ_XBAR_PER_CHANNEL.
 hlq_status compress_launches(const void* x, bool bf16, int64_t T, int64_t Cin, int rank,
-                             int bits, int8_t* xbar, float* xscale, unsigned int* amax,
+                             int fmt, int8_t* xbar, float* xscale, unsigned int* amax,
                              unsigned int* status, cudaStream_t s) {
   const int64_t Tp = T / 16 * rank;
-  HLQ_TRY(cudaMemsetAsync(amax, 0, 4, s));
+  const bool per_ch = xbar_per_channel(fmt);
+  const int out = xbar_code_bits(fmt) == 4 ? kHlaOutI4 : kHlaOutI8;
+  HLQ_TRY(cudaMemsetAsync(amax, 0, (size_t)(per_ch ? Cin : 1) * 4, s));
   HLQ_LAUNCH("hla_x_amax", s,
              launch_hla(x, bf16, T, Cin, rank, true, kHlaOutI8, amax, nullptr, 0, nullptr,
-                        status, s));
+                        status, s, per_ch));
   HLQ_LAUNCH("hla_x_quant", s,
-             launch_hla(x, bf16, T, Cin, rank, false, bits == 4 ? kHlaOutI4 : kHlaOutI8, amax,
-                        xbar, Tp, xscale, status, s));
+             launch_hla(x, bf16, T, Cin, rank, false, out, amax, xbar, Tp, xscale, status, s,
+                        per_ch));
   return HLQ_OK;
 }
 
@@ -340,13 +370,13 @@ hlq_status hla_gy_launches(const void* gy, bool bf16, int64_t T, int64_t Cout, i
 }
 
 // ACBP buffer widened to bf16, then the g_w GEMM with its dequantization.
-hlq_status gw_gemm_launches(const int8_t* xbar, int bits, const float* xscale, int64_t Cin,
+hlq_status gw_gemm_launches(const int8_t* xbar, int fmt, const float* xscale, int64_t Cin,
                             int64_t Cout, int64_t Tp, const GwLayout& L, uint8_t* base,
                             float* gw, int32_t* dbg_acc, unsigned int* status,
                             cudaStream_t s) {
   void* xw = base + L.xw;
   const float* sg = reinterpret_cast<const float*>(base + L.sg);
-  if (bits == 4)
+  if (xbar_code_bits(fmt) == 4)
     HLQ_LAUNCH("widen_xbar", s,
                launch_widen_i4_bf16(reinterpret_cast<const uint8_t*>(xbar), xw, Cin, Tp, L.ld,
                                     s));
@@ -357,11 +387,12 @@ hlq_status gw_gemm_launches(const int8_t* xbar, int bits, const float* xscale, i
   const GemmPlan plan = plan_gemm_tc(1, Cout, Cin, Tp, sms, 16);
   HLQ_LAUNCH("gemm_gw_tc", s,
              launch_gemm_tc(1, base + L.qg, L.ld, xw, L.ld, Cout, Cin, Tp, plan, sg, false,
-                            xscale, gw, dbg_acc, base + L.split, status, s));
+                            xscale, gw, dbg_acc, base + L.split, status, s,
+                            xbar_per_channel(fmt)));
   return HLQ_OK;
 }
 
-hlq_status gw_impl(const void* gy, int dt, const int8_t* xbar, int bits,
+hlq_status gw_impl(const void* gy, int dt, const int8_t* xbar, int fmt,
                    const float* xscale, int64_t T, int64_t Cin, int64_t Cout,
                    int block, int rank, float* gw, void* ws, size_t ws_bytes,
                    int8_t* dbg_qg, float* dbg_sg, int32_t* dbg_acc,
@@ -369,7 +400,7 @@ hlq_status gw_impl(const void* gy, int dt, const int8_t* xbar, int bits,
   hlq_status st = check_common(dt, T, Cin, Cout, block);
   if (st != HLQ_OK) return st;
   if (!rank_ok(rank)) return HLQ_ERR_INVALID_ARG;
-  st = xbar_bits_check(bits, rank);
+  st = xbar_fmt_check(fmt, rank);
   if (st != HLQ_OK) return st;
   const int64_t Tp = T / 16 * rank;
   const int64_t n_gw = Cout * Cin;
@@ -379,7 +410,8 @@ hlq_status gw_impl(const void* gy, int dt, const int8_t* xbar, int bits,
   if (!xscale) return HLQ_ERR_INVALID_ARG;
   if (!aligned16(gy) || !aligned16(xbar) || !aligned16(gw)) return HLQ_ERR_ALIGN;
   // |acc| <= T' * 127 * qmax_x must stay below 2^31
-  if (Tp * 127 * (bits == 4 ? 7 : 127) >= ((int64_t)1 << 31)) return HLQ_ERR_OVERFLOW;
+  if (Tp * 127 * (xbar_code_bits(fmt) == 4 ? 7 : 127) >= ((int64_t)1 << 31))
+    return HLQ_ERR_OVERFLOW;
   const GwLayout L = gw_layout(T, Cin, Cout, rank);
   if (!ws || ws_bytes < L.total) return HLQ_ERR_WORKSPACE;
   if (!aligned256(ws)) return HLQ_ERR_ALIGN;
@@ -401,7 +433,7 @@ hlq_status gw_impl(const void* gy, int dt, const int8_t* xbar, int bits,
 
   st = hla_gy_launches(gy, bf16, T, Cout, rank, amax, qg, L.ld, sg, status, s);
   if (st != HLQ_OK) return st;
-  st = gw_gemm_launches(xbar, bits, xscale, Cin, Cout, Tp, L, base, gw, dbg_acc, status, s);
+  st = gw_gemm_launches(xbar, fmt, xscale, Cin, Cout, Tp, L, base, gw, dbg_acc, status, s);
   if (st != HLQ_OK) return st;
   if (dbg_qg) HLQ_TRY(launch_decode_bf16(qg, dbg_qg, Cout, Tp, L.ld, s));
   if (dbg_sg) HLQ_TRY(cudaMemcpyAsync(dbg_sg, sg, 4, cudaMemcpyDeviceToDevice, s));
@@ -487,19 +519,21 @@ size_t hlq_workspace_bytes(int op, int64_t T, int64_t Cin, int64_t Cout,
     case HLQ_OP_ABLATION_GW_HQ:
       // amax slots, the two scales, codes [Cout, T] and [Cin, T]
       return 2 * kAlign + align_up((size_t)Cout * (size_t)T) + align_up((size_t)Cin * (size_t)T);
+    case HLQ_OP_ABLATION_GX_HLA:
+      return gx_hla_layout(T, Cin, Cout, rank_ok(rank) ? rank : 16).total;
     default:
       return 0;
   }
 }
 
 hlq_status hlq_compress_activation(const void* d_x, int dt, int64_t T,
-                                   int64_t Cin, int block, int rank, int xbar_bits,
+                                   int64_t Cin, int block, int rank, int xbar_fmt,
                                    int8_t* d_xbar, float* d_xbar_scale,
                                    void* d_ws, size_t ws_bytes, void* stream) {
   hlq_status st = check_common(dt, T, Cin, 16, block);
   if (st != HLQ_OK) return st;
   if (!rank_ok(rank)) return HLQ_ERR_INVALID_ARG;
-  st = xbar_bits_check(xbar_bits, rank);
+  st = xbar_fmt_check(xbar_fmt, rank);
   if (st != HLQ_OK) return st;
   const int64_t Tp = T / 16 * rank;
   if (!d_xbar_scale) return HLQ_ERR_INVALID_ARG;
@@ -509,19 +543,20 @@ hlq_status hlq_compress_activation(const void* d_x, int dt, int64_t T,
   if (!aligned256(d_ws)) return HLQ_ERR_ALIGN;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (Cin * Tp == 0) {
-    HLQ_TRY(cudaMemsetAsync(d_xbar_scale, 0, 4, s));
+    const int64_t n_scales = xbar_per_channel(xbar_fmt) ? Cin : 1;
+    if (n_scales > 0) HLQ_TRY(cudaMemsetAsync(d_xbar_scale, 0, (size_t)n_scales * 4, s));
     return HLQ_OK;
   }
   unsigned int* status = device_status_ptr();
   if (!status) return HLQ_ERR_CUDA;
-  return compress_launches(d_x, dt == HLQ_BF16, T, Cin, rank, xbar_bits, d_xbar,
+  return compress_launches(d_x, dt == HLQ_BF16, T, Cin, rank, xbar_fmt, d_xbar,
                            d_xbar_scale, static_cast<unsigned int*>(d_ws), status, s);
 }
 
 hlq_status hlq_linear_backward(const void* d_gy, const void* d_w, const int8_t* d_xbar,
                                const float* d_xbar_scale, int dt, int64_t T,
                                int64_t Cin, int64_t Cout, int block, int rank,
-                               int xbar_bits, int gran_gy, int gran_w, int rnd, uint64_t seed,
+                               int xbar_fmt, int gran_gy, int gran_w, int rnd, uint64_t seed,
                                float* d_gx, float* d_gw, void* d_ws, size_t ws_bytes,
                                void* stream) {
   hlq_status st = check_common(dt, T, Cin, Cout, block);
@@ -536,7 +571,7 @@ hlq_status hlq_linear_backward(const void* d_gy, const void* d_w, const int8_t* 
   cudaStream_t a = aux_stream(0), aw = aux_stream(1);
   if (!a || !aw) return HLQ_ERR_CUDA;
   // validate both branches before forking (nothing enqueued on failure)
-  st = gw_impl(d_gy, dt, d_xbar, xbar_bits, d_xbar_scale, T, Cin, Cout, block, rank, d_gw,
+  st = gw_impl(d_gy, dt, d_xbar, xbar_fmt, d_xbar_scale, T, Cin, Cout, block, rank, d_gw,
                base + gx_bytes, gw_bytes, nullptr, nullptr, nullptr, nullptr,
                /*validate_only=*/true);
   if (st != HLQ_OK) return st;
@@ -555,7 +590,7 @@ hlq_status hlq_linear_backward(const void* d_gy, const void* d_w, const int8_t* 
   if (cudaEventRecord(fork, s) != cudaSuccess || cudaStreamWaitEvent(a, fork, 0) != cudaSuccess)
     r = HLQ_ERR_CUDA;
   if (r == HLQ_OK)  // g_w branch on the auxiliary stream
-    r = gw_impl(d_gy, dt, d_xbar, xbar_bits, d_xbar_scale, T, Cin, Cout, block, rank, d_gw,
+    r = gw_impl(d_gy, dt, d_xbar, xbar_fmt, d_xbar_scale, T, Cin, Cout, block, rank, d_gw,
                 base + gx_bytes, gw_bytes, nullptr, nullptr, nullptr, a, false);
   if (r == HLQ_OK)  // g_x branch on the caller's stream, its HQ of w on a third
     r = gx_impl(d_gy, d_w, dt, T, Cin, Cout, block, gran_gy, gran_w, rnd, seed, d_gx,
@@ -654,6 +689,58 @@ hlq_status hlq_ablation_gw_hq(const void* d_gy, const void* d_x, int dt, int64_t
   return HLQ_OK;
 }
 
+hlq_status hlq_ablation_gx_hla(const void* d_gy, const void* d_w, int dt, int64_t T,
+                               int64_t Cin, int64_t Cout, int block, int rank, float* d_gx,
+                               int32_t* d_acc, void* d_ws, size_t ws_bytes, void* stream) {
+  hlq_status st = check_common(dt, T, Cin, Cout, block);
+  if (st != HLQ_OK) return st;
+  if (!rank_ok(rank)) return HLQ_ERR_INVALID_ARG;
+  if ((T * Cout > 0 && !d_gy) || (Cout * Cin > 0 && !d_w) || (T * Cin > 0 && !d_gx))
+    return HLQ_ERR_INVALID_ARG;
+  if (!aligned16(d_gy) || !aligned16(d_w) || !aligned16(d_gx) || !aligned16(d_acc))
+    return HLQ_ERR_ALIGN;
+  const int64_t Kp = Cout / 16 * rank;
+  if (Kp * 127 * 127 >= ((int64_t)1 << 31)) return HLQ_ERR_OVERFLOW;
+  const GxHlaLayout L = gx_hla_layout(T, Cin, Cout, rank);
+  if (!d_ws || ws_bytes < L.total) return HLQ_ERR_WORKSPACE;
+  if (!aligned256(d_ws)) return HLQ_ERR_ALIGN;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (T * Cin == 0) return HLQ_OK;
+  if (Kp == 0) {  // empty contraction
+    HLQ_TRY(cudaMemsetAsync(d_gx, 0, (size_t)(T * Cin) * 4, s));
+    if (d_acc) HLQ_TRY(cudaMemsetAsync(d_acc, 0, (size_t)(T * Cin) * 4, s));
+    return HLQ_OK;
+  }
+  unsigned int* status = device_status_ptr();
+  if (!status) return HLQ_ERR_CUDA;
+  uint8_t* base = static_cast<uint8_t*>(d_ws);
+  unsigned int* amax = reinterpret_cast<unsigned int*>(base + L.amax);  // [0] g_y, [1] w
+  float* sg = reinterpret_cast<float*>(base + L.s);
+  float* sw = sg + 4;
+  void* qg = base + L.qg;
+  void* qw = base + L.qw;
+  const bool bf16 = dt == HLQ_BF16;
+  HLQ_TRY(cudaMemsetAsync(amax, 0, 8, s));
+  HLQ_LAUNCH("hla_rows_gy_amax", s,
+             launch_hla_rows(d_gy, bf16, T, Cout, rank, true, amax, nullptr, 0, nullptr,
+                             status, s));
+  HLQ_LAUNCH("hla_rows_gy_quant", s,
+             launch_hla_rows(d_gy, bf16, T, Cout, rank, false, amax, qg, L.ld, sg, status, s));
+  HLQ_LAUNCH("hla_w_amax", s,
+             launch_hla(d_w, bf16, Cout, Cin, rank, true, kHlaOutBf16, amax + 1, nullptr, 0,
+                        nullptr, status, s));
+  HLQ_LAUNCH("hla_w_quant", s,
+             launch_hla(d_w, bf16, Cout, Cin, rank, false, kHlaOutBf16, amax + 1, qw, L.ld, sw,
+                        status, s));
+  const int sms = device_sm_count();
+  if (sms <= 0) return HLQ_ERR_CUDA;
+  const GemmPlan plan = plan_gemm_tc(1, T, Cin, Kp, sms, 1);
+  HLQ_LAUNCH("gemm_gx_hla_tc", s,
+             launch_gemm_tc(1, qg, L.ld, qw, L.ld, T, Cin, Kp, plan, sg, false, sw, d_gx, d_acc,
+                            nullptr, status, s));
+  return HLQ_OK;
+}
+
 size_t hlq_layer_step_host_workspace_bytes(int dt, int64_t T, int64_t Cin, int64_t Cout,
                                            int block, int rank) {
   (void)block;
@@ -663,7 +750,7 @@ size_t hlq_layer_step_host_workspace_bytes(int dt, int64_t T, int64_t Cin, int64
 
 hlq_status hlq_layer_step_host(const void* h_x, const void* h_gy, const void* h_w, int dt,
                                int64_t T, int64_t Cin, int64_t Cout, int block, int rank,
-                               int xbar_bits, int gran_gy, int gran_w, int rnd, uint64_t seed,
+                               int xbar_fmt, int gran_gy, int gran_w, int rnd, uint64_t seed,
                                float* h_gx,
                                float* h_gw, int8_t* d_xbar, float* d_xbar_scale,
                                int64_t chunk_tokens, void* d_ws, size_t ws_bytes,
@@ -689,7 +776,7 @@ hlq_status hlq_layer_step_host(const void* h_x, const void* h_gy, const void* h_
   st = gx_impl(gy, w, dt, T, Cin, Cout, block, gran_gy, gran_w, rnd, seed, gx, base + L.gxws,
                gx_bytes, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, true);
   if (st != HLQ_OK) return st;
-  st = gw_impl(gy, dt, d_xbar, xbar_bits, d_xbar_scale, T, Cin, Cout, block, rank, gw,
+  st = gw_impl(gy, dt, d_xbar, xbar_fmt, d_xbar_scale, T, Cin, Cout, block, rank, gw,
                base + L.gwws, gw_bytes, nullptr, nullptr, nullptr, nullptr, true);
   if (st != HLQ_OK) return st;
   if (!d_xbar_scale) return HLQ_ERR_INVALID_ARG;
@@ -708,14 +795,14 @@ hlq_status hlq_layer_step_host(const void* h_x, const void* h_gy, const void* h_
     HLQ_TRY(h2d(x, h_x, (size_t)(T * Cin) * esz, s));
     HLQ_TRY(h2d(gy, h_gy, (size_t)(T * Cout) * esz, s));
     HLQ_TRY(h2d(w, h_w, (size_t)(Cout * Cin) * esz, s));
-    st = hlq_compress_activation(x, dt, T, Cin, block, rank, xbar_bits, d_xbar, d_xbar_scale,
+    st = hlq_compress_activation(x, dt, T, Cin, block, rank, xbar_fmt, d_xbar, d_xbar_scale,
                                  base + L.cws, compress_ws(T, Cin), stream);
     if (st != HLQ_OK) return st;
     st = hlq_linear_backward_gx(gy, w, dt, T, Cin, Cout, block, gran_gy, gran_w, rnd, seed,
                                 gx, base + L.gxws, gx_bytes, stream);
     if (st != HLQ_OK) return st;
     st = hlq_linear_backward_gw(gy, dt, d_xbar, d_xbar_scale, T, Cin, Cout, block, rank,
-                                xbar_bits, gw,
+                                xbar_fmt, gw,
                                 base + L.gwws, gw_bytes, stream);
     if (st != HLQ_OK) return st;
     HLQ_TRY(d2h(h_gx, gx, (size_t)(T * Cin) * 4, s));
@@ -834,10 +921,10 @@ hlq_status hlq_layer_step_host(const void* h_x, const void* h_gy, const void* h_
     r = hla_gy_launches(gy, bf16, T, Cout, rank, gw_amax, gwb + WL.qg, WL.ld, sg, status, a_gw);
   fail(cudaStreamWaitEvent(a_gw, x_in, 0));
   if (r == HLQ_OK)
-    r = compress_launches(x, bf16, T, Cin, rank, xbar_bits, d_xbar, d_xbar_scale,
+    r = compress_launches(x, bf16, T, Cin, rank, xbar_fmt, d_xbar, d_xbar_scale,
                           reinterpret_cast<unsigned int*>(base + L.cws), status, a_gw);
   if (r == HLQ_OK)
-    r = gw_gemm_launches(d_xbar, xbar_bits, d_xbar_scale, Cin, Cout, Tp, WL, gwb, gw, nullptr,
+    r = gw_gemm_launches(d_xbar, xbar_fmt, d_xbar_scale, Cin, Cout, Tp, WL, gwb, gw, nullptr,
                          status,
                          a_gw);
   fail(cudaEventRecord(gw_done, a_gw));
@@ -870,9 +957,9 @@ hlq_status hlq_linear_backward_gw(const void* d_gy, int dt,
                                   const int8_t* d_xbar,
                                   const float* d_xbar_scale, int64_t T,
                                   int64_t Cin, int64_t Cout, int block,
-                                  int rank, int xbar_bits, float* d_gw, void* d_ws,
+                                  int rank, int xbar_fmt, float* d_gw, void* d_ws,
                                   size_t ws_bytes, void* stream) {
-  return gw_impl(d_gy, dt, d_xbar, xbar_bits, d_xbar_scale, T, Cin, Cout, block, rank,
+  return gw_impl(d_gy, dt, d_xbar, xbar_fmt, d_xbar_scale, T, Cin, Cout, block, rank,
                  d_gw, d_ws, ws_bytes, nullptr, nullptr, nullptr, stream);
 }
 
@@ -890,10 +977,10 @@ hlq_status hlq_debug_gx_parts(const void* d_gy, const void* d_w, int dt,
 hlq_status hlq_debug_gw_parts(const void* d_gy, int dt, const int8_t* d_xbar,
                               const float* d_xbar_scale, int64_t T,
                               int64_t Cin, int64_t Cout, int block, int rank,
-                              int xbar_bits, float* d_gw, void* d_ws, size_t ws_bytes,
+                              int xbar_fmt, float* d_gw, void* d_ws, size_t ws_bytes,
                               int8_t* d_qg, float* d_sg, int32_t* d_acc,
                               void* stream) {
-  return gw_impl(d_gy, dt, d_xbar, xbar_bits, d_xbar_scale, T, Cin, Cout, block, rank,
+  return gw_impl(d_gy, dt, d_xbar, xbar_fmt, d_xbar_scale, T, Cin, Cout, block, rank,
                  d_gw, d_ws, ws_bytes, d_qg, d_sg, d_acc, stream);
 }
 
@@ -954,7 +1041,7 @@ hlq_status hlq_debug_tc_gemm(int kind, const void* d_a, int64_t lda, const void*
                              void* stream) {
   if (kind != 0 && kind != 1) return HLQ_ERR_INVALID_ARG;
   if (M < 0 || N < 0 || K < 0 || N % 16 || K % 16 || M % 16) return HLQ_ERR_SHAPE;
-  if (bn != 0 && bn != 128 && bn != 256) return HLQ_ERR_INVALID_ARG;
+  if (bn != 0 && bn != 96 && bn != 128 && bn != 256) return HLQ_ERR_INVALID_ARG;
   if (splits < 0 || splits > 64) return HLQ_ERR_INVALID_ARG;
   if (kind == 0 && splits > 1) return HLQ_ERR_INVALID_ARG;  // E4M3 GEMM runs unsplit
   const int esz = kind == 1 ? 2 : 1;

@@ -26,6 +26,41 @@ __device__ __forceinline__ void pdl_wait() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// Reads of what an earlier kernel of the stream wrote (amax slots, scales,
+// sums, stored codes).  Under programmatic dependent launch a kernel runs
+// while its predecessor may still be writing, and only pdl_wait() orders it
+// after those writes.  The read-only data path (ld.global.nc, which __ldg and
+// loads through const __restrict__ pointers may use) is valid only for data
+// that nothing writes during the kernel's lifetime, so these reads are
+// ordinary coherent loads, written as volatile asm so that they stay after
+// the wait.
+__device__ __forceinline__ unsigned int ld_dep_u32(const unsigned int* p) {
+  unsigned int v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ float ld_dep_f32(const float* p) {
+  float v;
+  asm volatile("ld.relaxed.gpu.global.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ double ld_dep_f64(const double* p) {
+  double v;
+  asm volatile("ld.relaxed.gpu.global.f64 %0, [%1];" : "=d"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint2 ld_dep_u2(const void* p) {
+  uint2 v;
+  asm volatile("ld.relaxed.gpu.global.v2.u32 {%0, %1}, [%2];"
+               : "=r"(v.x), "=r"(v.y) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint8_t ld_dep_u8(const void* p) {
+  unsigned short v;
+  asm volatile("ld.relaxed.gpu.global.u8 %0, [%1];" : "=h"(v) : "l"(p) : "memory");
+  return (uint8_t)v;
+}
+
 template <typename... Exp, typename... Act>
 static cudaError_t launch_pdl(void (*kernel)(Exp...), dim3 grid, dim3 block, size_t smem,
                               cudaStream_t st, Act&&... args) {

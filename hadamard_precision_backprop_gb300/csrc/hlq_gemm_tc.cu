@@ -108,17 +108,23 @@ __device__ __forceinline__ void tmem_ld_x32(uint32_t taddr, uint32_t (&r)[32]) {
 
 // The mainloop is bound by the latency of a TMA round trip (L2 -> shared
 // memory, MMA, release), so the ring holds as many stages as shared memory
-// allows: 6 of 32 KB for 128-wide tiles, 4 of 48 KB for 256-wide ones.
+// allows: 7 of 28 KB for 96-wide tiles, 6 of 32 KB for 128-wide ones, 4 of
+// 48 KB for 256-wide ones.  A 96-wide tile serves shapes where it needs
+// fewer waves than 128-wide ones.
 template <int BN>
 struct TcCfg {
-  static constexpr int kStages = BN == 128 ? 6 : 4;
-  static constexpr int kEpiWarps = BN / 32;               // 4 or 8
-  static constexpr int kColsPerThread = BN / (kEpiWarps / 4);  // 128
+  static_assert(BN == 96 || BN == 128 || BN == 256, "tile widths 96, 128, 256");
+  static constexpr int kStages = BN == 96 ? 7 : (BN == 128 ? 6 : 4);
+  static constexpr int kColGroups = BN > 128 ? 2 : 1;     // 128-column halves
+  static constexpr int kEpiWarps = 4 * kColGroups;        // 4 TMEM lane quarters each
+  static constexpr int kColsPerThread = BN / kColGroups;  // 96 or 128
   static constexpr int kThreads = 64 + 32 * kEpiWarps;
   static constexpr uint32_t kABytes = kBM * kRowBytes;
   static constexpr uint32_t kBBytes = BN * kRowBytes;
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;
-  static constexpr uint32_t kTmemCols = 2 * BN;           // two accumulators
+  // two accumulators, each starting on a 128-column boundary
+  static constexpr uint32_t kAccStride = BN <= 128 ? 128 : 256;
+  static constexpr uint32_t kTmemCols = 2 * kAccStride;
   // epilogue staging: one 32 x 32 fp32 box (128B-swizzled) per epilogue warp
   static constexpr uint32_t kStageOutBytes = 32 * 32 * 4;
   static constexpr size_t kSmem =
@@ -136,7 +142,8 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(
     const __grid_constant__ CUtensorMap tmOut, const __grid_constant__ CUtensorMap tmAcc,
     int M, int N, int num_kb, int chunk_kb, int kb_per_split, int splits, int tiles_n,
     int num_units, const float* __restrict__ sa, int per_row_a,
-    const float* __restrict__ sb, float* __restrict__ out, int32_t* __restrict__ acc_out,
+    const float* __restrict__ sb, int per_col_b, float* __restrict__ out,
+    int32_t* __restrict__ acc_out,
     int32_t* __restrict__ split_acc, unsigned int* __restrict__ slab_count,
     unsigned int* __restrict__ status) {
   using C = TcCfg<BN>;
@@ -241,7 +248,7 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(
             break;
           }
           tc_fence_after();
-          const uint32_t d = tmem_base + (uint32_t)(buf * BN);
+          const uint32_t d = tmem_base + (uint32_t)(buf * C::kAccStride);
           const int j_end = min(nkb, j + chunk_kb);
           for (int jj = 0; j < j_end; ++j, ++jj, ++i) {
             const int s = i % kStages;
@@ -286,7 +293,15 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(
       if (lane == 0) tma_store_2d(map, x, y, stg);
     };
     auto dequant_scale = [&](int m) {
-      return (out && m < M) ? (per_row_a ? sa[m] : sa[0]) * sb[0] * 0.0625f : 0.0f;
+      return (out && m < M) ? ld_dep_f32(sa + (per_row_a ? m : 0)) * ld_dep_f32(sb) * 0.0625f
+                            : 0.0f;
+    };
+    // per_col_b: the B scale of column n, sb[n], in the same product order
+    auto row_scale_a = [&](int m) {
+      return (out && m < M) ? ld_dep_f32(sa + (per_row_a ? m : 0)) : 0.0f;
+    };
+    auto col_scaled = [&](int32_t a, float ra, int n) {
+      return __float_as_uint((float)a * (ra * ld_dep_f32(sb + min(n, N - 1)) * 0.0625f));
     };
     int cc = 0;
     bool ok = true;
@@ -307,7 +322,7 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(
         if (!ok) break;
         tc_fence_after();
         const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) +
-                               (uint32_t)(buf * BN + colgrp * C::kColsPerThread);
+                               (uint32_t)(buf * C::kAccStride + colgrp * C::kColsPerThread);
         const float scale = dequant_scale(m);
 #pragma unroll
         for (int jc = 0; jc < C::kColsPerThread / 32; ++jc) {
@@ -347,7 +362,7 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(
         if (!ok) break;
         tc_fence_after();
         const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) +
-                               (uint32_t)(buf * BN + colgrp * C::kColsPerThread);
+                               (uint32_t)(buf * C::kAccStride + colgrp * C::kColsPerThread);
 #pragma unroll
         for (int jc = 0; jc < C::kColsPerThread / 32; ++jc) {
           uint32_t r[32];
@@ -374,8 +389,15 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(
             store_box(&tmAcc, x, y, v);
           }
           if (out) {
+            if (per_col_b) {
+              const float ra = row_scale_a(m);
 #pragma unroll
-            for (int q = 0; q < 32; ++q) v[q] = __float_as_uint((float)acc[32 * jc + q] * scale);
+              for (int q = 0; q < 32; ++q) v[q] = col_scaled(acc[32 * jc + q], ra, x + q);
+            } else {
+#pragma unroll
+              for (int q = 0; q < 32; ++q)
+                v[q] = __float_as_uint((float)acc[32 * jc + q] * scale);
+            }
             store_box(&tmOut, x, y, v);
           }
         }
@@ -399,12 +421,20 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(
       last = __shfl_sync(0xffffffffu, last, 0);
       if (last && m < M) {
         __threadfence();
-        const float scale = out ? (per_row_a ? sa[m] : sa[0]) * sb[0] * 0.0625f : 0.0f;
+        const float scale =
+            out ? ld_dep_f32(sa + (per_row_a ? m : 0)) * ld_dep_f32(sb) * 0.0625f : 0.0f;
+        const float ra = row_scale_a(m);
         for (int q = 0; q < C::kColsPerThread; q += 4) {
           const int n = nb + q;
           if (n + 4 <= N) {
             const int4 v = __ldcg(reinterpret_cast<const int4*>(split_acc + (size_t)m * N + n));
-            if (out)
+            if (out && per_col_b)
+              *reinterpret_cast<float4*>(out + (size_t)m * N + n) = make_float4(
+                  __uint_as_float(col_scaled(v.x, ra, n)),
+                  __uint_as_float(col_scaled(v.y, ra, n + 1)),
+                  __uint_as_float(col_scaled(v.z, ra, n + 2)),
+                  __uint_as_float(col_scaled(v.w, ra, n + 3)));
+            else if (out)
               *reinterpret_cast<float4*>(out + (size_t)m * N + n) =
                   make_float4((float)v.x * scale, (float)v.y * scale, (float)v.z * scale,
                               (float)v.w * scale);
@@ -482,8 +512,9 @@ template <int kKind, int BN>
 cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& mo,
                       const CUtensorMap& macc, int64_t M, int64_t N, int num_kb, int chunk_kb,
                       int splits, int num_sms, const float* sa, bool per_row_a,
-                      const float* sb, float* out, int32_t* acc_out, int32_t* split_acc,
-                      unsigned int* slab_count, unsigned int* status, cudaStream_t st) {
+                      const float* sb, bool per_col_b, float* out, int32_t* acc_out,
+                      int32_t* split_acc, unsigned int* slab_count, unsigned int* status,
+                      cudaStream_t st) {
   using C = TcCfg<BN>;
   auto kernel = gemm_tc_kernel<kKind, BN>;
   static bool attr_set[64] = {};
@@ -504,8 +535,8 @@ cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, const CUtensor
   const int grid = (int)(units < num_sms ? units : num_sms);
   cudaError_t le = launch_pdl(kernel, dim3(grid), dim3(C::kThreads), C::kSmem, st, a, b, mo,
                               macc, (int)M, (int)N, num_kb, chunk_kb, kb_per_split, splits,
-                              tiles_n, (int)units, sa, per_row_a ? 1 : 0, sb, out, acc_out,
-                              split_acc, slab_count, status);
+                              tiles_n, (int)units, sa, per_row_a ? 1 : 0, sb,
+                              per_col_b ? 1 : 0, out, acc_out, split_acc, slab_count, status);
   if (le != cudaSuccess) return le;
   return cudaGetLastError();
 }
@@ -544,13 +575,19 @@ GemmPlan plan_gemm_tc(int kind, int64_t M, int64_t N, int64_t K, int num_sms,
   if (p.chunk_kb < 1) p.chunk_kb = 1;
   if (num_sms < 1) num_sms = 1;
   const int64_t tiles_m = (M + kBM - 1) / kBM;
-  // Tile width: fewer waves of CTAs, a 256-wide tile counted as 1.6 waves of
-  // 128-wide ones (it moves less data per MMA).
+  // Tile width: fewer waves of CTAs, weighted by the measured cost of one
+  // tile relative to a 128-wide one: 1.6 for a 256-wide tile, and the same
+  // for a 96-wide one (the mainloop waits on k-block round trips, so the
+  // g_w GEMM of ViT-B qkv took 38.9 us on 144 SMs with 96-wide tiles and on
+  // 108 SMs with 128-wide ones).  A 96-wide tile is therefore taken only
+  // when it needs fewer waves, and ties leave SMs to concurrent kernels.
+  const int64_t t96 = tiles_m * ((N + 95) / 96);
   const int64_t t128 = tiles_m * ((N + 127) / 128);
   const int64_t t256 = tiles_m * ((N + 255) / 256);
+  const double w96 = (double)((t96 + num_sms - 1) / num_sms);
   const double w128 = (double)((t128 + num_sms - 1) / num_sms);
   const double w256 = (double)((t256 + num_sms - 1) / num_sms) * 1.6;
-  p.bn = (w256 <= w128) ? 256 : 128;
+  p.bn = (w256 <= w128 && w256 <= w96) ? 256 : (w96 < w128 ? 96 : 128);
   // K split: only when the tiles fill less than a third of the
   // SMs, because the int32 reduction through global atomics costs about as
   // much as the MMAs it parallelises.
@@ -569,11 +606,13 @@ cudaError_t launch_gemm_tc(int kind, const void* A, int64_t lda, const void* B,
                            int64_t ldb, int64_t M, int64_t N, int64_t K,
                            const GemmPlan& plan, const float* sa, bool per_row_a,
                            const float* sb, float* out, int32_t* acc_out,
-                           void* split_ws, unsigned int* status, cudaStream_t st) {
+                           void* split_ws, unsigned int* status, cudaStream_t st,
+                           bool per_col_b) {
   if (M == 0 || N == 0) return cudaSuccess;
   if (!get_encode()) return cudaErrorNotSupported;
   const bool bf16 = kind == 1;
-  if ((plan.bn != 128 && plan.bn != 256) || (plan.splits > 1 && kind == 0))
+  if ((plan.bn != 96 && plan.bn != 128 && plan.bn != 256) ||
+      (plan.splits > 1 && kind == 0) || (per_col_b && kind == 0))
     return cudaErrorInvalidValue;
   CUtensorMap ma, mb, mo, macc;
   if (!make_map(&ma, A, bf16, M, K, lda, kBM)) return cudaErrorInvalidValue;
@@ -589,7 +628,7 @@ cudaError_t launch_gemm_tc(int kind, const void* A, int64_t lda, const void* B,
     slab_count = reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(split_ws) +
                                                  (size_t)M * (size_t)N * 4);
     const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + plan.bn - 1) / plan.bn);
-    const int epi_warps = plan.bn / 32;
+    const int epi_warps = plan.bn > 128 ? 8 : 4;
     cudaError_t e = cudaMemsetAsync(
         split_ws, 0, (size_t)M * (size_t)N * 4 + (size_t)tiles * epi_warps * 4, st);
     if (e != cudaSuccess) return e;
@@ -601,10 +640,11 @@ cudaError_t launch_gemm_tc(int kind, const void* A, int64_t lda, const void* B,
     return cudaErrorInvalidDevice;
 #define TC(KIND, BN)                                                                  \
   launch_tc<KIND, BN>(ma, mb, mo, macc, M, N, plan.num_kb, plan.chunk_kb, plan.splits,  \
-                      sms, sa, per_row_a, sb, out, acc_out, split_acc, slab_count,      \
+                      sms, sa, per_row_a, sb, per_col_b, out, acc_out, split_acc,       \
+                      slab_count,                                                        \
                       status, st)
-  if (kind == 0) return plan.bn == 256 ? TC(0, 256) : TC(0, 128);
-  return plan.bn == 256 ? TC(1, 256) : TC(1, 128);
+  if (kind == 0) return plan.bn == 256 ? TC(0, 256) : (plan.bn == 96 ? TC(0, 96) : TC(0, 128));
+  return plan.bn == 256 ? TC(1, 256) : (plan.bn == 96 ? TC(1, 96) : TC(1, 128));
 #undef TC
 }
 

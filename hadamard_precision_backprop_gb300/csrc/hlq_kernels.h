@@ -46,10 +46,22 @@ constexpr int kHlaOutI8 = 0, kHlaOutBf16 = 1, kHlaOutI4 = 2;
 // HLA of src [T, C] along tokens -> codes [C, T*rank/16] in `out_fmt`,
 // per-tensor scale RN(amax/qmax) from *amax_slot (qmax 7 for int4, else 127).
 // out_ld: row stride of `out` in codes (>= T*rank/16).
+// per_col: one amax slot and one scale per column c of src (amax_slot[c],
+// scale[c]; the code row of channel c) instead of one for the tensor.
 cudaError_t launch_hla(const void* src, bool bf16, int64_t T, int64_t C,
                        int rank, bool amax_only, int out_fmt,
                        unsigned int* amax_slot, void* out, int64_t out_ld,
-                       float* scale, unsigned int* status, cudaStream_t st);
+                       float* scale, unsigned int* status, cudaStream_t st,
+                       bool per_col = false);
+
+// HLA along the rows of src [rows, cols]: per 16-block of a row the rank
+// lowest-sequency coefficients, per-tensor amax pass (amax_only) or int8 RNE
+// codes with s = RN(amax/127) stored as bf16 [rows, out_ld] (column
+// rank*b + k), scale[0] = s.
+cudaError_t launch_hla_rows(const void* src, bool bf16, int64_t rows, int64_t cols,
+                            int rank, bool amax_only, unsigned int* amax_slot, void* out,
+                            int64_t out_ld, float* scale, unsigned int* status,
+                            cudaStream_t st);
 
 // Transform only (fp32 coefficients), for bit-exact checks.
 cudaError_t launch_hq_rows_transform(const void* src, bool bf16, int64_t rows,
@@ -106,7 +118,8 @@ cudaError_t launch_gemm_tc(int kind, const void* A, int64_t lda, const void* B,
                            int64_t ldb, int64_t M, int64_t N, int64_t K,
                            const GemmPlan& plan, const float* sa, bool per_row_a,
                            const float* sb, float* out, int32_t* acc_out,
-                           void* split_ws, unsigned int* status, cudaStream_t st);
+                           void* split_ws, unsigned int* status, cudaStream_t st,
+                           bool per_col_b = false);  // sb[n] per column (kind 1)
 
 // The g_x path with a given workspace (the body of hlq_linear_backward_gx)
 // and the workspace it needs.

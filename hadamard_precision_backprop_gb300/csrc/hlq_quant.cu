@@ -354,7 +354,7 @@ __global__ void __launch_bounds__(256) hq_rows_kernel(
     }
     amax = warp_max(amax);
   } else {
-    amax = __uint_as_float(*amax_slot);
+    amax = __uint_as_float(ld_dep_u32(amax_slot));
   }
   const float s = __fdiv_rn(amax, 7.0f);
   if (lane == 0) {
@@ -649,7 +649,7 @@ template <bool kBf16, int kMode, int kOut, int kR>
 __global__ void __launch_bounds__(256, 2) hla_kernel(
     const void* __restrict__ src, int64_t T, int64_t C,
     unsigned int* __restrict__ amax_slot, void* __restrict__ out, int64_t out_ld,
-    float* __restrict__ scale, unsigned int* __restrict__ status) {
+    float* __restrict__ scale, unsigned int* __restrict__ status, int per_col) {
   pdl_trigger();
   pdl_wait();
   extern __shared__ __align__(16) uint8_t smem[];
@@ -665,9 +665,21 @@ __global__ void __launch_bounds__(256, 2) hla_kernel(
   const bool col_ok = c0 < C;
   const int nb = col_ok ? (int)imin64(kHlaBW, n_blk - b_first) : 0;
 
-  float s = 0.0f;
-  if (kMode == kQuant) s = __fdiv_rn(__uint_as_float(*amax_slot), ColFmt<kOut>::kQmax);
-  float amax = 0.0f;
+  // scales: one for the tensor, or (per_col) one per column of the pair
+  float sc[2] = {0.0f, 0.0f};
+  if (kMode == kQuant) {
+    if (!per_col) {
+      sc[0] = sc[1] = __fdiv_rn(__uint_as_float(ld_dep_u32(amax_slot)), F::kQmax);
+    } else if (col_ok) {
+      sc[0] = __fdiv_rn(__uint_as_float(ld_dep_u32(amax_slot + c0)), F::kQmax);
+      sc[1] = __fdiv_rn(__uint_as_float(ld_dep_u32(amax_slot + c0 + 1)), F::kQmax);
+      if (blockIdx.y == 0 && ty == 0) {
+        scale[c0] = sc[0];
+        scale[c0 + 1] = sc[1];
+      }
+    }
+  }
+  float am[2] = {0.0f, 0.0f};
   RawPairCol<kBf16> cur, nxt;
   if (nb > 0) load_pair_col<kBf16>(src, 16 * b_first * C + c0, C, cur);
 #pragma unroll 1
@@ -714,21 +726,27 @@ __global__ void __launch_bounds__(256, 2) hla_kernel(
       }
       if (kMode == kAmax) {
 #pragma unroll
-        for (int k = 0; k < kR; ++k) amax = fmaxf(amax, fabsf(coef[k]));
+        for (int k = 0; k < kR; ++k) am[c] = fmaxf(am[c], fabsf(coef[k]));
       } else {
         uint32_t p[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
 #pragma unroll
-        for (int k = 0; k < kR; ++k) pack_code<kOut>(p, k, quant_rne_f(coef[k], s, F::kQmax));
+        for (int k = 0; k < kR; ++k)
+          pack_code<kOut>(p, k, quant_rne_f(coef[k], sc[c], F::kQmax));
         store_chunk(smem + (size_t)(c * 32 + tx) * row_stride + bl * chunk, p, chunk);
       }
     }
     cur = nxt;
   }
   if (kMode == kAmax) {
-    cta_max_to_slot(amax, amax_slot);
+    if (!per_col) {
+      cta_max_to_slot(fmaxf(am[0], am[1]), amax_slot);
+    } else if (nb > 0) {
+      atomic_max_nonneg(&amax_slot[c0], am[0]);
+      atomic_max_nonneg(&amax_slot[c0 + 1], am[1]);
+    }
     return;
   }
-  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) scale[0] = s;
+  if (!per_col && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) scale[0] = sc[0];
   __syncthreads();
   // stage row r holds column tile_base + 2 * (r % 32) + r / 32
   const int64_t valid_b = imin64(kHlaBlocks, n_blk - b_cta);
@@ -770,6 +788,66 @@ __global__ void __launch_bounds__(256, 2) hla_kernel(
 }
 
 // ---------------------------------------------------------------------------
+// HLA along the rows of src [rows, cols] (blocks of 16 consecutive values of
+// a row; the ablation of the g_x path keeps the low-sequency Walsh rows of
+// g_y along Cout): the exactly rounded 16-point transform of each block as
+// in hq_rows_kernel (one warp per row, two lanes per block), the kR kept
+// coefficients in sequency order, per-tensor amax (kAmax) or RNE int8 codes
+// stored as bf16 [rows, out_ld] at column rank*b + k (kQuant).
+// ---------------------------------------------------------------------------
+template <bool kBf16, int kMode, int kR>
+__global__ void __launch_bounds__(256) hla_rows_kernel(
+    const void* __restrict__ src, int64_t rows, int64_t cols,
+    unsigned int* __restrict__ amax_slot, void* __restrict__ out, int64_t out_ld,
+    float* __restrict__ scale, unsigned int* __restrict__ status) {
+  pdl_trigger();
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int n_oct = (int)(cols >> 3);
+  const int iters = (n_oct + 31) >> 5;
+  float s = 0.0f;
+  if (kMode == kQuant) s = __fdiv_rn(__uint_as_float(ld_dep_u32(amax_slot)), 127.0f);
+  float amax = 0.0f;
+  if (row < rows) {  // warp-uniform: every lane of the warp reaches the shuffles
+    const int64_t base = row * cols;
+#pragma unroll 1
+    for (int it = 0; it < iters; ++it) {
+      const int oct = it * 32 + lane;
+      const bool valid = oct < n_oct;
+      const RawOct<kBf16> raw = load_raw<kBf16>(src, base + (int64_t)oct * 8, valid);
+      float v[8];
+      transform_raw<kBf16>(raw, v, status);  // v[k] = Y[8 * (lane & 1) + k]
+      float y[16];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float o = __shfl_xor_sync(0xffffffffu, v[k], 1);
+        y[k] = v[k];
+        y[8 + k] = o;
+      }
+      if (valid && (lane & 1) == 0) {  // the lower lane of the pair owns the block
+        if (kMode == kAmax) {
+#pragma unroll
+          for (int k = 0; k < kR; ++k) amax = fmaxf(amax, fabsf(y[sequency_row(k)]));
+        } else {
+          uint32_t p[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+#pragma unroll
+          for (int k = 0; k < kR; ++k)
+            pack_code<kColBf16>(p, k, quant_rne_f(y[sequency_row(k)], s, 127.0f));
+          const int64_t b = oct >> 1;
+          store_chunk(static_cast<uint8_t*>(out) + (row * out_ld + b * kR) * 2, p, 2 * kR);
+        }
+      }
+    }
+  }
+  if (kMode == kAmax) {
+    cta_max_to_slot(amax, amax_slot);
+  } else if (blockIdx.x == 0 && threadIdx.x == 0) {
+    scale[0] = s;
+  }
+}
+
+// ---------------------------------------------------------------------------
 // HLA through TMA-staged tiles.  A CTA owns 256 columns x kTmaBlocks
 // consecutive 16-token blocks; thread 0 starts one TMA copy per block (box
 // 16 rows x 256 columns) into its own shared-memory stage as soon as the
@@ -799,7 +877,7 @@ template <bool kBf16, int kMode, int kOut, int kR>
 __global__ void __launch_bounds__(128 * kTmaBlocks) hla_tma_kernel(
     const __grid_constant__ CUtensorMap tm, int64_t T, int64_t C,
     unsigned int* __restrict__ amax_slot, void* __restrict__ out, int64_t out_ld,
-    float* __restrict__ scale, unsigned int* __restrict__ status) {
+    float* __restrict__ scale, unsigned int* __restrict__ status, int per_col) {
   constexpr int kStage = 16 * kTmaCols * (kBf16 ? 2 : 4);
   using F = ColFmt<kOut>;
   constexpr int kChunk = kR * F::kNum / F::kDen;  // code bytes / block / column
@@ -834,9 +912,21 @@ __global__ void __launch_bounds__(128 * kTmaBlocks) hla_tma_kernel(
 
   const int64_t c0 = col0 + 2 * t;
   const bool col_ok = c0 < C;
-  float s = 0.0f;
-  if (kMode == kQuant) s = __fdiv_rn(__uint_as_float(*amax_slot), ColFmt<kOut>::kQmax);
-  float amax = 0.0f;
+  // scales: one for the tensor, or (per_col) one per column of the pair
+  float sc[2] = {0.0f, 0.0f};
+  if (kMode == kQuant) {
+    if (!per_col) {
+      sc[0] = sc[1] = __fdiv_rn(__uint_as_float(ld_dep_u32(amax_slot)), F::kQmax);
+    } else if (col_ok) {
+      sc[0] = __fdiv_rn(__uint_as_float(ld_dep_u32(amax_slot + c0)), F::kQmax);
+      sc[1] = __fdiv_rn(__uint_as_float(ld_dep_u32(amax_slot + c0 + 1)), F::kQmax);
+      if (b0 == 0 && i == 0) {
+        scale[c0] = sc[0];
+        scale[c0 + 1] = sc[1];
+      }
+    }
+  }
+  float am[2] = {0.0f, 0.0f};
   uint8_t* outb = static_cast<uint8_t*>(out);
   bool ok = true;
   if (i < nb) {
@@ -886,11 +976,12 @@ __global__ void __launch_bounds__(128 * kTmaBlocks) hla_tma_kernel(
       }
       if (kMode == kAmax) {
 #pragma unroll
-        for (int k = 0; k < kR; ++k) amax = fmaxf(amax, fabsf(coef[k]));
+        for (int k = 0; k < kR; ++k) am[c] = fmaxf(am[c], fabsf(coef[k]));
       } else {
         uint32_t p[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
 #pragma unroll
-        for (int k = 0; k < kR; ++k) pack_code<kOut>(p, k, quant_rne_f(coef[k], s, F::kQmax));
+        for (int k = 0; k < kR; ++k)
+          pack_code<kOut>(p, k, quant_rne_f(coef[k], sc[c], F::kQmax));
         store_chunk(outb + ((c0 + c) * out_ld + b * kR) * F::kNum / F::kDen, p, kChunk);
       }
     }
@@ -903,9 +994,14 @@ __global__ void __launch_bounds__(128 * kTmaBlocks) hla_tma_kernel(
     }
   }
   if (kMode == kAmax) {
-    cta_max_to_slot(amax, amax_slot);
-  } else if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
-    scale[0] = s;
+    if (!per_col) {
+      cta_max_to_slot(fmaxf(am[0], am[1]), amax_slot);
+    } else if (col_ok) {
+      atomic_max_nonneg(&amax_slot[c0], am[0]);
+      atomic_max_nonneg(&amax_slot[c0 + 1], am[1]);
+    }
+  } else if (!per_col && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
+    scale[0] = sc[0];
   }
 }
 
@@ -962,7 +1058,7 @@ __global__ void __launch_bounds__(256) hq_w_kernel(
     cta_max_to_slot(amax, amax_slot);
     return;
   }
-  const float s = __fdiv_rn(__uint_as_float(*amax_slot), 7.0f);
+  const float s = __fdiv_rn(__uint_as_float(ld_dep_u32(amax_slot)), 7.0f);
   if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) scale[0] = s;
   if (ok) {
     const PhiloxKeys keys = philox_keys(seed);
@@ -1046,7 +1142,7 @@ __global__ void __launch_bounds__(256) hq_mse_kernel(const void* __restrict__ sr
   }
   amax = warp_max(amax);
   const float st = __fdiv_rn(amax, 7.0f);
-  const float sg = __fdiv_rn(__uint_as_float(*amax_slot), 7.0f);
+  const float sg = __fdiv_rn(__uint_as_float(ld_dep_u32(amax_slot)), 7.0f);
   double et = 0.0, eg = 0.0;
   for (int it = 0; it < iters; ++it) {
     const int oct = it * 32 + lane;
@@ -1079,8 +1175,8 @@ __global__ void lqs_finalize_kernel(const double* __restrict__ sums, int64_t n,
   pdl_trigger();
   pdl_wait();
   if (threadIdx.x != 0 || blockIdx.x != 0) return;
-  const double mt = n > 0 ? sums[0] / (double)n : 0.0;
-  const double mk = n > 0 ? sums[1] / (double)n : 0.0;
+  const double mt = n > 0 ? ld_dep_f64(sums) / (double)n : 0.0;
+  const double mk = n > 0 ? ld_dep_f64(sums + 1) / (double)n : 0.0;
   mse[0] = mt;
   mse[1] = mk;
   *choice = mt > threshold * mk ? HLQ_PER_TOKEN : HLQ_PER_TENSOR;
@@ -1161,14 +1257,15 @@ __global__ void widen_i8_to_bf16_kernel(const int8_t* __restrict__ in,
   const int8_t* src = in + r * cols + c;
   __nv_bfloat16* dst = out + r * out_ld + c;
   if (c + 8 <= cols && (cols % 8) == 0) {
-    uint2 v = *reinterpret_cast<const uint2*>(src);
+    uint2 v = ld_dep_u2(src);
     const int8_t* b = reinterpret_cast<const int8_t*>(&v);
     __align__(16) __nv_bfloat16 o[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) o[k] = __int2bfloat16_rn(b[k]);
     *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(o);
   } else {
-    for (int k = 0; k < 8 && c + k < cols; ++k) dst[k] = __int2bfloat16_rn(src[k]);
+    for (int k = 0; k < 8 && c + k < cols; ++k)
+      dst[k] = __int2bfloat16_rn((int8_t)ld_dep_u8(src + k));
   }
 }
 
@@ -1245,6 +1342,34 @@ cudaError_t launch_hq_rows(const void* src, bool bf16, int64_t rows,
   return cudaGetLastError();
 }
 
+cudaError_t launch_hla_rows(const void* src, bool bf16, int64_t rows, int64_t cols,
+                            int rank, bool amax_only, unsigned int* amax_slot, void* out,
+                            int64_t out_ld, float* scale, unsigned int* status,
+                            cudaStream_t st) {
+  if (rows == 0) return cudaSuccess;
+  const dim3 grid(grid1(rows, 8));
+#define HLR(B, M, R)                                                                   \
+  launch_pdl(hla_rows_kernel<B, M, R>, grid, dim3(256), 0, st, src, rows, cols, amax_slot, \
+             out, out_ld, scale, status)
+#define HLR_RANK(B, M)                 \
+  switch (rank) {                      \
+    case 1: HLR(B, M, 1); break;       \
+    case 2: HLR(B, M, 2); break;       \
+    case 4: HLR(B, M, 4); break;       \
+    case 8: HLR(B, M, 8); break;       \
+    case 16: HLR(B, M, 16); break;     \
+    default: return cudaErrorInvalidValue; \
+  }
+  if (amax_only) {
+    if (bf16) { HLR_RANK(true, kAmax) } else { HLR_RANK(false, kAmax) }
+  } else {
+    if (bf16) { HLR_RANK(true, kQuant) } else { HLR_RANK(false, kQuant) }
+  }
+#undef HLR_RANK
+#undef HLR
+  return cudaGetLastError();
+}
+
 cudaError_t launch_hq_mse(const void* src, bool bf16, int64_t rows, int64_t cols,
                           const unsigned int* amax_slot, double* sums, double threshold,
                           double* mse, int32_t* choice, unsigned int* status,
@@ -1286,7 +1411,8 @@ cudaError_t launch_hq_cols(const void* src, bool bf16, int64_t rows,
 template <bool B, int M, int O, int R>
 static cudaError_t launch_hla_r(const void* src, int64_t T, int64_t C,
                                 unsigned int* amax_slot, void* out, int64_t out_ld,
-                                float* scale, unsigned int* status, cudaStream_t st) {
+                                float* scale, unsigned int* status, int per_col,
+                                cudaStream_t st) {
   // TMA-staged path: chunk stores of R codes need R-code-aligned rows
   using F = ColFmt<O>;
   const int chunk = R * F::kNum / F::kDen;
@@ -1300,7 +1426,7 @@ static cudaError_t launch_hla_r(const void* src, int64_t T, int64_t C,
     if (e != cudaSuccess) return e;
     dim3 grid(grid1(C, kTmaCols), grid1(T / 16, kTmaBlocks));
     launch_pdl(hla_tma_kernel<B, M, O, R>, grid, dim3(128 * kTmaBlocks), smem, st, tm, T,
-               C, amax_slot, out, out_ld, scale, status);
+               C, amax_slot, out, out_ld, scale, status, per_col);
     return cudaGetLastError();
   }
   const size_t smem = M == kAmax ? 0 : (size_t)kHlaCols * (kHlaBlocks + 1) * chunk;
@@ -1310,15 +1436,17 @@ static cudaError_t launch_hla_r(const void* src, int64_t T, int64_t C,
   }
   dim3 grid(grid1(C, kHlaCols), grid1(T / 16, kHlaBlocks));
   launch_pdl(hla_kernel<B, M, O, R>, grid, dim3(256), smem, st, src, T, C, amax_slot, out, out_ld,
-                                                  scale, status);
+             scale, status, per_col);
   return cudaGetLastError();
 }
 
 template <bool B, int M, int O>
 static cudaError_t launch_hla_o(const void* src, int64_t T, int64_t C, int rank,
                                 unsigned int* amax_slot, void* out, int64_t out_ld,
-                                float* scale, unsigned int* status, cudaStream_t st) {
-#define LHR(R) launch_hla_r<B, M, O, R>(src, T, C, amax_slot, out, out_ld, scale, status, st)
+                                float* scale, unsigned int* status, int per_col,
+                                cudaStream_t st) {
+#define LHR(R) \
+  launch_hla_r<B, M, O, R>(src, T, C, amax_slot, out, out_ld, scale, status, per_col, st)
   if constexpr (O == kColI4) {  // two codes per byte: even ranks only
     switch (rank) {
       case 2: return LHR(2);
@@ -1342,8 +1470,10 @@ static cudaError_t launch_hla_o(const void* src, int64_t T, int64_t C, int rank,
 cudaError_t launch_hla(const void* src, bool bf16, int64_t T, int64_t C,
                        int rank, bool amax_only, int out_fmt,
                        unsigned int* amax_slot, void* out, int64_t out_ld,
-                       float* scale, unsigned int* status, cudaStream_t st) {
-#define LHO(B, M, O) launch_hla_o<B, M, O>(src, T, C, rank, amax_slot, out, out_ld, scale, status, st)
+                       float* scale, unsigned int* status, cudaStream_t st, bool per_col) {
+  const int pc = per_col ? 1 : 0;
+#define LHO(B, M, O) \
+  launch_hla_o<B, M, O>(src, T, C, rank, amax_slot, out, out_ld, scale, status, pc, st)
   if (amax_only) return bf16 ? LHO(true, kAmax, kColI8) : LHO(false, kAmax, kColI8);
   if (out_fmt == kHlaOutBf16)
     return bf16 ? LHO(true, kQuant, kColBf16) : LHO(false, kQuant, kColBf16);
@@ -1393,11 +1523,11 @@ __global__ void widen_i4_to_bf16_kernel(const uint8_t* __restrict__ in,
   const uint8_t* src = in + (r * cols + c) / 2;
   __nv_bfloat16* dst = out + r * out_ld + c;
   auto code = [&](int k) {  // sign-extended nibble k of the run
-    const int v = (src[k >> 1] >> (4 * (k & 1))) & 0xf;
+    const int v = (ld_dep_u8(src + (k >> 1)) >> (4 * (k & 1))) & 0xf;
     return v >= 8 ? v - 16 : v;
   };
   if (c + 8 <= cols && (cols % 8) == 0) {
-    const uint32_t w = *reinterpret_cast<const uint32_t*>(src);
+    const uint32_t w = ld_dep_u32(reinterpret_cast<const unsigned int*>(src));
     __align__(16) __nv_bfloat16 o[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) {

@@ -70,7 +70,8 @@ typedef enum {
     HLQ_OP_BACKWARD_GW = 2,
     HLQ_OP_BACKWARD = 3, /* hlq_linear_backward: both gradients */
     HLQ_OP_SELECT_GRANULARITY = 4, /* hlq_select_gy_granularity */
-    HLQ_OP_ABLATION_GW_HQ = 5      /* hlq_ablation_gw_hq */
+    HLQ_OP_ABLATION_GW_HQ = 5,     /* hlq_ablation_gw_hq */
+    HLQ_OP_ABLATION_GX_HLA = 6     /* hlq_ablation_gx_hla */
 } hlq_op;
 
 /* Device status flags (hlq_read_device_status). */
@@ -247,7 +248,7 @@ hlq_status hlq_debug_reference_gemm(int kind, const void *d_a, const void *d_b,
  * kind 0: A, B hold E4M3 bytes of integers in [-7, 7] (the g_x GEMM);
  * kind 1: A, B hold bf16 values of integers in [-127, 127] (the g_w GEMM).
  * lda / ldb: row strides in elements (16-byte multiples).  bn: tile width
- * 128 or 256 (0 = the library's choice); splits: K split count (0 = the
+ * 96, 128 or 256 (0 = the library's choice); splits: K split count (0 = the
  * library's choice; > 1 needs d_ws of hlq_debug_tc_gemm_ws_bytes(M, N);
  * kind 0 runs unsplit).  M, N, K multiples of 16.  An unsupported plan is
  * HLQ_ERR_INVALID_ARG.
@@ -300,6 +301,28 @@ hlq_status hlq_ablation_gw_hq(const void *d_gy, const void *d_x, int dt, int64_t
                               int64_t Cin, int64_t Cout, int block, int rnd,
                               uint64_t seed, float *d_gw, int32_t *d_acc, void *d_ws,
                               size_t ws_bytes, void *stream);
+
+/*
+ * Ablation of the activation-gradient path, for numerical-error studies (HOT
+ * summary page, ablation table: internal HLA on a gradient path, the path
+ * labels read as swapped as for hlq_ablation_gw_hq, i.e. HLA on the g_x
+ * contraction; quantized with the int8 rule HLA is paired with on the g_w
+ * path): the contraction dim of g_x = g_y . w is Cout, and both operands
+ * keep the `rank` lowest-sequency Walsh rows of each 16-block of Cout,
+ *   Gb[t, r*b + k] = RN_f32( sum_j H16[sigma(k)][j] g_y[t, 16b + j] ),
+ *   Wb[i, r*b + k] = RN_f32( sum_j H16[sigma(k)][j] w[16b + j, i] ),
+ *   s = RN(amax/127) per tensor for each, RNE int8 codes,
+ *   acc[t, i] = sum_c' qG[t, c'] qW[i, c']  (exact, c' < Cout*rank/16),
+ *   g_x = acc * s_g * s_w / 16.
+ * d_gy [T, Cout], d_w [Cout, Cin] (dtype dt) -> d_gx [T, Cin] fp32; d_acc
+ * [T, Cin] int32 may be NULL (else it receives acc).  Needs
+ * Cout*rank/16 * 127^2 < 2^31.  rank in {1, 2, 4, 8, 16}.
+ * Workspace: hlq_workspace_bytes(HLQ_OP_ABLATION_GX_HLA, ..., rank).
+ */
+hlq_status hlq_ablation_gx_hla(const void *d_gy, const void *d_w, int dt, int64_t T,
+                               int64_t Cin, int64_t Cout, int block, int rank,
+                               float *d_gx, int32_t *d_acc, void *d_ws, size_t ws_bytes,
+                               void *stream);
 
 /*
  * One layer step from HOST buffers, every host<->device copy inside the

@@ -108,6 +108,9 @@ def test_gw_argument_validation(L):
     assert gw(L, bits=6) == 1                 # ACBP storage: 8 or 4 bits
     assert gw(L, bits=4, rank=1) == 4         # int4 codes pack two per byte
     assert gw(L, bits=4, T=266304) != 6       # T' * 127 * 7 < 2^31 still
+    assert gw(L, bits=8 | 0x200) == 1         # unknown format flag
+    assert gw(L, bits=8 | 0x100, ws_bytes=0) == 5   # per-channel scales: valid
+    assert gw(L, bits=4 | 0x100, rank=1) == 4
 
 
 def test_compress_argument_validation(L):
@@ -120,6 +123,12 @@ def test_compress_argument_validation(L):
     assert f(FAKE, 1, 256, 64, 16, 8, 8, FAKE, FAKE, FAKE_WS, 0, None) == 5
     assert f(FAKE, 1, 256, 64, 16, 8, 2, FAKE, FAKE, FAKE_WS, 1 << 20, None) == 1
     assert f(FAKE, 1, 256, 64, 16, 1, 4, FAKE, FAKE, FAKE_WS, 1 << 20, None) == 4
+    assert f(FAKE, 1, 256, 64, 16, 8, 8 | 0x200, FAKE, FAKE, FAKE_WS, 1 << 20, None) == 1
+    # one amax slot per channel: the workspace grows with Cin
+    need = hlq.hlq_workspace_bytes(hlq.OP_COMPRESS_ACTIVATION, 256, 4096, 16)
+    assert need >= 256 + 4096 * 4 and need % 256 == 0
+    assert f(FAKE, 1, 256, 4096, 16, 8, 8 | 0x100, FAKE, FAKE, FAKE_WS, need - 256,
+             None) == 5
 
 
 def test_tc_gemm_plan_validation(L):
@@ -133,6 +142,7 @@ def test_tc_gemm_plan_validation(L):
     assert call(kind=2) == 1
     assert call(splits=65) == 1
     assert call(kind=0, splits=2) == 1        # the E4M3 GEMM runs unsplit
+    assert call(bn=192) == 1
     assert call(M=200) == 2
 
 
@@ -199,6 +209,26 @@ def test_ablation_gw_hq_validation(L):
     assert call(T=40) == 2
     assert call(gw=FAKE + 8) == 3
     assert call(T=342400) == 6                 # 49 * T >= 2^24
+    assert call(ws_bytes=need - 256) == 5
+
+
+def test_ablation_gx_hla_validation(L):
+    f = L.hlq_ablation_gx_hla
+
+    def call(gy=FAKE, w=FAKE, T=256, Cout=128, rank=8, gx=FAKE, acc=None, ws=FAKE_WS,
+             ws_bytes=1 << 30):
+        return f(gy, w, 1, T, 64, Cout, 16, rank, gx, acc, ws, ws_bytes, None)
+
+    need = L.hlq_workspace_bytes(6, 256, 64, 128, 16, 8)
+    ld = 128 // 16 * 8                         # Cout' = 64 codes, 16-byte rows
+    assert need == 512 + 256 * ld * 2 + 64 * ld * 2
+    assert L.hlq_workspace_bytes(6, 256, 64, 128, 16, 1) == 512 + 256 * 16 + 64 * 16
+    assert call(w=None) == 1
+    assert call(rank=3) == 1
+    assert call(T=40) == 2
+    assert call(acc=FAKE + 4) == 3
+    assert call(Cout=1048576, rank=16) != 6    # Cout' * 127^2 < 2^31 still
+    assert call(Cout=16 * 65535 + 16) == 4     # over the transform grid limit
     assert call(ws_bytes=need - 256) == 5
 
 

@@ -42,7 +42,8 @@ def run(kind, A, B, bn, splits):
 @pytest.mark.parametrize("kind,qmax", [(0, 7), (1, 127)])
 @pytest.mark.parametrize("M,N,K", [(128, 128, 128), (16, 32, 16), (272, 400, 208),
                                    (384, 512, 2048), (1040, 144, 4112)])
-@pytest.mark.parametrize("bn,splits", [(128, 1), (256, 1), (128, 3), (256, 2)])
+@pytest.mark.parametrize("bn,splits", [(128, 1), (256, 1), (96, 1), (128, 3), (256, 2),
+                                       (96, 2)])
 def test_tc_gemm_exact(kind, qmax, M, N, K, bn, splits):
     rng = np.random.default_rng(M * 7 + N * 3 + K + bn + splits)
     A = rng.integers(-qmax, qmax + 1, (M, K))
