@@ -63,6 +63,9 @@ def parse_args():
     p.add_argument("--serial", action="store_true",
                    help="time the g_x and g_w branches one after the other "
                         "instead of concurrently (hlq_linear_backward)")
+    p.add_argument("--fused-gy", action="store_true",
+                   help="run the step through the fused reader of g_y "
+                        "(hlq_linear_backward(fused_gy=True))")
     p.add_argument("--no-variants", action="store_true",
                    help="skip the timings of the optional paths (int4 / "
                         "per-channel ACBP, quantizer selection, ablations)")
@@ -262,6 +265,7 @@ def config_of(wl):
             "input_dtype": wl.dtype, "block": wl.block, "rank": wl.rank,
             "gran_gy": "per-token" if wl.gran_gy else "per-tensor",
             "branches": "serial" if getattr(ARGS, "serial", False) else "overlapped",
+            "gy_reader": "fused" if getattr(ARGS, "fused_gy", False) else "separate",
             "l2": "flushed before every timed step (256 MiB write)"}
 
 
@@ -296,7 +300,7 @@ def run_ours(args, wl, rank, world, local_rank):
     x, gy, w = (t.to(dev) for t in (h_x, h_gy, h_w))
     T, Cin, Cout, Tp = wl.T, wl.Cin, wl.Cout, wl.Tp
     ws0 = hlq.workspace(hlq.OP_COMPRESS_ACTIVATION, T, Cin, Cout, 16, wl.rank, dev)
-    ws1 = hlq.workspace(hlq.OP_BACKWARD, T, Cin, Cout, 16, wl.rank, dev)
+    ws1 = hlq.workspace(hlq.OP_BACKWARD_FUSED, T, Cin, Cout, 16, wl.rank, dev)
     xbar = torch.empty((Cin, Tp), dtype=torch.int8, device=dev)
     sx = torch.empty(1, dtype=torch.float32, device=dev)
     gx = torch.empty((T, Cin), dtype=torch.float32, device=dev)
@@ -307,12 +311,13 @@ def run_ours(args, wl, rank, world, local_rank):
     def step(xx, gg, ww, overlap=None):
         # forward-time ACBP, then both gradients
         overlap = (not args.serial) if overlap is None else overlap
+        overlap = overlap or args.fused_gy   # the fused reader is one call
         hlq.hlq_compress_activation(xx, rank=wl.rank, out=xbar, scale=sx, ws=ws0)
         if overlap:   # g_w branch on a second stream inside the library
             hlq.hlq_linear_backward(gg, ww, xbar, sx, rank=wl.rank,
                                     gran_gy=wl.gran_gy, gran_w=wl.gran_w,
                                     rnd=hlq.SR, seed=wl.seed, out_gx=gx,
-                                    out_gw=gw, ws=ws1)
+                                    out_gw=gw, ws=ws1, fused_gy=args.fused_gy)
         else:
             hlq.hlq_linear_backward_gx(gg, ww, gran_gy=wl.gran_gy, gran_w=wl.gran_w,
                                        rnd=hlq.SR, seed=wl.seed, out=gx, ws=ws1)
@@ -458,6 +463,14 @@ def run_ours(args, wl, rank, world, local_rank):
                                     gran_w=wl.gran_w, rnd=hlq.SR, seed=wl.seed,
                                     out_gx=gx, out_gw=gw, ws=ws1, xbar_per_channel=True)
 
+        ws_f = hlq.workspace(hlq.OP_BACKWARD_FUSED, T, Cin, Cout, 16, wl.rank, dev)
+
+        def step_fused_gy():
+            hlq.hlq_compress_activation(x, rank=wl.rank, out=xbar, scale=sx, ws=ws0)
+            hlq.hlq_linear_backward(gy, w, xbar, sx, rank=wl.rank, gran_gy=wl.gran_gy,
+                                    gran_w=wl.gran_w, rnd=hlq.SR, seed=wl.seed,
+                                    out_gx=gx, out_gw=gw, ws=ws_f, fused_gy=True)
+
         def select():
             hlq.hlq_select_gy_granularity(gy, mse=mse, choice=choice, ws=ws_sel)
 
@@ -468,6 +481,8 @@ def run_ours(args, wl, rank, world, local_rank):
             hlq.hlq_ablation_gx_hla(gy, w, rank=wl.rank, out=gx_a, ws=ws_agx)
 
         for name, fn, what in [
+                ("fused_gy_step", step_fused_gy,
+                 "whole step with one fused reader of g_y for HQ and HLA"),
                 ("acbp_int4_step", step_int4,
                  "whole step with the stored activation as packed int4 codes"),
                 ("acbp_per_channel_step", step_per_channel,

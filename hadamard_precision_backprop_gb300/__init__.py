@@ -25,6 +25,7 @@ RNE, SR = 0, 1
 F32, BF16 = 0, 1
 OP_COMPRESS_ACTIVATION, OP_BACKWARD_GX, OP_BACKWARD_GW, OP_BACKWARD = 0, 1, 2, 3
 OP_SELECT_GRANULARITY, OP_ABLATION_GW_HQ, OP_ABLATION_GX_HLA = 4, 5, 6
+OP_BACKWARD_FUSED = 7
 XBAR_INT8, XBAR_INT4, XBAR_PER_CHANNEL = 8, 4, 0x100   # format word of the stored activation
 DEV_NONFINITE, DEV_TIMEOUT, DEV_BADCODE = 0x1, 0x2, 0x4
 
@@ -45,6 +46,7 @@ EXPORTS = [
     "hlq_select_gy_granularity",
     "hlq_ablation_gw_hq",
     "hlq_ablation_gx_hla",
+    "hlq_linear_backward_fused",
 ]
 
 _lock = threading.Lock()
@@ -101,6 +103,8 @@ def lib() -> ctypes.CDLL:
                                                      i32, i32, i32, u64, P, P]),
             "hlq_noalloc_scratch_bytes": (sz, []),
             "hlq_linear_backward": (i32, [P, P, P, P, i32, i64, i64, i64, i32, i32,
+                                          i32, i32, i32, i32, u64, P, P, P, sz, P]),
+            "hlq_linear_backward_fused": (i32, [P, P, P, P, i32, i64, i64, i64, i32, i32,
                                           i32, i32, i32, i32, u64, P, P, P, sz, P]),
             "hlq_layer_step_host": (i32, [P, P, P, i32, i64, i64, i64, i32, i32, i32,
                                           i32, i32, i32, u64, P, P, P, P, i64, P, sz, P]),
@@ -296,9 +300,12 @@ def hlq_linear_backward(g_y, w, xbar, xbar_scale, rank: int = 8,
                         gran_gy: int = PER_TOKEN, gran_w: int = PER_TENSOR,
                         rnd: int = SR, seed: int = 0, block: int = 16,
                         out_gx=None, out_gw=None, ws=None, xbar_bits: int = 8,
-                        stream=None, xbar_per_channel: bool = False):
+                        stream=None, xbar_per_channel: bool = False,
+                        fused_gy: bool = False):
     """Both gradients of the layer, the g_x and g_w branches overlapped on
-    the GPU: returns (g_x [T, Cin], g_w [Cout, Cin]) fp32."""
+    the GPU: returns (g_x [T, Cin], g_w [Cout, Cin]) fp32.  fused_gy: one
+    fused reader of g_y for both paths (hlq_linear_backward_fused; same
+    bits, workspace of OP_BACKWARD_FUSED)."""
     torch = _torch()
     _need_cuda_contig(g_y, w, xbar, xbar_scale)
     T, Cout = g_y.shape
@@ -311,13 +318,15 @@ def hlq_linear_backward(g_y, w, xbar, xbar_scale, rank: int = 8,
     if out_gw is None:
         out_gw = torch.empty((Cout, Cin), dtype=torch.float32, device=g_y.device)
     if ws is None:
-        ws = workspace(OP_BACKWARD, T, Cin, Cout, block, rank, g_y.device)
-    _check(lib().hlq_linear_backward(
+        ws = workspace(OP_BACKWARD_FUSED if fused_gy else OP_BACKWARD, T, Cin, Cout, block,
+                       rank, g_y.device)
+    fn = lib().hlq_linear_backward_fused if fused_gy else lib().hlq_linear_backward
+    _check(fn(
         _ptr(g_y), _ptr(w), _ptr(xbar), _ptr(xbar_scale), _dtype_code(g_y), T,
         Cin, Cout, block, rank, _xbar_fmt(xbar_bits, xbar_per_channel), gran_gy,
         gran_w, rnd, seed, _ptr(out_gx),
         _ptr(out_gw), _ptr(ws), ws.numel(), _stream(stream)),
-        "hlq_linear_backward")
+        "hlq_linear_backward_fused" if fused_gy else "hlq_linear_backward")
     return out_gx, out_gw
 
 

@@ -63,6 +63,17 @@ cudaError_t launch_hla_rows(const void* src, bool bf16, int64_t rows, int64_t co
                             int64_t out_ld, float* scale, unsigned int* status,
                             cudaStream_t st);
 
+// Fused reader of g_y [T, C] for both paths, one pass per call: amax_only
+// gives the HQ maxima (per row into hq_amax[T] when per_token, else one slot)
+// and the HLA maximum (hla_amax); otherwise the HQ E4M3 codes qy [T, C] with
+// scales sgy ([T] or [1]) and the HLA int8 codes as bf16 qg [C, hla_ld] with
+// scale sg[0], exactly as launch_hq_rows and launch_hla produce them.
+cudaError_t launch_gy_fused(const void* gy, bool bf16, int64_t T, int64_t C, int rank,
+                            bool per_token, bool amax_only, unsigned int* hq_amax,
+                            unsigned int* hla_amax, uint8_t* qy, float* sgy, void* qg,
+                            int64_t hla_ld, float* sg, int rnd, uint64_t seed,
+                            unsigned int* status, cudaStream_t st);
+
 // Transform only (fp32 coefficients), for bit-exact checks.
 cudaError_t launch_hq_rows_transform(const void* src, bool bf16, int64_t rows,
                                      int64_t cols, float* Y,

@@ -1006,6 +1006,230 @@ __global__ void __launch_bounds__(128 * kTmaBlocks) hla_tma_kernel(
 }
 
 // ---------------------------------------------------------------------------
+// Fused reader of g_y [T, Cout] for both gradient paths: one 16-token x
+// 256-column tile per CTA, loaded once by TMA, gives
+//   - the HQ of the tile's 16 rows (16-value blocks along Cout, the exactly
+//     rounded transform of hq_rows_kernel; thread t takes row t / 8 and the
+//     two blocks at columns 32 * (t % 8) .. of the tile), and
+//   - the HLA of its 256 columns (16-token blocks; thread t takes columns
+//     2t, 2t + 1 as hla_tma_kernel does).
+// kAmax: per-row (kPerToken, one atomicMax per row and tile into amax_rows)
+// or per-tensor HQ maxima, and the HLA maximum.  kQuant: E4M3 int4 codes of
+// the HQ (Philox SR stream 0, element t * Cout + c) with per-row or tensor
+// scales, and the HLA int8 codes as bf16 [Cout, hla_ld].  The two passes
+// replace the HQ kernel and the two HLA kernels: two reads of g_y instead
+// of three, and no transformed row staged in shared memory.
+// ---------------------------------------------------------------------------
+template <bool kBf16, int kR>
+__device__ __forceinline__ void hla_pair_col_coefs(const RawPairCol<kBf16>& cur, int c, int tier,
+                                                   uint32_t emax, float (&coef)[kR]) {
+  float xv[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) xv[j] = col_val(cur, c, j);
+  if (tier == 0) {
+    hla_fast<kR>(xv, coef);
+  } else if (tier == 1) {
+    float hi[16], lo[16], ch[kR];
+    split_high_low(xv, emax, hi, lo);
+    hla_fast<kR>(hi, coef);
+    hla_fast<kR>(lo, ch);
+#pragma unroll
+    for (int k = 0; k < kR; ++k) coef[k] += ch[k];  // exact + exact, one rounding
+  } else {
+    float in[16], o[16];  // rare: local memory for the out-of-line call
+#pragma unroll
+    for (int j = 0; j < 16; ++j) in[j] = xv[j];
+    slow_block16(in, o, kBf16 ? 1 : 0);
+#pragma unroll
+    for (int k = 0; k < kR; ++k) coef[k] = o[sequency_row(k)];
+  }
+}
+
+template <bool kBf16>
+__device__ __forceinline__ void pair_tiers(const RawPairCol<kBf16>& cur, int (&tier)[2],
+                                           uint32_t (&emax)[2], unsigned int* status) {
+  if constexpr (kBf16) {
+    pair_col_tiers_bf16(cur.p, tier, emax, status);
+  } else {
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      ExpRange er = exp_range_init();
+#pragma unroll
+      for (int j = 0; j < 16; ++j) exp_range_add(er, col_val(cur, c, j));
+      if (any_nonfinite(er)) raise_flag(status, HLQ_DEV_NONFINITE);
+      tier[c] = butterfly_exact<false>(er) ? 0 : 2;
+      emax[c] = er.emax;
+    }
+  }
+}
+
+// The 32 consecutive values of one tile row starting at column x0, as the
+// "pair" form of two 16-value blocks (low half / .x = block at x0, high
+// half / .y = block at x0 + 16), value j of each block in word j.
+template <bool kBf16>
+__device__ __forceinline__ void read_row_blocks(const uint8_t* stage, int row, int x0,
+                                                RawPairCol<kBf16>& r) {
+  if constexpr (kBf16) {
+    const uint4* q = reinterpret_cast<const uint4*>(stage + (row * kTmaCols + x0) * 2);
+    uint32_t w[16];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 a = q[i];
+      w[4 * i] = a.x; w[4 * i + 1] = a.y; w[4 * i + 2] = a.z; w[4 * i + 3] = a.w;
+    }
+#pragma unroll
+    for (int j = 0; j < 16; j += 2) {
+      r.p[j] = __byte_perm(w[j / 2], w[8 + j / 2], 0x5410);      // even columns
+      r.p[j + 1] = __byte_perm(w[j / 2], w[8 + j / 2], 0x7632);  // odd columns
+    }
+  } else {
+    const float4* q = reinterpret_cast<const float4*>(stage + (row * kTmaCols + x0) * 4);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float4 a = q[i], b = q[4 + i];
+      r.p[4 * i] = make_float2(a.x, b.x);
+      r.p[4 * i + 1] = make_float2(a.y, b.y);
+      r.p[4 * i + 2] = make_float2(a.z, b.z);
+      r.p[4 * i + 3] = make_float2(a.w, b.w);
+    }
+  }
+}
+
+template <bool kBf16, int kMode, bool kPerToken, int kR>
+__global__ void __launch_bounds__(128) gy_fused_kernel(
+    const __grid_constant__ CUtensorMap tm, int64_t T, int64_t C,
+    unsigned int* __restrict__ hq_amax, unsigned int* __restrict__ hla_amax,
+    uint8_t* __restrict__ qy, float* __restrict__ sgy, void* __restrict__ qg,
+    int64_t hla_ld, float* __restrict__ sg, int rnd, uint64_t seed,
+    unsigned int* __restrict__ status) {
+  constexpr int kStage = 16 * kTmaCols * (kBf16 ? 2 : 4);
+  using F = ColFmt<kColBf16>;
+  constexpr int kChunk = kR * 2;  // bf16 code bytes per block and column
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStage);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(full + 1);
+  __shared__ float partial[2][4];
+
+  const int t = threadIdx.x;
+  const int64_t n_cc = (C + kTmaCols - 1) / kTmaCols;
+  const int64_t u = blockIdx.x;
+  const int64_t col0 = (u % n_cc) * kTmaCols, b = u / n_cc;
+  pdl_trigger();
+  if (t == 0) {
+    mbar_init(full, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  pdl_wait();  // g_y and the amax slots come from earlier work
+  if (t == 0) {
+    mbar_expect_tx(full, kStage);
+    tma_load_2d(smem, &tm, full, (int)col0, (int)(16 * b));
+  }
+  __syncthreads();
+  // scales of the quant pass
+  const int hq_row = t >> 3;                  // 0..15
+  const int64_t tok = 16 * b + hq_row;
+  const int x0 = 32 * (t & 7);                // first column of the pair of blocks
+  float s_hla = 0.0f, s_hq = 0.0f;
+  if (kMode == kQuant) {
+    s_hla = __fdiv_rn(__uint_as_float(ld_dep_u32(hla_amax)), F::kQmax);
+    s_hq = __fdiv_rn(__uint_as_float(ld_dep_u32(kPerToken ? hq_amax + tok : hq_amax)), 7.0f);
+  }
+  const bool ok = mbar_wait(full, 0u, abort_flag, status);
+  float am_hla = 0.0f, am_hq = 0.0f;
+  // ---- HLA: column pair t ----
+  const int64_t c0 = col0 + 2 * t;
+  if (ok && c0 < C) {
+    RawPairCol<kBf16> cur;
+    read_pair_col<kBf16>(smem, t, cur);
+    int tier[2];
+    uint32_t emax[2];
+    pair_tiers<kBf16>(cur, tier, emax, status);
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      float coef[kR];
+      hla_pair_col_coefs<kBf16, kR>(cur, c, tier[c], emax[c], coef);
+      if (kMode == kAmax) {
+#pragma unroll
+        for (int k = 0; k < kR; ++k) am_hla = fmaxf(am_hla, fabsf(coef[k]));
+      } else {
+        uint32_t p[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+#pragma unroll
+        for (int k = 0; k < kR; ++k)
+          pack_code<kColBf16>(p, k, quant_rne_f(coef[k], s_hla, F::kQmax));
+        store_chunk(static_cast<uint8_t*>(qg) + ((c0 + c) * hla_ld + b * kR) * 2, p, kChunk);
+      }
+    }
+  }
+  // ---- HQ: row hq_row, blocks at columns x0 and x0 + 16 of the tile ----
+  const int64_t cb = col0 + x0;
+  const bool blk_ok[2] = {cb < C, cb + 16 < C};
+  if (ok && blk_ok[0]) {
+    RawPairCol<kBf16> cur;
+    read_row_blocks<kBf16>(smem, hq_row, x0, cur);
+    int tier[2];
+    uint32_t emax[2];
+    pair_tiers<kBf16>(cur, tier, emax, status);
+    float v[2][16];
+    unpack_pair_col<kBf16>(cur, v);
+    column_butterfly<kBf16>(v[0], tier[0], emax[0], 16, true);
+    column_butterfly<kBf16>(v[1], tier[1], emax[1], 16, true);
+    if (kMode == kAmax) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        am_hq = fmaxf(am_hq, fabsf(v[0][i]));
+        if (blk_ok[1]) am_hq = fmaxf(am_hq, fabsf(v[1][i]));
+      }
+    } else {
+      const PhiloxKeys keys = philox_keys(seed);
+      const int64_t e = tok * C + cb;
+      quantize_octet(v[0], s_hq, rnd, keys, 0u, e, 0, qy);
+      quantize_octet(v[0] + 8, s_hq, rnd, keys, 0u, e + 8, 0, qy);
+      if (blk_ok[1]) {
+        quantize_octet(v[1], s_hq, rnd, keys, 0u, e + 16, 0, qy);
+        quantize_octet(v[1] + 8, s_hq, rnd, keys, 0u, e + 24, 0, qy);
+      }
+    }
+  }
+  if (t == 0 && *abort_flag) {  // let the copy land before exit
+    const unsigned long long t0 = now_ns();
+    while (!mbar_test(full, 0u) && now_ns() - t0 < kWaitNs) {
+    }
+  }
+  if (kMode == kAmax) {
+    if (kPerToken) {  // the 8 threads of a row are consecutive lanes
+      am_hq = fmaxf(am_hq, __shfl_xor_sync(0xffffffffu, am_hq, 1));
+      am_hq = fmaxf(am_hq, __shfl_xor_sync(0xffffffffu, am_hq, 2));
+      am_hq = fmaxf(am_hq, __shfl_xor_sync(0xffffffffu, am_hq, 4));
+      if ((t & 7) == 0 && tok < T) atomic_max_nonneg(hq_amax + tok, am_hq);
+    }
+    am_hla = warp_max(am_hla);
+    if (!kPerToken) am_hq = warp_max(am_hq);
+    if ((t & 31) == 0) {
+      partial[0][t >> 5] = am_hla;
+      partial[1][t >> 5] = am_hq;
+    }
+    __syncthreads();
+    if (t == 0) {
+      atomic_max_nonneg(hla_amax, fmaxf(fmaxf(partial[0][0], partial[0][1]),
+                                        fmaxf(partial[0][2], partial[0][3])));
+      if (!kPerToken)
+        atomic_max_nonneg(hq_amax, fmaxf(fmaxf(partial[1][0], partial[1][1]),
+                                         fmaxf(partial[1][2], partial[1][3])));
+    }
+  } else {
+    if (u == 0 && t == 0) {
+      sg[0] = s_hla;
+      if (!kPerToken) sgy[0] = s_hq;
+    }
+    if (kPerToken && col0 == 0 && (t & 7) == 0 && tok < T) sgy[tok] = s_hq;
+  }
+}
+
+// ---------------------------------------------------------------------------
 // HQ of w [Cout, Cin] along Cout (blocks of 16 rows), codes written
 // transposed [Cin, Cout].  w is small next to g_y, so the kernel trades
 // redundant transforms for parallelism: thread (tx, ty) owns column pair tx
@@ -1480,6 +1704,49 @@ cudaError_t launch_hla(const void* src, bool bf16, int64_t T, int64_t C,
   if (out_fmt == kHlaOutI4) return bf16 ? LHO(true, kQuant, kColI4) : LHO(false, kQuant, kColI4);
   return bf16 ? LHO(true, kQuant, kColI8) : LHO(false, kQuant, kColI8);
 #undef LHO
+}
+
+cudaError_t launch_gy_fused(const void* gy, bool bf16, int64_t T, int64_t C, int rank,
+                            bool per_token, bool amax_only, unsigned int* hq_amax,
+                            unsigned int* hla_amax, uint8_t* qy, float* sgy, void* qg,
+                            int64_t hla_ld, float* sg, int rnd, uint64_t seed,
+                            unsigned int* status, cudaStream_t st) {
+  if (T == 0 || C == 0) return cudaSuccess;
+  CUtensorMap tm;
+  if (!make_tile_map_2d(&tm, gy, bf16, T, C, kTmaCols, 16)) return cudaErrorInvalidValue;
+  const size_t smem = 128 + (size_t)16 * kTmaCols * (bf16 ? 2 : 4) + 8 + 16;
+  const int64_t tiles = (int64_t)grid1(C, kTmaCols) * (T / 16);
+#define GYF(B, M, P, R)                                                                  \
+  do {                                                                                   \
+    cudaError_t e = ensure_smem_limit<gy_fused_kernel<B, M, P, R>>(smem);                \
+    if (e != cudaSuccess) return e;                                                      \
+    launch_pdl(gy_fused_kernel<B, M, P, R>, dim3((unsigned)tiles), dim3(128), smem, st, tm, \
+               T, C, hq_amax, hla_amax, qy, sgy, qg, hla_ld, sg, rnd, seed, status);     \
+  } while (0)
+#define GYF_R(B, M, P)                         \
+  switch (rank) {                              \
+    case 1: GYF(B, M, P, 1); break;            \
+    case 2: GYF(B, M, P, 2); break;            \
+    case 4: GYF(B, M, P, 4); break;            \
+    case 8: GYF(B, M, P, 8); break;            \
+    case 16: GYF(B, M, P, 16); break;          \
+    default: return cudaErrorInvalidValue;     \
+  }
+#define GYF_P(B, M)                            \
+  if (per_token) {                             \
+    GYF_R(B, M, true)                          \
+  } else {                                     \
+    GYF_R(B, M, false)                         \
+  }
+  if (amax_only) {
+    if (bf16) { GYF_P(true, kAmax) } else { GYF_P(false, kAmax) }
+  } else {
+    if (bf16) { GYF_P(true, kQuant) } else { GYF_P(false, kQuant) }
+  }
+#undef GYF_P
+#undef GYF_R
+#undef GYF
+  return cudaGetLastError();
 }
 
 cudaError_t launch_hq_rows_transform(const void* src, bool bf16, int64_t rows,

@@ -71,7 +71,8 @@ typedef enum {
     HLQ_OP_BACKWARD = 3, /* hlq_linear_backward: both gradients */
     HLQ_OP_SELECT_GRANULARITY = 4, /* hlq_select_gy_granularity */
     HLQ_OP_ABLATION_GW_HQ = 5,     /* hlq_ablation_gw_hq */
-    HLQ_OP_ABLATION_GX_HLA = 6     /* hlq_ablation_gx_hla */
+    HLQ_OP_ABLATION_GX_HLA = 6,    /* hlq_ablation_gx_hla */
+    HLQ_OP_BACKWARD_FUSED = 7      /* hlq_linear_backward_fused */
 } hlq_op;
 
 /* Device status flags (hlq_read_device_status). */
@@ -178,6 +179,26 @@ hlq_status hlq_linear_backward(const void *d_gy, const void *d_w, const int8_t *
                                int xbar_fmt, int gran_gy, int gran_w, int rnd, uint64_t seed,
                                float *d_gx, float *d_gw, void *d_ws, size_t ws_bytes,
                                void *stream);
+
+/*
+ * hlq_linear_backward with one fused reader of g_y for both paths: a first
+ * pass over g_y takes the HQ maxima (per token or per tensor) and the HLA
+ * maximum, a second writes the HQ int4 codes and the HLA int8 codes, each
+ * from one TMA-staged 16-token x 256-column tile of g_y per CTA (two full
+ * reads of g_y instead of three).  The HQ of w and the widening of the
+ * stored activation run on library streams meanwhile; the two GEMMs follow
+ * on `stream`.  Every output bit equals hlq_linear_backward's.
+ * Arguments as for hlq_linear_backward; workspace
+ * hlq_workspace_bytes(HLQ_OP_BACKWARD_FUSED, ...) (that of HLQ_OP_BACKWARD
+ * plus one amax slot per token).
+ */
+hlq_status hlq_linear_backward_fused(const void *d_gy, const void *d_w,
+                                     const int8_t *d_xbar, const float *d_xbar_scale,
+                                     int dt, int64_t T, int64_t Cin, int64_t Cout,
+                                     int block, int rank, int xbar_fmt, int gran_gy,
+                                     int gran_w, int rnd, uint64_t seed, float *d_gx,
+                                     float *d_gw, void *d_ws, size_t ws_bytes,
+                                     void *stream);
 
 /*
  * hlq_linear_backward_gx with its intermediates copied out, for bit-exact

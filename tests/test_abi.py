@@ -46,7 +46,7 @@ def test_workspace_sizes(L):
     # g_x workspace holds one byte per int4 code of g_y and of w
     n = hlq.hlq_workspace_bytes(1, 256, 64, 128)
     assert n >= 256 * 128 + 64 * 128
-    assert hlq.hlq_workspace_bytes(7, 16, 16, 16) == 0
+    assert hlq.hlq_workspace_bytes(8, 16, 16, 16) == 0          # unknown op
     assert hlq.hlq_workspace_bytes(1, -16, 16, 16) == 0
 
 
@@ -230,6 +230,22 @@ def test_ablation_gx_hla_validation(L):
     assert call(Cout=1048576, rank=16) != 6    # Cout' * 127^2 < 2^31 still
     assert call(Cout=16 * 65535 + 16) == 4     # over the transform grid limit
     assert call(ws_bytes=need - 256) == 5
+
+
+def test_fused_backward_workspace_and_validation(L):
+    f = L.hlq_linear_backward_fused
+    T, Cin, Cout = 256, 64, 128
+    need = L.hlq_workspace_bytes(7, T, Cin, Cout, 16, 8)
+    assert need == L.hlq_workspace_bytes(3, T, Cin, Cout, 16, 8) + T * 4
+    args = [FAKE, FAKE, FAKE, FAKE, 1, T, Cin, Cout, 16, 8, 8, 1, 0, 1, 0, FAKE, FAKE,
+            FAKE_WS]
+    assert f(*args, need - 256, None) == 5
+    bad = list(args)
+    bad[8] = 8                                # block
+    assert f(*bad, need, None) == 1
+    bad = list(args)
+    bad[12] = 1                               # per-token w
+    assert f(*bad, need, None) == 4
 
 
 def test_read_status_rejects_null(L):
