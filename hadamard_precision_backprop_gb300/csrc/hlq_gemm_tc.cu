@@ -140,6 +140,7 @@ template <int kKind, int BN>
 __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(
     const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
     const __grid_constant__ CUtensorMap tmOut, const __grid_constant__ CUtensorMap tmAcc,
+    const __grid_constant__ CUtensorMap tmSplit,
     int M, int N, int num_kb, int chunk_kb, int kb_per_split, int splits, int tiles_n,
     int num_units, const float* __restrict__ sa, int per_row_a,
     const float* __restrict__ sb, int per_col_b, float* __restrict__ out,
@@ -281,7 +282,8 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(
     // through the warp's staging buffer (128B swizzle: 16-byte chunk c of row
     // r at c ^ (r % 8), conflict-free) and a TMA store, which clips rows >= M
     // and columns >= N.
-    auto store_box = [&](const CUtensorMap* map, int x, int y, const uint32_t (&v)[32]) {
+    auto store_box = [&](const CUtensorMap* map, int x, int y, const uint32_t (&v)[32],
+                         bool reduce_add = false) {
       if (lane == 0) tma_store_wait_read();  // the previous box has been read
       __syncwarp();
 #pragma unroll
@@ -290,7 +292,12 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(
             make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) tma_store_2d(map, x, y, stg);
+      if (lane == 0) {
+        if (reduce_add)
+          tma_reduce_add_2d(map, x, y, stg);
+        else
+          tma_store_2d(map, x, y, stg);
+      }
     };
     auto dequant_scale = [&](int m) {
       return (out && m < M) ? ld_dep_f32(sa + (per_row_a ? m : 0)) * ld_dep_f32(sb) * 0.0625f
@@ -403,42 +410,60 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(
         }
         continue;
       }
-      // split unit: add the exact partial; the warp that completes a slab
-      // (its 32 rows x kColsPerThread columns) last dequantizes it
-      if (m < M) {
+      // split unit: add the exact partial into split_acc with TMA reduce-add
+      // boxes (32 rows x 32 columns, coalesced in L2); the warp that
+      // completes a slab (its 32 rows x kColsPerThread columns) last reads
+      // the sum back and stores it dequantized
 #pragma unroll
-        for (int q = 0; q < C::kColsPerThread; ++q)
-          if (nb + q < N) atomicAdd(&split_acc[(size_t)m * N + nb + q], acc[q]);
+      for (int jc = 0; jc < C::kColsPerThread / 32; ++jc) {
+        const int x = nb + 32 * jc;
+        if (x >= N) break;
+        uint32_t v[32];
+#pragma unroll
+        for (int q = 0; q < 32; ++q) v[q] = (uint32_t)acc[32 * jc + q];
+        store_box(&tmSplit, x, y, v, true);
       }
-      __threadfence();
-      __syncwarp();
       unsigned int last = 0;
       if (lane == 0) {
+        tma_store_wait_all();  // the reductions are performed
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        __threadfence();
         const int t = u / splits;
         last = atomicAdd(&slab_count[(size_t)t * C::kEpiWarps + ew], 1u) ==
                (unsigned int)(splits - 1);
+        if (last) __threadfence();
       }
       last = __shfl_sync(0xffffffffu, last, 0);
-      if (last && m < M) {
-        __threadfence();
-        const float scale =
-            out ? ld_dep_f32(sa + (per_row_a ? m : 0)) * ld_dep_f32(sb) * 0.0625f : 0.0f;
+      if (last) {
+        const float scale = dequant_scale(m);
         const float ra = row_scale_a(m);
-        for (int q = 0; q < C::kColsPerThread; q += 4) {
-          const int n = nb + q;
-          if (n + 4 <= N) {
-            const int4 v = __ldcg(reinterpret_cast<const int4*>(split_acc + (size_t)m * N + n));
-            if (out && per_col_b)
-              *reinterpret_cast<float4*>(out + (size_t)m * N + n) = make_float4(
-                  __uint_as_float(col_scaled(v.x, ra, n)),
-                  __uint_as_float(col_scaled(v.y, ra, n + 1)),
-                  __uint_as_float(col_scaled(v.z, ra, n + 2)),
-                  __uint_as_float(col_scaled(v.w, ra, n + 3)));
-            else if (out)
-              *reinterpret_cast<float4*>(out + (size_t)m * N + n) =
-                  make_float4((float)v.x * scale, (float)v.y * scale, (float)v.z * scale,
-                              (float)v.w * scale);
-            if (acc_out) *reinterpret_cast<int4*>(acc_out + (size_t)m * N + n) = v;
+#pragma unroll
+        for (int jc = 0; jc < C::kColsPerThread / 32; ++jc) {
+          const int x = nb + 32 * jc;
+          if (x >= N) break;
+          int32_t sum[32];
+          const int32_t* row = split_acc + (size_t)m * N + x;
+#pragma unroll
+          for (int q = 0; q < 32; q += 4) {
+            int4 w4 = make_int4(0, 0, 0, 0);
+            if (m < M && x + q < N) w4 = __ldcg(reinterpret_cast<const int4*>(row + q));
+            sum[q] = w4.x; sum[q + 1] = w4.y; sum[q + 2] = w4.z; sum[q + 3] = w4.w;
+          }
+          uint32_t v[32];
+          if (acc_out) {
+#pragma unroll
+            for (int q = 0; q < 32; ++q) v[q] = (uint32_t)sum[q];
+            store_box(&tmAcc, x, y, v);
+          }
+          if (out) {
+            if (per_col_b) {
+#pragma unroll
+              for (int q = 0; q < 32; ++q) v[q] = col_scaled(sum[q], ra, x + q);
+            } else {
+#pragma unroll
+              for (int q = 0; q < 32; ++q) v[q] = __float_as_uint((float)sum[q] * scale);
+            }
+            store_box(&tmOut, x, y, v);
           }
         }
       }
@@ -510,7 +535,8 @@ bool make_out_map(CUtensorMap* map, const void* ptr, bool is_int, int64_t rows,
 
 template <int kKind, int BN>
 cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& mo,
-                      const CUtensorMap& macc, int64_t M, int64_t N, int num_kb, int chunk_kb,
+                      const CUtensorMap& macc, const CUtensorMap& msplit, int64_t M, int64_t N,
+                      int num_kb, int chunk_kb,
                       int splits, int num_sms, const float* sa, bool per_row_a,
                       const float* sb, bool per_col_b, float* out, int32_t* acc_out,
                       int32_t* split_acc, unsigned int* slab_count, unsigned int* status,
@@ -534,7 +560,7 @@ cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, const CUtensor
   if (units > 0x7fffffff) return cudaErrorInvalidValue;
   const int grid = (int)(units < num_sms ? units : num_sms);
   cudaError_t le = launch_pdl(kernel, dim3(grid), dim3(C::kThreads), C::kSmem, st, a, b, mo,
-                              macc, (int)M, (int)N, num_kb, chunk_kb, kb_per_split, splits,
+                              macc, msplit, (int)M, (int)N, num_kb, chunk_kb, kb_per_split, splits,
                               tiles_n, (int)units, sa, per_row_a ? 1 : 0, sb,
                               per_col_b ? 1 : 0, out, acc_out, split_acc, slab_count, status);
   if (le != cudaSuccess) return le;
@@ -588,9 +614,12 @@ GemmPlan plan_gemm_tc(int kind, int64_t M, int64_t N, int64_t K, int num_sms,
   const double w128 = (double)((t128 + num_sms - 1) / num_sms);
   const double w256 = (double)((t256 + num_sms - 1) / num_sms) * 1.6;
   p.bn = (w256 <= w128 && w256 <= w96) ? 256 : (w96 < w128 ? 96 : 128);
-  // K split: only when the tiles fill less than a third of the
-  // SMs, because the int32 reduction through global atomics costs about as
-  // much as the MMAs it parallelises.
+  // K split: only when the tiles fill less than a third of the SMs.  The
+  // partial sums are added in L2 by TMA reduce-add boxes (ResNet-50 im2col
+  // g_w, 36 tiles x 4 splits: 59 us, against 111 us with per-element
+  // atomics), but a split still costs a memset, the reductions and a
+  // read-back, and for the ViT-B qkv g_w GEMM 256-wide tiles x 2 splits took
+  // 48 us against 39 us unsplit.
   p.splits = 1;
   if (max_splits > 1 && t128 * 3 < num_sms) {
     p.bn = 128;
@@ -614,17 +643,19 @@ cudaError_t launch_gemm_tc(int kind, const void* A, int64_t lda, const void* B,
   if ((plan.bn != 96 && plan.bn != 128 && plan.bn != 256) ||
       (plan.splits > 1 && kind == 0) || (per_col_b && kind == 0))
     return cudaErrorInvalidValue;
-  CUtensorMap ma, mb, mo, macc;
+  CUtensorMap ma, mb, mo, macc, msplit;
   if (!make_map(&ma, A, bf16, M, K, lda, kBM)) return cudaErrorInvalidValue;
   if (!make_map(&mb, B, bf16, N, K, ldb, plan.bn)) return cudaErrorInvalidValue;
   memset(&mo, 0, sizeof(mo));
   memset(&macc, 0, sizeof(macc));
+  memset(&msplit, 0, sizeof(msplit));
   if (out && !make_out_map(&mo, out, false, M, N)) return cudaErrorInvalidValue;
   if (acc_out && !make_out_map(&macc, acc_out, true, M, N)) return cudaErrorInvalidValue;
   int32_t* split_acc = nullptr;
   unsigned int* slab_count = nullptr;
   if (plan.splits > 1) {
     split_acc = static_cast<int32_t*>(split_ws);
+    if (!make_out_map(&msplit, split_acc, true, M, N)) return cudaErrorInvalidValue;
     slab_count = reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(split_ws) +
                                                  (size_t)M * (size_t)N * 4);
     const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + plan.bn - 1) / plan.bn);
@@ -639,7 +670,8 @@ cudaError_t launch_gemm_tc(int kind, const void* A, int64_t lda, const void* B,
       sms <= 0)
     return cudaErrorInvalidDevice;
 #define TC(KIND, BN)                                                                  \
-  launch_tc<KIND, BN>(ma, mb, mo, macc, M, N, plan.num_kb, plan.chunk_kb, plan.splits,  \
+  launch_tc<KIND, BN>(ma, mb, mo, macc, msplit, M, N, plan.num_kb, plan.chunk_kb,         \
+                      plan.splits,                                                       \
                       sms, sa, per_row_a, sb, per_col_b, out, acc_out, split_acc,       \
                       slab_count,                                                        \
                       status, st)

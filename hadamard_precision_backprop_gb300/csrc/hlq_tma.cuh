@@ -88,6 +88,17 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int x, int 
       : "memory");
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
+// Tiled reduce-add of a shared-memory box into global memory (element type
+// of the tensor map, here s32), the same bulk-group completion as the store.
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, int x, int y,
+                                                  const void* src) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group"
+      " [%0, {%1, %2}], [%3];" ::"l"(reinterpret_cast<uint64_t>(map)),
+      "r"(x), "r"(y), "r"(saddr(src))
+      : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
 __device__ __forceinline__ void tma_store_wait_read() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
