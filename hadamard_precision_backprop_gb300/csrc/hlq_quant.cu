@@ -1231,18 +1231,139 @@ __global__ void __launch_bounds__(128) gy_fused_kernel(
 
 // ---------------------------------------------------------------------------
 // HQ of w [Cout, Cin] along Cout (blocks of 16 rows), codes written
-// transposed [Cin, Cout].  w is small next to g_y, so the kernel trades
-// redundant transforms for parallelism: thread (tx, ty) owns column pair tx
-// (64 columns per CTA), block ty / 2 (4 blocks per CTA) and quantizes half
-// of its 16 coefficients (ty % 2), drawing one Philox block per coefficient
-// row for the pair.
+// transposed [Cin, Cout] (also the along-token HQ of the g_w ablation, with
+// rows = tokens).  Thread = (column quad, 16-row block): it loads the 16 x 4
+// values (8 or 16 bytes per row; consecutive threads take consecutive quads,
+// so a warp reads 256 or 512 contiguous bytes per row), transforms the four
+// columns, and quantizes coefficient row i of the quad with the one Philox
+// block that covers elements (16b + i) * cols + 4q .. + 3; each column's 16
+// codes leave as one 16-byte store into its row of the transposed output.
 // ---------------------------------------------------------------------------
+template <bool kBf16>
+struct RawQuad;
+template <>
+struct RawQuad<true> {
+  RawPairCol<true> lo, hi;  // columns 0, 1 and 2, 3
+};
+template <>
+struct RawQuad<false> {
+  RawPairCol<false> lo, hi;
+};
+
+template <bool kBf16>
+__device__ __forceinline__ void load_quad_col(const void* src, int64_t idx, int64_t ld,
+                                              RawQuad<kBf16>& r) {
+  if constexpr (kBf16) {
+    const uint16_t* p = static_cast<const uint16_t*>(src) + idx;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const uint2 w = __ldg(reinterpret_cast<const uint2*>(p + j * ld));
+      r.lo.p[j] = w.x;
+      r.hi.p[j] = w.y;
+    }
+  } else {
+    const float* p = static_cast<const float*>(src) + idx;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const float4 w = __ldg(reinterpret_cast<const float4*>(p + j * ld));
+      r.lo.p[j] = make_float2(w.x, w.y);
+      r.hi.p[j] = make_float2(w.z, w.w);
+    }
+  }
+}
+
+// All 16 exactly rounded coefficients (Sylvester order) of the two columns
+// of a pair, given their tiers.
+template <bool kBf16>
+__device__ __forceinline__ void pair_full_coefs(const RawPairCol<kBf16>& r, float (*v)[16],
+                                                unsigned int* status) {
+  if constexpr (kBf16) {
+    int tier[2];
+    uint32_t emax[2];
+    pair_col_tiers_bf16(r.p, tier, emax, status);
+    unpack_pair_col<kBf16>(r, v);
+    column_butterfly<kBf16>(v[0], tier[0], emax[0], 16, true);
+    column_butterfly<kBf16>(v[1], tier[1], emax[1], 16, true);
+  } else {
+    unpack_pair_col<kBf16>(r, v);
+    column_coeffs<kBf16>(v[0], 16, true, status);
+    column_coeffs<kBf16>(v[1], 16, true, status);
+  }
+}
+
+template <bool kBf16, int kMode>
+__global__ void __launch_bounds__(128) hq_w_kernel(
+    const void* __restrict__ src, int64_t rows, int64_t cols,
+    unsigned int* __restrict__ amax_slot, uint8_t* __restrict__ codes_t,
+    float* __restrict__ scale, int rnd, uint64_t seed, uint32_t stream,
+    unsigned int* __restrict__ status) {
+  pdl_trigger();
+  pdl_wait();
+  const int64_t n_q = cols >> 2, n_blk = rows >> 4;
+  const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const bool ok = idx < n_q * n_blk;
+  const int64_t q = ok ? idx % n_q : 0, b = ok ? idx / n_q : 0;
+  float v[4][16];
+  if (ok) {
+    RawQuad<kBf16> raw;
+    load_quad_col<kBf16>(src, 16 * b * cols + 4 * q, cols, raw);
+    pair_full_coefs<kBf16>(raw.lo, v, status);
+    pair_full_coefs<kBf16>(raw.hi, v + 2, status);
+  }
+  if (kMode == kAmax) {
+    float amax = 0.0f;
+    if (ok) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[c][i]));
+    }
+    cta_max_to_slot(amax, amax_slot);
+    return;
+  }
+  const float s = __fdiv_rn(__uint_as_float(ld_dep_u32(amax_slot)), 7.0f);
+  if (blockIdx.x == 0 && threadIdx.x == 0) scale[0] = s;
+  if (!ok) return;
+  const PhiloxKeys keys = philox_keys(seed);
+  uint32_t w[4][4] = {};  // column c's 16 code bytes (code i in byte i)
+#pragma unroll
+  for (int i = 0; i < 16; i += 2) {
+    float qv[2][4];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      // elements (16b + i + u) * cols + 4q + c of the transformed tensor
+      const uint64_t e = (uint64_t)((16 * b + i + u) * cols + 4 * q);
+      U4 r = {0u, 0u, 0u, 0u};
+      if (rnd == HLQ_SR) r = philox_block_k(keys, stream, e >> 2);
+      const uint32_t wd[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        qv[u][c] = rnd == HLQ_SR ? quant_sr_f(v[c][i + u], s, wd[c], 7.0f)
+                                 : quant_rne_f(v[c][i + u], s, 7.0f);
+    }
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      w[c][i >> 2] |= e4m3x2(qv[0][c], qv[1][c]) << (16 * ((i >> 1) & 1));
+  }
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+    *reinterpret_cast<uint4*>(codes_t + (4 * q + c) * rows + 16 * b) =
+        make_uint4(w[c][0], w[c][1], w[c][2], w[c][3]);
+}
+
+// The same HQ with two threads per column pair and block (each transforms
+// the pair and quantizes half of its 16 rows, drawing a Philox block per
+// row for the pair): twice the transforms and random words of the quad
+// kernel, but eight times its threads, which is what a small tensor (the w
+// of a ViT-B layer) needs to fill the GPU: thread (tx, ty) owns column pair
+// tx (64 columns per CTA) and block ty / 2 (4 blocks per CTA); the
+// transposed codes leave through shared memory in 8-byte chunks.
 constexpr int kWCols = 64;
 constexpr int kWBlocks = 4;
 constexpr int kWRowStride = kWBlocks * 16 + 8;  // bytes; 9 x 8-byte chunks
 
 template <bool kBf16, int kMode>
-__global__ void __launch_bounds__(256) hq_w_kernel(
+__global__ void __launch_bounds__(256) hq_w_pair_kernel(
     const void* __restrict__ src, int64_t rows, int64_t cols,
     unsigned int* __restrict__ amax_slot, uint8_t* __restrict__ codes_t,
     float* __restrict__ scale, int rnd, uint64_t seed, uint32_t stream,
@@ -1619,16 +1740,38 @@ cudaError_t launch_hq_cols(const void* src, bool bf16, int64_t rows,
                            float* scale, int rnd, uint64_t seed,
                            uint32_t stream_id, unsigned int* status,
                            cudaStream_t st) {
-  dim3 grid(grid1(cols, kWCols), grid1(rows / 16, kWBlocks));
-#define HQW(B, M)                                                                  \
-  launch_pdl(hq_w_kernel<B, M>, grid, dim3(256), 0, st, src, rows, cols, amax_slot, \
+  const int64_t threads = (cols / 4) * (rows / 16);
+  if (threads == 0) return cudaSuccess;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return cudaErrorInvalidDevice;
+  // quad kernel when it has at least 4 CTAs of 128 threads per SM, else the
+  // pair kernel's 8x more threads (ViT-B qkv w: 14.7 us pair, 18.7 us quad;
+  // Llama down_proj w: 219 us pair, 152 us quad)
+  if (threads >= (int64_t)sms * 4 * 128) {
+    const dim3 grid(grid1(threads, 128));
+#define HQW(B, M)                                                                   \
+  launch_pdl(hq_w_kernel<B, M>, grid, dim3(128), 0, st, src, rows, cols, amax_slot, \
              codes_t, scale, rnd, seed, stream_id, status)
-  if (amax_only) {
-    if (bf16) HQW(true, kAmax); else HQW(false, kAmax);
-  } else {
-    if (bf16) HQW(true, kQuant); else HQW(false, kQuant);
-  }
+    if (amax_only) {
+      if (bf16) HQW(true, kAmax); else HQW(false, kAmax);
+    } else {
+      if (bf16) HQW(true, kQuant); else HQW(false, kQuant);
+    }
 #undef HQW
+  } else {
+    const dim3 grid(grid1(cols, kWCols), grid1(rows / 16, kWBlocks));
+#define HQP(B, M)                                                                        \
+  launch_pdl(hq_w_pair_kernel<B, M>, grid, dim3(256), 0, st, src, rows, cols, amax_slot, \
+             codes_t, scale, rnd, seed, stream_id, status)
+    if (amax_only) {
+      if (bf16) HQP(true, kAmax); else HQP(false, kAmax);
+    } else {
+      if (bf16) HQP(true, kQuant); else HQP(false, kQuant);
+    }
+#undef HQP
+  }
   return cudaGetLastError();
 }
 
