@@ -25,7 +25,7 @@ RNE, SR = 0, 1
 F32, BF16 = 0, 1
 OP_COMPRESS_ACTIVATION, OP_BACKWARD_GX, OP_BACKWARD_GW, OP_BACKWARD = 0, 1, 2, 3
 OP_SELECT_GRANULARITY, OP_ABLATION_GW_HQ, OP_ABLATION_GX_HLA = 4, 5, 6
-OP_BACKWARD_FUSED = 7
+OP_BACKWARD_FUSED, OP_LAYER_STEP = 7, 8
 XBAR_INT8, XBAR_INT4, XBAR_PER_CHANNEL = 8, 4, 0x100   # format word of the stored activation
 DEV_NONFINITE, DEV_TIMEOUT, DEV_BADCODE = 0x1, 0x2, 0x4
 
@@ -47,6 +47,7 @@ EXPORTS = [
     "hlq_ablation_gw_hq",
     "hlq_ablation_gx_hla",
     "hlq_linear_backward_fused",
+    "hlq_layer_step",
 ]
 
 _lock = threading.Lock()
@@ -113,6 +114,8 @@ def lib() -> ctypes.CDLL:
                                                 P, P, P, sz, P]),
             "hlq_ablation_gw_hq": (i32, [P, P, i32, i64, i64, i64, i32, i32, u64, P, P, P,
                                          sz, P]),
+            "hlq_layer_step": (i32, [P, P, P, i32, i64, i64, i64, i32, i32, i32, i32, i32,
+                                     i32, u64, P, P, P, P, P, sz, P]),
             "hlq_ablation_gx_hla": (i32, [P, P, i32, i64, i64, i64, i32, i32, P, P, P, sz,
                                           P]),
             "hlq_trace_end": (i32, [P]),
@@ -328,6 +331,42 @@ def hlq_linear_backward(g_y, w, xbar, xbar_scale, rank: int = 8,
         _ptr(out_gw), _ptr(ws), ws.numel(), _stream(stream)),
         "hlq_linear_backward_fused" if fused_gy else "hlq_linear_backward")
     return out_gx, out_gw
+
+
+def hlq_layer_step(x, g_y, w, rank: int = 8, gran_gy: int = PER_TOKEN,
+                   gran_w: int = PER_TENSOR, rnd: int = SR, seed: int = 0, block: int = 16,
+                   out_gx=None, out_gw=None, xbar=None, xbar_scale=None, ws=None,
+                   xbar_bits: int = 8, xbar_per_channel: bool = False, stream=None):
+    """The ACBP compression of x and both gradients in one call (the
+    compression overlaps the g_x branch): returns (g_x, g_w, xbar,
+    xbar_scale)."""
+    torch = _torch()
+    _need_cuda_contig(x, g_y, w)
+    T, Cout = g_y.shape
+    Cin = w.shape[1]
+    if w.shape[0] != Cout or tuple(x.shape) != (T, Cin) or not (x.dtype == g_y.dtype == w.dtype):
+        raise ValueError("shape/dtype mismatch between x, g_y and w")
+    dev = g_y.device
+    if out_gx is None:
+        out_gx = torch.empty((T, Cin), dtype=torch.float32, device=dev)
+    if out_gw is None:
+        out_gw = torch.empty((Cout, Cin), dtype=torch.float32, device=dev)
+    if xbar is None:
+        xbar = torch.empty(xbar_shape(T, Cin, rank, xbar_bits),
+                           dtype=torch.int8 if xbar_bits == 8 else torch.uint8, device=dev)
+    if xbar_scale is None:
+        xbar_scale = torch.empty(Cin if xbar_per_channel else 1, dtype=torch.float32,
+                                 device=dev)
+    _need_cuda_contig(xbar, xbar_scale)
+    _check_xbar_scale(xbar_scale, Cin, xbar_per_channel)
+    if ws is None:
+        ws = workspace(OP_LAYER_STEP, T, Cin, Cout, block, rank, dev)
+    _check(lib().hlq_layer_step(
+        _ptr(x), _ptr(g_y), _ptr(w), _dtype_code(g_y), T, Cin, Cout, block, rank,
+        _xbar_fmt(xbar_bits, xbar_per_channel), gran_gy, gran_w, rnd, seed, _ptr(out_gx),
+        _ptr(out_gw), _ptr(xbar), _ptr(xbar_scale), _ptr(ws), ws.numel(), _stream(stream)),
+        "hlq_layer_step")
+    return out_gx, out_gw, xbar, xbar_scale
 
 
 def _need_cpu_contig(*ts):

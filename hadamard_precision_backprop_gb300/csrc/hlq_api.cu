@@ -521,6 +521,9 @@ size_t hlq_workspace_bytes(int op, int64_t T, int64_t Cin, int64_t Cout,
       return 2 * kAlign + align_up((size_t)Cout * (size_t)T) + align_up((size_t)Cin * (size_t)T);
     case HLQ_OP_ABLATION_GX_HLA:
       return gx_hla_layout(T, Cin, Cout, rank_ok(rank) ? rank : 16).total;
+    case HLQ_OP_LAYER_STEP:  // compression, then both layouts
+      return compress_ws(T, Cin) + gx_layout(T, Cin, Cout).total +
+             gw_layout(T, Cin, Cout, rank_ok(rank) ? rank : 16).total;
     case HLQ_OP_BACKWARD_FUSED:  // both layouts and one amax slot per token
       return gx_layout(T, Cin, Cout).total +
              gw_layout(T, Cin, Cout, rank_ok(rank) ? rank : 16).total +
@@ -606,6 +609,74 @@ hlq_status hlq_linear_backward(const void* d_gy, const void* d_w, const int8_t* 
     r = HLQ_ERR_CUDA;
   cudaEventDestroy(fork);
   cudaEventDestroy(join);
+  return r;
+}
+
+// The ACBP compression of x and both gradients in one call, from device
+// buffers: the compression runs first on the g_w branch (the only one that
+// needs the stored activation), so it overlaps the HQ of g_y and the g_x
+// GEMM on the caller's stream; the HQ of w runs on a third stream.  Same
+// bits as hlq_compress_activation followed by hlq_linear_backward.
+hlq_status hlq_layer_step(const void* d_x, const void* d_gy, const void* d_w, int dt,
+                          int64_t T, int64_t Cin, int64_t Cout, int block, int rank,
+                          int xbar_fmt, int gran_gy, int gran_w, int rnd, uint64_t seed,
+                          float* d_gx, float* d_gw, int8_t* d_xbar, float* d_xbar_scale,
+                          void* d_ws, size_t ws_bytes, void* stream) {
+  hlq_status st = check_common(dt, T, Cin, Cout, block);
+  if (st != HLQ_OK) return st;
+  if (!rank_ok(rank)) return HLQ_ERR_INVALID_ARG;
+  st = xbar_fmt_check(xbar_fmt, rank);
+  if (st != HLQ_OK) return st;
+  const int64_t Tp = T / 16 * rank;
+  if (!d_xbar_scale) return HLQ_ERR_INVALID_ARG;
+  if (Cin * Tp > 0 && (!d_x || !d_xbar)) return HLQ_ERR_INVALID_ARG;
+  if (!aligned16(d_x) || !aligned16(d_xbar)) return HLQ_ERR_ALIGN;
+  const size_t c_bytes = compress_ws(T, Cin);
+  const size_t gx_bytes = gx_layout(T, Cin, Cout).total;
+  const size_t gw_bytes = gw_layout(T, Cin, Cout, rank).total;
+  if (!d_ws || ws_bytes < c_bytes + gx_bytes + gw_bytes) return HLQ_ERR_WORKSPACE;
+  if (!aligned256(d_ws)) return HLQ_ERR_ALIGN;
+  uint8_t* base = static_cast<uint8_t*>(d_ws);
+  uint8_t* gxb = base + c_bytes;
+  uint8_t* gwb = gxb + gx_bytes;
+  st = gw_impl(d_gy, dt, d_xbar, xbar_fmt, d_xbar_scale, T, Cin, Cout, block, rank, d_gw, gwb,
+               gw_bytes, nullptr, nullptr, nullptr, nullptr, /*validate_only=*/true);
+  if (st != HLQ_OK) return st;
+  st = gx_impl(d_gy, d_w, dt, T, Cin, Cout, block, gran_gy, gran_w, rnd, seed, d_gx, gxb,
+               gx_bytes, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
+               /*validate_only=*/true);
+  if (st != HLQ_OK) return st;
+  if (T * Cin * Cout == 0) {  // degenerate sizes: the separate calls, in order
+    st = hlq_compress_activation(d_x, dt, T, Cin, block, rank, xbar_fmt, d_xbar,
+                                 d_xbar_scale, base, c_bytes, stream);
+    if (st != HLQ_OK) return st;
+    return hlq_linear_backward(d_gy, d_w, d_xbar, d_xbar_scale, dt, T, Cin, Cout, block, rank,
+                               xbar_fmt, gran_gy, gran_w, rnd, seed, d_gx, d_gw, gxb,
+                               gx_bytes + gw_bytes, stream);
+  }
+  unsigned int* status = device_status_ptr();
+  if (!status) return HLQ_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaStream_t a = aux_stream(0), aw = aux_stream(1);
+  if (!a || !aw) return HLQ_ERR_CUDA;
+  EventSet E;
+  cudaEvent_t fork = E.make(), join = E.make();
+  if (!fork || !join) return HLQ_ERR_CUDA;
+  hlq_status r = HLQ_OK;
+  if (cudaEventRecord(fork, s) != cudaSuccess || cudaStreamWaitEvent(a, fork, 0) != cudaSuccess)
+    r = HLQ_ERR_CUDA;
+  if (r == HLQ_OK)  // g_w branch: compression of x, HLA of g_y, widening, g_w GEMM
+    r = compress_launches(d_x, dt == HLQ_BF16, T, Cin, rank, xbar_fmt, d_xbar, d_xbar_scale,
+                          reinterpret_cast<unsigned int*>(base), status, a);
+  if (r == HLQ_OK)
+    r = gw_impl(d_gy, dt, d_xbar, xbar_fmt, d_xbar_scale, T, Cin, Cout, block, rank, d_gw,
+                gwb, gw_bytes, nullptr, nullptr, nullptr, a, false);
+  if (r == HLQ_OK)  // g_x branch on the caller's stream, its HQ of w on a third
+    r = gx_impl(d_gy, d_w, dt, T, Cin, Cout, block, gran_gy, gran_w, rnd, seed, d_gx, gxb,
+                gx_bytes, nullptr, nullptr, nullptr, nullptr, nullptr, stream, false, aw);
+  // join even after a failure
+  if (cudaEventRecord(join, a) != cudaSuccess || cudaStreamWaitEvent(s, join, 0) != cudaSuccess)
+    r = HLQ_ERR_CUDA;
   return r;
 }
 

@@ -72,7 +72,8 @@ typedef enum {
     HLQ_OP_SELECT_GRANULARITY = 4, /* hlq_select_gy_granularity */
     HLQ_OP_ABLATION_GW_HQ = 5,     /* hlq_ablation_gw_hq */
     HLQ_OP_ABLATION_GX_HLA = 6,    /* hlq_ablation_gx_hla */
-    HLQ_OP_BACKWARD_FUSED = 7      /* hlq_linear_backward_fused */
+    HLQ_OP_BACKWARD_FUSED = 7,     /* hlq_linear_backward_fused */
+    HLQ_OP_LAYER_STEP = 8          /* hlq_layer_step */
 } hlq_op;
 
 /* Device status flags (hlq_read_device_status). */
@@ -179,6 +180,21 @@ hlq_status hlq_linear_backward(const void *d_gy, const void *d_w, const int8_t *
                                int xbar_fmt, int gran_gy, int gran_w, int rnd, uint64_t seed,
                                float *d_gx, float *d_gw, void *d_ws, size_t ws_bytes,
                                void *stream);
+
+/*
+ * One layer step from device buffers: the ACBP compression of x (as
+ * hlq_compress_activation, into d_xbar / d_xbar_scale) and both gradients
+ * (as hlq_linear_backward), in one call.  The compression is the first step
+ * of the g_w branch, the only one that reads the stored activation, so it
+ * runs beside the HQ of g_y and the g_x GEMM instead of before them.  Every
+ * output bit equals the separate calls'.  Arguments as for those two calls;
+ * workspace hlq_workspace_bytes(HLQ_OP_LAYER_STEP, ...).
+ */
+hlq_status hlq_layer_step(const void *d_x, const void *d_gy, const void *d_w, int dt,
+                          int64_t T, int64_t Cin, int64_t Cout, int block, int rank,
+                          int xbar_fmt, int gran_gy, int gran_w, int rnd, uint64_t seed,
+                          float *d_gx, float *d_gw, int8_t *d_xbar, float *d_xbar_scale,
+                          void *d_ws, size_t ws_bytes, void *stream);
 
 /*
  * hlq_linear_backward with one fused reader of g_y for both paths: a first

@@ -46,7 +46,7 @@ def test_workspace_sizes(L):
     # g_x workspace holds one byte per int4 code of g_y and of w
     n = hlq.hlq_workspace_bytes(1, 256, 64, 128)
     assert n >= 256 * 128 + 64 * 128
-    assert hlq.hlq_workspace_bytes(8, 16, 16, 16) == 0          # unknown op
+    assert hlq.hlq_workspace_bytes(9, 16, 16, 16) == 0          # unknown op
     assert hlq.hlq_workspace_bytes(1, -16, 16, 16) == 0
 
 
@@ -246,6 +246,29 @@ def test_fused_backward_workspace_and_validation(L):
     bad = list(args)
     bad[12] = 1                               # per-token w
     assert f(*bad, need, None) == 4
+
+
+def test_layer_step_workspace_and_validation(L):
+    f = L.hlq_layer_step
+    T, Cin, Cout = 256, 64, 128
+    need = L.hlq_workspace_bytes(8, T, Cin, Cout, 16, 8)
+    assert need == (L.hlq_workspace_bytes(0, T, Cin, Cout, 16, 8) +
+                    L.hlq_workspace_bytes(3, T, Cin, Cout, 16, 8))
+
+    def call(**kw):
+        a = dict(x=FAKE, gy=FAKE, w=FAKE, dt=1, T=T, Cin=Cin, Cout=Cout, block=16, rank=8,
+                 fmt=8, gran_gy=1, gran_w=0, rnd=1, seed=0, gx=FAKE, gw=FAKE, xbar=FAKE,
+                 xs=FAKE, ws=FAKE_WS, ws_bytes=need)
+        a.update(kw)
+        return f(*a.values(), None)
+
+    assert call(ws_bytes=need - 256) == 5
+    assert call(x=None) == 1
+    assert call(xs=None) == 1
+    assert call(fmt=6) == 1
+    assert call(x=FAKE + 4) == 3
+    assert call(T=40) == 2
+    assert call(gran_w=1) == 4
 
 
 def test_read_status_rejects_null(L):
