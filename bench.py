@@ -260,6 +260,23 @@ def run_reference(args, wl, rank, world):
     return 0
 
 
+def max_over_ranks(value, dist=None, device="cpu"):
+    """The largest of every rank's value (the job is as slow as its slowest
+    replica); the value itself without a process group."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_us_per_layer(ms_per_step, world):
+    """Job-wide microseconds per layer step: `world` replicas each finish one
+    step in `ms_per_step` (weak scaling)."""
+    return ms_per_step * 1e3 / world
+
+
 def config_of(wl):
     return {"workload": wl.name, "T": wl.T, "Cin": wl.Cin, "Cout": wl.Cout,
             "input_dtype": wl.dtype, "block": wl.block, "rank": wl.rank,
@@ -392,10 +409,7 @@ def run_ours(args, wl, rank, world, local_rank):
     clk = clocks.stop()
     step_ms = [a.elapsed_time(b) for a, b in evs]
     ms = statistics.mean(step_ms)
-    if dist is not None:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dist, dev)
     launches = []
     for _ in range(args.steps):
         flush.fill_(1)
@@ -550,10 +564,7 @@ def run_ours(args, wl, rank, world, local_rank):
         b.synchronize()
         e2e_ms.append(a.elapsed_time(b))
     e2e = statistics.mean(e2e_ms)
-    if dist is not None:
-        t = torch.tensor([e2e], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e = float(t.item())
+    e2e = max_over_ranks(e2e, dist, dev)
     barrier()
 
     if rank != 0:
@@ -585,7 +596,7 @@ def run_ours(args, wl, rank, world, local_rank):
                 "unit": unit, "frac": kernels[top]["achieved"] / peak,
                 "traffic": traffic, "peak_source": peaks["source"]}
 
-    us = ms * 1e3 / world                 # job-wide us per layer step
+    us = job_us_per_layer(ms, world)      # job-wide us per layer step
     gemm_ops = 2 * T * Cin * Cout + 2 * Cout * Cin * Tp
     gemm_bitops = 2 * T * Cin * Cout * 4 + 2 * Cout * Cin * Tp * 8
     gemm_s = sum(v[1] for k, v in per_kernel.items() if k.startswith("gemm")) / args.steps / 1e3
@@ -614,7 +625,7 @@ def run_ours(args, wl, rank, world, local_rank):
         "gpu_launches": len(launches),
         "variants": variants,
         "clocks": clk,
-        "e2e": {"value": e2e * 1e3 / world, "unit": UNIT,
+        "e2e": {"value": job_us_per_layer(e2e, world), "unit": UNIT,
                 "h2d_bytes_per_step": (x.numel() + gy.numel() + w.numel()) * e,
                 "d2h_bytes_per_step": (gx.numel() + gw.numel()) * 4},
     }
