@@ -370,10 +370,31 @@ hlq_status hla_gy_launches(const void* gy, bool bf16, int64_t T, int64_t Cout, i
 }
 
 // ACBP buffer widened to bf16, then the g_w GEMM with its dequantization.
+// `after`: an event (the g_x GEMM's end, on another stream) that the GEMM
+// must follow, or null.  Both GEMMs are persistent grids of one CTA per SM
+// whose tiles are dealt out in advance; run side by side when each fills
+// the GPU alone, the later grid's CTAs wait for SMs while their tiles pile
+// up (Llama down_proj: 2497 us per step against 2219 us in sequence), while
+// smaller ones gain from sharing the SMs (ViT-B qkv: 190.6 us side by side,
+// 195.7 in sequence): see gemms_in_sequence.
+// Whether the g_w GEMM must follow the g_x GEMM (g_x GEMM over Mx rows):
+// only when each one alone has at least one unit per SM, so that running
+// them side by side cannot fill idle SMs and only delays the later grid.
+bool gemms_in_sequence(int64_t Mx, int64_t Cin, int64_t Cout, int64_t Tp) {
+  const int sms = device_sm_count();
+  if (sms <= 0) return false;
+  auto units = [](const GemmPlan& p, int64_t M, int64_t N) {
+    return ((M + 127) / 128) * ((N + p.bn - 1) / p.bn) * p.splits;
+  };
+  const GemmPlan px = plan_gemm_tc(0, Mx, Cin, Cout, sms, 1);
+  const GemmPlan pw = plan_gemm_tc(1, Cout, Cin, Tp, sms, 16);
+  return units(px, Mx, Cin) >= sms && units(pw, Cout, Cin) >= sms;
+}
+
 hlq_status gw_gemm_launches(const int8_t* xbar, int fmt, const float* xscale, int64_t Cin,
                             int64_t Cout, int64_t Tp, const GwLayout& L, uint8_t* base,
                             float* gw, int32_t* dbg_acc, unsigned int* status,
-                            cudaStream_t s) {
+                            cudaStream_t s, cudaEvent_t after = nullptr) {
   void* xw = base + L.xw;
   const float* sg = reinterpret_cast<const float*>(base + L.sg);
   if (xbar_code_bits(fmt) == 4)
@@ -385,6 +406,7 @@ hlq_status gw_gemm_launches(const int8_t* xbar, int fmt, const float* xscale, in
   const int sms = device_sm_count();
   if (sms <= 0) return HLQ_ERR_CUDA;
   const GemmPlan plan = plan_gemm_tc(1, Cout, Cin, Tp, sms, 16);
+  if (after) HLQ_TRY(cudaStreamWaitEvent(s, after, 0));
   HLQ_LAUNCH("gemm_gw_tc", s,
              launch_gemm_tc(1, base + L.qg, L.ld, xw, L.ld, Cout, Cin, Tp, plan, sg, false,
                             xscale, gw, dbg_acc, base + L.split, status, s,
@@ -396,7 +418,8 @@ hlq_status gw_impl(const void* gy, int dt, const int8_t* xbar, int fmt,
                    const float* xscale, int64_t T, int64_t Cin, int64_t Cout,
                    int block, int rank, float* gw, void* ws, size_t ws_bytes,
                    int8_t* dbg_qg, float* dbg_sg, int32_t* dbg_acc,
-                   void* stream, bool validate_only = false) {
+                   void* stream, bool validate_only = false,
+                   cudaEvent_t gemm_after = nullptr) {
   hlq_status st = check_common(dt, T, Cin, Cout, block);
   if (st != HLQ_OK) return st;
   if (!rank_ok(rank)) return HLQ_ERR_INVALID_ARG;
@@ -433,7 +456,8 @@ hlq_status gw_impl(const void* gy, int dt, const int8_t* xbar, int fmt,
 
   st = hla_gy_launches(gy, bf16, T, Cout, rank, amax, qg, L.ld, sg, status, s);
   if (st != HLQ_OK) return st;
-  st = gw_gemm_launches(xbar, fmt, xscale, Cin, Cout, Tp, L, base, gw, dbg_acc, status, s);
+  st = gw_gemm_launches(xbar, fmt, xscale, Cin, Cout, Tp, L, base, gw, dbg_acc, status, s,
+                        gemm_after);
   if (st != HLQ_OK) return st;
   if (dbg_qg) HLQ_TRY(launch_decode_bf16(qg, dbg_qg, Cout, Tp, L.ld, s));
   if (dbg_sg) HLQ_TRY(cudaMemcpyAsync(dbg_sg, sg, 4, cudaMemcpyDeviceToDevice, s));
@@ -593,22 +617,31 @@ hlq_status hlq_linear_backward(const void* d_gy, const void* d_w, const int8_t* 
     cudaEventDestroy(fork);
     return HLQ_ERR_CUDA;
   }
+  cudaEvent_t gx_done = nullptr;
+  if (cudaEventCreateWithFlags(&gx_done, cudaEventDisableTiming) != cudaSuccess) {
+    cudaEventDestroy(fork);
+    cudaEventDestroy(join);
+    return HLQ_ERR_CUDA;
+  }
   hlq_status r = HLQ_OK;
   if (cudaEventRecord(fork, s) != cudaSuccess || cudaStreamWaitEvent(a, fork, 0) != cudaSuccess)
     r = HLQ_ERR_CUDA;
-  if (r == HLQ_OK)  // g_w branch on the auxiliary stream
-    r = gw_impl(d_gy, dt, d_xbar, xbar_fmt, d_xbar_scale, T, Cin, Cout, block, rank, d_gw,
-                base + gx_bytes, gw_bytes, nullptr, nullptr, nullptr, a, false);
   if (r == HLQ_OK)  // g_x branch on the caller's stream, its HQ of w on a third
     r = gx_impl(d_gy, d_w, dt, T, Cin, Cout, block, gran_gy, gran_w, rnd, seed, d_gx,
                 base, gx_bytes, nullptr, nullptr, nullptr, nullptr, nullptr, stream,
                 false, aw);
+  if (r == HLQ_OK && cudaEventRecord(gx_done, s) != cudaSuccess) r = HLQ_ERR_CUDA;
+  if (r == HLQ_OK)  // g_w branch on the auxiliary stream (its GEMM maybe after g_x's)
+    r = gw_impl(d_gy, dt, d_xbar, xbar_fmt, d_xbar_scale, T, Cin, Cout, block, rank, d_gw,
+                base + gx_bytes, gw_bytes, nullptr, nullptr, nullptr, a, false,
+                gemms_in_sequence(T, Cin, Cout, T / 16 * rank) ? gx_done : nullptr);
   // join even after a failure, so the caller's stream never runs ahead of
   // work already enqueued on the auxiliary stream
   if (cudaEventRecord(join, a) != cudaSuccess || cudaStreamWaitEvent(s, join, 0) != cudaSuccess)
     r = HLQ_ERR_CUDA;
   cudaEventDestroy(fork);
   cudaEventDestroy(join);
+  cudaEventDestroy(gx_done);
   return r;
 }
 
@@ -660,20 +693,22 @@ hlq_status hlq_layer_step(const void* d_x, const void* d_gy, const void* d_w, in
   cudaStream_t a = aux_stream(0), aw = aux_stream(1);
   if (!a || !aw) return HLQ_ERR_CUDA;
   EventSet E;
-  cudaEvent_t fork = E.make(), join = E.make();
-  if (!fork || !join) return HLQ_ERR_CUDA;
+  cudaEvent_t fork = E.make(), join = E.make(), gx_done = E.make();
+  if (!fork || !join || !gx_done) return HLQ_ERR_CUDA;
   hlq_status r = HLQ_OK;
   if (cudaEventRecord(fork, s) != cudaSuccess || cudaStreamWaitEvent(a, fork, 0) != cudaSuccess)
     r = HLQ_ERR_CUDA;
+  if (r == HLQ_OK)  // g_x branch on the caller's stream, its HQ of w on a third
+    r = gx_impl(d_gy, d_w, dt, T, Cin, Cout, block, gran_gy, gran_w, rnd, seed, d_gx, gxb,
+                gx_bytes, nullptr, nullptr, nullptr, nullptr, nullptr, stream, false, aw);
+  if (r == HLQ_OK && cudaEventRecord(gx_done, s) != cudaSuccess) r = HLQ_ERR_CUDA;
   if (r == HLQ_OK)  // g_w branch: compression of x, HLA of g_y, widening, g_w GEMM
     r = compress_launches(d_x, dt == HLQ_BF16, T, Cin, rank, xbar_fmt, d_xbar, d_xbar_scale,
                           reinterpret_cast<unsigned int*>(base), status, a);
   if (r == HLQ_OK)
     r = gw_impl(d_gy, dt, d_xbar, xbar_fmt, d_xbar_scale, T, Cin, Cout, block, rank, d_gw,
-                gwb, gw_bytes, nullptr, nullptr, nullptr, a, false);
-  if (r == HLQ_OK)  // g_x branch on the caller's stream, its HQ of w on a third
-    r = gx_impl(d_gy, d_w, dt, T, Cin, Cout, block, gran_gy, gran_w, rnd, seed, d_gx, gxb,
-                gx_bytes, nullptr, nullptr, nullptr, nullptr, nullptr, stream, false, aw);
+                gwb, gw_bytes, nullptr, nullptr, nullptr, a, false,
+                gemms_in_sequence(T, Cin, Cout, Tp) ? gx_done : nullptr);
   // join even after a failure
   if (cudaEventRecord(join, a) != cudaSuccess || cudaStreamWaitEvent(s, join, 0) != cudaSuccess)
     r = HLQ_ERR_CUDA;
@@ -1122,8 +1157,9 @@ hlq_status hlq_layer_step_host(const void* h_x, const void* h_gy, const void* h_
                           reinterpret_cast<unsigned int*>(base + L.cws), status, a_gw);
   if (r == HLQ_OK)
     r = gw_gemm_launches(d_xbar, xbar_fmt, d_xbar_scale, Cin, Cout, Tp, WL, gwb, gw, nullptr,
-                         status,
-                         a_gw);
+                         status, a_gw,
+                         gemms_in_sequence(ch < T ? ch : T, Cin, Cout, Tp) ? gx_done[nc - 1]
+                                                                           : nullptr);
   fail(cudaEventRecord(gw_done, a_gw));
   // copy-out stream: g_x chunk by chunk as they finish, then g_w
   for (int c = 0; c < nc; ++c) {

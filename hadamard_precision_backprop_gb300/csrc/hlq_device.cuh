@@ -302,17 +302,59 @@ __device__ __forceinline__ void fwht16(float* x) {
       }
 }
 
-// 8-point butterfly (the three within-octet stages of a 16-point one).
+// Two fp32 lanes in one 64-bit register, and the packed IEEE add, subtract
+// and fused multiply-add of sm_100+ (each lane rounded to nearest exactly as
+// the scalar instruction rounds it).
+__device__ __forceinline__ unsigned long long f2_pack(float a, float b) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(unsigned long long r, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ unsigned long long f2_add(unsigned long long a, unsigned long long b) {
+  unsigned long long r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ unsigned long long f2_sub(unsigned long long a, unsigned long long b) {
+  unsigned long long r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ unsigned long long f2_fma(unsigned long long a, unsigned long long b,
+                                                     unsigned long long c) {
+  unsigned long long r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+
+// 8-point butterfly (the three within-octet stages of a 16-point one).  The
+// stages at distance 2 and 4 pair whole (x[2i], x[2i+1]) lanes and run as
+// packed adds; the stage at distance 1 follows as scalar adds.  Stages
+// commute, and the callers use this only where every partial sum is exact
+// (or on parts that are), so the order leaves the results unchanged.
 __device__ __forceinline__ void fwht8(float* x) {
+  unsigned long long p[4];
 #pragma unroll
-  for (int h = 1; h < 8; h <<= 1)
+  for (int i = 0; i < 4; ++i) p[i] = f2_pack(x[2 * i], x[2 * i + 1]);
 #pragma unroll
-    for (int a = 0; a < 8; ++a)
+  for (int h = 1; h < 4; h <<= 1)
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
       if ((a & h) == 0) {
-        float p = x[a], q = x[a + h];
-        x[a] = p + q;
-        x[a + h] = p - q;
+        const unsigned long long u = p[a], v = p[a + h];
+        p[a] = f2_add(u, v);
+        p[a + h] = f2_sub(u, v);
       }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float a, b;
+    f2_unpack(p[i], a, b);
+    x[2 * i] = a + b;
+    x[2 * i + 1] = a - b;
+  }
 }
 
 // Sylvester row of sequency k: bit-reversed (4 bits) Gray code of k.
@@ -416,18 +458,27 @@ __device__ __forceinline__ int quant_rne(float y, float s, int qmax) {
 
 // Float-valued forms of the two roundings (integer-valued results, clamped);
 // s == 0 gives 0.
-__device__ __forceinline__ float quant_sr_f(float y, float s, uint32_t word,
-                                            float qmax) {
+// The same for a scale known to be non-zero (callers that branch on s == 0
+// once per row or tensor).
+__device__ __forceinline__ float quant_sr_nz(float y, float s, uint32_t word, float qmax) {
   const float x = __fdiv_rn(y, s);
   const float f = floorf(x);
   const float frac = x - f;
   const float u = __uint2float_rn(word >> 8) * 5.9604644775390625e-08f;  // 2^-24
-  const float r = fminf(fmaxf(f + ((u < frac) ? 1.0f : 0.0f), -qmax), qmax);
+  return fminf(fmaxf(f + ((u < frac) ? 1.0f : 0.0f), -qmax), qmax);
+}
+__device__ __forceinline__ float quant_rne_nz(float y, float s, float qmax) {
+  return fminf(fmaxf(rintf(__fdiv_rn(y, s)), -qmax), qmax);
+}
+
+__device__ __forceinline__ float quant_sr_f(float y, float s, uint32_t word,
+                                            float qmax) {
+  const float r = quant_sr_nz(y, s, word, qmax);
   return s == 0.0f ? 0.0f : r;
 }
 
 __device__ __forceinline__ float quant_rne_f(float y, float s, float qmax) {
-  const float r = fminf(fmaxf(rintf(__fdiv_rn(y, s)), -qmax), qmax);
+  const float r = quant_rne_nz(y, s, qmax);
   return s == 0.0f ? 0.0f : r;
 }
 

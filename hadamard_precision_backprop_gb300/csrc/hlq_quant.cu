@@ -83,13 +83,17 @@ __device__ __noinline__ void slow_block16(const float* in, float* out, int bf16)
 // Butterfly of one octet (the lane pair 2p, 2p+1 holds one 16-block): the
 // fp32 butterfly over lanes, across the pair with one shuffle stage.
 __device__ __forceinline__ void octet_fwht(float* v) {
-  const bool upper = (threadIdx.x & 1) != 0;
+  // across the pair: lower lane v + o, upper lane o - v, as fma(v, +-1, o)
+  // (exact product, one rounding: the same result), two lanes per fma
+  const float sg = (threadIdx.x & 1) ? -1.0f : 1.0f;
+  const unsigned long long sg2 = f2_pack(sg, sg);
   fwht8(v);
+  float o[8];
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const float o = __shfl_xor_sync(0xffffffffu, v[k], 1);
-    v[k] = upper ? (o - v[k]) : (v[k] + o);
-  }
+  for (int k = 0; k < 8; ++k) o[k] = __shfl_xor_sync(0xffffffffu, v[k], 1);
+#pragma unroll
+  for (int k = 0; k < 8; k += 2)
+    f2_unpack(f2_fma(f2_pack(v[k], v[k + 1]), sg2, f2_pack(o[k], o[k + 1])), v[k], v[k + 1]);
 }
 
 // Exactly rounded transform of one octet in place.  tier (equal on both
@@ -247,6 +251,8 @@ __device__ __forceinline__ void unpack(const RawOct<false>& r, float* v) {
 // Quantize one transformed octet (elements e0 .. e0+7 of `codes`) to E4M3
 // int4 codes; the random words are those of elements e_off + e0 .. of the
 // whole tensor.
+// kNonZero: the caller has branched on s == 0 (all-zero codes) already.
+template <bool kNonZero = false>
 __device__ __forceinline__ void quantize_octet(const float* v, float s, int rnd,
                                                const PhiloxKeys& keys, uint32_t stream,
                                                int64_t e0, int64_t e_off, uint8_t* codes) {
@@ -255,17 +261,14 @@ __device__ __forceinline__ void quantize_octet(const float* v, float s, int rnd,
     const uint64_t q = (uint64_t)(e_off + e0) >> 2;
     const U4 a = philox_block_k(keys, stream, q);
     const U4 b = philox_block_k(keys, stream, q + 1);
-    r[0] = quant_sr_f(v[0], s, a.x, 7.0f);
-    r[1] = quant_sr_f(v[1], s, a.y, 7.0f);
-    r[2] = quant_sr_f(v[2], s, a.z, 7.0f);
-    r[3] = quant_sr_f(v[3], s, a.w, 7.0f);
-    r[4] = quant_sr_f(v[4], s, b.x, 7.0f);
-    r[5] = quant_sr_f(v[5], s, b.y, 7.0f);
-    r[6] = quant_sr_f(v[6], s, b.z, 7.0f);
-    r[7] = quant_sr_f(v[7], s, b.w, 7.0f);
+    const uint32_t wd[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      r[k] = kNonZero ? quant_sr_nz(v[k], s, wd[k], 7.0f) : quant_sr_f(v[k], s, wd[k], 7.0f);
   } else {
 #pragma unroll
-    for (int k = 0; k < 8; ++k) r[k] = quant_rne_f(v[k], s, 7.0f);
+    for (int k = 0; k < 8; ++k)
+      r[k] = kNonZero ? quant_rne_nz(v[k], s, 7.0f) : quant_rne_f(v[k], s, 7.0f);
   }
   const uint32_t lo = e4m3x2(r[0], r[1]) | (e4m3x2(r[2], r[3]) << 16);
   const uint32_t hi = e4m3x2(r[4], r[5]) | (e4m3x2(r[6], r[7]) << 16);
@@ -363,6 +366,12 @@ __global__ void __launch_bounds__(256) hq_rows_kernel(
   }
   const PhiloxKeys keys = philox_keys(seed);
   __syncwarp();
+  if (s == 0.0f) {  // warp-uniform: an all-zero row (or tensor) has all-zero codes
+#pragma unroll 1
+    for (int oct = lane; oct < n_oct; oct += 32)
+      *reinterpret_cast<uint2*>(codes + base + (int64_t)oct * 8) = make_uint2(0u, 0u);
+    return;
+  }
   if (kPerToken && stage) {
 #pragma unroll 1
     for (int it = 0; it < iters; ++it) {
@@ -370,7 +379,7 @@ __global__ void __launch_bounds__(256) hq_rows_kernel(
       if (oct >= n_oct) break;
       const float4 a = my[(2 * it) * 32 + lane], b = my[(2 * it + 1) * 32 + lane];
       const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-      quantize_octet(v, s, rnd, keys, stream, base + (int64_t)oct * 8, e_off, codes);
+      quantize_octet<true>(v, s, rnd, keys, stream, base + (int64_t)oct * 8, e_off, codes);
     }
     return;
   }
@@ -383,7 +392,8 @@ __global__ void __launch_bounds__(256) hq_rows_kernel(
                                         it + 1 < iters && nx < n_oct);
     float v[8];
     transform_raw<kBf16>(cur, v, status);
-    if (oct < n_oct) quantize_octet(v, s, rnd, keys, stream, base + (int64_t)oct * 8, e_off, codes);
+    if (oct < n_oct)
+      quantize_octet<true>(v, s, rnd, keys, stream, base + (int64_t)oct * 8, e_off, codes);
     cur = nxt;
   }
 }
