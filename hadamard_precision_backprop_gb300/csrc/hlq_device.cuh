@@ -302,6 +302,24 @@ __device__ __forceinline__ void fwht16(float* x) {
       }
 }
 
+// Two 16-bit unsigned lanes in one 32-bit register: lane-wise max, min and
+// modular add (sm_90+ packed integer instructions).
+__device__ __forceinline__ uint32_t u16x2_max(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.u16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+__device__ __forceinline__ uint32_t u16x2_min(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("min.u16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+__device__ __forceinline__ uint32_t u16x2_add(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("add.u16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
 // Two fp32 lanes in one 64-bit register, and the packed IEEE add, subtract
 // and fused multiply-add of sm_100+ (each lane rounded to nearest exactly as
 // the scalar instruction rounds it).

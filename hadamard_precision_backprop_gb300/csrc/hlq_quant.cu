@@ -181,19 +181,22 @@ __device__ __forceinline__ void transform_octet(float* v, unsigned int* status) 
 __device__ __forceinline__ void transform_octet_bf16(const uint4& raw, float* v,
                                                      unsigned int* status) {
   const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-  uint32_t hi = 0u, lom1 = 0xffffffffu;
+  // both 16-bit halves at once: |bits| max, and min of |bits| - 1 (mod 2^16)
+  uint32_t hi2 = 0u, lom2 = 0xffffffffu;
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    const uint32_t a0 = w[k] & 0x7fffu, a1 = (w[k] >> 16) & 0x7fffu;
-    hi = max(hi, max(a0, a1));
-    lom1 = min(lom1, min(a0 - 1u, a1 - 1u));
+    const uint32_t a = w[k] & 0x7fff7fffu;
+    hi2 = u16x2_max(hi2, a);
+    lom2 = u16x2_min(lom2, u16x2_add(a, 0xffffffffu));
   }
+  uint32_t hi = max(hi2 & 0xffffu, hi2 >> 16);
+  uint32_t lom1 = min(lom2 & 0xffffu, lom2 >> 16);  // 0xffff: all zero so far
   hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, 1));
   lom1 = min(lom1, __shfl_xor_sync(0xffffffffu, lom1, 1));
   const uint32_t emax = hi >> 7;
   if (emax == 255u) raise_flag(status, HLQ_DEV_NONFINITE);
-  const bool all_zero = lom1 == 0xffffffffu;
-  const uint32_t emin = max((lom1 + 1u) >> 7, 1u);
+  const bool all_zero = lom1 == 0xffffu;
+  const uint32_t emin = max(((lom1 + 1u) & 0xffffu) >> 7, 1u);
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     v[2 * k] = bf16_lo(w[k]);
@@ -580,17 +583,17 @@ __device__ __forceinline__ void column_coeffs(float* x, int rank, bool natural,
 __device__ __forceinline__ void pair_col_tiers_bf16(const uint32_t (&p)[16], int* tier,
                                                     uint32_t* emax_out,
                                                     unsigned int* status) {
-  uint32_t mx0 = 0u, mx1 = 0u, mn0 = 0xffffffffu, mn1 = 0xffffffffu;
+  // the two columns in the two 16-bit lanes: |bits| max, and min of
+  // |bits| - 1 (mod 2^16, so a zero becomes 0xffff and drops out)
+  uint32_t mx = 0u, mn = 0xffffffffu;
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
-    const uint32_t a0 = p[j] & 0x7fffu, a1 = p[j] & 0x7fff0000u;
-    mx0 = max(mx0, a0);
-    mx1 = max(mx1, a1);
-    mn0 = min(mn0, a0 - 1u);
-    mn1 = min(mn1, a1 - 1u);
+    const uint32_t a = p[j] & 0x7fff7fffu;
+    mx = u16x2_max(mx, a);
+    mn = u16x2_min(mn, u16x2_add(a, 0xffffffffu));
   }
-  const uint32_t hi[2] = {mx0, mx1 >> 16};
-  const uint32_t lo[2] = {mn0 + 1u, mn1 == 0xffffffffu ? 0u : (mn1 + 1u) >> 16};
+  const uint32_t hi[2] = {mx & 0xffffu, mx >> 16};
+  const uint32_t lo[2] = {((mn & 0xffffu) + 1u) & 0xffffu, ((mn >> 16) + 1u) & 0xffffu};
 #pragma unroll
   for (int c = 0; c < 2; ++c) {
     const uint32_t emax = hi[c] >> 7, emin = max(lo[c] >> 7, 1u);
