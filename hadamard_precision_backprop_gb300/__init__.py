@@ -48,6 +48,7 @@ EXPORTS = [
     "hlq_ablation_gx_hla",
     "hlq_linear_backward_fused",
     "hlq_layer_step",
+    "hlq_debug_gemm_plan",
 ]
 
 _lock = threading.Lock()
@@ -114,6 +115,7 @@ def lib() -> ctypes.CDLL:
                                                 P, P, P, sz, P]),
             "hlq_ablation_gw_hq": (i32, [P, P, i32, i64, i64, i64, i32, i32, u64, P, P, P,
                                          sz, P]),
+            "hlq_debug_gemm_plan": (i32, [i64, i64, i64, i32, i32, P, P, P, P, P]),
             "hlq_layer_step": (i32, [P, P, P, i32, i64, i64, i64, i32, i32, i32, i32, i32,
                                      i32, u64, P, P, P, P, P, sz, P]),
             "hlq_ablation_gx_hla": (i32, [P, P, i32, i64, i64, i64, i32, i32, P, P, P, sz,
@@ -566,6 +568,17 @@ def hlq_debug_reference_gemm(a, b, stream=None):
                                           _ptr(acc), _stream(stream)),
            "hlq_debug_reference_gemm")
     return acc
+
+
+def hlq_debug_gemm_plan(T: int, Cin: int, Cout: int, rank: int = 8, sms: int = 152):
+    """The GEMM plans of a layer on a GPU with `sms` SMs (host only): dict of
+    gx (bn, splits), gw (bn, splits) and in_sequence."""
+    vals = [ctypes.c_int(0) for _ in range(5)]
+    _check(lib().hlq_debug_gemm_plan(T, Cin, Cout, rank, sms,
+                                     *[ctypes.byref(v) for v in vals]),
+           "hlq_debug_gemm_plan")
+    g = [v.value for v in vals]
+    return {"gx": (g[0], g[1]), "gw": (g[2], g[3]), "in_sequence": bool(g[4])}
 
 
 def hlq_debug_tc_gemm(kind, a, b, bn=0, splits=0, stream=None):

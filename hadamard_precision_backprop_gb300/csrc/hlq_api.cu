@@ -380,8 +380,7 @@ hlq_status hla_gy_launches(const void* gy, bool bf16, int64_t T, int64_t Cout, i
 // Whether the g_w GEMM must follow the g_x GEMM (g_x GEMM over Mx rows):
 // only when each one alone has at least one unit per SM, so that running
 // them side by side cannot fill idle SMs and only delays the later grid.
-bool gemms_in_sequence(int64_t Mx, int64_t Cin, int64_t Cout, int64_t Tp) {
-  const int sms = device_sm_count();
+bool gemms_in_sequence_on(int64_t Mx, int64_t Cin, int64_t Cout, int64_t Tp, int sms) {
   if (sms <= 0) return false;
   auto units = [](const GemmPlan& p, int64_t M, int64_t N) {
     return ((M + 127) / 128) * ((N + p.bn - 1) / p.bn) * p.splits;
@@ -389,6 +388,9 @@ bool gemms_in_sequence(int64_t Mx, int64_t Cin, int64_t Cout, int64_t Tp) {
   const GemmPlan px = plan_gemm_tc(0, Mx, Cin, Cout, sms, 1);
   const GemmPlan pw = plan_gemm_tc(1, Cout, Cin, Tp, sms, 16);
   return units(px, Mx, Cin) >= sms && units(pw, Cout, Cin) >= sms;
+}
+bool gemms_in_sequence(int64_t Mx, int64_t Cin, int64_t Cout, int64_t Tp) {
+  return gemms_in_sequence_on(Mx, Cin, Cout, Tp, device_sm_count());
 }
 
 hlq_status gw_gemm_launches(const int8_t* xbar, int fmt, const float* xscale, int64_t Cin,
@@ -1298,6 +1300,22 @@ hlq_status hlq_debug_tc_gemm(int kind, const void* d_a, int64_t lda, const void*
   HLQ_LAUNCH(kind == 0 ? "gemm_gx_tc" : "gemm_gw_tc", s,
              launch_gemm_tc(kind, d_a, lda, d_b, ldb, M, N, K, plan, nullptr, false,
                             nullptr, nullptr, d_acc, d_ws, status, s));
+  return HLQ_OK;
+}
+
+hlq_status hlq_debug_gemm_plan(int64_t T, int64_t Cin, int64_t Cout, int rank, int sms,
+                               int* gx_bn, int* gx_splits, int* gw_bn, int* gw_splits,
+                               int* in_sequence) {
+  if (T < 0 || Cin < 0 || Cout < 0 || !rank_ok(rank) || sms <= 0) return HLQ_ERR_INVALID_ARG;
+  if (!gx_bn || !gx_splits || !gw_bn || !gw_splits || !in_sequence) return HLQ_ERR_INVALID_ARG;
+  const int64_t Tp = T / 16 * rank;
+  const GemmPlan px = plan_gemm_tc(0, T, Cin, Cout, sms, 1);
+  const GemmPlan pw = plan_gemm_tc(1, Cout, Cin, Tp, sms, 16);
+  *gx_bn = px.bn;
+  *gx_splits = px.splits;
+  *gw_bn = pw.bn;
+  *gw_splits = pw.splits;
+  *in_sequence = gemms_in_sequence_on(T, Cin, Cout, Tp, sms) ? 1 : 0;
   return HLQ_OK;
 }
 

@@ -297,6 +297,18 @@ hlq_status hlq_debug_tc_gemm(int kind, const void *d_a, int64_t lda,
 size_t hlq_debug_tc_gemm_ws_bytes(int64_t M, int64_t N);
 
 /*
+ * The plans the layer entries choose for the two GEMMs of a layer on a GPU
+ * with `sms` SMs (host computation only, nothing is launched): tile width
+ * and K split of the g_x GEMM (E4M3, M = T, N = Cin, K = Cout) and of the
+ * g_w GEMM (bf16, M = Cout, N = Cin, K = T*rank/16), and whether the g_w
+ * GEMM is ordered after the g_x GEMM (1: each has at least one unit per SM,
+ * so running them side by side would only delay the later one).
+ */
+hlq_status hlq_debug_gemm_plan(int64_t T, int64_t Cin, int64_t Cout, int rank, int sms,
+                               int *gx_bn, int *gx_splits, int *gw_bn, int *gw_splits,
+                               int *in_sequence);
+
+/*
  * Layer-wise quantizer selection for the HQ of g_y (HOT summary page,
  * Approach: per-token or per-tensor quantizer chosen per layer; Limitations:
  * chosen on a calibration set with a 50 % MSE-difference threshold).  On a
