@@ -49,6 +49,7 @@ EXPORTS = [
     "hlq_linear_backward_fused",
     "hlq_layer_step",
     "hlq_debug_gemm_plan",
+    "hlq_debug_wait_timeout",
 ]
 
 _lock = threading.Lock()
@@ -116,6 +117,7 @@ def lib() -> ctypes.CDLL:
             "hlq_ablation_gw_hq": (i32, [P, P, i32, i64, i64, i64, i32, i32, u64, P, P, P,
                                          sz, P]),
             "hlq_debug_gemm_plan": (i32, [i64, i64, i64, i32, i32, P, P, P, P, P]),
+            "hlq_debug_wait_timeout": (i32, [u64, P, P]),
             "hlq_layer_step": (i32, [P, P, P, i32, i64, i64, i64, i32, i32, i32, i32, i32,
                                      i32, u64, P, P, P, P, P, sz, P]),
             "hlq_ablation_gx_hla": (i32, [P, P, i32, i64, i64, i64, i32, i32, P, P, P, sz,
@@ -568,6 +570,16 @@ def hlq_debug_reference_gemm(a, b, stream=None):
                                           _ptr(acc), _stream(stream)),
            "hlq_debug_reference_gemm")
     return acc
+
+
+def hlq_debug_wait_timeout(limit_ns: int = 1_000_000, stream=None):
+    """Run the bounded-wait failure path once (a wait nothing completes,
+    given up after limit_ns): returns the device int32 result (0)."""
+    torch = _torch()
+    out = torch.full((4,), -1, dtype=torch.int32, device=torch.cuda.current_device())
+    _check(lib().hlq_debug_wait_timeout(int(limit_ns), _ptr(out), _stream(stream)),
+           "hlq_debug_wait_timeout")
+    return out[:1]
 
 
 def hlq_debug_gemm_plan(T: int, Cin: int, Cout: int, rank: int = 8, sms: int = 152):

@@ -1319,6 +1319,16 @@ hlq_status hlq_debug_gemm_plan(int64_t T, int64_t Cin, int64_t Cout, int rank, i
   return HLQ_OK;
 }
 
+hlq_status hlq_debug_wait_timeout(uint64_t limit_ns, int32_t* d_result, void* stream) {
+  if (!d_result || limit_ns == 0 || limit_ns > 1000000000ull) return HLQ_ERR_INVALID_ARG;
+  if (!aligned16(d_result)) return HLQ_ERR_ALIGN;
+  unsigned int* status = device_status_ptr();
+  if (!status) return HLQ_ERR_CUDA;
+  HLQ_TRY(launch_wait_timeout_probe(limit_ns, d_result, status,
+                                    static_cast<cudaStream_t>(stream)));
+  return HLQ_OK;
+}
+
 size_t hlq_debug_tc_gemm_ws_bytes(int64_t M, int64_t N) {
   return gemm_tc_split_ws_bytes(M, N);
 }

@@ -74,6 +74,11 @@ cudaError_t launch_gy_fused(const void* gy, bool bf16, int64_t T, int64_t C, int
                             int64_t hla_ld, float* sg, int rnd, uint64_t seed,
                             unsigned int* status, cudaStream_t st);
 
+// One CTA waiting on an mbarrier that never completes, for limit_ns: sets
+// *result = 0 and raises HLQ_DEV_TIMEOUT in the status word.
+cudaError_t launch_wait_timeout_probe(unsigned long long limit_ns, int32_t* result,
+                                      unsigned int* status, cudaStream_t st);
+
 // Transform only (fp32 coefficients), for bit-exact checks.
 cudaError_t launch_hq_rows_transform(const void* src, bool bf16, int64_t rows,
                                      int64_t cols, float* Y,

@@ -1981,6 +1981,30 @@ cudaError_t launch_widen_i8_bf16(const int8_t* in, void* out, int64_t rows,
   return cudaGetLastError();
 }
 
+// A bounded wait that runs out: one CTA waits on an mbarrier that nothing
+// arrives at, gives up after limit_ns, raises HLQ_DEV_TIMEOUT and returns
+// (the failure path of every pipeline wait, exercised without a fault).
+__global__ void wait_timeout_probe_kernel(unsigned long long limit_ns, int32_t* result,
+                                          unsigned int* status) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  const bool ok = mbar_wait_for(&bar, 0u, &abort_flag, status, limit_ns);
+  __syncthreads();
+  if (threadIdx.x == 0) *result = ok ? 1 : 0;
+}
+
+cudaError_t launch_wait_timeout_probe(unsigned long long limit_ns, int32_t* result,
+                                      unsigned int* status, cudaStream_t st) {
+  wait_timeout_probe_kernel<<<1, 32, 0, st>>>(limit_ns, result, status);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_decode_e4m3(const uint8_t* in, int8_t* out, int64_t n,
                                cudaStream_t st) {
   if (n == 0) return cudaSuccess;

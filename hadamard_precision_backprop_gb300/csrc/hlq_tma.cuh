@@ -48,21 +48,28 @@ __device__ __forceinline__ bool mbar_test(uint64_t* b, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for the phase of parity `parity` to complete; gives up after kWaitNs
-// (or as soon as another role gave up), raising HLQ_DEV_TIMEOUT once.
-__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity,
-                                          volatile int* abort_flag,
-                                          unsigned int* status) {
+// Wait for the phase of parity `parity` to complete; gives up after
+// `limit_ns` (or as soon as another role gave up), raising HLQ_DEV_TIMEOUT
+// once.
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* b, uint32_t parity,
+                                              volatile int* abort_flag,
+                                              unsigned int* status,
+                                              unsigned long long limit_ns) {
   if (mbar_test(b, parity)) return true;
   const unsigned long long t0 = now_ns();
   while (true) {
     if (mbar_test(b, parity)) return true;
     if (*abort_flag) return false;
-    if (now_ns() - t0 > kWaitNs) {
+    if (now_ns() - t0 > limit_ns) {
       if (atomicExch((int*)abort_flag, 1) == 0) atomicOr(status, HLQ_DEV_TIMEOUT);
       return false;
     }
   }
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity,
+                                          volatile int* abort_flag,
+                                          unsigned int* status) {
+  return mbar_wait_for(b, parity, abort_flag, status, kWaitNs);
 }
 
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map,

@@ -297,6 +297,15 @@ hlq_status hlq_debug_tc_gemm(int kind, const void *d_a, int64_t lda,
 size_t hlq_debug_tc_gemm_ws_bytes(int64_t M, int64_t N);
 
 /*
+ * The failure path of the library's bounded device waits, without a fault:
+ * one CTA waits on an mbarrier that nothing arrives at, gives up after
+ * limit_ns (0 < limit_ns <= 10^9), writes *d_result = 0 (device int32) and
+ * raises HLQ_DEV_TIMEOUT in the status word (hlq_read_device_status).  The
+ * context stays usable.
+ */
+hlq_status hlq_debug_wait_timeout(uint64_t limit_ns, int32_t *d_result, void *stream);
+
+/*
  * The plans the layer entries choose for the two GEMMs of a layer on a GPU
  * with `sms` SMs (host computation only, nothing is launched): tile width
  * and K split of the g_x GEMM (E4M3, M = T, N = Cin, K = Cout) and of the

@@ -271,6 +271,14 @@ def test_layer_step_workspace_and_validation(L):
     assert call(gran_w=1) == 4
 
 
+def test_wait_timeout_probe_validation(L):
+    f = L.hlq_debug_wait_timeout
+    assert f(0, FAKE, None) == 1                  # no limit
+    assert f(2_000_000_000, FAKE, None) == 1      # over one second
+    assert f(1000, None, None) == 1
+    assert f(1000, FAKE + 4, None) == 3
+
+
 def test_read_status_rejects_null(L):
     assert L.hlq_read_device_status(None, 0, None) == 1
 
