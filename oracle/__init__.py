@@ -11,8 +11,8 @@ Quantization" (TL;DR formulas) and "HOT: Hadamard-based Optimized Training"
 (Approach).
 
 Parity status: every function below is pinned by the CPU tests
-(closed forms, brute force on tiny shapes, quantizer error bounds), except
-Philox4x32-10, whose only external pin is cuRAND's generator on the GPU.
+(closed forms, brute force on tiny shapes, quantizer error bounds; the
+Philox4x32-10 words against cuRAND's host-side Philox4x32-10 generator).
 """
 from __future__ import annotations
 

@@ -2,8 +2,9 @@
 
 None of these re-derives a value with the oracle's own code: each compares
 the oracle with a library routine (scipy's Hadamard matrix, numpy fp64
-matmul), a closed form of the method, exact rational arithmetic, brute force
-on tiny inputs, or an error bound of the quantizer.
+matmul, cuRAND's host-side Philox4x32-10 generator), a closed form of the
+method, exact rational arithmetic, brute force on tiny inputs, or an error
+bound of the quantizer.
 """
 import math
 
@@ -448,6 +449,82 @@ def test_philox_uniformity_and_counter_sensitivity():
     # word e%4 of one block
     blk = oracle.philox4x32_10([3, 0, 0, 0], [5, 0])
     assert [oracle.philox_word(5, 0, 12 + i) for i in range(4)] == list(blk)
+
+
+CURAND_RNG_PSEUDO_PHILOX4_32_10 = 161         # curandRngType_t, curand.h
+
+
+def _curand_host_philox():
+    """cuRAND's host-side Philox4x32-10 generator (it runs on the CPU), or
+    None where libcurand is not installed."""
+    import ctypes
+    import ctypes.util
+    import glob
+    import os
+    names = []
+    for root in (os.environ.get("CUDA_HOME"), os.environ.get("CUDA_PATH"),
+                 "/usr/local/cuda"):
+        if root:
+            names += sorted(glob.glob(os.path.join(root, "lib64", "libcurand.so*")))
+            names += sorted(glob.glob(os.path.join(root, "targets", "*", "lib",
+                                                   "libcurand.so*")))
+    found = ctypes.util.find_library("curand")
+    if found:
+        names.append(found)
+    for name in names:
+        try:
+            lib = ctypes.CDLL(name)
+        except OSError:
+            continue
+        gen = ctypes.c_void_p()
+        if lib.curandCreateGeneratorHost(ctypes.byref(gen),
+                                         CURAND_RNG_PSEUDO_PHILOX4_32_10) == 0:
+            return lib, gen
+    return None
+
+
+def test_philox_matches_curand_host_generator():
+    """Oracle Philox words equal cuRAND's Philox4x32-10 stream.
+
+    cuRAND's default ordering emits block k (four words) of Philox4x32-10
+    under key (seed lo, seed hi) at counter (k >> 16 as a 64-bit number in
+    words 0-1, k mod 65536 in word 2, 0): that is the oracle's word
+    e = 4·(k >> 16) + j of stream k mod 65536.  The cases cover both key
+    halves, the stream word, counter word 0, and the carry from counter word
+    0 into word 1 (k = 2^48 - 1 -> 2^48).  A wrong multiplier, Weyl constant,
+    round count or output permutation in the oracle fails every word."""
+    import ctypes
+    found = _curand_host_philox()
+    if found is None:
+        pytest.skip("libcurand not installed")
+    lib, gen = found
+
+    def curand_words(seed, offset, n):
+        assert lib.curandSetPseudoRandomGeneratorSeed(gen, ctypes.c_ulonglong(seed)) == 0
+        assert lib.curandSetGeneratorOffset(gen, ctypes.c_ulonglong(offset)) == 0
+        buf = np.zeros(n, np.uint32)
+        assert lib.curandGenerate(gen, buf.ctypes.data_as(ctypes.c_void_p),
+                                  ctypes.c_size_t(n)) == 0
+        return buf
+
+    def oracle_words(seed, offset, n):
+        out = np.zeros(n, np.uint32)
+        for i in range(n):
+            k, j = divmod(offset + i, 4)
+            out[i] = oracle.philox_word(seed, k & 0xFFFF, 4 * (k >> 16) + j)
+        return out
+
+    try:
+        for seed in (0, 0x299F31D0A4093822, 0xFFFFFFFFFFFFFFFF):
+            for offset, n in ((0, 4 * 1024),                 # streams 0..1023, e < 4
+                              (4 * 65536 - 16, 64),          # e 0..3 -> 4..7
+                              (4 * 65536 * 37 + 4 * 9000, 32),
+                              (4 * ((1 << 48) - 2), 16)):    # counter word 0 -> word 1
+                got = oracle_words(seed, offset, n)
+                want = curand_words(seed, offset, n)
+                assert np.array_equal(got, want), (hex(seed), offset)
+    finally:
+        lib.curandDestroyGenerator(gen)
 
 
 # ------------------------------------------------------------ GEMM, packing
