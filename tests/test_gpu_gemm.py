@@ -39,18 +39,21 @@ def run(kind, A, B, bn, splits):
     return hlq.hlq_debug_tc_gemm(kind, a, b, bn=bn, splits=splits)
 
 
-@pytest.mark.parametrize("kind,qmax", [(0, 7), (1, 127)])
+# Every tile width, unsplit, for both kinds; K splits for the bf16 GEMM only
+# (the E4M3 GEMM runs unsplit: the ABI refuses a split plan for it, which the
+# CPU plan-validation test checks).
+PLANS = ([(kind, qmax, bn, 1) for kind, qmax in ((0, 7), (1, 127)) for bn in (128, 256, 96)]
+         + [(1, 127, bn, splits) for bn, splits in ((128, 3), (256, 2), (96, 2))])
+
+
+@pytest.mark.parametrize("kind,qmax,bn,splits", PLANS)
 @pytest.mark.parametrize("M,N,K", [(128, 128, 128), (16, 32, 16), (272, 400, 208),
                                    (384, 512, 2048), (1040, 144, 4112)])
-@pytest.mark.parametrize("bn,splits", [(128, 1), (256, 1), (96, 1), (128, 3), (256, 2),
-                                       (96, 2)])
 def test_tc_gemm_exact(kind, qmax, M, N, K, bn, splits):
     rng = np.random.default_rng(M * 7 + N * 3 + K + bn + splits)
     A = rng.integers(-qmax, qmax + 1, (M, K))
     B = rng.integers(-qmax, qmax + 1, (N, K))
     want = A.astype(np.int64) @ B.astype(np.int64).T
-    if kind == 0 and splits > 1:
-        pytest.skip("the E4M3 GEMM runs unsplit (a split plan is refused)")
     got = run(kind, A, B, bn, splits).cpu().numpy()
     np.testing.assert_array_equal(got.astype(np.int64), want)
     ref = hlq.hlq_debug_reference_gemm(torch.from_numpy(A.astype(np.int8)).cuda(),
