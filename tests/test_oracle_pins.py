@@ -432,6 +432,73 @@ def test_sr_uses_element_index_and_stream():
                 assert q[r, c] == (1 if (word >> 8) < (1 << 23) else 0)
 
 
+def test_sampled_rows_use_full_tensor_indices():
+    """Rows quantized on their own (the full-size parity tests' form), with
+    their row numbers in the full tensor: a value at k + 1/2 rounds up
+    exactly when Philox word row*cols + c of the stream has its top bit
+    clear, for row numbers far apart (one row repeated); the scale is
+    RN(amax/7) of the row, or of the tensor maximum passed in."""
+    cols = 32
+    ids = np.array([123456, 3, 1000, 3], np.int64)
+    Y = np.full((len(ids), cols), 0.5, np.float32)
+    Y[1, 7] = -3.5                                  # row amax 3.5 -> s = 0.5
+    for stream in (0, 1):
+        q, s = oracle.hq_quantize_rows(Y, ids, oracle.PER_TENSOR, oracle.SR, 99,
+                                       stream, tensor_amax=7.0)
+        assert list(s) == [1.0]
+        for i, row in enumerate(ids):
+            for c in range(cols):
+                if (i, c) == (1, 7):
+                    assert q[i, c] in (-3, -4)
+                    continue
+                word = oracle.philox_word(99, stream, int(row) * cols + c)
+                assert q[i, c] == (1 if (word >> 8) < (1 << 23) else 0)
+        assert np.array_equal(np.delete(q[1], 7), np.delete(q[3], 7))
+    q, s = oracle.hq_quantize_rows(Y, ids, oracle.PER_TOKEN, oracle.RNE, 0, 0)
+    assert list(s) == [np.float32(0.5) / np.float32(7), np.float32(3.5) / np.float32(7),
+                       np.float32(0.5) / np.float32(7), np.float32(0.5) / np.float32(7)]
+    assert np.all(q[[0, 2, 3]] == 7) and q[1, 7] == -7
+    assert np.all(np.delete(q[1], 7) == 1)          # 0.5 / 0.5 = 1 exactly
+
+
+def test_path_row_samples_equal_full_rows():
+    """Every path's ``rows`` sample equals those rows of the full result,
+    and the sampled quantizer reproduces the full tensor's codes."""
+    rng = np.random.default_rng(22)
+    T, Cin, Cout = 64, 32, 48
+    gy = (rng.standard_normal((T, Cout)) * 1e-3).astype(np.float32)
+    w = (rng.standard_normal((Cout, Cin)) * 0.02).astype(np.float32)
+    x = rng.standard_normal((T, Cin)).astype(np.float32)
+    tok = np.array([63, 0, 17, 17])
+    for gran in (oracle.PER_TOKEN, oracle.PER_TENSOR):
+        full = oracle.gx_path(gy, w, gran_gy=gran, seed=4)
+        part = oracle.gx_path(gy, w, gran_gy=gran, seed=4, rows=tok)
+        assert np.array_equal(part["acc"], full["acc"][tok])
+        assert np.array_equal(part["g_x"], full["g_x"][tok])
+        Y = full["Y"]
+        q, s = oracle.hq_quantize_rows(Y[tok], tok, gran, oracle.SR, 4,
+                                       oracle.STREAM_GY,
+                                       tensor_amax=float(np.max(np.abs(Y))))
+        assert np.array_equal(q, full["qY"][tok])
+        assert np.array_equal(s, full["s_gy"][tok] if gran == oracle.PER_TOKEN
+                              else full["s_gy"])
+    full = oracle.gx_hla_path(gy, w, 8)
+    part = oracle.gx_hla_path(gy, w, 8, rows=tok)
+    assert np.array_equal(part["acc"], full["acc"][tok])
+    assert np.array_equal(part["g_x"], full["g_x"][tok])
+    out = np.array([47, 1, 30])
+    for per_channel in (False, True):
+        xq, sx = oracle.compress_activation(x, 8, per_channel=per_channel)
+        full = oracle.gw_path(gy, xq, sx, 8)
+        part = oracle.gw_path(gy, xq, sx, 8, rows=out)
+        assert np.array_equal(part["acc"], full["acc"][out])
+        assert np.array_equal(part["g_w"], full["g_w"][out])
+    full = oracle.gw_hq_path(gy, x, seed=5)
+    part = oracle.gw_hq_path(gy, x, seed=5, rows=out)
+    assert np.array_equal(part["acc"], full["acc"][out])
+    assert np.array_equal(part["g_w"], full["g_w"][out])
+
+
 # ------------------------------------------------------------ Philox
 
 def test_philox_uniformity_and_counter_sensitivity():
