@@ -235,6 +235,20 @@ def test_hla_rank8_exact_on_equal_token_pairs():
 
 # ------------------------------------------------------------ quantizers
 
+def test_amax_matches_numpy():
+    rng = np.random.default_rng(23)
+    cases = [rng.standard_normal(1000).astype(np.float32),
+             np.array([-3.0, 2.0, -0.0], np.float32),            # max held by a negative
+             np.array([-0.0, 0.0], np.float32),
+             np.array([1e-45, -2e-45, 0.0], np.float32),          # subnormals
+             np.array([np.finfo(np.float32).max, -np.finfo(np.float32).max], np.float32),
+             np.zeros(0, np.float32)]
+    for v in cases:
+        want = np.float32(np.max(np.abs(v))) if v.size else np.float32(0)
+        got = oracle.amax(v)
+        assert got == want and not np.signbit(got), v
+
+
 def test_scale_rule_and_zero_tensor():
     Y = np.array([[0.0, -3.5, 1.0, 2.0]], np.float32)
     q, s = oracle.hq_quantize(Y, oracle.PER_TENSOR, oracle.RNE, 0, 0)
