@@ -400,6 +400,38 @@ def test_clamp_when_scale_rounds_down():
         Y = np.array([[amax, -amax]], np.float32)
         q, _ = oracle.hq_quantize(Y, oracle.PER_TENSOR, oracle.SR, 1, 0)
         assert list(q[0]) == [7, -7]
+    # Past the maximum by one ulp at most, SR reaches 8 only with probability
+    # ~2^-21; a subnormal maximum goes much further: RN(10·2^-149 / 7) is
+    # s = 2^-149, so the maximum lands at x = 10 and only the clamp brings
+    # it back to 7 (127 for the int8 rule: RN(190·2^-149 / 127) = 2^-149).
+    tiny = np.float32(2.0 ** -149)
+    for rnd in (oracle.RNE, oracle.SR):
+        Y = np.array([[10 * tiny, -10 * tiny, 3 * tiny]], np.float32)
+        q, s = oracle.hq_quantize(Y, oracle.PER_TENSOR, rnd, 1, 0)
+        assert s[0] == tiny and list(q[0]) == [7, -7, 3]
+        q, s = oracle.hq_quantize(Y, oracle.PER_TOKEN, rnd, 1, 0)
+        assert s[0] == tiny and list(q[0]) == [7, -7, 3]
+    v = np.array([190 * tiny, -190 * tiny, 5 * tiny], np.float32)
+    q8, s8 = oracle.int8_quantize(v)
+    assert s8 == tiny and list(q8) == [127, -127, 5]
+    q4, s4 = oracle.rne_quantize(v[:2] / np.float32(19), 7)
+    assert s4 == tiny and list(q4) == [7, -7]
+
+
+def test_scaling_divides_by_the_scale():
+    """x = RN(v / s) by IEEE division, not v times a rounded reciprocal:
+    with s = 7·2^-10 (1/s is inexact) and v = 6.5·s, v / s is the exact tie
+    6.5, whose even neighbour is 6, while v·RN(1/s) rounds to 6.5000005,
+    which goes to 7."""
+    s = np.float32(7 * 2.0 ** -10)
+    for qmax in (7, 127):
+        v = np.array([qmax * s, 6.5 * s, -6.5 * s, 2.5 * s], np.float32)
+        q, sc = oracle.rne_quantize(v, qmax)
+        assert sc == s and list(q) == [qmax, 6, -6, 2]
+    Y = np.array([[7 * s, 6.5 * s, -6.5 * s, 2.5 * s]], np.float32)
+    for gran in (oracle.PER_TENSOR, oracle.PER_TOKEN):
+        q, sc = oracle.hq_quantize(Y, gran, oracle.RNE, 0, 0)
+        assert sc[0] == s and list(q[0]) == [7, 6, -6, 2]
 
 
 def test_sr_error_bound_and_determinism():
@@ -670,6 +702,76 @@ def test_gx_path_lossless_equals_gy_w():
             assert np.allclose(r["g_x"], want, rtol=1e-12, atol=1e-15)
 
 
+def _with_coefficients(C, axis):
+    """Data whose exact 16-block Hadamard transform is C: along columns
+    (axis 0, as for g_y in the g_x path) or along rows (axis 1, as for w and
+    for the along-token transforms).  D is symmetric and D^-1 = D/16."""
+    if axis == 0:
+        D = np.kron(np.eye(C.shape[1] // 16, dtype=np.int64), H_SCIPY)
+        return (C @ D / 16.0).astype(np.float32)
+    D = np.kron(np.eye(C.shape[0] // 16, dtype=np.int64), H_SCIPY)
+    return (D @ C / 16.0).astype(np.float32)
+
+
+def _sr_half(seed, stream, e):
+    """SR code of a value at exactly 1/2 with scale 1: 1 when the Philox
+    word's top 24 bits give u < 1/2."""
+    return 1 if (oracle.philox_word(seed, stream, e) >> 8) < (1 << 23) else 0
+
+
+def test_path_streams_scales_and_element_indices():
+    """Which Philox stream, element index and scale each quantized operand
+    of the HQ paths takes: g_y stream 0 at t·Cout + c, one scale per token
+    or per tensor; w stream 1 at o·Cin + i of the transformed [Cout, Cin]
+    tensor, one scale per tensor; the g_w ablation's g_y and x streams 2 and
+    3 at t·C + c of their along-token transforms, one scale each.  Each
+    operand is built so that its exact transform is 1/2 everywhere but for a
+    7, so every other code shows the word it drew."""
+    seed = 31
+    T, Cin, Cout = 32, 16, 32
+    Cg = np.full((T, Cout), 0.5)
+    Cg[:, 0] = 7.0
+    Cg[1, 0] = 0.5                                   # token 1 has no 7
+    Cw = np.full((Cout, Cin), 0.5)
+    Cw[0, 0] = 7.0
+    gy = _with_coefficients(Cg, 0)
+    w = _with_coefficients(Cw, 1)
+    for gran in (oracle.PER_TOKEN, oracle.PER_TENSOR):
+        r = oracle.gx_path(gy, w, gran_gy=gran, rnd=oracle.SR, seed=seed)
+        assert np.array_equal(r["Y"], Cg.astype(np.float32))
+        assert list(r["s_w"]) == [1.0]
+        for o in range(Cout):
+            for i in range(Cin):
+                want = 7 if (o, i) == (0, 0) else _sr_half(seed, 1, o * Cin + i)
+                assert r["qW"][i, o] == want, (o, i)
+        if gran == oracle.PER_TOKEN:
+            assert r["s_gy"][1] == np.float32(0.5) / np.float32(7)
+            assert np.all(r["qY"][1] == 7)           # its own scale: 1/2 -> 7
+            assert np.all(np.delete(r["s_gy"], 1) == 1.0)
+        else:
+            assert list(r["s_gy"]) == [1.0]
+        for t in range(T):
+            if gran == oracle.PER_TOKEN and t == 1:
+                continue
+            for c in range(Cout):
+                want = 7 if Cg[t, c] == 7 else _sr_half(seed, 0, t * Cout + c)
+                assert r["qY"][t, c] == want, (t, c)
+    Cg2 = np.full((T, Cout), 0.5)
+    Cg2[0, 0] = 7.0
+    Cx2 = np.full((T, Cin), 0.5)
+    Cx2[3, 5] = -7.0
+    r = oracle.gw_hq_path(_with_coefficients(Cg2, 1), _with_coefficients(Cx2, 1),
+                          rnd=oracle.SR, seed=seed)
+    assert list(r["s_g"]) == [1.0] and list(r["s_x"]) == [1.0]
+    for t in range(T):
+        for c in range(Cout):
+            want = 7 if (t, c) == (0, 0) else _sr_half(seed, 2, t * Cout + c)
+            assert r["qG"][c, t] == want, (t, c)
+        for c in range(Cin):
+            want = -7 if (t, c) == (3, 5) else _sr_half(seed, 3, t * Cin + c)
+            assert r["qX"][c, t] == want, (t, c)
+
+
 def test_gw_path_lossless_equals_gyT_x():
     rng = np.random.default_rng(18)
     T, Cin, Cout = 64, 20, 24
@@ -685,6 +787,42 @@ def test_gw_path_lossless_equals_gyT_x():
     r = oracle.gw_path(gy, q, s, 8)
     # lossless only if every coefficient is an integer multiple of its scale
     assert np.array_equal(r["qG"].astype(np.float64) * r["s_g"], r["Gb"])
+    want = gy.astype(np.float64).T @ x.astype(np.float64)
+    assert np.allclose(r["g_w"], want, rtol=1e-12, atol=1e-15)
+
+
+def _in_kept_span(K, rank, s):
+    """[T, C] data whose rank-`rank` HLA coefficients are exactly K·s
+    (K [C, T·rank/16] integer codes): per 16-token block, the combination
+    (1/16)·Σ_k K[:, rank·b + k]·H[σ(k)] of the kept Walsh rows, which are
+    orthogonal with squared norm 16."""
+    C, Tp = K.shape
+    T = Tp // rank * 16
+    rows = np.array([H_SCIPY[gray_bitrev_sequency(k)] for k in range(rank)])
+    out = np.zeros((T, C))
+    for b in range(T // 16):
+        out[16 * b:16 * b + 16] = rows.T @ K[:, rank * b:rank * b + rank].T / 16.0
+    return (out * s).astype(np.float32)
+
+
+@pytest.mark.parametrize("rank", [1, 2, 4, 8, 16])
+def test_gw_path_lossless_every_rank(rank):
+    """Data in the span of the kept Walsh rows loses nothing at rank r:
+    with codes whose maximum is 127 and power-of-two scales, the int8 codes
+    are the constructed ones and g_w equals g_yᵀx exactly (Parseval over the
+    kept rows: Σ_t g_t x_t = (1/16) Σ_k G_k X_k per block)."""
+    rng = np.random.default_rng(60 + rank)
+    T, Cin, Cout = 64, 12, 20
+    Tp = T * rank // 16
+    Kg = rng.integers(-127, 128, (Cout, Tp))
+    Kx = rng.integers(-127, 128, (Cin, Tp))
+    Kg[0, 0], Kx[1, -1] = 127, -127
+    gy = _in_kept_span(Kg, rank, 2.0 ** -7)
+    x = _in_kept_span(Kx, rank, 2.0 ** -3)
+    q, s = oracle.compress_activation(x, rank)
+    assert s == np.float32(2.0 ** -3) and np.array_equal(q, Kx)
+    r = oracle.gw_path(gy, q, s, rank)
+    assert r["s_g"] == np.float32(2.0 ** -7) and np.array_equal(r["qG"], Kg)
     want = gy.astype(np.float64).T @ x.astype(np.float64)
     assert np.allclose(r["g_w"], want, rtol=1e-12, atol=1e-15)
 
