@@ -133,6 +133,26 @@ MUTANTS = [
     ("ablation x along channels", PY, "Yx = hq_transform(x, axis=1)",
      "Yx = hq_transform(x, axis=0)"),
     ("g_w rank fixed at 8", PY, "Gb = hla_transform(g_y, rank)", "Gb = hla_transform(g_y, 8)"),
+    ("stored activation rank fixed at 8", PY, "Xb = hla_transform(x, rank)",
+     "Xb = hla_transform(x, 8)"),
+    ("per-channel scales ignored", PY, "    if not per_channel:\n        return rne_quantize",
+     "    if True:\n        return rne_quantize"),
+    ("g_x ablation w as int4", PY, "qW, s_w = int8_quantize(Wb)",
+     "qW, s_w = rne_quantize(Wb, 7)"),
+    ("g_x ablation scale of w used twice", PY,
+     "g_x = dequant_gx(acc, np.array([s_g], np.float32), PER_TENSOR, s_w)",
+     "g_x = dequant_gx(acc, np.array([s_w], np.float32), PER_TENSOR, s_w)"),
+    ("LQS comparison reversed", PY,
+     "choice = PER_TOKEN if m_tensor > threshold * m_token else PER_TENSOR",
+     "choice = PER_TOKEN if m_token > threshold * m_tensor else PER_TENSOR"),
+    ("LQS threshold ignored", PY,
+     "choice = PER_TOKEN if m_tensor > threshold * m_token else PER_TENSOR",
+     "choice = PER_TOKEN if m_tensor > m_token else PER_TENSOR"),
+    ("LQS error with SR", PY, "q, s = hq_quantize(Y, gran, RNE, 0, STREAM_GY)",
+     "q, s = hq_quantize(Y, gran, SR, 0, STREAM_GY)"),
+    ("LQS error with the first token's scale", PY,
+     "sc = (np.asarray(s, np.float64)[:, None] if gran == PER_TOKEN",
+     "sc = (np.float64(s[0]) if gran == PER_TOKEN"),
     ("g_w channel scales collapsed", PY,
      "g_w = dequant_gw(acc, s_g, s_x)\n    return dict(Gb=Gb",
      "g_w = dequant_gw(acc, s_g, np.max(s_x))\n    return dict(Gb=Gb"),
