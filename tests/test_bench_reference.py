@@ -1,0 +1,52 @@
+"""The benchmark's reference arm: the CPU oracle timed on a token sample of
+the benchmark's workload.  Its JSON line carries the keys of the
+benchmark's own line with the same metric, unit and config; ranks other
+than 0 of a multi-process launch exit 0 without work."""
+import json
+import os
+import subprocess
+import sys
+
+import workloads
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _run(env_extra=None, *args):
+    env = dict(os.environ)
+    env.update(env_extra or {})
+    return subprocess.run(
+        [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+         "--steps", "2", "--warmup", "1", "--ref-sample-tokens", "64", *args],
+        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+
+
+def test_reference_arm_line():
+    r = _run()
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference"
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data",
+                "config", "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert (d["n_gpus"], d["steps"], d["warmup"]) == (1, 2, 1)
+    assert d["unit"] == "us/layer" and d["higher_is_better"] is False
+    assert d["value"] > 0 and abs(d["ms_per_step"] * 1e3 - d["value"]) <= 1e-9 * d["value"]
+    assert d["vs_baseline"] is None and d["data"] == "synthetic"
+    wl = workloads.WORKLOADS[1]
+    assert d["config"]["workload"] == wl.name
+    assert (d["config"]["T"], d["config"]["Cin"], d["config"]["Cout"]) == (wl.T, wl.Cin, wl.Cout)
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"]
+    assert cb["unit"] == d["unit"] and "64" in cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"],
+                        "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_reference_arm_other_ranks_exit_without_work():
+    r = _run({"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"}, "--gpus", "2")
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert r.stdout.strip() == ""
