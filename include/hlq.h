@@ -320,7 +320,8 @@ hlq_status hlq_debug_gemm_plan(int64_t T, int64_t Cin, int64_t Cout, int rank, i
 /*
  * Layer-wise quantizer selection for the HQ of g_y (HOT summary page,
  * Approach: per-token or per-tensor quantizer chosen per layer; Limitations:
- * chosen on a calibration set with a 50 % MSE-difference threshold).  On a
+ * the choice comes from calibration data, switching where the two
+ * quantizers' errors differ by half).  On a
  * calibration sample d_gy [T, Cout] (dtype dt): Y = the 16-point Hadamard
  * transform along Cout as in hlq_linear_backward_gx, quantized to int4 with
  * round-to-nearest-even codes at both granularities,

@@ -313,7 +313,8 @@ def hq_mse(Y, gran: int) -> float:
 def lqs_select(g_y, threshold: float = 1.5):
     """Layer-wise quantizer selection for the HQ of g_y (HOT summary page,
     Approach: per-token or per-tensor quantizer chosen per layer; Limitations:
-    a calibration set and a 50 % MSE-difference threshold): per-token iff the
+    the choice comes from calibration data, switching where the two
+    quantizers' errors differ by half): per-token iff the
     per-tensor MSE exceeds the per-token MSE by more than 50 %.  Returns
     (choice, mse_per_tensor, mse_per_token)."""
     Y = hq_transform(g_y, axis=0)

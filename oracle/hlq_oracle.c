@@ -18,7 +18,7 @@
  *    stored activation compressed at forward time (ACBP).
  *  - "HOT: Hadamard-based Optimized Training" (atlas summary), Approach:
  *    int4 HQ on the activation-gradient path, HLA + int8 on the weight-gradient
- *    path, compression of stored activations at forward time, and a per-token
+ *    path, the saved activation compressed when the forward pass runs, a per-token
  *    vs per-tensor quantizer chosen per layer.
  *
  * Readings where the pages are silent (block 16, rank 8, int4 range [-7,7],
