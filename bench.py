@@ -28,6 +28,7 @@ from __future__ import annotations
 import argparse
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -218,6 +219,28 @@ def oracle_layer_seconds(wl, inp, tokens):
     return t_w, t_tok
 
 
+def host_cpu(cpuinfo="/proc/cpuinfo"):
+    """The host the oracle runs on: machine, logical CPUs, and the CPU model
+    where /proc/cpuinfo names one (Arm hosts give implementer and part
+    codes instead).  Never raises."""
+    info = {"machine": platform.machine(), "nproc": os.cpu_count(), "model": None}
+    try:
+        fields = {}
+        with open(cpuinfo) as f:
+            for line in f:
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    fields.setdefault(k.strip().lower(), v.strip())
+        if fields.get("model name"):
+            info["model"] = fields["model name"]
+        elif fields.get("cpu implementer") or fields.get("cpu part"):
+            info["model"] = (f"implementer {fields.get('cpu implementer')} "
+                             f"part {fields.get('cpu part')}")
+    except (OSError, UnicodeDecodeError):
+        pass
+    return info
+
+
 def cpu_baseline(wl, inp, tokens):
     t_w, t_tok = oracle_layer_seconds(wl, inp, tokens)
     est = t_w + t_tok * (wl.T / tokens)
@@ -225,7 +248,7 @@ def cpu_baseline(wl, inp, tokens):
             "sample": (f"oracle on the first {tokens} of {wl.T} tokens "
                        f"({t_tok:.2f} s) scaled by T/{tokens}, plus the full "
                        f"HQ of w ({t_w:.2f} s); single thread"),
-            "measured_s": t_w + t_tok}
+            "measured_s": t_w + t_tok, "host": host_cpu()}
 
 
 # ----------------------------------------------------------------------------
@@ -252,7 +275,7 @@ def run_reference(args, wl, rank, world):
         "vs_baseline": None, "dtype": "int64", "data": "synthetic",
         "config": config_of(wl),
         "cpu_baseline": {"value": us, "unit": UNIT, "cores": 1,
-                         "kind": "oracle", "sample": sample},
+                         "kind": "oracle", "sample": sample, "host": host_cpu()},
         "e2e": {"value": us, "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }

@@ -42,6 +42,7 @@ def test_reference_arm_line():
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"]
     assert cb["unit"] == d["unit"] and "64" in cb["sample"]
+    assert cb["host"]["nproc"] >= 1 and cb["host"]["machine"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"],
                         "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
 
@@ -50,3 +51,38 @@ def test_reference_arm_other_ranks_exit_without_work():
     r = _run({"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"}, "--gpus", "2")
     assert r.returncode == 0, r.stderr[-2000:]
     assert r.stdout.strip() == ""
+
+
+def _bench():
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("bench_under_test",
+                                                  os.path.join(ROOT, "bench.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+def test_cpu_baseline_leg_on_a_small_sample():
+    """The oracle timing leg of the benchmark's own line, on the small
+    workload: a positive per-layer figure scaled from the token sample."""
+    bench = _bench()
+    wl = workloads.WORKLOADS[0]
+    inp = workloads.make_inputs(wl)
+    cb = bench.cpu_baseline(wl, inp, 32)
+    assert cb["kind"] == "oracle" and cb["cores"] == 1 and cb["unit"] == "us/layer"
+    assert cb["value"] > 0 and cb["measured_s"] > 0
+    assert cb["value"] >= cb["measured_s"] * 1e6 * 0.999      # scaled up to all T
+    assert f"first 32 of {wl.T} tokens" in cb["sample"]
+    assert cb["host"]["nproc"] >= 1
+
+
+def test_host_cpu_names_an_arm_part(tmp_path):
+    bench = _bench()
+    f = tmp_path / "cpuinfo"
+    f.write_text("processor\t: 0\nBogoMIPS\t: 2000.00\nCPU implementer\t: 0x41\n"
+                 "CPU architecture: 8\nCPU part\t: 0xd4f\n\nprocessor\t: 1\n"
+                 "CPU implementer\t: 0x41\nCPU part\t: 0xd4f\n")
+    assert bench.host_cpu(str(f))["model"] == "implementer 0x41 part 0xd4f"
+    f.write_text("processor\t: 0\nmodel name\t: Some CPU @ 3.0GHz\n")
+    assert bench.host_cpu(str(f))["model"] == "Some CPU @ 3.0GHz"
+    assert bench.host_cpu(str(tmp_path / "missing"))["model"] is None
