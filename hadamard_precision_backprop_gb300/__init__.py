@@ -176,10 +176,25 @@ def _dtype_code(t) -> int:
     raise TypeError(f"unsupported dtype {t.dtype}: use bfloat16 or float32")
 
 
-def _need_cuda_contig(*ts):
+def _need_cuda_contig(*ts, current_device=None):
+    """Contiguous CUDA tensors, all on the current device (the library
+    launches on the current device and stream)."""
+    index = None
     for t in ts:
-        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+        if t is None:
+            continue
+        if not t.is_cuda or not t.is_contiguous():
             raise ValueError("tensors must be contiguous CUDA tensors")
+        if index is None:
+            index = t.device.index
+        elif t.device.index != index:
+            raise ValueError(f"tensors must be on one device (cuda:{index} and "
+                             f"cuda:{t.device.index})")
+    if index is not None:
+        cur = _torch().cuda.current_device() if current_device is None else current_device
+        if index != cur:
+            raise ValueError(f"tensors are on cuda:{index} but cuda:{cur} is current; "
+                             "make their device current first")
 
 
 def hlq_workspace_bytes(op: int, T: int, Cin: int, Cout: int, block: int = 16,

@@ -288,3 +288,30 @@ def test_product_path_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(hlq, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="not built"):
         hlq.lib()
+
+
+class _FakeTensor:
+    """Stands in for a CUDA tensor: only what the binding's checks read."""
+
+    def __init__(self, index, cuda=True, contiguous=True):
+        self.is_cuda = cuda
+        self._contiguous = contiguous
+        self.device = type("Dev", (), {"index": index})()
+
+    def is_contiguous(self):
+        return self._contiguous
+
+
+def test_binding_checks_tensors_and_their_device():
+    check = hlq._need_cuda_contig
+    check(_FakeTensor(0), None, _FakeTensor(0), current_device=0)
+    check(_FakeTensor(1), _FakeTensor(1), current_device=1)
+    check(None, current_device=0)                       # nothing to check
+    with pytest.raises(ValueError, match="contiguous CUDA"):
+        check(_FakeTensor(0, cuda=False), current_device=0)
+    with pytest.raises(ValueError, match="contiguous CUDA"):
+        check(_FakeTensor(0, contiguous=False), current_device=0)
+    with pytest.raises(ValueError, match="one device"):
+        check(_FakeTensor(0), _FakeTensor(1), current_device=0)
+    with pytest.raises(ValueError, match="is current"):
+        check(_FakeTensor(1), _FakeTensor(1), current_device=0)
