@@ -6,8 +6,11 @@ One step = the whole hot path on one batch of synthetic input:
   backward pass: g_x through int4 Hadamard quantization
   (hlq_linear_backward_gx) and g_w through the Hadamard low-rank
   approximation with int8 (hlq_linear_backward_gw).
-Default workload: the ViT-B qkv layer, T = 64 x 197 = 12608 tokens,
-Cin = 768, Cout = 2304, bf16 inputs, per-token g_y quantizer.
+Default workload: the largest single-GPU layer of the five, a Llama-3-8B
+MLP down_proj: T = 8 x 2048 = 16384 tokens, Cin = 14336, Cout = 4096, bf16
+inputs, per-token g_y quantizer.  The other layers (ViT-B qkv and fc2,
+ResNet-50 3x3 im2col, the small single linear) are timed the same way in the
+line's `per_workload` block.
 
 Prints one JSON line (rank 0).  `value` is microseconds per layer step
 (lower is better), device-timed with CUDA events on the launching stream,
@@ -17,11 +20,17 @@ inputs resident in HBM, L2 flushed (256 MiB write) before every timed step.
 device -> host copies of g_x, g_w inside the timed region, pipelined with the
 kernels by the library.
 `roofline` is for the kernel with the largest device time, from per-launch
-CUDA events recorded by libhlq's tracing hooks; `cpu_baseline` times the CPU
-oracle on a bounded token sample on this host.
+CUDA events recorded by libhlq's tracing hooks.  Algorithmic bytes follow the
+method's data sizes, not the library's storage layout: one read of each
+input, int4 codes at half a byte, int8 codes at one byte, the scales; a
+per-tensor maximum pre-pass re-reads its input and is credited with no bytes;
+the GEMMs are credited with their integer operations, their roofline time
+being max(ops / tensor peak, (operands + output) / HBM peak).
+`cpu_baseline` times the CPU oracle on a bounded sample of the workload on
+this host and extrapolates it linearly to the whole layer.
 
 --impl reference times the CPU oracle itself (the only reference there is)
-per step on a bounded token sample and prints the same metric.
+per step on a bounded sample and prints the same metric.
 """
 from __future__ import annotations
 
@@ -48,19 +57,24 @@ UNIT = "us/layer"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0,
                   "bf16_tflops_sustained": 1700.0}
 NOMINAL_FP8_OVER_BF16 = 4.5 / 2.25
+DEFAULT_WORKLOAD = workloads.WORKLOADS[3]   # Llama-3-8B down_proj: the largest
 
 
-def parse_args():
+def parse_args(argv=None):
     p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=20)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", default=workloads.WORKLOADS[1].name,
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD.name,
                    help="workload name or index into workloads.WORKLOADS")
-    p.add_argument("--cpu-sample-tokens", type=int, default=4096)
-    p.add_argument("--ref-sample-tokens", type=int, default=512)
+    p.add_argument("--cpu-sample-tokens", type=int, default=256)
+    p.add_argument("--cpu-sample-w-rows", type=int, default=512)
+    p.add_argument("--ref-sample-tokens", type=int, default=16)
+    p.add_argument("--ref-sample-w-rows", type=int, default=64)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-per-workload", action="store_true",
+                   help="time only the main workload")
     p.add_argument("--serial", action="store_true",
                    help="time the g_x and g_w branches one after the other "
                         "instead of concurrently (hlq_linear_backward)")
@@ -70,7 +84,7 @@ def parse_args():
     p.add_argument("--no-variants", action="store_true",
                    help="skip the timings of the optional paths (int4 / "
                         "per-channel ACBP, quantizer selection, ablations)")
-    return p.parse_args()
+    return p.parse_args(argv)
 
 
 def pick_workload(spec):
@@ -92,44 +106,141 @@ def load_peaks():
 
 
 # ----------------------------------------------------------------------------
-# algorithmic work per kernel launch
+# algorithmic work per kernel launch and per step of the method
 # ----------------------------------------------------------------------------
 
-def algorithmic(name, wl, e):
-    """(bound, amount) of one launch: bytes for HBM-bound kernels, ops for
-    the GEMMs.  Reads count the input once, writes count the codes/scales.
-    The per-tensor amax pre-passes re-read the input; they are credited with
-    that read."""
+def _sizes(wl, xbar_bits=8):
+    """Bytes of the method's data: element size of the inputs, and the
+    code bytes of each quantized tensor (int4 at half a byte, int8 at one)."""
     T, Cin, Cout, Tp = wl.T, wl.Cin, wl.Cout, wl.Tp
+    e = 2 if wl.dtype == "bf16" else 4
     per_tok = wl.gran_gy == workloads.PER_TOKEN
+    return dict(
+        e=e,
+        gy=T * Cout * e, x=T * Cin * e, w=Cout * Cin * e,
+        qy=T * Cout // 2, s_gy=4 * T if per_tok else 4,       # HQ of g_y: int4
+        qw=Cin * Cout // 2, s_w=4,                            # HQ of w: int4
+        qg=Cout * Tp, s_g=4,                                  # HLA of g_y: int8
+        xb=Cin * Tp if xbar_bits == 8 else Cin * Tp // 2, s_x=4,   # ACBP codes
+        gx=T * Cin * 4, gw=Cout * Cin * 4,                    # fp32 outputs
+        ops_gx=2 * T * Cin * Cout, ops_gw=2 * Cout * Cin * Tp)
+
+
+# kernel -> (step of the method it belongs to, how it is credited)
+KERNEL_ROWS = {
+    "hla_x_amax": "a1", "hla_x_quant": "a1",
+    "hq_rows_amax": "a2", "hq_rows_quant": "a2",
+    "hq_cols_amax": "a3", "hq_cols_quant": "a3",
+    "gemm_gx_tc": "a4",
+    "hla_gy_amax": "a5", "hla_gy_quant": "a5",
+    "widen_xbar": "a6", "gemm_gw_tc": "a6",
+}
+ROW_NAMES = {"a1": "ACBP compression of x", "a2": "HQ of g_y", "a3": "HQ of w",
+             "a4": "g_x GEMM + dequant", "a5": "HLA of g_y",
+             "a6": "g_w GEMM + dequant"}
+
+
+def algorithmic(name, wl, xbar_bits=8):
+    """What one launch of `name` is credited with: ("hbm", bytes) for the
+    transform/quantize kernels, ("ops", integer ops, bytes) for the GEMMs.
+
+    Bytes are the method's: one read of the input plus the codes (int4 at
+    0.5 B, int8 at 1 B) and scales written.  The quantize pass of a
+    per-tensor quantizer carries them; its maximum pre-pass re-reads the
+    input and is credited with nothing, as is the int8 -> bf16 widening of
+    the stored activation (a layout step, not one of the method)."""
+    s = _sizes(wl, xbar_bits)
     table = {
-        "hla_x_amax": ("hbm", T * Cin * e),
-        "hla_x_quant": ("hbm", T * Cin * e + Cin * Tp),
-        "hq_rows_amax": ("hbm", T * Cout * e),
-        "hq_rows_quant": ("hbm", T * Cout * e + T * Cout + (4 * T if per_tok else 4)),
-        "hq_cols_amax": ("hbm", Cout * Cin * e),
-        "hq_cols_quant": ("hbm", Cout * Cin * e + Cin * Cout),
-        "hla_gy_amax": ("hbm", T * Cout * e),
-        "hla_gy_quant": ("hbm", T * Cout * e + Cout * Tp * 2),
-        "widen_xbar": ("hbm", Cin * Tp * 3),
-        "gemm_gx": ("ops", 2 * T * Cin * Cout),
-        "gemm_gw": ("ops", 2 * Cout * Cin * Tp),
+        "hla_x_amax": ("hbm", 0),
+        "hla_x_quant": ("hbm", s["x"] + s["xb"] + s["s_x"]),
+        "hq_rows_amax": ("hbm", 0),
+        "hq_rows_quant": ("hbm", s["gy"] + s["qy"] + s["s_gy"]),
+        "hq_cols_amax": ("hbm", 0),
+        "hq_cols_quant": ("hbm", s["w"] + s["qw"] + s["s_w"]),
+        "hla_gy_amax": ("hbm", 0),
+        "hla_gy_quant": ("hbm", s["gy"] + s["qg"] + s["s_g"]),
+        "widen_xbar": ("hbm", 0),
+        "gemm_gx_tc": ("ops", s["ops_gx"], s["qy"] + s["qw"] + s["gx"]),
+        "gemm_gw_tc": ("ops", s["ops_gw"], s["qg"] + s["xb"] + s["gw"]),
     }
-    return table.get(name.replace("_simple", "").replace("_tc", ""), ("hbm", 0))
+    return table.get(name, ("hbm", 0))
 
 
-def kernel_peak(name, peaks, sustained):
-    """(bound label, peak, unit) for a kernel; GEMM peaks per operand type."""
+ROW_WORK = {  # algorithmic work of each step of the method (same sizes)
+    "a1": lambda s: ("hbm", s["x"] + s["xb"] + s["s_x"]),
+    "a2": lambda s: ("hbm", s["gy"] + s["qy"] + s["s_gy"]),
+    "a3": lambda s: ("hbm", s["w"] + s["qw"] + s["s_w"]),
+    "a4": lambda s: ("ops", s["ops_gx"], s["qy"] + s["qw"] + s["gx"]),
+    "a5": lambda s: ("hbm", s["gy"] + s["qg"] + s["s_g"]),
+    "a6": lambda s: ("ops", s["ops_gw"], s["qg"] + s["xb"] + s["gw"]),
+}
+
+
+def tensor_peak(name, peaks, sustained=False):
+    """Tensor-pipe peak (TFLOP/s) of a GEMM by operand type: E4M3 operands on
+    the FP8 pipe (the measured bf16 figure x the nominal FP8/BF16 ratio),
+    bf16 operands at the measured bf16 figure."""
     bf16 = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
-    if name.endswith("_simple"):
-        # CUDA-core dp4a GEMM: 152 SMs x 64 dp4a/clk (assumed half rate)
-        # x 8 int ops x 2.07 GHz
-        return "alu", 152 * 64 * 8 * 2.07e9 / 1e12, "TOPS"
-    if name.startswith("gemm_gx"):       # E4M3 operands on the FP8 tensor pipe
-        return "tensor", bf16 * NOMINAL_FP8_OVER_BF16, "TFLOP/s"
-    if name.startswith("gemm_gw"):       # bf16 operands
-        return "tensor", bf16, "TFLOP/s"
-    return "hbm", peaks["hbm_gbs"], "GB/s"
+    if name.startswith("gemm_gx") or name == "a4":
+        return bf16 * NOMINAL_FP8_OVER_BF16
+    return bf16
+
+
+def roofline_of(name, work, seconds, peaks):
+    """Achieved rate and fraction of the binding roof for `work` done in
+    `seconds`.  A GEMM's roof time is max(ops / tensor peak, bytes / HBM
+    peak); the achieved figure is given in the unit of the binding roof."""
+    hbm = peaks["hbm_gbs"] * 1e9
+    if work[0] == "hbm":
+        achieved = work[1] / seconds / 1e9
+        return {"bound": "hbm", "achieved": achieved, "unit": "GB/s",
+                "peak": peaks["hbm_gbs"], "frac": achieved / peaks["hbm_gbs"],
+                "algorithmic": work[1]}
+    ops, nbytes = work[1], work[2]
+    tp = tensor_peak(name, peaks) * 1e12
+    if ops / tp >= nbytes / hbm:
+        achieved = ops / seconds / 1e12
+        return {"bound": "tensor", "achieved": achieved, "unit": "TFLOP/s",
+                "peak": tp / 1e12, "frac": achieved / (tp / 1e12),
+                "algorithmic": ops, "bytes": nbytes}
+    achieved = nbytes / seconds / 1e9
+    return {"bound": "hbm", "achieved": achieved, "unit": "GB/s",
+            "peak": peaks["hbm_gbs"], "frac": achieved / peaks["hbm_gbs"],
+            "algorithmic": nbytes, "ops": ops}
+
+
+def kernel_table(launches, wl, peaks, xbar_bits=8):
+    """Per-kernel and per-step summaries of traced launches [(name, ms)]."""
+    per_kernel = {}
+    for name, kms in launches:
+        d = per_kernel.setdefault(name, [0, 0.0])
+        d[0] += 1
+        d[1] += kms
+    total = sum(v[1] for v in per_kernel.values()) or 1.0
+    kernels = {}
+    for name, (n, tot) in sorted(per_kernel.items(), key=lambda kv: -kv[1][1]):
+        avg_s = tot / n / 1e3
+        entry = {"launches": n, "avg_us": avg_s * 1e6, "share": tot / total,
+                 "row": KERNEL_ROWS.get(name)}
+        work = algorithmic(name, wl, xbar_bits)
+        if work[1] > 0:
+            entry.update(roofline_of(name, work, avg_s, peaks))
+        else:
+            entry.update({"bound": "hbm", "achieved": 0.0, "frac": 0.0,
+                          "note": ("a re-read or layout pass: the method's bytes are "
+                                   "credited to the step's other pass")})
+        kernels[name] = entry
+    s = _sizes(wl, xbar_bits)
+    rows = {}
+    for row, fn in ROW_WORK.items():
+        names = [k for k, r in KERNEL_ROWS.items() if r == row and k in kernels]
+        if not names:
+            continue
+        us = sum(kernels[k]["avg_us"] for k in names)
+        r = roofline_of(row, fn(s), us / 1e6, peaks)
+        r.update({"what": ROW_NAMES[row], "us": us, "kernels": names})
+        rows[row] = r
+    return kernels, rows
 
 
 # ----------------------------------------------------------------------------
@@ -193,20 +304,27 @@ class ClockSampler:
 # CPU oracle timing (test infrastructure: only this leg runs it)
 # ----------------------------------------------------------------------------
 
-def oracle_layer_seconds(wl, inp, tokens):
-    """Oracle time of one layer step on the first `tokens` tokens, plus the
-    token-independent part (the HQ of w), in seconds."""
+def oracle_layer_seconds(wl, inp, tokens, w_rows=None):
+    """Oracle time of one layer step split into its two parts, in seconds:
+    the HQ of w on its first `w_rows` rows (whole 16-row blocks; all rows by
+    default), and everything that grows with the token count (compression
+    of x, HQ and HLA of g_y, both integer GEMMs, the dequantizations) on the
+    first `tokens` tokens.  Each part is linear in its sample size."""
     import oracle
     oracle.build()
     Ts = tokens
+    rows = wl.Cout if w_rows is None else max(16, min(wl.Cout, w_rows // 16 * 16))
     gy = inp["g_y"][:Ts]
     x = inp["x"][:Ts]
     t0 = time.perf_counter()
-    Wt = oracle.hq_transform(inp["w"], 1)
+    Wt = oracle.hq_transform(inp["w"][:rows], 1)
     qWt, s_w = oracle.hq_quantize(Wt, oracle.PER_TENSOR, oracle.SR, wl.seed,
                                   oracle.STREAM_W)
-    qW = np.ascontiguousarray(qWt.T)
     t_w = time.perf_counter() - t0
+    # the g_x GEMM contracts over all Cout: the sampled rows of w stand in
+    # for every block (timing only; the codes are not compared here)
+    reps = wl.Cout // rows
+    qW = np.ascontiguousarray(np.tile(qWt, (reps, 1)).T)
     t1 = time.perf_counter()
     qx, s_x = oracle.compress_activation(x, wl.rank)
     Y = oracle.hq_transform(gy, 0)
@@ -216,7 +334,7 @@ def oracle_layer_seconds(wl, inp, tokens):
     oracle.dequant_gx(acc, s_gy, wl.gran_gy, s_w[0])
     oracle.gw_path(gy, qx, s_x, wl.rank)
     t_tok = time.perf_counter() - t1
-    return t_w, t_tok
+    return t_w * (wl.Cout / rows), t_tok, rows
 
 
 def host_cpu(cpuinfo="/proc/cpuinfo"):
@@ -241,14 +359,23 @@ def host_cpu(cpuinfo="/proc/cpuinfo"):
     return info
 
 
-def cpu_baseline(wl, inp, tokens):
-    t_w, t_tok = oracle_layer_seconds(wl, inp, tokens)
+def _sample_text(wl, tokens, rows, t_tok=None, t_w=None):
+    tok = f" ({t_tok:.2f} s)" if t_tok is not None else ""
+    wpart = (f"the HQ of w on {rows} of {wl.Cout} rows"
+             + (f" ({t_w * rows / wl.Cout:.2f} s)" if t_w is not None else "")
+             + (f" scaled by Cout/{rows}" if rows < wl.Cout else ""))
+    return (f"oracle on the first {tokens} of {wl.T} tokens{tok} (compression, "
+            f"HQ and HLA of g_y, both integer GEMMs) scaled by T/{tokens}, plus "
+            f"{wpart}; single thread; extrapolated linearly")
+
+
+def cpu_baseline(wl, inp, tokens, w_rows=None):
+    t_w, t_tok, rows = oracle_layer_seconds(wl, inp, tokens, w_rows)
     est = t_w + t_tok * (wl.T / tokens)
     return {"value": est * 1e6, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": (f"oracle on the first {tokens} of {wl.T} tokens "
-                       f"({t_tok:.2f} s) scaled by T/{tokens}, plus the full "
-                       f"HQ of w ({t_w:.2f} s); single thread"),
-            "measured_s": t_w + t_tok, "host": host_cpu()}
+            "sample": _sample_text(wl, tokens, rows, t_tok, t_w),
+            "extrapolated": tokens < wl.T or rows < wl.Cout,
+            "measured_s": t_w * rows / wl.Cout + t_tok, "host": host_cpu()}
 
 
 # ----------------------------------------------------------------------------
@@ -258,24 +385,24 @@ def cpu_baseline(wl, inp, tokens):
 def run_reference(args, wl, rank, world):
     if rank != 0:
         return 0
-    inp = workloads.make_inputs(wl, T=max(args.ref_sample_tokens, 16))
+    tokens = max(16, args.ref_sample_tokens // 16 * 16)
+    inp = workloads.make_inputs(wl, T=tokens)
     per_step = []
+    rows = wl.Cout
     for i in range(args.warmup + args.steps):
-        t_w, t_tok = oracle_layer_seconds(wl, inp, args.ref_sample_tokens)
+        t_w, t_tok, rows = oracle_layer_seconds(wl, inp, tokens, args.ref_sample_w_rows)
         if i >= args.warmup:
-            per_step.append(t_w + t_tok * (wl.T / args.ref_sample_tokens))
+            per_step.append(t_w + t_tok * (wl.T / tokens))
     us = statistics.mean(per_step) * 1e6
-    sample = (f"oracle on the first {args.ref_sample_tokens} of {wl.T} tokens "
-              f"per step, token part scaled by T/{args.ref_sample_tokens}, "
-              "plus the full HQ of w; single thread")
     line = {
         "impl": "reference", "metric": METRIC, "value": us, "unit": UNIT,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": us / 1e3, "higher_is_better": False, "scaling": "weak",
         "vs_baseline": None, "dtype": "int64", "data": "synthetic",
         "config": config_of(wl),
-        "cpu_baseline": {"value": us, "unit": UNIT, "cores": 1,
-                         "kind": "oracle", "sample": sample, "host": host_cpu()},
+        "cpu_baseline": {"value": us, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": "per step: " + _sample_text(wl, tokens, rows),
+                         "extrapolated": True, "host": host_cpu()},
         "e2e": {"value": us, "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -312,18 +439,12 @@ def config_of(wl):
             "l2": "flushed before every timed step (256 MiB write)"}
 
 
-def run_ours(args, wl, rank, world, local_rank):
+def measure_workload(args, wl, dev, dist, headline):
+    """Device-timed step of one workload, its backward and compression alone,
+    and the per-kernel attribution; for the headline workload also the
+    optional paths, the end-to-end host-buffer step and the clocks."""
     import torch
     import hadamard_precision_backprop_gb300 as hlq
-    from hadamard_precision_backprop_gb300 import build as hbuild
-
-    hbuild.build()
-    hlq.lib()
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
 
     def barrier():
         if dist is not None:
@@ -337,7 +458,7 @@ def run_ours(args, wl, rank, world, local_rank):
             t = torch.from_numpy(inp[name + "_bits"].view(np.int16)).view(torch.bfloat16)
         else:
             t = torch.from_numpy(inp[name])
-        return t.pin_memory()
+        return t.pin_memory() if headline else t
 
     h_x, h_gy, h_w = host_tensor("x"), host_tensor("g_y"), host_tensor("w")
     x, gy, w = (t.to(dev) for t in (h_x, h_gy, h_w))
@@ -413,7 +534,7 @@ def run_ours(args, wl, rank, world, local_rank):
     torch.cuda.synchronize()
     barrier()
     torch.cuda.synchronize()
-    clocks = ClockSampler(local_rank)
+    clocks = ClockSampler(dev.index or 0)
     clocks.start()
     time.sleep(0.3)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
@@ -447,17 +568,7 @@ def run_ours(args, wl, rank, world, local_rank):
             launches += hlq.hlq_trace_end()
     if traced is not None:
         hlq.hlq_trace_free()
-    # the same step from eager launches, for reference (host gaps included)
-    eager = []
-    for _ in range(args.steps):
-        flush.fill_(1)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        step(x, gy, w)
-        b.record(stream)
-        eager.append((a, b))
-    torch.cuda.synchronize()
-    ms_eager = statistics.mean(a.elapsed_time(b) for a, b in eager)
+    del graph, traced
 
     # ---- the optional paths, each timed alone on the same inputs ----------
     # (graph replay, L2 flushed before each replay, mean over the steps)
@@ -496,9 +607,50 @@ def run_ours(args, wl, rank, world, local_rank):
 
     bwd_us = time_replays(backward_only)
     fwd_us = time_replays(forward_only)
+    peaks = load_peaks()
+    kernels, rows = kernel_table(launches, wl, peaks)
+    top = next(iter(kernels))
+    roofline = {k: kernels[top][k] for k in ("bound", "achieved", "peak", "unit", "frac")
+                if k in kernels[top]}
+    roofline.update({"kernel": top, "traffic": load_traffic(top, wl),
+                     "peak_source": peaks["source"]})
+    if "peak" not in roofline:
+        roofline["peak"] = peaks["hbm_gbs"]
+    gemm_s = sum(v["avg_us"] * v["launches"] for k, v in kernels.items()
+                 if k.startswith("gemm")) / args.steps / 1e6
+    gemm_ops = 2 * T * Cin * Cout + 2 * Cout * Cin * Tp
+    gemm_bitops = 2 * T * Cin * Cout * 4 + 2 * Cout * Cin * Tp * 8
+    res = {
+        "ms_per_step": ms,
+        "us_per_layer": ms * 1e3,
+        # each timed alone (graph replays, L2 flushed): the backward from the
+        # stored activation, and the forward-time compression; the step
+        # overlaps the compression with the g_x branch
+        "backward_us": bwd_us,
+        "forward_acbp_us": fwd_us,
+        # vanilla-equivalent work of the backward (two dense GEMMs of
+        # 2*T*Cin*Cout each) per second of the measured backward
+        "effective_tops": 4 * T * Cin * Cout / (bwd_us / 1e6) / 1e12,
+        # integer ops the two GEMMs execute (reduced K = T' on the g_w side),
+        # per second of their traced time; and those ops x operand bits
+        "gemm_int_tops": gemm_ops / gemm_s / 1e12 if gemm_s > 0 else None,
+        "gemm_tbops": gemm_bitops / gemm_s / 1e12 if gemm_s > 0 else None,
+        "roofline": roofline,
+        "kernels": kernels,
+        "rows": rows,
+        "gpu_launches": len(launches),
+        "timing": timing,
+        "clocks": clk,
+        "config": config_of(wl),
+    }
+    if not headline:
+        del x, gy, w, ws0, ws1, ws_step, xbar, gx, gw, flush
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        return res, inp
 
     variants = {}
-    if not args.no_variants and world == 1:
+    if not args.no_variants and (dist is None):
         xb4 = torch.empty(hlq.xbar_shape(T, Cin, wl.rank, 4), dtype=torch.uint8, device=dev)
         sxc = torch.empty(Cin, dtype=torch.float32, device=dev)
         mse = torch.empty(2, dtype=torch.float64, device=dev)
@@ -523,13 +675,11 @@ def run_ours(args, wl, rank, world, local_rank):
                                     gran_w=wl.gran_w, rnd=hlq.SR, seed=wl.seed,
                                     out_gx=gx, out_gw=gw, ws=ws1, xbar_per_channel=True)
 
-        ws_f = hlq.workspace(hlq.OP_BACKWARD_FUSED, T, Cin, Cout, 16, wl.rank, dev)
-
         def step_fused_gy():
             hlq.hlq_compress_activation(x, rank=wl.rank, out=xbar, scale=sx, ws=ws0)
             hlq.hlq_linear_backward(gy, w, xbar, sx, rank=wl.rank, gran_gy=wl.gran_gy,
                                     gran_w=wl.gran_w, rnd=hlq.SR, seed=wl.seed,
-                                    out_gx=gx, out_gw=gw, ws=ws_f, fused_gy=True)
+                                    out_gx=gx, out_gw=gw, ws=ws1, fused_gy=True)
 
         def select():
             hlq.hlq_select_gy_granularity(gy, mse=mse, choice=choice, ws=ws_sel)
@@ -558,6 +708,9 @@ def run_ours(args, wl, rank, world, local_rank):
             except Exception as exc:  # report, do not fail the main line
                 variants[name] = {"us": None, "error": f"{type(exc).__name__}: {exc}"}
         torch.cuda.synchronize()
+        del xb4, sxc, ws_sel, ws_agw, ws_agx, gw_a, gx_a
+        torch.cuda.empty_cache()
+    res["variants"] = variants
 
     # ---- end to end through host buffers ---------------------------------
     # libhlq's host-buffer entry: pinned inputs in, gradients back out, the
@@ -589,71 +742,68 @@ def run_ours(args, wl, rank, world, local_rank):
     e2e = statistics.mean(e2e_ms)
     e2e = max_over_ranks(e2e, dist, dev)
     barrier()
+    res["e2e_ms"] = e2e
+    res["e2e_bytes"] = ((x.numel() + gy.numel() + w.numel()) * e,
+                        (gx.numel() + gw.numel()) * 4)
+    res["acbp_stored_bytes"] = acbp_bytes(T, Cin, wl.rank, e)
+    return res, inp
 
+
+def run_ours(args, wl, rank, world, local_rank):
+    import torch
+    import hadamard_precision_backprop_gb300 as hlq
+    from hadamard_precision_backprop_gb300 import build as hbuild
+
+    hbuild.build()
+    hlq.lib()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+    res, inp = measure_workload(args, wl, dev, dist, headline=True)
+    per_workload = {}
+    if not args.no_per_workload:
+        for other in workloads.WORKLOADS:
+            if other.name == wl.name:
+                continue
+            r, _ = measure_workload(args, other, dev, dist, headline=False)
+            per_workload[other.name] = {
+                k: r[k] for k in ("us_per_layer", "backward_us", "forward_acbp_us",
+                                  "effective_tops", "gemm_int_tops", "roofline",
+                                  "rows", "kernels", "clocks")}
     if rank != 0:
         return 0
 
-    # ---- per-kernel attribution and roofline -----------------------------
-    peaks = load_peaks()
-    per_kernel = {}
-    for name, kms in launches:
-        d = per_kernel.setdefault(name, [0, 0.0])
-        d[0] += 1
-        d[1] += kms
-    kernels = {}
-    for name, (n, tot) in sorted(per_kernel.items(), key=lambda kv: -kv[1][1]):
-        bound, amount = algorithmic(name, wl, e)
-        avg_s = tot / n / 1e3
-        kind, peak, unit = kernel_peak(name, peaks, sustained=False)
-        achieved = amount / avg_s / (1e9 if unit == "GB/s" else 1e12)
-        kernels[name] = {"launches": n, "avg_us": avg_s * 1e6,
-                         "share": tot / sum(v[1] for v in per_kernel.values()),
-                         "bound": kind,
-                         "achieved": achieved, "unit": unit,
-                         "frac": achieved / peak}
-    top = next(iter(kernels))
-    kind, peak, unit = kernel_peak(top, peaks, sustained=False)
-    traffic = load_traffic(top, wl)
-    roofline = {"bound": kind, "kernel": top,
-                "achieved": kernels[top]["achieved"], "peak": peak,
-                "unit": unit, "frac": kernels[top]["achieved"] / peak,
-                "traffic": traffic, "peak_source": peaks["source"]}
-
-    us = job_us_per_layer(ms, world)      # job-wide us per layer step
-    gemm_ops = 2 * T * Cin * Cout + 2 * Cout * Cin * Tp
-    gemm_bitops = 2 * T * Cin * Cout * 4 + 2 * Cout * Cin * Tp * 8
-    gemm_s = sum(v[1] for k, v in per_kernel.items() if k.startswith("gemm")) / args.steps / 1e3
-    bwd_ms, fwd_ms = bwd_us / 1e3, fwd_us / 1e3
+    us = job_us_per_layer(res["ms_per_step"], world)      # job-wide us per layer step
     line = {
         "metric": METRIC, "value": us, "unit": UNIT, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms_per_step"],
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
         "dtype": "int4/int8", "data": "synthetic",
-        "config": config_of(wl),
-        # each timed alone (graph replays, L2 flushed): the backward from the
-        # stored activation, and the forward-time compression; the step
-        # overlaps the compression with the g_x branch
-        "backward_us": bwd_ms * 1e3,
-        "forward_acbp_us": fwd_ms * 1e3,
-        "effective_tops": 4 * T * Cin * Cout / (bwd_ms / 1e3) / 1e12,
-        # integer ops the two GEMMs execute (reduced K = T' on the g_w side),
-        # per second of their traced time; and those ops x operand bits
-        "gemm_int_tops": gemm_ops / gemm_s / 1e12 if gemm_s > 0 else None,
-        "gemm_tbops": gemm_bitops / gemm_s / 1e12 if gemm_s > 0 else None,
-        "acbp_stored_bytes": acbp_bytes(T, Cin, wl.rank, e),
-        "timing": timing,
-        "ms_per_step_eager": ms_eager,
-        "roofline": roofline,
-        "kernels": kernels,
-        "gpu_launches": len(launches),
-        "variants": variants,
-        "clocks": clk,
-        "e2e": {"value": job_us_per_layer(e2e, world), "unit": UNIT,
-                "h2d_bytes_per_step": (x.numel() + gy.numel() + w.numel()) * e,
-                "d2h_bytes_per_step": (gx.numel() + gw.numel()) * 4},
+        "config": res["config"],
+        "backward_us": res["backward_us"],
+        "forward_acbp_us": res["forward_acbp_us"],
+        "effective_tops": res["effective_tops"],
+        "gemm_int_tops": res["gemm_int_tops"],
+        "gemm_tbops": res["gemm_tbops"],
+        "acbp_stored_bytes": res["acbp_stored_bytes"],
+        "timing": res["timing"],
+        "roofline": res["roofline"],
+        "rows": res["rows"],
+        "kernels": res["kernels"],
+        "gpu_launches": res["gpu_launches"],
+        "variants": res["variants"],
+        "clocks": res["clocks"],
+        "e2e": {"value": job_us_per_layer(res["e2e_ms"], world), "unit": UNIT,
+                "h2d_bytes_per_step": res["e2e_bytes"][0],
+                "d2h_bytes_per_step": res["e2e_bytes"][1]},
+        "per_workload": per_workload,
     }
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(wl, inp, min(args.cpu_sample_tokens, wl.T))
+        line["cpu_baseline"] = cpu_baseline(wl, inp, min(args.cpu_sample_tokens, wl.T),
+                                            args.cpu_sample_w_rows)
     print(json.dumps(line), flush=True)
     return 0
 

@@ -197,6 +197,33 @@ def _need_cuda_contig(*ts, current_device=None):
                              "make their device current first")
 
 
+def _need_buf(t, shape, dtype, index, what):
+    """A caller-supplied output or buffer: a contiguous CUDA tensor on device
+    `index` (the inputs' device) with exactly `shape` (None: any shape) and
+    one of the dtypes `dtype`.  The kernels write through these pointers, so
+    a wrong device, size or type is refused here rather than written past."""
+    if not getattr(t, "is_cuda", False) or not t.is_contiguous():
+        raise ValueError(f"{what} must be a contiguous CUDA tensor")
+    if t.device.index != index:
+        raise ValueError(f"{what} is on cuda:{t.device.index}, the inputs on cuda:{index}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{what} must have shape {tuple(shape)}, not {tuple(t.shape)}")
+    dts = dtype if isinstance(dtype, tuple) else (dtype,)
+    if t.dtype not in dts:
+        raise ValueError(f"{what} must be of dtype {' or '.join(map(str, dts))}, "
+                         f"not {t.dtype}")
+
+
+def _ws_bytes(ws, index):
+    """Size in bytes of a caller-supplied workspace (any dtype), after the
+    same device and contiguity checks as an output."""
+    if not getattr(ws, "is_cuda", False) or not ws.is_contiguous():
+        raise ValueError("ws must be a contiguous CUDA tensor")
+    if ws.device.index != index:
+        raise ValueError(f"ws is on cuda:{ws.device.index}, the inputs on cuda:{index}")
+    return int(ws.numel()) * int(ws.element_size())
+
+
 def hlq_workspace_bytes(op: int, T: int, Cin: int, Cout: int, block: int = 16,
                         rank: int = 8) -> int:
     return int(lib().hlq_workspace_bytes(op, T, Cin, Cout, block, rank))
@@ -217,7 +244,7 @@ def _xbar_fmt(xbar_bits: int, per_channel: bool) -> int:
 
 def _check_xbar_scale(xbar_scale, Cin: int, per_channel: bool):
     need = Cin if per_channel else 1
-    if xbar_scale.dtype != _torch().float32 or xbar_scale.numel() < need:
+    if xbar_scale.dtype != _torch().float32 or xbar_scale.numel() != need:
         raise ValueError(f"xbar_scale must hold {need} fp32 value(s)")
 
 
@@ -226,6 +253,17 @@ def xbar_shape(T: int, Cin: int, rank: int = 8, xbar_bits: int = 8):
     of packed int4 codes."""
     Tp = T // 16 * rank
     return (Cin, Tp if xbar_bits == 8 else Tp // 2)
+
+
+def _check_xbar(xbar, xbar_scale, T: int, Cin: int, rank: int, xbar_bits: int,
+                per_channel: bool, index: int):
+    """The ACBP buffer and its scales as the library reads or writes them:
+    one-byte codes of exactly xbar_shape(...), fp32 scales [1] or [Cin]."""
+    torch = _torch()
+    _need_buf(xbar, xbar_shape(T, Cin, rank, xbar_bits), (torch.int8, torch.uint8), index,
+              "xbar")
+    _need_buf(xbar_scale, None, torch.float32, index, "xbar_scale")
+    _check_xbar_scale(xbar_scale, Cin, per_channel)
 
 
 def hlq_compress_activation(x, rank: int = 8, block: int = 16, out=None,
@@ -237,20 +275,22 @@ def hlq_compress_activation(x, rank: int = 8, block: int = 16, out=None,
     torch = _torch()
     _need_cuda_contig(x)
     T, Cin = x.shape
+    dev = x.device
     if out is None:
         out = torch.empty(xbar_shape(T, Cin, rank, xbar_bits),
                           dtype=torch.int8 if xbar_bits == 8 else torch.uint8,
-                          device=x.device)
+                          device=dev)
     if scale is None:
         scale = torch.empty(Cin if xbar_per_channel else 1, dtype=torch.float32,
-                            device=x.device)
-    _check_xbar_scale(scale, Cin, xbar_per_channel)
+                            device=dev)
+    _check_xbar(out, scale, T, Cin, rank, xbar_bits, xbar_per_channel, dev.index)
     if ws is None:
-        ws = workspace(OP_COMPRESS_ACTIVATION, T, Cin, 16, block, rank, x.device)
+        ws = workspace(OP_COMPRESS_ACTIVATION, T, Cin, 16, block, rank, dev)
     _check(lib().hlq_compress_activation(
         _ptr(x), _dtype_code(x), T, Cin, block, rank,
         _xbar_fmt(xbar_bits, xbar_per_channel), _ptr(out),
-        _ptr(scale), _ptr(ws), ws.numel(), _stream(stream)), "hlq_compress_activation")
+        _ptr(scale), _ptr(ws), _ws_bytes(ws, dev.index), _stream(stream)),
+        "hlq_compress_activation")
     return out, scale
 
 
@@ -265,13 +305,15 @@ def hlq_linear_backward_gx(g_y, w, gran_gy: int = PER_TOKEN,
     Cout2, Cin = w.shape
     if Cout2 != Cout or g_y.dtype != w.dtype:
         raise ValueError("shape/dtype mismatch between g_y and w")
+    dev = g_y.device
     if out is None:
-        out = torch.empty((T, Cin), dtype=torch.float32, device=g_y.device)
+        out = torch.empty((T, Cin), dtype=torch.float32, device=dev)
+    _need_buf(out, (T, Cin), torch.float32, dev.index, "out")
     if ws is None:
-        ws = workspace(OP_BACKWARD_GX, T, Cin, Cout, block, 16, g_y.device)
+        ws = workspace(OP_BACKWARD_GX, T, Cin, Cout, block, 16, dev)
     _check(lib().hlq_linear_backward_gx(
         _ptr(g_y), _ptr(w), _dtype_code(g_y), T, Cin, Cout, block, gran_gy,
-        gran_w, rnd, seed, _ptr(out), _ptr(ws), ws.numel(), _stream(stream)),
+        gran_w, rnd, seed, _ptr(out), _ptr(ws), _ws_bytes(ws, dev.index), _stream(stream)),
         "hlq_linear_backward_gx")
     return out
 
@@ -284,15 +326,17 @@ def hlq_linear_backward_gw(g_y, xbar, xbar_scale, rank: int = 8,
     _need_cuda_contig(g_y, xbar, xbar_scale)
     T, Cout = g_y.shape
     Cin = xbar.shape[0]
-    _check_xbar_scale(xbar_scale, Cin, xbar_per_channel)
+    dev = g_y.device
+    _check_xbar(xbar, xbar_scale, T, Cin, rank, xbar_bits, xbar_per_channel, dev.index)
     if out is None:
-        out = torch.empty((Cout, Cin), dtype=torch.float32, device=g_y.device)
+        out = torch.empty((Cout, Cin), dtype=torch.float32, device=dev)
+    _need_buf(out, (Cout, Cin), torch.float32, dev.index, "out")
     if ws is None:
-        ws = workspace(OP_BACKWARD_GW, T, Cin, Cout, block, rank, g_y.device)
+        ws = workspace(OP_BACKWARD_GW, T, Cin, Cout, block, rank, dev)
     _check(lib().hlq_linear_backward_gw(
         _ptr(g_y), _dtype_code(g_y), _ptr(xbar), _ptr(xbar_scale), T, Cin,
         Cout, block, rank, _xbar_fmt(xbar_bits, xbar_per_channel), _ptr(out), _ptr(ws),
-        ws.numel(), _stream(stream)),
+        _ws_bytes(ws, dev.index), _stream(stream)),
         "hlq_linear_backward_gw")
     return out
 
@@ -308,9 +352,12 @@ def hlq_linear_backward_gx_noalloc(g_y, w, gran_gy: int = PER_TOKEN,
     torch = _torch()
     _need_cuda_contig(g_y, w)
     T, Cout = g_y.shape
-    Cin = w.shape[1]
+    Cout2, Cin = w.shape
+    if Cout2 != Cout or g_y.dtype != w.dtype:
+        raise ValueError("shape/dtype mismatch between g_y and w")
     if out is None:
         out = torch.empty((T, Cin), dtype=torch.float32, device=g_y.device)
+    _need_buf(out, (T, Cin), torch.float32, g_y.device.index, "out")
     _check(lib().hlq_linear_backward_gx_noalloc(
         _ptr(g_y), _ptr(w), _dtype_code(g_y), T, Cin, Cout, block, gran_gy,
         gran_w, rnd, seed, _ptr(out), _stream(stream)),
@@ -334,20 +381,23 @@ def hlq_linear_backward(g_y, w, xbar, xbar_scale, rank: int = 8,
     Cin = w.shape[1]
     if w.shape[0] != Cout or g_y.dtype != w.dtype or xbar.shape[0] != Cin:
         raise ValueError("shape/dtype mismatch between g_y, w and xbar")
-    _check_xbar_scale(xbar_scale, Cin, xbar_per_channel)
+    dev = g_y.device
+    _check_xbar(xbar, xbar_scale, T, Cin, rank, xbar_bits, xbar_per_channel, dev.index)
     if out_gx is None:
-        out_gx = torch.empty((T, Cin), dtype=torch.float32, device=g_y.device)
+        out_gx = torch.empty((T, Cin), dtype=torch.float32, device=dev)
     if out_gw is None:
-        out_gw = torch.empty((Cout, Cin), dtype=torch.float32, device=g_y.device)
+        out_gw = torch.empty((Cout, Cin), dtype=torch.float32, device=dev)
+    _need_buf(out_gx, (T, Cin), torch.float32, dev.index, "out_gx")
+    _need_buf(out_gw, (Cout, Cin), torch.float32, dev.index, "out_gw")
     if ws is None:
         ws = workspace(OP_BACKWARD_FUSED if fused_gy else OP_BACKWARD, T, Cin, Cout, block,
-                       rank, g_y.device)
+                       rank, dev)
     fn = lib().hlq_linear_backward_fused if fused_gy else lib().hlq_linear_backward
     _check(fn(
         _ptr(g_y), _ptr(w), _ptr(xbar), _ptr(xbar_scale), _dtype_code(g_y), T,
         Cin, Cout, block, rank, _xbar_fmt(xbar_bits, xbar_per_channel), gran_gy,
         gran_w, rnd, seed, _ptr(out_gx),
-        _ptr(out_gw), _ptr(ws), ws.numel(), _stream(stream)),
+        _ptr(out_gw), _ptr(ws), _ws_bytes(ws, dev.index), _stream(stream)),
         "hlq_linear_backward_fused" if fused_gy else "hlq_linear_backward")
     return out_gx, out_gw
 
@@ -376,14 +426,16 @@ def hlq_layer_step(x, g_y, w, rank: int = 8, gran_gy: int = PER_TOKEN,
     if xbar_scale is None:
         xbar_scale = torch.empty(Cin if xbar_per_channel else 1, dtype=torch.float32,
                                  device=dev)
-    _need_cuda_contig(xbar, xbar_scale)
-    _check_xbar_scale(xbar_scale, Cin, xbar_per_channel)
+    _need_buf(out_gx, (T, Cin), torch.float32, dev.index, "out_gx")
+    _need_buf(out_gw, (Cout, Cin), torch.float32, dev.index, "out_gw")
+    _check_xbar(xbar, xbar_scale, T, Cin, rank, xbar_bits, xbar_per_channel, dev.index)
     if ws is None:
         ws = workspace(OP_LAYER_STEP, T, Cin, Cout, block, rank, dev)
     _check(lib().hlq_layer_step(
         _ptr(x), _ptr(g_y), _ptr(w), _dtype_code(g_y), T, Cin, Cout, block, rank,
         _xbar_fmt(xbar_bits, xbar_per_channel), gran_gy, gran_w, rnd, seed, _ptr(out_gx),
-        _ptr(out_gw), _ptr(xbar), _ptr(xbar_scale), _ptr(ws), ws.numel(), _stream(stream)),
+        _ptr(out_gw), _ptr(xbar), _ptr(xbar_scale), _ptr(ws), _ws_bytes(ws, dev.index),
+        _stream(stream)),
         "hlq_layer_step")
     return out_gx, out_gw, xbar, xbar_scale
 
@@ -392,6 +444,14 @@ def _need_cpu_contig(*ts):
     for t in ts:
         if t is not None and (t.is_cuda or not t.is_contiguous()):
             raise ValueError("host tensors must be contiguous CPU tensors")
+
+
+def _need_host_out(t, shape, what):
+    """A caller-supplied host output: a contiguous fp32 CPU tensor of exactly
+    `shape` (the library's copies write its whole extent)."""
+    _need_cpu_contig(t)
+    if tuple(t.shape) != tuple(shape) or t.dtype != _torch().float32:
+        raise ValueError(f"{what} must be a float32 CPU tensor of shape {tuple(shape)}")
 
 
 def hlq_layer_step_host_workspace_bytes(dtype_code: int, T: int, Cin: int, Cout: int,
@@ -414,13 +474,16 @@ def hlq_layer_step_host(x, g_y, w, xbar, xbar_scale, rank: int = 8,
     _need_cuda_contig(xbar, xbar_scale)
     T, Cout = g_y.shape
     Cin = w.shape[1]
-    _check_xbar_scale(xbar_scale, Cin, xbar_per_channel)
     if w.shape[0] != Cout or tuple(x.shape) != (T, Cin) or not (x.dtype == g_y.dtype == w.dtype):
         raise ValueError("shape/dtype mismatch between x, g_y and w")
+    index = xbar.device.index
+    _check_xbar(xbar, xbar_scale, T, Cin, rank, xbar_bits, xbar_per_channel, index)
     if out_gx is None:
         out_gx = torch.empty((T, Cin), dtype=torch.float32).pin_memory()
     if out_gw is None:
         out_gw = torch.empty((Cout, Cin), dtype=torch.float32).pin_memory()
+    _need_host_out(out_gx, (T, Cin), "out_gx")
+    _need_host_out(out_gw, (Cout, Cin), "out_gw")
     dt = _dtype_code(g_y)
     if ws is None:
         n = hlq_layer_step_host_workspace_bytes(dt, T, Cin, Cout, block, rank)
@@ -429,7 +492,8 @@ def hlq_layer_step_host(x, g_y, w, xbar, xbar_scale, rank: int = 8,
         _ptr(x), _ptr(g_y), _ptr(w), dt, T, Cin, Cout, block, rank,
         _xbar_fmt(xbar_bits, xbar_per_channel), gran_gy, gran_w,
         rnd, seed, _ptr(out_gx), _ptr(out_gw), _ptr(xbar), _ptr(xbar_scale),
-        chunk_tokens, _ptr(ws), ws.numel(), _stream(stream)), "hlq_layer_step_host")
+        chunk_tokens, _ptr(ws), _ws_bytes(ws, index), _stream(stream)),
+        "hlq_layer_step_host")
     return out_gx, out_gw
 
 
@@ -441,15 +505,19 @@ def hlq_select_gy_granularity(g_y, threshold: float = 1.5, block: int = 16,
     torch = _torch()
     _need_cuda_contig(g_y)
     T, Cout = g_y.shape
+    dev = g_y.device
     if mse is None:
-        mse = torch.empty(2, dtype=torch.float64, device=g_y.device)
+        mse = torch.empty(2, dtype=torch.float64, device=dev)
     if choice is None:
-        choice = torch.empty(1, dtype=torch.int32, device=g_y.device)
+        choice = torch.empty(1, dtype=torch.int32, device=dev)
+    _need_buf(mse, (2,), torch.float64, dev.index, "mse")
+    _need_buf(choice, (1,), torch.int32, dev.index, "choice")
     if ws is None:
-        ws = workspace(OP_SELECT_GRANULARITY, T, 16, Cout, block, 8, g_y.device)
+        ws = workspace(OP_SELECT_GRANULARITY, T, 16, Cout, block, 8, dev)
     _check(lib().hlq_select_gy_granularity(
         _ptr(g_y), _dtype_code(g_y), T, Cout, block, float(threshold), _ptr(mse),
-        _ptr(choice), _ptr(ws), ws.numel(), _stream(stream)), "hlq_select_gy_granularity")
+        _ptr(choice), _ptr(ws), _ws_bytes(ws, dev.index), _stream(stream)),
+        "hlq_select_gy_granularity")
     return mse, choice
 
 
@@ -463,15 +531,18 @@ def hlq_ablation_gw_hq(g_y, x, rnd: int = SR, seed: int = 0, block: int = 16,
     Cin = x.shape[1]
     if x.shape[0] != T or x.dtype != g_y.dtype:
         raise ValueError("shape/dtype mismatch between g_y and x")
-    gw = (torch.empty((Cout, Cin), dtype=torch.float32, device=g_y.device)
+    dev = g_y.device
+    gw = (torch.empty((Cout, Cin), dtype=torch.float32, device=dev)
           if out is None else out)
-    acc = (torch.empty((Cout, Cin), dtype=torch.int32, device=g_y.device)
+    _need_buf(gw, (Cout, Cin), torch.float32, dev.index, "out")
+    acc = (torch.empty((Cout, Cin), dtype=torch.int32, device=dev)
            if with_acc else None)
     if ws is None:
-        ws = workspace(OP_ABLATION_GW_HQ, T, Cin, Cout, block, 8, g_y.device)
+        ws = workspace(OP_ABLATION_GW_HQ, T, Cin, Cout, block, 8, dev)
     _check(lib().hlq_ablation_gw_hq(
         _ptr(g_y), _ptr(x), _dtype_code(g_y), T, Cin, Cout, block, rnd, seed, _ptr(gw),
-        _ptr(acc), _ptr(ws), ws.numel(), _stream(stream)), "hlq_ablation_gw_hq")
+        _ptr(acc), _ptr(ws), _ws_bytes(ws, dev.index), _stream(stream)),
+        "hlq_ablation_gw_hq")
     return (gw, acc) if with_acc else gw
 
 
@@ -485,15 +556,18 @@ def hlq_ablation_gx_hla(g_y, w, rank: int = 8, block: int = 16, with_acc: bool =
     Cin = w.shape[1]
     if w.shape[0] != Cout or w.dtype != g_y.dtype:
         raise ValueError("shape/dtype mismatch between g_y and w")
-    gx = (torch.empty((T, Cin), dtype=torch.float32, device=g_y.device)
+    dev = g_y.device
+    gx = (torch.empty((T, Cin), dtype=torch.float32, device=dev)
           if out is None else out)
-    acc = (torch.empty((T, Cin), dtype=torch.int32, device=g_y.device)
+    _need_buf(gx, (T, Cin), torch.float32, dev.index, "out")
+    acc = (torch.empty((T, Cin), dtype=torch.int32, device=dev)
            if with_acc else None)
     if ws is None:
-        ws = workspace(OP_ABLATION_GX_HLA, T, Cin, Cout, block, rank, g_y.device)
+        ws = workspace(OP_ABLATION_GX_HLA, T, Cin, Cout, block, rank, dev)
     _check(lib().hlq_ablation_gx_hla(
         _ptr(g_y), _ptr(w), _dtype_code(g_y), T, Cin, Cout, block, rank, _ptr(gx),
-        _ptr(acc), _ptr(ws), ws.numel(), _stream(stream)), "hlq_ablation_gx_hla")
+        _ptr(acc), _ptr(ws), _ws_bytes(ws, dev.index), _stream(stream)),
+        "hlq_ablation_gx_hla")
     return (gx, acc) if with_acc else gx
 
 
@@ -517,7 +591,7 @@ def hlq_debug_gx_parts(g_y, w, gran_gy=PER_TOKEN, gran_w=PER_TENSOR, rnd=SR,
     ws = workspace(OP_BACKWARD_GX, T, Cin, Cout, block, 16, dev)
     _check(lib().hlq_debug_gx_parts(
         _ptr(g_y), _ptr(w), _dtype_code(g_y), T, Cin, Cout, block, gran_gy,
-        gran_w, rnd, seed, _ptr(r["g_x"]), _ptr(ws), ws.numel(),
+        gran_w, rnd, seed, _ptr(r["g_x"]), _ptr(ws), _ws_bytes(ws, dev.index),
         _ptr(r["qgy"]), _ptr(r["sgy"]), _ptr(r["qw"]), _ptr(r["sw"]),
         _ptr(r["acc"]), _stream(stream)), "hlq_debug_gx_parts")
     return r
@@ -543,7 +617,7 @@ def hlq_debug_gw_parts(g_y, xbar, xbar_scale, rank=8, block=16, xbar_bits=8,
     _check(lib().hlq_debug_gw_parts(
         _ptr(g_y), _dtype_code(g_y), _ptr(xbar), _ptr(xbar_scale), T, Cin,
         Cout, block, rank, _xbar_fmt(xbar_bits, xbar_per_channel), _ptr(r["g_w"]), _ptr(ws),
-        ws.numel(), _ptr(r["qg"]),
+        _ws_bytes(ws, dev.index), _ptr(r["qg"]),
         _ptr(r["sg"]), _ptr(r["acc"]), _stream(stream)), "hlq_debug_gw_parts")
     return r
 
@@ -619,7 +693,7 @@ def hlq_debug_tc_gemm(kind, a, b, bn=0, splits=0, stream=None):
     nws = int(lib().hlq_debug_tc_gemm_ws_bytes(M, N))
     ws = torch.empty(max(nws, 256), dtype=torch.uint8, device=a.device)
     _check(lib().hlq_debug_tc_gemm(kind, _ptr(a), K, _ptr(b), K, M, N, K, bn,
-                                   splits, _ptr(acc), _ptr(ws), ws.numel(),
+                                   splits, _ptr(acc), _ptr(ws), _ws_bytes(ws, a.device.index),
                                    _stream(stream)), "hlq_debug_tc_gemm")
     return acc
 

@@ -489,13 +489,18 @@ StepLayout step_layout(int dt, int64_t T, int64_t Cin, int64_t Cout, int rank) {
   return L;
 }
 
+// At most this many token chunks of g_y per hlq_layer_step_host call.
+constexpr int kMaxHostChunks = 64;
+
 // Events of one hlq_layer_step_host call (destroyed when it returns; the
-// runtime keeps pending ones alive until they complete).
+// runtime keeps pending ones alive until they complete): six for the
+// streams' hand-offs and two per chunk of g_y.
 struct EventSet {
-  cudaEvent_t ev[72] = {};
+  static constexpr int kCap = 6 + 2 * kMaxHostChunks;
+  cudaEvent_t ev[kCap] = {};
   int n = 0;
   cudaEvent_t make() {
-    if (n >= 72) return nullptr;
+    if (n >= kCap) return nullptr;
     cudaEvent_t e = nullptr;
     if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return nullptr;
     ev[n++] = e;
@@ -1044,13 +1049,16 @@ hlq_status hlq_layer_step_host(const void* h_x, const void* h_gy, const void* h_
     return HLQ_OK;
   }
 
-  // chunks of g_y rows: multiples of 128 (GEMM tiles), ~16 MB each, <= 64
+  // chunks of g_y rows: multiples of 128 (GEMM tiles), ~16 MB each, at most
+  // kMaxHostChunks of them
   int64_t ch = chunk_tokens;
   if (ch == 0) ch = (int64_t)((16u << 20) / ((size_t)Cout * esz));
   ch = (ch + 127) / 128 * 128;
   if (ch < 128) ch = 128;
-  if ((T + ch - 1) / ch > 64) ch = ((T + 63) / 64 + 127) / 128 * 128;
+  if ((T + ch - 1) / ch > kMaxHostChunks)
+    ch = ((T + kMaxHostChunks - 1) / kMaxHostChunks + 127) / 128 * 128;
   const int nc = (int)((T + ch - 1) / ch);
+  if (nc < 1 || nc > kMaxHostChunks) return HLQ_ERR_INVALID_ARG;
 
   cudaStream_t a_gw = aux_stream(0), a_w = aux_stream(1), cin = aux_stream(2),
                cout = aux_stream(3);
@@ -1063,14 +1071,14 @@ hlq_status hlq_layer_step_host(const void* h_x, const void* h_gy, const void* h_
   EventSet E;
   cudaEvent_t fork = E.make(), w_in = E.make(), x_in = E.make(), w_done = E.make(),
               gw_done = E.make(), out_done = E.make();
-  cudaEvent_t gy_in[64], gx_done[64];
+  cudaEvent_t gy_in[kMaxHostChunks], gx_done[kMaxHostChunks];
+  bool events_ok = fork && w_in && x_in && w_done && gw_done && out_done;
   for (int c = 0; c < nc; ++c) {
     gy_in[c] = E.make();
     gx_done[c] = E.make();
+    events_ok = events_ok && gy_in[c] && gx_done[c];
   }
-  if (!fork || !w_in || !x_in || !w_done || !gw_done || !out_done || !gy_in[nc - 1] ||
-      !gx_done[nc - 1])
-    return HLQ_ERR_CUDA;
+  if (!events_ok) return HLQ_ERR_CUDA;
 
   const bool bf16 = dt == HLQ_BF16;
   const bool per_token = gran_gy == HLQ_PER_TOKEN;

@@ -6,9 +6,10 @@
 // latency-critical loops that forbid cudaMalloc/cudaFree after start-up
 // (both can synchronize the device).  This entry point needs neither a
 // workspace argument nor any allocation: its scratch (the int4 codes of g_y
-// and w, their scales and the amax slots) lives in one fixed device array
-// of this library, kNoAllocScratchBytes long, which every GPU that loads the
-// library holds until the process exits.
+// and w, stored one E4M3 byte per code for the tensor-core GEMM, their
+// scales and the amax slots) lives in one fixed device array of this
+// library, kNoAllocScratchBytes long, which every GPU that loads the library
+// holds until the process exits.
 #include <cstdint>
 #include <mutex>
 

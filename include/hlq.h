@@ -459,6 +459,10 @@ hlq_status hlq_trace_free(void);
  *    call clears what must start at zero.  Calls whose work overlaps on the
  *    GPU (other streams, other host threads) race on the array: order them
  *    on one stream or synchronize between them.
+ *  - The looked-up address is kept for the life of the process, like the
+ *    address of the library's device status word: a cudaDeviceReset while
+ *    the library is in use unloads its device code and leaves both stale,
+ *    and is not supported.
  */
 hlq_status hlq_linear_backward_gx_noalloc(const void *d_gy, const void *d_w, int dt,
                                           int64_t T, int64_t Cin, int64_t Cout,

@@ -293,13 +293,27 @@ def test_product_path_fails_loudly_without_library(monkeypatch, tmp_path):
 class _FakeTensor:
     """Stands in for a CUDA tensor: only what the binding's checks read."""
 
-    def __init__(self, index, cuda=True, contiguous=True):
+    def __init__(self, index, cuda=True, contiguous=True, shape=(4, 4), dtype=None,
+                 itemsize=4):
+        import torch
         self.is_cuda = cuda
         self._contiguous = contiguous
         self.device = type("Dev", (), {"index": index})()
+        self.shape = shape
+        self.dtype = torch.float32 if dtype is None else dtype
+        self._itemsize = itemsize
 
     def is_contiguous(self):
         return self._contiguous
+
+    def numel(self):
+        n = 1
+        for d in self.shape:
+            n *= d
+        return n
+
+    def element_size(self):
+        return self._itemsize
 
 
 def test_binding_checks_tensors_and_their_device():
@@ -315,3 +329,64 @@ def test_binding_checks_tensors_and_their_device():
         check(_FakeTensor(0), _FakeTensor(1), current_device=0)
     with pytest.raises(ValueError, match="is current"):
         check(_FakeTensor(1), _FakeTensor(1), current_device=0)
+
+
+def test_binding_checks_outputs_and_workspaces():
+    """Caller-supplied outputs and workspaces get the inputs' device and
+    contiguity checks, an exact shape and dtype, and a byte count that does
+    not depend on the workspace's dtype (refused before any launch)."""
+    import torch
+    buf = hlq._need_buf
+    buf(_FakeTensor(0, shape=(8, 4)), (8, 4), torch.float32, 0, "out")
+    with pytest.raises(ValueError, match="contiguous CUDA"):
+        buf(_FakeTensor(0, cuda=False, shape=(8, 4)), (8, 4), torch.float32, 0, "out")
+    with pytest.raises(ValueError, match="contiguous CUDA"):
+        buf(_FakeTensor(0, contiguous=False, shape=(8, 4)), (8, 4), torch.float32, 0, "out")
+    with pytest.raises(ValueError, match="cuda:1, the inputs on cuda:0"):
+        buf(_FakeTensor(1, shape=(8, 4)), (8, 4), torch.float32, 0, "out")
+    with pytest.raises(ValueError, match="shape"):     # too small: would be written past
+        buf(_FakeTensor(0, shape=(4, 4)), (8, 4), torch.float32, 0, "out")
+    with pytest.raises(ValueError, match="dtype"):
+        buf(_FakeTensor(0, shape=(8, 4), dtype=torch.float16), (8, 4), torch.float32, 0,
+            "out")
+    buf(_FakeTensor(0, shape=(3, 2), dtype=torch.uint8), (3, 2), (torch.int8, torch.uint8),
+        0, "xbar")
+    # workspace bytes = numel x element size, whatever its dtype
+    assert hlq._ws_bytes(_FakeTensor(0, shape=(1000,), dtype=torch.uint8, itemsize=1), 0) == 1000
+    assert hlq._ws_bytes(_FakeTensor(0, shape=(1000,), itemsize=4), 0) == 4000
+    with pytest.raises(ValueError, match="contiguous CUDA"):
+        hlq._ws_bytes(_FakeTensor(0, cuda=False, shape=(16,)), 0)
+    with pytest.raises(ValueError, match="cuda:2"):
+        hlq._ws_bytes(_FakeTensor(2, shape=(16,)), 0)
+
+
+def test_entry_points_refuse_a_wrong_output_before_calling_the_library(monkeypatch):
+    """The entry points check `out` before they reach the library: a stub
+    library that fails the test if called proves nothing was launched."""
+    import torch
+
+    class _NoCall:
+        def __getattr__(self, name):
+            raise AssertionError(f"library called: {name}")
+
+    monkeypatch.setattr(hlq, "lib", lambda: _NoCall())
+    monkeypatch.setattr(torch.cuda, "current_device", lambda: 0)
+    gy = _FakeTensor(0, shape=(32, 16), dtype=torch.bfloat16)
+    w = _FakeTensor(0, shape=(16, 48), dtype=torch.bfloat16)
+    small = _FakeTensor(0, shape=(16, 48))
+    ws = _FakeTensor(0, shape=(1 << 20,), dtype=torch.uint8, itemsize=1)
+    with pytest.raises(ValueError, match="shape"):
+        hlq.hlq_linear_backward_gx(gy, w, out=small, ws=ws)
+    with pytest.raises(ValueError, match="shape"):
+        hlq.hlq_linear_backward_gx_noalloc(gy, w, out=small)
+    wrong_dev = _FakeTensor(1, shape=(32, 48))
+    with pytest.raises(ValueError, match="cuda:1"):
+        hlq.hlq_linear_backward_gx(gy, w, out=wrong_dev, ws=ws)
+    xbar = _FakeTensor(0, shape=(48, 16), dtype=torch.int8, itemsize=1)
+    sx = _FakeTensor(0, shape=(1,))
+    with pytest.raises(ValueError, match="shape"):       # g_w is [Cout, Cin] = [16, 48]
+        hlq.hlq_linear_backward_gw(gy, xbar, sx, out=_FakeTensor(0, shape=(48, 16)), ws=ws)
+    with pytest.raises(ValueError, match="xbar must have shape"):
+        hlq.hlq_linear_backward_gw(gy, _FakeTensor(0, shape=(48, 8), dtype=torch.int8,
+                                                    itemsize=1), sx, ws=ws,
+                                   out=_FakeTensor(0, shape=(16, 48)))

@@ -17,7 +17,8 @@ def _run(env_extra=None, *args):
     env.update(env_extra or {})
     return subprocess.run(
         [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
-         "--steps", "2", "--warmup", "1", "--ref-sample-tokens", "64", *args],
+         "--steps", "2", "--warmup", "1", "--ref-sample-tokens", "16",
+         "--ref-sample-w-rows", "32", *args],
         cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
 
 
@@ -36,12 +37,14 @@ def test_reference_arm_line():
     assert d["unit"] == "us/layer" and d["higher_is_better"] is False
     assert d["value"] > 0 and abs(d["ms_per_step"] * 1e3 - d["value"]) <= 1e-9 * d["value"]
     assert d["vs_baseline"] is None and d["data"] == "synthetic"
-    wl = workloads.WORKLOADS[1]
+    wl = workloads.WORKLOADS[3]          # the largest layer is the default
     assert d["config"]["workload"] == wl.name
     assert (d["config"]["T"], d["config"]["Cin"], d["config"]["Cout"]) == (wl.T, wl.Cin, wl.Cout)
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"]
-    assert cb["unit"] == d["unit"] and "64" in cb["sample"]
+    assert cb["unit"] == d["unit"] and cb["extrapolated"] is True
+    assert f"first 16 of {wl.T} tokens" in cb["sample"]
+    assert f"32 of {wl.Cout} rows" in cb["sample"]
     assert cb["host"]["nproc"] >= 1 and cb["host"]["machine"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"],
                         "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}

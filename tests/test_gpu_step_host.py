@@ -26,8 +26,10 @@ def _host(inp, name, dtype):
     return torch.from_numpy(np.ascontiguousarray(inp[name], np.float32)).pin_memory()
 
 
+# (0, 5120, 128): 40 chunks, more than the event set of the first version
+# held; (0, 8960, 128): 70 requested, widened to 35 chunks of 256 tokens
 @pytest.mark.parametrize("wl_idx,T,chunk", [(1, 1024, 256), (1, 1024, 0), (2, 528, 128),
-                                            (0, 256, 128)])
+                                            (0, 256, 128), (0, 5120, 128), (0, 8960, 128)])
 def test_step_host_matches_device_path(wl_idx, T, chunk):
     wl = workloads.WORKLOADS[wl_idx]
     inp = workloads.make_inputs(wl, T=T)
