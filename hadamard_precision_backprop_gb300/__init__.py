@@ -100,7 +100,7 @@ def lib() -> ctypes.CDLL:
             "hlq_trace_begin": (i32, [i32]),
             "hlq_debug_reference_gemm": (i32, [i32, P, P, i64, i64, i64, P, P]),
             "hlq_debug_tc_gemm": (i32, [i32, P, i64, P, i64, i64, i64, i64, i32,
-                                        i32, P, P, sz, P]),
+                                        i32, i32, P, P, sz, P]),
             "hlq_debug_tc_gemm_ws_bytes": (sz, [i64, i64]),
             "hlq_linear_backward_gx_noalloc": (i32, [P, P, i32, i64, i64, i64, i32,
                                                      i32, i32, i32, u64, P, P]),
@@ -116,7 +116,7 @@ def lib() -> ctypes.CDLL:
                                                 P, P, P, sz, P]),
             "hlq_ablation_gw_hq": (i32, [P, P, i32, i64, i64, i64, i32, i32, u64, P, P, P,
                                          sz, P]),
-            "hlq_debug_gemm_plan": (i32, [i64, i64, i64, i32, i32, P, P, P, P, P]),
+            "hlq_debug_gemm_plan": (i32, [i64, i64, i64, i32, i32, P, P, P, P, P, P, P]),
             "hlq_debug_wait_timeout": (i32, [u64, P, P]),
             "hlq_layer_step": (i32, [P, P, P, i32, i64, i64, i64, i32, i32, i32, i32, i32,
                                      i32, u64, P, P, P, P, P, sz, P]),
@@ -674,17 +674,20 @@ def hlq_debug_wait_timeout(limit_ns: int = 1_000_000, stream=None):
 def hlq_debug_gemm_plan(T: int, Cin: int, Cout: int, rank: int = 8, sms: int = 152):
     """The GEMM plans of a layer on a GPU with `sms` SMs (host only): dict of
     gx (bn, splits), gw (bn, splits) and in_sequence."""
-    vals = [ctypes.c_int(0) for _ in range(5)]
+    vals = [ctypes.c_int(0) for _ in range(7)]
     _check(lib().hlq_debug_gemm_plan(T, Cin, Cout, rank, sms,
                                      *[ctypes.byref(v) for v in vals]),
            "hlq_debug_gemm_plan")
     g = [v.value for v in vals]
-    return {"gx": (g[0], g[1]), "gw": (g[2], g[3]), "in_sequence": bool(g[4])}
+    return {"gx": (g[0], g[1]), "gw": (g[2], g[3]), "in_sequence": bool(g[4]),
+            "gx_pair": bool(g[5]), "gw_pair": bool(g[6])}
 
 
-def hlq_debug_tc_gemm(kind, a, b, bn=0, splits=0, stream=None):
+def hlq_debug_tc_gemm(kind, a, b, bn=0, splits=0, pair=-1, stream=None):
     """int32 a @ b^T on the tensor cores with an explicit plan.  kind 0: a, b
-    are uint8 E4M3 codes [M, K] / [N, K]; kind 1: bf16 codes."""
+    are uint8 E4M3 codes [M, K] / [N, K]; kind 1: bf16 codes.  pair: 1 = CTA
+    pairs over 256-row tiles, 0 = one CTA per 128-row tile, -1 = the
+    library's choice."""
     torch = _torch()
     _need_cuda_contig(a, b)
     M, K = a.shape
@@ -693,7 +696,8 @@ def hlq_debug_tc_gemm(kind, a, b, bn=0, splits=0, stream=None):
     nws = int(lib().hlq_debug_tc_gemm_ws_bytes(M, N))
     ws = torch.empty(max(nws, 256), dtype=torch.uint8, device=a.device)
     _check(lib().hlq_debug_tc_gemm(kind, _ptr(a), K, _ptr(b), K, M, N, K, bn,
-                                   splits, _ptr(acc), _ptr(ws), _ws_bytes(ws, a.device.index),
+                                   splits, pair, _ptr(acc), _ptr(ws),
+                                   _ws_bytes(ws, a.device.index),
                                    _stream(stream)), "hlq_debug_tc_gemm")
     return acc
 

@@ -382,8 +382,9 @@ hlq_status hla_gy_launches(const void* gy, bool bf16, int64_t T, int64_t Cout, i
 // them side by side cannot fill idle SMs and only delays the later grid.
 bool gemms_in_sequence_on(int64_t Mx, int64_t Cin, int64_t Cout, int64_t Tp, int sms) {
   if (sms <= 0) return false;
-  auto units = [](const GemmPlan& p, int64_t M, int64_t N) {
-    return ((M + 127) / 128) * ((N + p.bn - 1) / p.bn) * p.splits;
+  auto units = [](const GemmPlan& p, int64_t M, int64_t N) {  // CTAs' worth of work
+    const int64_t tm = p.pair ? 2 * ((M + 255) / 256) : (M + 127) / 128;
+    return tm * ((N + p.bn - 1) / p.bn) * p.splits;
   };
   const GemmPlan px = plan_gemm_tc(0, Mx, Cin, Cout, sms, 1);
   const GemmPlan pw = plan_gemm_tc(1, Cout, Cin, Tp, sms, 16);
@@ -1280,12 +1281,14 @@ hlq_status hlq_debug_reference_gemm(int kind, const void* d_a, const void* d_b,
 
 hlq_status hlq_debug_tc_gemm(int kind, const void* d_a, int64_t lda, const void* d_b,
                              int64_t ldb, int64_t M, int64_t N, int64_t K, int bn,
-                             int splits, int32_t* d_acc, void* d_ws, size_t ws_bytes,
-                             void* stream) {
+                             int splits, int pair, int32_t* d_acc, void* d_ws,
+                             size_t ws_bytes, void* stream) {
   if (kind != 0 && kind != 1) return HLQ_ERR_INVALID_ARG;
   if (M < 0 || N < 0 || K < 0 || N % 16 || K % 16 || M % 16) return HLQ_ERR_SHAPE;
   if (bn != 0 && bn != 96 && bn != 128 && bn != 256) return HLQ_ERR_INVALID_ARG;
   if (splits < 0 || splits > 64) return HLQ_ERR_INVALID_ARG;
+  if (pair < -1 || pair > 1) return HLQ_ERR_INVALID_ARG;
+  if (pair == 1 && bn == 96) return HLQ_ERR_INVALID_ARG;    // pairs: 128 or 256 wide
   if (kind == 0 && splits > 1) return HLQ_ERR_INVALID_ARG;  // E4M3 GEMM runs unsplit
   const int esz = kind == 1 ? 2 : 1;
   if (lda < K || ldb < K || (lda * esz) % 16 || (ldb * esz) % 16) return HLQ_ERR_ALIGN;
@@ -1299,6 +1302,8 @@ hlq_status hlq_debug_tc_gemm(int kind, const void* d_a, int64_t lda, const void*
   GemmPlan plan = plan_gemm_tc(kind, M, N, K, sms, kind == 1 ? 16 : 1);
   if (bn) plan.bn = bn;
   if (splits) plan.splits = splits;
+  if (pair >= 0) plan.pair = pair;
+  if (plan.pair && plan.bn == 96) return HLQ_ERR_INVALID_ARG;
   if (plan.splits > 1 && (!d_ws || ws_bytes < gemm_tc_split_ws_bytes(M, N)))
     return HLQ_ERR_WORKSPACE;
   if (plan.splits > 1 && !aligned256(d_ws)) return HLQ_ERR_ALIGN;
@@ -1313,9 +1318,10 @@ hlq_status hlq_debug_tc_gemm(int kind, const void* d_a, int64_t lda, const void*
 
 hlq_status hlq_debug_gemm_plan(int64_t T, int64_t Cin, int64_t Cout, int rank, int sms,
                                int* gx_bn, int* gx_splits, int* gw_bn, int* gw_splits,
-                               int* in_sequence) {
+                               int* in_sequence, int* gx_pair, int* gw_pair) {
   if (T < 0 || Cin < 0 || Cout < 0 || !rank_ok(rank) || sms <= 0) return HLQ_ERR_INVALID_ARG;
-  if (!gx_bn || !gx_splits || !gw_bn || !gw_splits || !in_sequence) return HLQ_ERR_INVALID_ARG;
+  if (!gx_bn || !gx_splits || !gw_bn || !gw_splits || !in_sequence || !gx_pair || !gw_pair)
+    return HLQ_ERR_INVALID_ARG;
   const int64_t Tp = T / 16 * rank;
   const GemmPlan px = plan_gemm_tc(0, T, Cin, Cout, sms, 1);
   const GemmPlan pw = plan_gemm_tc(1, Cout, Cin, Tp, sms, 16);
@@ -1324,6 +1330,8 @@ hlq_status hlq_debug_gemm_plan(int64_t T, int64_t Cin, int64_t Cout, int rank, i
   *gw_bn = pw.bn;
   *gw_splits = pw.splits;
   *in_sequence = gemms_in_sequence_on(T, Cin, Cout, Tp, sms) ? 1 : 0;
+  *gx_pair = px.pair;
+  *gw_pair = pw.pair;
   return HLQ_OK;
 }
 

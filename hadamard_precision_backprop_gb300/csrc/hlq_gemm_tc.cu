@@ -14,8 +14,17 @@
 // int32 registers (49 * K < 2^24 lets the E4M3 path use one chunk; the bf16
 // path uses chunks of 16 k-blocks = 1024 codes, 1024 * 127^2 < 2^24).
 //
-// CTA layout (persistent over 128 x BN output tiles, each optionally split
-// along K with an exact int32 reduction through a workspace):
+// Two tile shapes.  One CTA per 128 x BN output tile (cta_group::1), or one
+// CTA pair (a cluster of two) per 256 x BN tile (kPair, cta_group::2): CTA r
+// of the pair loads rows 128 r .. 128 r + 127 of the tile's A block and rows
+// (BN/2) r .. of its B block into its own shared memory, CTA 0 issues the
+// M = 256 MMAs, which read both CTAs' shared memory at the same offsets and
+// leave each CTA's 128 accumulator rows in its own TMEM.  Each SM then
+// receives half the B bytes per k-block of the one-CTA tile of the same
+// width, which is what bounds the mainloop (operand delivery from L2).
+//
+// CTA layout (persistent over output tiles, each optionally split along K
+// with an exact int32 reduction through a workspace):
 //   warp 0      TMA producer (one lane): A and B k-blocks of 128 bytes per
 //               row into a ring of 128B-swizzled smem tiles (4-6 stages);
 //   warp 1      TMEM allocator and MMA issuer (one lane), 4 MMAs per k-block
@@ -64,9 +73,25 @@ __host__ __device__ constexpr uint32_t make_idesc(int kKind, int M, int N) {
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-template <int kKind>
+template <int kKind, bool kPair = false>
 __device__ __forceinline__ void mma_issue(uint32_t d_tmem, uint64_t a, uint64_t b,
                                           uint32_t idesc, uint32_t accumulate) {
+  if (kPair) {
+    if (kKind == 0) {
+      asm volatile(
+          "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+          "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+          "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+          : "memory");
+    } else {
+      asm volatile(
+          "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+          "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+          "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+          : "memory");
+    }
+    return;
+  }
   if (kKind == 0) {
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
@@ -87,6 +112,23 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
           saddr(bar))
       : "memory");
+}
+
+// Pair form: once the MMAs issued so far complete, arrive on the barrier at
+// the same shared-memory offset in both CTAs of the pair.
+__device__ __forceinline__ void mma_commit_pair(uint64_t* bar) {
+  const uint16_t both = 0x3;
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(saddr(bar)),
+      "h"(both)
+      : "memory");
+}
+
+template <bool kPair>
+__device__ __forceinline__ void mma_commit_to(uint64_t* bar) {
+  if (kPair) mma_commit_pair(bar);
+  else mma_commit(bar);
 }
 
 // 32 TMEM lanes x 32 consecutive 32-bit columns; thread i gets lane i.
@@ -111,16 +153,22 @@ __device__ __forceinline__ void tmem_ld_x32(uint32_t taddr, uint32_t (&r)[32]) {
 // allows: 7 of 28 KB for 96-wide tiles, 6 of 32 KB for 128-wide ones, 4 of
 // 48 KB for 256-wide ones.  A 96-wide tile serves shapes where it needs
 // fewer waves than 128-wide ones.
-template <int BN>
+// CTA pairs: 6 stages of 32 KB (16 KB of A, 16 KB of the B half) for 256-wide
+// tiles, 8 of 24 KB for 128-wide ones.
+template <int BN, bool kPair = false>
 struct TcCfg {
   static_assert(BN == 96 || BN == 128 || BN == 256, "tile widths 96, 128, 256");
-  static constexpr int kStages = BN == 96 ? 7 : (BN == 128 ? 6 : 4);
+  static_assert(!kPair || BN != 96, "CTA pairs take 128- or 256-wide tiles");
+  static constexpr int kStages =
+      kPair ? (BN == 256 ? 6 : 8) : (BN == 96 ? 7 : (BN == 128 ? 6 : 4));
   static constexpr int kColGroups = BN > 128 ? 2 : 1;     // 128-column halves
   static constexpr int kEpiWarps = 4 * kColGroups;        // 4 TMEM lane quarters each
   static constexpr int kColsPerThread = BN / kColGroups;  // 96 or 128
   static constexpr int kThreads = 64 + 32 * kEpiWarps;
+  static constexpr int kBRows = kPair ? BN / 2 : BN;      // B rows in this CTA
+  static constexpr int kTileM = kPair ? 2 * kBM : kBM;    // output rows per tile
   static constexpr uint32_t kABytes = kBM * kRowBytes;
-  static constexpr uint32_t kBBytes = BN * kRowBytes;
+  static constexpr uint32_t kBBytes = kBRows * kRowBytes;
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;
   // two accumulators, each starting on a 128-column boundary
   static constexpr uint32_t kAccStride = BN <= 128 ? 128 : 256;
@@ -132,12 +180,19 @@ struct TcCfg {
   static_assert(kSmem <= 232448, "227 KB of shared memory per CTA");
 };
 
-// Persistent: CTA b processes work units b, b + gridDim.x, ... where a unit
-// is (output tile, K split).  The TMA producer and the MMA issuer run through
-// their units without pausing between tiles; a unit's epilogue (stores, or
-// exact int32 atomics for a split unit) overlaps the next unit's MMAs.
-template <int kKind, int BN>
-__global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(
+// Persistent: CTA b (CTA pair b with kPair) processes work units b, b + G,
+// ... (G = the number of CTAs, or of pairs) where a unit is (output tile,
+// K split).  The TMA producer and the MMA issuer run through their units
+// without pausing between tiles; a unit's epilogue (stores, or exact int32
+// reductions for a split unit) overlaps the next unit's MMAs.
+//
+// With kPair, CTA 0 of the pair owns the barriers that gate the MMA: the
+// full barrier of a stage expects both CTAs' bytes (each CTA's loads signal
+// CTA 0's barrier), and the accumulator-empty barrier counts the epilogue
+// warps of both CTAs (CTA 1's arrive remotely).  The MMA commits arrive on
+// the stage-empty and accumulator-full barriers of both CTAs at once.
+template <int kKind, int BN, bool kPair>
+__global__ void __launch_bounds__(TcCfg<BN, kPair>::kThreads, 1) gemm_tc_kernel(
     const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
     const __grid_constant__ CUtensorMap tmOut, const __grid_constant__ CUtensorMap tmAcc,
     const __grid_constant__ CUtensorMap tmSplit,
@@ -147,7 +202,7 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(
     int32_t* __restrict__ acc_out,
     int32_t* __restrict__ split_acc, unsigned int* __restrict__ slab_count,
     unsigned int* __restrict__ status) {
-  using C = TcCfg<BN>;
+  using C = TcCfg<BN, kPair>;
   constexpr int kStages = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -161,7 +216,11 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int first_unit = (int)blockIdx.x, unit_step = (int)gridDim.x;
+  // rank in the pair (0 without pairs) and this CTA's (or pair's) place in
+  // the persistent grid
+  const uint32_t rank = kPair ? cluster_rank() : 0u;
+  const int first_unit = kPair ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int unit_step = kPair ? (int)(gridDim.x >> 1) : (int)gridDim.x;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -170,32 +229,44 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], C::kEpiWarps);
+      mbar_init(&tempty[b], kPair ? 2 * C::kEpiWarps : C::kEpiWarps);
     }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     saddr(tmem_holder)),
-                 "r"(C::kTmemCols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    if (kPair) {  // one warp of each CTA of the pair allocates together
+      asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                       saddr(tmem_holder)),
+                   "r"(C::kTmemCols)
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    } else {
+      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                       saddr(tmem_holder)),
+                   "r"(C::kTmemCols)
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
   }
   tc_fence_before();
   __syncthreads();
+  if (kPair) cluster_sync();  // the peer's barriers exist before any remote signal
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
+  // barriers of CTA 0 that both CTAs of a pair signal
+  const uint32_t full_lead = kPair ? cluster_map(saddr(full), 0) : 0u;
+  const uint32_t tempty_lead = kPair ? cluster_map(saddr(tempty), 0) : 0u;
   // the prologue above overlaps the previous kernel; operands, scales and
   // outputs are touched only after it has completed
   pdl_trigger();
   pdl_wait();
 
-  // unit -> (m0, n0, first k-block, k-blocks)
+  // unit -> (first row of the tile, n0, first k-block, k-blocks)
   auto unit_coords = [&](int u, int& m0, int& n0, int& kb0, int& nkb) {
     const int t = u / splits, z = u - t * splits;
-    m0 = (t / tiles_n) * kBM;
+    m0 = (t / tiles_n) * C::kTileM;
     n0 = (t % tiles_n) * BN;
     kb0 = z * kb_per_split;
     nkb = max(0, min(num_kb, kb0 + kb_per_split) - kb0);
@@ -216,14 +287,22 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(
           const int s = i % kStages;
           const uint32_t ph = (uint32_t)(i / kStages) & 1u;
           if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, status)) break;
-          mbar_expect_tx(&full[s], C::kStageBytes);
           uint8_t* a = smem + s * C::kStageBytes;
           const int kx = (kb0 + j) * elems;
-          tma_load_2d(a, &tmA, &full[s], kx, m0);
-          tma_load_2d(a + C::kABytes, &tmB, &full[s], kx, n0);
+          if (kPair) {
+            // CTA 0 expects both halves; each CTA's copies signal CTA 0
+            if (rank == 0) mbar_expect_tx(&full[s], 2 * C::kStageBytes);
+            const uint32_t bar = full_lead + (uint32_t)(s * sizeof(uint64_t));
+            tma_load_2d_pair(a, &tmA, bar, kx, m0 + (int)rank * kBM);
+            tma_load_2d_pair(a + C::kABytes, &tmB, bar, kx, n0 + (int)rank * C::kBRows);
+          } else {
+            mbar_expect_tx(&full[s], C::kStageBytes);
+            tma_load_2d(a, &tmA, &full[s], kx, m0);
+            tma_load_2d(a + C::kABytes, &tmB, &full[s], kx, n0);
+          }
         }
       }
-      if (*abort_flag) {  // let the copies already issued land before exit
+      if (*abort_flag && !kPair) {  // let the copies already issued land before exit
         for (int k = max(0, i - kStages); k < i; ++k) {
           const unsigned long long t0 = now_ns();
           while (!mbar_test(&full[k % kStages], (uint32_t)(k / kStages) & 1u) &&
@@ -233,8 +312,8 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      constexpr uint32_t idesc = make_idesc(kKind, kBM, BN);
+    if (lane == 0 && rank == 0) {  // the MMA issuer (CTA 0 of a pair)
+      constexpr uint32_t idesc = make_idesc(kKind, C::kTileM, BN);
       int i = 0, cc = 0;  // k-blocks and accumulation chunks consumed so far
       bool ok = true;
       for (int u = first_unit; u < num_units && ok; u += unit_step) {
@@ -244,7 +323,8 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(
         for (int c = 0, j = 0; c < nch && ok; ++c, ++cc) {
           const int buf = cc & 1;
           const uint32_t use = (uint32_t)(cc >> 1);
-          if (!mbar_wait(&tempty[buf], (use & 1u) ^ 1u, abort_flag, status)) {
+          // CTA 1's epilogue warps arrive here from the other SM of a pair
+          if (!mbar_wait(&tempty[buf], (use & 1u) ^ 1u, abort_flag, status, kPair)) {
             ok = false;
             break;
           }
@@ -263,11 +343,11 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(
             const uint32_t b = a + C::kABytes;
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-              mma_issue<kKind>(d, sw128_desc(a + 32 * k), sw128_desc(b + 32 * k), idesc,
-                               (jj > 0 || k > 0) ? 1u : 0u);
-            mma_commit(&empty[s]);
+              mma_issue<kKind, kPair>(d, sw128_desc(a + 32 * k), sw128_desc(b + 32 * k), idesc,
+                                      (jj > 0 || k > 0) ? 1u : 0u);
+            mma_commit_to<kPair>(&empty[s]);
           }
-          if (ok) mma_commit(&tfull[buf]);
+          if (ok) mma_commit_to<kPair>(&tfull[buf]);
         }
       }
     }
@@ -276,8 +356,19 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(
     const int ew = warp - 2;
     const int quarter = warp & 3;  // TMEM lanes this warp may access
     const int colgrp = ew >> 2;
-    const int row = quarter * 32 + lane;
+    const int row = (int)rank * kBM + quarter * 32 + lane;  // row within the tile
     uint8_t* stg = stage_out + ew * C::kStageOutBytes;
+    // accumulator buffer drained: tell the MMA issuer (CTA 0 of a pair)
+    auto release_acc = [&](int buf) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (kPair && rank != 0)
+          mbar_arrive_cluster(tempty_lead + (uint32_t)(buf * sizeof(uint64_t)));
+        else
+          mbar_arrive(&tempty[buf]);
+      }
+    };
     // One 32 x 32 box of 32-bit values (this thread's row, 32 columns)
     // through the warp's staging buffer (128B swizzle: 16-byte chunk c of row
     // r at c ^ (r % 8), conflict-free) and a TMA store, which clips rows >= M
@@ -317,7 +408,7 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(
       unit_coords(u, m0, n0, kb0, nkb);
       const int m = m0 + row;
       const int nb = n0 + colgrp * C::kColsPerThread;
-      const int y = m0 + quarter * 32;
+      const int y = m0 + (int)rank * kBM + quarter * 32;
       if constexpr (kKind == 0) {
         // one accumulation chunk, never split: stream each 32-column TMEM
         // slice straight into a store box
@@ -335,11 +426,7 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(
         for (int jc = 0; jc < C::kColsPerThread / 32; ++jc) {
           uint32_t r[32];
           tmem_ld_x32(taddr + 32 * jc, r);
-          if (jc == C::kColsPerThread / 32 - 1) {  // accumulator read out: release it
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&tempty[buf]);
-          }
+          if (jc == C::kColsPerThread / 32 - 1) release_acc(buf);  // read out
           const int x = nb + 32 * jc;
           if (x >= N) continue;
           if (acc_out) {
@@ -378,9 +465,7 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(
           for (int q = 0; q < 32; ++q)
             acc[32 * jc + q] += __float2int_rn(__uint_as_float(r[q]));
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tempty[buf]);
+        release_acc(buf);
       }
       if (!ok) break;
       if (splits == 1) {
@@ -428,9 +513,11 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(
         tma_store_wait_all();  // the reductions are performed
         asm volatile("fence.proxy.async.global;" ::: "memory");
         __threadfence();
+        // slab counters per (128-row half tile, epilogue warp)
         const int t = u / splits;
-        last = atomicAdd(&slab_count[(size_t)t * C::kEpiWarps + ew], 1u) ==
-               (unsigned int)(splits - 1);
+        const int half = (t / tiles_n) * (C::kTileM / kBM) + (int)rank;
+        const int slab = (half * tiles_n + t % tiles_n) * C::kEpiWarps + ew;
+        last = atomicAdd(&slab_count[slab], 1u) == (unsigned int)(splits - 1);
         if (last) __threadfence();
       }
       last = __shfl_sync(0xffffffffu, last, 0);
@@ -442,11 +529,11 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(
           const int x = nb + 32 * jc;
           if (x >= N) break;
           int32_t sum[32];
-          const int32_t* row = split_acc + (size_t)m * N + x;
+          const int32_t* rowp = split_acc + (size_t)m * N + x;
 #pragma unroll
           for (int q = 0; q < 32; q += 4) {
             int4 w4 = make_int4(0, 0, 0, 0);
-            if (m < M && x + q < N) w4 = __ldcg(reinterpret_cast<const int4*>(row + q));
+            if (m < M && x + q < N) w4 = __ldcg(reinterpret_cast<const int4*>(rowp + q));
             sum[q] = w4.x; sum[q + 1] = w4.y; sum[q + 2] = w4.z; sum[q + 3] = w4.w;
           }
           uint32_t v[32];
@@ -473,17 +560,25 @@ __global__ void __launch_bounds__(TcCfg<BN>::kThreads, 1) gemm_tc_kernel(
 
   tc_fence_before();
   __syncthreads();
-  if (*abort_flag) {  // let in-flight tensor-core work finish before freeing TMEM
+  if (*abort_flag) {  // let in-flight copies and tensor-core work finish
     const unsigned long long t0 = now_ns();
     while (now_ns() - t0 < 1000000ull) {
     }
   }
+  // a pair leaves together: no remote arrive or copy may target a CTA that
+  // has exited, and the peer's TMEM is freed only after CTA 0's MMAs
+  if (kPair) cluster_sync();
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
-                 "r"(C::kTmemCols)
-                 : "memory");
+    if (kPair)
+      asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                   "r"(C::kTmemCols)
+                   : "memory");
+    else
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                   "r"(C::kTmemCols)
+                   : "memory");
   }
 }
 
@@ -533,7 +628,10 @@ bool make_out_map(CUtensorMap* map, const void* ptr, bool is_int, int64_t rows,
   return r == CUDA_SUCCESS;
 }
 
-template <int kKind, int BN>
+// Persistent grid of one CTA per SM, or of as many CTA pairs as fit at once
+// (clusters of two need both SMs of a pair free; the count comes from the
+// occupancy query for this kernel, cached per device).
+template <int kKind, int BN, bool kPair>
 cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& mo,
                       const CUtensorMap& macc, const CUtensorMap& msplit, int64_t M, int64_t N,
                       int num_kb, int chunk_kb,
@@ -541,9 +639,10 @@ cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, const CUtensor
                       const float* sb, bool per_col_b, float* out, int32_t* acc_out,
                       int32_t* split_acc, unsigned int* slab_count, unsigned int* status,
                       cudaStream_t st) {
-  using C = TcCfg<BN>;
-  auto kernel = gemm_tc_kernel<kKind, BN>;
+  using C = TcCfg<BN, kPair>;
+  auto kernel = gemm_tc_kernel<kKind, BN, kPair>;
   static bool attr_set[64] = {};
+  static int max_pairs[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -556,13 +655,46 @@ cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, const CUtensor
   }
   const int kb_per_split = (num_kb + splits - 1) / splits;
   const int tiles_n = (int)((N + BN - 1) / BN);
-  const int64_t units = ((M + kBM - 1) / kBM) * tiles_n * splits;
+  const int64_t units = ((M + C::kTileM - 1) / C::kTileM) * tiles_n * splits;
   if (units > 0x7fffffff) return cudaErrorInvalidValue;
-  const int grid = (int)(units < num_sms ? units : num_sms);
-  cudaError_t le = launch_pdl(kernel, dim3(grid), dim3(C::kThreads), C::kSmem, st, a, b, mo,
-                              macc, msplit, (int)M, (int)N, num_kb, chunk_kb, kb_per_split, splits,
-                              tiles_n, (int)units, sa, per_row_a ? 1 : 0, sb,
-                              per_col_b ? 1 : 0, out, acc_out, split_acc, slab_count, status);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  int grid_ctas;
+  if (kPair) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 2;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    if (!max_pairs[dev]) {
+      cudaLaunchConfig_t q = {};
+      q.gridDim = dim3(2 * (num_sms / 2));
+      q.blockDim = dim3(C::kThreads);
+      q.dynamicSmemBytes = C::kSmem;
+      q.attrs = &attr[1];
+      q.numAttrs = 1;
+      int n = 0;
+      e = cudaOccupancyMaxActiveClusters(&n, kernel, &q);
+      if (e != cudaSuccess) return e;
+      if (n <= 0) return cudaErrorInvalidConfiguration;
+      max_pairs[dev] = n;
+    }
+    const int64_t pairs = units < max_pairs[dev] ? units : max_pairs[dev];
+    grid_ctas = (int)(2 * pairs);
+  } else {
+    grid_ctas = (int)(units < num_sms ? units : num_sms);
+  }
+  cfg.gridDim = dim3(grid_ctas);
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kSmem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = kPair ? 2 : 1;
+  cudaError_t le = cudaLaunchKernelEx(&cfg, kernel, a, b, mo, macc, msplit, (int)M, (int)N,
+                                      num_kb, chunk_kb, kb_per_split, splits, tiles_n,
+                                      (int)units, sa, per_row_a ? 1 : 0, sb, per_col_b ? 1 : 0,
+                                      out, acc_out, split_acc, slab_count, status);
   if (le != cudaSuccess) return le;
   return cudaGetLastError();
 }
@@ -585,11 +717,24 @@ bool make_tile_map_2d(CUtensorMap* map, const void* ptr, bool bf16, int64_t rows
   return r == CUDA_SUCCESS;
 }
 
+// Slab counters of a split plan: one per (128-row half tile, epilogue warp);
+// pair tiles are 256 rows, so M rounds up to a multiple of 256 there.
+static int64_t split_slabs(int64_t M, int64_t N, int bn, bool pair) {
+  const int64_t halves = pair ? 2 * ((M + 255) / 256) : (M + kBM - 1) / kBM;
+  return halves * ((N + bn - 1) / bn) * (bn > 128 ? 8 : 4);
+}
+
 size_t gemm_tc_split_ws_bytes(int64_t M, int64_t N) {
-  // int32 partial sums, then one counter per (tile, epilogue warp) slab
-  // (128-wide tiles x 8 slabs covers both tile widths)
-  const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + 127) / 128);
-  return (size_t)M * (size_t)N * 4 + (size_t)tiles * 8 * 4 + 256;
+  // int32 partial sums, then the slab counters of whichever tile shape the
+  // plan takes
+  int64_t slabs = 0;
+  for (int bn : {96, 128, 256})
+    for (bool pair : {false, true})
+      if (!(pair && bn == 96)) {
+        const int64_t n = split_slabs(M, N, bn, pair);
+        slabs = n > slabs ? n : slabs;
+      }
+  return (size_t)M * (size_t)N * 4 + (size_t)slabs * 4 + 256;
 }
 
 GemmPlan plan_gemm_tc(int kind, int64_t M, int64_t N, int64_t K, int num_sms,
@@ -628,6 +773,19 @@ GemmPlan plan_gemm_tc(int kind, int64_t M, int64_t N, int64_t K, int num_sms,
     while (s > 1 && (p.num_kb + s - 1) / s < 2 * p.chunk_kb) --s;
     p.splits = s > 1 ? s : 1;
   }
+  // CTA pairs: the same tile width over 256 rows per pair, i.e. the same
+  // output per SM with half the B bytes delivered to each SM.  They pay
+  // where the mainloop runs in steady state: at least 16 k-blocks per tile
+  // and 4 waves of tiles (Llama down_proj on GB300: g_x 679 -> 552 us,
+  // g_w 699 -> 564 us).  Short contractions and single-wave GEMMs ran
+  // slower on pairs, whose two epilogues gate each accumulator buffer
+  // together (ResNet-50 im2col g_x, K = 256: 80 -> 97 us; ViT-B fc2 g_x,
+  // K = 768: 41 -> 45 us; ViT-B qkv g_w, one wave: 41 -> 43 us).
+  const int64_t tiles1 = tiles_m * ((N + p.bn - 1) / p.bn);
+  p.pair = (p.splits == 1 && p.bn != 96 && M > kBM && p.num_kb >= 16 &&
+            tiles1 >= (int64_t)4 * num_sms)
+               ? 1
+               : 0;
   return p;
 }
 
@@ -641,11 +799,13 @@ cudaError_t launch_gemm_tc(int kind, const void* A, int64_t lda, const void* B,
   if (!get_encode()) return cudaErrorNotSupported;
   const bool bf16 = kind == 1;
   if ((plan.bn != 96 && plan.bn != 128 && plan.bn != 256) ||
-      (plan.splits > 1 && kind == 0) || (per_col_b && kind == 0))
+      (plan.splits > 1 && kind == 0) || (per_col_b && kind == 0) ||
+      (plan.pair && plan.bn == 96))
     return cudaErrorInvalidValue;
   CUtensorMap ma, mb, mo, macc, msplit;
   if (!make_map(&ma, A, bf16, M, K, lda, kBM)) return cudaErrorInvalidValue;
-  if (!make_map(&mb, B, bf16, N, K, ldb, plan.bn)) return cudaErrorInvalidValue;
+  if (!make_map(&mb, B, bf16, N, K, ldb, plan.pair ? plan.bn / 2 : plan.bn))
+    return cudaErrorInvalidValue;
   memset(&mo, 0, sizeof(mo));
   memset(&macc, 0, sizeof(macc));
   memset(&msplit, 0, sizeof(msplit));
@@ -658,10 +818,9 @@ cudaError_t launch_gemm_tc(int kind, const void* A, int64_t lda, const void* B,
     if (!make_out_map(&msplit, split_acc, true, M, N)) return cudaErrorInvalidValue;
     slab_count = reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(split_ws) +
                                                  (size_t)M * (size_t)N * 4);
-    const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + plan.bn - 1) / plan.bn);
-    const int epi_warps = plan.bn > 128 ? 8 : 4;
-    cudaError_t e = cudaMemsetAsync(
-        split_ws, 0, (size_t)M * (size_t)N * 4 + (size_t)tiles * epi_warps * 4, st);
+    const int64_t slabs = split_slabs(M, N, plan.bn, plan.pair != 0);
+    cudaError_t e = cudaMemsetAsync(split_ws, 0, (size_t)M * (size_t)N * 4 + (size_t)slabs * 4,
+                                    st);
     if (e != cudaSuccess) return e;
   }
   int dev = 0, sms = 0;
@@ -669,14 +828,17 @@ cudaError_t launch_gemm_tc(int kind, const void* A, int64_t lda, const void* B,
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
       sms <= 0)
     return cudaErrorInvalidDevice;
-#define TC(KIND, BN)                                                                  \
-  launch_tc<KIND, BN>(ma, mb, mo, macc, msplit, M, N, plan.num_kb, plan.chunk_kb,         \
-                      plan.splits,                                                       \
-                      sms, sa, per_row_a, sb, per_col_b, out, acc_out, split_acc,       \
-                      slab_count,                                                        \
-                      status, st)
-  if (kind == 0) return plan.bn == 256 ? TC(0, 256) : (plan.bn == 96 ? TC(0, 96) : TC(0, 128));
-  return plan.bn == 256 ? TC(1, 256) : (plan.bn == 96 ? TC(1, 96) : TC(1, 128));
+#define TC(KIND, BN, PAIR)                                                                 \
+  launch_tc<KIND, BN, PAIR>(ma, mb, mo, macc, msplit, M, N, plan.num_kb, plan.chunk_kb,      \
+                            plan.splits, sms, sa, per_row_a, sb, per_col_b, out, acc_out,    \
+                            split_acc, slab_count, status, st)
+  if (plan.pair) {
+    if (kind == 0) return plan.bn == 256 ? TC(0, 256, true) : TC(0, 128, true);
+    return plan.bn == 256 ? TC(1, 256, true) : TC(1, 128, true);
+  }
+  if (kind == 0)
+    return plan.bn == 256 ? TC(0, 256, false) : (plan.bn == 96 ? TC(0, 96, false) : TC(0, 128, false));
+  return plan.bn == 256 ? TC(1, 256, false) : (plan.bn == 96 ? TC(1, 96, false) : TC(1, 128, false));
 #undef TC
 }
 

@@ -122,10 +122,11 @@ bool make_tile_map_2d(CUtensorMap* map, const void* ptr, bool bf16, int64_t rows
 // kind 1: bf16 operands (int8 codes).  A [M, K] (row stride lda elements),
 // B [N, K] (ldb); out [M, N] fp32 = acc * sa[m or 0] * sb[0] / 16.
 struct GemmPlan {
-  int bn = 128;      // tile width (128 or 256)
+  int bn = 128;      // tile width (96, 128 or 256)
   int splits = 1;    // K split count (int32 workspace reduction)
   int num_kb = 0;    // k-blocks of 128 bytes
   int chunk_kb = 0;  // k-blocks per exact fp32 accumulation chunk
+  int pair = 0;      // 1: a CTA pair per 256-row tile (tcgen05 cta_group::2)
 };
 GemmPlan plan_gemm_tc(int kind, int64_t M, int64_t N, int64_t K, int num_sms,
                       int max_splits);

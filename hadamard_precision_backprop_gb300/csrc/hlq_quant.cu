@@ -1676,9 +1676,13 @@ cudaError_t launch_hq_rows(const void* src, bool bf16, int64_t rows,
   const int threads = 256, warps = threads / 32;
   dim3 grid(grid1(rows, warps));
   // per-token rows wait transformed (fp32) in shared memory between the two
-  // passes when 8 of them fit in 160 KB (Cout <= 5120), else re-read
+  // passes when the staging leaves room for three CTAs (24 warps) per SM
+  // (Cout <= 2304: 72 KB per CTA); longer rows are read again (from L1/L2,
+  // right after the first pass) and transformed again instead: with one
+  // CTA of 8 staged 4096-value rows per SM (128 KB) the Llama-shaped HQ of
+  // g_y took 236 us, issue-bound at 8 warps per SM
   const size_t row_bytes = (size_t)((cols / 8 + 31) / 32) * 64 * 16;
-  const bool stage = per_token && !amax_only && row_bytes * warps <= 160 * 1024;
+  const bool stage = per_token && !amax_only && row_bytes * warps <= 74 * 1024;
   const size_t smem = stage ? row_bytes * warps : 0;
 #define HQR(B, M, P)                                                              \
   do {                                                                            \

@@ -48,17 +48,35 @@ __device__ __forceinline__ bool mbar_test(uint64_t* b, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait with cluster-scope acquire, for barriers that threads of other
+// CTAs of the cluster arrive on (with release at cluster scope).
+__device__ __forceinline__ bool mbar_test_cluster(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(saddr(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait for the phase of parity `parity` to complete; gives up after
 // `limit_ns` (or as soon as another role gave up), raising HLQ_DEV_TIMEOUT
 // once.
 __device__ __forceinline__ bool mbar_wait_for(uint64_t* b, uint32_t parity,
                                               volatile int* abort_flag,
                                               unsigned int* status,
-                                              unsigned long long limit_ns) {
-  if (mbar_test(b, parity)) return true;
+                                              unsigned long long limit_ns,
+                                              bool cluster_scope = false) {
+  auto test = [&]() {
+    return cluster_scope ? mbar_test_cluster(b, parity) : mbar_test(b, parity);
+  };
+  if (test()) return true;
   const unsigned long long t0 = now_ns();
   while (true) {
-    if (mbar_test(b, parity)) return true;
+    if (test()) return true;
     if (*abort_flag) return false;
     if (now_ns() - t0 > limit_ns) {
       if (atomicExch((int*)abort_flag, 1) == 0) atomicOr(status, HLQ_DEV_TIMEOUT);
@@ -68,8 +86,50 @@ __device__ __forceinline__ bool mbar_wait_for(uint64_t* b, uint32_t parity,
 }
 __device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity,
                                           volatile int* abort_flag,
-                                          unsigned int* status) {
-  return mbar_wait_for(b, parity, abort_flag, status, kWaitNs);
+                                          unsigned int* status,
+                                          bool cluster_scope = false) {
+  return mbar_wait_for(b, parity, abort_flag, status, kWaitNs, cluster_scope);
+}
+
+// Address of the same shared-memory object in CTA `rank` of the cluster
+// (a shared::cluster address).
+__device__ __forceinline__ uint32_t cluster_map(uint32_t local_saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_saddr), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Every thread of every CTA of the cluster (release / acquire at cluster
+// scope, so shared-memory writes before it are seen by peers after it).
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Arrive on an mbarrier of another CTA of the cluster (shared::cluster
+// address), releasing this thread's earlier writes at cluster scope.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(
+                   cluster_addr)
+               : "memory");
+}
+
+// Tile load into this CTA's shared memory whose completion is signalled on
+// an mbarrier that may live in the peer CTA of a CTA pair (shared::cluster
+// address of the barrier): the operand loads of the pair GEMM.
+__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map,
+                                                 uint32_t bar_cluster, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".cta_group::2 [%0], [%1, {%2, %3}], [%4];" ::"r"(saddr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster)
+      : "memory");
 }
 
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map,

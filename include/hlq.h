@@ -287,12 +287,14 @@ hlq_status hlq_debug_reference_gemm(int kind, const void *d_a, const void *d_b,
  * lda / ldb: row strides in elements (16-byte multiples).  bn: tile width
  * 96, 128 or 256 (0 = the library's choice); splits: K split count (0 = the
  * library's choice; > 1 needs d_ws of hlq_debug_tc_gemm_ws_bytes(M, N);
- * kind 0 runs unsplit).  M, N, K multiples of 16.  An unsupported plan is
- * HLQ_ERR_INVALID_ARG.
+ * kind 0 runs unsplit); pair: 1 = a CTA pair per 256-row tile (tcgen05
+ * cta_group::2; tile widths 128 and 256), 0 = one CTA per 128-row tile,
+ * -1 = the library's choice.  M, N, K multiples of 16.  An unsupported
+ * plan is HLQ_ERR_INVALID_ARG.
  */
 hlq_status hlq_debug_tc_gemm(int kind, const void *d_a, int64_t lda,
                              const void *d_b, int64_t ldb, int64_t M, int64_t N,
-                             int64_t K, int bn, int splits, int32_t *d_acc,
+                             int64_t K, int bn, int splits, int pair, int32_t *d_acc,
                              void *d_ws, size_t ws_bytes, void *stream);
 size_t hlq_debug_tc_gemm_ws_bytes(int64_t M, int64_t N);
 
@@ -311,11 +313,12 @@ hlq_status hlq_debug_wait_timeout(uint64_t limit_ns, int32_t *d_result, void *st
  * and K split of the g_x GEMM (E4M3, M = T, N = Cin, K = Cout) and of the
  * g_w GEMM (bf16, M = Cout, N = Cin, K = T*rank/16), and whether the g_w
  * GEMM is ordered after the g_x GEMM (1: each has at least one unit per SM,
- * so running them side by side would only delay the later one).
+ * so running them side by side would only delay the later one), and
+ * whether each GEMM runs on CTA pairs (1) or one CTA per tile (0).
  */
 hlq_status hlq_debug_gemm_plan(int64_t T, int64_t Cin, int64_t Cout, int rank, int sms,
                                int *gx_bn, int *gx_splits, int *gw_bn, int *gw_splits,
-                               int *in_sequence);
+                               int *in_sequence, int *gx_pair, int *gw_pair);
 
 /*
  * Layer-wise quantizer selection for the HQ of g_y (HOT summary page,

@@ -134,8 +134,8 @@ def test_compress_argument_validation(L):
 def test_tc_gemm_plan_validation(L):
     f = L.hlq_debug_tc_gemm
 
-    def call(bn=128, splits=1, kind=1, M=256, N=256, K=256):
-        return f(kind, FAKE, K, FAKE, K, M, N, K, bn, splits, FAKE, FAKE_WS, 1 << 30,
+    def call(bn=128, splits=1, kind=1, M=256, N=256, K=256, pair=-1):
+        return f(kind, FAKE, K, FAKE, K, M, N, K, bn, splits, pair, FAKE, FAKE_WS, 1 << 30,
                  None)
 
     assert call(bn=64) == 1
@@ -144,6 +144,9 @@ def test_tc_gemm_plan_validation(L):
     assert call(kind=0, splits=2) == 1        # the E4M3 GEMM runs unsplit
     assert call(bn=192) == 1
     assert call(M=200) == 2
+    assert call(pair=2) == 1
+    assert call(pair=-2) == 1
+    assert call(bn=96, pair=1) == 1           # CTA pairs take 128- and 256-wide tiles
 
 
 def test_step_host_validation_and_workspace(L):

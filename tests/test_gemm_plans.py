@@ -17,15 +17,25 @@ def _lib():
     hlq.lib()
 
 
-@pytest.mark.parametrize("T,Cin,Cout,gx,gw,seq", [
-    (12608, 768, 2304, (256, 1), (128, 1), False),    # ViT-B qkv
-    (12608, 3072, 768, (256, 1), (128, 1), False),    # ViT-B fc2
-    (16384, 14336, 4096, (256, 1), (256, 1), True),   # Llama down_proj
-    (50176, 2304, 256, (256, 1), (128, 4), False),    # ResNet-50 im2col: 36 tiles, split
+# CTA pairs only where they were measured faster: long contractions over
+# several waves of tiles (Llama down_proj); not for the short-K g_x GEMMs of
+# fc2 and ResNet-50, nor for the single-wave g_w GEMMs of ViT-B.
+@pytest.mark.parametrize("T,Cin,Cout,gx,gw,seq,gx_pair,gw_pair", [
+    (12608, 768, 2304, (256, 1), (128, 1), False, False, False),   # ViT-B qkv
+    (12608, 3072, 768, (256, 1), (128, 1), False, False, False),   # ViT-B fc2
+    (16384, 14336, 4096, (256, 1), (256, 1), True, True, True),    # Llama down_proj
+    (50176, 2304, 256, (256, 1), (128, 4), False, False, False),   # ResNet-50 im2col
 ])
-def test_layer_plans_on_gb300(T, Cin, Cout, gx, gw, seq):
+def test_layer_plans_on_gb300(T, Cin, Cout, gx, gw, seq, gx_pair, gw_pair):
     p = hlq.hlq_debug_gemm_plan(T, Cin, Cout, rank=8, sms=152)
     assert p["gx"] == gx and p["gw"] == gw and p["in_sequence"] == seq
+    assert p["gx_pair"] is gx_pair and p["gw_pair"] is gw_pair
+
+
+def test_pairs_need_more_than_one_row_tile():
+    # a g_x GEMM over 128 tokens, a g_w GEMM over 128 output channels
+    p = hlq.hlq_debug_gemm_plan(128, 768, 128, rank=8, sms=152)
+    assert p["gx_pair"] is False and p["gw_pair"] is False
 
 
 def test_plan_rules():

@@ -29,32 +29,50 @@ def _lib():
     hlq.lib()
 
 
-def run(kind, A, B, bn, splits):
+def run(kind, A, B, bn, splits, pair=-1):
     if kind == 0:
         a = torch.from_numpy(e4m3_bytes(A)).cuda()
         b = torch.from_numpy(e4m3_bytes(B)).cuda()
     else:
         a = torch.from_numpy(A.astype(np.float32)).cuda().to(torch.bfloat16)
         b = torch.from_numpy(B.astype(np.float32)).cuda().to(torch.bfloat16)
-    return hlq.hlq_debug_tc_gemm(kind, a, b, bn=bn, splits=splits)
+    return hlq.hlq_debug_tc_gemm(kind, a, b, bn=bn, splits=splits, pair=pair)
 
 
-# Every tile width, unsplit, for both kinds; K splits for the bf16 GEMM only
-# (the E4M3 GEMM runs unsplit: the ABI refuses a split plan for it, which the
-# CPU plan-validation test checks).
-PLANS = ([(kind, qmax, bn, 1) for kind, qmax in ((0, 7), (1, 127)) for bn in (128, 256, 96)]
-         + [(1, 127, bn, splits) for bn, splits in ((128, 3), (256, 2), (96, 2))])
+def test_tc_gemm_pair_one_tile():
+    """The smallest CTA-pair GEMM: one 256 x 256 tile (one pair), one and
+    several k-blocks, both operand kinds; the first GPU check of the pair
+    path, kept apart so that it runs before the larger cases."""
+    for kind, qmax in ((0, 7), (1, 127)):
+        for K in (128, 256, 1024):
+            rng = np.random.default_rng(K + kind)
+            A = rng.integers(-qmax, qmax + 1, (256, K))
+            B = rng.integers(-qmax, qmax + 1, (256, K))
+            got = run(kind, A, B, 256, 1, pair=1).cpu().numpy()
+            np.testing.assert_array_equal(got.astype(np.int64),
+                                          A.astype(np.int64) @ B.astype(np.int64).T)
+    assert hlq.hlq_read_device_status() == 0
 
 
-@pytest.mark.parametrize("kind,qmax,bn,splits", PLANS)
+# Every tile width, unsplit, for both kinds, on one CTA per tile and on CTA
+# pairs (128- and 256-wide); K splits for the bf16 GEMM only (the E4M3 GEMM
+# runs unsplit: the ABI refuses a split plan for it, which the CPU
+# plan-validation test checks).
+PLANS = ([(kind, qmax, bn, 1, 0) for kind, qmax in ((0, 7), (1, 127)) for bn in (128, 256, 96)]
+         + [(kind, qmax, bn, 1, 1) for kind, qmax in ((0, 7), (1, 127)) for bn in (128, 256)]
+         + [(1, 127, bn, splits, 0) for bn, splits in ((128, 3), (256, 2), (96, 2))]
+         + [(1, 127, bn, splits, 1) for bn, splits in ((128, 3), (256, 2))])
+
+
+@pytest.mark.parametrize("kind,qmax,bn,splits,pair", PLANS)
 @pytest.mark.parametrize("M,N,K", [(128, 128, 128), (16, 32, 16), (272, 400, 208),
                                    (384, 512, 2048), (1040, 144, 4112)])
-def test_tc_gemm_exact(kind, qmax, M, N, K, bn, splits):
+def test_tc_gemm_exact(kind, qmax, M, N, K, bn, splits, pair):
     rng = np.random.default_rng(M * 7 + N * 3 + K + bn + splits)
     A = rng.integers(-qmax, qmax + 1, (M, K))
     B = rng.integers(-qmax, qmax + 1, (N, K))
     want = A.astype(np.int64) @ B.astype(np.int64).T
-    got = run(kind, A, B, bn, splits).cpu().numpy()
+    got = run(kind, A, B, bn, splits, pair).cpu().numpy()
     np.testing.assert_array_equal(got.astype(np.int64), want)
     ref = hlq.hlq_debug_reference_gemm(torch.from_numpy(A.astype(np.int8)).cuda(),
                                        torch.from_numpy(B.astype(np.int8)).cuda())
@@ -81,8 +99,8 @@ def test_tc_gemm_bf16_worst_case_magnitude():
     A = np.full((M, K), 127, np.int64)
     A[1::2] = -127
     B = np.full((N, K), 127, np.int64)
-    for splits in (1, 2, 5):
-        got = run(1, A, B, 128, splits).cpu().numpy()
+    for splits, pair in ((1, 0), (2, 0), (5, 0), (1, 1), (3, 1)):
+        got = run(1, A, B, 128, splits, pair).cpu().numpy()
         assert got[0, 0] == 16129 * K and got[1, 0] == -16129 * K
         assert np.all(got[0::2] == 16129 * K) and np.all(got[1::2] == -16129 * K)
 
@@ -93,5 +111,6 @@ def test_tc_gemm_e4m3_worst_case_magnitude():
     A[::3] = -7
     B = np.full((N, K), -7, np.int64)
     want = A[:, :1] * B[:, 0][None, :] * K
-    got = run(0, A, B, 256, 1).cpu().numpy()
-    np.testing.assert_array_equal(got, want)
+    for pair in (0, 1):
+        got = run(0, A, B, 256, 1, pair).cpu().numpy()
+        np.testing.assert_array_equal(got, want)
