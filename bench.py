@@ -84,6 +84,12 @@ def parse_args(argv=None):
     p.add_argument("--no-variants", action="store_true",
                    help="skip the timings of the optional paths (int4 / "
                         "per-channel ACBP, quantizer selection, ablations)")
+    p.add_argument("--profile", choices=["compress", "gx", "gw", "step"],
+                   help="no timing: call this one entry point --warmup times on "
+                        "the workload and exit (a small, fixed launch sequence "
+                        "for a profiler)")
+    p.add_argument("--tokens", type=int, default=0,
+                   help="with --profile: use the first TOKENS tokens only")
     return p.parse_args(argv)
 
 
@@ -730,12 +736,14 @@ def measure_workload(args, wl, dev, dist, headline):
         e2e_step()
     torch.cuda.synchronize()
     barrier()
-    e2e_ms = []
+    e2e_ms, enqueue_ms = [], []
     for _ in range(args.steps):
         flush.fill_(1)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
+        h0 = time.perf_counter()
         e2e_step()
+        enqueue_ms.append((time.perf_counter() - h0) * 1e3)
         b.record(stream)
         b.synchronize()
         e2e_ms.append(a.elapsed_time(b))
@@ -743,10 +751,55 @@ def measure_workload(args, wl, dev, dist, headline):
     e2e = max_over_ranks(e2e, dist, dev)
     barrier()
     res["e2e_ms"] = e2e
+    res["e2e_spread"] = {"min_us": min(e2e_ms) * 1e3, "median_us": statistics.median(e2e_ms) * 1e3,
+                         "max_us": max(e2e_ms) * 1e3,
+                         "host_enqueue_us": statistics.median(enqueue_ms) * 1e3}
     res["e2e_bytes"] = ((x.numel() + gy.numel() + w.numel()) * e,
                         (gx.numel() + gw.numel()) * 4)
     res["acbp_stored_bytes"] = acbp_bytes(T, Cin, wl.rank, e)
     return res, inp
+
+
+def run_profile(args, wl):
+    """Call one entry point of the step on the workload's inputs (optionally
+    its first --tokens tokens), --warmup times, and return: what a profiler
+    captures, with no timing of its own."""
+    import dataclasses
+    import torch
+    import hadamard_precision_backprop_gb300 as hlq
+    from hadamard_precision_backprop_gb300 import build as hbuild
+
+    hbuild.build()
+    if args.tokens:
+        wl = dataclasses.replace(wl, T=min(wl.T, args.tokens // 16 * 16))
+    inp = workloads.make_inputs(wl, T=wl.T)
+    torch.cuda.set_device(0)
+
+    def dev(name):
+        if wl.dtype == "bf16":
+            return torch.from_numpy(inp[name + "_bits"].view(np.int16)).view(
+                torch.bfloat16).cuda()
+        return torch.from_numpy(inp[name]).cuda()
+
+    x, gy, w = dev("x"), dev("g_y"), dev("w")
+    xbar, sx = hlq.hlq_compress_activation(x, rank=wl.rank)
+    torch.cuda.synchronize()
+    for _ in range(max(1, args.warmup)):
+        if args.profile == "compress":
+            hlq.hlq_compress_activation(x, rank=wl.rank, out=xbar, scale=sx)
+        elif args.profile == "gx":
+            hlq.hlq_linear_backward_gx(gy, w, gran_gy=wl.gran_gy, gran_w=wl.gran_w,
+                                       rnd=hlq.SR, seed=wl.seed)
+        elif args.profile == "gw":
+            hlq.hlq_linear_backward_gw(gy, xbar, sx, rank=wl.rank)
+        else:
+            hlq.hlq_layer_step(x, gy, w, rank=wl.rank, gran_gy=wl.gran_gy,
+                               gran_w=wl.gran_w, rnd=hlq.SR, seed=wl.seed,
+                               xbar=xbar, xbar_scale=sx)
+    torch.cuda.synchronize()
+    print(json.dumps({"profiled": args.profile, "workload": wl.name, "T": wl.T,
+                      "calls": max(1, args.warmup)}))
+    return 0
 
 
 def run_ours(args, wl, rank, world, local_rank):
@@ -798,7 +851,7 @@ def run_ours(args, wl, rank, world, local_rank):
         "clocks": res["clocks"],
         "e2e": {"value": job_us_per_layer(res["e2e_ms"], world), "unit": UNIT,
                 "h2d_bytes_per_step": res["e2e_bytes"][0],
-                "d2h_bytes_per_step": res["e2e_bytes"][1]},
+                "d2h_bytes_per_step": res["e2e_bytes"][1], **res["e2e_spread"]},
         "per_workload": per_workload,
     }
     if world == 1 and not args.no_cpu_baseline:
@@ -866,6 +919,8 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
         return run_reference(args, wl, rank, world)
+    if args.profile:
+        return run_profile(args, wl)
     if world > 1:
         import torch
         import torch.distributed as dist

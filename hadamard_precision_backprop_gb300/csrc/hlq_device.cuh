@@ -415,13 +415,15 @@ __device__ __forceinline__ U4 philox_block(uint64_t seed, uint32_t stream,
                        (uint32_t)seed, (uint32_t)(seed >> 32));
 }
 
-// The ten round keys of a seed, computed once per thread and reused for
-// every block it draws (the key schedule does not depend on the counter).
+// The ten round keys of a seed (the key schedule does not depend on the
+// counter).  The launchers compute them on the host and pass them by value,
+// so the kernels read them from the parameter (constant) bank instead of
+// holding twenty registers per thread.
 struct PhiloxKeys {
   uint32_t k0[10], k1[10];
 };
 
-__device__ __forceinline__ PhiloxKeys philox_keys(uint64_t seed) {
+__host__ __device__ __forceinline__ PhiloxKeys philox_keys(uint64_t seed) {
   PhiloxKeys k;
   uint32_t a = (uint32_t)seed, b = (uint32_t)(seed >> 32);
 #pragma unroll
@@ -452,32 +454,13 @@ __device__ __forceinline__ U4 philox_block_k(const PhiloxKeys& k, uint32_t strea
 }
 
 // ---------------------------------------------------------------------------
-// Quantizers.  s == 0 gives code 0.  Division is IEEE round-to-nearest.
+// Quantizers, float-valued (integer-valued results, clamped to +-qmax):
+//   SR:  x = RN(y / s), f = floor(x), q = f + [u < x - f], u = (word >> 8) 2^-24
+//   RNE: q = rint(RN(y / s))
+// Division is IEEE round-to-nearest.  The _nz forms are for a scale known
+// to be non-zero (callers that branch on s == 0 once per row or tensor);
+// the _f forms give 0 when s == 0.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ int quant_sr(float y, float s, uint32_t word,
-                                        int qmax) {
-  if (s == 0.0f) return 0;
-  float x = __fdiv_rn(y, s);
-  float f = floorf(x);
-  float frac = x - f;
-  float u = __uint2float_rn(word >> 8) * 5.9604644775390625e-08f;  // 2^-24
-  float r = f + ((u < frac) ? 1.0f : 0.0f);
-  r = fminf(fmaxf(r, -(float)qmax), (float)qmax);
-  return (int)r;
-}
-
-__device__ __forceinline__ int quant_rne(float y, float s, int qmax) {
-  if (s == 0.0f) return 0;
-  float x = __fdiv_rn(y, s);
-  float r = rintf(x);
-  r = fminf(fmaxf(r, -(float)qmax), (float)qmax);
-  return (int)r;
-}
-
-// Float-valued forms of the two roundings (integer-valued results, clamped);
-// s == 0 gives 0.
-// The same for a scale known to be non-zero (callers that branch on s == 0
-// once per row or tensor).
 __device__ __forceinline__ float quant_sr_nz(float y, float s, uint32_t word, float qmax) {
   const float x = __fdiv_rn(y, s);
   const float f = floorf(x);
@@ -489,8 +472,7 @@ __device__ __forceinline__ float quant_rne_nz(float y, float s, float qmax) {
   return fminf(fmaxf(rintf(__fdiv_rn(y, s)), -qmax), qmax);
 }
 
-__device__ __forceinline__ float quant_sr_f(float y, float s, uint32_t word,
-                                            float qmax) {
+__device__ __forceinline__ float quant_sr_f(float y, float s, uint32_t word, float qmax) {
   const float r = quant_sr_nz(y, s, word, qmax);
   return s == 0.0f ? 0.0f : r;
 }

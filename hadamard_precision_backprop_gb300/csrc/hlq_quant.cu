@@ -304,7 +304,7 @@ template <bool kBf16, int kMode, bool kPerToken>
 __global__ void __launch_bounds__(256) hq_rows_kernel(
     const void* __restrict__ src, int64_t rows, int64_t cols,
     unsigned int* __restrict__ amax_slot, uint8_t* __restrict__ codes,
-    float* __restrict__ scales, int rnd, uint64_t seed, uint32_t stream,
+    float* __restrict__ scales, int rnd, const PhiloxKeys keys, uint32_t stream,
     unsigned int* __restrict__ status, int stage, int64_t e_off) {
   pdl_trigger();
   pdl_wait();
@@ -367,7 +367,6 @@ __global__ void __launch_bounds__(256) hq_rows_kernel(
     if (kPerToken) scales[row] = s;
     else if (row == 0) scales[0] = s;
   }
-  const PhiloxKeys keys = philox_keys(seed);
   __syncwarp();
   if (s == 0.0f) {  // warp-uniform: an all-zero row (or tensor) has all-zero codes
 #pragma unroll 1
@@ -1113,7 +1112,7 @@ __global__ void __launch_bounds__(128) gy_fused_kernel(
     const __grid_constant__ CUtensorMap tm, int64_t T, int64_t C,
     unsigned int* __restrict__ hq_amax, unsigned int* __restrict__ hla_amax,
     uint8_t* __restrict__ qy, float* __restrict__ sgy, void* __restrict__ qg,
-    int64_t hla_ld, float* __restrict__ sg, int rnd, uint64_t seed,
+    int64_t hla_ld, float* __restrict__ sg, int rnd, const PhiloxKeys keys,
     unsigned int* __restrict__ status) {
   constexpr int kStage = 16 * kTmaCols * (kBf16 ? 2 : 4);
   using F = ColFmt<kColBf16>;
@@ -1197,7 +1196,6 @@ __global__ void __launch_bounds__(128) gy_fused_kernel(
         if (blk_ok[1]) am_hq = fmaxf(am_hq, fabsf(v[1][i]));
       }
     } else {
-      const PhiloxKeys keys = philox_keys(seed);
       const int64_t e = tok * C + cb;
       quantize_octet(v[0], s_hq, rnd, keys, 0u, e, 0, qy);
       quantize_octet(v[0] + 8, s_hq, rnd, keys, 0u, e + 8, 0, qy);
@@ -1308,7 +1306,7 @@ template <bool kBf16, int kMode>
 __global__ void __launch_bounds__(128) hq_w_kernel(
     const void* __restrict__ src, int64_t rows, int64_t cols,
     unsigned int* __restrict__ amax_slot, uint8_t* __restrict__ codes_t,
-    float* __restrict__ scale, int rnd, uint64_t seed, uint32_t stream,
+    float* __restrict__ scale, int rnd, const PhiloxKeys keys, uint32_t stream,
     unsigned int* __restrict__ status) {
   pdl_trigger();
   pdl_wait();
@@ -1337,7 +1335,6 @@ __global__ void __launch_bounds__(128) hq_w_kernel(
   const float s = __fdiv_rn(__uint_as_float(ld_dep_u32(amax_slot)), 7.0f);
   if (blockIdx.x == 0 && threadIdx.x == 0) scale[0] = s;
   if (!ok) return;
-  const PhiloxKeys keys = philox_keys(seed);
   uint32_t w[4][4] = {};  // column c's 16 code bytes (code i in byte i)
 #pragma unroll
   for (int i = 0; i < 16; i += 2) {
@@ -1379,7 +1376,7 @@ template <bool kBf16, int kMode>
 __global__ void __launch_bounds__(256) hq_w_pair_kernel(
     const void* __restrict__ src, int64_t rows, int64_t cols,
     unsigned int* __restrict__ amax_slot, uint8_t* __restrict__ codes_t,
-    float* __restrict__ scale, int rnd, uint64_t seed, uint32_t stream,
+    float* __restrict__ scale, int rnd, const PhiloxKeys keys, uint32_t stream,
     unsigned int* __restrict__ status) {
   pdl_trigger();
   pdl_wait();
@@ -1419,7 +1416,6 @@ __global__ void __launch_bounds__(256) hq_w_pair_kernel(
   const float s = __fdiv_rn(__uint_as_float(ld_dep_u32(amax_slot)), 7.0f);
   if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) scale[0] = s;
   if (ok) {
-    const PhiloxKeys keys = philox_keys(seed);
     const bool hi = (c0 & 2) != 0;
     float h8[2][8];  // this thread's half of the coefficients (static indexing)
 #pragma unroll
@@ -1690,7 +1686,7 @@ cudaError_t launch_hq_rows(const void* src, bool bf16, int64_t rows,
         ensure_smem_limit<hq_rows_kernel<B, M, P>>(160 * 1024) != cudaSuccess)    \
       return cudaGetLastError();                                                  \
     launch_pdl(hq_rows_kernel<B, M, P>, grid, dim3(threads), smem, st, src, rows,  \
-               cols, amax_slot, codes, scales, rnd, seed, stream_id, status,       \
+               cols, amax_slot, codes, scales, rnd, philox_keys(seed), stream_id, status,       \
                stage ? 1 : 0, row0 * cols);                                       \
   } while (0)
   if (amax_only) {
@@ -1765,12 +1761,14 @@ cudaError_t launch_hq_cols(const void* src, bool bf16, int64_t rows,
     return cudaErrorInvalidDevice;
   // quad kernel when it has at least 4 CTAs of 128 threads per SM, else the
   // pair kernel's 8x more threads (ViT-B qkv w: 14.7 us pair, 18.7 us quad;
-  // Llama down_proj w: 219 us pair, 152 us quad)
+  // Llama down_proj w: 219 us pair, 152 us quad; one thread per column pair
+  // with the quad's random words shared by shuffles measured 146 us against
+  // the quad kernel's 134 us there)
   if (threads >= (int64_t)sms * 4 * 128) {
     const dim3 grid(grid1(threads, 128));
 #define HQW(B, M)                                                                   \
   launch_pdl(hq_w_kernel<B, M>, grid, dim3(128), 0, st, src, rows, cols, amax_slot, \
-             codes_t, scale, rnd, seed, stream_id, status)
+             codes_t, scale, rnd, philox_keys(seed), stream_id, status)
     if (amax_only) {
       if (bf16) HQW(true, kAmax); else HQW(false, kAmax);
     } else {
@@ -1781,7 +1779,7 @@ cudaError_t launch_hq_cols(const void* src, bool bf16, int64_t rows,
     const dim3 grid(grid1(cols, kWCols), grid1(rows / 16, kWBlocks));
 #define HQP(B, M)                                                                        \
   launch_pdl(hq_w_pair_kernel<B, M>, grid, dim3(256), 0, st, src, rows, cols, amax_slot, \
-             codes_t, scale, rnd, seed, stream_id, status)
+             codes_t, scale, rnd, philox_keys(seed), stream_id, status)
     if (amax_only) {
       if (bf16) HQP(true, kAmax); else HQP(false, kAmax);
     } else {
@@ -1881,7 +1879,7 @@ cudaError_t launch_gy_fused(const void* gy, bool bf16, int64_t T, int64_t C, int
     cudaError_t e = ensure_smem_limit<gy_fused_kernel<B, M, P, R>>(smem);                \
     if (e != cudaSuccess) return e;                                                      \
     launch_pdl(gy_fused_kernel<B, M, P, R>, dim3((unsigned)tiles), dim3(128), smem, st, tm, \
-               T, C, hq_amax, hla_amax, qy, sgy, qg, hla_ld, sg, rnd, seed, status);     \
+               T, C, hq_amax, hla_amax, qy, sgy, qg, hla_ld, sg, rnd, philox_keys(seed), status);     \
   } while (0)
 #define GYF_R(B, M, P)                         \
   switch (rank) {                              \
