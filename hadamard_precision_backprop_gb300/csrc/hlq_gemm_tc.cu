@@ -197,7 +197,7 @@ __global__ void __launch_bounds__(TcCfg<BN, kPair>::kThreads, 1) gemm_tc_kernel(
     const __grid_constant__ CUtensorMap tmOut, const __grid_constant__ CUtensorMap tmAcc,
     const __grid_constant__ CUtensorMap tmSplit,
     int M, int N, int num_kb, int chunk_kb, int kb_per_split, int splits, int tiles_n,
-    int num_units, const float* __restrict__ sa, int per_row_a,
+    int tiles_m, int group_m, int num_units, const float* __restrict__ sa, int per_row_a,
     const float* __restrict__ sb, int per_col_b, float* __restrict__ out,
     int32_t* __restrict__ acc_out,
     int32_t* __restrict__ split_acc, unsigned int* __restrict__ slab_count,
@@ -263,13 +263,24 @@ __global__ void __launch_bounds__(TcCfg<BN, kPair>::kThreads, 1) gemm_tc_kernel(
   pdl_trigger();
   pdl_wait();
 
-  // unit -> (first row of the tile, n0, first k-block, k-blocks)
-  auto unit_coords = [&](int u, int& m0, int& n0, int& kb0, int& nkb) {
+  // unit -> (row tile, column tile, first k-block, k-blocks).  Tiles go in
+  // groups of group_m row tiles; within a group the row tile changes
+  // fastest, so the units in flight at once share their B tiles and the
+  // group's A rows stay in L2 while the column tiles go by.
+  auto unit_tile = [&](int u, int& tm, int& tn, int& kb0, int& nkb) {
     const int t = u / splits, z = u - t * splits;
-    m0 = (t / tiles_n) * C::kTileM;
-    n0 = (t % tiles_n) * BN;
+    const int g = t / (group_m * tiles_n), r = t - g * (group_m * tiles_n);
+    const int gm = min(group_m, tiles_m - g * group_m);  // rows of this group
+    tn = r / gm;
+    tm = g * group_m + (r - tn * gm);
     kb0 = z * kb_per_split;
     nkb = max(0, min(num_kb, kb0 + kb_per_split) - kb0);
+  };
+  auto unit_coords = [&](int u, int& m0, int& n0, int& kb0, int& nkb) {
+    int tm, tn;
+    unit_tile(u, tm, tn, kb0, nkb);
+    m0 = tm * C::kTileM;
+    n0 = tn * BN;
   };
 
   if (warp == 0) {
@@ -514,9 +525,10 @@ __global__ void __launch_bounds__(TcCfg<BN, kPair>::kThreads, 1) gemm_tc_kernel(
         asm volatile("fence.proxy.async.global;" ::: "memory");
         __threadfence();
         // slab counters per (128-row half tile, epilogue warp)
-        const int t = u / splits;
-        const int half = (t / tiles_n) * (C::kTileM / kBM) + (int)rank;
-        const int slab = (half * tiles_n + t % tiles_n) * C::kEpiWarps + ew;
+        int tm, tn, kb0u, nkbu;
+        unit_tile(u, tm, tn, kb0u, nkbu);
+        const int half = tm * (C::kTileM / kBM) + (int)rank;
+        const int slab = (half * tiles_n + tn) * C::kEpiWarps + ew;
         last = atomicAdd(&slab_count[slab], 1u) == (unsigned int)(splits - 1);
         if (last) __threadfence();
       }
@@ -655,8 +667,20 @@ cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, const CUtensor
   }
   const int kb_per_split = (num_kb + splits - 1) / splits;
   const int tiles_n = (int)((N + BN - 1) / BN);
-  const int64_t units = ((M + C::kTileM - 1) / C::kTileM) * tiles_n * splits;
+  const int tiles_m = (int)((M + C::kTileM - 1) / C::kTileM);
+  const int64_t units = (int64_t)tiles_m * tiles_n * splits;
   if (units > 0x7fffffff) return cudaErrorInvalidValue;
+  // row tiles per group: as many as keep the group's A rows within 48 MB of
+  // L2 (the Llama down_proj g_w GEMM, A rows of 4 MB per 256-row tile, read
+  // 2.9 GB from HBM for 0.3 GB of operands with the column tile changing
+  // fastest, 1.0 GB grouped: 564 -> 489 us; its g_x GEMM 553 -> 537 us).
+  // Short contractions (< 16 k-blocks) are bound by their fp32 output and
+  // keep the row-major tile order, whose stores fill whole output rows
+  // together (ResNet-50 im2col g_x, K = 256: 80 us row-major, 92 grouped).
+  const int64_t a_tile_bytes = (int64_t)C::kTileM * num_kb * kRowBytes;
+  int group_m = (int)((48ll << 20) / (a_tile_bytes > 0 ? a_tile_bytes : 1));
+  group_m = group_m < 1 ? 1 : (group_m > tiles_m ? tiles_m : group_m);
+  if (num_kb < 16) group_m = 1;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -692,9 +716,10 @@ cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, const CUtensor
   cfg.attrs = attr;
   cfg.numAttrs = kPair ? 2 : 1;
   cudaError_t le = cudaLaunchKernelEx(&cfg, kernel, a, b, mo, macc, msplit, (int)M, (int)N,
-                                      num_kb, chunk_kb, kb_per_split, splits, tiles_n,
-                                      (int)units, sa, per_row_a ? 1 : 0, sb, per_col_b ? 1 : 0,
-                                      out, acc_out, split_acc, slab_count, status);
+                                      num_kb, chunk_kb, kb_per_split, splits, tiles_n, tiles_m,
+                                      group_m, (int)units, sa, per_row_a ? 1 : 0, sb,
+                                      per_col_b ? 1 : 0, out, acc_out, split_acc, slab_count,
+                                      status);
   if (le != cudaSuccess) return le;
   return cudaGetLastError();
 }
