@@ -464,7 +464,7 @@ def measure_workload(args, wl, dev, dist, headline):
             t = torch.from_numpy(inp[name + "_bits"].view(np.int16)).view(torch.bfloat16)
         else:
             t = torch.from_numpy(inp[name])
-        return t.pin_memory() if headline else t
+        return t.pin_memory()
 
     h_x, h_gy, h_w = host_tensor("x"), host_tensor("g_y"), host_tensor("w")
     x, gy, w = (t.to(dev) for t in (h_x, h_gy, h_w))
@@ -649,14 +649,8 @@ def measure_workload(args, wl, dev, dist, headline):
         "clocks": clk,
         "config": config_of(wl),
     }
-    if not headline:
-        del x, gy, w, ws0, ws1, ws_step, xbar, gx, gw, flush
-        torch.cuda.synchronize()
-        torch.cuda.empty_cache()
-        return res, inp
-
     variants = {}
-    if not args.no_variants and (dist is None):
+    if headline and not args.no_variants and (dist is None):
         xb4 = torch.empty(hlq.xbar_shape(T, Cin, wl.rank, 4), dtype=torch.uint8, device=dev)
         sxc = torch.empty(Cin, dtype=torch.float32, device=dev)
         mse = torch.empty(2, dtype=torch.float64, device=dev)
@@ -757,6 +751,10 @@ def measure_workload(args, wl, dev, dist, headline):
     res["e2e_bytes"] = ((x.numel() + gy.numel() + w.numel()) * e,
                         (gx.numel() + gw.numel()) * 4)
     res["acbp_stored_bytes"] = acbp_bytes(T, Cin, wl.rank, e)
+    if not headline:
+        del x, gy, w, ws0, ws1, ws_step, xbar, gx, gw, flush, ws_host, h_gx, h_gw
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
     return res, inp
 
 
@@ -822,10 +820,13 @@ def run_ours(args, wl, rank, world, local_rank):
             if other.name == wl.name:
                 continue
             r, _ = measure_workload(args, other, dev, dist, headline=False)
-            per_workload[other.name] = {
-                k: r[k] for k in ("us_per_layer", "backward_us", "forward_acbp_us",
-                                  "effective_tops", "gemm_int_tops", "roofline",
-                                  "rows", "kernels", "clocks")}
+            entry = {k: r[k] for k in ("us_per_layer", "backward_us", "forward_acbp_us",
+                                       "effective_tops", "gemm_int_tops", "roofline",
+                                       "rows", "kernels", "clocks")}
+            entry["e2e"] = {"value": r["e2e_ms"] * 1e3, "unit": UNIT,
+                            "h2d_bytes_per_step": r["e2e_bytes"][0],
+                            "d2h_bytes_per_step": r["e2e_bytes"][1], **r["e2e_spread"]}
+            per_workload[other.name] = entry
     if rank != 0:
         return 0
 

@@ -91,7 +91,7 @@ def lib() -> ctypes.CDLL:
                                              i32, i32, P, P, sz, P]),
             "hlq_debug_gx_parts": (i32, [P, P, i32, i64, i64, i64, i32, i32,
                                          i32, i32, u64, P, P, sz, P, P, P, P,
-                                         P, P]),
+                                         P, P, P, P]),
             "hlq_debug_gw_parts": (i32, [P, i32, P, P, i64, i64, i64, i32, i32,
                                          i32, P, P, sz, P, P, P, P]),
             "hlq_read_device_status": (i32, [P, i32, P]),
@@ -573,7 +573,9 @@ def hlq_ablation_gx_hla(g_y, w, rank: int = 8, block: int = 16, with_acc: bool =
 
 def hlq_debug_gx_parts(g_y, w, gran_gy=PER_TOKEN, gran_w=PER_TENSOR, rnd=SR,
                        seed=0, block=16, stream=None):
-    """g_x plus its intermediates: dict(g_x, qgy, sgy, qw, sw, acc)."""
+    """g_x plus its intermediates: dict(g_x, qgy, sgy, qw, sw, acc, and the
+    codes as packed int4 bytes: qgy_packed [T, Cout/2], qw_packed [Cin,
+    Cout/2])."""
     torch = _torch()
     _need_cuda_contig(g_y, w)
     T, Cout = g_y.shape
@@ -587,13 +589,16 @@ def hlq_debug_gx_parts(g_y, w, gran_gy=PER_TOKEN, gran_w=PER_TENSOR, rnd=SR,
         qw=torch.empty((Cin, Cout), dtype=torch.int8, device=dev),
         sw=torch.empty(1, dtype=torch.float32, device=dev),
         acc=torch.empty((T, Cin), dtype=torch.int32, device=dev),
+        qgy_packed=torch.empty((T, Cout // 2), dtype=torch.uint8, device=dev),
+        qw_packed=torch.empty((Cin, Cout // 2), dtype=torch.uint8, device=dev),
     )
     ws = workspace(OP_BACKWARD_GX, T, Cin, Cout, block, 16, dev)
     _check(lib().hlq_debug_gx_parts(
         _ptr(g_y), _ptr(w), _dtype_code(g_y), T, Cin, Cout, block, gran_gy,
         gran_w, rnd, seed, _ptr(r["g_x"]), _ptr(ws), _ws_bytes(ws, dev.index),
         _ptr(r["qgy"]), _ptr(r["sgy"]), _ptr(r["qw"]), _ptr(r["sw"]),
-        _ptr(r["acc"]), _stream(stream)), "hlq_debug_gx_parts")
+        _ptr(r["acc"]), _ptr(r["qgy_packed"]), _ptr(r["qw_packed"]), _stream(stream)),
+        "hlq_debug_gx_parts")
     return r
 
 

@@ -255,7 +255,8 @@ hlq_status gx_impl(const void* gy, const void* w, int dt, int64_t T,
                    size_t ws_bytes, int8_t* dbg_qgy, float* dbg_sgy,
                    int8_t* dbg_qw, float* dbg_sw, int32_t* dbg_acc,
                    void* stream, bool validate_only = false,
-                   cudaStream_t w_stream = nullptr) {
+                   cudaStream_t w_stream = nullptr, uint8_t* dbg_qgy_packed = nullptr,
+                   uint8_t* dbg_qw_packed = nullptr) {
   hlq_status st = check_common(dt, T, Cin, Cout, block);
   if (st != HLQ_OK) return st;
   if (gran_gy != HLQ_PER_TENSOR && gran_gy != HLQ_PER_TOKEN) return HLQ_ERR_INVALID_ARG;
@@ -330,6 +331,8 @@ hlq_status gx_impl(const void* gy, const void* w, int dt, int64_t T,
                             per_token, sw, gx, dbg_acc, nullptr, status, s));
   if (dbg_qgy) HLQ_TRY(launch_decode_e4m3(qy, dbg_qgy, T * Cout, s));
   if (dbg_qw) HLQ_TRY(launch_decode_e4m3(qw, dbg_qw, Cin * Cout, s));
+  if (dbg_qgy_packed) HLQ_TRY(launch_pack_e4m3_int4(qy, dbg_qgy_packed, T * Cout, s));
+  if (dbg_qw_packed) HLQ_TRY(launch_pack_e4m3_int4(qw, dbg_qw_packed, Cin * Cout, s));
   if (dbg_sgy)
     HLQ_TRY(cudaMemcpyAsync(dbg_sgy, sgy, (size_t)(per_token ? T : 1) * 4,
                             cudaMemcpyDeviceToDevice, s));
@@ -1212,10 +1215,11 @@ hlq_status hlq_debug_gx_parts(const void* d_gy, const void* d_w, int dt,
                               int gran_gy, int gran_w, int rnd, uint64_t seed,
                               float* d_gx, void* d_ws, size_t ws_bytes,
                               int8_t* d_qgy, float* d_sgy, int8_t* d_qw,
-                              float* d_sw, int32_t* d_acc, void* stream) {
+                              float* d_sw, int32_t* d_acc, uint8_t* d_qgy_packed,
+                              uint8_t* d_qw_packed, void* stream) {
   return gx_impl(d_gy, d_w, dt, T, Cin, Cout, block, gran_gy, gran_w, rnd,
                  seed, d_gx, d_ws, ws_bytes, d_qgy, d_sgy, d_qw, d_sw, d_acc,
-                 stream);
+                 stream, false, nullptr, d_qgy_packed, d_qw_packed);
 }
 
 hlq_status hlq_debug_gw_parts(const void* d_gy, int dt, const int8_t* d_xbar,

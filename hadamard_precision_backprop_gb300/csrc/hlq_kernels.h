@@ -95,6 +95,8 @@ cudaError_t launch_widen_i4_bf16(const uint8_t* in, void* out, int64_t rows, int
                                  int64_t out_ld, cudaStream_t st);
 cudaError_t launch_widen_i8_bf16(const int8_t* in, void* out, int64_t rows,
                                  int64_t cols, int64_t out_ld, cudaStream_t st);
+cudaError_t launch_pack_e4m3_int4(const uint8_t* in, uint8_t* out, int64_t n,
+                                  cudaStream_t st);
 cudaError_t launch_decode_e4m3(const uint8_t* in, int8_t* out, int64_t n,
                                cudaStream_t st);
 cudaError_t launch_decode_bf16(const void* in, int8_t* out, int64_t rows,

@@ -1472,6 +1472,43 @@ __global__ void __launch_bounds__(256) hq_w_pair_kernel(
 // transform of the row (it is still in L1/L2) gives both errors
 // (q * s - Y)^2, exact differences in fp64, summed per warp and added into
 // sums[0] (per tensor, scale from *amax_slot) and sums[1] (per token).
+// Squared quantization errors of one quantizer, accumulated without fp64
+// arithmetic per element (GB300's fp64 rate is a small fraction of its fp32
+// rate): with s scaled by 2^-E (E its exponent, so the scaled errors sit
+// near 1 and no square underflows) and the element by the same power of
+// two (exact), the error q s - y is the exact pair
+//   (RN(q s) - y) + (q s - RN(q s)),
+// the first difference exact by Sterbenz's lemma (q != 0 means y / s rounds
+// to q, so y and q s are within a factor of two; q == 0 gives -y), the
+// second the product's exact rounding error from one fused multiply-add.
+// Its square is a^2 (split exactly by another FMA) + 2 a b (rounded: a
+// correction ~2^-22 of a^2), the tiny b^2 dropped; the running sum is a
+// double-float pair updated with an exact two-sum.  About 46 significant
+// bits in all: the sums agree with an fp64 evaluation (exact differences,
+// rounded squares and sums) to far better than 1e-9 relative.
+struct ErrSum {
+  float hi = 0.0f, lo = 0.0f;
+  __device__ __forceinline__ void add_sq(float q, float s_scaled, float y_scaled) {
+    const float p = q * s_scaled;
+    const float pe = fmaf(q, s_scaled, -p);   // q s - RN(q s), exact
+    const float a = p - y_scaled;             // exact (Sterbenz)
+    const float sq = a * a;
+    const float sq_e = fmaf(a, a, -sq);       // a^2 - RN(a^2), exact
+    const float t = hi + sq;                  // two-sum of hi and sq
+    const float bv = t - hi;
+    const float err = (hi - (t - bv)) + (sq - bv);
+    hi = t;
+    lo += err + sq_e + 2.0f * a * pe;
+  }
+};
+
+// 2^-E for the scale's exponent E, clamped to [-100, 100] (0 for s == 0)
+__device__ __forceinline__ int scale_exp(float s) {
+  if (!(s > 0.0f)) return 0;
+  const int e = (int)((__float_as_uint(s) >> 23) & 0xffu) - 127;
+  return e < -100 ? -100 : (e > 100 ? 100 : e);
+}
+
 template <bool kBf16>
 __global__ void __launch_bounds__(256) hq_mse_kernel(const void* __restrict__ src,
                                                      int64_t rows, int64_t cols,
@@ -1497,7 +1534,10 @@ __global__ void __launch_bounds__(256) hq_mse_kernel(const void* __restrict__ sr
   amax = warp_max(amax);
   const float st = __fdiv_rn(amax, 7.0f);
   const float sg = __fdiv_rn(__uint_as_float(ld_dep_u32(amax_slot)), 7.0f);
-  double et = 0.0, eg = 0.0;
+  const int et = scale_exp(st), eg = scale_exp(sg);
+  const float pt = ldexpf(1.0f, -et), pg = ldexpf(1.0f, -eg);
+  const float st_s = st * pt, sg_s = sg * pg;
+  ErrSum at, ag;
   for (int it = 0; it < iters; ++it) {
     const int oct = it * 32 + lane;
     float v[8];
@@ -1505,20 +1545,20 @@ __global__ void __launch_bounds__(256) hq_mse_kernel(const void* __restrict__ sr
     if (oct >= n_oct) continue;
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-      const double dt = (double)quant_rne_f(v[k], st, 7.0f) * st - (double)v[k];
-      const double dg = (double)quant_rne_f(v[k], sg, 7.0f) * sg - (double)v[k];
-      et += dt * dt;
-      eg += dg * dg;
+      at.add_sq(quant_rne_f(v[k], st, 7.0f), st_s, v[k] * pt);
+      ag.add_sq(quant_rne_f(v[k], sg, 7.0f), sg_s, v[k] * pg);
     }
   }
+  double et_sum = ldexp((double)at.hi + (double)at.lo, 2 * et);
+  double eg_sum = ldexp((double)ag.hi + (double)ag.lo, 2 * eg);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
-    et += __shfl_xor_sync(0xffffffffu, et, o);
-    eg += __shfl_xor_sync(0xffffffffu, eg, o);
+    et_sum += __shfl_xor_sync(0xffffffffu, et_sum, o);
+    eg_sum += __shfl_xor_sync(0xffffffffu, eg_sum, o);
   }
   if (lane == 0) {
-    atomicAdd(&sums[0], eg);
-    atomicAdd(&sums[1], et);
+    atomicAdd(&sums[0], eg_sum);
+    atomicAdd(&sums[1], et_sum);
   }
 }
 
@@ -1628,6 +1668,18 @@ __global__ void decode_e4m3_kernel(const uint8_t* __restrict__ in,
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
        i += (int64_t)gridDim.x * blockDim.x)
     out[i] = (int8_t)int_of_e4m3(in[i]);
+}
+
+// E4M3 code bytes (integers in [-7, 7]) to packed int4: byte i holds codes
+// 2i (low nibble) and 2i + 1 (high nibble), two's complement.
+__global__ void pack_e4m3_int4_kernel(const uint8_t* __restrict__ in,
+                                      uint8_t* __restrict__ out, int64_t n_bytes) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_bytes;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const uint32_t lo = (uint32_t)int_of_e4m3(in[2 * i]) & 0xfu;
+    const uint32_t hi = (uint32_t)int_of_e4m3(in[2 * i + 1]) & 0xfu;
+    out[i] = (uint8_t)(lo | (hi << 4));
+  }
 }
 
 __global__ void decode_bf16_kernel(const __nv_bfloat16* __restrict__ in,
@@ -2004,6 +2056,14 @@ __global__ void wait_timeout_probe_kernel(unsigned long long limit_ns, int32_t* 
 cudaError_t launch_wait_timeout_probe(unsigned long long limit_ns, int32_t* result,
                                       unsigned int* status, cudaStream_t st) {
   wait_timeout_probe_kernel<<<1, 32, 0, st>>>(limit_ns, result, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pack_e4m3_int4(const uint8_t* in, uint8_t* out, int64_t n,
+                                  cudaStream_t st) {
+  const int64_t nb = n / 2;
+  if (nb == 0) return cudaSuccess;
+  pack_e4m3_int4_kernel<<<(unsigned)imin64(grid1(nb, 256), 4096), 256, 0, st>>>(in, out, nb);
   return cudaGetLastError();
 }
 

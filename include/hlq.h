@@ -221,15 +221,20 @@ hlq_status hlq_linear_backward_fused(const void *d_gy, const void *d_w,
  * checks (same formulas):
  *   d_qgy [T, Cout]  int8 codes of Y,   d_sgy [T] or [1] fp32,
  *   d_qw  [Cin, Cout] int8 codes of Wt (transposed: contraction dim
- *   contiguous),  d_sw [1],  d_acc [T, Cin] int32 accumulators.
- * Any of the five may be NULL.  Workspace as for HLQ_OP_BACKWARD_GX.
+ *   contiguous),  d_sw [1],  d_acc [T, Cin] int32 accumulators,
+ *   d_qgy_packed [T, Cout/2], d_qw_packed [Cin, Cout/2] bytes: the same
+ *   codes as packed int4 (two's-complement nibbles, code 2k of a row in
+ *   the low nibble of byte k), the layout of the method's int4 operands;
+ *   the GEMM itself reads one E4M3 byte per code.
+ * Any of the seven may be NULL.  Workspace as for HLQ_OP_BACKWARD_GX.
  */
 hlq_status hlq_debug_gx_parts(const void *d_gy, const void *d_w, int dt,
                               int64_t T, int64_t Cin, int64_t Cout, int block,
                               int gran_gy, int gran_w, int rnd, uint64_t seed,
                               float *d_gx, void *d_ws, size_t ws_bytes,
                               int8_t *d_qgy, float *d_sgy, int8_t *d_qw,
-                              float *d_sw, int32_t *d_acc, void *stream);
+                              float *d_sw, int32_t *d_acc, uint8_t *d_qgy_packed,
+                              uint8_t *d_qw_packed, void *stream);
 
 /*
  * hlq_linear_backward_gw with its intermediates copied out:

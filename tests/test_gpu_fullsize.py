@@ -81,6 +81,7 @@ def test_full_size_sampled(idx):
     qW = np.ascontiguousarray(qWt.T)
     assert_equal(host(r["sw"]), s_w, "s_w")
     assert_equal(host(r["qw"]), qW, "qW")
+    assert_equal(host(r["qw_packed"]), oracle.pack_int4(qW), "qW packed int4")
     rows = _sample_rows(wl.T, 1024, rng)
     if wl.gran_gy == workloads.PER_TOKEN:
         # every row's codes and scale (rows are independent under per-token
@@ -94,6 +95,8 @@ def test_full_size_sampled(idx):
         s_all = np.concatenate([p[1] for p in parts])
         assert_equal(host(r["sgy"]), s_all, "s_gy (every row)")
         assert_equal(host(r["qgy"]), qY_all, "qY (every row)")
+        assert_equal(host(r["qgy_packed"]), oracle.pack_int4(qY_all),
+                     "qY packed int4 (every row)")
         qYr, s_r = qY_all[rows], s_all[rows]
         del qY_all, parts
     else:

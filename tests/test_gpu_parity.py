@@ -38,6 +38,9 @@ def check_gx(inp, dtype, gran, rnd, seed):
     assert_equal(host(r["sw"]), ref["s_w"], "s_w")
     assert_equal(host(r["qgy"]), ref["qY"], "qY")
     assert_equal(host(r["qw"]), ref["qW"], "qW")
+    # the same codes in the method's packed int4 layout
+    assert_equal(host(r["qgy_packed"]), oracle.pack_int4(ref["qY"]), "qY packed int4")
+    assert_equal(host(r["qw_packed"]), oracle.pack_int4(ref["qW"]), "qW packed int4")
     assert_equal(host(r["acc"]).astype(np.int64), ref["acc"], "acc_gx")
     assert_rel(host(r["g_x"]), ref["g_x"], TOL, "g_x")
     # the public entry point runs the same kernels
