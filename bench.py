@@ -35,6 +35,7 @@ per step on a bounded sample and prints the same metric.
 from __future__ import annotations
 
 import argparse
+import gc
 import json
 import os
 import platform
@@ -90,7 +91,15 @@ def parse_args(argv=None):
                         "for a profiler)")
     p.add_argument("--tokens", type=int, default=0,
                    help="with --profile: use the first TOKENS tokens only")
+    p.add_argument("--gw-operands", choices=list(GW_MODES), default="auto",
+                   help="how the g_w GEMM takes its int8 operands "
+                        "(hlq_set_gw_operands): the library's default, x-bar "
+                        "widened by its own kernel, x-bar widened in the GEMM's "
+                        "shared memory, or both operands kept int8")
     return p.parse_args(argv)
+
+
+GW_MODES = {"auto": 0, "widen": 1, "int8_x": 2, "int8_both": 3}
 
 
 def pick_workload(spec):
@@ -442,6 +451,7 @@ def config_of(wl):
             "entry": ("hlq_compress_activation + hlq_linear_backward"
                       if getattr(ARGS, "serial", False) or getattr(ARGS, "fused_gy", False)
                       else "hlq_layer_step (compression beside the g_x branch)"),
+            "gw_operands": getattr(ARGS, "gw_operands", "auto"),
             "l2": "flushed before every timed step (256 MiB write)"}
 
 
@@ -690,6 +700,16 @@ def measure_workload(args, wl, dev, dist, headline):
         def ablation_gx():
             hlq.hlq_ablation_gx_hla(gy, w, rank=wl.rank, out=gx_a, ws=ws_agx)
 
+        def step_gw_mode(mode):
+            def fn():
+                prev = hlq.hlq_get_gw_operands()
+                hlq.hlq_set_gw_operands(mode)
+                try:
+                    step(x, gy, w)
+                finally:
+                    hlq.hlq_set_gw_operands(prev)
+            return fn
+
         for name, fn, what in [
                 ("fused_gy_step", step_fused_gy,
                  "whole step with one fused reader of g_y for HQ and HLA"),
@@ -702,7 +722,13 @@ def measure_workload(args, wl, dev, dist, headline):
                 ("ablation_gw_hq", ablation_gw,
                  "g_w through HQ along tokens and an int4 GEMM over T"),
                 ("ablation_gx_hla", ablation_gx,
-                 "g_x through HLA along Cout and an int8 GEMM over Cout*rank/16")]:
+                 "g_x through HLA along Cout and an int8 GEMM over Cout*rank/16"),
+                ("gw_widen_step", step_gw_mode(hlq.GW_WIDEN),
+                 "whole step, x-bar widened to fp16 by its own kernel"),
+                ("gw_int8_x_step", step_gw_mode(hlq.GW_INT8_X),
+                 "whole step, the g_w GEMM widening int8 x-bar in shared memory"),
+                ("gw_int8_both_step", step_gw_mode(hlq.GW_INT8_BOTH),
+                 "whole step, both g_w operands int8 in HBM, widened in shared memory")]:
             try:
                 variants[name] = {"us": time_replays(fn), "what": what}
             except Exception as exc:  # report, do not fail the main line
@@ -731,6 +757,10 @@ def measure_workload(args, wl, dev, dist, headline):
     torch.cuda.synchronize()
     barrier()
     e2e_ms, enqueue_ms = [], []
+    # the host enqueues every step inside the timed region, so a collection
+    # pause of the interpreter would be timed as GPU idle: none during it
+    gc.collect()
+    gc.disable()
     for _ in range(args.steps):
         flush.fill_(1)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -741,6 +771,7 @@ def measure_workload(args, wl, dev, dist, headline):
         b.record(stream)
         b.synchronize()
         e2e_ms.append(a.elapsed_time(b))
+    gc.enable()
     e2e = statistics.mean(e2e_ms)
     e2e = max_over_ranks(e2e, dist, dev)
     barrier()
@@ -768,6 +799,8 @@ def run_profile(args, wl):
     from hadamard_precision_backprop_gb300 import build as hbuild
 
     hbuild.build()
+    hlq.lib()
+    hlq.hlq_set_gw_operands(GW_MODES[args.gw_operands])
     if args.tokens:
         wl = dataclasses.replace(wl, T=min(wl.T, args.tokens // 16 * 16))
     inp = workloads.make_inputs(wl, T=wl.T)
@@ -807,6 +840,7 @@ def run_ours(args, wl, rank, world, local_rank):
 
     hbuild.build()
     hlq.lib()
+    hlq.hlq_set_gw_operands(GW_MODES[args.gw_operands])
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     dist = None

@@ -50,6 +50,7 @@ EXPORTS = [
     "hlq_layer_step",
     "hlq_debug_gemm_plan",
     "hlq_debug_wait_timeout",
+    "hlq_set_gw_operands", "hlq_get_gw_operands",
 ]
 
 _lock = threading.Lock()
@@ -125,6 +126,8 @@ def lib() -> ctypes.CDLL:
             "hlq_trace_end": (i32, [P]),
             "hlq_trace_get": (i32, [i32, P, P]),
             "hlq_trace_free": (i32, []),
+            "hlq_set_gw_operands": (i32, [i32]),
+            "hlq_get_gw_operands": (i32, []),
             "hlq_status_string": (ctypes.c_char_p, [i32]),
             "hlq_version": (i32, []),
         }
@@ -690,7 +693,8 @@ def hlq_debug_gemm_plan(T: int, Cin: int, Cout: int, rank: int = 8, sms: int = 1
 
 def hlq_debug_tc_gemm(kind, a, b, bn=0, splits=0, pair=-1, stream=None):
     """int32 a @ b^T on the tensor cores with an explicit plan.  kind 0: a, b
-    are uint8 E4M3 codes [M, K] / [N, K]; kind 1: bf16 codes.  pair: 1 = CTA
+    are uint8 E4M3 codes [M, K] / [N, K]; kind 1: fp16 codes; kind 2: a fp16,
+    b int8 codes (widened in the GEMM); kind 3: a and b int8.  pair: 1 = CTA
     pairs over 256-row tiles, 0 = one CTA per 128-row tile, -1 = the
     library's choice."""
     torch = _torch()
@@ -705,6 +709,22 @@ def hlq_debug_tc_gemm(kind, a, b, bn=0, splits=0, pair=-1, stream=None):
                                    _ws_bytes(ws, a.device.index),
                                    _stream(stream)), "hlq_debug_tc_gemm")
     return acc
+
+
+GW_AUTO, GW_WIDEN, GW_INT8_X, GW_INT8_BOTH = 0, 1, 2, 3
+
+
+def hlq_set_gw_operands(mode: int):
+    """How the g_w GEMMs take their int8 operands, for the whole process:
+    GW_WIDEN (x-bar widened to fp16 by its own kernel), GW_INT8_X (the GEMM
+    widens x-bar tiles in shared memory), GW_INT8_BOTH (the HLA codes of g_y
+    stay int8 too), GW_AUTO (the library's default).  Results are identical
+    in every mode."""
+    _check(lib().hlq_set_gw_operands(int(mode)), "hlq_set_gw_operands")
+
+
+def hlq_get_gw_operands() -> int:
+    return int(lib().hlq_get_gw_operands())
 
 
 def hlq_trace_begin(capacity: int = 4096):

@@ -109,7 +109,8 @@ struct GxLayout {
 };
 struct GwLayout {
   size_t amax, sg, qg, xw, split, total;
-  int64_t ld;  // row stride (codes) of the bf16 operand buffers
+  int64_t ld;   // row stride (codes) of the fp16 operand buffers
+  int64_t ld8;  // row stride of the HLA codes of g_y when they are kept int8
 };
 
 GxLayout gx_layout(int64_t T, int64_t Cin, int64_t Cout) {
@@ -127,18 +128,19 @@ GxLayout gx_layout(int64_t T, int64_t Cin, int64_t Cout) {
 GwLayout gw_layout(int64_t T, int64_t Cin, int64_t Cout, int rank) {
   GwLayout L{};
   const int64_t Tp = T / 16 * rank;
-  L.ld = (Tp + 7) / 8 * 8;  // 16-byte rows for the TMA
+  L.ld = (Tp + 7) / 8 * 8;     // 16-byte rows for the TMA
+  L.ld8 = (Tp + 15) / 16 * 16;  // the same for int8 rows (ld8 <= 2 ld)
   size_t o = 0;
   L.amax = o;  o += kAlign;
   L.sg = o;    o += kAlign;
-  L.qg = o;    o += align_up((size_t)Cout * (size_t)L.ld * 2);  // bf16 [Cout, ld]
-  L.xw = o;    o += align_up((size_t)Cin * (size_t)L.ld * 2);   // bf16 [Cin, ld]
+  L.qg = o;    o += align_up((size_t)Cout * (size_t)L.ld * 2);  // fp16 [Cout, ld] or int8 [Cout, ld8]
+  L.xw = o;    o += align_up((size_t)Cin * (size_t)L.ld * 2);   // fp16 [Cin, ld]
   L.split = o; o += align_up(gemm_tc_split_ws_bytes(Cout, Cin)); // int32 split-K
   L.total = o;
   return L;
 }
 
-// Workspace of the g_x HLA ablation: two amax slots, the two scales, bf16
+// Workspace of the g_x HLA ablation: two amax slots, the two scales, fp16
 // codes of g_y [T, ld] and of w [Cin, ld] (ld = Cout' rounded up to 8 codes
 // for 16-byte rows).
 struct GxHlaLayout {
@@ -358,17 +360,38 @@ hlq_status compress_launches(const void* x, bool bf16, int64_t T, int64_t Cin, i
   return HLQ_OK;
 }
 
-// HLA of g_y: per-tensor amax pass, then int8 codes stored as bf16 [Cout, ld].
+// How the g_w GEMM takes its operands (hlq_set_gw_operands): kRawB when it
+// reads the int8 x-bar itself, kRawA when the HLA codes of g_y stay int8 too.
+// The in-GEMM widening takes int8 x-bar whose rows are whole 16-byte runs
+// from a 16-byte aligned base; anything else goes through the widening
+// kernel.  The fused reader writes fp16 HLA codes (fused = true).
+int g_gw_operands = HLQ_GW_AUTO;
+
+int gw_raw(int fmt, int64_t Tp, const void* xbar, bool fused) {
+  // the default widens x-bar with its own kernel: measured on GB300, the
+  // g_w GEMM that widens int8 tiles in shared memory (its epilogue warps
+  // convert each stage before the MMA may read it) ran 1669 us at Llama
+  // down_proj against 489 + 68 (widening kernel) us, and 62.6 against
+  // 41.8 + 9.7 us at ViT-B qkv; both operands int8: 2214 and 73.7 us
+  int mode = g_gw_operands;
+  if (mode == HLQ_GW_AUTO) mode = HLQ_GW_WIDEN;
+  if (mode == HLQ_GW_WIDEN || xbar_code_bits(fmt) != 8 || Tp % 16 != 0 || !aligned16(xbar))
+    return 0;
+  return (mode == HLQ_GW_INT8_BOTH && !fused) ? (kRawA | kRawB) : kRawB;
+}
+
+// HLA of g_y: per-tensor amax pass, then int8 codes stored as fp16 [Cout, ld]
+// or, with i8, as int8 [Cout, ld8].
 hlq_status hla_gy_launches(const void* gy, bool bf16, int64_t T, int64_t Cout, int rank,
                            unsigned int* amax, void* qg, int64_t ld, float* sg,
-                           unsigned int* status, cudaStream_t s) {
+                           unsigned int* status, cudaStream_t s, bool i8 = false) {
   HLQ_TRY(cudaMemsetAsync(amax, 0, 4, s));
   HLQ_LAUNCH("hla_gy_amax", s,
-             launch_hla(gy, bf16, T, Cout, rank, true, kHlaOutBf16, amax, nullptr, 0, nullptr,
+             launch_hla(gy, bf16, T, Cout, rank, true, kHlaOutF16, amax, nullptr, 0, nullptr,
                         status, s));
   HLQ_LAUNCH("hla_gy_quant", s,
-             launch_hla(gy, bf16, T, Cout, rank, false, kHlaOutBf16, amax, qg, ld, sg, status,
-                        s));
+             launch_hla(gy, bf16, T, Cout, rank, false, i8 ? kHlaOutI8 : kHlaOutF16, amax, qg,
+                        ld, sg, status, s));
   return HLQ_OK;
 }
 
@@ -397,26 +420,34 @@ bool gemms_in_sequence(int64_t Mx, int64_t Cin, int64_t Cout, int64_t Tp) {
   return gemms_in_sequence_on(Mx, Cin, Cout, Tp, device_sm_count());
 }
 
+// The g_w GEMM over the HLA codes of g_y (fp16, or int8 with kRawA in raw)
+// and x-bar: read as int8 by the GEMM (kRawB in raw), or first widened to
+// fp16 in the workspace.
 hlq_status gw_gemm_launches(const int8_t* xbar, int fmt, const float* xscale, int64_t Cin,
                             int64_t Cout, int64_t Tp, const GwLayout& L, uint8_t* base,
                             float* gw, int32_t* dbg_acc, unsigned int* status,
-                            cudaStream_t s, cudaEvent_t after = nullptr) {
+                            cudaStream_t s, cudaEvent_t after, int raw) {
   void* xw = base + L.xw;
   const float* sg = reinterpret_cast<const float*>(base + L.sg);
-  if (xbar_code_bits(fmt) == 4)
-    HLQ_LAUNCH("widen_xbar", s,
-               launch_widen_i4_bf16(reinterpret_cast<const uint8_t*>(xbar), xw, Cin, Tp, L.ld,
-                                    s));
-  else
-    HLQ_LAUNCH("widen_xbar", s, launch_widen_i8_bf16(xbar, xw, Cin, Tp, L.ld, s));
+  if (!(raw & kRawB)) {
+    if (xbar_code_bits(fmt) == 4)
+      HLQ_LAUNCH("widen_xbar", s,
+                 launch_widen_i4_f16(reinterpret_cast<const uint8_t*>(xbar), xw, Cin, Tp, L.ld,
+                                     s));
+    else
+      HLQ_LAUNCH("widen_xbar", s, launch_widen_i8_f16(xbar, xw, Cin, Tp, L.ld, s));
+  }
   const int sms = device_sm_count();
   if (sms <= 0) return HLQ_ERR_CUDA;
   const GemmPlan plan = plan_gemm_tc(1, Cout, Cin, Tp, sms, 16);
   if (after) HLQ_TRY(cudaStreamWaitEvent(s, after, 0));
+  const void* b = (raw & kRawB) ? static_cast<const void*>(xbar) : xw;
+  const int64_t ldb = (raw & kRawB) ? Tp : L.ld;
+  const int64_t lda = (raw & kRawA) ? L.ld8 : L.ld;
   HLQ_LAUNCH("gemm_gw_tc", s,
-             launch_gemm_tc(1, base + L.qg, L.ld, xw, L.ld, Cout, Cin, Tp, plan, sg, false,
-                            xscale, gw, dbg_acc, base + L.split, status, s,
-                            xbar_per_channel(fmt)));
+             launch_gemm_tc(1, base + L.qg, lda, b, ldb, Cout, Cin, Tp, plan, sg, false, xscale,
+                            gw, dbg_acc, base + L.split, status, s, xbar_per_channel(fmt),
+                            raw));
   return HLQ_OK;
 }
 
@@ -460,12 +491,19 @@ hlq_status gw_impl(const void* gy, int dt, const int8_t* xbar, int fmt,
   void* qg = base + L.qg;
   const bool bf16 = dt == HLQ_BF16;
 
-  st = hla_gy_launches(gy, bf16, T, Cout, rank, amax, qg, L.ld, sg, status, s);
+  const int raw = gw_raw(fmt, Tp, xbar, false);
+  const bool qg_i8 = (raw & kRawA) != 0;
+  st = hla_gy_launches(gy, bf16, T, Cout, rank, amax, qg, qg_i8 ? L.ld8 : L.ld, sg, status, s,
+                       qg_i8);
   if (st != HLQ_OK) return st;
   st = gw_gemm_launches(xbar, fmt, xscale, Cin, Cout, Tp, L, base, gw, dbg_acc, status, s,
-                        gemm_after);
+                        gemm_after, raw);
   if (st != HLQ_OK) return st;
-  if (dbg_qg) HLQ_TRY(launch_decode_bf16(qg, dbg_qg, Cout, Tp, L.ld, s));
+  if (dbg_qg && qg_i8)
+    HLQ_TRY(cudaMemcpy2DAsync(dbg_qg, (size_t)Tp, qg, (size_t)L.ld8, (size_t)Tp, (size_t)Cout,
+                              cudaMemcpyDeviceToDevice, s));
+  else if (dbg_qg)
+    HLQ_TRY(launch_decode_f16(qg, dbg_qg, Cout, Tp, L.ld, s));
   if (dbg_sg) HLQ_TRY(cudaMemcpyAsync(dbg_sg, sg, 4, cudaMemcpyDeviceToDevice, s));
   return HLQ_OK;
 }
@@ -848,10 +886,10 @@ hlq_status hlq_ablation_gx_hla(const void* d_gy, const void* d_w, int dt, int64_
   HLQ_LAUNCH("hla_rows_gy_quant", s,
              launch_hla_rows(d_gy, bf16, T, Cout, rank, false, amax, qg, L.ld, sg, status, s));
   HLQ_LAUNCH("hla_w_amax", s,
-             launch_hla(d_w, bf16, Cout, Cin, rank, true, kHlaOutBf16, amax + 1, nullptr, 0,
+             launch_hla(d_w, bf16, Cout, Cin, rank, true, kHlaOutF16, amax + 1, nullptr, 0,
                         nullptr, status, s));
   HLQ_LAUNCH("hla_w_quant", s,
-             launch_hla(d_w, bf16, Cout, Cin, rank, false, kHlaOutBf16, amax + 1, qw, L.ld, sw,
+             launch_hla(d_w, bf16, Cout, Cin, rank, false, kHlaOutF16, amax + 1, qw, L.ld, sw,
                         status, s));
   const int sms = device_sm_count();
   if (sms <= 0) return HLQ_ERR_CUDA;
@@ -932,15 +970,17 @@ hlq_status hlq_linear_backward_fused(const void* d_gy, const void* d_w, const in
   fail(cudaMemsetAsync(gx_amax + 1, 0, 4, aw));
   if (r == HLQ_OK) r = hq_w_launches(d_w, bf16, Cout, Cin, gx_amax + 1, qw, sw, rnd, seed, status, aw);
   fail(cudaEventRecord(w_done, aw));
-  // the stored activation widened to bf16 meanwhile
+  // the stored activation widened to fp16 meanwhile (unless the GEMM reads
+  // the int8 codes itself)
+  const int gw_rw = gw_raw(xbar_fmt, Tp, d_xbar, true);
   fail(cudaStreamWaitEvent(a, fork, 0));
-  if (r == HLQ_OK) {
+  if (r == HLQ_OK && !(gw_rw & kRawB)) {
     trace_before(a);
     if (xbar_code_bits(xbar_fmt) == 4)
-      fail(launch_widen_i4_bf16(reinterpret_cast<const uint8_t*>(d_xbar), gwb + WL.xw, Cin, Tp,
+      fail(launch_widen_i4_f16(reinterpret_cast<const uint8_t*>(d_xbar), gwb + WL.xw, Cin, Tp,
                                 WL.ld, a));
     else
-      fail(launch_widen_i8_bf16(d_xbar, gwb + WL.xw, Cin, Tp, WL.ld, a));
+      fail(launch_widen_i8_f16(d_xbar, gwb + WL.xw, Cin, Tp, WL.ld, a));
     trace_after("widen_xbar", a);
   }
   // the two passes over g_y
@@ -976,9 +1016,10 @@ hlq_status hlq_linear_backward_fused(const void* d_gy, const void* d_w, const in
   if (r == HLQ_OK) {
     const GemmPlan pw = plan_gemm_tc(1, Cout, Cin, Tp, sms, 16);
     trace_before(s);
-    fail(launch_gemm_tc(1, gwb + WL.qg, WL.ld, gwb + WL.xw, WL.ld, Cout, Cin, Tp, pw, sg,
-                        false, d_xbar_scale, d_gw, nullptr, gwb + WL.split, status, s,
-                        xbar_per_channel(xbar_fmt)));
+    fail(launch_gemm_tc(1, gwb + WL.qg, WL.ld, (gw_rw & kRawB) ? (const void*)d_xbar : gwb + WL.xw,
+                        (gw_rw & kRawB) ? Tp : WL.ld, Cout, Cin, Tp, pw, sg, false,
+                        d_xbar_scale, d_gw, nullptr, gwb + WL.split, status, s,
+                        xbar_per_channel(xbar_fmt), gw_rw));
     trace_after("gemm_gw_tc", s);
   }
   return r;
@@ -1163,8 +1204,11 @@ hlq_status hlq_layer_step_host(const void* h_x, const void* h_gy, const void* h_
   }
   // g_w branch: HLA of g_y once all of it is in, then x's compression
   fail(cudaStreamWaitEvent(a_gw, gy_in[nc - 1], 0));
+  const int gw_rw = gw_raw(xbar_fmt, Tp, d_xbar, false);
   if (r == HLQ_OK)
-    r = hla_gy_launches(gy, bf16, T, Cout, rank, gw_amax, gwb + WL.qg, WL.ld, sg, status, a_gw);
+    r = hla_gy_launches(gy, bf16, T, Cout, rank, gw_amax, gwb + WL.qg,
+                        (gw_rw & kRawA) ? WL.ld8 : WL.ld, sg, status, a_gw,
+                        (gw_rw & kRawA) != 0);
   fail(cudaStreamWaitEvent(a_gw, x_in, 0));
   if (r == HLQ_OK)
     r = compress_launches(x, bf16, T, Cin, rank, xbar_fmt, d_xbar, d_xbar_scale,
@@ -1173,7 +1217,8 @@ hlq_status hlq_layer_step_host(const void* h_x, const void* h_gy, const void* h_
     r = gw_gemm_launches(d_xbar, xbar_fmt, d_xbar_scale, Cin, Cout, Tp, WL, gwb, gw, nullptr,
                          status, a_gw,
                          gemms_in_sequence(ch < T ? ch : T, Cin, Cout, Tp) ? gx_done[nc - 1]
-                                                                           : nullptr);
+                                                                           : nullptr,
+                         gw_rw);
   fail(cudaEventRecord(gw_done, a_gw));
   // copy-out stream: g_x chunk by chunk as they finish, then g_w
   for (int c = 0; c < nc; ++c) {
@@ -1287,23 +1332,29 @@ hlq_status hlq_debug_tc_gemm(int kind, const void* d_a, int64_t lda, const void*
                              int64_t ldb, int64_t M, int64_t N, int64_t K, int bn,
                              int splits, int pair, int32_t* d_acc, void* d_ws,
                              size_t ws_bytes, void* stream) {
-  if (kind != 0 && kind != 1) return HLQ_ERR_INVALID_ARG;
+  if (kind < 0 || kind > 3) return HLQ_ERR_INVALID_ARG;
   if (M < 0 || N < 0 || K < 0 || N % 16 || K % 16 || M % 16) return HLQ_ERR_SHAPE;
   if (bn != 0 && bn != 96 && bn != 128 && bn != 256) return HLQ_ERR_INVALID_ARG;
   if (splits < 0 || splits > 64) return HLQ_ERR_INVALID_ARG;
   if (pair < -1 || pair > 1) return HLQ_ERR_INVALID_ARG;
   if (pair == 1 && bn == 96) return HLQ_ERR_INVALID_ARG;    // pairs: 128 or 256 wide
   if (kind == 0 && splits > 1) return HLQ_ERR_INVALID_ARG;  // E4M3 GEMM runs unsplit
-  const int esz = kind == 1 ? 2 : 1;
-  if (lda < K || ldb < K || (lda * esz) % 16 || (ldb * esz) % 16) return HLQ_ERR_ALIGN;
+  // element bytes of A and B: E4M3 (kind 0), fp16 (kind 1; A of kind 2),
+  // int8 widened in the GEMM (B of kinds 2 and 3, A of kind 3)
+  const int esz_a = (kind == 1 || kind == 2) ? 2 : 1;
+  const int esz_b = kind == 1 ? 2 : 1;
+  if (lda < K || ldb < K || (lda * esz_a) % 16 || (ldb * esz_b) % 16) return HLQ_ERR_ALIGN;
   if (M * N > 0 && (!d_a || !d_b || !d_acc)) return HLQ_ERR_INVALID_ARG;
   if (!aligned16(d_a) || !aligned16(d_b) || !aligned16(d_acc)) return HLQ_ERR_ALIGN;
   if (kind == 0 && 49 * K >= ((int64_t)1 << 24)) return HLQ_ERR_OVERFLOW;
-  if (kind == 1 && K * 127 * 127 >= ((int64_t)1 << 31)) return HLQ_ERR_OVERFLOW;
+  if (kind != 0 && K * 127 * 127 >= ((int64_t)1 << 31)) return HLQ_ERR_OVERFLOW;
   if (M * N == 0) return HLQ_OK;
+  if (kind >= 2 && K == 0) return HLQ_ERR_SHAPE;
   const int sms = device_sm_count();
   if (sms <= 0) return HLQ_ERR_CUDA;
-  GemmPlan plan = plan_gemm_tc(kind, M, N, K, sms, kind == 1 ? 16 : 1);
+  const int gk = kind == 0 ? 0 : 1;  // the GEMM kind
+  const int raw = kind == 2 ? kRawB : (kind == 3 ? (kRawA | kRawB) : 0);
+  GemmPlan plan = plan_gemm_tc(gk, M, N, K, sms, gk == 1 ? 16 : 1);
   if (bn) plan.bn = bn;
   if (splits) plan.splits = splits;
   if (pair >= 0) plan.pair = pair;
@@ -1315,10 +1366,18 @@ hlq_status hlq_debug_tc_gemm(int kind, const void* d_a, int64_t lda, const void*
   if (!status) return HLQ_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   HLQ_LAUNCH(kind == 0 ? "gemm_gx_tc" : "gemm_gw_tc", s,
-             launch_gemm_tc(kind, d_a, lda, d_b, ldb, M, N, K, plan, nullptr, false,
-                            nullptr, nullptr, d_acc, d_ws, status, s));
+             launch_gemm_tc(gk, d_a, lda, d_b, ldb, M, N, K, plan, nullptr, false,
+                            nullptr, nullptr, d_acc, d_ws, status, s, false, raw));
   return HLQ_OK;
 }
+
+hlq_status hlq_set_gw_operands(int mode) {
+  if (mode < HLQ_GW_AUTO || mode > HLQ_GW_INT8_BOTH) return HLQ_ERR_INVALID_ARG;
+  g_gw_operands = mode;
+  return HLQ_OK;
+}
+
+int hlq_get_gw_operands(void) { return g_gw_operands; }
 
 hlq_status hlq_debug_gemm_plan(int64_t T, int64_t Cin, int64_t Cout, int rank, int sms,
                                int* gx_bn, int* gx_splits, int* gw_bn, int* gw_splits,

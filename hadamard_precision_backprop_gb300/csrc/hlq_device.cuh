@@ -6,6 +6,7 @@
 #include <cstdint>
 #include <utility>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 

@@ -22,7 +22,7 @@ __device__ __forceinline__ int decode_code(const void* base, int fmt,
   if (fmt == kFmtE4M3)
     return int_of_e4m3(static_cast<const uint8_t*>(base)[idx]);
   if (fmt == kFmtI8) return static_cast<const int8_t*>(base)[idx];
-  return __bfloat162int_rn(static_cast<const __nv_bfloat16*>(base)[idx]);
+  return __half2int_rn(static_cast<const __half*>(base)[idx]);
 }
 
 // Load 4 consecutive codes (k..k+3, zero past K) as a packed int8x4 word.

@@ -7,7 +7,9 @@
 // sm_103a has no integer MMA kind, so the integer codes ride on float
 // operand types that hold them exactly:
 //   - g_x path: int4 codes in [-7, 7] as E4M3 bytes, tcgen05.mma kind::f8f6f4;
-//   - g_w path: int8 codes in [-127, 127] as bf16, tcgen05.mma kind::f16.
+//   - g_w path: int8 codes in [-127, 127] as fp16, tcgen05.mma kind::f16.
+// A g_w operand may also stay int8 in HBM: its tiles are loaded as bytes
+// and widened to fp16 in shared memory by the epilogue warps (kCvt).
 // Products are integers and the fp32 TMEM accumulator holds every partial
 // sum exactly while it stays below 2^24; the K loop is therefore cut into
 // chunks of at most `chunk_kb` k-blocks whose accumulators are drained into
@@ -30,7 +32,8 @@
 //   warp 1      TMEM allocator and MMA issuer (one lane), 4 MMAs per k-block
 //               into one of two TMEM accumulators (double buffer per chunk);
 //   warps 2..   epilogue: drain TMEM (tcgen05.ld) into int32 registers per
-//               chunk, then dequantize and store fp32 rows.
+//               chunk, then dequantize and store fp32 rows; with int8
+//               operands they first widen each stage's tiles.
 // Every mbarrier wait is bounded (HLQ_DEV_TIMEOUT, then the CTA winds down).
 #include <cstdint>
 #include <cstring>
@@ -67,10 +70,10 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t addr) {
 }
 
 // Instruction descriptor: fp32 accumulator, A/B K-major, shape M x N.
-// kKind 0: kind::f8f6f4 with E4M3 operands; kKind 1: kind::f16 with bf16.
+// Operand formats 0: E4M3 under kind::f8f6f4 (kKind 0), fp16 under
+// kind::f16 (kKind 1).
 __host__ __device__ constexpr uint32_t make_idesc(int kKind, int M, int N) {
-  return (1u << 4) | ((kKind == 1 ? 1u : 0u) << 7) | ((kKind == 1 ? 1u : 0u) << 10) |
-         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+  return (void)kKind, (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 template <int kKind, bool kPair = false>
@@ -148,6 +151,19 @@ __device__ __forceinline__ void tmem_ld_x32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// 32 TMEM lanes x 16 consecutive 32-bit columns (the drains of the GEMMs
+// that widen int8 operands, which hold more registers between drains).
+__device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+        "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),
+        "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
 // The mainloop is bound by the latency of a TMA round trip (L2 -> shared
 // memory, MMA, release), so the ring holds as many stages as shared memory
 // allows: 7 of 28 KB for 96-wide tiles, 6 of 32 KB for 128-wide ones, 4 of
@@ -155,7 +171,10 @@ __device__ __forceinline__ void tmem_ld_x32(uint32_t taddr, uint32_t (&r)[32]) {
 // fewer waves than 128-wide ones.
 // CTA pairs: 6 stages of 32 KB (16 KB of A, 16 KB of the B half) for 256-wide
 // tiles, 8 of 24 KB for 128-wide ones.
-template <int BN, bool kPair = false>
+// kCvt (kind 1): kRawB / kRawA mark operands that arrive as int8 codes; the
+// TMA puts them, unswizzled, in the upper half of their fp16 slot and the
+// epilogue warps widen them in place (same stage sizes).
+template <int BN, bool kPair = false, int kCvt = 0>
 struct TcCfg {
   static_assert(BN == 96 || BN == 128 || BN == 256, "tile widths 96, 128, 256");
   static_assert(!kPair || BN != 96, "CTA pairs take 128- or 256-wide tiles");
@@ -170,6 +189,15 @@ struct TcCfg {
   static constexpr uint32_t kABytes = kBM * kRowBytes;
   static constexpr uint32_t kBBytes = kBRows * kRowBytes;
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;
+  // bytes the TMA delivers per stage (int8 operands: half their fp16 slot)
+  static constexpr uint32_t kLoadBytes =
+      ((kCvt & kRawA) ? kABytes / 2 : kABytes) + ((kCvt & kRawB) ? kBBytes / 2 : kBBytes);
+  // 16-code pieces of the int8 tiles per converting (epilogue) thread
+  static constexpr int kConvThreads = 32 * kEpiWarps;
+  static constexpr int kAPieces = (kCvt & kRawA) ? kBM * 4 / kConvThreads : 0;
+  static constexpr int kBPieces = (kCvt & kRawB) ? kBRows * 4 / kConvThreads : 0;
+  static_assert((kBRows * 4) % kConvThreads == 0 && (kBM * 4) % kConvThreads == 0,
+                "whole pieces per converting thread");
   // two accumulators, each starting on a 128-column boundary
   static constexpr uint32_t kAccStride = BN <= 128 ? 128 : 256;
   static constexpr uint32_t kTmemCols = 2 * kAccStride;
@@ -178,7 +206,47 @@ struct TcCfg {
   static constexpr size_t kSmem =
       1024 + (size_t)kStages * kStageBytes + (size_t)kEpiWarps * kStageOutBytes + 256;
   static_assert(kSmem <= 232448, "227 KB of shared memory per CTA");
+  static_assert(3 * kStages * 8 + 4 * 8 + 8 <= 256, "barriers fit their 256 bytes");
 };
+
+// Barrier over the `n` epilogue threads (named barrier 1) that also returns
+// whether `pred` held in every one of them.
+__device__ __forceinline__ bool epi_barrier_all(bool pred, int n) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.and.pred p, 1, %2, q;\n\tselp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(r)
+      : "r"(pred ? 1u : 0u), "r"(n)
+      : "memory");
+  return r != 0;
+}
+
+// Two int8 codes of a word (flipped to c + 128 by the caller) as fp16x2:
+// the permute builds the fp16 bit patterns 0x64uu = 1024 + c + 128, exact
+// integers, and one fp16x2 subtraction of 1152 (0x6480) leaves c exactly.
+__device__ __forceinline__ uint32_t f16x2_of_biased_i8(uint32_t biased, uint32_t sel) {
+  uint32_t h, r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(h) : "r"(biased), "r"(0x64646464u), "r"(sel));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(0x64806480u));
+  return r;
+}
+
+// Piece q of an int8 tile (16 codes: row q / 4, codes 16 (q % 4) ..) to the
+// two 16-byte chunks of its fp16 row in the 128B-swizzled tile layout the
+// MMA descriptors expect (chunk c of row r at c ^ (r % 8)).
+__device__ __forceinline__ void put_widened_piece(uint8_t* slot, int q, uint4 v) {
+  const uint32_t a = v.x ^ 0x80808080u, b = v.y ^ 0x80808080u;
+  const uint32_t c = v.z ^ 0x80808080u, d = v.w ^ 0x80808080u;
+  const uint4 lo = make_uint4(f16x2_of_biased_i8(a, 0x4140u), f16x2_of_biased_i8(a, 0x4342u),
+                              f16x2_of_biased_i8(b, 0x4140u), f16x2_of_biased_i8(b, 0x4342u));
+  const uint4 hi = make_uint4(f16x2_of_biased_i8(c, 0x4140u), f16x2_of_biased_i8(c, 0x4342u),
+                              f16x2_of_biased_i8(d, 0x4140u), f16x2_of_biased_i8(d, 0x4342u));
+  const int row = q >> 2, c0 = (q & 3) * 2;
+  uint8_t* rp = slot + row * kRowBytes;
+  *reinterpret_cast<uint4*>(rp + ((c0 ^ (row & 7)) << 4)) = lo;
+  *reinterpret_cast<uint4*>(rp + (((c0 + 1) ^ (row & 7)) << 4)) = hi;
+}
 
 // Persistent: CTA b (CTA pair b with kPair) processes work units b, b + G,
 // ... (G = the number of CTAs, or of pairs) where a unit is (output tile,
@@ -191,8 +259,14 @@ struct TcCfg {
 // CTA 0's barrier), and the accumulator-empty barrier counts the epilogue
 // warps of both CTAs (CTA 1's arrive remotely).  The MMA commits arrive on
 // the stage-empty and accumulator-full barriers of both CTAs at once.
-template <int kKind, int BN, bool kPair>
-__global__ void __launch_bounds__(TcCfg<BN, kPair>::kThreads, 1) gemm_tc_kernel(
+//
+// With kCvt, each CTA's loads signal its own full barrier; its epilogue
+// warps wait there, widen the int8 codes of the stage, and arrive on the
+// stage's converted barrier (CTA 0's, for a pair), which gates the MMA.  The
+// same warps drain the accumulators, each chunk's drain placed after the
+// first few conversions of the next chunk.
+template <int kKind, int BN, bool kPair, int kCvt>
+__global__ void __launch_bounds__(TcCfg<BN, kPair, kCvt>::kThreads, 1) gemm_tc_kernel(
     const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
     const __grid_constant__ CUtensorMap tmOut, const __grid_constant__ CUtensorMap tmAcc,
     const __grid_constant__ CUtensorMap tmSplit,
@@ -202,7 +276,8 @@ __global__ void __launch_bounds__(TcCfg<BN, kPair>::kThreads, 1) gemm_tc_kernel(
     int32_t* __restrict__ acc_out,
     int32_t* __restrict__ split_acc, unsigned int* __restrict__ slab_count,
     unsigned int* __restrict__ status) {
-  using C = TcCfg<BN, kPair>;
+  using C = TcCfg<BN, kPair, kCvt>;
+  static_assert(kCvt == 0 || kKind == 1, "int8 operands feed the fp16 GEMM");
   constexpr int kStages = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -210,7 +285,8 @@ __global__ void __launch_bounds__(TcCfg<BN, kPair>::kThreads, 1) gemm_tc_kernel(
   uint8_t* stage_out = smem + kStages * C::kStageBytes;  // [kEpiWarps][4 KB]
   uint64_t* full = reinterpret_cast<uint64_t*>(stage_out + C::kEpiWarps * C::kStageOutBytes);
   uint64_t* empty = full + kStages;
-  uint64_t* tfull = empty + kStages;  // [2]
+  uint64_t* conv = empty + kStages;   // [kStages], kCvt only
+  uint64_t* tfull = conv + kStages;   // [2]
   uint64_t* tempty = tfull + 2;       // [2]
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(tempty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
@@ -226,6 +302,7 @@ __global__ void __launch_bounds__(TcCfg<BN, kPair>::kThreads, 1) gemm_tc_kernel(
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
+      mbar_init(&conv[s], kPair ? 2 * C::kEpiWarps : C::kEpiWarps);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
@@ -257,6 +334,7 @@ __global__ void __launch_bounds__(TcCfg<BN, kPair>::kThreads, 1) gemm_tc_kernel(
   const uint32_t tmem_base = *tmem_holder;
   // barriers of CTA 0 that both CTAs of a pair signal
   const uint32_t full_lead = kPair ? cluster_map(saddr(full), 0) : 0u;
+  const uint32_t conv_lead = kPair ? cluster_map(saddr(conv), 0) : 0u;
   const uint32_t tempty_lead = kPair ? cluster_map(saddr(tempty), 0) : 0u;
   // the prologue above overlaps the previous kernel; operands, scales and
   // outputs are touched only after it has completed
@@ -300,7 +378,15 @@ __global__ void __launch_bounds__(TcCfg<BN, kPair>::kThreads, 1) gemm_tc_kernel(
           if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, status)) break;
           uint8_t* a = smem + s * C::kStageBytes;
           const int kx = (kb0 + j) * elems;
-          if (kPair) {
+          if (kCvt != 0) {
+            // this CTA's own barrier; int8 tiles land in the upper half of
+            // their slot, where the epilogue warps widen them
+            mbar_expect_tx(&full[s], C::kLoadBytes);
+            tma_load_2d(a + ((kCvt & kRawA) ? C::kABytes / 2 : 0u), &tmA, &full[s], kx,
+                        m0 + (int)rank * kBM);
+            tma_load_2d(a + C::kABytes + ((kCvt & kRawB) ? C::kBBytes / 2 : 0u), &tmB,
+                        &full[s], kx, n0 + (int)rank * C::kBRows);
+          } else if (kPair) {
             // CTA 0 expects both halves; each CTA's copies signal CTA 0
             if (rank == 0) mbar_expect_tx(&full[s], 2 * C::kStageBytes);
             const uint32_t bar = full_lead + (uint32_t)(s * sizeof(uint64_t));
@@ -313,7 +399,7 @@ __global__ void __launch_bounds__(TcCfg<BN, kPair>::kThreads, 1) gemm_tc_kernel(
           }
         }
       }
-      if (*abort_flag && !kPair) {  // let the copies already issued land before exit
+      if (*abort_flag && (!kPair || kCvt != 0)) {  // let the copies already issued land
         for (int k = max(0, i - kStages); k < i; ++k) {
           const unsigned long long t0 = now_ns();
           while (!mbar_test(&full[k % kStages], (uint32_t)(k / kStages) & 1u) &&
@@ -324,7 +410,7 @@ __global__ void __launch_bounds__(TcCfg<BN, kPair>::kThreads, 1) gemm_tc_kernel(
     }
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) {  // the MMA issuer (CTA 0 of a pair)
-      constexpr uint32_t idesc = make_idesc(kKind, C::kTileM, BN);
+      const uint32_t idesc = make_idesc(kKind, C::kTileM, BN);
       int i = 0, cc = 0;  // k-blocks and accumulation chunks consumed so far
       bool ok = true;
       for (int u = first_unit; u < num_units && ok; u += unit_step) {
@@ -345,7 +431,11 @@ __global__ void __launch_bounds__(TcCfg<BN, kPair>::kThreads, 1) gemm_tc_kernel(
           for (int jj = 0; j < j_end; ++j, ++jj, ++i) {
             const int s = i % kStages;
             const uint32_t ph = (uint32_t)(i / kStages) & 1u;
-            if (!mbar_wait(&full[s], ph, abort_flag, status)) {
+            // loaded (and, for int8 operands, widened by both CTAs)
+            const bool ready = kCvt != 0
+                                   ? mbar_wait(&conv[s], ph, abort_flag, status, kPair)
+                                   : mbar_wait(&full[s], ph, abort_flag, status);
+            if (!ready) {
               ok = false;
               break;
             }
@@ -414,13 +504,13 @@ __global__ void __launch_bounds__(TcCfg<BN, kPair>::kThreads, 1) gemm_tc_kernel(
     };
     int cc = 0;
     bool ok = true;
-    for (int u = first_unit; u < num_units && ok; u += unit_step) {
-      int m0, n0, kb0, nkb;
-      unit_coords(u, m0, n0, kb0, nkb);
-      const int m = m0 + row;
-      const int nb = n0 + colgrp * C::kColsPerThread;
-      const int y = m0 + (int)rank * kBM + quarter * 32;
-      if constexpr (kKind == 0) {
+    if constexpr (kKind == 0) {
+      for (int u = first_unit; u < num_units && ok; u += unit_step) {
+        int m0, n0, kb0, nkb;
+        unit_coords(u, m0, n0, kb0, nkb);
+        const int m = m0 + row;
+        const int nb = n0 + colgrp * C::kColsPerThread;
+        const int y = m0 + (int)rank * kBM + quarter * 32;
         // one accumulation chunk, never split: stream each 32-column TMEM
         // slice straight into a store box
         const int buf = cc & 1;
@@ -453,118 +543,235 @@ __global__ void __launch_bounds__(TcCfg<BN, kPair>::kThreads, 1) gemm_tc_kernel(
             store_box(&tmOut, x, y, r);
           }
         }
-        continue;
       }
-      const int nch = (nkb + chunk_kb - 1) / chunk_kb;
+    } else {
       int32_t acc[C::kColsPerThread];
 #pragma unroll
       for (int q = 0; q < C::kColsPerThread; ++q) acc[q] = 0;
-      for (int c = 0; c < nch; ++c, ++cc) {
+      // add the next accumulation chunk (in TMEM buffer cc & 1) into acc
+      auto drain = [&]() -> bool {
         const int buf = cc & 1;
         const uint32_t use = (uint32_t)(cc >> 1);
-        ok = mbar_wait(&tfull[buf], use & 1u, abort_flag, status);
-        ok = __all_sync(0xffffffffu, ok);  // also reconverges the warp
-        if (!ok) break;
+        ++cc;
+        bool w = mbar_wait(&tfull[buf], use & 1u, abort_flag, status);
+        w = __all_sync(0xffffffffu, w);  // also reconverges the warp
+        if (!w) return false;
         tc_fence_after();
         const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) +
                                (uint32_t)(buf * C::kAccStride + colgrp * C::kColsPerThread);
+        if constexpr (kCvt == 0) {
 #pragma unroll
-        for (int jc = 0; jc < C::kColsPerThread / 32; ++jc) {
-          uint32_t r[32];
-          tmem_ld_x32(taddr + 32 * jc, r);
+          for (int jc = 0; jc < C::kColsPerThread / 32; ++jc) {
+            uint32_t r[32];
+            tmem_ld_x32(taddr + 32 * jc, r);
 #pragma unroll
-          for (int q = 0; q < 32; ++q)
-            acc[32 * jc + q] += __float2int_rn(__uint_as_float(r[q]));
+            for (int q = 0; q < 32; ++q)
+              acc[32 * jc + q] += __float2int_rn(__uint_as_float(r[q]));
+          }
+        } else {
+#pragma unroll
+          for (int jc = 0; jc < C::kColsPerThread / 16; ++jc) {
+            uint32_t r[16];
+            tmem_ld_x16(taddr + 16 * jc, r);
+#pragma unroll
+            for (int q = 0; q < 16; ++q)
+              acc[16 * jc + q] += __float2int_rn(__uint_as_float(r[q]));
+          }
         }
         release_acc(buf);
-      }
-      if (!ok) break;
-      if (splits == 1) {
-        const float scale = dequant_scale(m);
+        return true;
+      };
+      // unit u's sums are complete in acc: store them dequantized, or add
+      // them into the split workspace (the last split of a slab stores)
+      auto finish_unit = [&](int u) {
+        int m0, n0, kb0, nkb;
+        unit_coords(u, m0, n0, kb0, nkb);
+        const int m = m0 + row;
+        const int nb = n0 + colgrp * C::kColsPerThread;
+        const int y = m0 + (int)rank * kBM + quarter * 32;
+        if (splits == 1) {
+          const float scale = dequant_scale(m);
+#pragma unroll
+          for (int jc = 0; jc < C::kColsPerThread / 32; ++jc) {
+            const int x = nb + 32 * jc;
+            if (x >= N) break;
+            uint32_t v[32];
+            if (acc_out) {
+#pragma unroll
+              for (int q = 0; q < 32; ++q) v[q] = (uint32_t)acc[32 * jc + q];
+              store_box(&tmAcc, x, y, v);
+            }
+            if (out) {
+              if (per_col_b) {
+                const float ra = row_scale_a(m);
+#pragma unroll
+                for (int q = 0; q < 32; ++q) v[q] = col_scaled(acc[32 * jc + q], ra, x + q);
+              } else {
+#pragma unroll
+                for (int q = 0; q < 32; ++q)
+                  v[q] = __float_as_uint((float)acc[32 * jc + q] * scale);
+              }
+              store_box(&tmOut, x, y, v);
+            }
+          }
+          return;
+        }
+        // split unit: add the exact partial into split_acc with TMA reduce-add
+        // boxes (32 rows x 32 columns, coalesced in L2); the warp that
+        // completes a slab (its 32 rows x kColsPerThread columns) last reads
+        // the sum back and stores it dequantized
 #pragma unroll
         for (int jc = 0; jc < C::kColsPerThread / 32; ++jc) {
           const int x = nb + 32 * jc;
           if (x >= N) break;
           uint32_t v[32];
-          if (acc_out) {
 #pragma unroll
-            for (int q = 0; q < 32; ++q) v[q] = (uint32_t)acc[32 * jc + q];
-            store_box(&tmAcc, x, y, v);
-          }
-          if (out) {
-            if (per_col_b) {
-              const float ra = row_scale_a(m);
+          for (int q = 0; q < 32; ++q) v[q] = (uint32_t)acc[32 * jc + q];
+          store_box(&tmSplit, x, y, v, true);
+        }
+        unsigned int last = 0;
+        if (lane == 0) {
+          tma_store_wait_all();  // the reductions are performed
+          asm volatile("fence.proxy.async.global;" ::: "memory");
+          __threadfence();
+          // slab counters per (128-row half tile, epilogue warp)
+          int tm, tn, kb0u, nkbu;
+          unit_tile(u, tm, tn, kb0u, nkbu);
+          const int half = tm * (C::kTileM / kBM) + (int)rank;
+          const int slab = (half * tiles_n + tn) * C::kEpiWarps + ew;
+          last = atomicAdd(&slab_count[slab], 1u) == (unsigned int)(splits - 1);
+          if (last) __threadfence();
+        }
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (last) {
+          const float scale = dequant_scale(m);
+          const float ra = row_scale_a(m);
 #pragma unroll
-              for (int q = 0; q < 32; ++q) v[q] = col_scaled(acc[32 * jc + q], ra, x + q);
-            } else {
+          for (int jc = 0; jc < C::kColsPerThread / 32; ++jc) {
+            const int x = nb + 32 * jc;
+            if (x >= N) break;
+            int32_t sum[32];
+            const int32_t* rowp = split_acc + (size_t)m * N + x;
 #pragma unroll
-              for (int q = 0; q < 32; ++q)
-                v[q] = __float_as_uint((float)acc[32 * jc + q] * scale);
+            for (int q = 0; q < 32; q += 4) {
+              int4 w4 = make_int4(0, 0, 0, 0);
+              if (m < M && x + q < N) w4 = __ldcg(reinterpret_cast<const int4*>(rowp + q));
+              sum[q] = w4.x; sum[q + 1] = w4.y; sum[q + 2] = w4.z; sum[q + 3] = w4.w;
             }
-            store_box(&tmOut, x, y, v);
+            uint32_t v[32];
+            if (acc_out) {
+#pragma unroll
+              for (int q = 0; q < 32; ++q) v[q] = (uint32_t)sum[q];
+              store_box(&tmAcc, x, y, v);
+            }
+            if (out) {
+              if (per_col_b) {
+#pragma unroll
+                for (int q = 0; q < 32; ++q) v[q] = col_scaled(sum[q], ra, x + q);
+              } else {
+#pragma unroll
+                for (int q = 0; q < 32; ++q) v[q] = __float_as_uint((float)sum[q] * scale);
+              }
+              store_box(&tmOut, x, y, v);
+            }
           }
         }
-        continue;
-      }
-      // split unit: add the exact partial into split_acc with TMA reduce-add
-      // boxes (32 rows x 32 columns, coalesced in L2); the warp that
-      // completes a slab (its 32 rows x kColsPerThread columns) last reads
-      // the sum back and stores it dequantized
+      };
+      auto zero_acc = [&]() {
 #pragma unroll
-      for (int jc = 0; jc < C::kColsPerThread / 32; ++jc) {
-        const int x = nb + 32 * jc;
-        if (x >= N) break;
-        uint32_t v[32];
-#pragma unroll
-        for (int q = 0; q < 32; ++q) v[q] = (uint32_t)acc[32 * jc + q];
-        store_box(&tmSplit, x, y, v, true);
-      }
-      unsigned int last = 0;
-      if (lane == 0) {
-        tma_store_wait_all();  // the reductions are performed
-        asm volatile("fence.proxy.async.global;" ::: "memory");
-        __threadfence();
-        // slab counters per (128-row half tile, epilogue warp)
-        int tm, tn, kb0u, nkbu;
-        unit_tile(u, tm, tn, kb0u, nkbu);
-        const int half = tm * (C::kTileM / kBM) + (int)rank;
-        const int slab = (half * tiles_n + tn) * C::kEpiWarps + ew;
-        last = atomicAdd(&slab_count[slab], 1u) == (unsigned int)(splits - 1);
-        if (last) __threadfence();
-      }
-      last = __shfl_sync(0xffffffffu, last, 0);
-      if (last) {
-        const float scale = dequant_scale(m);
-        const float ra = row_scale_a(m);
-#pragma unroll
-        for (int jc = 0; jc < C::kColsPerThread / 32; ++jc) {
-          const int x = nb + 32 * jc;
-          if (x >= N) break;
-          int32_t sum[32];
-          const int32_t* rowp = split_acc + (size_t)m * N + x;
-#pragma unroll
-          for (int q = 0; q < 32; q += 4) {
-            int4 w4 = make_int4(0, 0, 0, 0);
-            if (m < M && x + q < N) w4 = __ldcg(reinterpret_cast<const int4*>(rowp + q));
-            sum[q] = w4.x; sum[q + 1] = w4.y; sum[q + 2] = w4.z; sum[q + 3] = w4.w;
-          }
-          uint32_t v[32];
-          if (acc_out) {
-#pragma unroll
-            for (int q = 0; q < 32; ++q) v[q] = (uint32_t)sum[q];
-            store_box(&tmAcc, x, y, v);
-          }
-          if (out) {
-            if (per_col_b) {
-#pragma unroll
-              for (int q = 0; q < 32; ++q) v[q] = col_scaled(sum[q], ra, x + q);
-            } else {
-#pragma unroll
-              for (int q = 0; q < 32; ++q) v[q] = __float_as_uint((float)sum[q] * scale);
-            }
-            store_box(&tmOut, x, y, v);
-          }
+        for (int q = 0; q < C::kColsPerThread; ++q) acc[q] = 0;
+      };
+      if constexpr (kCvt == 0) {
+        for (int u = first_unit; u < num_units && ok; u += unit_step) {
+          int m0, n0, kb0, nkb;
+          unit_coords(u, m0, n0, kb0, nkb);
+          const int nch = (nkb + chunk_kb - 1) / chunk_kb;
+          zero_acc();
+          for (int c = 0; c < nch && ok; ++c) ok = drain();
+          if (!ok) break;
+          finish_unit(u);
         }
+      } else {
+        // widen stage i's int8 tiles in place; false (in every epilogue
+        // thread at once) when this or another thread's wait gave up
+        const int et = (int)threadIdx.x - 64;  // 0 .. kConvThreads - 1
+        int i = 0;
+        auto convert = [&]() -> bool {
+          const int s = i % kStages;
+          const uint32_t ph = (uint32_t)(i / kStages) & 1u;
+          ++i;
+          const bool w = mbar_wait(&full[s], ph, abort_flag, status);
+          uint8_t* a_slot = smem + s * C::kStageBytes;
+          uint8_t* b_slot = a_slot + C::kABytes;
+          uint4 ra[C::kAPieces > 0 ? C::kAPieces : 1];
+          uint4 rb[C::kBPieces > 0 ? C::kBPieces : 1];
+#pragma unroll
+          for (int p = 0; p < C::kAPieces; ++p)
+            ra[p] = *reinterpret_cast<const uint4*>(a_slot + C::kABytes / 2 +
+                                                    16 * (et + p * C::kConvThreads));
+#pragma unroll
+          for (int p = 0; p < C::kBPieces; ++p)
+            rb[p] = *reinterpret_cast<const uint4*>(b_slot + C::kBBytes / 2 +
+                                                    16 * (et + p * C::kConvThreads));
+          // every int8 piece is in registers before any fp16 row lands on it
+          __syncwarp();
+          if (!epi_barrier_all(ok && w, C::kConvThreads)) return false;
+#pragma unroll
+          for (int p = 0; p < C::kAPieces; ++p)
+            put_widened_piece(a_slot, et + p * C::kConvThreads, ra[p]);
+#pragma unroll
+          for (int p = 0; p < C::kBPieces; ++p)
+            put_widened_piece(b_slot, et + p * C::kConvThreads, rb[p]);
+          fence_proxy_async_smem();  // generic writes -> the MMA's reads
+          __syncwarp();
+          if (lane == 0) {
+            if (kPair && rank != 0)
+              mbar_arrive_cluster(conv_lead + (uint32_t)(s * sizeof(uint64_t)));
+            else
+              mbar_arrive(&conv[s]);
+          }
+          return true;
+        };
+        // Chunk c - 1 of a unit is drained once the first kLag stages of
+        // chunk c are converted (the MMA has finished it by then or soon
+        // after, and has converted stages to work on while the drain runs);
+        // a unit's last chunk is drained after the first kLag stages of the
+        // next unit are converted.  Every unit has k-blocks (the launcher
+        // drops empty splits).
+        constexpr int kLag = kStages / 2;
+        bool live = true;
+        int ahead = 0;  // k-blocks of this unit converted during the last one
+        for (int u = first_unit; u < num_units && live; u += unit_step) {
+          int m0, n0, kb0, nkb;
+          unit_coords(u, m0, n0, kb0, nkb);
+          const int nch = (nkb + chunk_kb - 1) / chunk_kb;
+          zero_acc();
+          for (int c = 0, j = 0; c < nch && live; ++c) {
+            const int len = min(nkb, j + chunk_kb) - j;
+            for (int jj = 0; jj < len; ++jj, ++j) {
+              if (j >= ahead && !convert()) {
+                live = false;
+                break;
+              }
+              if (c > 0 && jj + 1 == min(len, kLag)) ok = drain() && ok;
+            }
+          }
+          if (!live) break;
+          ahead = 0;
+          if (u + unit_step < num_units) {
+            int m1, n1, kb1, nkb1;
+            unit_coords(u + unit_step, m1, n1, kb1, nkb1);
+            for (; ahead < min(nkb1, kLag); ++ahead)
+              if (!convert()) {
+                live = false;
+                break;
+              }
+          }
+          if (!live) break;
+          ok = drain() && ok;
+          if (ok) finish_unit(u);
+        }
+        ok = ok && live;
       }
     }
     if (lane == 0) tma_store_wait_all();  // boxes written before the CTA exits
@@ -610,17 +817,33 @@ bool get_encode() {
 
 // 2-D K-major operand [rows, K] with row stride ld (elements), boxes of
 // 128 bytes x box_rows, 128-byte swizzle, zero fill outside the tensor.
-bool make_map(CUtensorMap* map, const void* ptr, bool bf16, int64_t rows, int64_t K,
+bool make_map(CUtensorMap* map, const void* ptr, bool f16, int64_t rows, int64_t K,
               int64_t ld, int box_rows) {
-  const int esz = bf16 ? 2 : 1;
+  const int esz = f16 ? 2 : 1;
   cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)(ld * esz)};
   cuuint32_t box[2] = {(cuuint32_t)(kRowBytes / esz), (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = g_encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8,
+  CUresult r = g_encode(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8,
                         2, const_cast<void*>(ptr), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// int8 operand [rows, K] (row stride ld bytes) for widening in shared
+// memory: boxes of 64 codes x box_rows, unswizzled (rows of 64 bytes, read
+// back by the converting threads in 16-byte pieces), zero fill outside.
+bool make_i8_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t K, int64_t ld,
+                 int box_rows) {
+  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)ld};
+  cuuint32_t box[2] = {(cuuint32_t)(kRowBytes / 2), (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -643,7 +866,7 @@ bool make_out_map(CUtensorMap* map, const void* ptr, bool is_int, int64_t rows,
 // Persistent grid of one CTA per SM, or of as many CTA pairs as fit at once
 // (clusters of two need both SMs of a pair free; the count comes from the
 // occupancy query for this kernel, cached per device).
-template <int kKind, int BN, bool kPair>
+template <int kKind, int BN, bool kPair, int kCvt = 0>
 cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& mo,
                       const CUtensorMap& macc, const CUtensorMap& msplit, int64_t M, int64_t N,
                       int num_kb, int chunk_kb,
@@ -651,8 +874,8 @@ cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, const CUtensor
                       const float* sb, bool per_col_b, float* out, int32_t* acc_out,
                       int32_t* split_acc, unsigned int* slab_count, unsigned int* status,
                       cudaStream_t st) {
-  using C = TcCfg<BN, kPair>;
-  auto kernel = gemm_tc_kernel<kKind, BN, kPair>;
+  using C = TcCfg<BN, kPair, kCvt>;
+  auto kernel = gemm_tc_kernel<kKind, BN, kPair, kCvt>;
   static bool attr_set[64] = {};
   static int max_pairs[64] = {};
   int dev = 0;
@@ -666,6 +889,8 @@ cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, const CUtensor
     attr_set[dev] = true;
   }
   const int kb_per_split = (num_kb + splits - 1) / splits;
+  // no empty splits: the last one holds at least one k-block
+  if (num_kb > 0) splits = (num_kb + kb_per_split - 1) / kb_per_split;
   const int tiles_n = (int)((N + BN - 1) / BN);
   const int tiles_m = (int)((M + C::kTileM - 1) / C::kTileM);
   const int64_t units = (int64_t)tiles_m * tiles_n * splits;
@@ -819,17 +1044,28 @@ cudaError_t launch_gemm_tc(int kind, const void* A, int64_t lda, const void* B,
                            const GemmPlan& plan, const float* sa, bool per_row_a,
                            const float* sb, float* out, int32_t* acc_out,
                            void* split_ws, unsigned int* status, cudaStream_t st,
-                           bool per_col_b) {
+                           bool per_col_b, int raw) {
   if (M == 0 || N == 0) return cudaSuccess;
   if (!get_encode()) return cudaErrorNotSupported;
-  const bool bf16 = kind == 1;
+  const bool f16 = kind == 1;
   if ((plan.bn != 96 && plan.bn != 128 && plan.bn != 256) ||
       (plan.splits > 1 && kind == 0) || (per_col_b && kind == 0) ||
-      (plan.pair && plan.bn == 96))
+      (plan.pair && plan.bn == 96) || (raw & ~(kRawA | kRawB)) || (raw && kind != 1) ||
+      (raw && K <= 0))
     return cudaErrorInvalidValue;
+  // int8 operands: TMA rows of 16-byte multiples from a 16-byte aligned base
+  auto i8_ok = [](const void* p, int64_t ld) {
+    return (reinterpret_cast<uintptr_t>(p) & 15u) == 0 && ld % 16 == 0;
+  };
+  if (((raw & kRawA) && !i8_ok(A, lda)) || ((raw & kRawB) && !i8_ok(B, ldb)))
+    return cudaErrorInvalidValue;
+  const int b_rows = plan.pair ? plan.bn / 2 : plan.bn;
   CUtensorMap ma, mb, mo, macc, msplit;
-  if (!make_map(&ma, A, bf16, M, K, lda, kBM)) return cudaErrorInvalidValue;
-  if (!make_map(&mb, B, bf16, N, K, ldb, plan.pair ? plan.bn / 2 : plan.bn))
+  if (!((raw & kRawA) ? make_i8_map(&ma, A, M, K, lda, kBM)
+                      : make_map(&ma, A, f16, M, K, lda, kBM)))
+    return cudaErrorInvalidValue;
+  if (!((raw & kRawB) ? make_i8_map(&mb, B, N, K, ldb, b_rows)
+                      : make_map(&mb, B, f16, N, K, ldb, b_rows)))
     return cudaErrorInvalidValue;
   memset(&mo, 0, sizeof(mo));
   memset(&macc, 0, sizeof(macc));
@@ -853,17 +1089,20 @@ cudaError_t launch_gemm_tc(int kind, const void* A, int64_t lda, const void* B,
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
       sms <= 0)
     return cudaErrorInvalidDevice;
-#define TC(KIND, BN, PAIR)                                                                 \
-  launch_tc<KIND, BN, PAIR>(ma, mb, mo, macc, msplit, M, N, plan.num_kb, plan.chunk_kb,      \
-                            plan.splits, sms, sa, per_row_a, sb, per_col_b, out, acc_out,    \
-                            split_acc, slab_count, status, st)
-  if (plan.pair) {
-    if (kind == 0) return plan.bn == 256 ? TC(0, 256, true) : TC(0, 128, true);
-    return plan.bn == 256 ? TC(1, 256, true) : TC(1, 128, true);
-  }
-  if (kind == 0)
-    return plan.bn == 256 ? TC(0, 256, false) : (plan.bn == 96 ? TC(0, 96, false) : TC(0, 128, false));
-  return plan.bn == 256 ? TC(1, 256, false) : (plan.bn == 96 ? TC(1, 96, false) : TC(1, 128, false));
+#define TC(KIND, BN, PAIR, CVT)                                                             \
+  launch_tc<KIND, BN, PAIR, CVT>(ma, mb, mo, macc, msplit, M, N, plan.num_kb, plan.chunk_kb,   \
+                                 plan.splits, sms, sa, per_row_a, sb, per_col_b, out,         \
+                                 acc_out, split_acc, slab_count, status, st)
+#define TC_BN(KIND, PAIR, CVT)                                                    \
+  (plan.bn == 256 ? TC(KIND, 256, PAIR, CVT)                                      \
+                  : (PAIR || plan.bn == 128) ? TC(KIND, 128, PAIR, CVT) : TC(KIND, 96, false, CVT))
+  if (kind == 0) return plan.pair ? TC_BN(0, true, 0) : TC_BN(0, false, 0);
+  if (raw == kRawB) return plan.pair ? TC_BN(1, true, kRawB) : TC_BN(1, false, kRawB);
+  if (raw == (kRawA | kRawB))
+    return plan.pair ? TC_BN(1, true, kRawA | kRawB) : TC_BN(1, false, kRawA | kRawB);
+  if (raw != 0) return cudaErrorInvalidValue;  // int8 A alone is not built
+  return plan.pair ? TC_BN(1, true, 0) : TC_BN(1, false, 0);
+#undef TC_BN
 #undef TC
 }
 

@@ -39,9 +39,9 @@ cudaError_t launch_hq_cols(const void* src, bool bf16, int64_t rows,
                            uint32_t stream_id, unsigned int* status,
                            cudaStream_t st);
 
-// Output formats of launch_hla: int8 codes, their bf16 values, or int4
+// Output formats of launch_hla: int8 codes, their fp16 values, or int4
 // codes packed two per byte (even ranks only).
-constexpr int kHlaOutI8 = 0, kHlaOutBf16 = 1, kHlaOutI4 = 2;
+constexpr int kHlaOutI8 = 0, kHlaOutF16 = 1, kHlaOutI4 = 2;
 
 // HLA of src [T, C] along tokens -> codes [C, T*rank/16] in `out_fmt`,
 // per-tensor scale RN(amax/qmax) from *amax_slot (qmax 7 for int4, else 127).
@@ -56,7 +56,7 @@ cudaError_t launch_hla(const void* src, bool bf16, int64_t T, int64_t C,
 
 // HLA along the rows of src [rows, cols]: per 16-block of a row the rank
 // lowest-sequency coefficients, per-tensor amax pass (amax_only) or int8 RNE
-// codes with s = RN(amax/127) stored as bf16 [rows, out_ld] (column
+// codes with s = RN(amax/127) stored as fp16 [rows, out_ld] (column
 // rank*b + k), scale[0] = s.
 cudaError_t launch_hla_rows(const void* src, bool bf16, int64_t rows, int64_t cols,
                             int rank, bool amax_only, unsigned int* amax_slot, void* out,
@@ -66,7 +66,7 @@ cudaError_t launch_hla_rows(const void* src, bool bf16, int64_t rows, int64_t co
 // Fused reader of g_y [T, C] for both paths, one pass per call: amax_only
 // gives the HQ maxima (per row into hq_amax[T] when per_token, else one slot)
 // and the HLA maximum (hla_amax); otherwise the HQ E4M3 codes qy [T, C] with
-// scales sgy ([T] or [1]) and the HLA int8 codes as bf16 qg [C, hla_ld] with
+// scales sgy ([T] or [1]) and the HLA int8 codes as fp16 qg [C, hla_ld] with
 // scale sg[0], exactly as launch_hq_rows and launch_hla produce them.
 cudaError_t launch_gy_fused(const void* gy, bool bf16, int64_t T, int64_t C, int rank,
                             bool per_token, bool amax_only, unsigned int* hq_amax,
@@ -90,20 +90,21 @@ cudaError_t launch_hla_transform(const void* src, bool bf16, int64_t T,
                                  int64_t C, int rank, float* out,
                                  unsigned int* status, cudaStream_t st);
 
-// in [rows, cols] int8 (row stride cols) -> out [rows, out_ld] bf16.
-cudaError_t launch_widen_i4_bf16(const uint8_t* in, void* out, int64_t rows, int64_t cols,
-                                 int64_t out_ld, cudaStream_t st);
-cudaError_t launch_widen_i8_bf16(const int8_t* in, void* out, int64_t rows,
-                                 int64_t cols, int64_t out_ld, cudaStream_t st);
+// in [rows, cols] int8 (row stride cols), or packed int4 -> out [rows, out_ld]
+// fp16.
+cudaError_t launch_widen_i4_f16(const uint8_t* in, void* out, int64_t rows, int64_t cols,
+                                int64_t out_ld, cudaStream_t st);
+cudaError_t launch_widen_i8_f16(const int8_t* in, void* out, int64_t rows,
+                                int64_t cols, int64_t out_ld, cudaStream_t st);
 cudaError_t launch_pack_e4m3_int4(const uint8_t* in, uint8_t* out, int64_t n,
                                   cudaStream_t st);
 cudaError_t launch_decode_e4m3(const uint8_t* in, int8_t* out, int64_t n,
                                cudaStream_t st);
-cudaError_t launch_decode_bf16(const void* in, int8_t* out, int64_t rows,
-                               int64_t cols, int64_t ld, cudaStream_t st);
+cudaError_t launch_decode_f16(const void* in, int8_t* out, int64_t rows,
+                              int64_t cols, int64_t ld, cudaStream_t st);
 
 // Operand code formats of the GEMMs.
-enum CodeFmt { kFmtE4M3 = 0, kFmtI8 = 1, kFmtBF16 = 2 };
+enum CodeFmt { kFmtE4M3 = 0, kFmtI8 = 1, kFmtF16 = 2 };
 
 // Exact integer GEMM on CUDA cores (dp4a): acc[m, n] = sum_k A[m,k] B[n,k],
 // A [M, K], B [N, K] (contraction dim contiguous).  Epilogue:
@@ -121,8 +122,11 @@ bool make_tile_map_2d(CUtensorMap* map, const void* ptr, bool bf16, int64_t rows
                       int64_t cols, int box_cols, int box_rows);
 
 // Tensor-core GEMM (hlq_gemm_tc.cu).  kind 0: E4M3 operands (int4 codes),
-// kind 1: bf16 operands (int8 codes).  A [M, K] (row stride lda elements),
+// kind 1: fp16 operands (int8 codes).  A [M, K] (row stride lda elements),
 // B [N, K] (ldb); out [M, N] fp32 = acc * sa[m or 0] * sb[0] / 16.
+// raw (kind 1 only): kRawB / kRawA mark an operand given as int8 codes in
+// HBM (row stride in bytes, a multiple of 16, base 16-byte aligned), widened
+// to fp16 in shared memory inside the GEMM.
 struct GemmPlan {
   int bn = 128;      // tile width (96, 128 or 256)
   int splits = 1;    // K split count (int32 workspace reduction)
@@ -138,7 +142,9 @@ cudaError_t launch_gemm_tc(int kind, const void* A, int64_t lda, const void* B,
                            const GemmPlan& plan, const float* sa, bool per_row_a,
                            const float* sb, float* out, int32_t* acc_out,
                            void* split_ws, unsigned int* status, cudaStream_t st,
-                           bool per_col_b = false);  // sb[n] per column (kind 1)
+                           bool per_col_b = false,  // sb[n] per column (kind 1)
+                           int raw = 0);
+constexpr int kRawB = 1, kRawA = 2;
 
 // The g_x path with a given workspace (the body of hlq_linear_backward_gx)
 // and the workspace it needs.

@@ -405,14 +405,14 @@ __global__ void __launch_bounds__(256) hq_rows_kernel(
 // apart): helpers shared by the w and HLA kernels and the transform-only
 // debug kernel.
 // ---------------------------------------------------------------------------
-enum ColOut { kColI8 = 1, kColBf16 = 2, kColI4 = 3 };
+enum ColOut { kColI8 = 1, kColF16 = 2, kColI4 = 3 };
 
 // Code storage of an HLA output format: bytes per code as num / den (int4
 // codes are packed two per byte, code 2k in the low nibble), and the
 // symmetric code range.
 template <int kOut>
 struct ColFmt {
-  static constexpr int kNum = kOut == kColBf16 ? 2 : 1;
+  static constexpr int kNum = kOut == kColF16 ? 2 : 1;
   static constexpr int kDen = kOut == kColI4 ? 2 : 1;
   static constexpr float kQmax = kOut == kColI4 ? 7.0f : 127.0f;
 };
@@ -420,8 +420,8 @@ struct ColFmt {
 // Pack code k (an integer-valued float) of a column's block into p.
 template <int kOut>
 __device__ __forceinline__ void pack_code(uint32_t* p, int k, float q) {
-  if (kOut == kColBf16)
-    p[k >> 1] |= (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(q)) << (16 * (k & 1));
+  if (kOut == kColF16)
+    p[k >> 1] |= (uint32_t)__half_as_ushort(__float2half_rn(q)) << (16 * (k & 1));
   else if (kOut == kColI4)
     p[k >> 3] |= ((uint32_t)(int)q & 0xfu) << (4 * (k & 7));
   else
@@ -845,7 +845,7 @@ __global__ void __launch_bounds__(256) hla_rows_kernel(
           uint32_t p[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
 #pragma unroll
           for (int k = 0; k < kR; ++k)
-            pack_code<kColBf16>(p, k, quant_rne_f(y[sequency_row(k)], s, 127.0f));
+            pack_code<kColF16>(p, k, quant_rne_f(y[sequency_row(k)], s, 127.0f));
           const int64_t b = oct >> 1;
           store_chunk(static_cast<uint8_t*>(out) + (row * out_ld + b * kR) * 2, p, 2 * kR);
         }
@@ -1115,8 +1115,8 @@ __global__ void __launch_bounds__(128) gy_fused_kernel(
     int64_t hla_ld, float* __restrict__ sg, int rnd, const PhiloxKeys keys,
     unsigned int* __restrict__ status) {
   constexpr int kStage = 16 * kTmaCols * (kBf16 ? 2 : 4);
-  using F = ColFmt<kColBf16>;
-  constexpr int kChunk = kR * 2;  // bf16 code bytes per block and column
+  using F = ColFmt<kColF16>;
+  constexpr int kChunk = kR * 2;  // fp16 code bytes per block and column
   extern __shared__ __align__(128) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
@@ -1171,7 +1171,7 @@ __global__ void __launch_bounds__(128) gy_fused_kernel(
         uint32_t p[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
 #pragma unroll
         for (int k = 0; k < kR; ++k)
-          pack_code<kColBf16>(p, k, quant_rne_f(coef[k], s_hla, F::kQmax));
+          pack_code<kColF16>(p, k, quant_rne_f(coef[k], s_hla, F::kQmax));
         store_chunk(static_cast<uint8_t*>(qg) + ((c0 + c) * hla_ld + b * kR) * 2, p, kChunk);
       }
     }
@@ -1636,10 +1636,10 @@ __global__ void __launch_bounds__(128) col_transform_kernel(
 // ---------------------------------------------------------------------------
 // Format conversions (GEMM operand widening and debug read-back).
 // ---------------------------------------------------------------------------
-// int8 codes [rows, cols] -> bf16 codes [rows, out_ld]; 8 codes per thread
+// int8 codes [rows, cols] -> fp16 codes [rows, out_ld]; 8 codes per thread
 // (cols is a multiple of 8 on the vector path).
-__global__ void widen_i8_to_bf16_kernel(const int8_t* __restrict__ in,
-                                        __nv_bfloat16* __restrict__ out,
+__global__ void widen_i8_to_f16_kernel(const int8_t* __restrict__ in,
+                                       __half* __restrict__ out,
                                         int64_t rows, int64_t cols,
                                         int64_t out_ld) {
   pdl_trigger();
@@ -1649,17 +1649,17 @@ __global__ void widen_i8_to_bf16_kernel(const int8_t* __restrict__ in,
   if (idx >= rows * per_row) return;
   const int64_t r = idx / per_row, c = (idx % per_row) * 8;
   const int8_t* src = in + r * cols + c;
-  __nv_bfloat16* dst = out + r * out_ld + c;
+  __half* dst = out + r * out_ld + c;
   if (c + 8 <= cols && (cols % 8) == 0) {
     uint2 v = ld_dep_u2(src);
     const int8_t* b = reinterpret_cast<const int8_t*>(&v);
-    __align__(16) __nv_bfloat16 o[8];
+    __align__(16) __half o[8];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) o[k] = __int2bfloat16_rn(b[k]);
+    for (int k = 0; k < 8; ++k) o[k] = __int2half_rn(b[k]);
     *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(o);
   } else {
     for (int k = 0; k < 8 && c + k < cols; ++k)
-      dst[k] = __int2bfloat16_rn((int8_t)ld_dep_u8(src + k));
+      dst[k] = __int2half_rn((int8_t)ld_dep_u8(src + k));
   }
 }
 
@@ -1682,13 +1682,13 @@ __global__ void pack_e4m3_int4_kernel(const uint8_t* __restrict__ in,
   }
 }
 
-__global__ void decode_bf16_kernel(const __nv_bfloat16* __restrict__ in,
+__global__ void decode_f16_kernel(const __half* __restrict__ in,
                                    int8_t* __restrict__ out, int64_t rows,
                                    int64_t cols, int64_t ld) {
   const int64_t n = rows * cols;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
        i += (int64_t)gridDim.x * blockDim.x)
-    out[i] = (int8_t)__bfloat162int_rn(in[(i / cols) * ld + i % cols]);
+    out[i] = (int8_t)__half2int_rn(in[(i / cols) * ld + i % cols]);
 }
 
 // ---------------------------------------------------------------------------
@@ -1909,8 +1909,8 @@ cudaError_t launch_hla(const void* src, bool bf16, int64_t T, int64_t C,
 #define LHO(B, M, O) \
   launch_hla_o<B, M, O>(src, T, C, rank, amax_slot, out, out_ld, scale, status, pc, st)
   if (amax_only) return bf16 ? LHO(true, kAmax, kColI8) : LHO(false, kAmax, kColI8);
-  if (out_fmt == kHlaOutBf16)
-    return bf16 ? LHO(true, kQuant, kColBf16) : LHO(false, kQuant, kColBf16);
+  if (out_fmt == kHlaOutF16)
+    return bf16 ? LHO(true, kQuant, kColF16) : LHO(false, kQuant, kColF16);
   if (out_fmt == kHlaOutI4) return bf16 ? LHO(true, kQuant, kColI4) : LHO(false, kQuant, kColI4);
   return bf16 ? LHO(true, kQuant, kColI8) : LHO(false, kQuant, kColI8);
 #undef LHO
@@ -1987,9 +1987,9 @@ cudaError_t launch_hla_transform(const void* src, bool bf16, int64_t T,
 }
 
 // Packed int4 codes [rows, cols/2 bytes] (code 2k in the low nibble) to
-// bf16 rows with stride out_ld; 8 codes per thread.
-__global__ void widen_i4_to_bf16_kernel(const uint8_t* __restrict__ in,
-                                        __nv_bfloat16* __restrict__ out, int64_t rows,
+// fp16 rows with stride out_ld; 8 codes per thread.
+__global__ void widen_i4_to_f16_kernel(const uint8_t* __restrict__ in,
+                                       __half* __restrict__ out, int64_t rows,
                                         int64_t cols, int64_t out_ld) {
   pdl_trigger();
   pdl_wait();
@@ -1998,40 +1998,40 @@ __global__ void widen_i4_to_bf16_kernel(const uint8_t* __restrict__ in,
   if (idx >= rows * per_row) return;
   const int64_t r = idx / per_row, c = (idx % per_row) * 8;
   const uint8_t* src = in + (r * cols + c) / 2;
-  __nv_bfloat16* dst = out + r * out_ld + c;
+  __half* dst = out + r * out_ld + c;
   auto code = [&](int k) {  // sign-extended nibble k of the run
     const int v = (ld_dep_u8(src + (k >> 1)) >> (4 * (k & 1))) & 0xf;
     return v >= 8 ? v - 16 : v;
   };
   if (c + 8 <= cols && (cols % 8) == 0) {
     const uint32_t w = ld_dep_u32(reinterpret_cast<const unsigned int*>(src));
-    __align__(16) __nv_bfloat16 o[8];
+    __align__(16) __half o[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
       const int v = (int)((w >> (4 * k)) & 0xfu);
-      o[k] = __int2bfloat16_rn(v >= 8 ? v - 16 : v);
+      o[k] = __int2half_rn(v >= 8 ? v - 16 : v);
     }
     *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(o);
   } else {
-    for (int k = 0; k < 8 && c + k < cols; ++k) dst[k] = __int2bfloat16_rn(code(k));
+    for (int k = 0; k < 8 && c + k < cols; ++k) dst[k] = __int2half_rn(code(k));
   }
 }
 
-cudaError_t launch_widen_i4_bf16(const uint8_t* in, void* out, int64_t rows, int64_t cols,
+cudaError_t launch_widen_i4_f16(const uint8_t* in, void* out, int64_t rows, int64_t cols,
                                  int64_t out_ld, cudaStream_t st) {
   if (rows * cols == 0) return cudaSuccess;
   const int64_t n = rows * ((cols + 7) / 8);
-  launch_pdl(widen_i4_to_bf16_kernel, dim3(grid1(n, 256)), dim3(256), 0, st, in,
-             static_cast<__nv_bfloat16*>(out), rows, cols, out_ld);
+  launch_pdl(widen_i4_to_f16_kernel, dim3(grid1(n, 256)), dim3(256), 0, st, in,
+             static_cast<__half*>(out), rows, cols, out_ld);
   return cudaGetLastError();
 }
 
-cudaError_t launch_widen_i8_bf16(const int8_t* in, void* out, int64_t rows,
+cudaError_t launch_widen_i8_f16(const int8_t* in, void* out, int64_t rows,
                                  int64_t cols, int64_t out_ld, cudaStream_t st) {
   if (rows * cols == 0) return cudaSuccess;
   const int64_t n = rows * ((cols + 7) / 8);
-  launch_pdl(widen_i8_to_bf16_kernel, dim3(grid1(n, 256)), dim3(256), 0, st, in,
-             static_cast<__nv_bfloat16*>(out), rows, cols, out_ld);
+  launch_pdl(widen_i8_to_f16_kernel, dim3(grid1(n, 256)), dim3(256), 0, st, in,
+             static_cast<__half*>(out), rows, cols, out_ld);
   return cudaGetLastError();
 }
 
@@ -2074,12 +2074,12 @@ cudaError_t launch_decode_e4m3(const uint8_t* in, int8_t* out, int64_t n,
   return cudaGetLastError();
 }
 
-cudaError_t launch_decode_bf16(const void* in, int8_t* out, int64_t rows,
+cudaError_t launch_decode_f16(const void* in, int8_t* out, int64_t rows,
                                int64_t cols, int64_t ld, cudaStream_t st) {
   const int64_t n = rows * cols;
   if (n == 0) return cudaSuccess;
-  decode_bf16_kernel<<<(unsigned)imin64(grid1(n, 256), 4096), 256, 0, st>>>(
-      static_cast<const __nv_bfloat16*>(in), out, rows, cols, ld);
+  decode_f16_kernel<<<(unsigned)imin64(grid1(n, 256), 4096), 256, 0, st>>>(
+      static_cast<const __half*>(in), out, rows, cols, ld);
   return cudaGetLastError();
 }
 

@@ -165,6 +165,34 @@ hlq_status hlq_linear_backward_gw(const void *d_gy, int dt, const int8_t *d_xbar
                                   size_t ws_bytes, void *stream);
 
 /*
+ * How every g_w GEMM of the library takes its int8 operands (HLQ TL;DR:
+ * int8 on the g_w path).  One setting for the process, read by each call
+ * when it enqueues its work; results are bit-identical in every mode, only
+ * the HBM layout and the kernels differ:
+ *   HLQ_GW_WIDEN      the int8 x-bar is widened to fp16 in the workspace by
+ *                     a kernel of its own; the HLA codes of g_y are written
+ *                     as fp16;
+ *   HLQ_GW_INT8_X     the GEMM loads the int8 x-bar itself and widens each
+ *                     tile to fp16 in shared memory; g_y codes as fp16;
+ *   HLQ_GW_INT8_BOTH  both operands int8 in HBM (the HLA codes of g_y too),
+ *                     both widened in shared memory (the fused reader of
+ *                     hlq_linear_backward_fused writes fp16 codes and takes
+ *                     HLQ_GW_INT8_X there);
+ *   HLQ_GW_AUTO       the library's default (the fastest measured).
+ * The in-GEMM widening needs int8 x-bar whose rows T' bytes are a multiple
+ * of 16 and a 16-byte aligned d_xbar; other calls use HLQ_GW_WIDEN.  The
+ * workspace sizes do not depend on the mode.  hlq_set_gw_operands returns
+ * HLQ_ERR_INVALID_ARG for an unknown mode; hlq_get_gw_operands returns the
+ * setting.
+ */
+#define HLQ_GW_AUTO 0
+#define HLQ_GW_WIDEN 1
+#define HLQ_GW_INT8_X 2
+#define HLQ_GW_INT8_BOTH 3
+hlq_status hlq_set_gw_operands(int mode);
+int hlq_get_gw_operands(void);
+
+/*
  * The whole backward pass of the layer: g_x exactly as hlq_linear_backward_gx
  * and g_w exactly as hlq_linear_backward_gw, with the independent branches
  * overlapped on the GPU.  The g_w branch and the HQ of w run on auxiliary
@@ -288,7 +316,10 @@ hlq_status hlq_debug_reference_gemm(int kind, const void *d_a, const void *d_b,
  * The tensor-core GEMM alone, with an explicit plan, for checks and tuning:
  *   d_acc[m, n] = sum_k A[m, k] * B[n, k]   (int32, exact)
  * kind 0: A, B hold E4M3 bytes of integers in [-7, 7] (the g_x GEMM);
- * kind 1: A, B hold bf16 values of integers in [-127, 127] (the g_w GEMM).
+ * kind 1: A, B hold fp16 values of integers in [-127, 127] (the g_w GEMM);
+ * kind 2: A as kind 1, B int8 codes in [-127, 127] widened to fp16 in shared
+ *         memory by the GEMM (the g_w GEMM under HLQ_GW_INT8_X);
+ * kind 3: A and B int8 codes, both widened (HLQ_GW_INT8_BOTH).
  * lda / ldb: row strides in elements (16-byte multiples).  bn: tile width
  * 96, 128 or 256 (0 = the library's choice); splits: K split count (0 = the
  * library's choice; > 1 needs d_ws of hlq_debug_tc_gemm_ws_bytes(M, N);

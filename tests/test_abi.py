@@ -139,7 +139,8 @@ def test_tc_gemm_plan_validation(L):
                  None)
 
     assert call(bn=64) == 1
-    assert call(kind=2) == 1
+    assert call(kind=4) == 1
+    assert call(kind=-1) == 1
     assert call(splits=65) == 1
     assert call(kind=0, splits=2) == 1        # the E4M3 GEMM runs unsplit
     assert call(bn=192) == 1
@@ -393,3 +394,15 @@ def test_entry_points_refuse_a_wrong_output_before_calling_the_library(monkeypat
         hlq.hlq_linear_backward_gw(gy, _FakeTensor(0, shape=(48, 8), dtype=torch.int8,
                                                     itemsize=1), sx, ws=ws,
                                    out=_FakeTensor(0, shape=(16, 48)))
+
+
+def test_gw_operand_mode_is_validated(L):
+    """The g_w operand layout switch: known modes round-trip, others are
+    refused and leave the setting alone (no GPU needed)."""
+    for mode in (hlq.GW_WIDEN, hlq.GW_INT8_X, hlq.GW_INT8_BOTH, hlq.GW_AUTO):
+        hlq.hlq_set_gw_operands(mode)
+        assert hlq.hlq_get_gw_operands() == mode
+    for bad in (4, 7, -1):
+        with pytest.raises(hlq.HLQError):
+            hlq.hlq_set_gw_operands(bad)
+        assert hlq.hlq_get_gw_operands() == hlq.GW_AUTO

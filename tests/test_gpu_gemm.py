@@ -1,6 +1,7 @@
 """The tensor-core GEMMs alone: exact int32 sums for every tile width and
-K split, ragged M/N/K, both operand kinds (E4M3 int4 codes, bf16 int8
-codes), against numpy int64 sums and the CUDA-core reference GEMM."""
+K split, ragged M/N/K, every operand kind (E4M3 int4 codes; fp16 int8 codes;
+int8 codes widened to fp16 in shared memory, for B alone or both operands),
+against numpy int64 sums and the CUDA-core reference GEMM."""
 import numpy as np
 import pytest
 import torch
@@ -29,21 +30,24 @@ def _lib():
     hlq.lib()
 
 
-def run(kind, A, B, bn, splits, pair=-1):
+def _operand(kind, X, which):
     if kind == 0:
-        a = torch.from_numpy(e4m3_bytes(A)).cuda()
-        b = torch.from_numpy(e4m3_bytes(B)).cuda()
-    else:
-        a = torch.from_numpy(A.astype(np.float32)).cuda().to(torch.bfloat16)
-        b = torch.from_numpy(B.astype(np.float32)).cuda().to(torch.bfloat16)
+        return torch.from_numpy(e4m3_bytes(X)).cuda()
+    if kind == 1 or (kind == 2 and which == "a"):
+        return torch.from_numpy(X.astype(np.float16)).cuda()
+    return torch.from_numpy(X.astype(np.int8)).cuda()
+
+
+def run(kind, A, B, bn, splits, pair=-1):
+    a, b = _operand(kind, A, "a"), _operand(kind, B, "b")
     return hlq.hlq_debug_tc_gemm(kind, a, b, bn=bn, splits=splits, pair=pair)
 
 
 def test_tc_gemm_pair_one_tile():
     """The smallest CTA-pair GEMM: one 256 x 256 tile (one pair), one and
-    several k-blocks, both operand kinds; the first GPU check of the pair
+    several k-blocks, every operand kind; the first GPU check of the pair
     path, kept apart so that it runs before the larger cases."""
-    for kind, qmax in ((0, 7), (1, 127)):
+    for kind, qmax in ((0, 7), (1, 127), (2, 127), (3, 127)):
         for K in (128, 256, 1024):
             rng = np.random.default_rng(K + kind)
             A = rng.integers(-qmax, qmax + 1, (256, K))
@@ -54,14 +58,17 @@ def test_tc_gemm_pair_one_tile():
     assert hlq.hlq_read_device_status() == 0
 
 
-# Every tile width, unsplit, for both kinds, on one CTA per tile and on CTA
-# pairs (128- and 256-wide); K splits for the bf16 GEMM only (the E4M3 GEMM
+# Every tile width, unsplit, for every kind, on one CTA per tile and on CTA
+# pairs (128- and 256-wide); K splits for the fp16 GEMMs only (the E4M3 GEMM
 # runs unsplit: the ABI refuses a split plan for it, which the CPU
 # plan-validation test checks).
-PLANS = ([(kind, qmax, bn, 1, 0) for kind, qmax in ((0, 7), (1, 127)) for bn in (128, 256, 96)]
-         + [(kind, qmax, bn, 1, 1) for kind, qmax in ((0, 7), (1, 127)) for bn in (128, 256)]
-         + [(1, 127, bn, splits, 0) for bn, splits in ((128, 3), (256, 2), (96, 2))]
-         + [(1, 127, bn, splits, 1) for bn, splits in ((128, 3), (256, 2))])
+_KINDS = ((0, 7), (1, 127), (2, 127), (3, 127))
+PLANS = ([(kind, qmax, bn, 1, 0) for kind, qmax in _KINDS for bn in (128, 256, 96)]
+         + [(kind, qmax, bn, 1, 1) for kind, qmax in _KINDS for bn in (128, 256)]
+         + [(kind, 127, bn, splits, 0) for kind in (1, 2, 3)
+            for bn, splits in ((128, 3), (256, 2), (96, 2))]
+         + [(kind, 127, bn, splits, 1) for kind in (1, 2, 3)
+            for bn, splits in ((128, 3), (256, 2))])
 
 
 @pytest.mark.parametrize("kind,qmax,bn,splits,pair", PLANS)
@@ -83,7 +90,9 @@ def test_tc_gemm_library_plan_exact():
     """The plan the library picks for the workload shapes (tile width, K
     split), at full size, checked on sampled rows."""
     for kind, qmax, M, N, K in [(0, 7, 12608, 768, 2304), (1, 127, 2304, 768, 6304),
-                                (1, 127, 256, 2304, 25088)]:
+                                (1, 127, 256, 2304, 25088), (2, 127, 2304, 768, 6304),
+                                (3, 127, 256, 2304, 25088), (2, 127, 4096, 2048, 8192),
+                                (3, 127, 4096, 2048, 8192)]:
         rng = np.random.default_rng(M + N + K)
         A = rng.integers(-qmax, qmax + 1, (M, K))
         B = rng.integers(-qmax, qmax + 1, (N, K))
@@ -92,17 +101,36 @@ def test_tc_gemm_library_plan_exact():
         np.testing.assert_array_equal(got[rows], A[rows].astype(np.int64) @ B.astype(np.int64).T)
 
 
-def test_tc_gemm_bf16_worst_case_magnitude():
+@pytest.mark.parametrize("kind", [1, 2, 3])
+def test_tc_gemm_f16_worst_case_magnitude(kind):
     """Every product 127*127 with one sign: |acc| = 16129*K, far above 2^24,
-    only exact through the chunked drains (and the int32 split reduction)."""
+    only exact through the chunked drains (and the int32 split reduction);
+    -127 and 127 are also the extreme codes of the in-GEMM widening."""
     M, N, K = 256, 256, 16384
     A = np.full((M, K), 127, np.int64)
     A[1::2] = -127
     B = np.full((N, K), 127, np.int64)
     for splits, pair in ((1, 0), (2, 0), (5, 0), (1, 1), (3, 1)):
-        got = run(1, A, B, 128, splits, pair).cpu().numpy()
+        got = run(kind, A, B, 128, splits, pair).cpu().numpy()
         assert got[0, 0] == 16129 * K and got[1, 0] == -16129 * K
         assert np.all(got[0::2] == 16129 * K) and np.all(got[1::2] == -16129 * K)
+
+
+def test_tc_gemm_widening_every_code():
+    """Every int8 code value (including -128, outside the codes the library
+    writes) at every position of a k-block, against a one-hot operand, so
+    that each widened code comes out alone: with kind 3 the codes are A
+    (acc = A . I = A), with kind 2 they are B (acc = I . B^T = B^T)."""
+    K = 256
+    P = np.tile(np.arange(-128, 128, dtype=np.int64), (256, 1))
+    for r in range(256):
+        P[r] = np.roll(P[r], 3 * r + (r >> 7))
+    E = np.eye(K, dtype=np.int64)
+    for pair in (0, 1):
+        got = run(3, P, E, 128, 1, pair).cpu().numpy()
+        np.testing.assert_array_equal(got.astype(np.int64), P)
+        got = run(2, E, P, 128, 1, pair).cpu().numpy()
+        np.testing.assert_array_equal(got.astype(np.int64), P.T)
 
 
 def test_tc_gemm_e4m3_worst_case_magnitude():
