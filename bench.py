@@ -510,6 +510,14 @@ def measure_workload(args, wl, dev, dist, headline):
                                        rnd=hlq.SR, seed=wl.seed, out=gx, ws=ws1)
             hlq.hlq_linear_backward_gw(gg, xbar, sx, rank=wl.rank, out=gw, ws=ws1)
 
+    def traced_step():
+        # the step's own call with every branch on this stream in turn
+        hlq.hlq_debug_serialize_branches(True)
+        try:
+            step(x, gy, w)
+        finally:
+            hlq.hlq_debug_serialize_branches(False)
+
     # ---- device-resident timing ------------------------------------------
     # The step is captured into a CUDA graph and replayed (no host launch
     # gaps).  Timed region: each step = L2 flush (outside the events), then
@@ -533,12 +541,13 @@ def measure_workload(args, wl, dev, dist, headline):
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
             step(x, gy, w)
-        # per-kernel attribution: the branches one after the other, so each
-        # kernel's traced time is its own (as in a serialised profiler run)
+        # per-kernel attribution: the same call with its branches one after
+        # the other, so each kernel's traced time is its own (as in a
+        # serialised profiler run)
         traced = torch.cuda.CUDAGraph()
         hlq.hlq_trace_begin(256)
         with torch.cuda.graph(traced):
-            step(x, gy, w, overlap=False)
+            traced_step()
         hlq.hlq_trace_end(keep=True)
         for _ in range(args.warmup):
             graph.replay()
@@ -579,7 +588,7 @@ def measure_workload(args, wl, dev, dist, headline):
             launches += hlq.hlq_trace_read()
         else:
             hlq.hlq_trace_begin(256)
-            step(x, gy, w, overlap=False)
+            traced_step()
             torch.cuda.synchronize()
             launches += hlq.hlq_trace_end()
     if traced is not None:
@@ -778,7 +787,9 @@ def measure_workload(args, wl, dev, dist, headline):
     res["e2e_ms"] = e2e
     res["e2e_spread"] = {"min_us": min(e2e_ms) * 1e3, "median_us": statistics.median(e2e_ms) * 1e3,
                          "max_us": max(e2e_ms) * 1e3,
-                         "host_enqueue_us": statistics.median(enqueue_ms) * 1e3}
+                         "host_enqueue_us": statistics.median(enqueue_ms) * 1e3,
+                         "host_enqueue_max_us": max(enqueue_ms) * 1e3,
+                         "steps_us": [round(t * 1e3, 1) for t in e2e_ms]}
     res["e2e_bytes"] = ((x.numel() + gy.numel() + w.numel()) * e,
                         (gx.numel() + gw.numel()) * 4)
     res["acbp_stored_bytes"] = acbp_bytes(T, Cin, wl.rank, e)

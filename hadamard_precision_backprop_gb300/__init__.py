@@ -50,7 +50,7 @@ EXPORTS = [
     "hlq_layer_step",
     "hlq_debug_gemm_plan",
     "hlq_debug_wait_timeout",
-    "hlq_set_gw_operands", "hlq_get_gw_operands",
+    "hlq_set_gw_operands", "hlq_get_gw_operands", "hlq_debug_serialize_branches",
 ]
 
 _lock = threading.Lock()
@@ -128,6 +128,7 @@ def lib() -> ctypes.CDLL:
             "hlq_trace_free": (i32, []),
             "hlq_set_gw_operands": (i32, [i32]),
             "hlq_get_gw_operands": (i32, []),
+            "hlq_debug_serialize_branches": (i32, [i32]),
             "hlq_status_string": (ctypes.c_char_p, [i32]),
             "hlq_version": (i32, []),
         }
@@ -725,6 +726,14 @@ def hlq_set_gw_operands(mode: int):
 
 def hlq_get_gw_operands() -> int:
     return int(lib().hlq_get_gw_operands())
+
+
+def hlq_debug_serialize_branches(on: bool):
+    """Run the branches of hlq_linear_backward / hlq_layer_step on the
+    caller's stream one after the other (same kernels, for per-kernel
+    timing), or forked again (on=False)."""
+    _check(lib().hlq_debug_serialize_branches(1 if on else 0),
+           "hlq_debug_serialize_branches")
 
 
 def hlq_trace_begin(capacity: int = 4096):

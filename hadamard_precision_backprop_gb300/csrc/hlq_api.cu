@@ -97,6 +97,16 @@ cudaStream_t aux_stream(int which) {
   return g_aux_stream[dev][which];
 }
 
+// hlq_debug_serialize_branches: every branch of the device entries on the
+// caller's stream, one after the other (for per-kernel timing).
+bool g_serial_branches = false;
+
+// The stream a branch of a device entry runs on: a library stream forked
+// from the caller's, or the caller's own when branches are serialised.
+cudaStream_t branch_stream(int which, cudaStream_t caller) {
+  return g_serial_branches ? caller : aux_stream(which);
+}
+
 constexpr size_t kAlign = 256;
 inline size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
@@ -538,7 +548,7 @@ constexpr int kMaxHostChunks = 64;
 // runtime keeps pending ones alive until they complete): six for the
 // streams' hand-offs and two per chunk of g_y.
 struct EventSet {
-  static constexpr int kCap = 6 + 2 * kMaxHostChunks;
+  static constexpr int kCap = 6 + 3 * kMaxHostChunks;
   cudaEvent_t ev[kCap] = {};
   int n = 0;
   cudaEvent_t make() {
@@ -648,8 +658,8 @@ hlq_status hlq_linear_backward(const void* d_gy, const void* d_w, const int8_t* 
   if (!aligned256(d_ws)) return HLQ_ERR_ALIGN;
   uint8_t* base = static_cast<uint8_t*>(d_ws);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaStream_t a = aux_stream(0), aw = aux_stream(1);
-  if (!a || !aw) return HLQ_ERR_CUDA;
+  cudaStream_t a = branch_stream(0, s), aw = branch_stream(1, s);
+  if (!g_serial_branches && (!a || !aw)) return HLQ_ERR_CUDA;  // (null: the legacy stream)
   // validate both branches before forking (nothing enqueued on failure)
   st = gw_impl(d_gy, dt, d_xbar, xbar_fmt, d_xbar_scale, T, Cin, Cout, block, rank, d_gw,
                base + gx_bytes, gw_bytes, nullptr, nullptr, nullptr, nullptr,
@@ -739,8 +749,8 @@ hlq_status hlq_layer_step(const void* d_x, const void* d_gy, const void* d_w, in
   unsigned int* status = device_status_ptr();
   if (!status) return HLQ_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaStream_t a = aux_stream(0), aw = aux_stream(1);
-  if (!a || !aw) return HLQ_ERR_CUDA;
+  cudaStream_t a = branch_stream(0, s), aw = branch_stream(1, s);
+  if (!g_serial_branches && (!a || !aw)) return HLQ_ERR_CUDA;  // (null: the legacy stream)
   EventSet E;
   cudaEvent_t fork = E.make(), join = E.make(), gx_done = E.make();
   if (!fork || !join || !gx_done) return HLQ_ERR_CUDA;
@@ -943,8 +953,8 @@ hlq_status hlq_linear_backward_fused(const void* d_gy, const void* d_w, const in
   if (!status) return HLQ_ERR_CUDA;
   const int sms = device_sm_count();
   if (sms <= 0) return HLQ_ERR_CUDA;
-  cudaStream_t a = aux_stream(0), aw = aux_stream(1);
-  if (!a || !aw) return HLQ_ERR_CUDA;
+  cudaStream_t a = branch_stream(0, s), aw = branch_stream(1, s);
+  if (!g_serial_branches && (!a || !aw)) return HLQ_ERR_CUDA;  // (null: the legacy stream)
   const GxLayout GL = gx_layout(T, Cin, Cout);
   const GwLayout WL = gw_layout(T, Cin, Cout, rank);
   unsigned int* gx_amax = reinterpret_cast<unsigned int*>(gxb + GL.amax);
@@ -1114,14 +1124,15 @@ hlq_status hlq_layer_step_host(const void* h_x, const void* h_gy, const void* h_
   if (sms <= 0) return HLQ_ERR_CUDA;
 
   EventSet E;
-  cudaEvent_t fork = E.make(), w_in = E.make(), x_in = E.make(), w_done = E.make(),
-              gw_done = E.make(), out_done = E.make();
-  cudaEvent_t gy_in[kMaxHostChunks], gx_done[kMaxHostChunks];
-  bool events_ok = fork && w_in && x_in && w_done && gw_done && out_done;
+  cudaEvent_t fork = E.make(), w_in = E.make(), w_done = E.make(), gw_done = E.make(),
+              out_done = E.make();
+  cudaEvent_t gy_in[kMaxHostChunks], x_in[kMaxHostChunks], gx_done[kMaxHostChunks];
+  bool events_ok = fork && w_in && w_done && gw_done && out_done;
   for (int c = 0; c < nc; ++c) {
     gy_in[c] = E.make();
+    x_in[c] = E.make();
     gx_done[c] = E.make();
-    events_ok = events_ok && gy_in[c] && gx_done[c];
+    events_ok = events_ok && gy_in[c] && x_in[c] && gx_done[c];
   }
   if (!events_ok) return HLQ_ERR_CUDA;
 
@@ -1144,7 +1155,7 @@ hlq_status hlq_layer_step_host(const void* h_x, const void* h_gy, const void* h_
     if (e != cudaSuccess && r == HLQ_OK) r = HLQ_ERR_CUDA;
   };
   fail(cudaEventRecord(fork, s));
-  // copy-in stream: w (first needed), the g_y chunks, then x
+  // copy-in stream: w (first needed), the g_y chunks, then the x chunks
   fail(cudaStreamWaitEvent(cin, fork, 0));
   fail(h2d(w, h_w, (size_t)(Cout * Cin) * esz, cin));
   fail(cudaEventRecord(w_in, cin));
@@ -1155,8 +1166,13 @@ hlq_status hlq_layer_step_host(const void* h_x, const void* h_gy, const void* h_
              (size_t)rows * Cout * esz, cin));
     fail(cudaEventRecord(gy_in[c], cin));
   }
-  fail(h2d(x, h_x, (size_t)(T * Cin) * esz, cin));
-  fail(cudaEventRecord(x_in, cin));
+  for (int c = 0; c < nc; ++c) {
+    const int64_t r0 = c * ch, rows = (r0 + ch <= T ? ch : T - r0);
+    fail(h2d(static_cast<uint8_t*>(x) + (size_t)r0 * Cin * esz,
+             static_cast<const uint8_t*>(h_x) + (size_t)r0 * Cin * esz,
+             (size_t)rows * Cin * esz, cin));
+    fail(cudaEventRecord(x_in[c], cin));
+  }
   // HQ of w
   fail(cudaStreamWaitEvent(a_w, w_in, 0));
   fail(cudaMemsetAsync(gx_amax + 1, 0, 4, a_w));
@@ -1202,17 +1218,47 @@ hlq_status hlq_layer_step_host(const void* h_x, const void* h_gy, const void* h_
     fail(cudaStreamWaitEvent(s, w_done, 0));
     for (int c = 0; c < nc; ++c) gemm_chunk(c);
   }
-  // g_w branch: HLA of g_y once all of it is in, then x's compression
-  fail(cudaStreamWaitEvent(a_gw, gy_in[nc - 1], 0));
+  // g_w branch.  The per-tensor maxima of the HLA of g_y and of the
+  // compression of x are gathered chunk by chunk as the chunks land (16-token
+  // blocks never straddle a chunk: chunks are multiples of 128 tokens), so
+  // that only the quant passes, the widening of x-bar, the g_w GEMM and its
+  // copy-out follow the last byte of x.
   const int gw_rw = gw_raw(xbar_fmt, Tp, d_xbar, false);
-  if (r == HLQ_OK)
-    r = hla_gy_launches(gy, bf16, T, Cout, rank, gw_amax, gwb + WL.qg,
-                        (gw_rw & kRawA) ? WL.ld8 : WL.ld, sg, status, a_gw,
-                        (gw_rw & kRawA) != 0);
-  fail(cudaStreamWaitEvent(a_gw, x_in, 0));
-  if (r == HLQ_OK)
-    r = compress_launches(x, bf16, T, Cin, rank, xbar_fmt, d_xbar, d_xbar_scale,
-                          reinterpret_cast<unsigned int*>(base + L.cws), status, a_gw);
+  const bool qg_i8 = (gw_rw & kRawA) != 0;
+  const bool x_per_ch = xbar_per_channel(xbar_fmt);
+  unsigned int* x_amax = reinterpret_cast<unsigned int*>(base + L.cws);
+  fail(cudaStreamWaitEvent(a_gw, fork, 0));
+  fail(cudaMemsetAsync(gw_amax, 0, 4, a_gw));
+  fail(cudaMemsetAsync(x_amax, 0, (size_t)(x_per_ch ? Cin : 1) * 4, a_gw));
+  for (int c = 0; c < nc && r == HLQ_OK; ++c) {
+    const int64_t r0 = c * ch, rows = (r0 + ch <= T ? ch : T - r0);
+    fail(cudaStreamWaitEvent(a_gw, gy_in[c], 0));
+    trace_before(a_gw);
+    fail(launch_hla(static_cast<const uint8_t*>(gy) + (size_t)r0 * Cout * esz, bf16, rows, Cout,
+                    rank, true, kHlaOutF16, gw_amax, nullptr, 0, nullptr, status, a_gw));
+    trace_after("hla_gy_amax", a_gw);
+  }
+  if (r == HLQ_OK) {
+    trace_before(a_gw);
+    fail(launch_hla(gy, bf16, T, Cout, rank, false, qg_i8 ? kHlaOutI8 : kHlaOutF16, gw_amax,
+                    gwb + WL.qg, qg_i8 ? WL.ld8 : WL.ld, sg, status, a_gw));
+    trace_after("hla_gy_quant", a_gw);
+  }
+  for (int c = 0; c < nc && r == HLQ_OK; ++c) {
+    const int64_t r0 = c * ch, rows = (r0 + ch <= T ? ch : T - r0);
+    fail(cudaStreamWaitEvent(a_gw, x_in[c], 0));
+    trace_before(a_gw);
+    fail(launch_hla(static_cast<const uint8_t*>(x) + (size_t)r0 * Cin * esz, bf16, rows, Cin,
+                    rank, true, kHlaOutI8, x_amax, nullptr, 0, nullptr, status, a_gw, x_per_ch));
+    trace_after("hla_x_amax", a_gw);
+  }
+  if (r == HLQ_OK) {
+    trace_before(a_gw);
+    fail(launch_hla(x, bf16, T, Cin, rank, false,
+                    xbar_code_bits(xbar_fmt) == 4 ? kHlaOutI4 : kHlaOutI8, x_amax, d_xbar, Tp,
+                    d_xbar_scale, status, a_gw, x_per_ch));
+    trace_after("hla_x_quant", a_gw);
+  }
   if (r == HLQ_OK)
     r = gw_gemm_launches(d_xbar, xbar_fmt, d_xbar_scale, Cin, Cout, Tp, WL, gwb, gw, nullptr,
                          status, a_gw,
@@ -1335,10 +1381,11 @@ hlq_status hlq_debug_tc_gemm(int kind, const void* d_a, int64_t lda, const void*
   if (kind < 0 || kind > 3) return HLQ_ERR_INVALID_ARG;
   if (M < 0 || N < 0 || K < 0 || N % 16 || K % 16 || M % 16) return HLQ_ERR_SHAPE;
   if (bn != 0 && bn != 96 && bn != 128 && bn != 256) return HLQ_ERR_INVALID_ARG;
-  if (splits < 0 || splits > 64) return HLQ_ERR_INVALID_ARG;
+  if (splits < -1 || splits > 64) return HLQ_ERR_INVALID_ARG;  // -1: stream-K
   if (pair < -1 || pair > 1) return HLQ_ERR_INVALID_ARG;
   if (pair == 1 && bn == 96) return HLQ_ERR_INVALID_ARG;    // pairs: 128 or 256 wide
-  if (kind == 0 && splits > 1) return HLQ_ERR_INVALID_ARG;  // E4M3 GEMM runs unsplit
+  if (kind == 0 && (splits > 1 || splits == -1)) return HLQ_ERR_INVALID_ARG;  // E4M3: unsplit
+  if (splits == -1 && pair == 1) return HLQ_ERR_INVALID_ARG;  // stream-K: one CTA per tile
   // element bytes of A and B: E4M3 (kind 0), fp16 (kind 1; A of kind 2),
   // int8 widened in the GEMM (B of kinds 2 and 3, A of kind 3)
   const int esz_a = (kind == 1 || kind == 2) ? 2 : 1;
@@ -1356,12 +1403,20 @@ hlq_status hlq_debug_tc_gemm(int kind, const void* d_a, int64_t lda, const void*
   const int raw = kind == 2 ? kRawB : (kind == 3 ? (kRawA | kRawB) : 0);
   GemmPlan plan = plan_gemm_tc(gk, M, N, K, sms, gk == 1 ? 16 : 1);
   if (bn) plan.bn = bn;
-  if (splits) plan.splits = splits;
+  if (splits > 0) {
+    plan.splits = splits;
+    plan.stream_k = 0;
+  } else if (splits == -1) {
+    plan.splits = 1;
+    plan.stream_k = 1;
+    plan.pair = 0;
+  }
   if (pair >= 0) plan.pair = pair;
+  if (plan.pair) plan.stream_k = 0;
   if (plan.pair && plan.bn == 96) return HLQ_ERR_INVALID_ARG;
-  if (plan.splits > 1 && (!d_ws || ws_bytes < gemm_tc_split_ws_bytes(M, N)))
-    return HLQ_ERR_WORKSPACE;
-  if (plan.splits > 1 && !aligned256(d_ws)) return HLQ_ERR_ALIGN;
+  const bool ws_used = plan.splits > 1 || plan.stream_k;
+  if (ws_used && (!d_ws || ws_bytes < gemm_tc_split_ws_bytes(M, N))) return HLQ_ERR_WORKSPACE;
+  if (ws_used && !aligned256(d_ws)) return HLQ_ERR_ALIGN;
   unsigned int* status = device_status_ptr();
   if (!status) return HLQ_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -1379,6 +1434,12 @@ hlq_status hlq_set_gw_operands(int mode) {
 
 int hlq_get_gw_operands(void) { return g_gw_operands; }
 
+hlq_status hlq_debug_serialize_branches(int on) {
+  if (on != 0 && on != 1) return HLQ_ERR_INVALID_ARG;
+  g_serial_branches = on != 0;
+  return HLQ_OK;
+}
+
 hlq_status hlq_debug_gemm_plan(int64_t T, int64_t Cin, int64_t Cout, int rank, int sms,
                                int* gx_bn, int* gx_splits, int* gw_bn, int* gw_splits,
                                int* in_sequence, int* gx_pair, int* gw_pair) {
@@ -1391,7 +1452,7 @@ hlq_status hlq_debug_gemm_plan(int64_t T, int64_t Cin, int64_t Cout, int rank, i
   *gx_bn = px.bn;
   *gx_splits = px.splits;
   *gw_bn = pw.bn;
-  *gw_splits = pw.splits;
+  *gw_splits = pw.stream_k ? -1 : pw.splits;  // -1: stream-K
   *in_sequence = gemms_in_sequence_on(T, Cin, Cout, Tp, sms) ? 1 : 0;
   *gx_pair = px.pair;
   *gw_pair = pw.pair;

@@ -271,7 +271,8 @@ __global__ void __launch_bounds__(TcCfg<BN, kPair, kCvt>::kThreads, 1) gemm_tc_k
     const __grid_constant__ CUtensorMap tmOut, const __grid_constant__ CUtensorMap tmAcc,
     const __grid_constant__ CUtensorMap tmSplit,
     int M, int N, int num_kb, int chunk_kb, int kb_per_split, int splits, int tiles_n,
-    int tiles_m, int group_m, int num_units, const float* __restrict__ sa, int per_row_a,
+    int tiles_m, int group_m, int num_units, int sk_len, const float* __restrict__ sa,
+    int per_row_a,
     const float* __restrict__ sb, int per_col_b, float* __restrict__ out,
     int32_t* __restrict__ acc_out,
     int32_t* __restrict__ split_acc, unsigned int* __restrict__ slab_count,
@@ -354,11 +355,37 @@ __global__ void __launch_bounds__(TcCfg<BN, kPair, kCvt>::kThreads, 1) gemm_tc_k
     kb0 = z * kb_per_split;
     nkb = max(0, min(num_kb, kb0 + kb_per_split) - kb0);
   };
-  auto unit_coords = [&](int u, int& m0, int& n0, int& kb0, int& nkb) {
-    int tm, tn;
-    unit_tile(u, tm, tn, kb0, nkb);
-    m0 = tm * C::kTileM;
-    n0 = tn * BN;
+  // The j-th unit of this CTA (pair): its tile, k-block range and how many
+  // units share the tile (`parts`; 1: the unit stores the tile itself).
+  // Without stream-K the units are u = first_unit + j * unit_step.  With
+  // stream-K (sk_len > 0, one CTA per SM, num_units = tiles, no pairs) CTA b
+  // takes the k-blocks [b sk_len, (b + 1) sk_len) of the tiles laid end to
+  // end, one unit per tile it touches: every SM gets the same share of a
+  // GEMM whose tiles fill less than one wave.
+  struct Unit {
+    int tm, tn, kb0, nkb, parts;
+  };
+  auto get_unit = [&](int j, Unit& w) -> bool {
+    if (sk_len == 0) {
+      const int u = first_unit + j * unit_step;
+      if (u >= num_units) return false;
+      unit_tile(u, w.tm, w.tn, w.kb0, w.nkb);
+      w.parts = splits;
+      return true;
+    }
+    const long long total = (long long)num_units * num_kb;
+    const long long s0 = (long long)first_unit * sk_len;
+    const long long e0 = min(s0 + (long long)sk_len, total);
+    const long long t = s0 / num_kb + j;
+    const long long ts = t * num_kb, te = ts + num_kb;
+    const long long a = max(s0, ts), e = min(e0, te);
+    if (a >= e) return false;
+    int kb_unused, nkb_unused;
+    unit_tile((int)t, w.tm, w.tn, kb_unused, nkb_unused);  // splits == 1 here
+    w.kb0 = (int)(a - ts);
+    w.nkb = (int)(e - a);
+    w.parts = (int)((te - 1) / sk_len - ts / sk_len + 1);
+    return true;
   };
 
   if (warp == 0) {
@@ -369,9 +396,9 @@ __global__ void __launch_bounds__(TcCfg<BN, kPair, kCvt>::kThreads, 1) gemm_tc_k
                    : "memory");
       const int elems = kRowBytes / (kKind == 1 ? 2 : 1);
       int i = 0;  // k-blocks issued by this CTA so far
-      for (int u = first_unit; u < num_units && !*abort_flag; u += unit_step) {
-        int m0, n0, kb0, nkb;
-        unit_coords(u, m0, n0, kb0, nkb);
+      Unit w;
+      for (int ju = 0; !*abort_flag && get_unit(ju, w); ++ju) {
+        const int m0 = w.tm * C::kTileM, n0 = w.tn * BN, kb0 = w.kb0, nkb = w.nkb;
         for (int j = 0; j < nkb; ++j, ++i) {
           const int s = i % kStages;
           const uint32_t ph = (uint32_t)(i / kStages) & 1u;
@@ -413,9 +440,9 @@ __global__ void __launch_bounds__(TcCfg<BN, kPair, kCvt>::kThreads, 1) gemm_tc_k
       const uint32_t idesc = make_idesc(kKind, C::kTileM, BN);
       int i = 0, cc = 0;  // k-blocks and accumulation chunks consumed so far
       bool ok = true;
-      for (int u = first_unit; u < num_units && ok; u += unit_step) {
-        int m0, n0, kb0, nkb;
-        unit_coords(u, m0, n0, kb0, nkb);
+      Unit w;
+      for (int ju = 0; ok && get_unit(ju, w); ++ju) {
+        const int nkb = w.nkb;
         const int nch = (nkb + chunk_kb - 1) / chunk_kb;
         for (int c = 0, j = 0; c < nch && ok; ++c, ++cc) {
           const int buf = cc & 1;
@@ -505,9 +532,9 @@ __global__ void __launch_bounds__(TcCfg<BN, kPair, kCvt>::kThreads, 1) gemm_tc_k
     int cc = 0;
     bool ok = true;
     if constexpr (kKind == 0) {
-      for (int u = first_unit; u < num_units && ok; u += unit_step) {
-        int m0, n0, kb0, nkb;
-        unit_coords(u, m0, n0, kb0, nkb);
+      Unit w;
+      for (int ju = 0; ok && get_unit(ju, w); ++ju) {
+        const int m0 = w.tm * C::kTileM, n0 = w.tn * BN;
         const int m = m0 + row;
         const int nb = n0 + colgrp * C::kColsPerThread;
         const int y = m0 + (int)rank * kBM + quarter * 32;
@@ -581,15 +608,14 @@ __global__ void __launch_bounds__(TcCfg<BN, kPair, kCvt>::kThreads, 1) gemm_tc_k
         release_acc(buf);
         return true;
       };
-      // unit u's sums are complete in acc: store them dequantized, or add
-      // them into the split workspace (the last split of a slab stores)
-      auto finish_unit = [&](int u) {
-        int m0, n0, kb0, nkb;
-        unit_coords(u, m0, n0, kb0, nkb);
+      // unit w's sums are complete in acc: store them dequantized, or add
+      // them into the split workspace (the last unit of a slab stores)
+      auto finish_unit = [&](const Unit& w) {
+        const int m0 = w.tm * C::kTileM, n0 = w.tn * BN;
         const int m = m0 + row;
         const int nb = n0 + colgrp * C::kColsPerThread;
         const int y = m0 + (int)rank * kBM + quarter * 32;
-        if (splits == 1) {
+        if (w.parts == 1) {
           const float scale = dequant_scale(m);
 #pragma unroll
           for (int jc = 0; jc < C::kColsPerThread / 32; ++jc) {
@@ -635,11 +661,9 @@ __global__ void __launch_bounds__(TcCfg<BN, kPair, kCvt>::kThreads, 1) gemm_tc_k
           asm volatile("fence.proxy.async.global;" ::: "memory");
           __threadfence();
           // slab counters per (128-row half tile, epilogue warp)
-          int tm, tn, kb0u, nkbu;
-          unit_tile(u, tm, tn, kb0u, nkbu);
-          const int half = tm * (C::kTileM / kBM) + (int)rank;
-          const int slab = (half * tiles_n + tn) * C::kEpiWarps + ew;
-          last = atomicAdd(&slab_count[slab], 1u) == (unsigned int)(splits - 1);
+          const int half = w.tm * (C::kTileM / kBM) + (int)rank;
+          const int slab = (half * tiles_n + w.tn) * C::kEpiWarps + ew;
+          last = atomicAdd(&slab_count[slab], 1u) == (unsigned int)(w.parts - 1);
           if (last) __threadfence();
         }
         last = __shfl_sync(0xffffffffu, last, 0);
@@ -682,14 +706,13 @@ __global__ void __launch_bounds__(TcCfg<BN, kPair, kCvt>::kThreads, 1) gemm_tc_k
         for (int q = 0; q < C::kColsPerThread; ++q) acc[q] = 0;
       };
       if constexpr (kCvt == 0) {
-        for (int u = first_unit; u < num_units && ok; u += unit_step) {
-          int m0, n0, kb0, nkb;
-          unit_coords(u, m0, n0, kb0, nkb);
-          const int nch = (nkb + chunk_kb - 1) / chunk_kb;
+        Unit w;
+        for (int ju = 0; ok && get_unit(ju, w); ++ju) {
+          const int nch = (w.nkb + chunk_kb - 1) / chunk_kb;
           zero_acc();
           for (int c = 0; c < nch && ok; ++c) ok = drain();
           if (!ok) break;
-          finish_unit(u);
+          finish_unit(w);
         }
       } else {
         // widen stage i's int8 tiles in place; false (in every epilogue
@@ -741,9 +764,9 @@ __global__ void __launch_bounds__(TcCfg<BN, kPair, kCvt>::kThreads, 1) gemm_tc_k
         constexpr int kLag = kStages / 2;
         bool live = true;
         int ahead = 0;  // k-blocks of this unit converted during the last one
-        for (int u = first_unit; u < num_units && live; u += unit_step) {
-          int m0, n0, kb0, nkb;
-          unit_coords(u, m0, n0, kb0, nkb);
+        Unit w;
+        for (int ju = 0; live && get_unit(ju, w); ++ju) {
+          const int nkb = w.nkb;
           const int nch = (nkb + chunk_kb - 1) / chunk_kb;
           zero_acc();
           for (int c = 0, j = 0; c < nch && live; ++c) {
@@ -758,10 +781,9 @@ __global__ void __launch_bounds__(TcCfg<BN, kPair, kCvt>::kThreads, 1) gemm_tc_k
           }
           if (!live) break;
           ahead = 0;
-          if (u + unit_step < num_units) {
-            int m1, n1, kb1, nkb1;
-            unit_coords(u + unit_step, m1, n1, kb1, nkb1);
-            for (; ahead < min(nkb1, kLag); ++ahead)
+          Unit w1;
+          if (get_unit(ju + 1, w1)) {
+            for (; ahead < min(w1.nkb, kLag); ++ahead)
               if (!convert()) {
                 live = false;
                 break;
@@ -769,7 +791,7 @@ __global__ void __launch_bounds__(TcCfg<BN, kPair, kCvt>::kThreads, 1) gemm_tc_k
           }
           if (!live) break;
           ok = drain() && ok;
-          if (ok) finish_unit(u);
+          if (ok) finish_unit(w);
         }
         ok = ok && live;
       }
@@ -873,7 +895,7 @@ cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, const CUtensor
                       int splits, int num_sms, const float* sa, bool per_row_a,
                       const float* sb, bool per_col_b, float* out, int32_t* acc_out,
                       int32_t* split_acc, unsigned int* slab_count, unsigned int* status,
-                      cudaStream_t st) {
+                      cudaStream_t st, bool stream_k) {
   using C = TcCfg<BN, kPair, kCvt>;
   auto kernel = gemm_tc_kernel<kKind, BN, kPair, kCvt>;
   static bool attr_set[64] = {};
@@ -911,7 +933,16 @@ cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, const CUtensor
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   int grid_ctas;
-  if (kPair) {
+  int sk_len = 0;
+  if (stream_k && !kPair && splits == 1 && num_kb > 0) {
+    // equal runs of k-blocks over the tiles laid end to end, one CTA per SM
+    const int64_t total = units * (int64_t)num_kb;
+    const int64_t g = total < num_sms ? total : num_sms;
+    const int64_t len = (total + g - 1) / g;
+    if (len > 0x7fffffff) return cudaErrorInvalidValue;
+    sk_len = (int)len;
+    grid_ctas = (int)((total + len - 1) / len);
+  } else if (kPair) {
     attr[1].id = cudaLaunchAttributeClusterDimension;
     attr[1].val.clusterDim.x = 2;
     attr[1].val.clusterDim.y = 1;
@@ -942,7 +973,7 @@ cudaError_t launch_tc(const CUtensorMap& a, const CUtensorMap& b, const CUtensor
   cfg.numAttrs = kPair ? 2 : 1;
   cudaError_t le = cudaLaunchKernelEx(&cfg, kernel, a, b, mo, macc, msplit, (int)M, (int)N,
                                       num_kb, chunk_kb, kb_per_split, splits, tiles_n, tiles_m,
-                                      group_m, (int)units, sa, per_row_a ? 1 : 0, sb,
+                                      group_m, (int)units, sk_len, sa, per_row_a ? 1 : 0, sb,
                                       per_col_b ? 1 : 0, out, acc_out, split_acc, slab_count,
                                       status);
   if (le != cudaSuccess) return le;
@@ -1036,6 +1067,13 @@ GemmPlan plan_gemm_tc(int kind, int64_t M, int64_t N, int64_t K, int num_sms,
             tiles1 >= (int64_t)4 * num_sms)
                ? 1
                : 0;
+  // Stream-K (equal k-block runs per SM over all tiles, partial tiles summed
+  // like K splits) is built but never planned: measured on GB300 it was
+  // slower for every g_w shape here -- ViT-B qkv 51.9 us against 39.6 us
+  // unsplit on 108 of 152 SMs (each k-block took 0.74 us on 152 SMs against
+  // 0.40 us on 108: the operand delivery to the SMs, not the idle SMs,
+  // bounds that GEMM), ViT-B fc2 56.5 against 39.6, ResNet-50 im2col 63.6
+  // against 58.0 with 4 K splits.
   return p;
 }
 
@@ -1051,7 +1089,8 @@ cudaError_t launch_gemm_tc(int kind, const void* A, int64_t lda, const void* B,
   if ((plan.bn != 96 && plan.bn != 128 && plan.bn != 256) ||
       (plan.splits > 1 && kind == 0) || (per_col_b && kind == 0) ||
       (plan.pair && plan.bn == 96) || (raw & ~(kRawA | kRawB)) || (raw && kind != 1) ||
-      (raw && K <= 0))
+      (raw && K <= 0) ||
+      (plan.stream_k && (kind != 1 || plan.pair || plan.splits > 1)))
     return cudaErrorInvalidValue;
   // int8 operands: TMA rows of 16-byte multiples from a 16-byte aligned base
   auto i8_ok = [](const void* p, int64_t ld) {
@@ -1074,7 +1113,7 @@ cudaError_t launch_gemm_tc(int kind, const void* A, int64_t lda, const void* B,
   if (acc_out && !make_out_map(&macc, acc_out, true, M, N)) return cudaErrorInvalidValue;
   int32_t* split_acc = nullptr;
   unsigned int* slab_count = nullptr;
-  if (plan.splits > 1) {
+  if (plan.splits > 1 || plan.stream_k) {
     split_acc = static_cast<int32_t*>(split_ws);
     if (!make_out_map(&msplit, split_acc, true, M, N)) return cudaErrorInvalidValue;
     slab_count = reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(split_ws) +
@@ -1092,7 +1131,8 @@ cudaError_t launch_gemm_tc(int kind, const void* A, int64_t lda, const void* B,
 #define TC(KIND, BN, PAIR, CVT)                                                             \
   launch_tc<KIND, BN, PAIR, CVT>(ma, mb, mo, macc, msplit, M, N, plan.num_kb, plan.chunk_kb,   \
                                  plan.splits, sms, sa, per_row_a, sb, per_col_b, out,         \
-                                 acc_out, split_acc, slab_count, status, st)
+                                 acc_out, split_acc, slab_count, status, st,                  \
+                                 plan.stream_k != 0)
 #define TC_BN(KIND, PAIR, CVT)                                                    \
   (plan.bn == 256 ? TC(KIND, 256, PAIR, CVT)                                      \
                   : (PAIR || plan.bn == 128) ? TC(KIND, 128, PAIR, CVT) : TC(KIND, 96, false, CVT))

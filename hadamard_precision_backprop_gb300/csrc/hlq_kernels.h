@@ -133,6 +133,8 @@ struct GemmPlan {
   int num_kb = 0;    // k-blocks of 128 bytes
   int chunk_kb = 0;  // k-blocks per exact fp32 accumulation chunk
   int pair = 0;      // 1: a CTA pair per 256-row tile (tcgen05 cta_group::2)
+  int stream_k = 0;  // 1: equal k-block runs per SM over all tiles (kind 1,
+                     // unsplit, no pairs; partial tiles summed like K splits)
 };
 GemmPlan plan_gemm_tc(int kind, int64_t M, int64_t N, int64_t K, int num_sms,
                       int max_splits);

@@ -193,6 +193,16 @@ hlq_status hlq_set_gw_operands(int mode);
 int hlq_get_gw_operands(void);
 
 /*
+ * For per-kernel timing: with on = 1, hlq_linear_backward (both readers of
+ * g_y) and hlq_layer_step run all their branches on the caller's stream,
+ * one after the other, instead of forking the g_w branch and the HQ of w to
+ * library streams; the kernels and their results are the same.  on = 0
+ * restores the default.  A process-wide setting read when a call enqueues
+ * its work; on outside {0, 1} is HLQ_ERR_INVALID_ARG.
+ */
+hlq_status hlq_debug_serialize_branches(int on);
+
+/*
  * The whole backward pass of the layer: g_x exactly as hlq_linear_backward_gx
  * and g_w exactly as hlq_linear_backward_gw, with the independent branches
  * overlapped on the GPU.  The g_w branch and the HQ of w run on auxiliary
@@ -323,7 +333,9 @@ hlq_status hlq_debug_reference_gemm(int kind, const void *d_a, const void *d_b,
  * lda / ldb: row strides in elements (16-byte multiples).  bn: tile width
  * 96, 128 or 256 (0 = the library's choice); splits: K split count (0 = the
  * library's choice; > 1 needs d_ws of hlq_debug_tc_gemm_ws_bytes(M, N);
- * kind 0 runs unsplit); pair: 1 = a CTA pair per 256-row tile (tcgen05
+ * -1 = stream-K: one CTA per SM, each taking an equal run of the tiles'
+ * k-blocks, the partial tiles summed exactly in d_ws; kinds 1-3 only, no
+ * pairs; kind 0 runs unsplit); pair: 1 = a CTA pair per 256-row tile (tcgen05
  * cta_group::2; tile widths 128 and 256), 0 = one CTA per 128-row tile,
  * -1 = the library's choice.  M, N, K multiples of 16.  An unsupported
  * plan is HLQ_ERR_INVALID_ARG.
@@ -347,7 +359,8 @@ hlq_status hlq_debug_wait_timeout(uint64_t limit_ns, int32_t *d_result, void *st
  * The plans the layer entries choose for the two GEMMs of a layer on a GPU
  * with `sms` SMs (host computation only, nothing is launched): tile width
  * and K split of the g_x GEMM (E4M3, M = T, N = Cin, K = Cout) and of the
- * g_w GEMM (bf16, M = Cout, N = Cin, K = T*rank/16), and whether the g_w
+ * g_w GEMM (fp16, M = Cout, N = Cin, K = T*rank/16; split -1: stream-K, as
+ * for hlq_debug_tc_gemm), and whether the g_w
  * GEMM is ordered after the g_x GEMM (1: each has at least one unit per SM,
  * so running them side by side would only delay the later one), and
  * whether each GEMM runs on CTA pairs (1) or one CTA per tile (0).

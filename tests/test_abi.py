@@ -142,6 +142,9 @@ def test_tc_gemm_plan_validation(L):
     assert call(kind=4) == 1
     assert call(kind=-1) == 1
     assert call(splits=65) == 1
+    assert call(splits=-2) == 1
+    assert call(kind=0, splits=-1) == 1       # stream-K is for the fp16 GEMM
+    assert call(splits=-1, pair=1) == 1       # stream-K takes one CTA per tile
     assert call(kind=0, splits=2) == 1        # the E4M3 GEMM runs unsplit
     assert call(bn=192) == 1
     assert call(M=200) == 2
@@ -406,3 +409,10 @@ def test_gw_operand_mode_is_validated(L):
         with pytest.raises(hlq.HLQError):
             hlq.hlq_set_gw_operands(bad)
         assert hlq.hlq_get_gw_operands() == hlq.GW_AUTO
+
+
+def test_serialize_branches_switch_is_validated(L):
+    assert L.hlq_debug_serialize_branches(1) == 0
+    assert L.hlq_debug_serialize_branches(0) == 0
+    assert L.hlq_debug_serialize_branches(2) == 1
+    assert L.hlq_debug_serialize_branches(-1) == 1

@@ -68,7 +68,9 @@ PLANS = ([(kind, qmax, bn, 1, 0) for kind, qmax in _KINDS for bn in (128, 256, 9
          + [(kind, 127, bn, splits, 0) for kind in (1, 2, 3)
             for bn, splits in ((128, 3), (256, 2), (96, 2))]
          + [(kind, 127, bn, splits, 1) for kind in (1, 2, 3)
-            for bn, splits in ((128, 3), (256, 2))])
+            for bn, splits in ((128, 3), (256, 2))]
+         # stream-K: equal k-block runs per SM, partial tiles summed exactly
+         + [(kind, 127, bn, -1, 0) for kind in (1, 2, 3) for bn in (128, 256, 96)])
 
 
 @pytest.mark.parametrize("kind,qmax,bn,splits,pair", PLANS)
@@ -84,6 +86,22 @@ def test_tc_gemm_exact(kind, qmax, M, N, K, bn, splits, pair):
     ref = hlq.hlq_debug_reference_gemm(torch.from_numpy(A.astype(np.int8)).cuda(),
                                        torch.from_numpy(B.astype(np.int8)).cuda())
     np.testing.assert_array_equal(ref.cpu().numpy(), got)
+
+
+def test_tc_gemm_stream_k_tile_boundaries():
+    """Stream-K runs that start and end inside tiles, several runs per tile
+    and several tiles per run: one 128 x 128 tile of 300 k-blocks shared by
+    every SM, and 3 x 5 tiles of 37 k-blocks whose runs cross tile edges."""
+    for M, N, K in [(128, 128, 300 * 64), (384, 640, 37 * 64), (400, 272, 2064)]:
+        rng = np.random.default_rng(M + N + K)
+        A = rng.integers(-127, 128, (M, K))
+        B = rng.integers(-127, 128, (N, K))
+        want = A.astype(np.int64) @ B.astype(np.int64).T
+        for kind in (1, 2):
+            for bn in (128, 256):
+                got = run(kind, A, B, bn, -1, 0).cpu().numpy()
+                np.testing.assert_array_equal(got.astype(np.int64), want)
+    assert hlq.hlq_read_device_status() == 0
 
 
 def test_tc_gemm_library_plan_exact():
@@ -110,7 +128,7 @@ def test_tc_gemm_f16_worst_case_magnitude(kind):
     A = np.full((M, K), 127, np.int64)
     A[1::2] = -127
     B = np.full((N, K), 127, np.int64)
-    for splits, pair in ((1, 0), (2, 0), (5, 0), (1, 1), (3, 1)):
+    for splits, pair in ((1, 0), (2, 0), (5, 0), (1, 1), (3, 1), (-1, 0)):
         got = run(kind, A, B, 128, splits, pair).cpu().numpy()
         assert got[0, 0] == 16129 * K and got[1, 0] == -16129 * K
         assert np.all(got[0::2] == 16129 * K) and np.all(got[1::2] == -16129 * K)

@@ -88,3 +88,25 @@ def test_layer_step_in_a_graph():
     torch.cuda.synchronize()
     for a, b in zip(ref, outs):
         assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("fused_gy", [False, True])
+def test_serialized_branches_give_the_same_bits(fused_gy):
+    """hlq_debug_serialize_branches runs the same kernels on one stream (the
+    bench's per-kernel trace): every output equals the forked run's."""
+    wl, inp = _inputs(3, 512, 528, 400)
+    x, gy, w = (to_dev(inp, n, "bf16") for n in ("x", "g_y", "w"))
+    ref_step = hlq.hlq_layer_step(x, gy, w, seed=5)
+    ref_bwd = hlq.hlq_linear_backward(gy, w, ref_step[2], ref_step[3], seed=5,
+                                      fused_gy=fused_gy)
+    hlq.hlq_debug_serialize_branches(True)
+    try:
+        got_step = hlq.hlq_layer_step(x, gy, w, seed=5)
+        got_bwd = hlq.hlq_linear_backward(gy, w, ref_step[2], ref_step[3], seed=5,
+                                          fused_gy=fused_gy)
+    finally:
+        hlq.hlq_debug_serialize_branches(False)
+    torch.cuda.synchronize()
+    for a, b in zip(ref_step + ref_bwd, got_step + got_bwd):
+        assert torch.equal(a, b)
+    assert hlq.hlq_read_device_status(clear=True) == 0
