@@ -790,6 +790,33 @@ def measure_workload(args, wl, dev, dist, headline):
                          "host_enqueue_us": statistics.median(enqueue_ms) * 1e3,
                          "host_enqueue_max_us": max(enqueue_ms) * 1e3,
                          "steps_us": [round(t * 1e3, 1) for t in e2e_ms]}
+    # the copies alone, the floor of that step: the same bytes with plain
+    # pinned-memory copies, host -> device and device -> host on two streams
+    # at once (the inputs are overwritten with their own values)
+    cin_s, cout_s = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def copies_only():
+        cin_s.wait_stream(stream)
+        cout_s.wait_stream(stream)
+        with torch.cuda.stream(cin_s):
+            for d, h in ((w, h_w), (gy, h_gy), (x, h_x)):
+                d.copy_(h, non_blocking=True)
+        with torch.cuda.stream(cout_s):
+            h_gx.copy_(gx, non_blocking=True)
+            h_gw.copy_(gw, non_blocking=True)
+        stream.wait_stream(cin_s)
+        stream.wait_stream(cout_s)
+
+    floor_ms = []
+    for i in range(2 + 5):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        copies_only()
+        b.record(stream)
+        b.synchronize()
+        if i >= 2:
+            floor_ms.append(a.elapsed_time(b))
+    res["e2e_spread"]["copy_floor_us"] = statistics.median(floor_ms) * 1e3
     res["e2e_bytes"] = ((x.numel() + gy.numel() + w.numel()) * e,
                         (gx.numel() + gw.numel()) * 4)
     res["acbp_stored_bytes"] = acbp_bytes(T, Cin, wl.rank, e)
