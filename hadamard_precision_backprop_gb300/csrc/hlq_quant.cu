@@ -889,7 +889,7 @@ template <bool kBf16, int kMode, int kOut, int kR>
 __global__ void __launch_bounds__(128 * kTmaBlocks) hla_tma_kernel(
     const __grid_constant__ CUtensorMap tm, int64_t T, int64_t C,
     unsigned int* __restrict__ amax_slot, void* __restrict__ out, int64_t out_ld,
-    float* __restrict__ scale, unsigned int* __restrict__ status, int per_col) {
+    float* __restrict__ scale, unsigned int* __restrict__ status, int per_col, int tok_fast) {
   constexpr int kStage = 16 * kTmaCols * (kBf16 ? 2 : 4);
   using F = ColFmt<kOut>;
   constexpr int kChunk = kR * F::kNum / F::kDen;  // code bytes / block / column
@@ -903,9 +903,12 @@ __global__ void __launch_bounds__(128 * kTmaBlocks) hla_tma_kernel(
   // thread (t, i): column pair t of block i of the tile
   const int t = threadIdx.x & 127, i = threadIdx.x >> 7;
   const int64_t n_blk = T >> 4;
-  const int64_t b0 = (int64_t)blockIdx.y * kTmaBlocks;
+  // tok_fast: token blocks along grid x, so that CTAs launched one after the
+  // other write neighbouring pieces of the same code rows (whole 32-byte
+  // sectors form in L2 before they are written back)
+  const int64_t b0 = (int64_t)(tok_fast ? blockIdx.x : blockIdx.y) * kTmaBlocks;
   const int nb = (int)imin64(kTmaBlocks, n_blk - b0);
-  const int64_t col0 = (int64_t)blockIdx.x * kTmaCols;
+  const int64_t col0 = (int64_t)(tok_fast ? blockIdx.y : blockIdx.x) * kTmaCols;
   pdl_trigger();
   if (threadIdx.x == 0) {
     for (int k = 0; k < kTmaBlocks; ++k) mbar_init(&full[k], 1);
@@ -1858,9 +1861,12 @@ static cudaError_t launch_hla_r(const void* src, int64_t T, int64_t C,
                         kTmaBlocks * 8 + 16;
     cudaError_t e = ensure_smem_limit<hla_tma_kernel<B, M, O, R>>(smem);
     if (e != cudaSuccess) return e;
-    dim3 grid(grid1(C, kTmaCols), grid1(T / 16, kTmaBlocks));
+    const int64_t col_tiles = grid1(C, kTmaCols), tok_tiles = grid1(T / 16, kTmaBlocks);
+    const int tok_fast = col_tiles <= 65535 ? 1 : 0;  // grid y limit
+    const dim3 grid = tok_fast ? dim3((unsigned)tok_tiles, (unsigned)col_tiles)
+                               : dim3((unsigned)col_tiles, (unsigned)tok_tiles);
     launch_pdl(hla_tma_kernel<B, M, O, R>, grid, dim3(128 * kTmaBlocks), smem, st, tm, T,
-               C, amax_slot, out, out_ld, scale, status, per_col);
+               C, amax_slot, out, out_ld, scale, status, per_col, tok_fast);
     return cudaGetLastError();
   }
   const size_t smem = M == kAmax ? 0 : (size_t)kHlaCols * (kHlaBlocks + 1) * chunk;
