@@ -149,10 +149,12 @@ KERNEL_ROWS = {
     "gemm_gx_tc": "a4",
     "hla_gy_amax": "a5", "hla_gy_quant": "a5",
     "widen_xbar": "a6", "gemm_gw_tc": "a6",
+    "gy_fused_amax": "a2+a5", "gy_fused_quant": "a2+a5",
 }
 ROW_NAMES = {"a1": "ACBP compression of x", "a2": "HQ of g_y", "a3": "HQ of w",
              "a4": "g_x GEMM + dequant", "a5": "HLA of g_y",
-             "a6": "g_w GEMM + dequant"}
+             "a6": "g_w GEMM + dequant",
+             "a2+a5": "HQ and HLA of g_y by one fused reader (per-tensor g_y scale)"}
 
 
 def algorithmic(name, wl, xbar_bits=8):
@@ -175,6 +177,8 @@ def algorithmic(name, wl, xbar_bits=8):
         "hla_gy_amax": ("hbm", 0),
         "hla_gy_quant": ("hbm", s["gy"] + s["qg"] + s["s_g"]),
         "widen_xbar": ("hbm", 0),
+        "gy_fused_amax": ("hbm", 0),
+        "gy_fused_quant": ("hbm", s["gy"] + s["qy"] + s["s_gy"] + s["qg"] + s["s_g"]),
         "gemm_gx_tc": ("ops", s["ops_gx"], s["qy"] + s["qw"] + s["gx"]),
         "gemm_gw_tc": ("ops", s["ops_gw"], s["qg"] + s["xb"] + s["gw"]),
     }
@@ -188,6 +192,7 @@ ROW_WORK = {  # algorithmic work of each step of the method (same sizes)
     "a4": lambda s: ("ops", s["ops_gx"], s["qy"] + s["qw"] + s["gx"]),
     "a5": lambda s: ("hbm", s["gy"] + s["qg"] + s["s_g"]),
     "a6": lambda s: ("ops", s["ops_gw"], s["qg"] + s["xb"] + s["gw"]),
+    "a2+a5": lambda s: ("hbm", s["gy"] + s["qy"] + s["s_gy"] + s["qg"] + s["s_g"]),
 }
 
 

@@ -79,3 +79,17 @@ def test_default_workload_is_the_largest_layer():
     b = _bench()
     big = max(workloads.WORKLOADS, key=lambda w: w.T * w.Cin * w.Cout)
     assert b.DEFAULT_WORKLOAD is big and b.parse_args([]).workload == big.name
+
+
+def test_fused_reader_credited_once_with_both_codes():
+    """The fused reader of g_y (per-tensor g_y scale) reads g_y once for both
+    quantizers: its codes pass carries one read plus the int4 HQ codes and the
+    int8 HLA codes, its maxima pass nothing; its row combines a2 and a5."""
+    b = _bench()
+    wl = workloads.WORKLOADS[4]        # ResNet-50 im2col, per-tensor g_y
+    T, Cout, Tp = wl.T, wl.Cout, wl.Tp
+    assert b.algorithmic("gy_fused_amax", wl)[1] == 0
+    assert b.algorithmic("gy_fused_quant", wl)[1] == T * Cout * 2 + T * Cout // 2 + 4 + Cout * Tp + 4
+    kernels, rows = b.kernel_table([("gy_fused_amax", 0.02), ("gy_fused_quant", 0.04)], wl, PEAKS)
+    assert rows["a2+a5"]["kernels"] == ["gy_fused_amax", "gy_fused_quant"]
+    assert "a2" not in rows and "a5" not in rows
