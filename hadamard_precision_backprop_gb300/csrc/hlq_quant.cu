@@ -868,15 +868,20 @@ __global__ void __launch_bounds__(256) hla_rows_kernel(
 // reading their 16 values per column out of shared memory (one 32-bit word
 // per lane per row: conflict-free).  Thread (t, i) takes column pair t of
 // the kTmaLoop consecutive blocks i * kTmaLoop .. (its code pieces of one
-// row follow each other in memory).  Two blocks per thread, two TMA tiles in
-// flight per CTA: Llama down_proj compression 118 + 172 -> 103 + 154 us
-// (maximum and quant passes), step 1761 -> 1715 us; ResNet-50 im2col step
-// 366 -> 349 us; four blocks: 1713, 352 us, and ViT-B qkv slower.
+// row follow each other in memory).  Blocks per thread, measured on Llama
+// down_proj (maximum pass, quant pass of the compression): one 118 + 172 us,
+// two 103 + 154 us, four 97 + 154 us; ResNet-50 im2col 63 + 88, 56 + 78,
+// 54 + 80 us; ViT-B qkv quant 14.2, 14.5, 15.9 us: up to four for the
+// maximum pass and two for the quant pass, fewer when the grid would have
+// less than two CTAs per SM (a 256-token layer: 17 -> 31 us of compression
+// with four).
 // ---------------------------------------------------------------------------
 constexpr int kTmaCols = 256;
-constexpr int kTmaBlocks = 1;                     // thread groups of 128
-constexpr int kTmaLoop = 2;                       // consecutive blocks per thread
-constexpr int kTmaTiles = kTmaBlocks * kTmaLoop;  // blocks (TMA tiles) per CTA
+constexpr int kTmaBlocks = 1;  // thread groups of 128
+template <int kMode>
+struct TmaLoop {
+  static constexpr int kMaxLoop = kMode == kAmax ? 4 : 2;  // consecutive blocks per thread
+};
 
 template <bool kBf16>
 __device__ __forceinline__ void read_pair_col(const uint8_t* stage, int t,
@@ -896,7 +901,8 @@ template <bool kBf16, int kMode, int kOut, int kR>
 __global__ void __launch_bounds__(128 * kTmaBlocks) hla_tma_kernel(
     const __grid_constant__ CUtensorMap tm, int64_t T, int64_t C,
     unsigned int* __restrict__ amax_slot, void* __restrict__ out, int64_t out_ld,
-    float* __restrict__ scale, unsigned int* __restrict__ status, int per_col, int tok_fast) {
+    float* __restrict__ scale, unsigned int* __restrict__ status, int per_col, int tok_fast,
+    int tma_loop) {
   constexpr int kStage = 16 * kTmaCols * (kBf16 ? 2 : 4);
   using F = ColFmt<kOut>;
   constexpr int kChunk = kR * F::kNum / F::kDen;  // code bytes / block / column
@@ -904,6 +910,9 @@ __global__ void __launch_bounds__(128 * kTmaBlocks) hla_tma_kernel(
   extern __shared__ __align__(128) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  // tma_loop (1 .. kMaxLoop) consecutive blocks per thread, as many tiles
+  // per CTA (the launch sized the shared memory for them)
+  const int kTmaLoop = tma_loop, kTmaTiles = kTmaBlocks * tma_loop;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kTmaTiles * kStage);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(full + kTmaTiles);
 
@@ -1865,6 +1874,19 @@ static cudaError_t launch_hla_r(const void* src, int64_t T, int64_t C,
                         (out_ld * F::kNum / F::kDen) % (chunk >= 16 ? 16 : chunk) == 0;
   CUtensorMap tm;
   if (chunk_ok && make_tile_map_2d(&tm, src, B, T, C, kTmaCols, 16)) {
+    // blocks per thread: the mode's maximum, halved while the grid would
+    // have fewer than two CTAs per SM
+    static int sms_of[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!sms_of[dev] &&
+        cudaDeviceGetAttribute(&sms_of[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return cudaErrorInvalidDevice;
+    int loop = TmaLoop<M>::kMaxLoop;
+    while (loop > 1 && (int64_t)grid1(T / 16, kTmaBlocks * loop) * grid1(C, kTmaCols) <
+                           2 * (int64_t)sms_of[dev])
+      loop /= 2;
+    const int kTmaTiles = kTmaBlocks * loop;
     const size_t smem = 128 + (size_t)kTmaTiles * 16 * kTmaCols * (B ? 2 : 4) +
                         kTmaTiles * 8 + 16;
     cudaError_t e = ensure_smem_limit<hla_tma_kernel<B, M, O, R>>(smem);
@@ -1874,7 +1896,7 @@ static cudaError_t launch_hla_r(const void* src, int64_t T, int64_t C,
     const dim3 grid = tok_fast ? dim3((unsigned)tok_tiles, (unsigned)col_tiles)
                                : dim3((unsigned)col_tiles, (unsigned)tok_tiles);
     launch_pdl(hla_tma_kernel<B, M, O, R>, grid, dim3(128 * kTmaBlocks), smem, st, tm, T,
-               C, amax_slot, out, out_ld, scale, status, per_col, tok_fast);
+               C, amax_slot, out, out_ld, scale, status, per_col, tok_fast, loop);
     return cudaGetLastError();
   }
   const size_t smem = M == kAmax ? 0 : (size_t)kHlaCols * (kHlaBlocks + 1) * chunk;
