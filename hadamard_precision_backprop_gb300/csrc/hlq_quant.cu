@@ -1127,116 +1127,139 @@ __device__ __forceinline__ void read_row_blocks(const uint8_t* stage, int row, i
   }
 }
 
+constexpr int kFusedTiles = 2;  // 16-token tiles per CTA of the fused reader
+
 template <bool kBf16, int kMode, bool kPerToken, int kR>
 __global__ void __launch_bounds__(128) gy_fused_kernel(
     const __grid_constant__ CUtensorMap tm, int64_t T, int64_t C,
     unsigned int* __restrict__ hq_amax, unsigned int* __restrict__ hla_amax,
     uint8_t* __restrict__ qy, float* __restrict__ sgy, void* __restrict__ qg,
     int64_t hla_ld, float* __restrict__ sg, int rnd, const PhiloxKeys keys,
-    unsigned int* __restrict__ status) {
+    unsigned int* __restrict__ status, int tiles) {
+  // tiles (1 .. 2): consecutive 16-token tiles of the same 256 columns per
+  // CTA, all loaded at once, processed in order
   constexpr int kStage = 16 * kTmaCols * (kBf16 ? 2 : 4);
   using F = ColFmt<kColF16>;
   constexpr int kChunk = kR * 2;  // fp16 code bytes per block and column
   extern __shared__ __align__(128) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStage);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(full + 1);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + tiles * kStage);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(full + tiles);
   __shared__ float partial[2][4];
 
   const int t = threadIdx.x;
   const int64_t n_cc = (C + kTmaCols - 1) / kTmaCols;
+  const int64_t n_blk = T >> 4;
   const int64_t u = blockIdx.x;
-  const int64_t col0 = (u % n_cc) * kTmaCols, b = u / n_cc;
+  const int64_t col0 = (u % n_cc) * kTmaCols, b0 = (u / n_cc) * tiles;
+  const int nb = (int)imin64(tiles, n_blk - b0);
   pdl_trigger();
   if (t == 0) {
-    mbar_init(full, 1);
+    for (int k = 0; k < tiles; ++k) mbar_init(&full[k], 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   pdl_wait();  // g_y and the amax slots come from earlier work
   if (t == 0) {
-    mbar_expect_tx(full, kStage);
-    tma_load_2d(smem, &tm, full, (int)col0, (int)(16 * b));
+    for (int k = 0; k < nb; ++k) {
+      mbar_expect_tx(&full[k], kStage);
+      tma_load_2d(smem + k * kStage, &tm, &full[k], (int)col0, (int)(16 * (b0 + k)));
+    }
   }
   __syncthreads();
-  // scales of the quant pass
   const int hq_row = t >> 3;                  // 0..15
-  const int64_t tok = 16 * b + hq_row;
   const int x0 = 32 * (t & 7);                // first column of the pair of blocks
-  float s_hla = 0.0f, s_hq = 0.0f;
-  if (kMode == kQuant) {
-    s_hla = __fdiv_rn(__uint_as_float(ld_dep_u32(hla_amax)), F::kQmax);
-    s_hq = __fdiv_rn(__uint_as_float(ld_dep_u32(kPerToken ? hq_amax + tok : hq_amax)), 7.0f);
-  }
-  const bool ok = mbar_wait(full, 0u, abort_flag, status);
+  float s_hla = 0.0f;
+  if (kMode == kQuant) s_hla = __fdiv_rn(__uint_as_float(ld_dep_u32(hla_amax)), F::kQmax);
   float am_hla = 0.0f, am_hq = 0.0f;
-  // ---- HLA: column pair t ----
   const int64_t c0 = col0 + 2 * t;
-  if (ok && c0 < C) {
-    RawPairCol<kBf16> cur;
-    read_pair_col<kBf16>(smem, t, cur);
-    int tier[2];
-    uint32_t emax[2];
-    pair_tiers<kBf16>(cur, tier, emax, status);
-#pragma unroll
-    for (int c = 0; c < 2; ++c) {
-      float coef[kR];
-      hla_pair_col_coefs<kBf16, kR>(cur, c, tier[c], emax[c], coef);
-      if (kMode == kAmax) {
-#pragma unroll
-        for (int k = 0; k < kR; ++k) am_hla = fmaxf(am_hla, fabsf(coef[k]));
-      } else {
-        uint32_t p[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-#pragma unroll
-        for (int k = 0; k < kR; ++k)
-          pack_code<kColF16>(p, k, quant_rne_f(coef[k], s_hla, F::kQmax));
-        store_chunk(static_cast<uint8_t*>(qg) + ((c0 + c) * hla_ld + b * kR) * 2, p, kChunk);
-      }
-    }
-  }
-  // ---- HQ: row hq_row, blocks at columns x0 and x0 + 16 of the tile ----
   const int64_t cb = col0 + x0;
   const bool blk_ok[2] = {cb < C, cb + 16 < C};
-  if (ok && blk_ok[0]) {
-    RawPairCol<kBf16> cur;
-    read_row_blocks<kBf16>(smem, hq_row, x0, cur);
-    int tier[2];
-    uint32_t emax[2];
-    pair_tiers<kBf16>(cur, tier, emax, status);
-    float v[2][16];
-    unpack_pair_col<kBf16>(cur, v);
-    column_butterfly<kBf16>(v[0], tier[0], emax[0], 16, true);
-    column_butterfly<kBf16>(v[1], tier[1], emax[1], 16, true);
-    if (kMode == kAmax) {
+  bool live = true;
+#pragma unroll 1
+  for (int l = 0; l < nb && live; ++l) {
+    const int64_t b = b0 + l;
+    const int64_t tok = 16 * b + hq_row;
+    float s_hq = 0.0f;
+    if (kMode == kQuant)
+      s_hq = __fdiv_rn(__uint_as_float(ld_dep_u32(kPerToken ? hq_amax + tok : hq_amax)), 7.0f);
+    live = mbar_wait(&full[l], 0u, abort_flag, status);
+    const uint8_t* stage = smem + l * kStage;
+    float am_row = 0.0f;  // this tile's HQ maximum of the thread's row part
+    // ---- HLA: column pair t ----
+    if (live && c0 < C) {
+      RawPairCol<kBf16> cur;
+      read_pair_col<kBf16>(stage, t, cur);
+      int tier[2];
+      uint32_t emax[2];
+      pair_tiers<kBf16>(cur, tier, emax, status);
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        am_hq = fmaxf(am_hq, fabsf(v[0][i]));
-        if (blk_ok[1]) am_hq = fmaxf(am_hq, fabsf(v[1][i]));
-      }
-    } else {
-      const int64_t e = tok * C + cb;
-      quantize_octet(v[0], s_hq, rnd, keys, 0u, e, 0, qy);
-      quantize_octet(v[0] + 8, s_hq, rnd, keys, 0u, e + 8, 0, qy);
-      if (blk_ok[1]) {
-        quantize_octet(v[1], s_hq, rnd, keys, 0u, e + 16, 0, qy);
-        quantize_octet(v[1] + 8, s_hq, rnd, keys, 0u, e + 24, 0, qy);
+      for (int c = 0; c < 2; ++c) {
+        float coef[kR];
+        hla_pair_col_coefs<kBf16, kR>(cur, c, tier[c], emax[c], coef);
+        if (kMode == kAmax) {
+#pragma unroll
+          for (int k = 0; k < kR; ++k) am_hla = fmaxf(am_hla, fabsf(coef[k]));
+        } else {
+          uint32_t p[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+#pragma unroll
+          for (int k = 0; k < kR; ++k)
+            pack_code<kColF16>(p, k, quant_rne_f(coef[k], s_hla, F::kQmax));
+          store_chunk(static_cast<uint8_t*>(qg) + ((c0 + c) * hla_ld + b * kR) * 2, p, kChunk);
+        }
       }
     }
+    // ---- HQ: row hq_row, blocks at columns x0 and x0 + 16 of the tile ----
+    if (live && blk_ok[0]) {
+      RawPairCol<kBf16> cur;
+      read_row_blocks<kBf16>(stage, hq_row, x0, cur);
+      int tier[2];
+      uint32_t emax[2];
+      pair_tiers<kBf16>(cur, tier, emax, status);
+      float v[2][16];
+      unpack_pair_col<kBf16>(cur, v);
+      column_butterfly<kBf16>(v[0], tier[0], emax[0], 16, true);
+      column_butterfly<kBf16>(v[1], tier[1], emax[1], 16, true);
+      if (kMode == kAmax) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          am_row = fmaxf(am_row, fabsf(v[0][i]));
+          if (blk_ok[1]) am_row = fmaxf(am_row, fabsf(v[1][i]));
+        }
+      } else {
+        const int64_t e = tok * C + cb;
+        quantize_octet(v[0], s_hq, rnd, keys, 0u, e, 0, qy);
+        quantize_octet(v[0] + 8, s_hq, rnd, keys, 0u, e + 8, 0, qy);
+        if (blk_ok[1]) {
+          quantize_octet(v[1], s_hq, rnd, keys, 0u, e + 16, 0, qy);
+          quantize_octet(v[1] + 8, s_hq, rnd, keys, 0u, e + 24, 0, qy);
+        }
+      }
+    }
+    if (kMode == kAmax) {
+      if (kPerToken) {  // the 8 threads of a row are consecutive lanes
+        am_row = fmaxf(am_row, __shfl_xor_sync(0xffffffffu, am_row, 1));
+        am_row = fmaxf(am_row, __shfl_xor_sync(0xffffffffu, am_row, 2));
+        am_row = fmaxf(am_row, __shfl_xor_sync(0xffffffffu, am_row, 4));
+        if ((t & 7) == 0 && tok < T) atomic_max_nonneg(hq_amax + tok, am_row);
+      } else {
+        am_hq = fmaxf(am_hq, am_row);
+      }
+    } else if (kPerToken && col0 == 0 && (t & 7) == 0 && tok < T) {
+      sgy[tok] = s_hq;
+    }
+    live = __all_sync(0xffffffffu, live);  // warp-uniform for the shuffles above
   }
-  if (t == 0 && *abort_flag) {  // let the copy land before exit
-    const unsigned long long t0 = now_ns();
-    while (!mbar_test(full, 0u) && now_ns() - t0 < kWaitNs) {
+  if (t == 0 && *abort_flag) {  // let the copies land before exit
+    for (int k = 0; k < nb; ++k) {
+      const unsigned long long t0 = now_ns();
+      while (!mbar_test(&full[k], 0u) && now_ns() - t0 < kWaitNs) {
+      }
     }
   }
   if (kMode == kAmax) {
-    if (kPerToken) {  // the 8 threads of a row are consecutive lanes
-      am_hq = fmaxf(am_hq, __shfl_xor_sync(0xffffffffu, am_hq, 1));
-      am_hq = fmaxf(am_hq, __shfl_xor_sync(0xffffffffu, am_hq, 2));
-      am_hq = fmaxf(am_hq, __shfl_xor_sync(0xffffffffu, am_hq, 4));
-      if ((t & 7) == 0 && tok < T) atomic_max_nonneg(hq_amax + tok, am_hq);
-    }
     am_hla = warp_max(am_hla);
     if (!kPerToken) am_hq = warp_max(am_hq);
     if ((t & 31) == 0) {
@@ -1251,12 +1274,10 @@ __global__ void __launch_bounds__(128) gy_fused_kernel(
         atomic_max_nonneg(hq_amax, fmaxf(fmaxf(partial[1][0], partial[1][1]),
                                          fmaxf(partial[1][2], partial[1][3])));
     }
-  } else {
-    if (u == 0 && t == 0) {
-      sg[0] = s_hla;
-      if (!kPerToken) sgy[0] = s_hq;
-    }
-    if (kPerToken && col0 == 0 && (t & 7) == 0 && tok < T) sgy[tok] = s_hq;
+  } else if (u == 0 && t == 0) {
+    sg[0] = s_hla;
+    if (!kPerToken)
+      sgy[0] = __fdiv_rn(__uint_as_float(ld_dep_u32(hq_amax)), 7.0f);
   }
 }
 
@@ -1960,14 +1981,26 @@ cudaError_t launch_gy_fused(const void* gy, bool bf16, int64_t T, int64_t C, int
   if (T == 0 || C == 0) return cudaSuccess;
   CUtensorMap tm;
   if (!make_tile_map_2d(&tm, gy, bf16, T, C, kTmaCols, 16)) return cudaErrorInvalidValue;
-  const size_t smem = 128 + (size_t)16 * kTmaCols * (bf16 ? 2 : 4) + 8 + 16;
-  const int64_t tiles = (int64_t)grid1(C, kTmaCols) * (T / 16);
+  // two 16-token tiles per CTA, one when that would leave fewer than two CTAs
+  // per SM (as for the HLA kernel)
+  static int sms_of[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!sms_of[dev] &&
+      cudaDeviceGetAttribute(&sms_of[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return cudaErrorInvalidDevice;
+  const int64_t n_cc = grid1(C, kTmaCols);
+  int per_cta = kFusedTiles;
+  while (per_cta > 1 && n_cc * grid1(T / 16, per_cta) < 2 * (int64_t)sms_of[dev]) per_cta /= 2;
+  const size_t smem = 128 + (size_t)per_cta * (16 * kTmaCols * (bf16 ? 2 : 4) + 8) + 16;
+  const int64_t tiles = n_cc * grid1(T / 16, per_cta);
 #define GYF(B, M, P, R)                                                                  \
   do {                                                                                   \
     cudaError_t e = ensure_smem_limit<gy_fused_kernel<B, M, P, R>>(smem);                \
     if (e != cudaSuccess) return e;                                                      \
     launch_pdl(gy_fused_kernel<B, M, P, R>, dim3((unsigned)tiles), dim3(128), smem, st, tm, \
-               T, C, hq_amax, hla_amax, qy, sgy, qg, hla_ld, sg, rnd, philox_keys(seed), status);     \
+               T, C, hq_amax, hla_amax, qy, sgy, qg, hla_ld, sg, rnd, philox_keys(seed), status, \
+               per_cta);                                                                 \
   } while (0)
 #define GYF_R(B, M, P)                         \
   switch (rank) {                              \
