@@ -1,6 +1,7 @@
 // hlq_api.cu -- the C ABI of libhlq (declared in include/hlq.h): argument
 // validation, workspace layout and the launch sequence of each step.
 #include <cstdint>
+#include <atomic>
 #include <mutex>
 #include <cstring>
 #include <cuda_runtime.h>
@@ -99,12 +100,12 @@ cudaStream_t aux_stream(int which) {
 
 // hlq_debug_serialize_branches: every branch of the device entries on the
 // caller's stream, one after the other (for per-kernel timing).
-bool g_serial_branches = false;
+std::atomic<bool> g_serial_branches{false};
 
 // The stream a branch of a device entry runs on: a library stream forked
 // from the caller's, or the caller's own when branches are serialised.
-cudaStream_t branch_stream(int which, cudaStream_t caller) {
-  return g_serial_branches ? caller : aux_stream(which);
+cudaStream_t branch_stream(int which, cudaStream_t caller, bool serial) {
+  return serial ? caller : aux_stream(which);
 }
 
 constexpr size_t kAlign = 256;
@@ -375,7 +376,7 @@ hlq_status compress_launches(const void* x, bool bf16, int64_t T, int64_t Cin, i
 // The in-GEMM widening takes int8 x-bar whose rows are whole 16-byte runs
 // from a 16-byte aligned base; anything else goes through the widening
 // kernel.  The fused reader writes fp16 HLA codes (fused = true).
-int g_gw_operands = HLQ_GW_AUTO;
+std::atomic<int> g_gw_operands{HLQ_GW_AUTO};
 
 int gw_raw(int fmt, int64_t Tp, const void* xbar, bool fused) {
   // the default widens x-bar with its own kernel: measured on GB300, the
@@ -383,7 +384,7 @@ int gw_raw(int fmt, int64_t Tp, const void* xbar, bool fused) {
   // convert each stage before the MMA may read it) ran 1669 us at Llama
   // down_proj against 489 + 68 (widening kernel) us, and 62.6 against
   // 41.8 + 9.7 us at ViT-B qkv; both operands int8: 2214 and 73.7 us
-  int mode = g_gw_operands;
+  int mode = g_gw_operands.load();
   if (mode == HLQ_GW_AUTO) mode = HLQ_GW_WIDEN;
   if (mode == HLQ_GW_WIDEN || xbar_code_bits(fmt) != 8 || Tp % 16 != 0 || !aligned16(xbar))
     return 0;
@@ -658,8 +659,9 @@ hlq_status hlq_linear_backward(const void* d_gy, const void* d_w, const int8_t* 
   if (!aligned256(d_ws)) return HLQ_ERR_ALIGN;
   uint8_t* base = static_cast<uint8_t*>(d_ws);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaStream_t a = branch_stream(0, s), aw = branch_stream(1, s);
-  if (!g_serial_branches && (!a || !aw)) return HLQ_ERR_CUDA;  // (null: the legacy stream)
+  const bool serial = g_serial_branches.load();  // one reading per call
+  cudaStream_t a = branch_stream(0, s, serial), aw = branch_stream(1, s, serial);
+  if (!serial && (!a || !aw)) return HLQ_ERR_CUDA;  // (null: the legacy stream)
   // validate both branches before forking (nothing enqueued on failure)
   st = gw_impl(d_gy, dt, d_xbar, xbar_fmt, d_xbar_scale, T, Cin, Cout, block, rank, d_gw,
                base + gx_bytes, gw_bytes, nullptr, nullptr, nullptr, nullptr,
@@ -767,8 +769,9 @@ hlq_status hlq_layer_step(const void* d_x, const void* d_gy, const void* d_w, in
                           reinterpret_cast<unsigned int*>(base), s);
   unsigned int* status = device_status_ptr();
   if (!status) return HLQ_ERR_CUDA;
-  cudaStream_t a = branch_stream(0, s), aw = branch_stream(1, s);
-  if (!g_serial_branches && (!a || !aw)) return HLQ_ERR_CUDA;  // (null: the legacy stream)
+  const bool serial = g_serial_branches.load();  // one reading per call
+  cudaStream_t a = branch_stream(0, s, serial), aw = branch_stream(1, s, serial);
+  if (!serial && (!a || !aw)) return HLQ_ERR_CUDA;  // (null: the legacy stream)
   EventSet E;
   cudaEvent_t fork = E.make(), join = E.make(), gx_done = E.make();
   if (!fork || !join || !gx_done) return HLQ_ERR_CUDA;
@@ -948,8 +951,9 @@ static hlq_status fused_launches(const void* d_gy, const void* d_w, const void* 
   if (!status) return HLQ_ERR_CUDA;
   const int sms = device_sm_count();
   if (sms <= 0) return HLQ_ERR_CUDA;
-  cudaStream_t a = branch_stream(0, s), aw = branch_stream(1, s);
-  if (!g_serial_branches && (!a || !aw)) return HLQ_ERR_CUDA;  // (null: the legacy stream)
+  const bool serial = g_serial_branches.load();  // one reading per call
+  cudaStream_t a = branch_stream(0, s, serial), aw = branch_stream(1, s, serial);
+  if (!serial && (!a || !aw)) return HLQ_ERR_CUDA;  // (null: the legacy stream)
   const GxLayout GL = gx_layout(T, Cin, Cout);
   const GwLayout WL = gw_layout(T, Cin, Cout, rank);
   unsigned int* gx_amax = reinterpret_cast<unsigned int*>(gxb + GL.amax);
@@ -1464,15 +1468,15 @@ hlq_status hlq_debug_tc_gemm(int kind, const void* d_a, int64_t lda, const void*
 
 hlq_status hlq_set_gw_operands(int mode) {
   if (mode < HLQ_GW_AUTO || mode > HLQ_GW_INT8_BOTH) return HLQ_ERR_INVALID_ARG;
-  g_gw_operands = mode;
+  g_gw_operands.store(mode);
   return HLQ_OK;
 }
 
-int hlq_get_gw_operands(void) { return g_gw_operands; }
+int hlq_get_gw_operands(void) { return g_gw_operands.load(); }
 
 hlq_status hlq_debug_serialize_branches(int on) {
   if (on != 0 && on != 1) return HLQ_ERR_INVALID_ARG;
-  g_serial_branches = on != 0;
+  g_serial_branches.store(on != 0);
   return HLQ_OK;
 }
 
