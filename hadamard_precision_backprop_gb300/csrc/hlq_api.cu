@@ -11,10 +11,6 @@
 
 namespace hlq {
 
-// Device status word of this library (HLQ_DEV_* flags).  Host code reaches
-// it only through its device address (device_status_ptr).
-__device__ unsigned int g_status_word;
-
 namespace {
 
 constexpr int kMaxDevices = 64;
@@ -26,9 +22,9 @@ unsigned int* device_status_ptr() {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
     return nullptr;
   if (!g_status_ptr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
-    g_status_ptr[dev] = static_cast<unsigned int*>(p);
+    unsigned int* p = nullptr;
+    if (status_word_address(&p) != cudaSuccess) return nullptr;
+    g_status_ptr[dev] = p;
   }
   return g_status_ptr[dev];
 }

@@ -76,6 +76,10 @@ cudaError_t launch_gy_fused(const void* gy, bool bf16, int64_t T, int64_t C, int
 
 // One CTA waiting on an mbarrier that never completes, for limit_ns: sets
 // *result = 0 and raises HLQ_DEV_TIMEOUT in the status word.
+// Device address of the library's status word (HLQ_DEV_* flags) on the
+// current device; the word lives with the kernels that raise its flags.
+cudaError_t status_word_address(unsigned int** out);
+
 cudaError_t launch_wait_timeout_probe(unsigned long long limit_ns, int32_t* result,
                                       unsigned int* status, cudaStream_t st);
 

@@ -1738,6 +1738,17 @@ __global__ void decode_f16_kernel(const __half* __restrict__ in,
     out[i] = (int8_t)__half2int_rn(in[(i / cols) * ld + i % cols]);
 }
 
+// Device status word of this library (HLQ_DEV_* flags): every kernel that
+// can detect a device-side condition takes its address.
+__device__ unsigned int g_status_word;
+
+cudaError_t status_word_address(unsigned int** out) {
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_status_word);
+  *out = static_cast<unsigned int*>(p);
+  return e;
+}
+
 // ---------------------------------------------------------------------------
 // Host-side launchers.
 // ---------------------------------------------------------------------------
