@@ -674,32 +674,22 @@ hlq_status hlq_linear_backward(const void* d_gy, const void* d_w, const int8_t* 
                base, gx_bytes, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
                /*validate_only=*/true);
   if (st != HLQ_OK) return st;
-  cudaStream_t ah = branch_stream(4, s, serial);  // the HLA of g_y
-  if (!serial && !ah) return HLQ_ERR_CUDA;
-  EventSet E;
-  cudaEvent_t fork = E.make(), join = E.make(), gx_done = E.make(), hla_done = E.make();
-  if (!fork || !join || !gx_done || !hla_done) return HLQ_ERR_CUDA;
-  unsigned int* status = device_status_ptr();
-  if (!status) return HLQ_ERR_CUDA;
-  hlq_status r = HLQ_OK;
-  if (cudaEventRecord(fork, s) != cudaSuccess || cudaStreamWaitEvent(a, fork, 0) != cudaSuccess ||
-      cudaStreamWaitEvent(ah, fork, 0) != cudaSuccess)
-    r = HLQ_ERR_CUDA;
-  // the HLA of g_y on its own stream, beside the widening of x-bar and the
-  // g_x branch (as in hlq_layer_step); the g_w GEMM waits for it
-  const int64_t Tp = T / 16 * rank;
-  const int rw = gw_raw(xbar_fmt, Tp, d_xbar, false);
-  if (Cout * Cin > 0 && Tp > 0) {
-    uint8_t* gwb = base + gx_bytes;
-    const GwLayout WL = gw_layout(T, Cin, Cout, rank);
-    const bool qg_i8 = (rw & kRawA) != 0;
-    if (r == HLQ_OK)
-      r = hla_gy_launches(d_gy, dt == HLQ_BF16, T, Cout, rank,
-                          reinterpret_cast<unsigned int*>(gwb + WL.amax), gwb + WL.qg,
-                          qg_i8 ? WL.ld8 : WL.ld, reinterpret_cast<float*>(gwb + WL.sg), status,
-                          ah, qg_i8);
+  cudaEvent_t fork = nullptr, join = nullptr;
+  if (cudaEventCreateWithFlags(&fork, cudaEventDisableTiming) != cudaSuccess)
+    return HLQ_ERR_CUDA;
+  if (cudaEventCreateWithFlags(&join, cudaEventDisableTiming) != cudaSuccess) {
+    cudaEventDestroy(fork);
+    return HLQ_ERR_CUDA;
   }
-  if (cudaEventRecord(hla_done, ah) != cudaSuccess && r == HLQ_OK) r = HLQ_ERR_CUDA;
+  cudaEvent_t gx_done = nullptr;
+  if (cudaEventCreateWithFlags(&gx_done, cudaEventDisableTiming) != cudaSuccess) {
+    cudaEventDestroy(fork);
+    cudaEventDestroy(join);
+    return HLQ_ERR_CUDA;
+  }
+  hlq_status r = HLQ_OK;
+  if (cudaEventRecord(fork, s) != cudaSuccess || cudaStreamWaitEvent(a, fork, 0) != cudaSuccess)
+    r = HLQ_ERR_CUDA;
   if (r == HLQ_OK)  // g_x branch on the caller's stream, its HQ of w on a third
     r = gx_impl(d_gy, d_w, dt, T, Cin, Cout, block, gran_gy, gran_w, rnd, seed, d_gx,
                 base, gx_bytes, nullptr, nullptr, nullptr, nullptr, nullptr, stream,
@@ -708,12 +698,14 @@ hlq_status hlq_linear_backward(const void* d_gy, const void* d_w, const int8_t* 
   if (r == HLQ_OK)  // g_w branch on the auxiliary stream (its GEMM maybe after g_x's)
     r = gw_impl(d_gy, dt, d_xbar, xbar_fmt, d_xbar_scale, T, Cin, Cout, block, rank, d_gw,
                 base + gx_bytes, gw_bytes, nullptr, nullptr, nullptr, a, false,
-                gemms_in_sequence(T, Cin, Cout, Tp) ? gx_done : nullptr, hla_done, rw);
+                gemms_in_sequence(T, Cin, Cout, T / 16 * rank) ? gx_done : nullptr);
   // join even after a failure, so the caller's stream never runs ahead of
-  // work already enqueued on the auxiliary streams
-  if (cudaStreamWaitEvent(a, hla_done, 0) != cudaSuccess ||
-      cudaEventRecord(join, a) != cudaSuccess || cudaStreamWaitEvent(s, join, 0) != cudaSuccess)
+  // work already enqueued on the auxiliary stream
+  if (cudaEventRecord(join, a) != cudaSuccess || cudaStreamWaitEvent(s, join, 0) != cudaSuccess)
     r = HLQ_ERR_CUDA;
+  cudaEventDestroy(fork);
+  cudaEventDestroy(join);
+  cudaEventDestroy(gx_done);
   return r;
 }
 
