@@ -224,9 +224,12 @@ hlq_status hlq_linear_backward(const void *d_gy, const void *d_w, const int8_t *
  * hlq_compress_activation, into d_xbar / d_xbar_scale) and both gradients
  * (as hlq_linear_backward), in one call.  The compression is the first step
  * of the g_w branch, the only one that reads the stored activation, so it
- * runs beside the HQ of g_y and the g_x GEMM instead of before them.  Every
- * output bit equals the separate calls'.  Arguments as for those two calls;
- * workspace hlq_workspace_bytes(HLQ_OP_LAYER_STEP, ...).
+ * runs beside the HQ of g_y and the g_x GEMM instead of before them.  With a
+ * per-token g_y scale the HLA of g_y runs on a library stream of its own
+ * beside the compression; with a per-tensor one a single fused reader of
+ * g_y serves both paths (as hlq_linear_backward_fused).  Every output bit
+ * equals the separate calls'.  Arguments as for those two calls; workspace
+ * hlq_workspace_bytes(HLQ_OP_LAYER_STEP, ...).
  */
 hlq_status hlq_layer_step(const void *d_x, const void *d_gy, const void *d_w, int dt,
                           int64_t T, int64_t Cin, int64_t Cout, int block, int rank,
